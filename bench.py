@@ -1,0 +1,362 @@
+"""Throughput benchmark of the DeltaProduct forward on GB300.
+
+One step = one dp_forward call over the whole workload
+(B4 H8 T2048 n_h2 D128 bf16 by default): every row of the hot path (extended
+sequence, gate, chunk Gram, UT transform, W/U, state pass, masked readout,
+state I/O) runs inside that call.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Arms:
+  ours       the library's kernels through the C ABI. `value` is tokens/s with
+             inputs resident in HBM; `e2e` is the same call fed from pinned host
+             buffers with the host->device copies of the inputs and the
+             device->host copy of the outputs inside the timed region.
+  reference  the fp64 CPU oracle on the host cores (the only reference this
+             method has), on a bounded sample of the same workload.
+Under torchrun each rank runs its own copy of the workload (independent
+problems, no collective; weak scaling); rank 0 prints one JSON line.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from deltaproduct_householder_product_gb300 import workloads as W  # noqa: E402
+
+WORKLOADS = {"base": W.BASE, "neardup": W.NEARDUP, "gated": W.GATED, "long": W.LONG}
+METRIC = "DeltaProduct fwd tokens/s on 1 GB300; % of tensor-pipe/HBM roofline"
+L2_BYTES = 129 * 2 ** 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="base", choices=list(WORKLOADS))
+    ap.add_argument("--kernel", default="auto", choices=["auto", "recurrent", "chunk_tc"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def make_copies(w, n_copies, device):
+    """n_copies independent device copies of the inputs and outputs so that
+    consecutive steps never reuse data still resident in L2."""
+    x = W.make_inputs(w)
+    copies = []
+    for _ in range(n_copies):
+        c = {k: (None if v is None else v.to(device)) for k, v in x.items()}
+        c["o"] = torch.empty((w.B, w.T, w.H, w.Dv), dtype=w.torch_dtype, device=device)
+        c["hf"] = torch.empty((w.B, w.H, w.Dk, w.Dv), dtype=torch.float32, device=device)
+        copies.append(c)
+    return x, copies
+
+
+def forward_calls(dp, L, w, copies, kernel, stream):
+    """Pre-marshalled dp_forward calls, one per input copy (keeps per-call host
+    work to the ABI call itself)."""
+    import ctypes
+    from deltaproduct_householder_product_gb300 import _lib
+    dims = _lib.make_dims(w.B, w.T, w.H, w.Dk, w.Dv, w.nh, w.torch_dtype, kernel)
+    need = _lib.workspace_size(dims)
+    calls = []
+    s = ctypes.c_void_p(stream.cuda_stream)
+    for c in copies:
+        c["ws"] = torch.zeros(need, dtype=torch.uint8, device=c["q"].device)
+        args = (ctypes.byref(dims), _lib._ptr(c["q"]), _lib._ptr(c["k"]), _lib._ptr(c["v"]),
+                _lib._ptr(c["beta"]), _lib._ptr(c["g"]), _lib._ptr(c["h0"]), _lib._ptr(c["o"]),
+                _lib._ptr(c["hf"]), _lib._ptr(c["ws"]), ctypes.c_size_t(need), s)
+        calls.append((L.dp_forward, args))
+    return calls, dims
+
+
+def run_calls(calls, n, start=0):
+    for i in range(start, start + n):
+        fn, args = calls[i % len(calls)]
+        rc = fn(*args)
+        if rc != 0:
+            raise RuntimeError(f"dp_forward returned {rc}")
+
+
+def oracle_sample(w, x, seconds, threads):
+    """Time the fp64 oracle on a bounded sample of the workload: every
+    (batch, head) sequence, cut to the token prefix that fits `seconds` (the
+    whole workload when it fits). Returns (tokens_per_s, description, cores, s)."""
+    import oracle
+    pairs = [(b, h) for b in range(w.B) for h in range(w.H)]
+    flops_tok_head = W.algorithmic_flops(w.scaled(B=1, T=1, H=1))
+
+    def sub(T_s):
+        bs = [p[0] for p in pairs]
+        hs = [p[1] for p in pairs]
+        def take(t, lead):
+            if t is None:
+                return None
+            y = t[bs, :T_s, hs] if lead else t[bs, hs]
+            return y.unsqueeze(2) if lead else y.unsqueeze(1)
+        return dict(q=take(x["q"], True), k=take(x["k"], True), v=take(x["v"], True),
+                    beta=take(x["beta"], True), g=take(x["g"], True),
+                    h0=None if x["h0"] is None else take(x["h0"], False))
+    # calibrate on a short prefix
+    T_cal = min(w.T, 64)
+    s = sub(T_cal)
+    t0 = time.perf_counter()
+    oracle.forward(s["q"], s["k"], s["v"], s["beta"], s["g"], s["h0"], threads=threads)
+    rate = len(pairs) * T_cal * flops_tok_head / max(time.perf_counter() - t0, 1e-6)
+    T_s = int(max(1, min(w.T, seconds * rate / (len(pairs) * flops_tok_head))))
+    s = sub(T_s)
+    t0 = time.perf_counter()
+    oracle.forward(s["q"], s["k"], s["v"], s["beta"], s["g"], s["h0"], threads=threads)
+    dt = time.perf_counter() - t0
+    # tokens/s of the full problem = (token-heads/s) / H
+    tok_per_s = len(pairs) * T_s / dt / w.H
+    desc = (f"{len(pairs)} of {w.B * w.H} (batch,head) sequences x first {T_s} of {w.T} tokens, "
+            f"fp64, {dt:.2f} s; tokens/s = token-heads/s / H")
+    return tok_per_s, desc, min(threads, len(pairs)), dt
+
+
+def reference_arm(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    x = W.make_inputs(w)
+    per_step = max(0.05, 120.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(w, x, per_step, threads)
+    times, vals, desc, cores = [], [], "", 1
+    for _ in range(args.steps):
+        v, desc, cores, dt = oracle_sample(w, x, per_step, threads)
+        vals.append(v)
+        times.append(dt)
+    value = statistics.median(vals)
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "nh": w.nh,
+                       "Dk": w.Dk, "Dv": w.Dv},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def ours_arm(args, w):
+    import deltaproduct_householder_product_gb300 as dp
+    from deltaproduct_householder_product_gb300 import _lib
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    L = _lib.lib()
+    stream = torch.cuda.current_stream()
+
+    wbytes = W.algorithmic_bytes(w)
+    n_copies = max(2, -(-3 * L2_BYTES // wbytes))          # rotate copies: > 3x L2 in total
+    x, copies = make_copies(w, n_copies, dev)
+    calls, dims = forward_calls(dp, L, w, copies, args.kernel, stream)
+
+    run_calls(calls, args.warmup)
+    torch.cuda.synchronize()
+    for c in copies:
+        dp.check_status(c["ws"])
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    sampler = ClockSampler(local).start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall = time.perf_counter()
+    ev0.record(stream)
+    run_calls(calls, args.steps, start=args.warmup)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    wall_timed = time.perf_counter() - t_wall
+    barrier()
+    # keep the GPU busy with the same step while the clock sampler catches up
+    soak_until = time.perf_counter() + max(0.0, 1.5 - wall_timed)
+    i = args.warmup + args.steps
+    while time.perf_counter() < soak_until:
+        run_calls(calls, 50, start=i)
+        i += 50
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    clocks["window"] = "timed region" + (" + soak of the same step" if wall_timed < 1.5 else "")
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    for c in copies:
+        dp.check_status(c["ws"])
+
+    # e2e: pinned host inputs -> device, forward, outputs -> host, every step
+    host = {k: (None if v is None else v.pin_memory()) for k, v in x.items()}
+    c0 = copies[0]
+    o_host = torch.empty(c0["o"].shape, dtype=c0["o"].dtype).pin_memory()
+    hf_host = torch.empty(c0["hf"].shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    d2h = o_host.numel() * o_host.element_size() + hf_host.numel() * 4
+
+    def e2e_step():
+        for kname in ("q", "k", "v", "beta", "g", "h0"):
+            if host[kname] is not None:
+                c0[kname].copy_(host[kname], non_blocking=True)
+        run_calls(calls[:1], 1)
+        o_host.copy_(c0["o"], non_blocking=True)
+        hf_host.copy_(c0["hf"], non_blocking=True)
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        return
+    tokens = w.B * w.T * world
+    hbm_peak, _, peak_kind = measured_peaks()
+    achieved = wbytes / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": tokens / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "nh": w.nh, "Dk": w.Dk,
+                   "Dv": w.Dv, "kernel": args.kernel, "gated": w.gated,
+                   "l2": f"{n_copies} rotating input/output copies "
+                         f"({n_copies * wbytes / 1e6:.0f} MB > 129 MB L2)",
+                   "parallelism": f"replicas x{world}"},
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * KERNELS_PER_FORWARD,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": TRAFFIC.get((w.name, args.kernel)),
+                     "peak_kind": peak_kind, "algorithmic_bytes": wbytes},
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        v, desc, cores, _ = oracle_sample(w, x, 8.0, os.cpu_count() or 1)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores,
+                                "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+
+
+# dp_forward enqueues exactly one kernel (no memset, no helper kernels)
+KERNELS_PER_FORWARD = 1
+# per-launch DRAM bytes (read + write) from an ncu capture of the current kernel,
+# keyed by (workload, kernel family); absent = not captured for this build
+TRAFFIC = {}
+
+
+def main():
+    args = parse()
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        reference_arm(args, w)
+    else:
+        ours_arm(args, w)
+
+
+if __name__ == "__main__":
+    main()

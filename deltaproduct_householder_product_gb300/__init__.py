@@ -1,1 +1,122 @@
-"""Package for the GB300 DeltaProduct forward path (C-ABI + CUDA kernels)."""
+"""GB300 DeltaProduct forward recurrence: Python face of libdp.so.
+
+The recurrence (DeltaProduct paper, Sec.4 Eq.(2)-(3), gated variant): per
+(batch, head) and token t, H <- g_t H, then n_h ordered steps
+H <- H + beta k (v - H^T k)^T, then o_t = H^T q_t. All arithmetic runs in the
+library's CUDA kernels; these functions only marshal arguments (see
+``_lib.py``) and raise on any non-zero status.
+"""
+import torch
+
+from . import _lib
+from ._lib import DPError, STATE_EXPORT, STATE_IMPORT, STATE_ZERO  # noqa: F401
+
+__all__ = ["forward", "supports", "decode_step", "state_io", "check_status", "workspace_size",
+           "DPError", "abi_version"]
+
+
+def abi_version():
+    return _lib.lib().dp_abi_version()
+
+
+def workspace_size(B, T, H, Dk, Dv, nh, dtype=torch.bfloat16, impl="auto"):
+    """Device workspace bytes dp_forward needs for this problem."""
+    return _lib.workspace_size(_lib.make_dims(B, T, H, Dk, Dv, nh, dtype, impl))
+
+
+def supports(impl, B, T, H, Dk, Dv, nh, dtype=torch.bfloat16):
+    """True when kernel family ``impl`` handles this problem."""
+    try:
+        _lib.workspace_size(_lib.make_dims(B, T, H, Dk, Dv, nh, dtype, impl))
+        return True
+    except DPError as e:
+        if e.code == 2:
+            return False
+        raise
+
+
+def forward(q, k, v, beta, g=None, h0=None, *, impl="auto", out=None, h_final=True,
+            workspace=None, stream=None):
+    """Run the recurrence over whole sequences.
+
+    q [B,T,H,Dk], k [B,T,H,nh,Dk], v [B,T,H,nh,Dv], beta [B,T,H,nh], g [B,T,H]
+    or None (ungated), all CUDA tensors of one dtype (float32 or bfloat16);
+    h0 [B,H,Dk,Dv] float32 or None (zeros). ``h_final`` may be True (allocate),
+    False/None (do not write) or a float32 [B,H,Dk,Dv] tensor (may be h0).
+    Returns (o, h_final_or_None).
+    """
+    B, T, H, nh, Dk = k.shape
+    Dv = v.shape[-1]
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g)):
+        _lib._need_cuda(name, t, dt)
+    _lib._need_cuda("h0", h0, torch.float32)
+    if q.shape != (B, T, H, Dk) or v.shape != (B, T, H, nh, Dv) or beta.shape != (B, T, H, nh):
+        raise ValueError("inconsistent shapes for q, k, v, beta")
+    if g is not None and g.shape != (B, T, H):
+        raise ValueError("g must be [B,T,H]")
+    if h0 is not None and h0.shape != (B, H, Dk, Dv):
+        raise ValueError("h0 must be [B,H,Dk,Dv]")
+    dims = _lib.make_dims(B, T, H, Dk, Dv, nh, dt, impl)
+    if out is None:
+        out = torch.empty((B, T, H, Dv), dtype=dt, device=q.device)
+    _lib._need_cuda("out", out, dt)
+    if h_final is True:
+        h_final = torch.empty((B, H, Dk, Dv), dtype=torch.float32, device=q.device)
+    elif h_final is False:
+        h_final = None
+    _lib._need_cuda("h_final", h_final, torch.float32)
+    need = _lib.workspace_size(dims)
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    _lib._need_cuda("workspace", workspace)
+    rc = _lib.lib().dp_forward(
+        dims, _lib._ptr(q), _lib._ptr(k), _lib._ptr(v), _lib._ptr(beta), _lib._ptr(g),
+        _lib._ptr(h0), _lib._ptr(out), _lib._ptr(h_final), _lib._ptr(workspace),
+        workspace.numel() * workspace.element_size(), _lib._stream(stream))
+    _lib._check(rc, "dp_forward")
+    return out, h_final
+
+
+def decode_step(q, k, v, beta, g, state, *, out=None, stream=None):
+    """One token on a carried fp32 state (updated in place).
+
+    q [B,H,Dk], k [B,H,nh,Dk], v [B,H,nh,Dv], beta [B,H,nh], g [B,H] or None,
+    state [B,H,Dk,Dv] float32. Returns o [B,H,Dv].
+    """
+    B, H, nh, Dk = k.shape
+    Dv = v.shape[-1]
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g)):
+        _lib._need_cuda(name, t, dt)
+    _lib._need_cuda("state", state, torch.float32)
+    if state.shape != (B, H, Dk, Dv):
+        raise ValueError("state must be [B,H,Dk,Dv]")
+    if out is None:
+        out = torch.empty((B, H, Dv), dtype=dt, device=q.device)
+    _lib._need_cuda("out", out, dt)
+    dims = _lib.make_dims(B, 1, H, Dk, Dv, nh, dt)
+    rc = _lib.lib().dp_decode_step(dims, _lib._ptr(q), _lib._ptr(k), _lib._ptr(v),
+                                   _lib._ptr(beta), _lib._ptr(g), _lib._ptr(state),
+                                   _lib._ptr(out), _lib._stream(stream))
+    _lib._check(rc, "dp_decode_step")
+    return out
+
+
+def state_io(op, state, ext=None, transposed=False, stream=None):
+    """ZERO / IMPORT (ext -> state) / EXPORT (state -> ext) of a [B,H,Dk,Dv] state."""
+    _lib._need_cuda("state", state, torch.float32)
+    _lib._need_cuda("ext", ext)
+    B, H, Dk, Dv = state.shape
+    ext_dt = _lib.DP_F32 if ext is None else _lib._dtype_code(ext.dtype)
+    rc = _lib.lib().dp_state_io(int(op), B, H, Dk, Dv, _lib._ptr(state), _lib._ptr(ext),
+                                ext_dt, int(bool(transposed)), _lib._stream(stream))
+    _lib._check(rc, "dp_state_io")
+    return state if op != STATE_EXPORT else ext
+
+
+def check_status(workspace, stream=None):
+    """Synchronise and raise if the device recorded an error in ``workspace``."""
+    _lib._need_cuda("workspace", workspace)
+    _lib._check(_lib.lib().dp_check_status(_lib._ptr(workspace), _lib._stream(stream)),
+                "dp_check_status")

@@ -1,0 +1,198 @@
+// C ABI of libdp.so: argument validation, workspace layout and dispatch.
+// See include/dp.h for the contract of every entry point.
+#include <string.h>
+
+#include "internal.h"
+
+namespace {
+
+constexpr size_t kStatusBlock = 256;   // status word + padding, start of the workspace
+
+bool supported_dim(int d) { return d == 32 || d == 64 || d == 128; }
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// The pointer must be usable by a kernel on the current device.
+bool device_pointer(const void *p)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+dp_status check_dims(const dp_dims *d, bool decode)
+{
+    if (!d) return DP_ERR_INVALID_ARG;
+    if (d->B < 0 || d->H < 0 || (!decode && d->T < 0)) return DP_ERR_INVALID_ARG;
+    if (d->dtype != DP_F32 && d->dtype != DP_BF16) return DP_ERR_INVALID_ARG;
+    if (d->impl < DP_IMPL_AUTO || d->impl > DP_IMPL_CHUNK_TC) return DP_ERR_INVALID_ARG;
+    if (!supported_dim(d->Dk) || !supported_dim(d->Dv)) return DP_ERR_UNSUPPORTED;
+    if (d->nh < 1 || d->nh > 4) return DP_ERR_UNSUPPORTED;
+    // indices are formed in 64-bit, but keep every extent within int range
+    const long long tok = (long long)d->B * (decode ? 1 : d->T) * d->H;
+    if (tok * d->nh * (d->Dk > d->Dv ? d->Dk : d->Dv) > (1ll << 40)) return DP_ERR_UNSUPPORTED;
+    return DP_OK;
+}
+
+// Required pointer: non-NULL, device-accessible, aligned to `align` bytes.
+dp_status check_ptr(const void *p, size_t align)
+{
+    if (!p) return DP_ERR_INVALID_ARG;
+    if (((uintptr_t)p & (align - 1)) != 0) return DP_ERR_ALIGNMENT;
+    if (!device_pointer(p)) return DP_ERR_INVALID_ARG;
+    return DP_OK;
+}
+
+#define DP_TRY(expr)                         \
+    do {                                     \
+        dp_status s_ = (expr);               \
+        if (s_ != DP_OK) return s_;          \
+    } while (0)
+
+dp::Problem make_problem(const dp_dims *d, int T)
+{
+    dp::Problem p;
+    memset(&p, 0, sizeof(p));
+    p.B = d->B; p.T = T; p.H = d->H; p.Dk = d->Dk; p.Dv = d->Dv; p.nh = d->nh;
+    p.dtype = d->dtype;
+    return p;
+}
+
+dp_status check_io(const dp::Problem &p, bool has_g)
+{
+    const size_t el = p.dtype == DP_F32 ? 4 : 2;
+    const bool any = (size_t)p.B * p.H * p.T > 0;
+    if (any) {
+        DP_TRY(check_ptr(p.q, 16));
+        DP_TRY(check_ptr(p.k, 16));
+        DP_TRY(check_ptr(p.v, 16));
+        DP_TRY(check_ptr(p.o, 16));
+        DP_TRY(check_ptr(p.beta, el));
+        if (has_g) DP_TRY(check_ptr(p.g, el));
+    }
+    return DP_OK;
+}
+
+dp_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DP_OK : DP_ERR_CUDA; }
+
+bool use_chunk_tc(const dp_dims *d, const dp::Problem &p)
+{
+    if (d->impl == DP_IMPL_RECURRENT) return false;
+    return dp::chunk_tc_supported(p);
+}
+
+}  // namespace
+
+extern "C" {
+
+int dp_abi_version(void) { return DP_ABI_VERSION; }
+
+const char *dp_status_string(dp_status s)
+{
+    switch (s) {
+    case DP_OK: return "ok";
+    case DP_ERR_INVALID_ARG: return "invalid argument";
+    case DP_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case DP_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case DP_ERR_WORKSPACE: return "workspace missing or too small";
+    case DP_ERR_CUDA: return "CUDA runtime error";
+    case DP_ERR_TIMEOUT: return "device-side wait timed out";
+    case DP_ERR_DEVICE: return "device reported an inconsistency";
+    }
+    return "unknown status";
+}
+
+dp_status dp_forward_workspace_size(const dp_dims *dims, size_t *bytes)
+{
+    if (!bytes) return DP_ERR_INVALID_ARG;
+    DP_TRY(check_dims(dims, false));
+    if (dims->impl == DP_IMPL_CHUNK_TC) {
+        dp::Problem p = make_problem(dims, dims->T);
+        if (!dp::chunk_tc_supported(p)) return DP_ERR_UNSUPPORTED;
+    }
+    dp::Problem p = make_problem(dims, dims->T);
+    size_t extra = use_chunk_tc(dims, p) ? dp::chunk_tc_scratch_bytes(p) : 0;
+    *bytes = kStatusBlock + ((extra + 255) & ~(size_t)255);
+    return DP_OK;
+}
+
+dp_status dp_forward(const dp_dims *dims, const void *q, const void *k, const void *v,
+                     const void *beta, const void *g, const float *h0, void *o,
+                     float *h_final, void *workspace, size_t workspace_bytes,
+                     dp_stream_t stream)
+{
+    DP_TRY(check_dims(dims, false));
+    dp::Problem p = make_problem(dims, dims->T);
+    p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g; p.h0 = h0; p.o = o;
+    p.h_final = h_final;
+    p.stream = (cudaStream_t)stream;
+    const bool tc = use_chunk_tc(dims, p);
+    if (dims->impl == DP_IMPL_CHUNK_TC && !tc) return DP_ERR_UNSUPPORTED;
+    DP_TRY(check_io(p, g != nullptr));
+    if (h0) DP_TRY(check_ptr(h0, 16));
+    if (h_final) DP_TRY(check_ptr(h_final, 16));
+    size_t need = 0;
+    DP_TRY(dp_forward_workspace_size(dims, &need));
+    if (!workspace || workspace_bytes < need) return DP_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return DP_ERR_ALIGNMENT;
+    if (!device_pointer(workspace)) return DP_ERR_INVALID_ARG;
+    p.status = (uint32_t *)workspace;
+    p.scratch = (char *)workspace + kStatusBlock;
+    p.scratch_bytes = need - kStatusBlock;
+
+    if ((size_t)p.B * p.H == 0) return DP_OK;
+    return from_cuda(tc ? dp::launch_chunk_tc(p) : dp::launch_recurrent(p));
+}
+
+dp_status dp_decode_step(const dp_dims *dims, const void *q, const void *k, const void *v,
+                         const void *beta, const void *g, float *state, void *o,
+                         dp_stream_t stream)
+{
+    DP_TRY(check_dims(dims, true));
+    dp::Problem p = make_problem(dims, 1);
+    p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g; p.o = o;
+    p.h0 = state;
+    p.h_final = state;
+    p.stream = (cudaStream_t)stream;
+    if ((size_t)p.B * p.H == 0) return DP_OK;
+    DP_TRY(check_io(p, g != nullptr));
+    DP_TRY(check_ptr(state, 16));
+    return from_cuda(dp::launch_recurrent(p));
+}
+
+dp_status dp_state_io(int op, int B, int H, int Dk, int Dv, float *state, void *ext,
+                      int ext_dtype, int ext_transposed, dp_stream_t stream)
+{
+    if (op < DP_STATE_ZERO || op > DP_STATE_EXPORT) return DP_ERR_INVALID_ARG;
+    if (B < 0 || H < 0) return DP_ERR_INVALID_ARG;
+    if (!supported_dim(Dk) || !supported_dim(Dv)) return DP_ERR_UNSUPPORTED;
+    if (ext_dtype != DP_F32 && ext_dtype != DP_BF16) return DP_ERR_INVALID_ARG;
+    if ((size_t)B * H == 0) return DP_OK;
+    DP_TRY(check_ptr(state, 16));
+    if (op != DP_STATE_ZERO) DP_TRY(check_ptr(ext, ext_dtype == DP_F32 ? 4 : 2));
+    return from_cuda(dp::launch_state_io(op, B, H, Dk, Dv, state, ext, ext_dtype,
+                                         ext_transposed, (cudaStream_t)stream));
+}
+
+dp_status dp_check_status(const void *workspace, dp_stream_t stream)
+{
+    if (!workspace) return DP_ERR_INVALID_ARG;
+    if (!aligned16(workspace)) return DP_ERR_ALIGNMENT;
+    if (!device_pointer(workspace)) return DP_ERR_INVALID_ARG;
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost,
+                        (cudaStream_t)stream) != cudaSuccess)
+        return DP_ERR_CUDA;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DP_ERR_CUDA;
+    if (word == dp::kDevOk) return DP_OK;
+    // read-and-clear: the next calls start from a clean word
+    if (cudaMemsetAsync((void *)workspace, 0, sizeof(word), (cudaStream_t)stream) != cudaSuccess ||
+        cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess)
+        return DP_ERR_CUDA;
+    if (word == dp::kDevTimeout) return DP_ERR_TIMEOUT;
+    return DP_ERR_DEVICE;
+}
+
+}  // extern "C"

@@ -1,0 +1,43 @@
+// Internal declarations shared by the translation units of libdp.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dp.h"
+
+namespace dp {
+
+// One validated forward / decode problem (device pointers, row-major layouts
+// as documented in dp.h).
+struct Problem {
+    int B, T, H, Dk, Dv, nh;
+    int dtype;                 // dp_dtype
+    const void *q, *k, *v, *beta, *g;
+    const float *h0;
+    void *o;
+    float *h_final;
+    uint32_t *status;          // device status word (may be NULL for decode)
+    void *scratch;             // workspace bytes after the status block
+    size_t scratch_bytes;
+    cudaStream_t stream;
+};
+
+// Sequential (token by token) SIMT kernel: any supported D_k, D_v, n_h and
+// dtype. Also serves dp_decode_step (T = 1, state in place).
+cudaError_t launch_recurrent(const Problem &p);
+
+// Tensor-core chunked kernel (tcgen05 / TMEM / TMA): bf16, D_k = D_v = 128.
+bool chunk_tc_supported(const Problem &p);
+size_t chunk_tc_scratch_bytes(const Problem &p);
+cudaError_t launch_chunk_tc(const Problem &p);
+
+cudaError_t launch_state_io(int op, int B, int H, int Dk, int Dv, float *state,
+                            void *ext, int ext_dtype, int ext_transposed,
+                            cudaStream_t stream);
+
+// Device status codes written into the status word (first one wins).
+enum : uint32_t { kDevOk = 0, kDevTimeout = 1, kDevBadState = 2 };
+
+}  // namespace dp

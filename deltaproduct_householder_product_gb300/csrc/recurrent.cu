@@ -1,0 +1,153 @@
+// Token-by-token DeltaProduct recurrence on CUDA cores, fp32 arithmetic.
+//
+// DeltaProduct paper, Sec.4 Eq.(3) and the gated per-token pseudocode
+// (Sec.4, Appendix B.1): H <- g H; for each of the n_h steps
+// e = v - H^T k, H <- H + beta k e^T; then o = H^T q.
+//
+// Serves three calls: the fp32 path of dp_forward (and any head size the
+// tensor-core kernel does not take), dp_decode_step (T = 1 with the state
+// updated in place), and the state import/export of dp_state_io.
+//
+// Work split: one CTA owns a 32-column slice of one (batch, head) state and
+// keeps it in registers for the whole sequence: 4 warps x 32 lanes, lane =
+// value column, warp w = a contiguous block of D_k/4 key rows. A matvec
+// H^T x is a per-thread partial dot over its rows followed by a 4-way
+// shared-memory reduction across the warps.
+#include "internal.h"
+
+namespace dp {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kCols = 32;
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ void from_f(float *p, float x) { *p = x; }
+__device__ __forceinline__ void from_f(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+template <int DK, typename TIn>
+__global__ void __launch_bounds__(kWarps * 32)
+recurrent_kernel(int T, int H, int Dv, int nh,
+                 const TIn *__restrict__ q, const TIn *__restrict__ k,
+                 const TIn *__restrict__ v, const TIn *__restrict__ beta,
+                 const TIn *__restrict__ g, const float *h0, TIn *__restrict__ o,
+                 float *h_final)
+{
+    constexpr int R = DK / kWarps;            // key rows per warp
+    __shared__ float kbuf[2][DK];
+    __shared__ float part[2][kWarps][kCols];
+
+    const int bh = blockIdx.x;                // b * H + h
+    const int b = bh / H, h = bh - b * H;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int col = blockIdx.y * kCols + lane;
+    const int row0 = w * R;
+    const size_t state_base = (size_t)bh * DK * Dv;
+
+    float S[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        S[r] = h0 ? h0[state_base + (size_t)(row0 + r) * Dv + col] : 0.f;
+
+    int buf = 0;   // alternating buffers: one barrier per matvec
+    for (int t = 0; t < T; ++t) {
+        const size_t tok = ((size_t)b * T + t) * H + h;
+        if (g) {
+            const float gt = to_f(g[tok]);
+#pragma unroll
+            for (int r = 0; r < R; ++r) S[r] *= gt;
+        }
+        for (int j = 0; j <= nh; ++j) {
+            // j < nh: one Householder step with key k_{t,j}; j == nh: readout with q_t
+            const TIn *x = (j < nh) ? k + (tok * nh + j) * DK : q + tok * DK;
+            for (int i = threadIdx.x; i < DK; i += kWarps * 32) kbuf[buf][i] = to_f(x[i]);
+            __syncthreads();
+            float acc = 0.f;
+#pragma unroll
+            for (int r = 0; r < R; ++r) acc = fmaf(S[r], kbuf[buf][row0 + r], acc);
+            part[buf][w][lane] = acc;
+            __syncthreads();
+            float hx = 0.f;
+#pragma unroll
+            for (int i = 0; i < kWarps; ++i) hx += part[buf][i][lane];
+            if (j < nh) {
+                const float vj = to_f(v[(tok * nh + j) * Dv + col]);
+                const float bj = to_f(beta[tok * nh + j]);
+                const float e = bj * (vj - hx);
+#pragma unroll
+                for (int r = 0; r < R; ++r) S[r] = fmaf(kbuf[buf][row0 + r], e, S[r]);
+            } else if (w == 0) {
+                from_f(o + tok * Dv + col, hx);
+            }
+            buf ^= 1;
+        }
+    }
+    if (h_final) {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            h_final[state_base + (size_t)(row0 + r) * Dv + col] = S[r];
+    }
+}
+
+template <typename TIn>
+cudaError_t launch_typed(const Problem &p)
+{
+    dim3 grid(p.B * p.H, p.Dv / kCols), block(kWarps * 32);
+    const TIn *q = (const TIn *)p.q, *k = (const TIn *)p.k, *v = (const TIn *)p.v;
+    const TIn *be = (const TIn *)p.beta, *g = (const TIn *)p.g;
+    TIn *o = (TIn *)p.o;
+    switch (p.Dk) {
+    case 32:
+        recurrent_kernel<32, TIn><<<grid, block, 0, p.stream>>>(p.T, p.H, p.Dv, p.nh, q, k, v, be, g, p.h0, o, p.h_final);
+        break;
+    case 64:
+        recurrent_kernel<64, TIn><<<grid, block, 0, p.stream>>>(p.T, p.H, p.Dv, p.nh, q, k, v, be, g, p.h0, o, p.h_final);
+        break;
+    default:
+        recurrent_kernel<128, TIn><<<grid, block, 0, p.stream>>>(p.T, p.H, p.Dv, p.nh, q, k, v, be, g, p.h0, o, p.h_final);
+        break;
+    }
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- state I/O
+template <typename TExt>
+__global__ void state_io_kernel(int op, size_t n, int Dk, int Dv, float *state, TExt *ext,
+                                int transposed)
+{
+    const size_t per = (size_t)Dk * Dv;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const size_t head = i / per, rem = i - head * per;
+        const int r = (int)(rem / Dv), c = (int)(rem - (size_t)r * Dv);
+        const size_t e = transposed ? head * per + (size_t)c * Dk + r : i;
+        if (op == DP_STATE_IMPORT) state[i] = to_f(ext[e]);
+        else from_f(ext + e, state[i]);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_recurrent(const Problem &p)
+{
+    if (p.B * p.H == 0) return cudaSuccess;
+    return p.dtype == DP_F32 ? launch_typed<float>(p) : launch_typed<__nv_bfloat16>(p);
+}
+
+cudaError_t launch_state_io(int op, int B, int H, int Dk, int Dv, float *state, void *ext,
+                            int ext_dtype, int ext_transposed, cudaStream_t stream)
+{
+    const size_t n = (size_t)B * H * Dk * Dv;
+    if (n == 0) return cudaSuccess;
+    if (op == DP_STATE_ZERO) return cudaMemsetAsync(state, 0, n * sizeof(float), stream);
+    const int threads = 256;
+    const int blocks = (int)((n + threads - 1) / threads < 4096 ? (n + threads - 1) / threads : 4096);
+    if (ext_dtype == DP_F32)
+        state_io_kernel<float><<<blocks, threads, 0, stream>>>(op, n, Dk, Dv, state, (float *)ext, ext_transposed);
+    else
+        state_io_kernel<__nv_bfloat16><<<blocks, threads, 0, stream>>>(op, n, Dk, Dv, state, (__nv_bfloat16 *)ext, ext_transposed);
+    return cudaGetLastError();
+}
+
+}  // namespace dp

@@ -1,0 +1,124 @@
+/*
+ * dp.h -- C ABI of the GB300 DeltaProduct forward library (libdp.so).
+ *
+ * The operation (DeltaProduct: Improving State-Tracking in Linear RNNs via
+ * Householder Products, Sec.4 Eq.(2)-(3), the gated variant of Sec.4 and the
+ * per-token pseudocode of Sec.4 / Appendix B.1): for every batch b, head h
+ * and token t, with the D_k x D_v matrix state H,
+ *
+ *     H <- g_t H                                   (optional gate, once per token)
+ *     for j = 1..n_h:  H <- H + beta_{t,j} k_{t,j} (v_{t,j} - H^T k_{t,j})^T
+ *                    (= (I - beta k k^T) H + beta k v^T, a generalised Householder step)
+ *     o_t = H^T q_t                                (readout of the post-update state)
+ *
+ * Keys are expected unit-norm and beta in [0,1] or [0,2]; the library does
+ * not renormalise or clamp (those are properties of the caller's inputs).
+ *
+ * Memory: every pointer is a DEVICE pointer on the current CUDA device,
+ * owned by the caller. The library allocates no device memory and keeps no
+ * state between calls; all work is enqueued asynchronously on `stream`.
+ * Layouts are contiguous row-major:
+ *     q    [B, T, H, D_k]          k    [B, T, H, n_h, D_k]
+ *     v    [B, T, H, n_h, D_v]     beta [B, T, H, n_h]
+ *     g    [B, T, H]  (NULL: ungated)
+ *     o    [B, T, H, D_v]
+ *     state (h0, h_final, decode state) [B, H, D_k, D_v], always fp32.
+ * q, k, v, beta, g and o share the element type `dims->dtype`.
+ *
+ * Errors: every entry point validates its arguments on the host first and
+ * returns a non-zero dp_status without enqueuing anything when a check
+ * fails (outputs untouched). A failed launch returns DP_ERR_CUDA. Conditions
+ * found on the device (a bounded wait that expired) are recorded in the
+ * first word of the caller's workspace and read back (and cleared) by
+ * dp_check_status. Zero a workspace once after allocating it; the library
+ * never sets that word except on a device-side error.
+ * No entry point aborts, traps or throws.
+ */
+#ifndef DP_H_
+#define DP_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *dp_stream_t;   /* same type as cudaStream_t */
+
+typedef enum {
+    DP_OK = 0,
+    DP_ERR_INVALID_ARG = 1,   /* NULL / host pointer, negative size, bad enum */
+    DP_ERR_UNSUPPORTED = 2,   /* D_k, D_v not in {32,64,128}; n_h not in 1..4 */
+    DP_ERR_ALIGNMENT = 3,     /* q, k, v, o, state, workspace not 16-byte aligned */
+    DP_ERR_WORKSPACE = 4,     /* workspace NULL or smaller than required */
+    DP_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
+    DP_ERR_TIMEOUT = 6,       /* a device-side bounded wait expired */
+    DP_ERR_DEVICE = 7         /* the device reported another inconsistency */
+} dp_status;
+
+typedef enum { DP_F32 = 0, DP_BF16 = 1 } dp_dtype;
+
+/* Kernel family for dp_forward. AUTO picks the tensor-core chunked kernel
+ * where it applies (bf16, D_k = D_v = 128) and the recurrent kernel
+ * otherwise; the others force one family (CHUNK_TC returns
+ * DP_ERR_UNSUPPORTED where it does not apply). */
+typedef enum { DP_IMPL_AUTO = 0, DP_IMPL_RECURRENT = 1, DP_IMPL_CHUNK_TC = 2 } dp_impl;
+
+typedef struct {
+    int B, T, H;     /* batch, tokens, heads (T may be 0) */
+    int Dk, Dv;      /* key and value head dims: 32, 64 or 128 */
+    int nh;          /* Householder steps per token (n_h), 1..4 */
+    int dtype;       /* dp_dtype of q, k, v, beta, g, o */
+    int impl;        /* dp_impl */
+} dp_dims;
+
+/* ABI version of this header (bumped on any signature change). */
+#define DP_ABI_VERSION 1
+int dp_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *dp_status_string(dp_status s);
+
+/* Bytes of device workspace dp_forward needs for `dims` (>= 256). The first
+ * 4 bytes hold the device status word. */
+dp_status dp_forward_workspace_size(const dp_dims *dims, size_t *bytes);
+
+/* Whole-sequence forward (the extended T*n_h sequence of the paper's Sec.5.1,
+ * processed in chunks by the tensor-core kernel):
+ *   h0       initial state, NULL = zeros;
+ *   h_final  final state, NULL = not written; may alias h0;
+ *   o        outputs for every token.
+ * T = 0 copies h0 (or zeros) to h_final. */
+dp_status dp_forward(const dp_dims *dims,
+                     const void *q, const void *k, const void *v,
+                     const void *beta, const void *g,
+                     const float *h0, void *o, float *h_final,
+                     void *workspace, size_t workspace_bytes,
+                     dp_stream_t stream);
+
+/* One decode step (dims->T is ignored and taken as 1) on a carried state,
+ * updated in place. Shapes drop the T axis: q [B,H,D_k], k [B,H,n_h,D_k],
+ * v [B,H,n_h,D_v], beta [B,H,n_h], g [B,H] or NULL, o [B,H,D_v],
+ * state [B,H,D_k,D_v] fp32. Same recurrence as dp_forward with T = 1. */
+dp_status dp_decode_step(const dp_dims *dims,
+                         const void *q, const void *k, const void *v,
+                         const void *beta, const void *g,
+                         float *state, void *o, dp_stream_t stream);
+
+/* State import / export / reset between the library's canonical fp32
+ * [B,H,D_k,D_v] state and a caller buffer `ext` of type ext_dtype, laid out
+ * [B,H,D_k,D_v] or, when ext_transposed != 0, [B,H,D_v,D_k] (the S = H^T
+ * convention). ZERO ignores ext. */
+typedef enum { DP_STATE_ZERO = 0, DP_STATE_IMPORT = 1, DP_STATE_EXPORT = 2 } dp_state_op;
+dp_status dp_state_io(int op, int B, int H, int Dk, int Dv, float *state,
+                      void *ext, int ext_dtype, int ext_transposed,
+                      dp_stream_t stream);
+
+/* Synchronises `stream`, returns the status the device recorded in the
+ * workspace since it was last cleared, and clears it. */
+dp_status dp_check_status(const void *workspace, dp_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DP_H_ */

@@ -63,11 +63,11 @@ static int run_pair(oracle_job *J, int b, int h, double *S, double *e)
             const double *kk = J->k + (tok * nh + j) * (size_t)Dk;
             const double *vv = J->v + (tok * nh + j) * (size_t)Dv;
             const double bt = J->beta[tok * nh + j];
-            /* e = v - H^T k */
-            for (int c = 0; c < Dv; ++c) {
-                double acc = 0.0;
-                for (int r = 0; r < Dk; ++r) acc += S[(size_t)r * Dv + c] * kk[r];
-                e[c] = vv[c] - acc;
+            /* e = v - H^T k  (accumulated row by row of H) */
+            for (int c = 0; c < Dv; ++c) e[c] = vv[c];
+            for (int r = 0; r < Dk; ++r) {
+                const double *row = S + (size_t)r * Dv;
+                for (int c = 0; c < Dv; ++c) e[c] -= row[c] * kk[r];
             }
             /* H += beta k e^T */
             for (int r = 0; r < Dk; ++r) {
@@ -79,10 +79,10 @@ static int run_pair(oracle_job *J, int b, int h, double *S, double *e)
         /* o_t = H^T q_t */
         const double *qq = J->q + tok * (size_t)Dk;
         double *oo = J->o + tok * (size_t)Dv;
-        for (int c = 0; c < Dv; ++c) {
-            double acc = 0.0;
-            for (int r = 0; r < Dk; ++r) acc += S[(size_t)r * Dv + c] * qq[r];
-            oo[c] = acc;
+        for (int c = 0; c < Dv; ++c) oo[c] = 0.0;
+        for (int r = 0; r < Dk; ++r) {
+            const double *row = S + (size_t)r * Dv;
+            for (int c = 0; c < Dv; ++c) oo[c] += row[c] * qq[r];
         }
     }
     if (J->h_final)

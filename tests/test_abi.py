@@ -1,0 +1,92 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments before touching the device. CPU only:
+none of these calls reaches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from deltaproduct_householder_product_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dp.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dp_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from deltaproduct_householder_product_gb300 import build
+    build.build()
+    return _lib.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert "dp_forward" in names and "dp_decode_step" in names and "dp_state_io" in names
+    for n in names:
+        assert hasattr(L, n), f"libdp.so does not export {n}"
+
+
+def test_abi_version_matches_header(L):
+    m = re.search(r"#define DP_ABI_VERSION (\d+)", open(HEADER).read())
+    assert L.dp_abi_version() == int(m.group(1))
+
+
+def test_status_strings(L):
+    for code in range(8):
+        assert L.dp_status_string(code)
+    assert L.dp_status_string(99) == b"unknown status"
+
+
+def ws(L, **kw):
+    d = dict(B=1, T=64, H=2, Dk=128, Dv=128, nh=2, dtype=_lib.DP_BF16, impl=0)
+    d.update(kw)
+    dims = _lib.Dims(**d)
+    n = ctypes.c_size_t(0)
+    rc = L.dp_forward_workspace_size(ctypes.byref(dims), ctypes.byref(n))
+    return rc, n.value
+
+
+def test_workspace_size_and_validation(L):
+    rc, n = ws(L)
+    assert rc == 0 and n >= 256 and n % 256 == 0
+    assert ws(L, Dk=96)[0] == 2            # DP_ERR_UNSUPPORTED
+    assert ws(L, Dv=256)[0] == 2
+    assert ws(L, nh=0)[0] == 2
+    assert ws(L, nh=5)[0] == 2
+    assert ws(L, B=-1)[0] == 1             # DP_ERR_INVALID_ARG
+    assert ws(L, dtype=7)[0] == 1
+    assert ws(L, impl=9)[0] == 1
+    assert ws(L, T=0)[0] == 0
+    assert ws(L, Dk=32, Dv=32, dtype=_lib.DP_F32, impl=1)[0] == 0
+    n_null = L.dp_forward_workspace_size(None, ctypes.byref(ctypes.c_size_t()))
+    assert n_null == 1
+
+
+def test_forward_rejects_before_launch(L):
+    dims = _lib.Dims(1, 64, 2, 128, 128, 2, _lib.DP_BF16, 0)
+    null = [None] * 9
+    # NULL inputs -> invalid argument, nothing enqueued
+    assert L.dp_forward(ctypes.byref(dims), *null, 0, None) == 1
+    bad = _lib.Dims(1, 64, 2, 100, 128, 2, _lib.DP_BF16, 0)
+    assert L.dp_forward(ctypes.byref(bad), *null, 0, None) == 2
+    assert L.dp_forward(None, *null, 0, None) == 1
+    # misaligned q pointer is reported as an alignment error before any CUDA call
+    args = [ctypes.c_void_p(0x1001)] + [ctypes.c_void_p(0x1000)] * 8
+    assert L.dp_forward(ctypes.byref(dims), *args, 1 << 20, None) == 3
+
+
+def test_decode_and_state_io_reject(L):
+    dims = _lib.Dims(1, 1, 2, 128, 128, 2, _lib.DP_BF16, 0)
+    assert L.dp_decode_step(ctypes.byref(dims), *([None] * 7), None) == 1
+    assert L.dp_state_io(5, 1, 1, 128, 128, None, None, 0, 0, None) == 1
+    assert L.dp_state_io(0, 1, 1, 100, 128, None, None, 0, 0, None) == 2
+    assert L.dp_state_io(0, 1, 1, 128, 128, None, None, 0, 0, None) == 1
+    assert L.dp_state_io(0, 0, 1, 128, 128, None, None, 0, 0, None) == 0   # empty: no-op
+    assert L.dp_check_status(None, None) == 1
