@@ -19,9 +19,9 @@ def abi_version():
     return _lib.lib().dp_abi_version()
 
 
-def workspace_size(B, T, H, Dk, Dv, nh, dtype=torch.bfloat16, impl="auto"):
+def workspace_size(B, T, H, Dk, Dv, nh, dtype=torch.bfloat16, impl="auto", out_dtype=None):
     """Device workspace bytes dp_forward needs for this problem."""
-    return _lib.workspace_size(_lib.make_dims(B, T, H, Dk, Dv, nh, dtype, impl))
+    return _lib.workspace_size(_lib.make_dims(B, T, H, Dk, Dv, nh, dtype, impl, out_dtype))
 
 
 def supports(impl, B, T, H, Dk, Dv, nh, dtype=torch.bfloat16):
@@ -36,12 +36,14 @@ def supports(impl, B, T, H, Dk, Dv, nh, dtype=torch.bfloat16):
 
 
 def forward(q, k, v, beta, g=None, h0=None, *, impl="auto", out=None, h_final=True,
-            workspace=None, stream=None):
+            workspace=None, stream=None, out_dtype=None):
     """Run the recurrence over whole sequences.
 
     q [B,T,H,Dk], k [B,T,H,nh,Dk], v [B,T,H,nh,Dv], beta [B,T,H,nh], g [B,T,H]
     or None (ungated), all CUDA tensors of one dtype (float32 or bfloat16);
-    h0 [B,H,Dk,Dv] float32 or None (zeros). ``h_final`` may be True (allocate),
+    h0 [B,H,Dk,Dv] float32 or None (zeros). ``out_dtype`` is the dtype of o
+    (default: the input dtype; float32 is allowed with bfloat16 inputs, or
+    taken from ``out``). ``h_final`` may be True (allocate),
     False/None (do not write) or a float32 [B,H,Dk,Dv] tensor (may be h0).
     Returns (o, h_final_or_None).
     """
@@ -57,10 +59,12 @@ def forward(q, k, v, beta, g=None, h0=None, *, impl="auto", out=None, h_final=Tr
         raise ValueError("g must be [B,T,H]")
     if h0 is not None and h0.shape != (B, H, Dk, Dv):
         raise ValueError("h0 must be [B,H,Dk,Dv]")
-    dims = _lib.make_dims(B, T, H, Dk, Dv, nh, dt, impl)
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else dt
+    dims = _lib.make_dims(B, T, H, Dk, Dv, nh, dt, impl, out_dtype)
     if out is None:
-        out = torch.empty((B, T, H, Dv), dtype=dt, device=q.device)
-    _lib._need_cuda("out", out, dt)
+        out = torch.empty((B, T, H, Dv), dtype=out_dtype, device=q.device)
+    _lib._need_cuda("out", out, out_dtype)
     if h_final is True:
         h_final = torch.empty((B, H, Dk, Dv), dtype=torch.float32, device=q.device)
     elif h_final is False:
@@ -78,7 +82,7 @@ def forward(q, k, v, beta, g=None, h0=None, *, impl="auto", out=None, h_final=Tr
     return out, h_final
 
 
-def decode_step(q, k, v, beta, g, state, *, out=None, stream=None):
+def decode_step(q, k, v, beta, g, state, *, out=None, stream=None, out_dtype=None):
     """One token on a carried fp32 state (updated in place).
 
     q [B,H,Dk], k [B,H,nh,Dk], v [B,H,nh,Dv], beta [B,H,nh], g [B,H] or None,
@@ -92,10 +96,12 @@ def decode_step(q, k, v, beta, g, state, *, out=None, stream=None):
     _lib._need_cuda("state", state, torch.float32)
     if state.shape != (B, H, Dk, Dv):
         raise ValueError("state must be [B,H,Dk,Dv]")
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else dt
     if out is None:
-        out = torch.empty((B, H, Dv), dtype=dt, device=q.device)
-    _lib._need_cuda("out", out, dt)
-    dims = _lib.make_dims(B, 1, H, Dk, Dv, nh, dt)
+        out = torch.empty((B, H, Dv), dtype=out_dtype, device=q.device)
+    _lib._need_cuda("out", out, out_dtype)
+    dims = _lib.make_dims(B, 1, H, Dk, Dv, nh, dt, "auto", out_dtype)
     rc = _lib.lib().dp_decode_step(dims, _lib._ptr(q), _lib._ptr(k), _lib._ptr(v),
                                    _lib._ptr(beta), _lib._ptr(g), _lib._ptr(state),
                                    _lib._ptr(out), _lib._stream(stream))

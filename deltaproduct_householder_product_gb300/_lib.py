@@ -29,7 +29,7 @@ class DPError(RuntimeError):
 class Dims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
                 ("Dk", ctypes.c_int), ("Dv", ctypes.c_int), ("nh", ctypes.c_int),
-                ("dtype", ctypes.c_int), ("impl", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("impl", ctypes.c_int), ("out_dtype", ctypes.c_int)]
 
 
 _LIB = None
@@ -99,9 +99,13 @@ def _need_cuda(name, t, dtype=None):
         raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
 
 
-def make_dims(B, T, H, Dk, Dv, nh, dtype, impl="auto"):
-    return Dims(B, T, H, Dk, Dv, nh, dtype if isinstance(dtype, int) else _dtype_code(dtype),
-                IMPLS[impl] if isinstance(impl, str) else int(impl))
+def make_dims(B, T, H, Dk, Dv, nh, dtype, impl="auto", out_dtype=None):
+    dt = dtype if isinstance(dtype, int) else _dtype_code(dtype)
+    if out_dtype is None:
+        od = dt
+    else:
+        od = out_dtype if isinstance(out_dtype, int) else _dtype_code(out_dtype)
+    return Dims(B, T, H, Dk, Dv, nh, dt, IMPLS[impl] if isinstance(impl, str) else int(impl), od)
 
 
 def workspace_size(dims):

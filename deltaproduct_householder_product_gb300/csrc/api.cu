@@ -28,6 +28,7 @@ dp_status check_dims(const dp_dims *d, bool decode)
     if (d->B < 0 || d->H < 0 || (!decode && d->T < 0)) return DP_ERR_INVALID_ARG;
     if (d->dtype != DP_F32 && d->dtype != DP_BF16) return DP_ERR_INVALID_ARG;
     if (d->impl < DP_IMPL_AUTO || d->impl > DP_IMPL_CHUNK_TC) return DP_ERR_INVALID_ARG;
+    if (d->out_dtype != d->dtype && d->out_dtype != DP_F32) return DP_ERR_INVALID_ARG;
     if (!supported_dim(d->Dk) || !supported_dim(d->Dv)) return DP_ERR_UNSUPPORTED;
     if (d->nh < 1 || d->nh > 4) return DP_ERR_UNSUPPORTED;
     // indices are formed in 64-bit, but keep every extent within int range
@@ -57,6 +58,7 @@ dp::Problem make_problem(const dp_dims *d, int T)
     memset(&p, 0, sizeof(p));
     p.B = d->B; p.T = T; p.H = d->H; p.Dk = d->Dk; p.Dv = d->Dv; p.nh = d->nh;
     p.dtype = d->dtype;
+    p.out_dtype = d->out_dtype;
     return p;
 }
 

@@ -13,7 +13,8 @@ namespace dp {
 // as documented in dp.h).
 struct Problem {
     int B, T, H, Dk, Dv, nh;
-    int dtype;                 // dp_dtype
+    int dtype;                 // dp_dtype of the inputs
+    int out_dtype;             // dp_dtype of o
     const void *q, *k, *v, *beta, *g;
     const float *h0;
     void *o;

@@ -26,12 +26,12 @@ __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float
 __device__ __forceinline__ void from_f(float *p, float x) { *p = x; }
 __device__ __forceinline__ void from_f(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
 
-template <int DK, typename TIn>
+template <int DK, typename TIn, typename TOut>
 __global__ void __launch_bounds__(kWarps * 32)
 recurrent_kernel(int T, int H, int Dv, int nh,
                  const TIn *__restrict__ q, const TIn *__restrict__ k,
                  const TIn *__restrict__ v, const TIn *__restrict__ beta,
-                 const TIn *__restrict__ g, const float *h0, TIn *__restrict__ o,
+                 const TIn *__restrict__ g, const float *h0, TOut *__restrict__ o,
                  float *h_final)
 {
     constexpr int R = DK / kWarps;            // key rows per warp
@@ -90,22 +90,22 @@ recurrent_kernel(int T, int H, int Dv, int nh,
     }
 }
 
-template <typename TIn>
+template <typename TIn, typename TOut>
 cudaError_t launch_typed(const Problem &p)
 {
     dim3 grid(p.B * p.H, p.Dv / kCols), block(kWarps * 32);
     const TIn *q = (const TIn *)p.q, *k = (const TIn *)p.k, *v = (const TIn *)p.v;
     const TIn *be = (const TIn *)p.beta, *g = (const TIn *)p.g;
-    TIn *o = (TIn *)p.o;
+    TOut *o = (TOut *)p.o;
     switch (p.Dk) {
     case 32:
-        recurrent_kernel<32, TIn><<<grid, block, 0, p.stream>>>(p.T, p.H, p.Dv, p.nh, q, k, v, be, g, p.h0, o, p.h_final);
+        recurrent_kernel<32, TIn, TOut><<<grid, block, 0, p.stream>>>(p.T, p.H, p.Dv, p.nh, q, k, v, be, g, p.h0, o, p.h_final);
         break;
     case 64:
-        recurrent_kernel<64, TIn><<<grid, block, 0, p.stream>>>(p.T, p.H, p.Dv, p.nh, q, k, v, be, g, p.h0, o, p.h_final);
+        recurrent_kernel<64, TIn, TOut><<<grid, block, 0, p.stream>>>(p.T, p.H, p.Dv, p.nh, q, k, v, be, g, p.h0, o, p.h_final);
         break;
     default:
-        recurrent_kernel<128, TIn><<<grid, block, 0, p.stream>>>(p.T, p.H, p.Dv, p.nh, q, k, v, be, g, p.h0, o, p.h_final);
+        recurrent_kernel<128, TIn, TOut><<<grid, block, 0, p.stream>>>(p.T, p.H, p.Dv, p.nh, q, k, v, be, g, p.h0, o, p.h_final);
         break;
     }
     return cudaGetLastError();
@@ -132,7 +132,9 @@ __global__ void state_io_kernel(int op, size_t n, int Dk, int Dv, float *state, 
 cudaError_t launch_recurrent(const Problem &p)
 {
     if (p.B * p.H == 0) return cudaSuccess;
-    return p.dtype == DP_F32 ? launch_typed<float>(p) : launch_typed<__nv_bfloat16>(p);
+    if (p.dtype == DP_F32) return launch_typed<float, float>(p);
+    if (p.out_dtype == DP_F32) return launch_typed<__nv_bfloat16, float>(p);
+    return launch_typed<__nv_bfloat16, __nv_bfloat16>(p);
 }
 
 cudaError_t launch_state_io(int op, int B, int H, int Dk, int Dv, float *state, void *ext,

@@ -117,10 +117,12 @@ def make_decode_inputs(w: Workload, steps: int, seed: int = LONG_DECODE_SEED):
                 g=None if g is None else g.to(dt).contiguous())
 
 
-def algorithmic_bytes(w: Workload, with_state_io=True):
-    """HBM bytes one forward call must move: q, k, v, beta, g, o, state I/O."""
+def algorithmic_bytes(w: Workload, with_state_io=True, out_bytes=None):
+    """HBM bytes one forward call must move: q, k, v, beta, g, o, state I/O.
+    ``out_bytes`` is the size of one element of o (default: the input size)."""
     el = 4 if w.dtype == "f32" else 2
-    per_tok_head = (w.Dk + w.nh * w.Dk + w.nh * w.Dv + w.nh + w.Dv) * el
+    ob = el if out_bytes is None else out_bytes
+    per_tok_head = (w.Dk + w.nh * w.Dk + w.nh * w.Dv + w.nh) * el + w.Dv * ob
     if w.gated:
         per_tok_head += el
     total = per_tok_head * w.B * w.T * w.H

@@ -23,7 +23,9 @@
  *     g    [B, T, H]  (NULL: ungated)
  *     o    [B, T, H, D_v]
  *     state (h0, h_final, decode state) [B, H, D_k, D_v], always fp32.
- * q, k, v, beta, g and o share the element type `dims->dtype`.
+ * q, k, v, beta and g share the element type `dims->dtype`; o has type
+ * `dims->out_dtype` (the input type, or fp32 with bf16 inputs: an fp32 o
+ * carries the kernel's fp32 accumulation without a final bf16 rounding).
  *
  * Errors: every entry point validates its arguments on the host first and
  * returns a non-zero dp_status without enqueuing anything when a check
@@ -68,12 +70,13 @@ typedef struct {
     int B, T, H;     /* batch, tokens, heads (T may be 0) */
     int Dk, Dv;      /* key and value head dims: 32, 64 or 128 */
     int nh;          /* Householder steps per token (n_h), 1..4 */
-    int dtype;       /* dp_dtype of q, k, v, beta, g, o */
+    int dtype;       /* dp_dtype of q, k, v, beta, g */
     int impl;        /* dp_impl */
+    int out_dtype;   /* dp_dtype of o: equal to dtype, or DP_F32 with bf16 inputs */
 } dp_dims;
 
 /* ABI version of this header (bumped on any signature change). */
-#define DP_ABI_VERSION 1
+#define DP_ABI_VERSION 2
 int dp_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */

@@ -1,0 +1,208 @@
+"""GPU parity of the tensor-core chunked kernel (tcgen05/TMEM/TMA) against the
+fp64 oracle, through the C ABI: small cases spanning several chunks with ragged
+tails, every n_h, gated/ungated, and the full-size workloads on sampled heads."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deltaproduct_householder_product_gb300 import workloads as W
+from tests.parity import assert_parity, err_stats
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dp():
+    from deltaproduct_householder_product_gb300 import build
+    build.build()
+    import deltaproduct_householder_product_gb300 as dp
+    assert torch.cuda.is_available()
+    assert dp.supports("chunk_tc", 1, 64, 1, 128, 128, 2), "tensor-core kernel unavailable"
+    return dp
+
+
+def cuda(x):
+    return {k: (None if v is None else v.cuda()) for k, v in x.items()}
+
+
+def run(dp, x, impl="chunk_tc", h0=True, out_dtype=torch.float32):
+    """Forward through the C ABI; o in fp32 by default (the tolerance is on the
+    kernel's arithmetic; a bf16 o adds its own final rounding, tested below)."""
+    xc = cuda(x)
+    ws = torch.zeros(dp.workspace_size(*_dims(x), impl=impl), dtype=torch.uint8, device="cuda")
+    o, hf = dp.forward(xc["q"], xc["k"], xc["v"], xc["beta"], xc["g"],
+                       xc["h0"] if h0 else None, impl=impl, workspace=ws, out_dtype=out_dtype)
+    dp.check_status(ws)
+    return o, hf
+
+
+def _dims(x):
+    B, T, H, nh, Dk = x["k"].shape
+    return B, T, H, Dk, x["v"].shape[-1], nh, x["q"].dtype
+
+
+def ref(x, h0=True):
+    return oracle.forward(x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"] if h0 else None)
+
+
+CASES = [(base, nh, T) for base in (W.BASE, W.NEARDUP, W.GATED, W.LONG)
+         for nh, T in ((base.nh, 150),)] + [
+    (W.BASE, 1, 200), (W.BASE, 3, 70), (W.BASE, 4, 33), (W.GATED, 1, 130), (W.GATED, 2, 97),
+    (W.GATED, 3, 64), (W.NEARDUP, 2, 65), (W.LONG, 4, 1), (W.LONG, 1, 5), (W.GATED, 4, 17)]
+
+
+@pytest.mark.parametrize("base,nh,T", CASES, ids=lambda v: getattr(v, "name", str(v)))
+def test_small_parity(dp, base, nh, T):
+    w = base.scaled(B=2, H=3, T=T, nh=nh)
+    x = W.make_inputs(w)
+    o, hf = run(dp, x)
+    ro, rh = ref(x)
+    assert_parity(o, ro, "bf16", "o")
+    assert_parity(hf, rh, "bf16", "h_final")
+
+
+@pytest.mark.parametrize("base", [W.BASE, W.GATED, W.NEARDUP], ids=lambda w: w.name)
+def test_bf16_output_is_rounded_fp32_output(dp, base):
+    """The bf16-output variant runs the same arithmetic and only rounds the final
+    store: it must equal the fp32 output rounded to nearest-even bf16, bit for bit."""
+    x = W.make_inputs(base.scaled(B=1, H=2, T=200))
+    o32, h32 = run(dp, x, out_dtype=torch.float32)
+    o16, h16 = run(dp, x, out_dtype=torch.bfloat16)
+    assert o16.dtype == torch.bfloat16
+    assert torch.equal(o16, o32.to(torch.bfloat16))
+    assert torch.equal(h16, h32)
+
+
+def test_zero_initial_state_and_no_final(dp):
+    w = W.GATED.scaled(B=1, H=2, T=100)
+    x = W.make_inputs(w)
+    xc = cuda(x)
+    o, hf = dp.forward(xc["q"], xc["k"], xc["v"], xc["beta"], xc["g"], None, impl="chunk_tc",
+                       h_final=False, out_dtype=torch.float32)
+    assert hf is None
+    ro, _ = ref(x, h0=False)
+    assert_parity(o, ro, "bf16", "o")
+
+
+def test_gate_reset_and_beta_zero(dp):
+    """g = 0 (reset) inside chunks and beta = 0 rows (pure decay): special cases
+    the gated chunk algebra must handle without NaN/Inf."""
+    w = W.GATED.scaled(B=1, H=2, T=90, nh=2)
+    x = W.make_inputs(w)
+    x["g"][:, 10] = 0.0
+    x["g"][:, 45] = 0.0
+    x["beta"][:, 20:40] = 0.0
+    o, hf = run(dp, x)
+    ro, rh = ref(x)
+    assert_parity(o, ro, "bf16", "o")
+    assert_parity(hf, rh, "bf16", "h_final")
+
+
+def test_matches_recurrent_kernel(dp):
+    w = W.NEARDUP.scaled(B=1, H=4, T=256)
+    x = W.make_inputs(w)
+    o1, h1 = run(dp, x, "chunk_tc")
+    o2, h2 = run(dp, x, "recurrent")
+    ro, rh = ref(x)
+    s1, s2 = err_stats(o1, ro), err_stats(o2, ro)
+    assert s1["rel_max"] <= 2e-2 and s2["rel_max"] <= 2e-2, (s1, s2)
+
+
+def sample_heads(x, pairs):
+    """Sub-problem with the chosen (b, h) sequences as a batch of single heads."""
+    out = {}
+    for k in ("q", "k", "v", "beta", "g"):
+        out[k] = None if x[k] is None else torch.stack([x[k][b, :, h] for b, h in pairs]).unsqueeze(2)
+    out["h0"] = None if x["h0"] is None else torch.stack([x["h0"][b, h] for b, h in pairs]).unsqueeze(1)
+    return out
+
+
+def gather_heads(t, pairs, time_axis=True):
+    """GPU result rows for the sampled (b, h) pairs, shaped like the oracle's."""
+    if time_axis:
+        return torch.stack([t[b, :, h] for b, h in pairs]).unsqueeze(2)
+    return torch.stack([t[b, h] for b, h in pairs]).unsqueeze(1)
+
+
+@pytest.mark.parametrize("base", [W.BASE, W.NEARDUP, W.GATED, W.LONG], ids=lambda w: w.name)
+def test_full_size_sampled_heads(dp, base):
+    """The full workload in the launch configuration the bench times; the oracle
+    checks a few whole (batch, head) sequences."""
+    x = W.make_inputs(base)
+    o, hf = run(dp, x)
+    rng = np.random.default_rng(7)
+    n = 2 if base.T > 10000 else 3
+    pairs = [(int(rng.integers(base.B)), int(rng.integers(base.H))) for _ in range(n)]
+    sub = sample_heads(x, pairs)
+    ro, rh = ref(sub)
+    assert_parity(gather_heads(o, pairs), ro, "bf16", "o")
+    assert_parity(gather_heads(hf, pairs, False), rh, "bf16", "h_final")
+
+
+def test_state_carry_on_chunk_boundaries_is_bit_exact(dp):
+    """When every call length is a multiple of the chunk (32 tokens at n_h = 2),
+    carrying the state across calls runs exactly the same arithmetic."""
+    w = W.BASE.scaled(B=2, H=4, T=1024)
+    xc = cuda(W.make_inputs(w))
+    o_one, h_one = dp.forward(xc["q"], xc["k"], xc["v"], xc["beta"], impl="chunk_tc",
+                              out_dtype=torch.float32)
+    state = torch.zeros_like(h_one)
+    outs = []
+    for s in range(4):
+        sl = slice(s * 256, (s + 1) * 256)
+        o_s, _ = dp.forward(xc["q"][:, sl].contiguous(), xc["k"][:, sl].contiguous(),
+                            xc["v"][:, sl].contiguous(), xc["beta"][:, sl].contiguous(), None,
+                            state, impl="chunk_tc", h_final=state, out_dtype=torch.float32)
+        outs.append(o_s)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat(outs, 1), o_one)
+    assert torch.equal(state, h_one)
+
+
+def test_long_state_carry_and_decode(dp):
+    """8 carried 4096-token calls vs one 32768-token call, then 4096 decode steps
+    continuing from the final state; checked against the oracle on sampled heads."""
+    w = W.LONG
+    x = W.make_inputs(w)
+    xc = cuda(x)
+    o_one, h_one = dp.forward(xc["q"], xc["k"], xc["v"], xc["beta"], None, None, impl="chunk_tc",
+                              out_dtype=torch.float32)
+    seg = w.T // W.LONG_CALLS
+    state = torch.zeros_like(h_one)
+    outs = []
+    for s in range(W.LONG_CALLS):
+        sl = slice(s * seg, (s + 1) * seg)
+        o_s, _ = dp.forward(xc["q"][:, sl].contiguous(), xc["k"][:, sl].contiguous(),
+                            xc["v"][:, sl].contiguous(), xc["beta"][:, sl].contiguous(), None,
+                            state, impl="chunk_tc", h_final=state, out_dtype=torch.float32)
+        outs.append(o_s)
+    o_car = torch.cat(outs, 1)
+    torch.cuda.synchronize()
+    # with n_h = 3 a chunk holds 21 tokens, so 4096-token calls cut the chunk
+    # grid elsewhere than one 32768-token call: both must meet the tolerance
+    # against the oracle; their mutual difference is rounding only
+    hs = [3, 11]
+    pairs = [(0, h) for h in hs]
+    sub = sample_heads(x, pairs)
+    ro, rh = ref(sub)                                   # [2, T, 1, Dv], [2, 1, Dk, Dv]
+    assert_parity(gather_heads(o_one, pairs), ro, "bf16", "o (single call)")
+    assert_parity(gather_heads(h_one, pairs, False), rh, "bf16", "h_final (single call)")
+    assert_parity(gather_heads(o_car, pairs), ro, "bf16", "o (8 carried calls)")
+    assert_parity(gather_heads(state, pairs, False), rh, "bf16", "h_final (8 carried calls)")
+    mutual = err_stats(o_car, o_one)
+    assert mutual["rel_max"] <= 2e-2, mutual
+
+    steps = 4096
+    d = W.make_decode_inputs(w, steps)
+    dc = cuda(d)
+    st = h_one.clone()
+    o_dec = torch.empty(steps, w.B, w.H, w.Dv, dtype=torch.float32, device="cuda")
+    for i in range(steps):
+        dp.decode_step(dc["q"][i], dc["k"][i], dc["v"][i], dc["beta"][i], None, st, out=o_dec[i])
+    torch.cuda.synchronize()
+    # the oracle runs the same decode inputs as one sequence from its own final state
+    seq = {k: torch.stack([d[k][:, 0, h] for h in hs]).unsqueeze(2) for k in ("q", "k", "v", "beta")}
+    rdo, rdh = oracle.forward(seq["q"], seq["k"], seq["v"], seq["beta"], None, rh)
+    assert_parity(torch.stack([o_dec[:, 0, h] for h in hs]).unsqueeze(2), rdo, "bf16", "decode o")
+    assert_parity(gather_heads(st, pairs, False), rdh, "bf16", "decode state")
