@@ -11,7 +11,7 @@ import torch
 from . import _lib
 from ._lib import DPError, STATE_EXPORT, STATE_IMPORT, STATE_ZERO  # noqa: F401
 
-__all__ = ["forward", "supports", "decode_step", "state_io", "check_status", "workspace_size",
+__all__ = ["forward", "forward_noalloc", "supports", "decode_step", "state_io", "check_status", "workspace_size",
            "DPError", "abi_version"]
 
 
@@ -79,6 +79,28 @@ def forward(q, k, v, beta, g=None, h0=None, *, impl="auto", out=None, h_final=Tr
         _lib._ptr(h0), _lib._ptr(out), _lib._ptr(h_final), _lib._ptr(workspace),
         workspace.numel() * workspace.element_size(), _lib._stream(stream))
     _lib._check(rc, "dp_forward")
+    return out, h_final
+
+
+def forward_noalloc(q, k, v, beta, g=None, h0=None, *, impl="auto", out, h_final=None,
+                    stream=None):
+    """dp_forward_noalloc: ``forward`` without a device workspace, for callers
+    that cannot allocate device memory; the library's fixed scratch array is
+    used instead. ``out`` (and ``h_final`` if wanted) must be given. Calls on
+    one device whose kernels overlap on the GPU race on that shared scratch."""
+    B, T, H, nh, Dk = k.shape
+    Dv = v.shape[-1]
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g)):
+        _lib._need_cuda(name, t, dt)
+    _lib._need_cuda("h0", h0, torch.float32)
+    _lib._need_cuda("out", out)
+    _lib._need_cuda("h_final", h_final, torch.float32)
+    dims = _lib.make_dims(B, T, H, Dk, Dv, nh, dt, impl, out.dtype)
+    rc = _lib.lib().dp_forward_noalloc(
+        dims, _lib._ptr(q), _lib._ptr(k), _lib._ptr(v), _lib._ptr(beta), _lib._ptr(g),
+        _lib._ptr(h0), _lib._ptr(out), _lib._ptr(h_final), _lib._stream(stream))
+    _lib._check(rc, "dp_forward_noalloc")
     return out, h_final
 
 

@@ -52,8 +52,9 @@ def lib():
         L.dp_decode_step.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 7 + [_vp]
         L.dp_state_io.argtypes = [ctypes.c_int] * 5 + [_vp, _vp, ctypes.c_int, ctypes.c_int, _vp]
         L.dp_check_status.argtypes = [_vp, _vp]
+        L.dp_forward_noalloc.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 9
         for name in ("dp_forward_workspace_size", "dp_forward", "dp_decode_step",
-                     "dp_state_io", "dp_check_status"):
+                     "dp_state_io", "dp_check_status", "dp_forward_noalloc"):
             getattr(L, name).restype = ctypes.c_int
         _LIB = L
     return _LIB

@@ -121,6 +121,27 @@ dp_status dp_state_io(int op, int B, int H, int Dk, int Dv, float *state,
  * workspace since it was last cleared, and clears it. */
 dp_status dp_check_status(const void *workspace, dp_stream_t stream);
 
+/* dp_forward for callers that cannot allocate device memory (their HBM is
+ * owned by a framework allocator or a fixed memory budget, or cudaMalloc's
+ * implicit synchronisation is not acceptable on their path). This entry
+ * point is a library facility; the DeltaProduct paper has no counterpart.
+ * Same arguments, layouts and results as dp_forward, without the workspace:
+ * the scratch lives in a fixed 64 KiB device array inside libdp.so that
+ * every GPU loading the library holds until the process exits, and the call
+ * allocates nothing. Problems whose dp_forward_workspace_size exceeds 64 KiB
+ * return DP_ERR_WORKSPACE. The first call made with a device current looks
+ * up the array's device address (cudaGetSymbolAddress); make that first
+ * call before any stream capture. All calls on a device share the array:
+ * calls whose kernels overlap on the GPU (unordered streams) race on it;
+ * calls ordered on one stream are safe. Device-side wait timeouts are not
+ * reported by this entry point (each call clears the array's status word
+ * behind its kernel); host-side validation and launch errors are. */
+dp_status dp_forward_noalloc(const dp_dims *dims,
+                             const void *q, const void *k, const void *v,
+                             const void *beta, const void *g,
+                             const float *h0, void *o, float *h_final,
+                             dp_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
