@@ -5,19 +5,42 @@
 // form an extended T*n_h DeltaNet sequence, the gate is applied once per
 // token, only the last step of each token is read out; chunk transform from
 // the OSDN paper, App.A.2 / App.C, with write key = read key, state H = S^T).
-// Per chunk of ct = floor(64/n_h) whole tokens (R = ct*n_h <= 64 rows of the
-// extended sequence, padded with beta = 0 rows, which are exact no-ops), with
-// L_r the cumulative log-gate from the chunk start, Gamma_r = exp(L_r),
+// Per chunk of ct whole tokens (R = ct*n_h <= 32 rows of the extended
+// sequence, padded with beta = 0 rows, which are exact no-ops), with L_r the
+// cumulative log-gate from the chunk start, Gamma_r = exp(L_r) and
 // E_rs = exp(L_r - L_s):
-//   G     = tril(diag(beta) (K K^T * E), -1)          Gram        (tcgen05)
-//   T     = (I + G)^{-1}                              UT transform (CUDA cores)
-//   W     = T diag(beta*Gamma) K,  U = T diag(beta) V              (tcgen05)
-//   U'    = U - W H0                                  state pass   (tcgen05)
-//   H     = Gamma_C H0 + K^T diag(Gamma_C/Gamma) U'               (tcgen05)
-//   o_t   = Gamma_r H0^T q_t + sum_{s<=r} E_rs (q_t.k_s) u'_s, r = last row of t
-// The state stays in TMEM for the whole sequence. Everything is computed in
-// the transposed orientation (M = D_v = 128 lanes: lane = value column) so
-// that the state and U' feed the next MMA straight from TMEM as the A operand.
+//   G   = tril(diag(beta) (K K^T * E), -1)               Gram
+//   T   = (I + G)^{-1}                                   UT transform
+//   W   = T diag(beta*Gamma) K,  U = T diag(beta) V
+//   U'  = U - W S0                                       state pass, part 1
+//   S   = Gamma_C S0 + K^T diag(Gamma_C/Gamma) U'        state pass, part 2
+//   o_t = Gamma_r S0^T q_t + sum_{s<=r} E_rs (q_t.k_s) u'_s,  r = last row of t
+//
+// Organisation (one CTA per (batch, head), the state S^T resident in TMEM
+// for the whole sequence, lanes = value columns):
+//  * warp 20   TMA producer: K, Q, V tiles of each chunk, 3-stage ring.
+//  * warp 21   state-pass MMA issuer (one thread, tf32):
+//              [U' | O_b] += S [-W; Gamma q]^T and [S | O_a] += U'^T [K^T; P].
+//              These MMAs read S and U' straight from their fp32 TMEM
+//              accumulators as the A operand; consecutive MMAs are executed
+//              in issue order, so the chain S -> U' -> S needs no thread
+//              round trip. The readout rides along in the same instructions
+//              (stacked B operands), since each MMA instruction costs about
+//              the same issue time whatever its N.
+//  * warp 22   prep MMA issuer (bf16: [K;Q] K^T, U, W), one chunk ahead, on
+//              its own thread so its issue latency overlaps the state pass.
+//  * warps 4-11 and 12-19: two prep groups, taking even and odd chunks.
+//              Phase A (needs only the chunk's inputs): turn the Gram MMA
+//              into G and P, solve T on CUDA cores (16x16 diagonal blocks by
+//              forward substitution, one lane per column, then the
+//              off-diagonal block), write T as bf16 hi/lo tiles for the U/W
+//              MMAs. Phase B (once the state pass has released the group's
+//              buffers): write the fp32 B tiles of the state pass (P, Gamma q,
+//              decayed K^T, and -W once the W MMA is done).
+//  * warps 0-3 epilogue: initial state in, outputs and final state out; for
+//              gated inputs also S <- Gamma_C S between the two halves.
+// Every wait on an mbarrier is bounded; on expiry the CTA records a timeout
+// in the caller's status word, drains what it has in flight and exits.
 #include <string.h>
 
 #include "internal.h"
@@ -30,43 +53,66 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kD = 128;            // D_k = D_v
-constexpr int kC = 64;             // extended rows per chunk (padded)
-constexpr int kThreads = 128;      // thread i <-> TMEM lane i
+constexpr int kD = 128;        // D_k = D_v
+constexpr int kC = 32;         // extended rows per chunk (padded)
+constexpr int kNQ = 16;        // readout columns per chunk (tokens, padded)
+constexpr int kNS = 3;         // TMA stages
 
-// TMEM column map (512 columns allocated)
-// The state and U' enter their MMAs as A operands from TMEM in two bf16
-// parts, x = hi + lo with hi = bf16(x) and lo = bf16(x - hi), which carries
-// about 16 mantissa bits; the B operands are single bf16 tiles.
-constexpr uint32_t kColS = 0;      // S^T fp32, lane = dv, 128 cols = dk
-constexpr uint32_t kColSB = 128;   // bf16 hi part of S^T, 64 cols
-constexpr uint32_t kColUN = 192;   // U'^T fp32, 64 cols = chunk rows; then lo parts of U'
-constexpr uint32_t kColUB = 256;   // bf16 hi part of U'^T, 32 cols
-constexpr uint32_t kColUBD = 288;  // bf16 hi part of U'^T * Gamma_C/Gamma_s (gated), 32 cols
-constexpr uint32_t kColO = 320;    // O^T fp32, up to 64 cols = tokens
-constexpr uint32_t kColGW = 384;   // [K;Q] K^T fp32, then W^T fp32 (lane = dk); then lo part of S^T
-constexpr uint32_t kColSBL = kColGW;       // bf16 lo part of S^T, 64 cols
-constexpr uint32_t kColUBL = kColUN;       // bf16 lo part of U'^T, 32 cols
-constexpr uint32_t kColUBDL = kColUN + 32; // bf16 lo part of the decayed U'^T, 32 cols
+constexpr int kPrepWarp = 4;   // warps 0-3 epilogue; 4-11 prep group 0, 12-19 prep group 1
+constexpr int kPrepThreads = 256;
+constexpr int kTmaWarp = 20;   // warp 21: state-pass MMA issuer; warp 22: prep MMA issuer
+constexpr int kChainWarp = 21;
+constexpr int kThreads = 23 * 32;
+
+// ---- TMEM columns (512 allocated)
+// The readout accumulates in two parts per chunk buffer g: O_b next to
+// U'[g] (filled by the first state-pass MMA, B = [-W; Gamma q]) and O_a next
+// to S (filled by the second, B = [K^T; P] or [P; K^T]); o = O_a + O_b.
+constexpr uint32_t kColOa0 = 0;    // O_a[0]: 16 columns, left of S
+constexpr uint32_t kColS = 16;     // S^T fp32: 128 columns (dk), lane = dv
+constexpr uint32_t kColOa1 = 144;  // O_a[1]: 16 columns, right of S
+constexpr uint32_t kColUN = 160;   // U'^T[g] at 160 + 48 g (32 columns), O_b[g] right after (16)
+constexpr uint32_t kColGQ = 256;   // [K;Q] K^T fp32 (M = 64 layout): 2 x 32 columns
+constexpr uint32_t kColW = 320;    // W^T fp32: 2 x 32 columns (chunk rows), lane = dk
 constexpr uint32_t kTmemCols = 512;
+__host__ __device__ constexpr uint32_t col_un(int g) { return kColUN + 48 * g; }
+__host__ __device__ constexpr uint32_t col_ob(int g) { return kColUN + 48 * g + 32; }
+__host__ __device__ constexpr uint32_t col_oa(int g) { return g ? kColOa1 : kColOa0; }
 
-// Shared memory map (bytes from a 1024-aligned base)
-constexpr uint32_t kKQBytes = 2 * 128 * 128;       // 2 blocks of 64 dk x 128 rows (K rows 0..63, Q rows 64..127)
-constexpr uint32_t kVBytes = 2 * 64 * 128;         // 2 blocks of 64 dv x 64 rows
-constexpr uint32_t kStageBytes = kKQBytes + kVBytes;
-constexpr uint32_t kOffStage = 0;                  // 2 stages
-constexpr uint32_t kOffTb = 2 * kStageBytes;       // T diag(beta), bf16 64 x 64, K-major
-constexpr uint32_t kOffTbg = kOffTb + 8192;        // T diag(beta Gamma)
-constexpr uint32_t kOffP = kOffTbg + 8192;         // P = tril(Q K^T * E), bf16 hi part, 64 x 64
-constexpr uint32_t kOffPL = kOffP + 8192;          // bf16 lo part of P
-constexpr uint32_t kOffNW = kOffPL + 8192;         // -W, MN-major (rows dk, 64 i), 16 KB
-constexpr uint32_t kOffG = kOffNW + 16384;         // fp32 G [64][65]
-constexpr uint32_t kLd = 65;
-constexpr uint32_t kOffT = kOffG + 64 * kLd * 4;   // fp32 T [64][65]
-constexpr uint32_t kOffX = kOffT + 64 * kLd * 4;   // fp32 scratch [3][16][17]
-constexpr uint32_t kOffVec = kOffX + 3 * 16 * 17 * 4;   // beta[64], L[64]
-constexpr uint32_t kOffBar = kOffVec + 2 * 64 * 4;      // barriers + misc (64 B)
-constexpr uint32_t kSmemBytes = kOffBar + 64 + 1024;    // + alignment slack
+// ---- shared memory (offsets from a 1024-aligned base)
+// TMA stage: KQ = 2 blocks (dk 0-63, 64-127) x 64 rows x 128 B (rows 0-31 K,
+// rows 32-47 Q), V = 2 blocks (dv halves) x 32 rows x 128 B; bf16, 128-B swizzle.
+constexpr uint32_t kKQBlock = 64 * 128;
+constexpr uint32_t kVBlock = 32 * 128;
+constexpr uint32_t kStageBytes = 2 * kKQBlock + 2 * kVBlock;          // 24 KB
+// Per prep group: fp32 B tiles of the state pass (K-major, 128-B swizzle,
+// 32 fp32 per 128-B row) and bf16 T tiles.
+// X = [-W (rows 0-31); Gamma q (rows 32-47)]: 4 K-blocks (dk) x 48 rows.
+// Y = decayed K^T (128 rows, dk) and P (16 rows, token) over K = 32 chunk
+// rows: group 0 stores [P; K^T], group 1 [K^T; P], matching O_a's side of S.
+constexpr uint32_t kXRows = kC + kNQ;                 // 48
+constexpr uint32_t kXBlock = kXRows * 128;            // 6 KB
+constexpr uint32_t kYRows = kD + kNQ;                 // 144
+constexpr uint32_t kGX = 0;
+constexpr uint32_t kGY = kGX + 4 * kXBlock;           // 24 KB
+constexpr uint32_t kGTb = kGY + kYRows * 128;         // + 18 KB; T tiles: 4 x (32 rows x 128 B)
+constexpr uint32_t kTTile = 32 * 128;
+constexpr uint32_t kGroupTiles = kGTb + 4 * kTTile;  // 58 KB
+constexpr uint32_t kLd = 33;                          // fp32 scratch row stride
+constexpr uint32_t kGGs = 0;                          // G [32][33]
+constexpr uint32_t kGTs = kGGs + 32 * kLd * 4;        // T [32][33]
+constexpr uint32_t kGXs = kGTs + 32 * kLd * 4;        // X [16][17]
+constexpr uint32_t kGPs = kGXs + 16 * 17 * 4;         // P staging [16][33]
+constexpr uint32_t kGBeta = kGPs + 16 * kLd * 4;      // beta[32]
+constexpr uint32_t kGL = kGBeta + 32 * 4;             // L[32]
+constexpr uint32_t kGroupScratch = ((kGL + 32 * 4) + 15) & ~15u;
+
+constexpr uint32_t kOffStage = 0;
+constexpr uint32_t kOffGroup = kOffStage + kNS * kStageBytes;
+constexpr uint32_t kOffScratch = kOffGroup + 2 * kGroupTiles;
+constexpr uint32_t kOffBar = kOffScratch + 2 * kGroupScratch;
+constexpr uint32_t kNumBars = 2 * kNS + 2 * 6 + 5;
+constexpr uint32_t kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
 
 constexpr uint32_t kWaitTries = 1u << 22;
 
@@ -76,7 +122,7 @@ struct Params {
     void *o;
     float *h_final;
     uint32_t *status;
-    int T, H, nh, ct, nq, n_chunks;
+    int T, H, nh, ct, n_chunks;
 };
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
@@ -110,27 +156,59 @@ bool encode(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+enum : int {
+    kBarFull = 0,                 // [kNS] TMA stage loaded (transaction bytes)
+    kBarEmpty = kBarFull + kNS,   // [kNS] stage consumed by its prep group
+    kBarGQ = kBarEmpty + kNS,     // [2] Gram MMA of the group's chunk done
+    kBarTb = kBarGQ + 2,          // [2] T tiles written
+    kBarUW = kBarTb + 2,          // [2] U and W MMAs done
+    kBarReady = kBarUW + 2,       // [2] state-pass B tiles written
+    kBarM2 = kBarReady + 2,       // [2] chunk's state pass and readout done
+    kBarOFree = kBarM2 + 2,       // [2] O buffers drained by the epilogue
+    kBarM1 = kBarOFree + 2,       // first half (U', S^T q) done (gated)
+    kBarScaled,                   // S scaled by Gamma_C (gated)
+    kBarInit,                     // initial state in TMEM
+    kBarFinal,                    // [2] every MMA of an issuer retired (teardown)
+    kBarCount = kBarFinal + 2
+};
+static_assert(kBarCount == (int)kNumBars, "barrier count");
 
-__device__ __forceinline__ void flag_error(uint32_t *status, volatile uint32_t *abort_s, uint32_t code)
+struct Smem {
+    uint8_t *base;
+    uint64_t *bar;
+    uint32_t *tmem_slot;
+    volatile uint32_t *abort;
+    __device__ uint8_t *stage(int st) const { return base + kOffStage + st * kStageBytes; }
+    __device__ uint8_t *group(int g) const { return base + kOffGroup + g * kGroupTiles; }
+    __device__ uint8_t *scratch(int g) const { return base + kOffScratch + g * kGroupScratch; }
+};
+
+__device__ __forceinline__ void flag_error(uint32_t *status, volatile uint32_t *abort, uint32_t code)
 {
-    *abort_s = 1;
+    *abort = 1;
     if (status) atomicCAS(status, 0u, code);
 }
 
-// Load 64 consecutive fp32 TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld64f(uint32_t taddr, float (&v)[64])
+__device__ __forceinline__ bool wait_bar(const Smem &s, int idx, uint32_t parity, uint32_t *status)
 {
-    uint32_t r[16];
-#pragma unroll
-    for (int c0 = 0; c0 < 64; c0 += 16) {
-        tmem_ld16(taddr + c0, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) v[c0 + j] = __uint_as_float(r[j]);
-    }
+    if (mbar_wait(&s.bar[idx], parity, kWaitTries, s.abort)) return true;
+    flag_error(status, s.abort, kDevTimeout);
+    return false;
 }
 
-// hi/lo bf16 pairs of (a, b): hi = bf16(x), lo = bf16(x - hi)
+// OR of `v` over the `count` threads of named barrier `id` (also a barrier).
+__device__ __forceinline__ bool group_any(uint32_t id, uint32_t count, bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 __device__ __forceinline__ void split_pack(float a, float b, uint32_t &hi, uint32_t &lo)
 {
     hi = pack_bf16x2(a, b);
@@ -141,443 +219,502 @@ __device__ __forceinline__ void split_pack(float a, float b, uint32_t &hi, uint3
 __device__ __forceinline__ void store_out(float *o, size_t i, float x) { o[i] = x; }
 __device__ __forceinline__ void store_out(__nv_bfloat16 *o, size_t i, float x) { o[i] = __float2bfloat16_rn(x); }
 
+// ------------------------------------------------------------------ TMA producer
+__device__ void tma_role(const Smem &s, const Params &p, const CUtensorMap *tk,
+                         const CUtensorMap *tv, const CUtensorMap *tq, int b, int h)
+{
+    const int ct = p.ct, R = ct * p.nh;
+    const uint32_t bytes = 512u * R + 256u * ct;   // K and V: 2 x R rows x 128 B each; Q: 2 x ct rows
+    int last_use[kNS];
+    for (int i = 0; i < kNS; ++i) last_use[i] = -1;
+    for (int c = 0; c < p.n_chunks; ++c) {
+        const int st = c % kNS, u = c / kNS;
+        if (u >= 1 && !wait_bar(s, kBarEmpty + st, (u - 1) & 1, p.status)) break;
+        uint8_t *kq = s.stage(st), *vv = kq + 2 * kKQBlock;
+        uint64_t *bar = &s.bar[kBarFull + st];
+        mbar_arrive_expect_tx(bar, bytes);
+        const int t0 = c * ct;
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+            tma_load_5d(kq + kb * kKQBlock, tk, bar, kb * 64, 0, h, t0, b);
+            tma_load_4d(kq + kb * kKQBlock + kC * 128, tq, bar, kb * 64, h, t0, b);
+            tma_load_5d(vv + kb * kVBlock, tv, bar, kb * 64, 0, h, t0, b);
+        }
+        last_use[st] = u;
+    }
+    // every issued load must have landed before shared memory is released
+    uint32_t no_abort = 0;
+    for (int st = 0; st < kNS; ++st)
+        if (last_use[st] >= 0) mbar_wait(&s.bar[kBarFull + st], last_use[st] & 1, kWaitTries, &no_abort);
+}
+
+// ------------------------------------------------------------------ MMA issuers
+// Prep MMAs (bf16): [K;Q] K^T, U^T = V^T (T diag beta)^T, W^T = K^T (T diag(beta Gamma))^T.
+// They run one chunk ahead of the state pass and are issued by their own
+// thread so that their issue latency overlaps the state pass's.
+__device__ void prep_mma_role(const Smem &s, const Params &p, uint32_t tbase)
+{
+    const bool gated = p.g != nullptr;
+    const int n = p.n_chunks;
+    const uint32_t id_gq = idesc_bf16(64, kC, false, false);
+    const uint32_t id_uw = idesc_bf16(128, kC, true, false);
+
+    // [K;Q] K^T: A = 64 rows (K rows 0-31, Q rows 32-47, zero rows), B = K rows
+    auto issue_gq = [&](int c) {
+        const int g = c & 1;
+        const uint32_t kq = smem_addr(s.stage(c % kNS));
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t d = sdesc_sw128(kq + (kk >> 2) * kKQBlock + (kk & 3) * 32, 16, 1024);
+            mma_ss(tbase + kColGQ + g * 32, d, d, id_gq, kk > 0);
+        }
+        mma_commit(&s.bar[kBarGQ + g]);
+    };
+    // T enters as hi + lo bf16 tiles
+    auto issue_uw = [&](int c) {
+        const int g = c & 1;
+        const uint32_t kq = smem_addr(s.stage(c % kNS)), vv = kq + 2 * kKQBlock;
+        const uint32_t tt = smem_addr(s.group(g)) + kGTb;
+        const uint32_t tg = tt + (gated ? 2 * kTTile : 0);
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk)
+                mma_ss(tbase + col_un(g), sdesc_sw128(vv + kk * 2048, kVBlock, 1024),
+                       sdesc_sw128(tt + part * kTTile + kk * 32, 16, 1024), id_uw, part | kk);
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk)
+                mma_ss(tbase + kColW + g * 32, sdesc_sw128(kq + kk * 2048, kKQBlock, 1024),
+                       sdesc_sw128(tg + part * kTTile + kk * 32, 16, 1024), id_uw, part | kk);
+        mma_commit(&s.bar[kBarUW + g]);
+    };
+    // U/W of chunk u: its T tiles are written, and the state pass of chunk
+    // u - 2 (which read U'[g]) has finished
+    auto uw_ready = [&](int u) {
+        if (!wait_bar(s, kBarTb + (u & 1), (u >> 1) & 1, p.status)) return false;
+        if (u >= 2 && !wait_bar(s, kBarM2 + (u & 1), ((u - 2) >> 1) & 1, p.status)) return false;
+        tc_fence_after();
+        return true;
+    };
+
+    bool ok = true;
+    for (int c = 0; c < n && ok; ++c) {
+        if (!(ok = wait_bar(s, kBarFull + c % kNS, (c / kNS) & 1, p.status))) break;
+        tc_fence_after();
+        issue_gq(c);
+        if (c >= 1) {
+            if (!(ok = uw_ready(c - 1))) break;
+            issue_uw(c - 1);
+        }
+    }
+    if (ok && uw_ready(n - 1)) issue_uw(n - 1);
+    mma_commit(&s.bar[kBarFinal + 1]);
+    uint32_t no_abort = 0;
+    mbar_wait(&s.bar[kBarFinal + 1], 0, kWaitTries, &no_abort);
+}
+
+// State-pass MMAs (tf32, A = the fp32 accumulators in TMEM):
+//   [U'^T | O_b] += S^T [-W; Gamma q]^T          (16 instructions, N = 48)
+//   [S^T | O_a] or [O_a | S^T] += U'^T [K^T; P]   (4 instructions, N = 144)
+// Consecutive MMAs run in issue order, so S -> U' -> S needs no round trip.
+__device__ void chain_role(const Smem &s, const Params &p, uint32_t tbase)
+{
+    const bool gated = p.g != nullptr;
+    const int n = p.n_chunks;
+    const uint32_t id_x = idesc_tf32(128, kXRows);
+    const uint32_t id_y = idesc_tf32(128, kYRows);
+    bool ok = wait_bar(s, kBarInit, 0, p.status);
+    for (int c = 0; c < n && ok; ++c) {
+        const int g = c & 1;
+        const uint32_t gb = smem_addr(s.group(g));
+        if (!(ok = wait_bar(s, kBarReady + g, (c >> 1) & 1, p.status))) break;
+        if (c >= 2 && !(ok = wait_bar(s, kBarOFree + g, ((c - 2) >> 1) & 1, p.status))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk)
+            mma_ts_tf32(tbase + col_un(g), tbase + kColS + kk * 8,
+                        sdesc_sw128(gb + kGX + (kk >> 2) * kXBlock + (kk & 3) * 32, 16, 1024), id_x, 1);
+        if (gated) {
+            mma_commit(&s.bar[kBarM1]);
+            if (!(ok = wait_bar(s, kBarScaled, c & 1, p.status))) break;
+            tc_fence_after();
+        }
+        const uint32_t d_y = g ? tbase + kColS : tbase + kColOa0;   // O_a[0] | S  or  S | O_a[1]
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_ts_tf32(d_y, tbase + col_un(g) + kk * 8, sdesc_sw128(gb + kGY + kk * 32, 16, 1024), id_y, 1);
+        mma_commit(&s.bar[kBarM2 + g]);
+    }
+    mma_commit(&s.bar[kBarFinal]);
+    uint32_t no_abort = 0;
+    mbar_wait(&s.bar[kBarFinal], 0, kWaitTries, &no_abort);
+}
+
+// ------------------------------------------------------------------ prep groups
+// Per-row betas and cumulative log-gates of one chunk, held by warp 0 of a
+// prep group (lane = extended row), loaded one chunk ahead.
+struct RowVals {
+    float beta, lg;
+};
+
+__device__ __forceinline__ RowVals load_rows(const Params &p, int c, int b, int h, int lane)
+{
+    RowVals v{0.f, 0.f};
+    if (c >= p.n_chunks) return v;
+    const int nh = p.nh, R = p.ct * nh, tl = lane / nh, j = lane - tl * nh, t = c * p.ct + tl;
+    if (lane < R && t < p.T) {
+        const size_t tok = ((size_t)b * p.T + t) * p.H + h;
+        v.beta = __bfloat162float(p.beta[tok * nh + j]);
+        if (p.g != nullptr && j == 0) v.lg = fmaxf(logf(__bfloat162float(p.g[tok])), -80.f);
+    }
+    return v;
+}
+
+// Row offsets of K^T and P inside the group's Y tile.
+__device__ __forceinline__ int y_row_k(int g) { return g ? 0 : kNQ; }
+__device__ __forceinline__ int y_row_p(int g) { return g ? kD : 0; }
+
+__device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g, int b, int h)
+{
+    const int lt = threadIdx.x - (kPrepWarp + 8 * g) * 32, lw = lt >> 5, lane = lt & 31;
+    const int lq = lw & 3, hf = lw >> 2;                          // TMEM lane quarter, column half
+    const uint32_t bar_id = 1 + g;
+    const uint32_t trow = tbase + ((uint32_t)(lq * 32) << 16);   // this warp's TMEM lanes
+    uint8_t *gt = s.group(g), *sc = s.scratch(g);
+    float *Gs = (float *)(sc + kGGs), *Ts = (float *)(sc + kGTs), *Xs = (float *)(sc + kGXs);
+    float *Ps = (float *)(sc + kGPs), *beta_s = (float *)(sc + kGBeta), *L_s = (float *)(sc + kGL);
+    const int nh = p.nh, ct = p.ct;
+    const bool gated = p.g != nullptr;
+
+    RowVals rv{0.f, 0.f};
+    if (lw == 0) rv = load_rows(p, g, b, h, lane);
+
+    for (int c = g; c < p.n_chunks; c += 2) {
+        const int st = c % kNS;
+        const uint8_t *kq = s.stage(st);
+
+        // ---------------- phase A: G, P, T (needs only this chunk's inputs)
+        if (lw == 0) {
+            float lg = rv.lg;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, lg, d);
+                if (lane >= d) lg += y;
+            }
+            beta_s[lane] = rv.beta;
+            L_s[lane] = lg;
+            rv = load_rows(p, c + 2, b, h, lane);        // next chunk of this group
+        }
+        bool ok = wait_bar(s, kBarFull + st, (c / kNS) & 1, p.status);
+        if (ok) ok = wait_bar(s, kBarGQ + g, (c >> 1) & 1, p.status);
+        if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) break;
+        tc_fence_after();
+
+        // Gram MMA (M = 64 layout): quarter lq's lanes 0..15 hold rows
+        // 16*lq .. 16*lq + 15; half hf takes columns 16*hf .. 16*hf + 15.
+        {
+            uint32_t r[16];
+            tmem_ld16(trow + kColGQ + g * 32 + 16 * hf, r);
+            tmem_wait_ld();
+            const int m = 16 * lq + lane;
+            if (lane < 16 && m < kC) {
+                const float br = beta_s[m], Lr = L_s[m];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int s2 = 16 * hf + j;
+                    float v = 0.f;
+                    if (s2 < m) {
+                        v = br * __uint_as_float(r[j]);
+                        if (gated) v *= __expf(Lr - L_s[s2]);
+                    }
+                    Gs[m * kLd + s2] = v;
+                }
+            } else if (lane < 16 && m < kC + kNQ) {
+                const int i = m - kC, rr = i * nh + nh - 1;
+                const bool valid = i < ct;
+                const float Lr = valid ? L_s[rr] : 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int s2 = 16 * hf + j;
+                    float x = 0.f;
+                    if (valid && s2 <= rr) {
+                        x = __uint_as_float(r[j]);
+                        if (gated) x *= __expf(Lr - L_s[s2]);
+                    }
+                    Ps[i * kLd + s2] = x;
+                }
+            }
+        }
+        tc_fence_before();
+        named_sync(bar_id, kPrepThreads);
+
+        // T = (I + G)^{-1}: diagonal 16x16 blocks (one lane per column,
+        // forward substitution), then T_10 = -T_11 (G_10 T_00)
+        if (lw < 2 && lane < 16) {
+            const int base = 16 * lw, col = base + lane;
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[i] = (i == lane) ? 1.f : 0.f;
+#pragma unroll
+            for (int s2 = 0; s2 < 16; ++s2) {
+                const float xs = x[s2];
+#pragma unroll
+                for (int i = s2 + 1; i < 16; ++i) x[i] = fmaf(-Gs[(base + i) * kLd + base + s2], xs, x[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) Ts[(base + i) * kLd + col] = x[i];
+        }
+        named_sync(bar_id, kPrepThreads);
+        {
+            const int i = lt >> 4, j = lt & 15;
+            float a = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) a = fmaf(Gs[(16 + i) * kLd + m], Ts[m * kLd + j], a);
+            Xs[i * 17 + j] = a;
+        }
+        named_sync(bar_id, kPrepThreads);
+        {
+            const int i = lt >> 4, j = lt & 15;
+            float a = 0.f;
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+                if (u <= i) a = fmaf(Ts[(16 + i) * kLd + 16 + u], Xs[u * 17 + j], a);
+            Ts[(16 + i) * kLd + j] = -a;
+        }
+        named_sync(bar_id, kPrepThreads);
+
+        // T diag(beta) and T diag(beta Gamma) as hi + lo bf16 tiles:
+        // one (tile, row, 8-element chunk) per thread
+        if (lt < (gated ? 256 : 128)) {
+            const int pr = lt >> 7, i = (lt >> 2) & 31, ch = lt & 3;
+            uint8_t *hi = gt + kGTb + 2 * pr * kTTile, *lo = hi + kTTile;
+            uint32_t wh[4], wl[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int s0 = ch * 8 + 2 * e;
+                float v0 = s0 <= i ? Ts[i * kLd + s0] * beta_s[s0] : 0.f;
+                float v1 = s0 + 1 <= i ? Ts[i * kLd + s0 + 1] * beta_s[s0 + 1] : 0.f;
+                if (pr) {
+                    v0 *= __expf(L_s[s0]);
+                    v1 *= __expf(L_s[s0 + 1]);
+                }
+                split_pack(v0, v1, wh[e], wl[e]);
+            }
+            *(uint4 *)(hi + sw128_offset(i, ch)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+            *(uint4 *)(lo + sw128_offset(i, ch)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        }
+        fence_proxy_async_smem();
+        named_sync(bar_id, kPrepThreads);
+        if (lt == 0) mbar_arrive(&s.bar[kBarTb + g]);
+
+        // ---------------- phase B: the state pass's fp32 B tiles
+        ok = (c < 2) || wait_bar(s, kBarM2 + g, ((c - 2) >> 1) & 1, p.status);
+        if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) break;
+        // P (16 rows x 8 float4)
+        if (lt < kNQ * 8) {
+            const int i = lt >> 3, ch = lt & 7;
+            const float *src = Ps + i * kLd + 4 * ch;
+            *(float4 *)(gt + kGY + sw128_offset(y_row_p(g) + i, ch)) = make_float4(src[0], src[1], src[2], src[3]);
+        }
+        // Gamma-scaled q: (token row i, dk block kb4, 8-element group q)
+        {
+            const int i = lt >> 4, kb4 = (lt >> 2) & 3, q = lt & 3;
+            const bool valid = i < ct;
+            const float gr = !valid ? 0.f : (gated ? __expf(L_s[i * nh + nh - 1]) : 1.f);
+            const uint4 u = *(const uint4 *)(kq + (kb4 >> 1) * kKQBlock + sw128_offset(kC + i, (kb4 & 1) * 4 + q));
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                f[2 * e] = __uint_as_float(w[e] << 16) * gr;
+                f[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u) * gr;
+            }
+            uint8_t *dst = gt + kGX + kb4 * kXBlock;
+            *(float4 *)(dst + sw128_offset(kC + i, 2 * q)) = make_float4(f[0], f[1], f[2], f[3]);
+            *(float4 *)(dst + sw128_offset(kC + i, 2 * q + 1)) = make_float4(f[4], f[5], f[6], f[7]);
+        }
+        // decayed K^T: row dk, four groups of 4 chunk rows per thread
+        {
+            const int dk = lt & 127, q0 = (lt >> 7) * 4;
+            const float Lend = L_s[kC - 1];
+            const uint8_t *src = kq + (dk >> 6) * kKQBlock;
+            const int chunk = (dk & 63) >> 3, e = dk & 7;
+#pragma unroll
+            for (int q = q0; q < q0 + 4; ++q) {
+                float f[4];
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    const int s2 = 4 * q + k4;
+                    const float x = __bfloat162float(*(const __nv_bfloat16 *)(src + sw128_offset(s2, chunk) + e * 2));
+                    f[k4] = gated ? x * __expf(Lend - L_s[s2]) : x;
+                }
+                *(float4 *)(gt + kGY + sw128_offset(y_row_k(g) + dk, q)) = make_float4(f[0], f[1], f[2], f[3]);
+            }
+        }
+        // -W (lane = dk; half hf takes chunk rows 16*hf .. 16*hf + 15)
+        ok = wait_bar(s, kBarUW + g, (c >> 1) & 1, p.status);
+        if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) break;
+        tc_fence_after();
+        {
+            uint32_t r[16];
+            tmem_ld16(trow + kColW + g * 32 + 16 * hf, r);
+            tmem_wait_ld();
+            const int dk = 32 * lq + lane, pos = dk & 31;
+            uint8_t *dst = gt + kGX + (dk >> 5) * kXBlock + (pos & 3) * 4;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                *(float *)(dst + sw128_offset(16 * hf + j, pos >> 2)) = -__uint_as_float(r[j]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_sync(bar_id, kPrepThreads);
+        if (lt == 0) {
+            mbar_arrive(&s.bar[kBarReady + g]);
+            mbar_arrive(&s.bar[kBarEmpty + st]);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ epilogue
+template <typename TOut>
+__device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, int b, int h)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t bar_id = 3;
+    const uint32_t trow = tbase + ((uint32_t)(warp * 32) << 16);
+    const size_t bh = (size_t)b * p.H + h;
+    const bool gated = p.g != nullptr;
+    TOut *o = (TOut *)p.o;
+
+    {   // S^T <- h0^T (lane = dv, column = dk), or zeros; readout accumulators zero
+        uint32_t r[32];
+        for (int c0 = 0; c0 < kD; c0 += 32) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                r[j] = __float_as_uint(p.h0 ? p.h0[(bh * kD + c0 + j) * kD + tid] : 0.f);
+            tmem_st32(trow + kColS + c0, r);
+        }
+        uint32_t z[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) z[j] = 0u;
+        tmem_st16(trow + col_oa(0), z);
+        tmem_st16(trow + col_oa(1), z);
+        tmem_st16(trow + col_ob(0), z);
+        tmem_st16(trow + col_ob(1), z);
+        tmem_wait_st();
+    }
+    tc_fence_before();
+    named_sync(bar_id, 128);
+    if (tid == 0) mbar_arrive(&s.bar[kBarInit]);
+
+    bool failed = false;
+    for (int c = 0; c < p.n_chunks; ++c) {
+        const int g = c & 1, t0 = c * p.ct;
+        if (gated) {
+            // Gamma_C: product of the chunk's token gates (log domain, clamped)
+            float lg = 0.f;
+            if (lane < p.ct && t0 + lane < p.T)
+                lg = fmaxf(logf(__bfloat162float(p.g[((size_t)b * p.T + t0 + lane) * p.H + h])), -80.f);
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) lg += __shfl_xor_sync(0xffffffffu, lg, d);
+            const float gC = __expf(lg);
+            const bool ok = wait_bar(s, kBarM1, c & 1, p.status);
+            if (group_any(bar_id, 128, !ok || *s.abort)) { failed = true; break; }
+            tc_fence_after();
+            uint32_t r[32];
+            for (int c0 = 0; c0 < kD; c0 += 32) {
+                tmem_ld32(trow + kColS + c0, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gC);
+                tmem_st32(trow + kColS + c0, r);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            named_sync(bar_id, 128);
+            if (tid == 0) mbar_arrive(&s.bar[kBarScaled]);
+        }
+        const bool ok = wait_bar(s, kBarM2 + g, (c >> 1) & 1, p.status);
+        if (group_any(bar_id, 128, !ok || *s.abort)) { failed = true; break; }
+        tc_fence_after();
+        uint32_t ra[16], rb[16];
+        tmem_ld16(trow + col_oa(g), ra);
+        tmem_ld16(trow + col_ob(g), rb);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < kNQ; ++i) {
+            const int t = t0 + i;
+            if (i < p.ct && t < p.T)
+                store_out(o, (((size_t)b * p.T + t) * p.H + h) * kD + tid,
+                          __uint_as_float(ra[i]) + __uint_as_float(rb[i]));
+            ra[i] = 0u;
+        }
+        tmem_st16(trow + col_oa(g), ra);   // both parts accumulate: clear them for chunk c + 2
+        tmem_st16(trow + col_ob(g), ra);
+        tmem_wait_st();
+        tc_fence_before();
+        named_sync(bar_id, 128);
+        if (tid == 0) mbar_arrive(&s.bar[kBarOFree + g]);
+    }
+    if (!failed && p.h_final) {
+        uint32_t r[32];
+        for (int c0 = 0; c0 < kD; c0 += 32) {
+            tmem_ld32(trow + kColS + c0, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) p.h_final[(bh * kD + c0 + j) * kD + tid] = __uint_as_float(r[j]);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ kernel
 template <typename TOut>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 const __grid_constant__ CUtensorMap tm_q, const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    float *Gs = (float *)(sm + kOffG);
-    float *Ts = (float *)(sm + kOffT);
-    float *Xs = (float *)(sm + kOffX);
-    float *beta_s = (float *)(sm + kOffVec);
-    float *L_s = beta_s + 64;
-    uint64_t *bar_tma = (uint64_t *)(sm + kOffBar);   // [2], one per stage
-    uint64_t *bar_mma = bar_tma + 2;
-    uint32_t *tmem_slot = (uint32_t *)(bar_mma + 1);
-    volatile uint32_t *abort_s = tmem_slot + 1;
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    Smem s;
+    s.base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    s.bar = (uint64_t *)(s.base + kOffBar);
+    s.tmem_slot = (uint32_t *)(s.bar + kNumBars);
+    s.abort = s.tmem_slot + 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x, b = bh / p.H, h = bh - b * p.H;
-    const int nh = p.nh, ct = p.ct, R = ct * nh, nq = p.nq, T = p.T;
-    const bool gated = p.g != nullptr;
 
-    // Zero every tile once: rows TMA never writes (query rows >= ct, the
-    // padding row when 64 % n_h != 0) must hold finite zeros.
-    for (uint32_t i = tid * 16; i < kOffG; i += kThreads * 16)
-        *(uint4 *)(sm + i) = make_uint4(0, 0, 0, 0);
-    if (tid == 0) {
-        mbar_init(&bar_tma[0], 1);
-        mbar_init(&bar_tma[1], 1);
-        mbar_init(bar_mma, 1);
-        *abort_s = 0;
+    // Zero every tile once: rows TMA never writes (padding rows, query rows
+    // beyond the chunk's tokens) must hold finite zeros.
+    for (uint32_t i = threadIdx.x * 16; i < kOffScratch; i += kThreads * 16)
+        *(uint4 *)(s.base + i) = make_uint4(0, 0, 0, 0);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < (int)kNumBars; ++i) mbar_init(&s.bar[i], 1);
+        *s.abort = 0;
         fence_mbar_init();
+    }
+    if (warp == kTmaWarp && lane == 0) {
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_q);
     }
-    if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
+    if (warp == 0) tmem_alloc(s.tmem_slot, kTmemCols);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tbase = *tmem_slot;
-    const uint32_t trow = tbase + ((uint32_t)(warp * 32) << 16);   // this thread's lane, column 0
+    const uint32_t tbase = *s.tmem_slot;
 
-    auto issue_loads = [&](int chunk) {
-        const int st = chunk & 1;
-        uint8_t *kq = sm + kOffStage + st * kStageBytes;
-        uint8_t *vv = kq + kKQBytes;
-        const int t0 = chunk * ct;
-        mbar_arrive_expect_tx(&bar_tma[st], (uint32_t)(512 * R + 256 * ct));
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-            tma_load_5d(kq + kb * 16384, &tm_k, &bar_tma[st], kb * 64, 0, h, t0, b);
-            tma_load_4d(kq + kb * 16384 + 64 * 128, &tm_q, &bar_tma[st], kb * 64, h, t0, b);
-            tma_load_5d(vv + kb * 8192, &tm_v, &bar_tma[st], kb * 64, 0, h, t0, b);
-        }
-    };
-
-    // S^T <- h0^T (lane = dv, column = dk), or zeros
-    {
-        uint32_t r[16];
-        for (int c0 = 0; c0 < kD; c0 += 16) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                r[j] = __float_as_uint(p.h0 ? p.h0[((size_t)bh * kD + c0 + j) * kD + tid] : 0.f);
-            tmem_st16(trow + kColS + c0, r);
-        }
-        tmem_wait_st();
-    }
-
-    int issued = 0, landed = 0;
-    if (tid == 0) issue_loads(0);
-    issued = 1;
-    if (p.n_chunks > 1) {
-        if (tid == 0) issue_loads(1);
-        issued = 2;
-    }
-    uint32_t mma_phase = 0;
-    bool mma_pending = false;
-
-    for (int c = 0; c < p.n_chunks; ++c) {
-        const int st = c & 1;
-        uint8_t *kq = sm + kOffStage + st * kStageBytes;
-        uint8_t *vv = kq + kKQBytes;
-        const int t0 = c * ct;
-
-        // (1) betas and cumulative log-gates of the chunk's rows
-        if (tid < kC) {
-            const int r = tid, tl = r / nh, j = r - tl * nh, t = t0 + tl;
-            const bool valid = (r < R) && (t < T);
-            const size_t tok = ((size_t)b * T + t) * p.H + h;
-            beta_s[r] = valid ? __bfloat162float(p.beta[tok * nh + j]) : 0.f;
-            float lg = 0.f;
-            if (gated && valid && j == 0) lg = fmaxf(logf(__bfloat162float(p.g[tok])), -80.f);
-            Xs[r] = lg;
-        }
-        __syncthreads();
-        if (tid < kC) {
-            float acc = 0.f;
-            for (int s = 0; s <= tid; ++s) acc += Xs[s];
-            L_s[tid] = acc;
-        }
-        // (2) this chunk's K, Q, V tiles
-        if (!mbar_wait(&bar_tma[st], (c >> 1) & 1, kWaitTries, abort_s)) flag_error(p.status, abort_s, kDevTimeout);
-        __syncthreads();
-        if (*abort_s) break;
-        landed = c + 1;
-
-        // (3) [K;Q] K^T -> TMEM (lanes 0..63 Gram rows, 64..127 query rows)
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t id = idesc_bf16(128, 64, false, false);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t a = smem_addr(kq) + (kk >> 2) * 16384 + (kk & 3) * 32;
-                mma_ss(tbase + kColGW, sdesc_sw128(a, 16, 1024), sdesc_sw128(a, 16, 1024), id, kk > 0);
-            }
-            mma_commit(bar_mma);
-        }
-        mma_pending = true;
-        if (!mbar_wait(bar_mma, mma_phase, kWaitTries, abort_s)) flag_error(p.status, abort_s, kDevTimeout);
-        mma_phase ^= 1;
-        __syncthreads();
-        if (*abort_s) break;
-        mma_pending = false;
-        tc_fence_after();
-
-        // (4) Gram rows -> G (fp32), query rows -> P (bf16 hi + lo parts)
-        {
-            float gq[64];
-            tmem_ld64f(trow + kColGW, gq);
-            if (tid < kC) {
-                const int r = tid;
-                const float br = beta_s[r], Lr = L_s[r];
-#pragma unroll
-                for (int s = 0; s < kC; ++s) {
-                    float v = 0.f;
-                    if (s < r) {
-                        v = br * gq[s];
-                        if (gated) v *= __expf(Lr - L_s[s]);
-                    }
-                    Gs[r * kLd + s] = v;
-                }
-            } else {
-                const int i = tid - kC;
-                const int r = i * nh + nh - 1;
-                const bool valid = i < ct;
-                const float Lr = valid ? L_s[r] : 0.f;
-                uint8_t *P = sm + kOffP, *PL = sm + kOffPL;
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint32_t w[4], wl[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int s0 = ch * 8 + 2 * e;
-                        float v0 = 0.f, v1 = 0.f;
-                        if (valid && s0 <= r) v0 = gated ? gq[s0] * __expf(Lr - L_s[s0]) : gq[s0];
-                        if (valid && s0 + 1 <= r) v1 = gated ? gq[s0 + 1] * __expf(Lr - L_s[s0 + 1]) : gq[s0 + 1];
-                        split_pack(v0, v1, w[e], wl[e]);
-                    }
-                    *(uint4 *)(P + sw128_offset(i, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
-                    *(uint4 *)(PL + sw128_offset(i, ch)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-                }
-            }
-        }
-        tc_fence_before();
-        __syncthreads();
-
-        // (5) T = (I + G)^{-1}: 16x16 diagonal blocks by forward substitution
-        // (one warp per block, one column per lane), then the off-diagonal
-        // blocks level by level: T_ab = -T_aa sum_{m=b}^{a-1} G_am T_mb.
-        if (lane < 16) {
-            const int base = warp * 16, col = base + lane;
-            float x[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float acc = (i == lane) ? 1.f : 0.f;
-#pragma unroll
-                for (int s2 = 0; s2 < i; ++s2) acc = fmaf(-Gs[(base + i) * kLd + base + s2], x[s2], acc);
-                x[i] = acc;
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) Ts[(base + i) * kLd + col] = x[i];
-        }
-        __syncthreads();
-        for (int d = 1; d < 4; ++d) {
-            const int nblk = 4 - d;
-            for (int e = tid; e < nblk * 256; e += kThreads) {
-                const int bb = e >> 8, i = (e >> 4) & 15, j = e & 15, a = bb + d;
-                float acc = 0.f;
-                for (int m = 16 * bb; m < 16 * a; ++m)
-                    acc = fmaf(Gs[(16 * a + i) * kLd + m], Ts[m * kLd + 16 * bb + j], acc);
-                Xs[(bb * 16 + i) * 17 + j] = acc;
-            }
-            __syncthreads();
-            for (int e = tid; e < nblk * 256; e += kThreads) {
-                const int bb = e >> 8, i = (e >> 4) & 15, j = e & 15, a = bb + d;
-                float acc = 0.f;
-                for (int u = 0; u <= i; ++u)
-                    acc = fmaf(Ts[(16 * a + i) * kLd + 16 * a + u], Xs[(bb * 16 + u) * 17 + j], acc);
-                Ts[(16 * a + i) * kLd + 16 * bb + j] = -acc;
-            }
-            __syncthreads();
-        }
-        // T diag(beta) -> Tb (threads 0..63), T diag(beta Gamma) -> Tbg (64..127, gated)
-        {
-            const int i = tid & 63;
-            const bool second = tid >= 64;
-            if (!second || gated) {
-                uint8_t *dst = sm + (second ? kOffTbg : kOffTb);
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int s0 = ch * 8 + 2 * e;
-                        float v0 = s0 <= i ? Ts[i * kLd + s0] * beta_s[s0] : 0.f;
-                        float v1 = s0 + 1 <= i ? Ts[i * kLd + s0 + 1] * beta_s[s0 + 1] : 0.f;
-                        if (second) {
-                            v0 *= __expf(L_s[s0]);
-                            v1 *= __expf(L_s[s0 + 1]);
-                        }
-                        w[e] = pack_bf16x2(v0, v1);
-                    }
-                    *(uint4 *)(dst + sw128_offset(i, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-            }
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
-
-        // (6) U^T = V^T Tb^T -> UN (lane = dv);  W^T = K^T Tbg^T -> GW (lane = dk)
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t id = idesc_bf16(128, 64, true, false);
-            const uint32_t tb = smem_addr(sm + kOffTb), tbg = smem_addr(sm + (gated ? kOffTbg : kOffTb));
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_ss(tbase + kColUN, sdesc_sw128(smem_addr(vv) + kk * 2048, 8192, 1024),
-                       sdesc_sw128(tb + kk * 32, 16, 1024), id, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_ss(tbase + kColGW, sdesc_sw128(smem_addr(kq) + kk * 2048, 16384, 1024),
-                       sdesc_sw128(tbg + kk * 32, 16, 1024), id, kk > 0);
-            mma_commit(bar_mma);
-        }
-        mma_pending = true;
-        if (!mbar_wait(bar_mma, mma_phase, kWaitTries, abort_s)) flag_error(p.status, abort_s, kDevTimeout);
-        mma_phase ^= 1;
-        __syncthreads();
-        if (*abort_s) break;
-        mma_pending = false;
-        tc_fence_after();
-
-        // (7) -W as the MN-major B tile (row dk = this lane); S^T -> bf16 copy
-        // (and S <- Gamma_C S when gated)
-        const float Lend = L_s[kC - 1];
-        {
-            float wv[64];
-            tmem_ld64f(trow + kColGW, wv);
-            uint8_t *NW = sm + kOffNW;
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) w[e] = pack_bf16x2(-wv[ch * 8 + 2 * e], -wv[ch * 8 + 2 * e + 1]);
-                *(uint4 *)(NW + sw128_offset(tid, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-        }
-        {
-            const float gC = gated ? __expf(Lend) : 1.f;
-            uint32_t r[16], r2[16], pk[16], pl[16];
-            for (int c0 = 0; c0 < kD; c0 += 32) {
-                tmem_ld16(trow + kColS + c0, r);
-                tmem_ld16(trow + kColS + c0 + 16, r2);
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    split_pack(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]), pk[j], pl[j]);
-                    split_pack(__uint_as_float(r2[2 * j]), __uint_as_float(r2[2 * j + 1]), pk[8 + j], pl[8 + j]);
-                }
-                tmem_st16(trow + kColSB + c0 / 2, pk);
-                tmem_st16(trow + kColSBL + c0 / 2, pl);
-                if (gated) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        r[j] = __float_as_uint(__uint_as_float(r[j]) * gC);
-                        r2[j] = __float_as_uint(__uint_as_float(r2[j]) * gC);
-                    }
-                    tmem_st16(trow + kColS + c0, r);
-                    tmem_st16(trow + kColS + c0 + 16, r2);
-                }
-            }
-            tmem_wait_st();
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // (8) U'^T = U^T - S^T W^T;  O^T = S^T Q^T
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t idU = idesc_bf16(128, 64, false, true);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t bd = sdesc_sw128(smem_addr(sm + kOffNW) + kk * 2048, 8192, 1024);
-                mma_ts(tbase + kColUN, tbase + kColSB + kk * 8, bd, idU, 1);
-                mma_ts(tbase + kColUN, tbase + kColSBL + kk * 8, bd, idU, 1);
-            }
-            const uint32_t idO = idesc_bf16(128, nq, false, false);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t a = smem_addr(kq) + (kk >> 2) * 16384 + 64 * 128 + (kk & 3) * 32;
-                const uint64_t bd = sdesc_sw128(a, 16, 1024);
-                mma_ts(tbase + kColO, tbase + kColSB + kk * 8, bd, idO, kk > 0);
-                mma_ts(tbase + kColO, tbase + kColSBL + kk * 8, bd, idO, 1);
-            }
-            mma_commit(bar_mma);
-        }
-        mma_pending = true;
-        if (!mbar_wait(bar_mma, mma_phase, kWaitTries, abort_s)) flag_error(p.status, abort_s, kDevTimeout);
-        mma_phase ^= 1;
-        __syncthreads();
-        if (*abort_s) break;
-        mma_pending = false;
-        tc_fence_after();
-
-        // (9) U'^T -> bf16 hi/lo copies (readout; decayed for the state update when
-        // gated); gated: O^T columns scaled by Gamma of their readout rows
-        {
-            // all 64 fp32 columns are read before any lo part overwrites them
-            float un[64];
-            tmem_ld64f(trow + kColUN, un);
-            uint32_t pk[16], pl[16];
-            for (int c0 = 0; c0 < kC; c0 += 32) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) split_pack(un[c0 + 2 * j], un[c0 + 2 * j + 1], pk[j], pl[j]);
-                tmem_st16(trow + kColUB + c0 / 2, pk);
-                tmem_st16(trow + kColUBL + c0 / 2, pl);
-                if (gated) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int s0 = c0 + 2 * j;
-                        split_pack(un[s0] * __expf(Lend - L_s[s0]), un[s0 + 1] * __expf(Lend - L_s[s0 + 1]),
-                                   pk[j], pl[j]);
-                    }
-                    tmem_st16(trow + kColUBD + c0 / 2, pk);
-                    tmem_st16(trow + kColUBDL + c0 / 2, pl);
-                }
-            }
-            if (gated) {
-                // O^T column i holds S0^T q_i: scale it by Gamma at token i's readout row
-                uint32_t r[16];
-                for (int c0 = 0; c0 < nq; c0 += 16) {
-                    tmem_ld16(trow + kColO + c0, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int i = c0 + j;
-                        const float gr = i < ct ? __expf(L_s[i * nh + nh - 1]) : 0.f;
-                        r[j] = __float_as_uint(__uint_as_float(r[j]) * gr);
-                    }
-                    tmem_st16(trow + kColO + c0, r);
-                }
-            }
-            tmem_wait_st();
-        }
-        tc_fence_before();
-        __syncthreads();
-
-        // (10) S^T += U'^T(decayed) K;  O^T += U'^T P^T
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t idS = idesc_bf16(128, 128, false, true);
-            const uint32_t ubd = gated ? kColUBD : kColUB, ubdl = gated ? kColUBDL : kColUBL;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t bd = sdesc_sw128(smem_addr(kq) + kk * 2048, 16384, 1024);
-                mma_ts(tbase + kColS, tbase + ubd + kk * 8, bd, idS, 1);
-                mma_ts(tbase + kColS, tbase + ubdl + kk * 8, bd, idS, 1);
-            }
-            const uint32_t idO = idesc_bf16(128, nq, false, false);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t bd = sdesc_sw128(smem_addr(sm + kOffP) + kk * 32, 16, 1024);
-                const uint64_t bdl = sdesc_sw128(smem_addr(sm + kOffPL) + kk * 32, 16, 1024);
-                mma_ts(tbase + kColO, tbase + kColUB + kk * 8, bd, idO, 1);
-                mma_ts(tbase + kColO, tbase + kColUBL + kk * 8, bd, idO, 1);
-                mma_ts(tbase + kColO, tbase + kColUB + kk * 8, bdl, idO, 1);
-            }
-            mma_commit(bar_mma);
-        }
-        mma_pending = true;
-        if (!mbar_wait(bar_mma, mma_phase, kWaitTries, abort_s)) flag_error(p.status, abort_s, kDevTimeout);
-        mma_phase ^= 1;
-        __syncthreads();
-        if (*abort_s) break;
-        mma_pending = false;
-        tc_fence_after();
-        // stage st is free: prefetch chunk c + 2 into it
-        if (c + 2 < p.n_chunks) {
-            if (tid == 0) issue_loads(c + 2);
-            issued = c + 3;
-        }
-
-        // (11) outputs of the chunk's tokens (lane = dv)
-        {
-            uint32_t r[16];
-            for (int c0 = 0; c0 < nq; c0 += 16) {
-                tmem_ld16(trow + kColO + c0, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int i = c0 + j, t = t0 + i;
-                    if (i < ct && t < T)
-                        store_out((TOut *)p.o, (((size_t)b * T + t) * p.H + h) * kD + tid, __uint_as_float(r[j]));
-                }
-            }
-        }
-        tc_fence_before();
-    }
-
-    if (*abort_s) {
-        // drain what is still in flight before releasing TMEM and shared memory
-        uint32_t no_abort = 0;   // these waits must not be cut short by the flag
-        if (mma_pending) mbar_wait(bar_mma, mma_phase ^ 1, kWaitTries, &no_abort);
-        for (int cc = landed; cc < issued; ++cc)
-            mbar_wait(&bar_tma[cc & 1], (cc >> 1) & 1, kWaitTries, &no_abort);
-    } else if (p.h_final) {
-        uint32_t r[16];
-        for (int c0 = 0; c0 < kD; c0 += 16) {
-            tmem_ld16(trow + kColS + c0, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                p.h_final[((size_t)bh * kD + c0 + j) * kD + tid] = __uint_as_float(r[j]);
-        }
+    if (warp < kPrepWarp) {
+        epi_role<TOut>(s, p, tbase, b, h);
+    } else if (warp < kTmaWarp) {
+        prep_role(s, p, tbase, (warp - kPrepWarp) >> 3, b, h);
+    } else if (warp == kTmaWarp) {
+        if (lane == 0) tma_role(s, p, &tm_k, &tm_v, &tm_q, b, h);
+    } else if (warp == kChainWarp) {
+        if (lane == 0) chain_role(s, p, tbase);
+    } else {
+        if (lane == 0) prep_mma_role(s, p, tbase);
     }
     tc_fence_before();
     __syncthreads();
@@ -596,7 +733,7 @@ size_t chunk_tc_scratch_bytes(const Problem &) { return 0; }
 
 cudaError_t launch_chunk_tc(const Problem &p)
 {
-    const int nh = p.nh, ct = kC / nh;
+    const int nh = p.nh, ct = (kC / nh < kNQ) ? kC / nh : kNQ;
     const cuuint64_t B = p.B, T = p.T, H = p.H;
     CUtensorMap tk, tv, tq;
     const cuuint64_t dk[5] = {kD, (cuuint64_t)nh, H, T, B};
@@ -623,7 +760,6 @@ cudaError_t launch_chunk_tc(const Problem &p)
     pr.H = p.H;
     pr.nh = nh;
     pr.ct = ct;
-    pr.nq = (ct + 15) & ~15;
     pr.n_chunks = (p.T + ct - 1) / ct;
     kernel<<<p.B * p.H, kThreads, kSmemBytes, p.stream>>>(tk, tv, tq, pr);
     return cudaGetLastError();
