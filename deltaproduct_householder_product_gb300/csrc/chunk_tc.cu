@@ -407,8 +407,12 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
             L_s[lane] = lg;
             rv = load_rows(p, c + 2, b, h, lane);        // next chunk of this group
         }
-        bool ok = wait_bar(s, kBarFull + st, (c / kNS) & 1, p.status);
-        if (ok) ok = wait_bar(s, kBarGQ + g, (c >> 1) & 1, p.status);
+        // one thread polls the mbarriers; the group barrier spreads the outcome
+        bool ok = true;
+        if (lt == 0) {
+            ok = wait_bar(s, kBarFull + st, (c / kNS) & 1, p.status);
+            if (ok) ok = wait_bar(s, kBarGQ + g, (c >> 1) & 1, p.status);
+        }
         if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) break;
         tc_fence_after();
 
@@ -510,7 +514,7 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
         if (lt == 0) mbar_arrive(&s.bar[kBarTb + g]);
 
         // ---------------- phase B: the state pass's fp32 B tiles
-        ok = (c < 2) || wait_bar(s, kBarM2 + g, ((c - 2) >> 1) & 1, p.status);
+        ok = (c < 2 || lt != 0) || wait_bar(s, kBarM2 + g, ((c - 2) >> 1) & 1, p.status);
         if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) break;
         // P (16 rows x 8 float4)
         if (lt < kNQ * 8) {
@@ -554,7 +558,7 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
             }
         }
         // -W (lane = dk; half hf takes chunk rows 16*hf .. 16*hf + 15)
-        ok = wait_bar(s, kBarUW + g, (c >> 1) & 1, p.status);
+        ok = (lt != 0) || wait_bar(s, kBarUW + g, (c >> 1) & 1, p.status);
         if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) break;
         tc_fence_after();
         {
@@ -620,7 +624,7 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, int b, 
 #pragma unroll
             for (int d = 16; d > 0; d >>= 1) lg += __shfl_xor_sync(0xffffffffu, lg, d);
             const float gC = __expf(lg);
-            const bool ok = wait_bar(s, kBarM1, c & 1, p.status);
+            const bool ok = (tid != 0) || wait_bar(s, kBarM1, c & 1, p.status);
             if (group_any(bar_id, 128, !ok || *s.abort)) { failed = true; break; }
             tc_fence_after();
             uint32_t r[32];
@@ -636,7 +640,7 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, int b, 
             named_sync(bar_id, 128);
             if (tid == 0) mbar_arrive(&s.bar[kBarScaled]);
         }
-        const bool ok = wait_bar(s, kBarM2 + g, (c >> 1) & 1, p.status);
+        const bool ok = (tid != 0) || wait_bar(s, kBarM2 + g, (c >> 1) & 1, p.status);
         if (group_any(bar_id, 128, !ok || *s.abort)) { failed = true; break; }
         tc_fence_after();
         uint32_t ra[16], rb[16];
