@@ -349,7 +349,7 @@ def ours_arm(args, w):
 KERNELS_PER_FORWARD = 1
 # per-launch DRAM bytes (read + write) from an ncu capture of the current kernel,
 # keyed by (workload, kernel family); absent = not captured for this build
-TRAFFIC = {}
+TRAFFIC = {("b4h8t2048-nh2-d128-bf16", "auto"): 96_673_536}
 
 
 def main():
