@@ -51,6 +51,9 @@ def parse():
     ap.add_argument("--kernel", default="auto", choices=["auto", "recurrent", "chunk_tc"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused", action="store_true",
+                    help="give dp_forward only the minimum workspace: the chunk path then "
+                         "runs as one fused kernel instead of prep + state-pass kernels")
     return ap.parse_args()
 
 
@@ -137,13 +140,13 @@ def make_copies(w, n_copies, device):
     return x, copies
 
 
-def forward_calls(dp, L, w, copies, kernel, stream):
+def forward_calls(dp, L, w, copies, kernel, stream, fused=False):
     """Pre-marshalled dp_forward calls, one per input copy (keeps per-call host
     work to the ABI call itself)."""
     import ctypes
     from deltaproduct_householder_product_gb300 import _lib
     dims = _lib.make_dims(w.B, w.T, w.H, w.Dk, w.Dv, w.nh, w.torch_dtype, kernel, OUT_DTYPE)
-    need = _lib.workspace_size(dims)
+    need = _lib.workspace_size(dims, fast=not fused)
     calls = []
     s = ctypes.c_void_p(stream.cuda_stream)
     for c in copies:
@@ -152,7 +155,10 @@ def forward_calls(dp, L, w, copies, kernel, stream):
                 _lib._ptr(c["beta"]), _lib._ptr(c["g"]), _lib._ptr(c["h0"]), _lib._ptr(c["o"]),
                 _lib._ptr(c["hf"]), _lib._ptr(c["ws"]), ctypes.c_size_t(need), s)
         calls.append((L.dp_forward, args))
-    return calls, dims
+    # the chunk path splits into a prep kernel and the state-pass kernel when
+    # the workspace holds the per-chunk records
+    launches = 2 if need > _lib.workspace_size(dims) else 1
+    return calls, dims, launches
 
 
 def run_calls(calls, n, start=0):
@@ -244,7 +250,7 @@ def ours_arm(args, w):
     wbytes = W.algorithmic_bytes(w, out_bytes=4)
     n_copies = max(2, -(-3 * L2_BYTES // wbytes))          # rotate copies: > 3x L2 in total
     x, copies = make_copies(w, n_copies, dev)
-    calls, dims = forward_calls(dp, L, w, copies, args.kernel, stream)
+    calls, dims, launches = forward_calls(dp, L, w, copies, args.kernel, stream, args.fused)
 
     run_calls(calls, args.warmup)
     torch.cuda.synchronize()
@@ -327,15 +333,19 @@ def ours_arm(args, w):
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "nh": w.nh, "Dk": w.Dk,
                    "Dv": w.Dv, "kernel": args.kernel, "gated": w.gated,
+                   "path": "fused" if launches == 1 and args.kernel != "recurrent" else
+                           ("split" if launches == 2 else "recurrent"),
                    "l2": f"{n_copies} rotating input/output copies "
                          f"({n_copies * wbytes / 1e6:.0f} MB > 129 MB L2)",
                    "parallelism": f"replicas x{world}"},
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * KERNELS_PER_FORWARD,
+        "gpu_launches": args.steps * launches,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": TRAFFIC.get((w.name, args.kernel)),
-                     "peak_kind": peak_kind, "algorithmic_bytes": wbytes},
+                     "frac": achieved / hbm_peak,
+                     "traffic": TRAFFIC.get((w.name, args.kernel, launches)),
+                     "peak_kind": peak_kind, "algorithmic_bytes": wbytes,
+                     "scope": "one forward: every launch dp_forward enqueues"},
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:
@@ -345,11 +355,10 @@ def ours_arm(args, w):
     print(json.dumps(line), flush=True)
 
 
-# dp_forward enqueues exactly one kernel (no memset, no helper kernels)
-KERNELS_PER_FORWARD = 1
-# per-launch DRAM bytes (read + write) from an ncu capture of the current kernel,
-# keyed by (workload, kernel family); absent = not captured for this build
-TRAFFIC = {("b4h8t2048-nh2-d128-bf16", "auto"): 96_673_536}
+# DRAM bytes (read + write) per forward, summed over its launches, from an ncu
+# capture of the current kernels; keyed by (workload, kernel family, launches
+# per forward); absent = not captured for this build
+TRAFFIC = {}
 
 
 def main():

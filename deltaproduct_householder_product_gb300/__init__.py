@@ -19,9 +19,12 @@ def abi_version():
     return _lib.lib().dp_abi_version()
 
 
-def workspace_size(B, T, H, Dk, Dv, nh, dtype=torch.bfloat16, impl="auto", out_dtype=None):
-    """Device workspace bytes dp_forward needs for this problem."""
-    return _lib.workspace_size(_lib.make_dims(B, T, H, Dk, Dv, nh, dtype, impl, out_dtype))
+def workspace_size(B, T, H, Dk, Dv, nh, dtype=torch.bfloat16, impl="auto", out_dtype=None,
+                   fast=False):
+    """Device workspace bytes dp_forward needs for this problem; with ``fast``,
+    the size with which it takes its fastest path (the chunk path's parallel
+    prep kernel and per-chunk records)."""
+    return _lib.workspace_size(_lib.make_dims(B, T, H, Dk, Dv, nh, dtype, impl, out_dtype), fast)
 
 
 def supports(impl, B, T, H, Dk, Dv, nh, dtype=torch.bfloat16):
@@ -70,7 +73,7 @@ def forward(q, k, v, beta, g=None, h0=None, *, impl="auto", out=None, h_final=Tr
     elif h_final is False:
         h_final = None
     _lib._need_cuda("h_final", h_final, torch.float32)
-    need = _lib.workspace_size(dims)
+    need = _lib.workspace_size(dims, fast=True)
     if workspace is None:
         workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
     _lib._need_cuda("workspace", workspace)

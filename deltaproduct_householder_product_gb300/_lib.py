@@ -48,12 +48,13 @@ def lib():
         L.dp_status_string.argtypes = [ctypes.c_int]
         L.dp_status_string.restype = ctypes.c_char_p
         L.dp_forward_workspace_size.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(ctypes.c_size_t)]
+        L.dp_forward_workspace_size_fast.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(ctypes.c_size_t)]
         L.dp_forward.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 9 + [ctypes.c_size_t, _vp]
         L.dp_decode_step.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 7 + [_vp]
         L.dp_state_io.argtypes = [ctypes.c_int] * 5 + [_vp, _vp, ctypes.c_int, ctypes.c_int, _vp]
         L.dp_check_status.argtypes = [_vp, _vp]
         L.dp_forward_noalloc.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 9
-        for name in ("dp_forward_workspace_size", "dp_forward", "dp_decode_step",
+        for name in ("dp_forward_workspace_size", "dp_forward_workspace_size_fast", "dp_forward", "dp_decode_step",
                      "dp_state_io", "dp_check_status", "dp_forward_noalloc"):
             getattr(L, name).restype = ctypes.c_int
         _LIB = L
@@ -109,8 +110,9 @@ def make_dims(B, T, H, Dk, Dv, nh, dtype, impl="auto", out_dtype=None):
     return Dims(B, T, H, Dk, Dv, nh, dt, IMPLS[impl] if isinstance(impl, str) else int(impl), od)
 
 
-def workspace_size(dims):
+def workspace_size(dims, fast=False):
+    """dp_forward_workspace_size, or dp_forward_workspace_size_fast if ``fast``."""
     n = ctypes.c_size_t(0)
-    _check(lib().dp_forward_workspace_size(ctypes.byref(dims), ctypes.byref(n)),
-           "dp_forward_workspace_size")
+    name = "dp_forward_workspace_size_fast" if fast else "dp_forward_workspace_size"
+    _check(getattr(lib(), name)(ctypes.byref(dims), ctypes.byref(n)), name)
     return n.value

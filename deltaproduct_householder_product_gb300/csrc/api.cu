@@ -114,9 +114,15 @@ dp_status dp_forward_workspace_size(const dp_dims *dims, size_t *bytes)
         dp::Problem p = make_problem(dims, dims->T);
         if (!dp::chunk_tc_supported(p)) return DP_ERR_UNSUPPORTED;
     }
+    *bytes = kStatusBlock;
+    return DP_OK;
+}
+
+dp_status dp_forward_workspace_size_fast(const dp_dims *dims, size_t *bytes)
+{
+    DP_TRY(dp_forward_workspace_size(dims, bytes));
     dp::Problem p = make_problem(dims, dims->T);
-    size_t extra = use_chunk_tc(dims, p) ? dp::chunk_tc_scratch_bytes(p) : 0;
-    *bytes = kStatusBlock + ((extra + 255) & ~(size_t)255);
+    if (use_chunk_tc(dims, p)) *bytes += (dp::chunk_tc_records_bytes(p) + 255) & ~(size_t)255;
     return DP_OK;
 }
 
@@ -142,7 +148,7 @@ dp_status dp_forward(const dp_dims *dims, const void *q, const void *k, const vo
     if (!device_pointer(workspace)) return DP_ERR_INVALID_ARG;
     p.status = (uint32_t *)workspace;
     p.scratch = (char *)workspace + kStatusBlock;
-    p.scratch_bytes = need - kStatusBlock;
+    p.scratch_bytes = workspace_bytes - kStatusBlock;
 
     if ((size_t)p.B * p.H == 0) return DP_OK;
     return from_cuda(tc ? dp::launch_chunk_tc(p) : dp::launch_recurrent(p));

@@ -16,9 +16,19 @@
 //   S   = Gamma_C S0 + K^T diag(Gamma_C/Gamma) U'        state pass, part 2
 //   o_t = Gamma_r S0^T q_t + sum_{s<=r} E_rs (q_t.k_s) u'_s,  r = last row of t
 //
-// Organisation (one CTA per (batch, head), the state S^T resident in TMEM
-// for the whole sequence, lanes = value columns):
-//  * warp 20   TMA producer: K, Q, V tiles of each chunk, 3-stage ring.
+// Two ways to run it, same arithmetic and bit-identical results:
+//  * split (two kernels): chunk_prep_kernel does "phase A" (G, P, T: the work
+//    that needs only one chunk's inputs) for every chunk of every head at
+//    once and writes a record per chunk into the workspace; the state-pass
+//    kernel then streams the records in with the inputs. The sequential
+//    kernel keeps only the work that has to follow the state.
+//  * fused (one kernel, no workspace beyond the status word): the state-pass
+//    kernel's prep groups do phase A themselves, one chunk ahead.
+//
+// State-pass kernel organisation (one CTA per (batch, head), the state S^T
+// resident in TMEM for the whole sequence, lanes = value columns):
+//  * warp 20   TMA producer: K, Q, V tiles of each chunk (and its record in
+//              split mode), 3-stage ring.
 //  * warp 21   state-pass MMA issuer (one thread, tf32):
 //              [U' | O_b] += S [-W; Gamma q]^T and [S | O_a] += U'^T [K^T; P].
 //              These MMAs read S and U' straight from their fp32 TMEM
@@ -27,14 +37,15 @@
 //              round trip. The readout rides along in the same instructions
 //              (stacked B operands), since each MMA instruction costs about
 //              the same issue time whatever its N.
-//  * warp 22   prep MMA issuer (bf16: [K;Q] K^T, U, W), one chunk ahead, on
-//              its own thread so its issue latency overlaps the state pass.
+//  * warp 22   prep MMA issuer (bf16: [K;Q] K^T in fused mode, U, W), one
+//              chunk ahead, on its own thread so its issue latency overlaps
+//              the state pass.
 //  * warps 4-11 and 12-19: two prep groups, taking even and odd chunks.
-//              Phase A (needs only the chunk's inputs): turn the Gram MMA
-//              into G and P, solve T on CUDA cores (16x16 diagonal blocks by
-//              forward substitution, one lane per column, then the
-//              off-diagonal block), write T as bf16 hi/lo tiles for the U/W
-//              MMAs. Phase B (once the state pass has released the group's
+//              Phase A (fused mode only): turn the Gram MMA into G and P,
+//              solve T on CUDA cores (16x16 diagonal blocks by forward
+//              substitution, one lane per column, then the off-diagonal
+//              block), write T as bf16 hi/lo tiles for the U/W MMAs.
+//              Phase B (once the state pass has released the group's
 //              buffers): write the fp32 B tiles of the state pass (P, Gamma q,
 //              decayed K^T, and -W once the W MMA is done).
 //  * warps 0-3 epilogue: initial state in, outputs and final state out; for
@@ -72,7 +83,7 @@ constexpr uint32_t kColOa0 = 0;    // O_a[0]: 16 columns, left of S
 constexpr uint32_t kColS = 16;     // S^T fp32: 128 columns (dk), lane = dv
 constexpr uint32_t kColOa1 = 144;  // O_a[1]: 16 columns, right of S
 constexpr uint32_t kColUN = 160;   // U'^T[g] at 160 + 48 g (32 columns), O_b[g] right after (16)
-constexpr uint32_t kColGQ = 256;   // [K;Q] K^T fp32 (M = 64 layout): 2 x 32 columns
+constexpr uint32_t kColGQ = 256;   // [K;Q] K^T fp32 (M = 64 layout): 2 x 32 columns (fused mode)
 constexpr uint32_t kColW = 320;    // W^T fp32: 2 x 32 columns (chunk rows), lane = dk
 constexpr uint32_t kTmemCols = 512;
 __host__ __device__ constexpr uint32_t col_un(int g) { return kColUN + 48 * g; }
@@ -84,9 +95,9 @@ __host__ __device__ constexpr uint32_t col_oa(int g) { return g ? kColOa1 : kCol
 // rows 32-47 Q), V = 2 blocks (dv halves) x 32 rows x 128 B; bf16, 128-B swizzle.
 constexpr uint32_t kKQBlock = 64 * 128;
 constexpr uint32_t kVBlock = 32 * 128;
-constexpr uint32_t kStageBytes = 2 * kKQBlock + 2 * kVBlock;          // 24 KB
+constexpr uint32_t kStageIn = 2 * kKQBlock + 2 * kVBlock;             // 24 KB of inputs
 // Per prep group: fp32 B tiles of the state pass (K-major, 128-B swizzle,
-// 32 fp32 per 128-B row) and bf16 T tiles.
+// 32 fp32 per 128-B row) and, in fused mode, the bf16 T tiles.
 // X = [-W (rows 0-31); Gamma q (rows 32-47)]: 4 K-blocks (dk) x 48 rows.
 // Y = decayed K^T (128 rows, dk) and P (16 rows, token) over K = 32 chunk
 // rows: group 0 stores [P; K^T], group 1 [K^T; P], matching O_a's side of S.
@@ -97,7 +108,6 @@ constexpr uint32_t kGX = 0;
 constexpr uint32_t kGY = kGX + 4 * kXBlock;           // 24 KB
 constexpr uint32_t kGTb = kGY + kYRows * 128;         // + 18 KB; T tiles: 4 x (32 rows x 128 B)
 constexpr uint32_t kTTile = 32 * 128;
-constexpr uint32_t kGroupTiles = kGTb + 4 * kTTile;  // 58 KB
 constexpr uint32_t kLd = 33;                          // fp32 scratch row stride
 constexpr uint32_t kGGs = 0;                          // G [32][33]
 constexpr uint32_t kGTs = kGGs + 32 * kLd * 4;        // T [32][33]
@@ -105,14 +115,36 @@ constexpr uint32_t kGXs = kGTs + 32 * kLd * 4;        // X [16][17]
 constexpr uint32_t kGPs = kGXs + 16 * 17 * 4;         // P staging [16][33]
 constexpr uint32_t kGBeta = kGPs + 16 * kLd * 4;      // beta[32]
 constexpr uint32_t kGL = kGBeta + 32 * 4;             // L[32]
-constexpr uint32_t kGroupScratch = ((kGL + 32 * 4) + 15) & ~15u;
+constexpr uint32_t kPrepScratch = ((kGL + 32 * 4) + 15) & ~15u;
 
-constexpr uint32_t kOffStage = 0;
-constexpr uint32_t kOffGroup = kOffStage + kNS * kStageBytes;
-constexpr uint32_t kOffScratch = kOffGroup + 2 * kGroupTiles;
-constexpr uint32_t kOffBar = kOffScratch + 2 * kGroupScratch;
+// ---- per-chunk record (split mode), written by chunk_prep_kernel into the
+// workspace and copied verbatim into the chunk's stage:
+//   T diag(beta) hi, lo | T diag(beta Gamma) hi, lo  (bf16, 32 rows x 128 B,
+//   128-B swizzled as in shared memory; the Gamma pair only for gated input)
+//   P [16][32] fp32 | beta [32] fp32 | L [32] fp32 (cumulative log-gate)
+constexpr uint32_t kRecT = 0;
+constexpr uint32_t kRecP = 4 * kTTile;                // 16 KB
+constexpr uint32_t kRecBeta = kRecP + kNQ * kC * 4;   // + 2 KB
+constexpr uint32_t kRecL = kRecBeta + kC * 4;
+constexpr uint32_t kRecBytes = kRecL + kC * 4;        // 18688
+static_assert(kRecBytes % 16 == 0, "bulk copies move 16-byte multiples");
+
+// Shared-memory layout of the state-pass kernel in each mode.
+template <bool kSplit>
+struct Layout {
+    // split: the record follows the inputs in the stage (T tiles 1024-aligned)
+    static constexpr uint32_t kStage = kSplit ? ((kStageIn + kRecBytes + 1023) & ~1023u) : kStageIn;
+    static constexpr uint32_t kGroup = kSplit ? kGTb : kGTb + 4 * kTTile;
+    static constexpr uint32_t kScratch = kSplit ? 0 : kPrepScratch;
+    static constexpr uint32_t kOffGroup = kNS * kStage;
+    static constexpr uint32_t kOffScratch = kOffGroup + 2 * kGroup;
+    static constexpr uint32_t kOffBar = kOffScratch + 2 * kScratch;
+};
+
 constexpr uint32_t kNumBars = 2 * kNS + 2 * 6 + 5;
-constexpr uint32_t kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
+template <bool kSplit>
+constexpr uint32_t smem_bytes() { return Layout<kSplit>::kOffBar + kNumBars * 8 + 16 + 1024; }
+static_assert(smem_bytes<true>() <= 227 * 1024 && smem_bytes<false>() <= 227 * 1024, "shared memory");
 
 constexpr uint32_t kWaitTries = 1u << 22;
 
@@ -122,8 +154,14 @@ struct Params {
     void *o;
     float *h_final;
     uint32_t *status;
+    uint8_t *rec;              // per-chunk records (split mode), [B*H][n_chunks][kRecBytes]
     int T, H, nh, ct, n_chunks;
 };
+
+__device__ __forceinline__ size_t rec_index(const Params &p, int b, int h, int c)
+{
+    return ((size_t)b * p.H + h) * (size_t)p.n_chunks + c;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 {
@@ -159,8 +197,8 @@ bool encode(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims
 enum : int {
     kBarFull = 0,                 // [kNS] TMA stage loaded (transaction bytes)
     kBarEmpty = kBarFull + kNS,   // [kNS] stage consumed by its prep group
-    kBarGQ = kBarEmpty + kNS,     // [2] Gram MMA of the group's chunk done
-    kBarTb = kBarGQ + 2,          // [2] T tiles written
+    kBarGQ = kBarEmpty + kNS,     // [2] Gram MMA of the group's chunk done (fused)
+    kBarTb = kBarGQ + 2,          // [2] T tiles written (fused)
     kBarUW = kBarTb + 2,          // [2] U and W MMAs done
     kBarReady = kBarUW + 2,       // [2] state-pass B tiles written
     kBarM2 = kBarReady + 2,       // [2] chunk's state pass and readout done
@@ -178,9 +216,10 @@ struct Smem {
     uint64_t *bar;
     uint32_t *tmem_slot;
     volatile uint32_t *abort;
-    __device__ uint8_t *stage(int st) const { return base + kOffStage + st * kStageBytes; }
-    __device__ uint8_t *group(int g) const { return base + kOffGroup + g * kGroupTiles; }
-    __device__ uint8_t *scratch(int g) const { return base + kOffScratch + g * kGroupScratch; }
+    uint32_t stage_bytes, group_off, group_bytes, scratch_off;
+    __device__ uint8_t *stage(int st) const { return base + st * stage_bytes; }
+    __device__ uint8_t *group(int g) const { return base + group_off + g * group_bytes; }
+    __device__ uint8_t *scratch(int g) const { return base + scratch_off + g * kPrepScratch; }
 };
 
 __device__ __forceinline__ void flag_error(uint32_t *status, volatile uint32_t *abort, uint32_t code)
@@ -219,12 +258,29 @@ __device__ __forceinline__ void split_pack(float a, float b, uint32_t &hi, uint3
 __device__ __forceinline__ void store_out(float *o, size_t i, float x) { o[i] = x; }
 __device__ __forceinline__ void store_out(__nv_bfloat16 *o, size_t i, float x) { o[i] = __float2bfloat16_rn(x); }
 
+// Gram MMA [K;Q] K^T of the chunk in the KQ tiles at `kq` (A = 64 rows: K
+// rows 0-31, Q rows 32-47, zero rows; B = the K rows), into 32 TMEM columns.
+__device__ __forceinline__ void issue_gram(uint32_t d_tmem, uint32_t kq)
+{
+    const uint32_t id_gq = idesc_bf16(64, kC, false, false);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t d = sdesc_sw128(kq + (kk >> 2) * kKQBlock + (kk & 3) * 32, 16, 1024);
+        mma_ss(d_tmem, d, d, id_gq, kk > 0);
+    }
+}
+
 // ------------------------------------------------------------------ TMA producer
+template <bool kSplit>
 __device__ void tma_role(const Smem &s, const Params &p, const CUtensorMap *tk,
                          const CUtensorMap *tv, const CUtensorMap *tq, int b, int h)
 {
     const int ct = p.ct, R = ct * p.nh;
-    const uint32_t bytes = 512u * R + 256u * ct;   // K and V: 2 x R rows x 128 B each; Q: 2 x ct rows
+    const bool gated = p.g != nullptr;
+    // K and V: 2 x R rows x 128 B each; Q: 2 x ct rows. Record: the T tiles
+    // it uses (2 or 4) and P, beta, L.
+    const uint32_t rec_t = (gated ? 4 : 2) * kTTile, rec_tail = kRecBytes - kRecP;
+    const uint32_t bytes = 512u * R + 256u * ct + (kSplit ? rec_t + rec_tail : 0u);
     int last_use[kNS];
     for (int i = 0; i < kNS; ++i) last_use[i] = -1;
     for (int c = 0; c < p.n_chunks; ++c) {
@@ -240,6 +296,12 @@ __device__ void tma_role(const Smem &s, const Params &p, const CUtensorMap *tk,
             tma_load_4d(kq + kb * kKQBlock + kC * 128, tq, bar, kb * 64, h, t0, b);
             tma_load_5d(vv + kb * kVBlock, tv, bar, kb * 64, 0, h, t0, b);
         }
+        if (kSplit) {
+            const uint8_t *rec = p.rec + rec_index(p, b, h, c) * kRecBytes;
+            uint8_t *dst = kq + kStageIn;
+            bulk_load(dst + kRecT, rec + kRecT, rec_t, bar);
+            bulk_load(dst + kRecP, rec + kRecP, rec_tail, bar);
+        }
         last_use[st] = u;
     }
     // every issued load must have landed before shared memory is released
@@ -249,32 +311,22 @@ __device__ void tma_role(const Smem &s, const Params &p, const CUtensorMap *tk,
 }
 
 // ------------------------------------------------------------------ MMA issuers
-// Prep MMAs (bf16): [K;Q] K^T, U^T = V^T (T diag beta)^T, W^T = K^T (T diag(beta Gamma))^T.
-// They run one chunk ahead of the state pass and are issued by their own
-// thread so that their issue latency overlaps the state pass's.
+// Prep MMAs (bf16): [K;Q] K^T (fused mode), U^T = V^T (T diag beta)^T,
+// W^T = K^T (T diag(beta Gamma))^T. They run one chunk ahead of the state
+// pass and are issued by their own thread so that their issue latency
+// overlaps the state pass's.
+template <bool kSplit>
 __device__ void prep_mma_role(const Smem &s, const Params &p, uint32_t tbase)
 {
     const bool gated = p.g != nullptr;
     const int n = p.n_chunks;
-    const uint32_t id_gq = idesc_bf16(64, kC, false, false);
     const uint32_t id_uw = idesc_bf16(128, kC, true, false);
 
-    // [K;Q] K^T: A = 64 rows (K rows 0-31, Q rows 32-47, zero rows), B = K rows
-    auto issue_gq = [&](int c) {
-        const int g = c & 1;
-        const uint32_t kq = smem_addr(s.stage(c % kNS));
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t d = sdesc_sw128(kq + (kk >> 2) * kKQBlock + (kk & 3) * 32, 16, 1024);
-            mma_ss(tbase + kColGQ + g * 32, d, d, id_gq, kk > 0);
-        }
-        mma_commit(&s.bar[kBarGQ + g]);
-    };
-    // T enters as hi + lo bf16 tiles
+    // T enters as hi + lo bf16 tiles (in the group's tiles, or in the stage's record)
     auto issue_uw = [&](int c) {
         const int g = c & 1;
         const uint32_t kq = smem_addr(s.stage(c % kNS)), vv = kq + 2 * kKQBlock;
-        const uint32_t tt = smem_addr(s.group(g)) + kGTb;
+        const uint32_t tt = kSplit ? kq + kStageIn + kRecT : smem_addr(s.group(g)) + kGTb;
         const uint32_t tg = tt + (gated ? 2 * kTTile : 0);
 #pragma unroll
         for (int part = 0; part < 2; ++part)
@@ -290,26 +342,36 @@ __device__ void prep_mma_role(const Smem &s, const Params &p, uint32_t tbase)
                        sdesc_sw128(tg + part * kTTile + kk * 32, 16, 1024), id_uw, part | kk);
         mma_commit(&s.bar[kBarUW + g]);
     };
-    // U/W of chunk u: its T tiles are written, and the state pass of chunk
-    // u - 2 (which read U'[g]) has finished
+    // U/W of chunk u: its T tiles are in place, and the state pass of chunk
+    // u - 2 (which read U'[g]; W[g] was drained before it started) has finished
     auto uw_ready = [&](int u) {
-        if (!wait_bar(s, kBarTb + (u & 1), (u >> 1) & 1, p.status)) return false;
+        if (kSplit) {
+            if (!wait_bar(s, kBarFull + u % kNS, (u / kNS) & 1, p.status)) return false;
+        } else {
+            if (!wait_bar(s, kBarTb + (u & 1), (u >> 1) & 1, p.status)) return false;
+        }
         if (u >= 2 && !wait_bar(s, kBarM2 + (u & 1), ((u - 2) >> 1) & 1, p.status)) return false;
         tc_fence_after();
         return true;
     };
 
     bool ok = true;
-    for (int c = 0; c < n && ok; ++c) {
-        if (!(ok = wait_bar(s, kBarFull + c % kNS, (c / kNS) & 1, p.status))) break;
-        tc_fence_after();
-        issue_gq(c);
-        if (c >= 1) {
-            if (!(ok = uw_ready(c - 1))) break;
-            issue_uw(c - 1);
+    if (kSplit) {
+        for (int c = 0; c < n && ok; ++c)
+            if ((ok = uw_ready(c))) issue_uw(c);
+    } else {
+        for (int c = 0; c < n && ok; ++c) {
+            if (!(ok = wait_bar(s, kBarFull + c % kNS, (c / kNS) & 1, p.status))) break;
+            tc_fence_after();
+            issue_gram(tbase + kColGQ + (c & 1) * 32, smem_addr(s.stage(c % kNS)));
+            mma_commit(&s.bar[kBarGQ + (c & 1)]);
+            if (c >= 1) {
+                if (!(ok = uw_ready(c - 1))) break;
+                issue_uw(c - 1);
+            }
         }
+        if (ok && uw_ready(n - 1)) issue_uw(n - 1);
     }
-    if (ok && uw_ready(n - 1)) issue_uw(n - 1);
     mma_commit(&s.bar[kBarFinal + 1]);
     uint32_t no_abort = 0;
     mbar_wait(&s.bar[kBarFinal + 1], 0, kWaitTries, &no_abort);
@@ -352,9 +414,8 @@ __device__ void chain_role(const Smem &s, const Params &p, uint32_t tbase)
     mbar_wait(&s.bar[kBarFinal], 0, kWaitTries, &no_abort);
 }
 
-// ------------------------------------------------------------------ prep groups
-// Per-row betas and cumulative log-gates of one chunk, held by warp 0 of a
-// prep group (lane = extended row), loaded one chunk ahead.
+// ------------------------------------------------------------------ prep work
+// Per-row betas and log-gates of one chunk (lane = extended row).
 struct RowVals {
     float beta, lg;
 };
@@ -372,39 +433,250 @@ __device__ __forceinline__ RowVals load_rows(const Params &p, int c, int b, int 
     return v;
 }
 
+// beta and the cumulative log-gate L (inclusive scan over the chunk's rows;
+// the token gate sits on its first row) into shared memory. One warp.
+__device__ __forceinline__ void scan_rows(RowVals rv, int lane, float *beta_s, float *L_s)
+{
+    float lg = rv.lg;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, lg, d);
+        if (lane >= d) lg += y;
+    }
+    beta_s[lane] = rv.beta;
+    L_s[lane] = lg;
+}
+
+struct PrepScratch {
+    float *Gs, *Ts, *Xs, *Ps, *beta_s, *L_s;
+};
+
+__device__ __forceinline__ PrepScratch prep_scratch(uint8_t *sc)
+{
+    return {(float *)(sc + kGGs), (float *)(sc + kGTs), (float *)(sc + kGXs),
+            (float *)(sc + kGPs), (float *)(sc + kGBeta), (float *)(sc + kGL)};
+}
+
+// Phase A of one chunk, by the 256 threads `lt` of named barrier `bar_id`
+// (warps whose index mod 4 is lt / 32 mod 4, for TMEM lane access): G and P
+// from the finished Gram accumulator at TMEM columns `gq_col`, T by blocked
+// forward substitution, then T diag(beta) and (gated) T diag(beta Gamma) as
+// hi + lo bf16 tiles at `tdst` (shared or global memory, 128-B swizzled
+// rows). Needs beta_s / L_s in place. Leaves P in w.Ps.
+__device__ void phase_a(const PrepScratch &w, uint32_t tbase, uint32_t gq_col, uint8_t *tdst,
+                        int lt, int nh, int ct, bool gated, uint32_t bar_id)
+{
+    const int lw = lt >> 5, lane = lt & 31, lq = lw & 3, hf = lw >> 2;   // TMEM lane quarter, column half
+    float *Gs = w.Gs, *Ts = w.Ts, *Xs = w.Xs, *Ps = w.Ps;
+    const float *beta_s = w.beta_s, *L_s = w.L_s;
+
+    // Gram MMA (M = 64 layout): quarter lq's lanes 0..15 hold rows
+    // 16*lq .. 16*lq + 15; half hf takes columns 16*hf .. 16*hf + 15.
+    {
+        uint32_t r[16];
+        tmem_ld16(tbase + ((uint32_t)(lq * 32) << 16) + gq_col + 16 * hf, r);
+        tmem_wait_ld();
+        const int m = 16 * lq + lane;
+        if (lane < 16 && m < kC) {
+            const float br = beta_s[m], Lr = L_s[m];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int s2 = 16 * hf + j;
+                float v = 0.f;
+                if (s2 < m) {
+                    v = br * __uint_as_float(r[j]);
+                    if (gated) v *= __expf(Lr - L_s[s2]);
+                }
+                Gs[m * kLd + s2] = v;
+            }
+        } else if (lane < 16 && m < kC + kNQ) {
+            const int i = m - kC, rr = i * nh + nh - 1;
+            const bool valid = i < ct;
+            const float Lr = valid ? L_s[rr] : 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int s2 = 16 * hf + j;
+                float x = 0.f;
+                if (valid && s2 <= rr) {
+                    x = __uint_as_float(r[j]);
+                    if (gated) x *= __expf(Lr - L_s[s2]);
+                }
+                Ps[i * kLd + s2] = x;
+            }
+        }
+    }
+    tc_fence_before();
+    named_sync(bar_id, kPrepThreads);
+
+    // T = (I + G)^{-1}: diagonal 16x16 blocks (one lane per column,
+    // forward substitution), then T_10 = -T_11 (G_10 T_00)
+    if (lw < 2 && lane < 16) {
+        const int base = 16 * lw, col = base + lane;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = (i == lane) ? 1.f : 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < 16; ++s2) {
+            const float xs = x[s2];
+#pragma unroll
+            for (int i = s2 + 1; i < 16; ++i) x[i] = fmaf(-Gs[(base + i) * kLd + base + s2], xs, x[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) Ts[(base + i) * kLd + col] = x[i];
+    }
+    named_sync(bar_id, kPrepThreads);
+    {
+        const int i = lt >> 4, j = lt & 15;
+        float a = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) a = fmaf(Gs[(16 + i) * kLd + m], Ts[m * kLd + j], a);
+        Xs[i * 17 + j] = a;
+    }
+    named_sync(bar_id, kPrepThreads);
+    {
+        const int i = lt >> 4, j = lt & 15;
+        float a = 0.f;
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+            if (u <= i) a = fmaf(Ts[(16 + i) * kLd + 16 + u], Xs[u * 17 + j], a);
+        Ts[(16 + i) * kLd + j] = -a;
+    }
+    named_sync(bar_id, kPrepThreads);
+
+    // T diag(beta) and T diag(beta Gamma) as hi + lo bf16 tiles:
+    // one (tile, row, 8-element chunk) per thread
+    if (lt < (gated ? 256 : 128)) {
+        const int pr = lt >> 7, i = (lt >> 2) & 31, ch = lt & 3;
+        uint8_t *hi = tdst + 2 * pr * kTTile, *lo = hi + kTTile;
+        uint32_t wh[4], wl[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int s0 = ch * 8 + 2 * e;
+            float v0 = s0 <= i ? Ts[i * kLd + s0] * beta_s[s0] : 0.f;
+            float v1 = s0 + 1 <= i ? Ts[i * kLd + s0 + 1] * beta_s[s0 + 1] : 0.f;
+            if (pr) {
+                v0 *= __expf(L_s[s0]);
+                v1 *= __expf(L_s[s0 + 1]);
+            }
+            split_pack(v0, v1, wh[e], wl[e]);
+        }
+        *(uint4 *)(hi + sw128_offset(i, ch)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        *(uint4 *)(lo + sw128_offset(i, ch)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+    }
+}
+
 // Row offsets of K^T and P inside the group's Y tile.
 __device__ __forceinline__ int y_row_k(int g) { return g ? 0 : kNQ; }
 __device__ __forceinline__ int y_row_p(int g) { return g ? kD : 0; }
 
+// Phase B of chunk c (group g): the state pass's fp32 B tiles. P comes from
+// `Psrc` (row stride `pld` floats), the cumulative log-gates from `L_s`, K
+// and Q from the stage at `kq`. Returns false, uniformly over the group, if a
+// wait failed or the CTA is aborting.
+__device__ bool phase_b(const Smem &s, const Params &p, uint32_t tbase, uint8_t *gt,
+                        const uint8_t *kq, const float *Psrc, int pld, const float *L_s, int c,
+                        int g, int lt, uint32_t bar_id)
+{
+    const int lw = lt >> 5, lane = lt & 31, lq = lw & 3, hf = lw >> 2;
+    const int nh = p.nh, ct = p.ct;
+    const bool gated = p.g != nullptr;
+    bool ok = (c < 2 || lt != 0) || wait_bar(s, kBarM2 + g, ((c - 2) >> 1) & 1, p.status);
+    if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) return false;
+    // P (16 rows x 8 float4)
+    if (lt < kNQ * 8) {
+        const int i = lt >> 3, ch = lt & 7;
+        const float *src = Psrc + i * pld + 4 * ch;
+        *(float4 *)(gt + kGY + sw128_offset(y_row_p(g) + i, ch)) = make_float4(src[0], src[1], src[2], src[3]);
+    }
+    // Gamma-scaled q: (token row i, dk block kb4, 8-element group q)
+    {
+        const int i = lt >> 4, kb4 = (lt >> 2) & 3, q = lt & 3;
+        const bool valid = i < ct;
+        const float gr = !valid ? 0.f : (gated ? __expf(L_s[i * nh + nh - 1]) : 1.f);
+        const uint4 u = *(const uint4 *)(kq + (kb4 >> 1) * kKQBlock + sw128_offset(kC + i, (kb4 & 1) * 4 + q));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            f[2 * e] = __uint_as_float(w[e] << 16) * gr;
+            f[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u) * gr;
+        }
+        uint8_t *dst = gt + kGX + kb4 * kXBlock;
+        *(float4 *)(dst + sw128_offset(kC + i, 2 * q)) = make_float4(f[0], f[1], f[2], f[3]);
+        *(float4 *)(dst + sw128_offset(kC + i, 2 * q + 1)) = make_float4(f[4], f[5], f[6], f[7]);
+    }
+    // decayed K^T: row dk, four groups of 4 chunk rows per thread
+    {
+        const int dk = lt & 127, q0 = (lt >> 7) * 4;
+        const float Lend = L_s[kC - 1];
+        const uint8_t *src = kq + (dk >> 6) * kKQBlock;
+        const int chunk = (dk & 63) >> 3, e = dk & 7;
+#pragma unroll
+        for (int q = q0; q < q0 + 4; ++q) {
+            float f[4];
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+                const int s2 = 4 * q + k4;
+                const float x = __bfloat162float(*(const __nv_bfloat16 *)(src + sw128_offset(s2, chunk) + e * 2));
+                f[k4] = gated ? x * __expf(Lend - L_s[s2]) : x;
+            }
+            *(float4 *)(gt + kGY + sw128_offset(y_row_k(g) + dk, q)) = make_float4(f[0], f[1], f[2], f[3]);
+        }
+    }
+    // -W (lane = dk; half hf takes chunk rows 16*hf .. 16*hf + 15)
+    ok = (lt != 0) || wait_bar(s, kBarUW + g, (c >> 1) & 1, p.status);
+    if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) return false;
+    tc_fence_after();
+    {
+        uint32_t r[16];
+        tmem_ld16(tbase + ((uint32_t)(lq * 32) << 16) + kColW + g * 32 + 16 * hf, r);
+        tmem_wait_ld();
+        const int dk = 32 * lq + lane, pos = dk & 31;
+        uint8_t *dst = gt + kGX + (dk >> 5) * kXBlock + (pos & 3) * 4;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            *(float *)(dst + sw128_offset(16 * hf + j, pos >> 2)) = -__uint_as_float(r[j]);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    named_sync(bar_id, kPrepThreads);
+    return true;
+}
+
+// Prep group g of the state-pass kernel: chunks g, g + 2, ...
+template <bool kSplit>
 __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g, int b, int h)
 {
     const int lt = threadIdx.x - (kPrepWarp + 8 * g) * 32, lw = lt >> 5, lane = lt & 31;
-    const int lq = lw & 3, hf = lw >> 2;                          // TMEM lane quarter, column half
     const uint32_t bar_id = 1 + g;
-    const uint32_t trow = tbase + ((uint32_t)(lq * 32) << 16);   // this warp's TMEM lanes
-    uint8_t *gt = s.group(g), *sc = s.scratch(g);
-    float *Gs = (float *)(sc + kGGs), *Ts = (float *)(sc + kGTs), *Xs = (float *)(sc + kGXs);
-    float *Ps = (float *)(sc + kGPs), *beta_s = (float *)(sc + kGBeta), *L_s = (float *)(sc + kGL);
-    const int nh = p.nh, ct = p.ct;
+    uint8_t *gt = s.group(g);
     const bool gated = p.g != nullptr;
 
+    if (kSplit) {
+        for (int c = g; c < p.n_chunks; c += 2) {
+            const int st = c % kNS;
+            const uint8_t *kq = s.stage(st), *rec = kq + kStageIn;
+            const bool ok = (lt != 0) || wait_bar(s, kBarFull + st, (c / kNS) & 1, p.status);
+            if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) break;
+            if (!phase_b(s, p, tbase, gt, kq, (const float *)(rec + kRecP), kC,
+                         (const float *)(rec + kRecL), c, g, lt, bar_id))
+                break;
+            if (lt == 0) {
+                mbar_arrive(&s.bar[kBarReady + g]);
+                mbar_arrive(&s.bar[kBarEmpty + st]);
+            }
+        }
+        return;
+    }
+
+    const PrepScratch w = prep_scratch(s.scratch(g));
     RowVals rv{0.f, 0.f};
     if (lw == 0) rv = load_rows(p, g, b, h, lane);
-
     for (int c = g; c < p.n_chunks; c += 2) {
         const int st = c % kNS;
         const uint8_t *kq = s.stage(st);
-
-        // ---------------- phase A: G, P, T (needs only this chunk's inputs)
         if (lw == 0) {
-            float lg = rv.lg;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, lg, d);
-                if (lane >= d) lg += y;
-            }
-            beta_s[lane] = rv.beta;
-            L_s[lane] = lg;
+            scan_rows(rv, lane, w.beta_s, w.L_s);
             rv = load_rows(p, c + 2, b, h, lane);        // next chunk of this group
         }
         // one thread polls the mbarriers; the group barrier spreads the outcome
@@ -415,165 +687,11 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
         }
         if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) break;
         tc_fence_after();
-
-        // Gram MMA (M = 64 layout): quarter lq's lanes 0..15 hold rows
-        // 16*lq .. 16*lq + 15; half hf takes columns 16*hf .. 16*hf + 15.
-        {
-            uint32_t r[16];
-            tmem_ld16(trow + kColGQ + g * 32 + 16 * hf, r);
-            tmem_wait_ld();
-            const int m = 16 * lq + lane;
-            if (lane < 16 && m < kC) {
-                const float br = beta_s[m], Lr = L_s[m];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int s2 = 16 * hf + j;
-                    float v = 0.f;
-                    if (s2 < m) {
-                        v = br * __uint_as_float(r[j]);
-                        if (gated) v *= __expf(Lr - L_s[s2]);
-                    }
-                    Gs[m * kLd + s2] = v;
-                }
-            } else if (lane < 16 && m < kC + kNQ) {
-                const int i = m - kC, rr = i * nh + nh - 1;
-                const bool valid = i < ct;
-                const float Lr = valid ? L_s[rr] : 0.f;
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int s2 = 16 * hf + j;
-                    float x = 0.f;
-                    if (valid && s2 <= rr) {
-                        x = __uint_as_float(r[j]);
-                        if (gated) x *= __expf(Lr - L_s[s2]);
-                    }
-                    Ps[i * kLd + s2] = x;
-                }
-            }
-        }
-        tc_fence_before();
-        named_sync(bar_id, kPrepThreads);
-
-        // T = (I + G)^{-1}: diagonal 16x16 blocks (one lane per column,
-        // forward substitution), then T_10 = -T_11 (G_10 T_00)
-        if (lw < 2 && lane < 16) {
-            const int base = 16 * lw, col = base + lane;
-            float x[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] = (i == lane) ? 1.f : 0.f;
-#pragma unroll
-            for (int s2 = 0; s2 < 16; ++s2) {
-                const float xs = x[s2];
-#pragma unroll
-                for (int i = s2 + 1; i < 16; ++i) x[i] = fmaf(-Gs[(base + i) * kLd + base + s2], xs, x[i]);
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) Ts[(base + i) * kLd + col] = x[i];
-        }
-        named_sync(bar_id, kPrepThreads);
-        {
-            const int i = lt >> 4, j = lt & 15;
-            float a = 0.f;
-#pragma unroll
-            for (int m = 0; m < 16; ++m) a = fmaf(Gs[(16 + i) * kLd + m], Ts[m * kLd + j], a);
-            Xs[i * 17 + j] = a;
-        }
-        named_sync(bar_id, kPrepThreads);
-        {
-            const int i = lt >> 4, j = lt & 15;
-            float a = 0.f;
-#pragma unroll
-            for (int u = 0; u < 16; ++u)
-                if (u <= i) a = fmaf(Ts[(16 + i) * kLd + 16 + u], Xs[u * 17 + j], a);
-            Ts[(16 + i) * kLd + j] = -a;
-        }
-        named_sync(bar_id, kPrepThreads);
-
-        // T diag(beta) and T diag(beta Gamma) as hi + lo bf16 tiles:
-        // one (tile, row, 8-element chunk) per thread
-        if (lt < (gated ? 256 : 128)) {
-            const int pr = lt >> 7, i = (lt >> 2) & 31, ch = lt & 3;
-            uint8_t *hi = gt + kGTb + 2 * pr * kTTile, *lo = hi + kTTile;
-            uint32_t wh[4], wl[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int s0 = ch * 8 + 2 * e;
-                float v0 = s0 <= i ? Ts[i * kLd + s0] * beta_s[s0] : 0.f;
-                float v1 = s0 + 1 <= i ? Ts[i * kLd + s0 + 1] * beta_s[s0 + 1] : 0.f;
-                if (pr) {
-                    v0 *= __expf(L_s[s0]);
-                    v1 *= __expf(L_s[s0 + 1]);
-                }
-                split_pack(v0, v1, wh[e], wl[e]);
-            }
-            *(uint4 *)(hi + sw128_offset(i, ch)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-            *(uint4 *)(lo + sw128_offset(i, ch)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-        }
+        phase_a(w, tbase, kColGQ + g * 32, gt + kGTb, lt, p.nh, p.ct, gated, bar_id);
         fence_proxy_async_smem();
         named_sync(bar_id, kPrepThreads);
         if (lt == 0) mbar_arrive(&s.bar[kBarTb + g]);
-
-        // ---------------- phase B: the state pass's fp32 B tiles
-        ok = (c < 2 || lt != 0) || wait_bar(s, kBarM2 + g, ((c - 2) >> 1) & 1, p.status);
-        if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) break;
-        // P (16 rows x 8 float4)
-        if (lt < kNQ * 8) {
-            const int i = lt >> 3, ch = lt & 7;
-            const float *src = Ps + i * kLd + 4 * ch;
-            *(float4 *)(gt + kGY + sw128_offset(y_row_p(g) + i, ch)) = make_float4(src[0], src[1], src[2], src[3]);
-        }
-        // Gamma-scaled q: (token row i, dk block kb4, 8-element group q)
-        {
-            const int i = lt >> 4, kb4 = (lt >> 2) & 3, q = lt & 3;
-            const bool valid = i < ct;
-            const float gr = !valid ? 0.f : (gated ? __expf(L_s[i * nh + nh - 1]) : 1.f);
-            const uint4 u = *(const uint4 *)(kq + (kb4 >> 1) * kKQBlock + sw128_offset(kC + i, (kb4 & 1) * 4 + q));
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                f[2 * e] = __uint_as_float(w[e] << 16) * gr;
-                f[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u) * gr;
-            }
-            uint8_t *dst = gt + kGX + kb4 * kXBlock;
-            *(float4 *)(dst + sw128_offset(kC + i, 2 * q)) = make_float4(f[0], f[1], f[2], f[3]);
-            *(float4 *)(dst + sw128_offset(kC + i, 2 * q + 1)) = make_float4(f[4], f[5], f[6], f[7]);
-        }
-        // decayed K^T: row dk, four groups of 4 chunk rows per thread
-        {
-            const int dk = lt & 127, q0 = (lt >> 7) * 4;
-            const float Lend = L_s[kC - 1];
-            const uint8_t *src = kq + (dk >> 6) * kKQBlock;
-            const int chunk = (dk & 63) >> 3, e = dk & 7;
-#pragma unroll
-            for (int q = q0; q < q0 + 4; ++q) {
-                float f[4];
-#pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) {
-                    const int s2 = 4 * q + k4;
-                    const float x = __bfloat162float(*(const __nv_bfloat16 *)(src + sw128_offset(s2, chunk) + e * 2));
-                    f[k4] = gated ? x * __expf(Lend - L_s[s2]) : x;
-                }
-                *(float4 *)(gt + kGY + sw128_offset(y_row_k(g) + dk, q)) = make_float4(f[0], f[1], f[2], f[3]);
-            }
-        }
-        // -W (lane = dk; half hf takes chunk rows 16*hf .. 16*hf + 15)
-        ok = (lt != 0) || wait_bar(s, kBarUW + g, (c >> 1) & 1, p.status);
-        if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) break;
-        tc_fence_after();
-        {
-            uint32_t r[16];
-            tmem_ld16(trow + kColW + g * 32 + 16 * hf, r);
-            tmem_wait_ld();
-            const int dk = 32 * lq + lane, pos = dk & 31;
-            uint8_t *dst = gt + kGX + (dk >> 5) * kXBlock + (pos & 3) * 4;
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                *(float *)(dst + sw128_offset(16 * hf + j, pos >> 2)) = -__uint_as_float(r[j]);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        named_sync(bar_id, kPrepThreads);
+        if (!phase_b(s, p, tbase, gt, kq, w.Ps, kLd, w.L_s, c, g, lt, bar_id)) break;
         if (lt == 0) {
             mbar_arrive(&s.bar[kBarReady + g]);
             mbar_arrive(&s.bar[kBarEmpty + st]);
@@ -673,24 +791,29 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, int b, 
     }
 }
 
-// ------------------------------------------------------------------ kernel
-template <typename TOut>
+// ------------------------------------------------------------------ state-pass kernel
+template <typename TOut, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 const __grid_constant__ CUtensorMap tm_q, const Params p)
 {
+    using Lay = Layout<kSplit>;
     extern __shared__ uint8_t smem_raw[];
     Smem s;
     s.base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    s.bar = (uint64_t *)(s.base + kOffBar);
+    s.bar = (uint64_t *)(s.base + Lay::kOffBar);
     s.tmem_slot = (uint32_t *)(s.bar + kNumBars);
     s.abort = s.tmem_slot + 1;
+    s.stage_bytes = Lay::kStage;
+    s.group_off = Lay::kOffGroup;
+    s.group_bytes = Lay::kGroup;
+    s.scratch_off = Lay::kOffScratch;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x, b = bh / p.H, h = bh - b * p.H;
 
     // Zero every tile once: rows TMA never writes (padding rows, query rows
     // beyond the chunk's tokens) must hold finite zeros.
-    for (uint32_t i = threadIdx.x * 16; i < kOffScratch; i += kThreads * 16)
+    for (uint32_t i = threadIdx.x * 16; i < Lay::kOffScratch; i += kThreads * 16)
         *(uint4 *)(s.base + i) = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
         for (int i = 0; i < (int)kNumBars; ++i) mbar_init(&s.bar[i], 1);
@@ -712,17 +835,103 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     if (warp < kPrepWarp) {
         epi_role<TOut>(s, p, tbase, b, h);
     } else if (warp < kTmaWarp) {
-        prep_role(s, p, tbase, (warp - kPrepWarp) >> 3, b, h);
+        prep_role<kSplit>(s, p, tbase, (warp - kPrepWarp) >> 3, b, h);
     } else if (warp == kTmaWarp) {
-        if (lane == 0) tma_role(s, p, &tm_k, &tm_v, &tm_q, b, h);
+        if (lane == 0) tma_role<kSplit>(s, p, &tm_k, &tm_v, &tm_q, b, h);
     } else if (warp == kChainWarp) {
         if (lane == 0) chain_role(s, p, tbase);
     } else {
-        if (lane == 0) prep_mma_role(s, p, tbase);
+        if (lane == 0) prep_mma_role<kSplit>(s, p, tbase);
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, kTmemCols);
+}
+
+// ------------------------------------------------------------------ prep kernel
+// Phase A for one chunk per CTA, all chunks of all heads in parallel: TMA the
+// chunk's K and Q, Gram MMA into 32 TMEM columns, phase_a with the T tiles
+// going straight to the chunk's record, then P, beta and L.
+constexpr int kPrepKThreads = 256;
+constexpr uint32_t kPKScratch = 2 * kKQBlock;                       // after the KQ tiles
+constexpr uint32_t kPKBar = kPKScratch + kPrepScratch;
+constexpr uint32_t kPKSmem = kPKBar + 2 * 8 + 16 + 1024;
+constexpr uint32_t kPKTmemCols = 32;
+
+__global__ void __launch_bounds__(kPrepKThreads, 4)
+chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+                  const Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t *bar = (uint64_t *)(base + kPKBar);                     // [0] loads, [1] Gram MMA
+    uint32_t *tmem_slot = (uint32_t *)(bar + 2);
+    volatile uint32_t *abort = tmem_slot + 1;
+    const int lt = threadIdx.x, warp = lt >> 5, lane = lt & 31;
+    const int c = blockIdx.x % p.n_chunks, bh = blockIdx.x / p.n_chunks;
+    const int b = bh / p.H, h = bh - b * p.H;
+    const int ct = p.ct, R = ct * p.nh;
+    const PrepScratch w = prep_scratch(base + kPKScratch);
+
+    // rows TMA does not write (padding, queries beyond the chunk) stay zero
+    for (uint32_t i = lt * 16; i < 2 * kKQBlock; i += kPrepKThreads * 16)
+        *(uint4 *)(base + i) = make_uint4(0, 0, 0, 0);
+    if (lt == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        *abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_q);
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, kPKTmemCols);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+
+    if (lt == 0) {
+        mbar_arrive_expect_tx(&bar[0], 256u * R + 256u * ct);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+            tma_load_5d(base + kb * kKQBlock, &tm_k, &bar[0], kb * 64, 0, h, c * ct, b);
+            tma_load_4d(base + kb * kKQBlock + kC * 128, &tm_q, &bar[0], kb * 64, h, c * ct, b);
+        }
+    }
+    if (warp == 0) scan_rows(load_rows(p, c, b, h, lane), lane, w.beta_s, w.L_s);
+    bool ok = true, issued = false;
+    if (lt == 0) {
+        ok = mbar_wait(&bar[0], 0, kWaitTries, abort);
+        if (ok) {
+            tc_fence_after();
+            issue_gram(tbase, smem_addr(base));
+            mma_commit(&bar[1]);
+            issued = true;
+            ok = mbar_wait(&bar[1], 0, kWaitTries, abort);
+        }
+        if (!ok) flag_error(p.status, abort, kDevTimeout);
+    }
+    if (!group_any(1, kPrepKThreads, !ok)) {
+        tc_fence_after();
+        uint8_t *rec = p.rec + rec_index(p, b, h, c) * kRecBytes;
+        phase_a(w, tbase, 0, rec + kRecT, lt, p.nh, ct, p.g != nullptr, 1);
+        float *rp = (float *)(rec + kRecP);
+        for (int i = lt; i < kNQ * kC; i += kPrepKThreads) rp[i] = w.Ps[(i >> 5) * kLd + (i & 31)];
+        if (lt < kC) {
+            ((float *)(rec + kRecBeta))[lt] = w.beta_s[lt];
+            ((float *)(rec + kRecL))[lt] = w.L_s[lt];
+        }
+    } else if (lt == 0) {
+        // loads or the MMA may still be in flight: let them finish (bounded)
+        // before shared memory and TMEM are released
+        uint32_t no_abort = 0;
+        mbar_wait(&bar[0], 0, kWaitTries, &no_abort);
+        if (issued) mbar_wait(&bar[1], 0, kWaitTries, &no_abort);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, kPKTmemCols);
 }
 
 }  // namespace
@@ -733,11 +942,20 @@ bool chunk_tc_supported(const Problem &p)
            tensor_map_encoder() != nullptr;
 }
 
-size_t chunk_tc_scratch_bytes(const Problem &) { return 0; }
+namespace {
+int chunk_tokens(int nh) { return (kC / nh < kNQ) ? kC / nh : kNQ; }
+}  // namespace
+
+size_t chunk_tc_records_bytes(const Problem &p)
+{
+    const int ct = chunk_tokens(p.nh);
+    const size_t n_chunks = p.T > 0 ? (size_t)(p.T + ct - 1) / ct : 0;
+    return (size_t)p.B * p.H * n_chunks * kRecBytes;
+}
 
 cudaError_t launch_chunk_tc(const Problem &p)
 {
-    const int nh = p.nh, ct = (kC / nh < kNQ) ? kC / nh : kNQ;
+    const int nh = p.nh, ct = chunk_tokens(nh);
     const cuuint64_t B = p.B, T = p.T, H = p.H;
     CUtensorMap tk, tv, tq;
     const cuuint64_t dk[5] = {kD, (cuuint64_t)nh, H, T, B};
@@ -749,10 +967,6 @@ cudaError_t launch_chunk_tc(const Problem &p)
     if (!encode(&tk, p.k, 5, dk, sk, bk) || !encode(&tv, p.v, 5, dk, sk, bk) ||
         !encode(&tq, p.q, 4, dq, sq, bq))
         return cudaErrorInvalidValue;
-    auto kernel = p.out_dtype == DP_F32 ? chunk_tc_kernel<float> : chunk_tc_kernel<__nv_bfloat16>;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
     Params pr;
     pr.beta = (const __nv_bfloat16 *)p.beta;
     pr.g = (const __nv_bfloat16 *)p.g;
@@ -760,12 +974,33 @@ cudaError_t launch_chunk_tc(const Problem &p)
     pr.o = p.o;
     pr.h_final = p.h_final;
     pr.status = p.status;
+    pr.rec = (uint8_t *)p.scratch;
     pr.T = p.T;
     pr.H = p.H;
     pr.nh = nh;
     pr.ct = ct;
     pr.n_chunks = (p.T + ct - 1) / ct;
-    kernel<<<p.B * p.H, kThreads, kSmemBytes, p.stream>>>(tk, tv, tq, pr);
+
+    // split whenever the workspace holds every chunk's record
+    const size_t rec_bytes = chunk_tc_records_bytes(p);
+    const bool split = p.scratch != nullptr && rec_bytes > 0 && p.scratch_bytes >= rec_bytes;
+    cudaError_t e;
+    if (split) {
+        e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kPKSmem);
+        if (e != cudaSuccess) return e;
+        const size_t n_ctas = (size_t)p.B * p.H * pr.n_chunks;
+        if (n_ctas > 0x7fffffffu) return cudaErrorInvalidValue;
+        chunk_prep_kernel<<<(unsigned)n_ctas, kPrepKThreads, kPKSmem, p.stream>>>(tk, tq, pr);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    auto kernel = p.out_dtype == DP_F32
+                      ? (split ? chunk_tc_kernel<float, true> : chunk_tc_kernel<float, false>)
+                      : (split ? chunk_tc_kernel<__nv_bfloat16, true> : chunk_tc_kernel<__nv_bfloat16, false>);
+    const uint32_t smem = split ? smem_bytes<true>() : smem_bytes<false>();
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kernel<<<p.B * p.H, kThreads, smem, p.stream>>>(tk, tv, tq, pr);
     return cudaGetLastError();
 }
 

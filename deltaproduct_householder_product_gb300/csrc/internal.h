@@ -31,7 +31,10 @@ cudaError_t launch_recurrent(const Problem &p);
 
 // Tensor-core chunked kernel (tcgen05 / TMEM / TMA): bf16, D_k = D_v = 128.
 bool chunk_tc_supported(const Problem &p);
-size_t chunk_tc_scratch_bytes(const Problem &p);
+// Workspace bytes (after the status block) of the per-chunk records that
+// let launch_chunk_tc split into a parallel prep kernel and the state-pass
+// kernel; with less scratch it runs the fused single kernel.
+size_t chunk_tc_records_bytes(const Problem &p);
 cudaError_t launch_chunk_tc(const Problem &p);
 
 cudaError_t launch_state_io(int op, int B, int H, int Dk, int Dv, float *state,

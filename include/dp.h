@@ -76,7 +76,7 @@ typedef struct {
 } dp_dims;
 
 /* ABI version of this header (bumped on any signature change). */
-#define DP_ABI_VERSION 2
+#define DP_ABI_VERSION 3
 int dp_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -85,6 +85,16 @@ const char *dp_status_string(dp_status s);
 /* Bytes of device workspace dp_forward needs for `dims` (>= 256). The first
  * 4 bytes hold the device status word. */
 dp_status dp_forward_workspace_size(const dp_dims *dims, size_t *bytes);
+
+/* Bytes of device workspace with which dp_forward runs its fastest path
+ * (>= dp_forward_workspace_size). For the tensor-core chunk path this adds
+ * one 18688-byte record per (batch, head, chunk) of ceil(T / ct) chunks,
+ * ct = min(16, 32 / n_h) tokens: a first kernel then prepares every chunk's
+ * UT transform in parallel and the state-pass kernel streams the records in.
+ * With a workspace of at least dp_forward_workspace_size but less than
+ * this, dp_forward runs one fused kernel instead: slower, bit-identical
+ * results. Both sizes are equal for the recurrent path. */
+dp_status dp_forward_workspace_size_fast(const dp_dims *dims, size_t *bytes);
 
 /* Whole-sequence forward (the extended T*n_h sequence of the paper's Sec.5.1,
  * processed in chunks by the tensor-core kernel):

@@ -26,11 +26,14 @@ def cuda(x):
     return {k: (None if v is None else v.cuda()) for k, v in x.items()}
 
 
-def run(dp, x, impl="chunk_tc", h0=True, out_dtype=torch.float32):
+def run(dp, x, impl="chunk_tc", h0=True, out_dtype=torch.float32, path="split"):
     """Forward through the C ABI; o in fp32 by default (the tolerance is on the
-    kernel's arithmetic; a bf16 o adds its own final rounding, tested below)."""
+    kernel's arithmetic; a bf16 o adds its own final rounding, tested below).
+    ``path`` "split" hands dp_forward the fast workspace (parallel prep kernel +
+    state-pass kernel), "fused" only the minimum (one fused kernel)."""
     xc = cuda(x)
-    ws = torch.zeros(dp.workspace_size(*_dims(x), impl=impl), dtype=torch.uint8, device="cuda")
+    size = dp.workspace_size(*_dims(x), impl=impl, fast=(path == "split"))
+    ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
     o, hf = dp.forward(xc["q"], xc["k"], xc["v"], xc["beta"], xc["g"],
                        xc["h0"] if h0 else None, impl=impl, workspace=ws, out_dtype=out_dtype)
     dp.check_status(ws)
@@ -52,14 +55,43 @@ CASES = [(base, nh, T) for base in (W.BASE, W.NEARDUP, W.GATED, W.LONG)
     (W.GATED, 3, 64), (W.NEARDUP, 2, 65), (W.LONG, 4, 1), (W.LONG, 1, 5), (W.GATED, 4, 17)]
 
 
+@pytest.mark.parametrize("path", ["split", "fused"])
 @pytest.mark.parametrize("base,nh,T", CASES, ids=lambda v: getattr(v, "name", str(v)))
-def test_small_parity(dp, base, nh, T):
+def test_small_parity(dp, base, nh, T, path):
     w = base.scaled(B=2, H=3, T=T, nh=nh)
     x = W.make_inputs(w)
-    o, hf = run(dp, x)
+    o, hf = run(dp, x, path=path)
     ro, rh = ref(x)
     assert_parity(o, ro, "bf16", "o")
     assert_parity(hf, rh, "bf16", "h_final")
+
+
+def test_workspace_sizes(dp):
+    """The minimum workspace is the status block; the fast one adds one
+    18688-byte record per (batch, head, chunk), chunks of min(16, 32 / n_h)
+    tokens. The recurrent path needs no records."""
+    for nh, T in ((1, 100), (2, 2048), (3, 31), (4, 8)):
+        ct = min(16, 32 // nh)
+        lo = dp.workspace_size(3, T, 5, 128, 128, nh, impl="chunk_tc")
+        hi = dp.workspace_size(3, T, 5, 128, 128, nh, impl="chunk_tc", fast=True)
+        assert lo == 256
+        assert hi - lo >= 3 * 5 * (-(-T // ct)) * 18688 and (hi - lo) % 256 == 0
+        assert dp.workspace_size(3, T, 5, 128, 128, nh, impl="recurrent", fast=True) == 256
+
+
+@pytest.mark.parametrize("base,nh,T,h0", [(W.BASE, 2, 300, True), (W.GATED, 3, 77, True),
+                                          (W.GATED, 1, 129, False), (W.NEARDUP, 4, 50, True),
+                                          (W.LONG, 2, 17, False)],
+                         ids=lambda v: getattr(v, "name", str(v)))
+def test_split_equals_fused_bitwise(dp, base, nh, T, h0):
+    """Both ways of running the chunk path share every arithmetic step (the
+    prep kernel runs the fused kernel's phase A and hands its bytes over
+    unchanged), so outputs and final states agree bit for bit."""
+    x = W.make_inputs(base.scaled(B=2, H=3, T=T, nh=nh))
+    o_s, h_s = run(dp, x, h0=h0, path="split")
+    o_f, h_f = run(dp, x, h0=h0, path="fused")
+    assert torch.equal(o_s, o_f)
+    assert torch.equal(h_s, h_f)
 
 
 @pytest.mark.parametrize("base", [W.BASE, W.GATED, W.NEARDUP], ids=lambda w: w.name)
