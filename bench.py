@@ -358,7 +358,7 @@ def ours_arm(args, w):
 # DRAM bytes (read + write) per forward, summed over its launches, from an ncu
 # capture of the current kernels; keyed by (workload, kernel family, launches
 # per forward); absent = not captured for this build
-TRAFFIC = {}
+TRAFFIC = {("b4h8t2048-nh2-d128-bf16", "auto", 2): 199_753_472}
 
 
 def main():
