@@ -155,10 +155,8 @@ def forward_calls(dp, L, w, copies, kernel, stream, fused=False):
                 _lib._ptr(c["beta"]), _lib._ptr(c["g"]), _lib._ptr(c["h0"]), _lib._ptr(c["o"]),
                 _lib._ptr(c["hf"]), _lib._ptr(c["ws"]), ctypes.c_size_t(need), s)
         calls.append((L.dp_forward, args))
-    # the chunk path splits into a prep kernel and the state-pass kernel when
-    # the workspace holds the per-chunk records
-    launches = 2 if need > _lib.workspace_size(dims) else 1
-    return calls, dims, launches
+    path = _lib.forward_path(dims, need)
+    return calls, dims, path
 
 
 def run_calls(calls, n, start=0):
@@ -250,7 +248,8 @@ def ours_arm(args, w):
     wbytes = W.algorithmic_bytes(w, out_bytes=4)
     n_copies = max(2, -(-3 * L2_BYTES // wbytes))          # rotate copies: > 3x L2 in total
     x, copies = make_copies(w, n_copies, dev)
-    calls, dims, launches = forward_calls(dp, L, w, copies, args.kernel, stream, args.fused)
+    calls, dims, path = forward_calls(dp, L, w, copies, args.kernel, stream, args.fused)
+    launches = _lib.LAUNCHES[path]
 
     run_calls(calls, args.warmup)
     torch.cuda.synchronize()
@@ -333,8 +332,7 @@ def ours_arm(args, w):
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "nh": w.nh, "Dk": w.Dk,
                    "Dv": w.Dv, "kernel": args.kernel, "gated": w.gated,
-                   "path": "fused" if launches == 1 and args.kernel != "recurrent" else
-                           ("split" if launches == 2 else "recurrent"),
+                   "path": path,
                    "l2": f"{n_copies} rotating input/output copies "
                          f"({n_copies * wbytes / 1e6:.0f} MB > 129 MB L2)",
                    "parallelism": f"replicas x{world}"},
@@ -343,7 +341,7 @@ def ours_arm(args, w):
         "gpu_launches": args.steps * launches,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak,
-                     "traffic": TRAFFIC.get((w.name, args.kernel, launches)),
+                     "traffic": TRAFFIC.get((w.name, path)),
                      "peak_kind": peak_kind, "algorithmic_bytes": wbytes,
                      "scope": "one forward: every launch dp_forward enqueues"},
         "clocks": clocks,
@@ -356,9 +354,9 @@ def ours_arm(args, w):
 
 
 # DRAM bytes (read + write) per forward, summed over its launches, from an ncu
-# capture of the current kernels; keyed by (workload, kernel family, launches
-# per forward); absent = not captured for this build
-TRAFFIC = {("b4h8t2048-nh2-d128-bf16", "auto", 2): 199_753_472}
+# capture of the current kernels; keyed by (workload, path); absent = not
+# captured for this build
+TRAFFIC = {("b4h8t2048-nh2-d128-bf16", "chunk_coop"): 146_669_312}
 
 
 def main():

@@ -11,7 +11,8 @@ import torch
 from . import _lib
 from ._lib import DPError, STATE_EXPORT, STATE_IMPORT, STATE_ZERO  # noqa: F401
 
-__all__ = ["forward", "forward_noalloc", "supports", "decode_step", "state_io", "check_status", "workspace_size",
+__all__ = ["forward", "forward_noalloc", "forward_path", "supports", "decode_step", "state_io", "check_status",
+           "workspace_size",
            "DPError", "abi_version"]
 
 
@@ -25,6 +26,13 @@ def workspace_size(B, T, H, Dk, Dv, nh, dtype=torch.bfloat16, impl="auto", out_d
     the size with which it takes its fastest path (the chunk path's parallel
     prep kernel and per-chunk records)."""
     return _lib.workspace_size(_lib.make_dims(B, T, H, Dk, Dv, nh, dtype, impl, out_dtype), fast)
+
+
+def forward_path(B, T, H, Dk, Dv, nh, workspace_bytes, dtype=torch.bfloat16, impl="auto", out_dtype=None):
+    """How ``forward`` runs this problem with a workspace of ``workspace_bytes``:
+    "recurrent", "chunk_fused", "chunk_split" (two kernels) or "chunk_coop"
+    (one cooperative launch)."""
+    return _lib.forward_path(_lib.make_dims(B, T, H, Dk, Dv, nh, dtype, impl, out_dtype), workspace_bytes)
 
 
 def supports(impl, B, T, H, Dk, Dv, nh, dtype=torch.bfloat16):

@@ -49,12 +49,14 @@ def lib():
         L.dp_status_string.restype = ctypes.c_char_p
         L.dp_forward_workspace_size.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(ctypes.c_size_t)]
         L.dp_forward_workspace_size_fast.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(ctypes.c_size_t)]
+        L.dp_forward_path.argtypes = [ctypes.POINTER(Dims), ctypes.c_size_t, ctypes.POINTER(ctypes.c_int)]
         L.dp_forward.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 9 + [ctypes.c_size_t, _vp]
         L.dp_decode_step.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 7 + [_vp]
         L.dp_state_io.argtypes = [ctypes.c_int] * 5 + [_vp, _vp, ctypes.c_int, ctypes.c_int, _vp]
         L.dp_check_status.argtypes = [_vp, _vp]
         L.dp_forward_noalloc.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 9
-        for name in ("dp_forward_workspace_size", "dp_forward_workspace_size_fast", "dp_forward", "dp_decode_step",
+        for name in ("dp_forward_workspace_size", "dp_forward_workspace_size_fast", "dp_forward_path",
+                     "dp_forward", "dp_decode_step",
                      "dp_state_io", "dp_check_status", "dp_forward_noalloc"):
             getattr(L, name).restype = ctypes.c_int
         _LIB = L
@@ -108,6 +110,18 @@ def make_dims(B, T, H, Dk, Dv, nh, dtype, impl="auto", out_dtype=None):
     else:
         od = out_dtype if isinstance(out_dtype, int) else _dtype_code(out_dtype)
     return Dims(B, T, H, Dk, Dv, nh, dt, IMPLS[impl] if isinstance(impl, str) else int(impl), od)
+
+
+PATHS = {0: "recurrent", 1: "chunk_fused", 2: "chunk_split", 3: "chunk_coop"}
+LAUNCHES = {"recurrent": 1, "chunk_fused": 1, "chunk_split": 2, "chunk_coop": 1}
+
+
+def forward_path(dims, workspace_bytes):
+    """dp_forward_path: the path name dp_forward takes with this workspace."""
+    code = ctypes.c_int(-1)
+    _check(lib().dp_forward_path(ctypes.byref(dims), ctypes.c_size_t(workspace_bytes), ctypes.byref(code)),
+           "dp_forward_path")
+    return PATHS[code.value]
 
 
 def workspace_size(dims, fast=False):

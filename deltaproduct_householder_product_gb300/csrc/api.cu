@@ -126,6 +126,22 @@ dp_status dp_forward_workspace_size_fast(const dp_dims *dims, size_t *bytes)
     return DP_OK;
 }
 
+dp_status dp_forward_path(const dp_dims *dims, size_t workspace_bytes, int *path)
+{
+    if (!path) return DP_ERR_INVALID_ARG;
+    DP_TRY(check_dims(dims, false));
+    size_t need = 0;
+    DP_TRY(dp_forward_workspace_size(dims, &need));
+    if (workspace_bytes < need) return DP_ERR_WORKSPACE;
+    dp::Problem p = make_problem(dims, dims->T);
+    if (!use_chunk_tc(dims, p)) {
+        *path = DP_PATH_RECURRENT;
+        return DP_OK;
+    }
+    p.scratch_bytes = workspace_bytes - kStatusBlock;
+    return from_cuda(dp::chunk_tc_path(p, path));
+}
+
 dp_status dp_forward(const dp_dims *dims, const void *q, const void *k, const void *v,
                      const void *beta, const void *g, const float *h0, void *o,
                      float *h_final, void *workspace, size_t workspace_bytes,

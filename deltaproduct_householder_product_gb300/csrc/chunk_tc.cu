@@ -155,8 +155,31 @@ struct Params {
     float *h_final;
     uint32_t *status;
     uint8_t *rec;              // per-chunk records (split mode), [B*H][n_chunks][kRecBytes]
-    int T, H, nh, ct, n_chunks;
+    uint32_t *flags;           // cooperative mode: record published, [B*H][n_chunks]
+    uint32_t *sync;            // cooperative mode: [0] launch generation, [1] CTAs finished
+    int T, H, nh, ct, n_chunks, bh_count;
 };
+
+// Cooperative mode: a record is published by storing generation + 1 into
+// its flag (release); the state pass acquires it before loading the record.
+__device__ __forceinline__ void flag_publish(uint32_t *flag, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t flag_read(const uint32_t *flag)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t read_generation(const uint32_t *sync)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(sync) : "memory");
+    return v;
+}
 
 __device__ __forceinline__ size_t rec_index(const Params &p, int b, int h, int c)
 {
@@ -271,11 +294,14 @@ __device__ __forceinline__ void issue_gram(uint32_t d_tmem, uint32_t kq)
 }
 
 // ------------------------------------------------------------------ TMA producer
-template <bool kSplit>
+constexpr uint32_t kFlagTries = 1u << 24;   // x >= 64 ns each: seconds, then a timeout
+
+template <bool kSplit, bool kCoop>
 __device__ void tma_role(const Smem &s, const Params &p, const CUtensorMap *tk,
                          const CUtensorMap *tv, const CUtensorMap *tq, int b, int h)
 {
     const int ct = p.ct, R = ct * p.nh;
+    const uint32_t want = kCoop ? read_generation(p.sync) + 1 : 0;
     const bool gated = p.g != nullptr;
     // K and V: 2 x R rows x 128 B each; Q: 2 x ct rows. Record: the T tiles
     // it uses (2 or 4) and P, beta, L.
@@ -286,6 +312,18 @@ __device__ void tma_role(const Smem &s, const Params &p, const CUtensorMap *tk,
     for (int c = 0; c < p.n_chunks; ++c) {
         const int st = c % kNS, u = c / kNS;
         if (u >= 1 && !wait_bar(s, kBarEmpty + st, (u - 1) & 1, p.status)) break;
+        if (kCoop) {
+            // the prep CTAs of this launch publish the chunk's record: acquire
+            // it, then order the bulk copy (async proxy) after that read
+            const uint32_t *flag = p.flags + rec_index(p, b, h, c);
+            uint32_t tries = 0;
+            while (flag_read(flag) != want && ++tries < kFlagTries && !*s.abort) __nanosleep(64);
+            if (tries >= kFlagTries || *s.abort) {
+                flag_error(p.status, s.abort, kDevTimeout);
+                break;
+            }
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
         uint8_t *kq = s.stage(st), *vv = kq + 2 * kKQBlock;
         uint64_t *bar = &s.bar[kBarFull + st];
         mbar_arrive_expect_tx(bar, bytes);
@@ -792,10 +830,9 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, int b, 
 }
 
 // ------------------------------------------------------------------ state-pass kernel
-template <typename TOut, bool kSplit>
-__global__ void __launch_bounds__(kThreads, 1)
-chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                const __grid_constant__ CUtensorMap tm_q, const Params p)
+template <typename TOut, bool kSplit, bool kCoop>
+__device__ __forceinline__ void state_pass_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                                               const CUtensorMap &tm_q, const Params &p, int bh)
 {
     using Lay = Layout<kSplit>;
     extern __shared__ uint8_t smem_raw[];
@@ -809,7 +846,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     s.group_bytes = Lay::kGroup;
     s.scratch_off = Lay::kOffScratch;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x, b = bh / p.H, h = bh - b * p.H;
+    const int b = bh / p.H, h = bh - b * p.H;
 
     // Zero every tile once: rows TMA never writes (padding rows, query rows
     // beyond the chunk's tokens) must hold finite zeros.
@@ -837,7 +874,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     } else if (warp < kTmaWarp) {
         prep_role<kSplit>(s, p, tbase, (warp - kPrepWarp) >> 3, b, h);
     } else if (warp == kTmaWarp) {
-        if (lane == 0) tma_role<kSplit>(s, p, &tm_k, &tm_v, &tm_q, b, h);
+        if (lane == 0) tma_role<kSplit, kCoop>(s, p, &tm_k, &tm_v, &tm_q, b, h);
     } else if (warp == kChainWarp) {
         if (lane == 0) chain_role(s, p, tbase);
     } else {
@@ -848,11 +885,75 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
+template <typename TOut, bool kSplit>
+__global__ void __launch_bounds__(kThreads, 1)
+chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                const __grid_constant__ CUtensorMap tm_q, const Params p)
+{
+    state_pass_cta<TOut, kSplit, false>(tm_k, tm_v, tm_q, p, blockIdx.x);
+}
+
 // ------------------------------------------------------------------ prep kernel
-// Phase A for one chunk per CTA, all chunks of all heads in parallel: TMA the
-// chunk's K and Q, Gram MMA into 32 TMEM columns, phase_a with the T tiles
-// going straight to the chunk's record, then P, beta and L.
-constexpr int kPrepKThreads = 256;
+// Prep of one chunk by a group of 256 threads (`lt` = 0..255; warps whose
+// index mod 4 is lt / 32 mod 4, for TMEM lane access): TMA its K and Q tiles
+// into `stage` (rows TMA never writes must already be zero), Gram MMA into
+// TMEM columns `gq_col`, phase_a with the T tiles going straight to the
+// chunk's record, then P, beta and L. `bars` = [loads, Gram MMA], used at
+// phase `parity`. Returns false, uniformly over the group, after a timeout
+// (the group's loads and MMA drained first).
+__device__ bool prep_chunk(const Params &p, const CUtensorMap *tk, const CUtensorMap *tq,
+                           uint8_t *stage, const PrepScratch &w, uint64_t *bars, uint32_t parity,
+                           volatile uint32_t *abort, uint32_t tbase, uint32_t gq_col, int lt,
+                           uint32_t bar_id, int b, int h, int c)
+{
+    const int lane = lt & 31, ct = p.ct, R = ct * p.nh;
+    if (lt == 0) {
+        mbar_arrive_expect_tx(&bars[0], 256u * R + 256u * ct);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+            tma_load_5d(stage + kb * kKQBlock, tk, &bars[0], kb * 64, 0, h, c * ct, b);
+            tma_load_4d(stage + kb * kKQBlock + kC * 128, tq, &bars[0], kb * 64, h, c * ct, b);
+        }
+    }
+    if (lt < 32) scan_rows(load_rows(p, c, b, h, lane), lane, w.beta_s, w.L_s);
+    bool ok = true;
+    if (lt == 0) {
+        bool issued = false;
+        ok = mbar_wait(&bars[0], parity, kWaitTries, abort);
+        if (ok) {
+            tc_fence_after();
+            issue_gram(tbase + gq_col, smem_addr(stage));
+            mma_commit(&bars[1]);
+            issued = true;
+            ok = mbar_wait(&bars[1], parity, kWaitTries, abort);
+        }
+        if (!ok) {
+            flag_error(p.status, abort, kDevTimeout);
+            // the loads or the MMA may still be in flight: let them finish
+            // (bounded) before shared memory and TMEM are released
+            uint32_t no_abort = 0;
+            mbar_wait(&bars[0], parity, kWaitTries, &no_abort);
+            if (issued) mbar_wait(&bars[1], parity, kWaitTries, &no_abort);
+        }
+    }
+    if (group_any(bar_id, kPrepThreads, !ok || *abort)) return false;
+    tc_fence_after();
+    uint8_t *rec = p.rec + rec_index(p, b, h, c) * kRecBytes;
+    phase_a(w, tbase, gq_col, rec + kRecT, lt, p.nh, ct, p.g != nullptr, bar_id);
+    float *rp = (float *)(rec + kRecP);
+    for (int i = lt; i < kNQ * kC; i += kPrepThreads) rp[i] = w.Ps[(i >> 5) * kLd + (i & 31)];
+    if (lt < kC) {
+        ((float *)(rec + kRecBeta))[lt] = w.beta_s[lt];
+        ((float *)(rec + kRecL))[lt] = w.L_s[lt];
+    }
+    // the record is complete and the scratch free for the next chunk
+    tc_fence_before();
+    named_sync(bar_id, kPrepThreads);
+    return true;
+}
+
+// Phase A for every chunk of every head in parallel, one chunk per CTA.
+constexpr int kPrepKThreads = kPrepThreads;
 constexpr uint32_t kPKScratch = 2 * kKQBlock;                       // after the KQ tiles
 constexpr uint32_t kPKBar = kPKScratch + kPrepScratch;
 constexpr uint32_t kPKSmem = kPKBar + 2 * 8 + 16 + 1024;
@@ -867,11 +968,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     uint64_t *bar = (uint64_t *)(base + kPKBar);                     // [0] loads, [1] Gram MMA
     uint32_t *tmem_slot = (uint32_t *)(bar + 2);
     volatile uint32_t *abort = tmem_slot + 1;
-    const int lt = threadIdx.x, warp = lt >> 5, lane = lt & 31;
+    const int lt = threadIdx.x, warp = lt >> 5;
     const int c = blockIdx.x % p.n_chunks, bh = blockIdx.x / p.n_chunks;
     const int b = bh / p.H, h = bh - b * p.H;
-    const int ct = p.ct, R = ct * p.nh;
-    const PrepScratch w = prep_scratch(base + kPKScratch);
 
     // rows TMA does not write (padding, queries beyond the chunk) stay zero
     for (uint32_t i = lt * 16; i < 2 * kKQBlock; i += kPrepKThreads * 16)
@@ -890,48 +989,90 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
-
-    if (lt == 0) {
-        mbar_arrive_expect_tx(&bar[0], 256u * R + 256u * ct);
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-            tma_load_5d(base + kb * kKQBlock, &tm_k, &bar[0], kb * 64, 0, h, c * ct, b);
-            tma_load_4d(base + kb * kKQBlock + kC * 128, &tm_q, &bar[0], kb * 64, h, c * ct, b);
-        }
-    }
-    if (warp == 0) scan_rows(load_rows(p, c, b, h, lane), lane, w.beta_s, w.L_s);
-    bool ok = true, issued = false;
-    if (lt == 0) {
-        ok = mbar_wait(&bar[0], 0, kWaitTries, abort);
-        if (ok) {
-            tc_fence_after();
-            issue_gram(tbase, smem_addr(base));
-            mma_commit(&bar[1]);
-            issued = true;
-            ok = mbar_wait(&bar[1], 0, kWaitTries, abort);
-        }
-        if (!ok) flag_error(p.status, abort, kDevTimeout);
-    }
-    if (!group_any(1, kPrepKThreads, !ok)) {
-        tc_fence_after();
-        uint8_t *rec = p.rec + rec_index(p, b, h, c) * kRecBytes;
-        phase_a(w, tbase, 0, rec + kRecT, lt, p.nh, ct, p.g != nullptr, 1);
-        float *rp = (float *)(rec + kRecP);
-        for (int i = lt; i < kNQ * kC; i += kPrepKThreads) rp[i] = w.Ps[(i >> 5) * kLd + (i & 31)];
-        if (lt < kC) {
-            ((float *)(rec + kRecBeta))[lt] = w.beta_s[lt];
-            ((float *)(rec + kRecL))[lt] = w.L_s[lt];
-        }
-    } else if (lt == 0) {
-        // loads or the MMA may still be in flight: let them finish (bounded)
-        // before shared memory and TMEM are released
-        uint32_t no_abort = 0;
-        mbar_wait(&bar[0], 0, kWaitTries, &no_abort);
-        if (issued) mbar_wait(&bar[1], 0, kWaitTries, &no_abort);
-    }
+    prep_chunk(p, &tm_k, &tm_q, base, prep_scratch(base + kPKScratch), bar, 0, abort, tbase, 0, lt, 1,
+               b, h, c);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, kPKTmemCols);
+}
+
+// ------------------------------------------------------------------ cooperative mode
+// One launch: CTAs 0 .. B*H-1 run the state pass (split mode), the others
+// prepare the chunks in chunk-major order, two chunks at a time per CTA
+// (warps 0-7 and 8-15), and publish each record through its flag. The
+// state pass waits for a record's flag (bounded) before loading it. All CTAs
+// are resident together (cooperative launch), and no prep CTA waits on a
+// state-pass CTA. Flags carry the launch generation + 1; the last CTA to
+// finish advances the generation, so flags of earlier launches never match.
+constexpr uint32_t kCoopScratch = (kPrepScratch + 127) & ~127u;
+
+__device__ void prep_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const Params &p, int pcta,
+                         int n_pcta)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    constexpr uint32_t kStg = 2 * kKQBlock;                          // 16 KB per group
+    uint8_t *scr = base + 2 * kStg;
+    uint64_t *bar = (uint64_t *)(scr + 2 * kCoopScratch);            // [group][loads, MMA]
+    uint32_t *tmem_slot = (uint32_t *)(bar + 4);
+    volatile uint32_t *abort = tmem_slot + 1;
+    const int warp = threadIdx.x >> 5;
+
+    for (uint32_t i = threadIdx.x * 16; i < 2 * kStg; i += kThreads * 16)
+        *(uint4 *)(base + i) = make_uint4(0, 0, 0, 0);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
+        *abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_q);
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, 64);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+    const uint32_t want = read_generation(p.sync) + 1;
+
+    if (warp < 16) {
+        const int gi = warp >> 3, lt = threadIdx.x - gi * kPrepThreads;
+        const int total = p.n_chunks * p.bh_count;
+        const PrepScratch w = prep_scratch(scr + gi * kCoopScratch);
+        uint32_t k = 0;
+        for (int idx = pcta * 2 + gi; idx < total; idx += n_pcta * 2, ++k) {
+            const int c = idx / p.bh_count, bh = idx - c * p.bh_count, b = bh / p.H, h = bh - b * p.H;
+            if (!prep_chunk(p, &tm_k, &tm_q, base + gi * kStg, w, bar + 2 * gi, k & 1, abort, tbase,
+                            gi * 32, lt, 1 + gi, b, h, c))
+                break;
+            if (lt == 0) {
+                __threadfence();
+                flag_publish(p.flags + rec_index(p, b, h, c), want);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, 64);
+}
+
+template <typename TOut>
+__global__ void __launch_bounds__(kThreads, 1)
+chunk_coop_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_q, const Params p)
+{
+    if ((int)blockIdx.x < p.bh_count)
+        state_pass_cta<TOut, true, true>(tm_k, tm_v, tm_q, p, blockIdx.x);
+    else
+        prep_cta(tm_k, tm_q, p, blockIdx.x - p.bh_count, gridDim.x - p.bh_count);
+    // every thread of this CTA is done (the role ended with a CTA barrier)
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(&p.sync[1], 1u) == gridDim.x - 1) {
+            atomicExch(&p.sync[1], 0u);
+            atomicAdd(&p.sync[0], 1u);
+        }
+    }
 }
 
 }  // namespace
@@ -946,11 +1087,62 @@ namespace {
 int chunk_tokens(int nh) { return (kC / nh < kNQ) ? kC / nh : kNQ; }
 }  // namespace
 
-size_t chunk_tc_records_bytes(const Problem &p)
+namespace {
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+size_t n_chunks_total(const Problem &p)
 {
     const int ct = chunk_tokens(p.nh);
-    const size_t n_chunks = p.T > 0 ? (size_t)(p.T + ct - 1) / ct : 0;
-    return (size_t)p.B * p.H * n_chunks * kRecBytes;
+    return p.T > 0 ? (size_t)p.B * p.H * ((size_t)(p.T + ct - 1) / ct) : 0;
+}
+}  // namespace
+
+// Records, then one flag per chunk, then the two cooperative-mode words.
+size_t chunk_tc_records_bytes(const Problem &p)
+{
+    const size_t n = n_chunks_total(p);
+    return n ? round256(n * kRecBytes) + round256(n * 4) + 256 : 0;
+}
+
+namespace {
+// Grid of the cooperative launch (state-pass CTAs + prep CTAs), or 0 when
+// this problem and device do not take it.
+cudaError_t coop_grid(const Problem &p, long long *grid)
+{
+    *grid = 0;
+    const size_t n_total = n_chunks_total(p);
+    if (n_total == 0 || p.scratch_bytes < chunk_tc_records_bytes(p)) return cudaSuccess;
+    int dev = 0, sms = 0, coop = 0, per_sm = 0;
+    auto kernel = p.out_dtype == DP_F32 ? chunk_coop_kernel<float> : chunk_coop_kernel<__nv_bfloat16>;
+    const uint32_t smem = smem_bytes<true>();
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess ||
+        (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem)) != cudaSuccess)
+        return e;
+    const long long bh = (long long)p.B * p.H, slots = (long long)sms * per_sm;
+    if (coop && per_sm >= 1 && 2 * bh <= slots) {
+        const long long want_prep = ((long long)n_total + 1) / 2;
+        *grid = bh + (slots - bh < want_prep ? slots - bh : want_prep);
+    }
+    return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t chunk_tc_path(const Problem &p, int *path)
+{
+    long long grid = 0;
+    const cudaError_t e = coop_grid(p, &grid);
+    if (e != cudaSuccess) return e;
+    const size_t n_total = n_chunks_total(p);
+    if (grid > 0)
+        *path = DP_PATH_CHUNK_COOP;
+    else if (n_total > 0 && p.scratch_bytes >= round256(n_total * kRecBytes))
+        *path = DP_PATH_CHUNK_SPLIT;
+    else
+        *path = DP_PATH_CHUNK_FUSED;
+    return cudaSuccess;
 }
 
 cudaError_t launch_chunk_tc(const Problem &p)
@@ -975,16 +1167,34 @@ cudaError_t launch_chunk_tc(const Problem &p)
     pr.h_final = p.h_final;
     pr.status = p.status;
     pr.rec = (uint8_t *)p.scratch;
+    pr.flags = nullptr;
+    pr.sync = nullptr;
+    pr.bh_count = p.B * p.H;
     pr.T = p.T;
     pr.H = p.H;
     pr.nh = nh;
     pr.ct = ct;
     pr.n_chunks = (p.T + ct - 1) / ct;
 
-    // split whenever the workspace holds every chunk's record
-    const size_t rec_bytes = chunk_tc_records_bytes(p);
-    const bool split = p.scratch != nullptr && rec_bytes > 0 && p.scratch_bytes >= rec_bytes;
+    // split whenever the workspace holds every chunk's record; cooperative
+    // (one launch) when it also holds the flags and the heads leave at least
+    // as many SMs for the prep CTAs as the state pass takes
+    const size_t n_total = n_chunks_total(p);
+    const size_t rec_bytes = round256(n_total * kRecBytes);
+    const bool split = p.scratch != nullptr && n_total > 0 && p.scratch_bytes >= rec_bytes;
     cudaError_t e;
+    long long grid = 0;
+    if (split && (e = coop_grid(p, &grid)) != cudaSuccess) return e;
+    if (grid > 0) {
+        auto kernel = p.out_dtype == DP_F32 ? chunk_coop_kernel<float> : chunk_coop_kernel<__nv_bfloat16>;
+        pr.flags = (uint32_t *)((uint8_t *)p.scratch + rec_bytes);
+        pr.sync = (uint32_t *)((uint8_t *)pr.flags + round256(n_total * 4));
+        void *args[] = {(void *)&tk, (void *)&tv, (void *)&tq, (void *)&pr};
+        e = cudaLaunchCooperativeKernel((const void *)kernel, dim3((unsigned)grid), dim3(kThreads), args,
+                                        smem_bytes<true>(), p.stream);
+        if (e == cudaSuccess) return cudaSuccess;
+        cudaGetLastError();   // not launchable together here: two launches instead
+    }
     if (split) {
         e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kPKSmem);

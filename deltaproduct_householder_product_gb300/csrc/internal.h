@@ -35,6 +35,9 @@ bool chunk_tc_supported(const Problem &p);
 // let launch_chunk_tc split into a parallel prep kernel and the state-pass
 // kernel; with less scratch it runs the fused single kernel.
 size_t chunk_tc_records_bytes(const Problem &p);
+// Which way launch_chunk_tc runs this problem with p.scratch_bytes of scratch
+// (a dp_path value).
+cudaError_t chunk_tc_path(const Problem &p, int *path);
 cudaError_t launch_chunk_tc(const Problem &p);
 
 cudaError_t launch_state_io(int op, int B, int H, int Dk, int Dv, float *state,

@@ -87,14 +87,31 @@ const char *dp_status_string(dp_status s);
 dp_status dp_forward_workspace_size(const dp_dims *dims, size_t *bytes);
 
 /* Bytes of device workspace with which dp_forward runs its fastest path
- * (>= dp_forward_workspace_size). For the tensor-core chunk path this adds
- * one 18688-byte record per (batch, head, chunk) of ceil(T / ct) chunks,
- * ct = min(16, 32 / n_h) tokens: a first kernel then prepares every chunk's
- * UT transform in parallel and the state-pass kernel streams the records in.
- * With a workspace of at least dp_forward_workspace_size but less than
- * this, dp_forward runs one fused kernel instead: slower, bit-identical
- * results. Both sizes are equal for the recurrent path. */
+ * (>= dp_forward_workspace_size). For the tensor-core chunk path this adds,
+ * per (batch, head, chunk) of ceil(T / ct) chunks, ct = min(16, 32 / n_h)
+ * tokens, an 18688-byte record and a 4-byte flag, plus 256 bytes: every
+ * chunk's UT transform is then prepared in parallel (by the other CTAs of
+ * one cooperative launch when B*H leaves at least half the SMs free, else by
+ * a first kernel) and the state pass streams the records in. With at least
+ * dp_forward_workspace_size bytes but less than this, dp_forward runs one
+ * fused kernel instead: slower, bit-identical results. Both sizes are equal
+ * for the recurrent path. Like the status word, the flags must start at
+ * zero: zero the workspace once after allocating it; calls sharing a
+ * workspace must be ordered (one stream). */
 dp_status dp_forward_workspace_size_fast(const dp_dims *dims, size_t *bytes);
+
+/* How dp_forward runs a problem given `workspace_bytes` of workspace
+ * (library facility, no counterpart in the paper): the kernel family and,
+ * for the chunk path, its mode, which fixes the number of kernels one call
+ * enqueues (1, or 2 for DP_PATH_CHUNK_SPLIT). Queries the current device;
+ * enqueues nothing. */
+typedef enum {
+    DP_PATH_RECURRENT = 0,    /* token-by-token SIMT kernel */
+    DP_PATH_CHUNK_FUSED = 1,  /* one tensor-core kernel, prep inside */
+    DP_PATH_CHUNK_SPLIT = 2,  /* prep kernel, then the state-pass kernel */
+    DP_PATH_CHUNK_COOP = 3    /* one cooperative launch: prep CTAs beside the state pass */
+} dp_path;
+dp_status dp_forward_path(const dp_dims *dims, size_t workspace_bytes, int *path);
 
 /* Whole-sequence forward (the extended T*n_h sequence of the paper's Sec.5.1,
  * processed in chunks by the tensor-core kernel):

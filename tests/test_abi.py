@@ -90,3 +90,16 @@ def test_decode_and_state_io_reject(L):
     assert L.dp_state_io(0, 1, 1, 128, 128, None, None, 0, 0, None) == 1
     assert L.dp_state_io(0, 0, 1, 128, 128, None, None, 0, 0, None) == 0   # empty: no-op
     assert L.dp_check_status(None, None) == 1
+
+
+def test_forward_path_validation(L):
+    """dp_forward_path validates like dp_forward: NULL output, bad dims and a
+    workspace below the minimum are rejected; a valid query names a path."""
+    dims = _lib.make_dims(1, 16, 2, 64, 64, 2, _lib.DP_BF16, "recurrent")
+    code = ctypes.c_int(-1)
+    assert L.dp_forward_path(ctypes.byref(dims), 256, None) == 1
+    assert L.dp_forward_path(ctypes.byref(dims), 255, ctypes.byref(code)) == 4
+    bad = _lib.make_dims(1, 16, 2, 48, 64, 2, _lib.DP_BF16, "recurrent")
+    assert L.dp_forward_path(ctypes.byref(bad), 256, ctypes.byref(code)) == 2
+    assert L.dp_forward_path(ctypes.byref(dims), 256, ctypes.byref(code)) == 0
+    assert _lib.PATHS[code.value] == "recurrent"

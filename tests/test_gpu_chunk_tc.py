@@ -32,12 +32,26 @@ def run(dp, x, impl="chunk_tc", h0=True, out_dtype=torch.float32, path="split"):
     ``path`` "split" hands dp_forward the fast workspace (parallel prep kernel +
     state-pass kernel), "fused" only the minimum (one fused kernel)."""
     xc = cuda(x)
-    size = dp.workspace_size(*_dims(x), impl=impl, fast=(path == "split"))
+    size = workspace_for(dp, x, impl, path)
     ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
     o, hf = dp.forward(xc["q"], xc["k"], xc["v"], xc["beta"], xc["g"],
                        xc["h0"] if h0 else None, impl=impl, workspace=ws, out_dtype=out_dtype)
     dp.check_status(ws)
     return o, hf
+
+
+def workspace_for(dp, x, impl, path):
+    """Workspace bytes selecting a path: "split" the fast size (one cooperative
+    launch when the heads leave room, else prep + state-pass kernels),
+    "split2" records only (always the two launches), "fused" the minimum."""
+    if path == "split":
+        return dp.workspace_size(*_dims(x), impl=impl, fast=True)
+    lo = dp.workspace_size(*_dims(x), impl=impl)
+    if path == "fused":
+        return lo
+    B, T, H, nh, _ = x["k"].shape
+    ct = min(16, 32 // nh)
+    return lo + ((B * H * (-(-T // ct)) * 18688 + 255) // 256) * 256
 
 
 def _dims(x):
@@ -84,14 +98,43 @@ def test_workspace_sizes(dp):
                                           (W.LONG, 2, 17, False)],
                          ids=lambda v: getattr(v, "name", str(v)))
 def test_split_equals_fused_bitwise(dp, base, nh, T, h0):
-    """Both ways of running the chunk path share every arithmetic step (the
-    prep kernel runs the fused kernel's phase A and hands its bytes over
-    unchanged), so outputs and final states agree bit for bit."""
+    """Every way of running the chunk path shares every arithmetic step (the
+    prep CTAs or kernel run the fused kernel's phase A and hand its bytes
+    over unchanged), so outputs and final states agree bit for bit."""
     x = W.make_inputs(base.scaled(B=2, H=3, T=T, nh=nh))
-    o_s, h_s = run(dp, x, h0=h0, path="split")
     o_f, h_f = run(dp, x, h0=h0, path="fused")
-    assert torch.equal(o_s, o_f)
-    assert torch.equal(h_s, h_f)
+    for path in ("split", "split2"):
+        o_s, h_s = run(dp, x, h0=h0, path=path)
+        assert torch.equal(o_s, o_f), path
+        assert torch.equal(h_s, h_f), path
+
+
+def test_forward_path_names_the_launch(dp):
+    """dp_forward_path reports the mode each workspace size selects (a few
+    heads leave room for the cooperative launch on a GB300)."""
+    x = W.make_inputs(W.BASE.scaled(B=2, H=3, T=100))
+    dims = (2, 100, 3, 128, 128, 2)
+    for path, name in (("split", "chunk_coop"), ("split2", "chunk_split"), ("fused", "chunk_fused")):
+        assert dp.forward_path(*dims, workspace_for(dp, x, "chunk_tc", path)) == name
+    assert dp.forward_path(*dims, 256, impl="recurrent") == "recurrent"
+
+
+def test_workspace_reuse_across_calls(dp):
+    """The cooperative path keeps its record flags in the workspace; calls that
+    reuse one workspace (different inputs, a shorter sequence, then the first
+    inputs again) must each see only their own records."""
+    xa = W.make_inputs(W.GATED.scaled(B=2, H=3, T=160, nh=2))
+    xb = W.make_inputs(W.BASE.scaled(B=2, H=3, T=160, nh=2, seed=11))
+    xc_ = W.make_inputs(W.BASE.scaled(B=2, H=3, T=70, nh=2, seed=12))
+    ws = torch.zeros(workspace_for(dp, xa, "chunk_tc", "split"), dtype=torch.uint8, device="cuda")
+    for x in (xa, xb, xc_, xa):
+        g = cuda(x)
+        o, hf = dp.forward(g["q"], g["k"], g["v"], g["beta"], g["g"], g["h0"], impl="chunk_tc",
+                           workspace=ws, out_dtype=torch.float32)
+        dp.check_status(ws)
+        o_f, h_f = run(dp, x, path="fused")
+        assert torch.equal(o, o_f)
+        assert torch.equal(hf, h_f)
 
 
 @pytest.mark.parametrize("base", [W.BASE, W.GATED, W.NEARDUP], ids=lambda w: w.name)
