@@ -51,6 +51,7 @@ def parse():
     ap.add_argument("--kernel", default="auto", choices=["auto", "recurrent", "chunk_tc"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
     ap.add_argument("--fused", action="store_true",
                     help="give dp_forward only the minimum workspace: the chunk path then "
                          "runs as one fused kernel instead of prep + state-pass kernels")
@@ -233,6 +234,66 @@ def reference_arm(args, w):
     print(json.dumps(line), flush=True)
 
 
+def decode_measure(dev, hbm_peak, n_steps=256, reps=5):
+    """The decode step (one token on a carried fp32 state, in place) on the
+    long workload's heads: B1 H16 n_h 3 D128 bf16. Per-step device time with
+    one dp_decode_step call per step, and with n_steps calls captured once in
+    a CUDA graph and replayed (no host work between steps). Roofline: the
+    step must read and write every state once (2 x 64 KiB per (b,h)) plus
+    its inputs and o."""
+    import ctypes
+    from deltaproduct_householder_product_gb300 import _lib
+    w = W.LONG
+    d = {k: (None if v is None else v.to(dev)) for k, v in W.make_decode_inputs(w, n_steps).items()}
+    state = torch.zeros(w.B, w.H, w.Dk, w.Dv, dtype=torch.float32, device=dev)
+    o = torch.empty(n_steps, w.B, w.H, w.Dv, dtype=torch.float32, device=dev)
+    dims = _lib.make_dims(w.B, 1, w.H, w.Dk, w.Dv, w.nh, w.torch_dtype, "auto", torch.float32)
+    L = _lib.lib()
+
+    def run(stream):
+        s = ctypes.c_void_p(stream.cuda_stream)
+        for i in range(n_steps):
+            rc = L.dp_decode_step(ctypes.byref(dims), _lib._ptr(d["q"][i]), _lib._ptr(d["k"][i]),
+                                  _lib._ptr(d["v"][i]), _lib._ptr(d["beta"][i]), None, _lib._ptr(state),
+                                  _lib._ptr(o[i]), s)
+            if rc != 0:
+                raise RuntimeError(f"dp_decode_step returned {rc}")
+
+    stream = torch.cuda.current_stream()
+    run(stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us_launch = 1e3 * e0.elapsed_time(e1) / n_steps
+    us_graph = None
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            run(torch.cuda.current_stream())
+        graph.replay()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us_graph = 1e3 * e0.elapsed_time(e1) / (reps * n_steps)
+    except Exception as exc:   # capture not possible here: report the launched figure only
+        print(f"decode graph capture failed: {exc}", file=sys.stderr)
+    per_head = (w.Dk + w.nh * (w.Dk + w.Dv + 1)) * 2 + w.Dv * 4 + 2 * w.Dk * w.Dv * 4
+    step_bytes = w.B * w.H * per_head
+    best = us_graph if us_graph is not None else us_launch
+    achieved = step_bytes / (best * 1e-6) / 1e9
+    return {"workload": "b1h16-nh3-d128-bf16 decode (fp32 state, fp32 o)", "steps": n_steps,
+            "us_per_step_launched": us_launch, "us_per_step_graph": us_graph,
+            "steps_per_s": 1e6 / best,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "algorithmic_bytes": step_bytes}}
+
+
 def ours_arm(args, w):
     import deltaproduct_householder_product_gb300 as dp
     from deltaproduct_householder_product_gb300 import _lib
@@ -346,6 +407,8 @@ def ours_arm(args, w):
                      "scope": "one forward: every launch dp_forward enqueues"},
         "clocks": clocks,
     }
+    if not args.no_decode:
+        line["decode"] = decode_measure(dev, hbm_peak)
     if not args.no_cpu_baseline:
         v, desc, cores, _ = oracle_sample(w, x, 8.0, os.cpu_count() or 1)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores,
