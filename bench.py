@@ -29,6 +29,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 from deltaproduct_householder_product_gb300 import workloads as W  # noqa: E402
@@ -52,6 +53,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
+    ap.add_argument("--no-varlen", action="store_true", help="skip the packed variable-length measurement")
     ap.add_argument("--fused", action="store_true",
                     help="give dp_forward only the minimum workspace: the chunk path then "
                          "runs as one fused kernel instead of prep + state-pass kernels")
@@ -294,6 +296,49 @@ def decode_measure(dev, hbm_peak, n_steps=256, reps=5):
                          "frac": achieved / hbm_peak, "algorithmic_bytes": step_bytes}}
 
 
+VARLEN_LENGTHS = [384, 2944, 1024, 512, 1792, 256, 896, 384]   # 8 sequences, 8192 tokens
+
+
+def varlen_measure(dp, dev, hbm_peak, steps=20, warmup=3):
+    """Packed variable-length sequences (dp_forward_varlen) with the bench
+    workload's heads and token count (H8 n_h 2 D128 bf16, fp32 o): the eight
+    lengths above, drawn with the bench workload's recipe. Whole-call
+    tokens/s from CUDA events (inputs resident; one workspace reused)."""
+    from deltaproduct_householder_product_gb300 import _lib
+    T, N = sum(VARLEN_LENGTHS), len(VARLEN_LENGTHS)
+    w = W.BASE.scaled(B=1, T=T)
+    x = {k: (None if v is None else v[0].to(dev).contiguous()) for k, v in W.make_inputs(w).items()
+         if k in ("q", "k", "v", "beta")}
+    cu = torch.tensor([0] + list(np.cumsum(VARLEN_LENGTHS)), dtype=torch.int32, device=dev)
+    max_len = max(VARLEN_LENGTHS)
+    dims = _lib.make_dims(N, T, w.H, w.Dk, w.Dv, w.nh, w.torch_dtype, "auto", torch.float32, max_len)
+    ws = torch.zeros(_lib.workspace_size(dims, fast=True), dtype=torch.uint8, device=dev)
+    o = torch.empty(T, w.H, w.Dv, dtype=torch.float32, device=dev)
+    hf = torch.empty(N, w.H, w.Dk, w.Dv, dtype=torch.float32, device=dev)
+
+    def call():
+        dp.forward_varlen(x["q"], x["k"], x["v"], x["beta"], None, None, cu_seqlens=cu, max_seqlen=max_len,
+                          out=o, h_final=hf, workspace=ws)
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dp.check_status(ws)
+    ms = e0.elapsed_time(e1) / steps
+    wbytes = W.algorithmic_bytes(w, out_bytes=4) - w.B * w.H * w.Dk * w.Dv * 4 + N * w.H * w.Dk * w.Dv * 4
+    achieved = wbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"H{w.H} n_h {w.nh} D{w.Dk} bf16, {N} packed sequences of lengths {VARLEN_LENGTHS}",
+            "path": _lib.forward_path(dims, ws.numel()), "ms_per_call": ms, "tokens_per_s": T / (ms * 1e-3),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "algorithmic_bytes": wbytes}}
+
+
 def ours_arm(args, w):
     import deltaproduct_householder_product_gb300 as dp
     from deltaproduct_householder_product_gb300 import _lib
@@ -409,6 +454,8 @@ def ours_arm(args, w):
     }
     if not args.no_decode:
         line["decode"] = decode_measure(dev, hbm_peak)
+    if not args.no_varlen:
+        line["varlen"] = varlen_measure(dp, dev, hbm_peak)
     if not args.no_cpu_baseline:
         v, desc, cores, _ = oracle_sample(w, x, 8.0, os.cpu_count() or 1)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores,

@@ -11,7 +11,7 @@ import torch
 from . import _lib
 from ._lib import DPError, STATE_EXPORT, STATE_IMPORT, STATE_ZERO  # noqa: F401
 
-__all__ = ["forward", "forward_noalloc", "forward_path", "supports", "decode_step", "state_io", "check_status",
+__all__ = ["forward", "forward_varlen", "forward_noalloc", "forward_path", "supports", "decode_step", "state_io", "check_status",
            "workspace_size",
            "DPError", "abi_version"]
 
@@ -90,6 +90,56 @@ def forward(q, k, v, beta, g=None, h0=None, *, impl="auto", out=None, h_final=Tr
         _lib._ptr(h0), _lib._ptr(out), _lib._ptr(h_final), _lib._ptr(workspace),
         workspace.numel() * workspace.element_size(), _lib._stream(stream))
     _lib._check(rc, "dp_forward")
+    return out, h_final
+
+
+def forward_varlen(q, k, v, beta, g=None, h0=None, *, cu_seqlens, max_seqlen=None, impl="auto", out=None,
+                   h_final=True, workspace=None, stream=None, out_dtype=None):
+    """Run the recurrence over N variable-length sequences packed along T.
+
+    q [T,H,Dk], k [T,H,nh,Dk], v [T,H,nh,Dv], beta [T,H,nh], g [T,H] or None;
+    cu_seqlens int32 CUDA tensor [N+1] of token offsets (0, ..., T); h0
+    [N,H,Dk,Dv] float32 or None. ``max_seqlen`` bounds the longest sequence
+    (read from cu_seqlens when None, which synchronises). Returns (o [T,H,Dv],
+    h_final [N,H,Dk,Dv] or None). Every sequence starts from its own h0.
+    """
+    T, H, nh, Dk = k.shape
+    Dv = v.shape[-1]
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g)):
+        _lib._need_cuda(name, t, dt)
+    _lib._need_cuda("cu_seqlens", cu_seqlens, torch.int32)
+    N = cu_seqlens.numel() - 1
+    if N < 0:
+        raise ValueError("cu_seqlens needs at least one entry")
+    _lib._need_cuda("h0", h0, torch.float32)
+    if q.shape != (T, H, Dk) or v.shape != (T, H, nh, Dv) or beta.shape != (T, H, nh):
+        raise ValueError("inconsistent shapes for q, k, v, beta")
+    if g is not None and g.shape != (T, H):
+        raise ValueError("g must be [T,H]")
+    if h0 is not None and h0.shape != (N, H, Dk, Dv):
+        raise ValueError("h0 must be [N,H,Dk,Dv]")
+    if max_seqlen is None:
+        max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if N > 0 else 0
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else dt
+    dims = _lib.make_dims(N, T, H, Dk, Dv, nh, dt, impl, out_dtype, max_seqlen)
+    if out is None:
+        out = torch.empty((T, H, Dv), dtype=out_dtype, device=q.device)
+    _lib._need_cuda("out", out, out_dtype)
+    if h_final is True:
+        h_final = torch.empty((N, H, Dk, Dv), dtype=torch.float32, device=q.device)
+    elif h_final is False:
+        h_final = None
+    _lib._need_cuda("h_final", h_final, torch.float32)
+    if workspace is None:
+        workspace = torch.zeros(_lib.workspace_size(dims, fast=True), dtype=torch.uint8, device=q.device)
+    _lib._need_cuda("workspace", workspace)
+    rc = _lib.lib().dp_forward_varlen(
+        dims, _lib._ptr(cu_seqlens), _lib._ptr(q), _lib._ptr(k), _lib._ptr(v), _lib._ptr(beta), _lib._ptr(g),
+        _lib._ptr(h0), _lib._ptr(out), _lib._ptr(h_final), _lib._ptr(workspace),
+        workspace.numel() * workspace.element_size(), _lib._stream(stream))
+    _lib._check(rc, "dp_forward_varlen")
     return out, h_final
 
 

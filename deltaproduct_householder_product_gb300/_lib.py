@@ -29,7 +29,8 @@ class DPError(RuntimeError):
 class Dims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
                 ("Dk", ctypes.c_int), ("Dv", ctypes.c_int), ("nh", ctypes.c_int),
-                ("dtype", ctypes.c_int), ("impl", ctypes.c_int), ("out_dtype", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("impl", ctypes.c_int), ("out_dtype", ctypes.c_int),
+                ("max_seqlen", ctypes.c_int)]
 
 
 _LIB = None
@@ -51,12 +52,13 @@ def lib():
         L.dp_forward_workspace_size_fast.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(ctypes.c_size_t)]
         L.dp_forward_path.argtypes = [ctypes.POINTER(Dims), ctypes.c_size_t, ctypes.POINTER(ctypes.c_int)]
         L.dp_forward.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 9 + [ctypes.c_size_t, _vp]
+        L.dp_forward_varlen.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 10 + [ctypes.c_size_t, _vp]
         L.dp_decode_step.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 7 + [_vp]
         L.dp_state_io.argtypes = [ctypes.c_int] * 5 + [_vp, _vp, ctypes.c_int, ctypes.c_int, _vp]
         L.dp_check_status.argtypes = [_vp, _vp]
         L.dp_forward_noalloc.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 9
         for name in ("dp_forward_workspace_size", "dp_forward_workspace_size_fast", "dp_forward_path",
-                     "dp_forward", "dp_decode_step",
+                     "dp_forward", "dp_forward_varlen", "dp_decode_step",
                      "dp_state_io", "dp_check_status", "dp_forward_noalloc"):
             getattr(L, name).restype = ctypes.c_int
         _LIB = L
@@ -103,13 +105,14 @@ def _need_cuda(name, t, dtype=None):
         raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
 
 
-def make_dims(B, T, H, Dk, Dv, nh, dtype, impl="auto", out_dtype=None):
+def make_dims(B, T, H, Dk, Dv, nh, dtype, impl="auto", out_dtype=None, max_seqlen=0):
     dt = dtype if isinstance(dtype, int) else _dtype_code(dtype)
     if out_dtype is None:
         od = dt
     else:
         od = out_dtype if isinstance(out_dtype, int) else _dtype_code(out_dtype)
-    return Dims(B, T, H, Dk, Dv, nh, dt, IMPLS[impl] if isinstance(impl, str) else int(impl), od)
+    return Dims(B, T, H, Dk, Dv, nh, dt, IMPLS[impl] if isinstance(impl, str) else int(impl), od,
+                max_seqlen)
 
 
 PATHS = {0: "recurrent", 1: "chunk_fused", 2: "chunk_split", 3: "chunk_coop"}

@@ -26,6 +26,7 @@ dp_status check_dims(const dp_dims *d, bool decode)
 {
     if (!d) return DP_ERR_INVALID_ARG;
     if (d->B < 0 || d->H < 0 || (!decode && d->T < 0)) return DP_ERR_INVALID_ARG;
+    if (d->max_seqlen < 0 || (!decode && d->max_seqlen > d->T)) return DP_ERR_INVALID_ARG;
     if (d->dtype != DP_F32 && d->dtype != DP_BF16) return DP_ERR_INVALID_ARG;
     if (d->impl < DP_IMPL_AUTO || d->impl > DP_IMPL_CHUNK_TC) return DP_ERR_INVALID_ARG;
     if (d->out_dtype != d->dtype && d->out_dtype != DP_F32) return DP_ERR_INVALID_ARG;
@@ -59,6 +60,7 @@ dp::Problem make_problem(const dp_dims *d, int T)
     p.B = d->B; p.T = T; p.H = d->H; p.Dk = d->Dk; p.Dv = d->Dv; p.nh = d->nh;
     p.dtype = d->dtype;
     p.out_dtype = d->out_dtype;
+    p.max_T = d->max_seqlen > 0 ? d->max_seqlen : T;
     return p;
 }
 
@@ -142,13 +144,16 @@ dp_status dp_forward_path(const dp_dims *dims, size_t workspace_bytes, int *path
     return from_cuda(dp::chunk_tc_path(p, path));
 }
 
-dp_status dp_forward(const dp_dims *dims, const void *q, const void *k, const void *v,
-                     const void *beta, const void *g, const float *h0, void *o,
-                     float *h_final, void *workspace, size_t workspace_bytes,
-                     dp_stream_t stream)
+}  // extern "C"
+
+namespace {
+dp_status forward_impl(const dp_dims *dims, const int *cu, const void *q, const void *k, const void *v,
+                       const void *beta, const void *g, const float *h0, void *o, float *h_final,
+                       void *workspace, size_t workspace_bytes, dp_stream_t stream)
 {
     DP_TRY(check_dims(dims, false));
     dp::Problem p = make_problem(dims, dims->T);
+    p.cu = cu;
     p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g; p.h0 = h0; p.o = o;
     p.h_final = h_final;
     p.stream = (cudaStream_t)stream;
@@ -168,6 +173,31 @@ dp_status dp_forward(const dp_dims *dims, const void *q, const void *k, const vo
 
     if ((size_t)p.B * p.H == 0) return DP_OK;
     return from_cuda(tc ? dp::launch_chunk_tc(p) : dp::launch_recurrent(p));
+}
+}  // namespace
+
+extern "C" {
+
+dp_status dp_forward(const dp_dims *dims, const void *q, const void *k, const void *v,
+                     const void *beta, const void *g, const float *h0, void *o,
+                     float *h_final, void *workspace, size_t workspace_bytes,
+                     dp_stream_t stream)
+{
+    if (dims && dims->max_seqlen != 0) return DP_ERR_INVALID_ARG;   // dense calls: every sequence is T long
+    return forward_impl(dims, nullptr, q, k, v, beta, g, h0, o, h_final, workspace, workspace_bytes, stream);
+}
+
+dp_status dp_forward_varlen(const dp_dims *dims, const int *cu_seqlens, const void *q, const void *k,
+                            const void *v, const void *beta, const void *g, const float *h0, void *o,
+                            float *h_final, void *workspace, size_t workspace_bytes, dp_stream_t stream)
+{
+    DP_TRY(check_dims(dims, false));
+    if ((size_t)dims->B * dims->H == 0) return DP_OK;
+    if (dims->T > 0 && dims->max_seqlen < 1) return DP_ERR_INVALID_ARG;
+    DP_TRY(check_ptr(cu_seqlens, 4));
+    // the packed layouts are the dense ones with one batch row of T tokens
+    dp_dims flat = *dims;
+    return forward_impl(&flat, cu_seqlens, q, k, v, beta, g, h0, o, h_final, workspace, workspace_bytes, stream);
 }
 
 dp_status dp_decode_step(const dp_dims *dims, const void *q, const void *k, const void *v,

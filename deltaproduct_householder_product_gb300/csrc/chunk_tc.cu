@@ -157,8 +157,56 @@ struct Params {
     uint8_t *rec;              // per-chunk records (split mode), [B*H][n_chunks][kRecBytes]
     uint32_t *flags;           // cooperative mode: record published, [B*H][n_chunks]
     uint32_t *sync;            // cooperative mode: [0] launch generation, [1] CTAs finished
-    int T, H, nh, ct, n_chunks, bh_count;
+    int T, H, nh, ct;
+    int n_chunks;              // chunks of the longest sequence: records per (sequence, head)
+    int bh_count;
+    const int *cu;             // packed sequences: token offsets [B+1] (NULL: dense [B,T] layout)
+    int B;
+    int max_T;                 // longest sequence (T for dense calls)
 };
+
+// The (sequence, head) pair one state-pass CTA, or one prep step, works on.
+// Dense calls (kPacked = false): sequence b is batch row b, T tokens, and
+// every extent comes straight from the kernel parameters. Packed calls: the
+// extent is read from cu (and checked) once.
+template <bool kPacked>
+struct Job {
+    int b, h;          // sequence and head
+    int b_map, t0;     // packed: token t sits at row (b_map * T + t0 + t) of the token layouts
+    int len, nc;       // packed: its tokens and chunks
+    bool valid;        // packed: false when the offsets broke their contract for this sequence
+    __device__ __forceinline__ int row_b() const { return kPacked ? b_map : b; }
+    __device__ __forceinline__ int first() const { return kPacked ? t0 : 0; }
+    __device__ __forceinline__ int tokens(const Params &p) const { return kPacked ? len : p.T; }
+    __device__ __forceinline__ int chunks(const Params &p) const { return kPacked ? nc : p.n_chunks; }
+    __device__ __forceinline__ bool ok() const { return kPacked ? valid : true; }
+};
+
+template <bool kPacked>
+__device__ __forceinline__ Job<kPacked> make_job(const Params &p, int bh)
+{
+    Job<kPacked> j;
+    j.b = bh / p.H;
+    j.h = bh - j.b * p.H;
+    j.b_map = j.t0 = j.len = j.nc = 0;
+    j.valid = true;
+    if (kPacked) {
+        const SeqRange r = seq_range(p.cu, j.b, p.B, p.T, p.max_T);
+        j.b_map = r.b_map;
+        j.t0 = r.t0;
+        j.len = r.len;
+        j.valid = r.ok;
+        j.nc = (r.len + p.ct - 1) / p.ct;
+    }
+    return j;
+}
+
+// (token, head) index of token t of the job: rows of q, g, o (x n_h for k, v, beta)
+template <bool kPacked>
+__device__ __forceinline__ size_t tok_row(const Params &p, const Job<kPacked> &j, int t)
+{
+    return ((size_t)j.row_b() * p.T + j.first() + t) * p.H + j.h;
+}
 
 // Cooperative mode: a record is published by storing generation + 1 into
 // its flag (release); the state pass acquires it before loading the record.
@@ -181,9 +229,10 @@ __device__ __forceinline__ uint32_t read_generation(const uint32_t *sync)
     return v;
 }
 
-__device__ __forceinline__ size_t rec_index(const Params &p, int b, int h, int c)
+template <bool kPacked>
+__device__ __forceinline__ size_t rec_index(const Params &p, const Job<kPacked> &j, int c)
 {
-    return ((size_t)b * p.H + h) * (size_t)p.n_chunks + c;
+    return ((size_t)j.b * p.H + j.h) * (size_t)p.n_chunks + c;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
@@ -296,10 +345,11 @@ __device__ __forceinline__ void issue_gram(uint32_t d_tmem, uint32_t kq)
 // ------------------------------------------------------------------ TMA producer
 constexpr uint32_t kFlagTries = 1u << 24;   // x >= 64 ns each: seconds, then a timeout
 
-template <bool kSplit, bool kCoop>
+template <bool kSplit, bool kCoop, bool kPacked>
 __device__ void tma_role(const Smem &s, const Params &p, const CUtensorMap *tk,
-                         const CUtensorMap *tv, const CUtensorMap *tq, int b, int h)
+                         const CUtensorMap *tv, const CUtensorMap *tq, const Job<kPacked> &jb)
 {
+    const int h = jb.h;
     const int ct = p.ct, R = ct * p.nh;
     const uint32_t want = kCoop ? read_generation(p.sync) + 1 : 0;
     const bool gated = p.g != nullptr;
@@ -309,13 +359,13 @@ __device__ void tma_role(const Smem &s, const Params &p, const CUtensorMap *tk,
     const uint32_t bytes = 512u * R + 256u * ct + (kSplit ? rec_t + rec_tail : 0u);
     int last_use[kNS];
     for (int i = 0; i < kNS; ++i) last_use[i] = -1;
-    for (int c = 0; c < p.n_chunks; ++c) {
+    for (int c = 0; c < jb.chunks(p); ++c) {
         const int st = c % kNS, u = c / kNS;
         if (u >= 1 && !wait_bar(s, kBarEmpty + st, (u - 1) & 1, p.status)) break;
         if (kCoop) {
             // the prep CTAs of this launch publish the chunk's record: acquire
             // it, then order the bulk copy (async proxy) after that read
-            const uint32_t *flag = p.flags + rec_index(p, b, h, c);
+            const uint32_t *flag = p.flags + rec_index(p, jb, c);
             uint32_t tries = 0;
             while (flag_read(flag) != want && ++tries < kFlagTries && !*s.abort) __nanosleep(64);
             if (tries >= kFlagTries || *s.abort) {
@@ -327,7 +377,7 @@ __device__ void tma_role(const Smem &s, const Params &p, const CUtensorMap *tk,
         uint8_t *kq = s.stage(st), *vv = kq + 2 * kKQBlock;
         uint64_t *bar = &s.bar[kBarFull + st];
         mbar_arrive_expect_tx(bar, bytes);
-        const int t0 = c * ct;
+        const int t0 = jb.first() + c * ct, b = jb.row_b();
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
             tma_load_5d(kq + kb * kKQBlock, tk, bar, kb * 64, 0, h, t0, b);
@@ -335,7 +385,7 @@ __device__ void tma_role(const Smem &s, const Params &p, const CUtensorMap *tk,
             tma_load_5d(vv + kb * kVBlock, tv, bar, kb * 64, 0, h, t0, b);
         }
         if (kSplit) {
-            const uint8_t *rec = p.rec + rec_index(p, b, h, c) * kRecBytes;
+            const uint8_t *rec = p.rec + rec_index(p, jb, c) * kRecBytes;
             uint8_t *dst = kq + kStageIn;
             bulk_load(dst + kRecT, rec + kRecT, rec_t, bar);
             bulk_load(dst + kRecP, rec + kRecP, rec_tail, bar);
@@ -354,10 +404,9 @@ __device__ void tma_role(const Smem &s, const Params &p, const CUtensorMap *tk,
 // pass and are issued by their own thread so that their issue latency
 // overlaps the state pass's.
 template <bool kSplit>
-__device__ void prep_mma_role(const Smem &s, const Params &p, uint32_t tbase)
+__device__ void prep_mma_role(const Smem &s, const Params &p, uint32_t tbase, int n)
 {
     const bool gated = p.g != nullptr;
-    const int n = p.n_chunks;
     const uint32_t id_uw = idesc_bf16(128, kC, true, false);
 
     // T enters as hi + lo bf16 tiles (in the group's tiles, or in the stage's record)
@@ -408,7 +457,7 @@ __device__ void prep_mma_role(const Smem &s, const Params &p, uint32_t tbase)
                 issue_uw(c - 1);
             }
         }
-        if (ok && uw_ready(n - 1)) issue_uw(n - 1);
+        if (ok && n > 0 && uw_ready(n - 1)) issue_uw(n - 1);   // an empty sequence has no chunk
     }
     mma_commit(&s.bar[kBarFinal + 1]);
     uint32_t no_abort = 0;
@@ -419,10 +468,9 @@ __device__ void prep_mma_role(const Smem &s, const Params &p, uint32_t tbase)
 //   [U'^T | O_b] += S^T [-W; Gamma q]^T          (16 instructions, N = 48)
 //   [S^T | O_a] or [O_a | S^T] += U'^T [K^T; P]   (4 instructions, N = 144)
 // Consecutive MMAs run in issue order, so S -> U' -> S needs no round trip.
-__device__ void chain_role(const Smem &s, const Params &p, uint32_t tbase)
+__device__ void chain_role(const Smem &s, const Params &p, uint32_t tbase, int n)
 {
     const bool gated = p.g != nullptr;
-    const int n = p.n_chunks;
     const uint32_t id_x = idesc_tf32(128, kXRows);
     const uint32_t id_y = idesc_tf32(128, kYRows);
     bool ok = wait_bar(s, kBarInit, 0, p.status);
@@ -458,13 +506,14 @@ struct RowVals {
     float beta, lg;
 };
 
-__device__ __forceinline__ RowVals load_rows(const Params &p, int c, int b, int h, int lane)
+template <bool kPacked>
+__device__ __forceinline__ RowVals load_rows(const Params &p, const Job<kPacked> &jb, int c, int lane)
 {
     RowVals v{0.f, 0.f};
-    if (c >= p.n_chunks) return v;
+    if (c >= jb.chunks(p)) return v;
     const int nh = p.nh, R = p.ct * nh, tl = lane / nh, j = lane - tl * nh, t = c * p.ct + tl;
-    if (lane < R && t < p.T) {
-        const size_t tok = ((size_t)b * p.T + t) * p.H + h;
+    if (lane < R && t < jb.tokens(p)) {   // rows past the sequence's end: beta = 0, exact no-ops
+        const size_t tok = tok_row(p, jb, t);
         v.beta = __bfloat162float(p.beta[tok * nh + j]);
         if (p.g != nullptr && j == 0) v.lg = fmaxf(logf(__bfloat162float(p.g[tok])), -80.f);
     }
@@ -682,8 +731,8 @@ __device__ bool phase_b(const Smem &s, const Params &p, uint32_t tbase, uint8_t 
 }
 
 // Prep group g of the state-pass kernel: chunks g, g + 2, ...
-template <bool kSplit>
-__device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g, int b, int h)
+template <bool kSplit, bool kPacked>
+__device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g, const Job<kPacked> &jb)
 {
     const int lt = threadIdx.x - (kPrepWarp + 8 * g) * 32, lw = lt >> 5, lane = lt & 31;
     const uint32_t bar_id = 1 + g;
@@ -691,7 +740,7 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
     const bool gated = p.g != nullptr;
 
     if (kSplit) {
-        for (int c = g; c < p.n_chunks; c += 2) {
+        for (int c = g; c < jb.chunks(p); c += 2) {
             const int st = c % kNS;
             const uint8_t *kq = s.stage(st), *rec = kq + kStageIn;
             const bool ok = (lt != 0) || wait_bar(s, kBarFull + st, (c / kNS) & 1, p.status);
@@ -709,13 +758,13 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
 
     const PrepScratch w = prep_scratch(s.scratch(g));
     RowVals rv{0.f, 0.f};
-    if (lw == 0) rv = load_rows(p, g, b, h, lane);
-    for (int c = g; c < p.n_chunks; c += 2) {
+    if (lw == 0) rv = load_rows(p, jb, g, lane);
+    for (int c = g; c < jb.chunks(p); c += 2) {
         const int st = c % kNS;
         const uint8_t *kq = s.stage(st);
         if (lw == 0) {
             scan_rows(rv, lane, w.beta_s, w.L_s);
-            rv = load_rows(p, c + 2, b, h, lane);        // next chunk of this group
+            rv = load_rows(p, jb, c + 2, lane);          // next chunk of this group
         }
         // one thread polls the mbarriers; the group barrier spreads the outcome
         bool ok = true;
@@ -738,15 +787,17 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
 }
 
 // ------------------------------------------------------------------ epilogue
-template <typename TOut>
-__device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, int b, int h)
+template <typename TOut, bool kPacked>
+__device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, const Job<kPacked> &jb)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t bar_id = 3;
     const uint32_t trow = tbase + ((uint32_t)(warp * 32) << 16);
-    const size_t bh = (size_t)b * p.H + h;
+    const size_t bh = (size_t)jb.b * p.H + jb.h;
     const bool gated = p.g != nullptr;
-    TOut *o = (TOut *)p.o;
+    // o row of the sequence's first token, this thread's value column
+    TOut *const o_seq = (TOut *)p.o + tok_row(p, jb, 0) * kD + tid;
+    const size_t tok_stride = (size_t)p.H * kD;
 
     {   // S^T <- h0^T (lane = dv, column = dk), or zeros; readout accumulators zero
         uint32_t r[32];
@@ -770,13 +821,13 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, int b, 
     if (tid == 0) mbar_arrive(&s.bar[kBarInit]);
 
     bool failed = false;
-    for (int c = 0; c < p.n_chunks; ++c) {
+    for (int c = 0; c < jb.chunks(p); ++c) {
         const int g = c & 1, t0 = c * p.ct;
         if (gated) {
             // Gamma_C: product of the chunk's token gates (log domain, clamped)
             float lg = 0.f;
-            if (lane < p.ct && t0 + lane < p.T)
-                lg = fmaxf(logf(__bfloat162float(p.g[((size_t)b * p.T + t0 + lane) * p.H + h])), -80.f);
+            if (lane < p.ct && t0 + lane < jb.tokens(p))
+                lg = fmaxf(logf(__bfloat162float(p.g[tok_row(p, jb, t0 + lane)])), -80.f);
 #pragma unroll
             for (int d = 16; d > 0; d >>= 1) lg += __shfl_xor_sync(0xffffffffu, lg, d);
             const float gC = __expf(lg);
@@ -803,12 +854,11 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, int b, 
         tmem_ld16(trow + col_oa(g), ra);
         tmem_ld16(trow + col_ob(g), rb);
         tmem_wait_ld();
+        TOut *oc = o_seq + (size_t)t0 * tok_stride;
 #pragma unroll
         for (int i = 0; i < kNQ; ++i) {
-            const int t = t0 + i;
-            if (i < p.ct && t < p.T)
-                store_out(o, (((size_t)b * p.T + t) * p.H + h) * kD + tid,
-                          __uint_as_float(ra[i]) + __uint_as_float(rb[i]));
+            if (i < p.ct && t0 + i < jb.tokens(p))
+                store_out(oc, (size_t)i * tok_stride, __uint_as_float(ra[i]) + __uint_as_float(rb[i]));
             ra[i] = 0u;
         }
         tmem_st16(trow + col_oa(g), ra);   // both parts accumulate: clear them for chunk c + 2
@@ -818,7 +868,7 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, int b, 
         named_sync(bar_id, 128);
         if (tid == 0) mbar_arrive(&s.bar[kBarOFree + g]);
     }
-    if (!failed && p.h_final) {
+    if (!failed && jb.ok() && p.h_final) {
         uint32_t r[32];
         for (int c0 = 0; c0 < kD; c0 += 32) {
             tmem_ld32(trow + kColS + c0, r);
@@ -830,7 +880,7 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, int b, 
 }
 
 // ------------------------------------------------------------------ state-pass kernel
-template <typename TOut, bool kSplit, bool kCoop>
+template <typename TOut, bool kSplit, bool kCoop, bool kPacked>
 __device__ __forceinline__ void state_pass_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                                const CUtensorMap &tm_q, const Params &p, int bh)
 {
@@ -846,7 +896,9 @@ __device__ __forceinline__ void state_pass_cta(const CUtensorMap &tm_k, const CU
     s.group_bytes = Lay::kGroup;
     s.scratch_off = Lay::kOffScratch;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int b = bh / p.H, h = bh - b * p.H;
+    // a sequence with bad packed offsets runs no chunk
+    const Job<kPacked> jb = make_job<kPacked>(p, bh);
+    if (kPacked && threadIdx.x == 0 && !jb.ok()) report_bad_sequence(p.status);
 
     // Zero every tile once: rows TMA never writes (padding rows, query rows
     // beyond the chunk's tokens) must hold finite zeros.
@@ -870,27 +922,27 @@ __device__ __forceinline__ void state_pass_cta(const CUtensorMap &tm_k, const CU
     const uint32_t tbase = *s.tmem_slot;
 
     if (warp < kPrepWarp) {
-        epi_role<TOut>(s, p, tbase, b, h);
+        epi_role<TOut, kPacked>(s, p, tbase, jb);
     } else if (warp < kTmaWarp) {
-        prep_role<kSplit>(s, p, tbase, (warp - kPrepWarp) >> 3, b, h);
+        prep_role<kSplit, kPacked>(s, p, tbase, (warp - kPrepWarp) >> 3, jb);
     } else if (warp == kTmaWarp) {
-        if (lane == 0) tma_role<kSplit, kCoop>(s, p, &tm_k, &tm_v, &tm_q, b, h);
+        if (lane == 0) tma_role<kSplit, kCoop, kPacked>(s, p, &tm_k, &tm_v, &tm_q, jb);
     } else if (warp == kChainWarp) {
-        if (lane == 0) chain_role(s, p, tbase);
+        if (lane == 0) chain_role(s, p, tbase, jb.chunks(p));
     } else {
-        if (lane == 0) prep_mma_role<kSplit>(s, p, tbase);
+        if (lane == 0) prep_mma_role<kSplit>(s, p, tbase, jb.chunks(p));
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
-template <typename TOut, bool kSplit>
+template <typename TOut, bool kSplit, bool kPacked>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 const __grid_constant__ CUtensorMap tm_q, const Params p)
 {
-    state_pass_cta<TOut, kSplit, false>(tm_k, tm_v, tm_q, p, blockIdx.x);
+    state_pass_cta<TOut, kSplit, false, kPacked>(tm_k, tm_v, tm_q, p, blockIdx.x);
 }
 
 // ------------------------------------------------------------------ prep kernel
@@ -901,21 +953,23 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 // chunk's record, then P, beta and L. `bars` = [loads, Gram MMA], used at
 // phase `parity`. Returns false, uniformly over the group, after a timeout
 // (the group's loads and MMA drained first).
+template <bool kPacked>
 __device__ bool prep_chunk(const Params &p, const CUtensorMap *tk, const CUtensorMap *tq,
                            uint8_t *stage, const PrepScratch &w, uint64_t *bars, uint32_t parity,
                            volatile uint32_t *abort, uint32_t tbase, uint32_t gq_col, int lt,
-                           uint32_t bar_id, int b, int h, int c)
+                           uint32_t bar_id, const Job<kPacked> &jb, int c)
 {
     const int lane = lt & 31, ct = p.ct, R = ct * p.nh;
     if (lt == 0) {
         mbar_arrive_expect_tx(&bars[0], 256u * R + 256u * ct);
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
-            tma_load_5d(stage + kb * kKQBlock, tk, &bars[0], kb * 64, 0, h, c * ct, b);
-            tma_load_4d(stage + kb * kKQBlock + kC * 128, tq, &bars[0], kb * 64, h, c * ct, b);
+            const int t0 = jb.first() + c * ct;
+            tma_load_5d(stage + kb * kKQBlock, tk, &bars[0], kb * 64, 0, jb.h, t0, jb.row_b());
+            tma_load_4d(stage + kb * kKQBlock + kC * 128, tq, &bars[0], kb * 64, jb.h, t0, jb.row_b());
         }
     }
-    if (lt < 32) scan_rows(load_rows(p, c, b, h, lane), lane, w.beta_s, w.L_s);
+    if (lt < 32) scan_rows(load_rows(p, jb, c, lane), lane, w.beta_s, w.L_s);
     bool ok = true;
     if (lt == 0) {
         bool issued = false;
@@ -938,7 +992,7 @@ __device__ bool prep_chunk(const Params &p, const CUtensorMap *tk, const CUtenso
     }
     if (group_any(bar_id, kPrepThreads, !ok || *abort)) return false;
     tc_fence_after();
-    uint8_t *rec = p.rec + rec_index(p, b, h, c) * kRecBytes;
+    uint8_t *rec = p.rec + rec_index(p, jb, c) * kRecBytes;
     phase_a(w, tbase, gq_col, rec + kRecT, lt, p.nh, ct, p.g != nullptr, bar_id);
     float *rp = (float *)(rec + kRecP);
     for (int i = lt; i < kNQ * kC; i += kPrepThreads) rp[i] = w.Ps[(i >> 5) * kLd + (i & 31)];
@@ -959,6 +1013,7 @@ constexpr uint32_t kPKBar = kPKScratch + kPrepScratch;
 constexpr uint32_t kPKSmem = kPKBar + 2 * 8 + 16 + 1024;
 constexpr uint32_t kPKTmemCols = 32;
 
+template <bool kPacked>
 __global__ void __launch_bounds__(kPrepKThreads, 4)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                   const Params p)
@@ -969,8 +1024,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     uint32_t *tmem_slot = (uint32_t *)(bar + 2);
     volatile uint32_t *abort = tmem_slot + 1;
     const int lt = threadIdx.x, warp = lt >> 5;
-    const int c = blockIdx.x % p.n_chunks, bh = blockIdx.x / p.n_chunks;
-    const int b = bh / p.H, h = bh - b * p.H;
+    const int c = blockIdx.x % p.n_chunks;
+    const Job<kPacked> jb = make_job<kPacked>(p, blockIdx.x / p.n_chunks);
+    if (c >= jb.chunks(p)) return;   // past the sequence's end (packed calls), or a bad sequence
 
     // rows TMA does not write (padding, queries beyond the chunk) stay zero
     for (uint32_t i = lt * 16; i < 2 * kKQBlock; i += kPrepKThreads * 16)
@@ -989,8 +1045,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
-    prep_chunk(p, &tm_k, &tm_q, base, prep_scratch(base + kPKScratch), bar, 0, abort, tbase, 0, lt, 1,
-               b, h, c);
+    prep_chunk(p, &tm_k, &tm_q, base, prep_scratch(base + kPKScratch), bar, 0, abort, tbase, 0, lt, 1, jb, c);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, kPKTmemCols);
@@ -1006,6 +1061,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 // finish advances the generation, so flags of earlier launches never match.
 constexpr uint32_t kCoopScratch = (kPrepScratch + 127) & ~127u;
 
+template <bool kPacked>
 __device__ void prep_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const Params &p, int pcta,
                          int n_pcta)
 {
@@ -1039,15 +1095,18 @@ __device__ void prep_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const
         const int gi = warp >> 3, lt = threadIdx.x - gi * kPrepThreads;
         const int total = p.n_chunks * p.bh_count;
         const PrepScratch w = prep_scratch(scr + gi * kCoopScratch);
-        uint32_t k = 0;
-        for (int idx = pcta * 2 + gi; idx < total; idx += n_pcta * 2, ++k) {
-            const int c = idx / p.bh_count, bh = idx - c * p.bh_count, b = bh / p.H, h = bh - b * p.H;
+        uint32_t k = 0;   // chunks prepared by this group: the phase of its barriers
+        for (int idx = pcta * 2 + gi; idx < total; idx += n_pcta * 2) {
+            const int c = idx / p.bh_count;
+            const Job<kPacked> jb = make_job<kPacked>(p, idx - c * p.bh_count);
+            if (c >= jb.chunks(p)) continue;   // past the sequence's end (packed calls): nobody waits for it
             if (!prep_chunk(p, &tm_k, &tm_q, base + gi * kStg, w, bar + 2 * gi, k & 1, abort, tbase,
-                            gi * 32, lt, 1 + gi, b, h, c))
+                            gi * 32, lt, 1 + gi, jb, c))
                 break;
+            ++k;
             if (lt == 0) {
                 __threadfence();
-                flag_publish(p.flags + rec_index(p, b, h, c), want);
+                flag_publish(p.flags + rec_index(p, jb, c), want);
             }
         }
     }
@@ -1056,15 +1115,15 @@ __device__ void prep_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const
     if (warp == 0) tmem_dealloc(tbase, 64);
 }
 
-template <typename TOut>
+template <typename TOut, bool kPacked>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_coop_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_q, const Params p)
 {
     if ((int)blockIdx.x < p.bh_count)
-        state_pass_cta<TOut, true, true>(tm_k, tm_v, tm_q, p, blockIdx.x);
+        state_pass_cta<TOut, true, true, kPacked>(tm_k, tm_v, tm_q, p, blockIdx.x);
     else
-        prep_cta(tm_k, tm_q, p, blockIdx.x - p.bh_count, gridDim.x - p.bh_count);
+        prep_cta<kPacked>(tm_k, tm_q, p, blockIdx.x - p.bh_count, gridDim.x - p.bh_count);
     // every thread of this CTA is done (the role ended with a CTA barrier)
     if (threadIdx.x == 0) {
         __threadfence();
@@ -1089,11 +1148,13 @@ int chunk_tokens(int nh) { return (kC / nh < kNQ) ? kC / nh : kNQ; }
 
 namespace {
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
-size_t n_chunks_total(const Problem &p)
+// Records are laid out for the longest sequence: ceil(max_T / ct) per (sequence, head).
+size_t chunks_per_seq(const Problem &p)
 {
     const int ct = chunk_tokens(p.nh);
-    return p.T > 0 ? (size_t)p.B * p.H * ((size_t)(p.T + ct - 1) / ct) : 0;
+    return p.T > 0 ? (size_t)(p.max_T + ct - 1) / ct : 0;
 }
+size_t n_chunks_total(const Problem &p) { return (size_t)p.B * p.H * chunks_per_seq(p); }
 }  // namespace
 
 // Records, then one flag per chunk, then the two cooperative-mode words.
@@ -1112,7 +1173,9 @@ cudaError_t coop_grid(const Problem &p, long long *grid)
     const size_t n_total = n_chunks_total(p);
     if (n_total == 0 || p.scratch_bytes < chunk_tc_records_bytes(p)) return cudaSuccess;
     int dev = 0, sms = 0, coop = 0, per_sm = 0;
-    auto kernel = p.out_dtype == DP_F32 ? chunk_coop_kernel<float> : chunk_coop_kernel<__nv_bfloat16>;
+    const bool f32 = p.out_dtype == DP_F32, packed = p.cu != nullptr;
+    auto kernel = f32 ? (packed ? chunk_coop_kernel<float, true> : chunk_coop_kernel<float, false>)
+                      : (packed ? chunk_coop_kernel<__nv_bfloat16, true> : chunk_coop_kernel<__nv_bfloat16, false>);
     const uint32_t smem = smem_bytes<true>();
     cudaError_t e;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
@@ -1148,7 +1211,8 @@ cudaError_t chunk_tc_path(const Problem &p, int *path)
 cudaError_t launch_chunk_tc(const Problem &p)
 {
     const int nh = p.nh, ct = chunk_tokens(nh);
-    const cuuint64_t B = p.B, T = p.T, H = p.H;
+    // packed calls: one batch row of T tokens, sequences found through cu
+    const cuuint64_t B = p.cu ? 1 : p.B, T = p.T, H = p.H;
     CUtensorMap tk, tv, tq;
     const cuuint64_t dk[5] = {kD, (cuuint64_t)nh, H, T, B};
     const cuuint64_t sk[4] = {kD * 2, (cuuint64_t)nh * kD * 2, H * nh * kD * 2, T * H * nh * kD * 2};
@@ -1170,11 +1234,14 @@ cudaError_t launch_chunk_tc(const Problem &p)
     pr.flags = nullptr;
     pr.sync = nullptr;
     pr.bh_count = p.B * p.H;
+    pr.cu = p.cu;
+    pr.B = p.B;
     pr.T = p.T;
     pr.H = p.H;
     pr.nh = nh;
     pr.ct = ct;
-    pr.n_chunks = (p.T + ct - 1) / ct;
+    pr.max_T = p.max_T;
+    pr.n_chunks = (int)chunks_per_seq(p);
 
     // split whenever the workspace holds every chunk's record; cooperative
     // (one launch) when it also holds the flags and the heads leave at least
@@ -1186,7 +1253,10 @@ cudaError_t launch_chunk_tc(const Problem &p)
     long long grid = 0;
     if (split && (e = coop_grid(p, &grid)) != cudaSuccess) return e;
     if (grid > 0) {
-        auto kernel = p.out_dtype == DP_F32 ? chunk_coop_kernel<float> : chunk_coop_kernel<__nv_bfloat16>;
+        const bool packed = p.cu != nullptr;
+        auto kernel = p.out_dtype == DP_F32
+                          ? (packed ? chunk_coop_kernel<float, true> : chunk_coop_kernel<float, false>)
+                          : (packed ? chunk_coop_kernel<__nv_bfloat16, true> : chunk_coop_kernel<__nv_bfloat16, false>);
         pr.flags = (uint32_t *)((uint8_t *)p.scratch + rec_bytes);
         pr.sync = (uint32_t *)((uint8_t *)pr.flags + round256(n_total * 4));
         void *args[] = {(void *)&tk, (void *)&tv, (void *)&tq, (void *)&pr};
@@ -1195,18 +1265,23 @@ cudaError_t launch_chunk_tc(const Problem &p)
         if (e == cudaSuccess) return cudaSuccess;
         cudaGetLastError();   // not launchable together here: two launches instead
     }
+    const bool packed = p.cu != nullptr;
     if (split) {
-        e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kPKSmem);
+        auto prep = packed ? chunk_prep_kernel<true> : chunk_prep_kernel<false>;
+        e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPKSmem);
         if (e != cudaSuccess) return e;
         const size_t n_ctas = (size_t)p.B * p.H * pr.n_chunks;
         if (n_ctas > 0x7fffffffu) return cudaErrorInvalidValue;
-        chunk_prep_kernel<<<(unsigned)n_ctas, kPrepKThreads, kPKSmem, p.stream>>>(tk, tq, pr);
+        prep<<<(unsigned)n_ctas, kPrepKThreads, kPKSmem, p.stream>>>(tk, tq, pr);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     auto kernel = p.out_dtype == DP_F32
-                      ? (split ? chunk_tc_kernel<float, true> : chunk_tc_kernel<float, false>)
-                      : (split ? chunk_tc_kernel<__nv_bfloat16, true> : chunk_tc_kernel<__nv_bfloat16, false>);
+                      ? (split ? (packed ? chunk_tc_kernel<float, true, true> : chunk_tc_kernel<float, true, false>)
+                               : (packed ? chunk_tc_kernel<float, false, true> : chunk_tc_kernel<float, false, false>))
+                      : (split ? (packed ? chunk_tc_kernel<__nv_bfloat16, true, true>
+                                         : chunk_tc_kernel<__nv_bfloat16, true, false>)
+                               : (packed ? chunk_tc_kernel<__nv_bfloat16, false, true>
+                                         : chunk_tc_kernel<__nv_bfloat16, false, false>));
     const uint32_t smem = split ? smem_bytes<true>() : smem_bytes<false>();
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

@@ -20,6 +20,8 @@ struct Problem {
     void *o;
     float *h_final;
     uint32_t *status;          // device status word (may be NULL for decode)
+    const int *cu;             // packed sequences: int32 [B+1] token offsets (NULL: dense [B,T] layout)
+    int max_T;                 // longest sequence (T for dense calls)
     void *scratch;             // workspace bytes after the status block
     size_t scratch_bytes;
     cudaStream_t stream;
@@ -46,5 +48,30 @@ cudaError_t launch_state_io(int op, int B, int H, int Dk, int Dv, float *state,
 
 // Device status codes written into the status word (first one wins).
 enum : uint32_t { kDevOk = 0, kDevTimeout = 1, kDevBadState = 2 };
+
+// The token range of sequence b: token t (0 <= t < len) sits at row
+// (b_map * T + t0 + t) of the [.., T, H, ..] layouts. Dense calls: b_map =
+// b, t0 = 0, len = T. Packed calls: b_map = 0, t0 = cu[b], len = cu[b+1] -
+// cu[b], after checking cu[b] <= cu[b+1] <= T, len <= max_len, cu[0] = 0
+// and cu[N] = T; a sequence that fails the check gets ok = false and len = 0
+// (nothing of it is read or written).
+struct SeqRange {
+    int b_map, t0, len;
+    bool ok;
+};
+
+__device__ __forceinline__ SeqRange seq_range(const int *cu, int b, int N, int T, int max_len)
+{
+    if (!cu) return {b, 0, T, true};
+    const int a = cu[b], e = cu[b + 1];
+    const bool ok = 0 <= a && a <= e && e <= T && e - a <= max_len && (b > 0 || a == 0) &&
+                    (b < N - 1 || e == T);
+    return ok ? SeqRange{0, a, e - a, true} : SeqRange{0, 0, 0, false};
+}
+
+__device__ __forceinline__ void report_bad_sequence(uint32_t *status)
+{
+    if (status) atomicCAS(status, 0u, kDevBadState);
+}
 
 }  // namespace dp

@@ -8,6 +8,9 @@
 // tensor-core kernel does not take), dp_decode_step (T = 1 with the state
 // updated in place), and the state import/export of dp_state_io.
 //
+// Packed variable-length calls (cu != NULL): CTA row b is sequence b, whose
+// tokens are found through seq_range.
+//
 // Work split: one CTA owns a 32-column slice of one (batch, head) state and
 // keeps it in registers for the whole sequence: 4 warps x 32 lanes, lane =
 // value column, warp w = a contiguous block of D_k/4 key rows. A matvec
@@ -28,7 +31,7 @@ __device__ __forceinline__ void from_f(__nv_bfloat16 *p, float x) { *p = __float
 
 template <int DK, typename TIn, typename TOut>
 __global__ void __launch_bounds__(kWarps * 32)
-recurrent_kernel(int T, int H, int Dv, int nh,
+recurrent_kernel(int T, int H, int Dv, int nh, const int *cu, int N, int max_T, uint32_t *status,
                  const TIn *__restrict__ q, const TIn *__restrict__ k,
                  const TIn *__restrict__ v, const TIn *__restrict__ beta,
                  const TIn *__restrict__ g, const float *h0, TOut *__restrict__ o,
@@ -44,6 +47,11 @@ recurrent_kernel(int T, int H, int Dv, int nh,
     const int col = blockIdx.y * kCols + lane;
     const int row0 = w * R;
     const size_t state_base = (size_t)bh * DK * Dv;
+    const SeqRange sq = seq_range(cu, b, N, T, max_T);
+    if (!sq.ok) {   // nothing of this sequence is touched
+        if (threadIdx.x == 0 && blockIdx.y == 0) report_bad_sequence(status);
+        return;
+    }
 
     float S[R];
 #pragma unroll
@@ -51,8 +59,8 @@ recurrent_kernel(int T, int H, int Dv, int nh,
         S[r] = h0 ? h0[state_base + (size_t)(row0 + r) * Dv + col] : 0.f;
 
     int buf = 0;   // alternating buffers: one barrier per matvec
-    for (int t = 0; t < T; ++t) {
-        const size_t tok = ((size_t)b * T + t) * H + h;
+    for (int t = 0; t < sq.len; ++t) {
+        const size_t tok = ((size_t)sq.b_map * T + sq.t0 + t) * H + h;
         if (g) {
             const float gt = to_f(g[tok]);
 #pragma unroll
@@ -99,13 +107,16 @@ cudaError_t launch_typed(const Problem &p)
     TOut *o = (TOut *)p.o;
     switch (p.Dk) {
     case 32:
-        recurrent_kernel<32, TIn, TOut><<<grid, block, 0, p.stream>>>(p.T, p.H, p.Dv, p.nh, q, k, v, be, g, p.h0, o, p.h_final);
+        recurrent_kernel<32, TIn, TOut><<<grid, block, 0, p.stream>>>(
+            p.T, p.H, p.Dv, p.nh, p.cu, p.B, p.max_T, p.status, q, k, v, be, g, p.h0, o, p.h_final);
         break;
     case 64:
-        recurrent_kernel<64, TIn, TOut><<<grid, block, 0, p.stream>>>(p.T, p.H, p.Dv, p.nh, q, k, v, be, g, p.h0, o, p.h_final);
+        recurrent_kernel<64, TIn, TOut><<<grid, block, 0, p.stream>>>(
+            p.T, p.H, p.Dv, p.nh, p.cu, p.B, p.max_T, p.status, q, k, v, be, g, p.h0, o, p.h_final);
         break;
     default:
-        recurrent_kernel<128, TIn, TOut><<<grid, block, 0, p.stream>>>(p.T, p.H, p.Dv, p.nh, q, k, v, be, g, p.h0, o, p.h_final);
+        recurrent_kernel<128, TIn, TOut><<<grid, block, 0, p.stream>>>(
+            p.T, p.H, p.Dv, p.nh, p.cu, p.B, p.max_T, p.status, q, k, v, be, g, p.h0, o, p.h_final);
         break;
     }
     return cudaGetLastError();

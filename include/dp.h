@@ -73,10 +73,12 @@ typedef struct {
     int dtype;       /* dp_dtype of q, k, v, beta, g */
     int impl;        /* dp_impl */
     int out_dtype;   /* dp_dtype of o: equal to dtype, or DP_F32 with bf16 inputs */
+    int max_seqlen;  /* dp_forward_varlen: the longest packed sequence (bounds the
+                        workspace); 0 for every other call */
 } dp_dims;
 
 /* ABI version of this header (bumped on any signature change). */
-#define DP_ABI_VERSION 3
+#define DP_ABI_VERSION 4
 int dp_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -125,6 +127,28 @@ dp_status dp_forward(const dp_dims *dims,
                      const float *h0, void *o, float *h_final,
                      void *workspace, size_t workspace_bytes,
                      dp_stream_t stream);
+
+/* Variable-length sequences packed back to back (a library facility for
+ * training batches; the paper's Sec.4 recurrence runs on each sequence
+ * independently: every sequence starts from its own initial state and no
+ * state crosses a boundary, as with a gate of 0 at each sequence start).
+ * dims->B = N sequences, dims->T = total tokens, dims->max_seqlen >= the
+ * longest sequence (sizes the workspace, see dp_forward_workspace_size*).
+ * cu_seqlens: int32 [N+1] in device memory, 0 = cu[0] <= cu[1] <= ... <=
+ * cu[N] = T; sequence s holds tokens cu[s] .. cu[s+1]-1.
+ * Layouts drop the batch axis: q [T,H,D_k], k [T,H,n_h,D_k],
+ * v [T,H,n_h,D_v], beta [T,H,n_h], g [T,H] or NULL, o [T,H,D_v];
+ * h0 / h_final [N,H,D_k,D_v] fp32 (NULL as in dp_forward).
+ * The host cannot read cu_seqlens: each CTA checks its sequence's bounds
+ * before touching any token and, if they break the rules above or exceed
+ * max_seqlen, records DP_ERR_DEVICE (dp_check_status) and computes nothing
+ * for that sequence. */
+dp_status dp_forward_varlen(const dp_dims *dims, const int *cu_seqlens,
+                            const void *q, const void *k, const void *v,
+                            const void *beta, const void *g,
+                            const float *h0, void *o, float *h_final,
+                            void *workspace, size_t workspace_bytes,
+                            dp_stream_t stream);
 
 /* One decode step (dims->T is ignored and taken as 1) on a carried state,
  * updated in place. Shapes drop the T axis: q [B,H,D_k], k [B,H,n_h,D_k],

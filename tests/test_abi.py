@@ -103,3 +103,18 @@ def test_forward_path_validation(L):
     assert L.dp_forward_path(ctypes.byref(bad), 256, ctypes.byref(code)) == 2
     assert L.dp_forward_path(ctypes.byref(dims), 256, ctypes.byref(code)) == 0
     assert _lib.PATHS[code.value] == "recurrent"
+
+
+def test_varlen_validation(L):
+    """dp_forward rejects a nonzero max_seqlen; dp_forward_varlen rejects a
+    missing or host cu_seqlens and a max_seqlen beyond T, before any launch."""
+    import ctypes as C
+    dims = _lib.make_dims(2, 16, 2, 64, 64, 2, _lib.DP_BF16, "recurrent", max_seqlen=8)
+    null = None
+    args = [null] * 9 + [C.c_size_t(0), null]
+    assert L.dp_forward(C.byref(dims), *args) == 1
+    host_cu = (C.c_int * 3)(0, 8, 16)
+    vargs = [C.cast(host_cu, C.c_void_p)] + [null] * 9 + [C.c_size_t(0), null]
+    assert L.dp_forward_varlen(C.byref(dims), *vargs) == 1
+    bad = _lib.make_dims(2, 16, 2, 64, 64, 2, _lib.DP_BF16, "recurrent", max_seqlen=17)
+    assert L.dp_forward_varlen(C.byref(bad), *vargs) == 1
