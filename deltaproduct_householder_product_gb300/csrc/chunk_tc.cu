@@ -274,9 +274,9 @@ enum : int {
     kBarUW = kBarTb + 2,          // [2] U and W MMAs done
     kBarReady = kBarUW + 2,       // [2] state-pass B tiles written
     kBarM2 = kBarReady + 2,       // [2] chunk's state pass and readout done
-    kBarOFree = kBarM2 + 2,       // [2] O buffers drained by the epilogue
+    kBarOFree = kBarM2 + 2,       // [2] O buffers drained by the epilogue (one arrival per warp)
     kBarM1 = kBarOFree + 2,       // first half (U', S^T q) done (gated)
-    kBarScaled,                   // S scaled by Gamma_C (gated)
+    kBarScaled,                   // S scaled by Gamma_C (gated; one arrival per epilogue warp)
     kBarInit,                     // initial state in TMEM
     kBarFinal,                    // [2] every MMA of an issuer retired (teardown)
     kBarCount = kBarFinal + 2
@@ -318,6 +318,15 @@ __device__ __forceinline__ bool group_any(uint32_t id, uint32_t count, bool v)
         : "r"((uint32_t)v), "r"(id), "r"(count)
         : "memory");
     return r != 0;
+}
+
+// Lane 0 waits (bounded); the warp agrees on the outcome, which is false
+// when the wait expired or another role aborted.
+__device__ __forceinline__ bool warp_wait(const Smem &s, int idx, uint32_t parity, uint32_t *status)
+{
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = wait_bar(s, idx, parity, status) && !*s.abort;
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
 __device__ __forceinline__ void split_pack(float a, float b, uint32_t &hi, uint32_t &lo)
@@ -820,6 +829,10 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, const J
     named_sync(bar_id, 128);
     if (tid == 0) mbar_arrive(&s.bar[kBarInit]);
 
+    // Each warp owns 32 TMEM lanes (value columns) and runs on its own: it
+    // waits for the chain's commits itself and arrives once per warp on the
+    // barriers the chain waits for, and it releases a chunk's O buffers
+    // before storing the outputs from registers.
     bool failed = false;
     for (int c = 0; c < jb.chunks(p); ++c) {
         const int g = c & 1, t0 = c * p.ct;
@@ -831,8 +844,7 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, const J
 #pragma unroll
             for (int d = 16; d > 0; d >>= 1) lg += __shfl_xor_sync(0xffffffffu, lg, d);
             const float gC = __expf(lg);
-            const bool ok = (tid != 0) || wait_bar(s, kBarM1, c & 1, p.status);
-            if (group_any(bar_id, 128, !ok || *s.abort)) { failed = true; break; }
+            if (!warp_wait(s, kBarM1, c & 1, p.status)) { failed = true; break; }
             tc_fence_after();
             uint32_t r[32];
             for (int c0 = 0; c0 < kD; c0 += 32) {
@@ -844,29 +856,30 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, const J
             }
             tmem_wait_st();
             tc_fence_before();
-            named_sync(bar_id, 128);
-            if (tid == 0) mbar_arrive(&s.bar[kBarScaled]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.bar[kBarScaled]);
         }
-        const bool ok = (tid != 0) || wait_bar(s, kBarM2 + g, (c >> 1) & 1, p.status);
-        if (group_any(bar_id, 128, !ok || *s.abort)) { failed = true; break; }
+        if (!warp_wait(s, kBarM2 + g, (c >> 1) & 1, p.status)) { failed = true; break; }
         tc_fence_after();
         uint32_t ra[16], rb[16];
         tmem_ld16(trow + col_oa(g), ra);
         tmem_ld16(trow + col_ob(g), rb);
         tmem_wait_ld();
-        TOut *oc = o_seq + (size_t)t0 * tok_stride;
 #pragma unroll
         for (int i = 0; i < kNQ; ++i) {
-            if (i < p.ct && t0 + i < jb.tokens(p))
-                store_out(oc, (size_t)i * tok_stride, __uint_as_float(ra[i]) + __uint_as_float(rb[i]));
-            ra[i] = 0u;
+            ra[i] = __float_as_uint(__uint_as_float(ra[i]) + __uint_as_float(rb[i]));
+            rb[i] = 0u;
         }
-        tmem_st16(trow + col_oa(g), ra);   // both parts accumulate: clear them for chunk c + 2
-        tmem_st16(trow + col_ob(g), ra);
+        tmem_st16(trow + col_oa(g), rb);   // both parts accumulate: clear them for chunk c + 2
+        tmem_st16(trow + col_ob(g), rb);
         tmem_wait_st();
         tc_fence_before();
-        named_sync(bar_id, 128);
-        if (tid == 0) mbar_arrive(&s.bar[kBarOFree + g]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.bar[kBarOFree + g]);
+        TOut *oc = o_seq + (size_t)t0 * tok_stride;
+#pragma unroll
+        for (int i = 0; i < kNQ; ++i)
+            if (i < p.ct && t0 + i < jb.tokens(p)) store_out(oc, (size_t)i * tok_stride, __uint_as_float(ra[i]));
     }
     if (!failed && jb.ok() && p.h_final) {
         uint32_t r[32];
@@ -905,7 +918,8 @@ __device__ __forceinline__ void state_pass_cta(const CUtensorMap &tm_k, const CU
     for (uint32_t i = threadIdx.x * 16; i < Lay::kOffScratch; i += kThreads * 16)
         *(uint4 *)(s.base + i) = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
-        for (int i = 0; i < (int)kNumBars; ++i) mbar_init(&s.bar[i], 1);
+        for (int i = 0; i < (int)kNumBars; ++i)
+            mbar_init(&s.bar[i], (i == kBarOFree || i == kBarOFree + 1 || i == kBarScaled) ? kPrepWarp : 1);
         *s.abort = 0;
         fence_mbar_init();
     }
