@@ -9,6 +9,8 @@ Three independent restatements live here:
 * ``forward`` -- the plain sequential recurrence in C (``recurrence.c``):
   DeltaProduct paper, Sec.4 Eq.(2)-(3), gated variant and per-token
   pseudocode (Sec.4, Appendix B.1).
+* ``backward`` -- reverse-mode gradients of that recurrence in C (the chain
+  rule applied to each sub-step, readout and gate, in reverse token order).
 * ``product_form`` -- the per-token transition A_i = F_{n_h}...F_1 and write
   B_i = sum_j F_{n_h}...F_{j+1} C_j built by explicit matrix products
   (DeltaProduct paper, Sec.4, the expanded form of Eq.(3)).
@@ -38,6 +40,8 @@ def _lib():
         dp = ctypes.POINTER(ctypes.c_double)
         lib.oracle_forward.argtypes = [ctypes.c_int] * 6 + [dp] * 8 + [ctypes.c_int]
         lib.oracle_forward.restype = ctypes.c_int
+        lib.oracle_backward.argtypes = [ctypes.c_int] * 6 + [dp] * 14 + [ctypes.c_int]
+        lib.oracle_backward.restype = ctypes.c_int
         _LIB = lib
     return _LIB
 
@@ -85,6 +89,35 @@ def forward(q, k, v, beta, g=None, h0=None, threads=None):
     if rc != 0:
         raise RuntimeError(f"oracle_forward failed with code {rc}")
     return o, hf
+
+
+def backward(q, k, v, beta, g=None, h0=None, d_o=None, dh_final=None, threads=None):
+    """Gradients of L = <d_o, o> + <dh_final, h_final> through the recurrence
+    (reverse mode, fp64). Returns dict dq, dk, dv, dbeta, dg (None when
+    ungated), dh0, in the layouts of the corresponding inputs.
+
+    d_o [B,T,H,Dv] (None = zeros), dh_final [B,H,Dk,Dv] or None (zeros).
+    Memory: (T + 1) * Dk * Dv doubles per (batch, head) in flight.
+    """
+    q, k, v, beta, g, h0, d_o, dh_final = (_as_f64(x) for x in (q, k, v, beta, g, h0, d_o, dh_final))
+    B, T, H, nh, Dk = k.shape
+    Dv = v.shape[-1]
+    assert q.shape == (B, T, H, Dk) and v.shape == (B, T, H, nh, Dv) and beta.shape == (B, T, H, nh)
+    if d_o is None:
+        d_o = np.zeros((B, T, H, Dv))
+    assert d_o.shape == (B, T, H, Dv), d_o.shape
+    if dh_final is not None:
+        assert dh_final.shape == (B, H, Dk, Dv), dh_final.shape
+    out = {"dq": np.zeros_like(q), "dk": np.zeros_like(k), "dv": np.zeros_like(v),
+           "dbeta": np.zeros_like(beta), "dg": None if g is None else np.zeros_like(g),
+           "dh0": np.zeros((B, H, Dk, Dv))}
+    rc = _lib().oracle_backward(B, T, H, Dk, Dv, nh, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
+                                _ptr(h0), _ptr(d_o), _ptr(dh_final), _ptr(out["dq"]), _ptr(out["dk"]),
+                                _ptr(out["dv"]), _ptr(out["dbeta"]), _ptr(out["dg"]), _ptr(out["dh0"]),
+                                int(threads or default_threads()))
+    if rc != 0:
+        raise RuntimeError(f"oracle_backward failed with code {rc}")
+    return out
 
 
 def decode_step(q, k, v, beta, g, state, threads=None):
