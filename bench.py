@@ -54,6 +54,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
     ap.add_argument("--no-varlen", action="store_true", help="skip the packed variable-length measurement")
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward-pass measurement")
     ap.add_argument("--fused", action="store_true",
                     help="give dp_forward only the minimum workspace: the chunk path then "
                          "runs as one fused kernel instead of prep + state-pass kernels")
@@ -296,6 +297,48 @@ def decode_measure(dev, hbm_peak, n_steps=256, reps=5):
                          "frac": achieved / hbm_peak, "algorithmic_bytes": step_bytes}}
 
 
+def backward_measure(dp, dev, hbm_peak, steps=5, warmup=2):
+    """The backward pass (dp_backward) on the bench workload (B4 H8 T2048
+    n_h 2 D128 bf16, fp32 d_o and dh_final, fp32 gradients): tokens/s from
+    CUDA events, inputs resident. Roofline: every input and cotangent read
+    once, every gradient written once, the states h0 / dh_final / dh0 once
+    per (b,h); the checkpoints the kernel keeps are its own traffic."""
+    w = W.BASE
+    x = {k: (None if v is None else v.to(dev)) for k, v in W.make_inputs(w).items()}
+    gen = torch.Generator().manual_seed(140)
+    d_o = torch.randn(w.B, w.T, w.H, w.Dv, generator=gen).to(dev)
+    dhf = torch.randn(w.B, w.H, w.Dk, w.Dv, generator=gen).to(dev)
+    from deltaproduct_householder_product_gb300 import _lib
+    dims = _lib.make_dims(w.B, w.T, w.H, w.Dk, w.Dv, w.nh, w.torch_dtype, "auto", torch.float32)
+    ws = torch.zeros(_lib.backward_workspace_size(dims), dtype=torch.uint8, device=dev)
+
+    def call():
+        return dp.backward(x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"], d_o=d_o, dh_final=dhf,
+                           workspace=ws)
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    nh, Dk, Dv = w.nh, w.Dk, w.Dv
+    gated = 1 if w.gated else 0
+    per_tok = 2 * (Dk + nh * Dk + nh * Dv + nh + gated) + 4 * Dv + 4 * (Dk + nh * Dk + nh * Dv + nh + gated)
+    states = (3 if w.h0_std > 0 else 2) * Dk * Dv * 4
+    step_bytes = w.B * w.T * w.H * per_tok + w.B * w.H * states
+    achieved = step_bytes / (ms * 1e-3) / 1e9
+    return {"workload": f"{w.name} backward (fp32 d_o, dh_final and gradients)", "ms_per_call": ms,
+            "tokens_per_s": w.B * w.T / (ms * 1e-3), "kernel": "backward_kernel (recurrent, CUDA cores)",
+            "checkpoint_bytes": int(ws.numel()),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "algorithmic_bytes": step_bytes}}
+
+
 VARLEN_LENGTHS = [384, 2944, 1024, 512, 1792, 256, 896, 384]   # 8 sequences, 8192 tokens
 
 
@@ -456,6 +499,8 @@ def ours_arm(args, w):
         line["decode"] = decode_measure(dev, hbm_peak)
     if not args.no_varlen:
         line["varlen"] = varlen_measure(dp, dev, hbm_peak)
+    if not args.no_backward:
+        line["backward"] = backward_measure(dp, dev, hbm_peak)
     if not args.no_cpu_baseline:
         v, desc, cores, _ = oracle_sample(w, x, 8.0, os.cpu_count() or 1)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores,

@@ -93,6 +93,46 @@ def forward(q, k, v, beta, g=None, h0=None, *, impl="auto", out=None, h_final=Tr
     return out, h_final
 
 
+def backward(q, k, v, beta, g=None, h0=None, *, d_o, dh_final=None, want_dh0=True, workspace=None,
+             stream=None):
+    """Gradients of <d_o, o> + <dh_final, h_final> through ``forward``.
+
+    Inputs as for ``forward``; d_o [B,T,H,Dv] (float32, or the input dtype);
+    dh_final float32 [B,H,Dk,Dv] or None (zeros). Returns a dict of float32
+    tensors dq, dk, dv, dbeta, dg (None when ungated) and dh0 (None unless
+    ``want_dh0``), in the layouts of the corresponding inputs.
+    """
+    B, T, H, nh, Dk = k.shape
+    Dv = v.shape[-1]
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g)):
+        _lib._need_cuda(name, t, dt)
+    _lib._need_cuda("h0", h0, torch.float32)
+    _lib._need_cuda("d_o", d_o)
+    _lib._need_cuda("dh_final", dh_final, torch.float32)
+    if q.shape != (B, T, H, Dk) or v.shape != (B, T, H, nh, Dv) or beta.shape != (B, T, H, nh):
+        raise ValueError("inconsistent shapes for q, k, v, beta")
+    if d_o.shape != (B, T, H, Dv):
+        raise ValueError("d_o must be [B,T,H,Dv]")
+    dims = _lib.make_dims(B, T, H, Dk, Dv, nh, dt, "auto", d_o.dtype)
+    f32 = dict(dtype=torch.float32, device=q.device)
+    out = {"dq": torch.empty((B, T, H, Dk), **f32), "dk": torch.empty((B, T, H, nh, Dk), **f32),
+           "dv": torch.empty((B, T, H, nh, Dv), **f32), "dbeta": torch.empty((B, T, H, nh), **f32),
+           "dg": None if g is None else torch.empty((B, T, H), **f32),
+           "dh0": torch.empty((B, H, Dk, Dv), **f32) if want_dh0 else None}
+    need = _lib.backward_workspace_size(dims)
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    _lib._need_cuda("workspace", workspace)
+    rc = _lib.lib().dp_backward(
+        dims, _lib._ptr(q), _lib._ptr(k), _lib._ptr(v), _lib._ptr(beta), _lib._ptr(g), _lib._ptr(h0),
+        _lib._ptr(d_o), _lib._ptr(dh_final), _lib._ptr(out["dq"]), _lib._ptr(out["dk"]), _lib._ptr(out["dv"]),
+        _lib._ptr(out["dbeta"]), _lib._ptr(out["dg"]), _lib._ptr(out["dh0"]), _lib._ptr(workspace),
+        workspace.numel() * workspace.element_size(), _lib._stream(stream))
+    _lib._check(rc, "dp_backward")
+    return out
+
+
 def forward_varlen(q, k, v, beta, g=None, h0=None, *, cu_seqlens, max_seqlen=None, impl="auto", out=None,
                    h_final=True, workspace=None, stream=None, out_dtype=None):
     """Run the recurrence over N variable-length sequences packed along T.

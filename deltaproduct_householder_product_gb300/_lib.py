@@ -57,9 +57,12 @@ def lib():
         L.dp_state_io.argtypes = [ctypes.c_int] * 5 + [_vp, _vp, ctypes.c_int, ctypes.c_int, _vp]
         L.dp_check_status.argtypes = [_vp, _vp]
         L.dp_forward_noalloc.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 9
+        L.dp_backward_workspace_size.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(ctypes.c_size_t)]
+        L.dp_backward.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 15 + [ctypes.c_size_t, _vp]
         for name in ("dp_forward_workspace_size", "dp_forward_workspace_size_fast", "dp_forward_path",
                      "dp_forward", "dp_forward_varlen", "dp_decode_step",
-                     "dp_state_io", "dp_check_status", "dp_forward_noalloc"):
+                     "dp_state_io", "dp_check_status", "dp_forward_noalloc",
+                     "dp_backward_workspace_size", "dp_backward"):
             getattr(L, name).restype = ctypes.c_int
         _LIB = L
     return _LIB
@@ -125,6 +128,13 @@ def forward_path(dims, workspace_bytes):
     _check(lib().dp_forward_path(ctypes.byref(dims), ctypes.c_size_t(workspace_bytes), ctypes.byref(code)),
            "dp_forward_path")
     return PATHS[code.value]
+
+
+def backward_workspace_size(dims):
+    """dp_backward_workspace_size."""
+    n = ctypes.c_size_t(0)
+    _check(lib().dp_backward_workspace_size(ctypes.byref(dims), ctypes.byref(n)), "dp_backward_workspace_size")
+    return n.value
 
 
 def workspace_size(dims, fast=False):

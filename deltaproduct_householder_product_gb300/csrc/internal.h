@@ -42,6 +42,26 @@ size_t chunk_tc_records_bytes(const Problem &p);
 cudaError_t chunk_tc_path(const Problem &p, int *path);
 cudaError_t launch_chunk_tc(const Problem &p);
 
+// One validated backward problem (dp_backward; layouts in dp.h).
+struct BwdProblem {
+    int B, T, H, Dk, Dv, nh;
+    int dtype;                 // dp_dtype of q, k, v, beta, g
+    int do_dtype;              // dp_dtype of d_o
+    const void *q, *k, *v, *beta, *g;
+    const float *h0;
+    const void *d_o;
+    const float *dh_final;
+    float *dq, *dk, *dv, *dbeta, *dg, *dh0;
+    void *scratch;             // checkpoint area (backward_scratch_bytes)
+    cudaStream_t stream;
+};
+
+// Recurrent backward on CUDA cores: checkpoints every
+// backward_segment_tokens(Dk) tokens in the scratch area.
+int backward_segment_tokens(int Dk);
+size_t backward_scratch_bytes(const BwdProblem &p);
+cudaError_t launch_backward(const BwdProblem &p);
+
 cudaError_t launch_state_io(int op, int B, int H, int Dk, int Dv, float *state,
                             void *ext, int ext_dtype, int ext_transposed,
                             cudaStream_t stream);

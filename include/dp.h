@@ -78,7 +78,7 @@ typedef struct {
 } dp_dims;
 
 /* ABI version of this header (bumped on any signature change). */
-#define DP_ABI_VERSION 4
+#define DP_ABI_VERSION 5
 int dp_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -166,6 +166,32 @@ dp_status dp_decode_step(const dp_dims *dims,
 typedef enum { DP_STATE_ZERO = 0, DP_STATE_IMPORT = 1, DP_STATE_EXPORT = 2 } dp_state_op;
 dp_status dp_state_io(int op, int B, int H, int Dk, int Dv, float *state,
                       void *ext, int ext_dtype, int ext_transposed,
+                      dp_stream_t stream);
+
+/* Backward pass: gradients of L = <d_o, o> + <dh_final, h_final> through
+ * the recurrence dp_forward computes (DeltaProduct paper, Sec.4 Eq.(2)-(3),
+ * gated variant), for training. Same dims and input layouts as dp_forward
+ * (dims->impl and dims->max_seqlen must be 0; dims->out_dtype is the type
+ * of d_o).
+ *   d_o      [B,T,H,D_v] gradient of the outputs;
+ *   dh_final [B,H,D_k,D_v] fp32 gradient of the final state, NULL = zeros;
+ * outputs, fp32, written in full:
+ *   dq [B,T,H,D_k], dk [B,T,H,n_h,D_k], dv [B,T,H,n_h,D_v],
+ *   dbeta [B,T,H,n_h], dg [B,T,H] (required iff g != NULL, else ignored),
+ *   dh0 [B,H,D_k,D_v] (NULL = not written; the gradient with respect to
+ *   h0, or to the zero initial state when h0 is NULL).
+ * The gradients with respect to the key rows and the scalars (dq, dk,
+ * dbeta, dg) are sums over the value columns that the kernel accumulates
+ * with fp32 atomic additions, so their last bits may vary between calls.
+ * workspace: at least dp_backward_workspace_size bytes (status block and
+ * the state checkpoints, fp32 D_k x D_v per (b,h) every few tokens). */
+dp_status dp_backward_workspace_size(const dp_dims *dims, size_t *bytes);
+dp_status dp_backward(const dp_dims *dims,
+                      const void *q, const void *k, const void *v,
+                      const void *beta, const void *g, const float *h0,
+                      const void *d_o, const float *dh_final,
+                      float *dq, float *dk, float *dv, float *dbeta, float *dg,
+                      float *dh0, void *workspace, size_t workspace_bytes,
                       dp_stream_t stream);
 
 /* Synchronises `stream`, returns the status the device recorded in the

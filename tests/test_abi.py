@@ -118,3 +118,28 @@ def test_varlen_validation(L):
     assert L.dp_forward_varlen(C.byref(dims), *vargs) == 1
     bad = _lib.make_dims(2, 16, 2, 64, 64, 2, _lib.DP_BF16, "recurrent", max_seqlen=17)
     assert L.dp_forward_varlen(C.byref(bad), *vargs) == 1
+
+
+def test_backward_workspace_and_validation(L):
+    """dp_backward_workspace_size: status block plus one fp32 D_k x D_v
+    checkpoint per (b,h) every segment of tokens; dp_backward rejects NULL
+    inputs, an explicit impl and a short workspace before any launch."""
+    import ctypes as C
+    n = C.c_size_t(0)
+    dims = _lib.make_dims(2, 100, 3, 128, 64, 2, _lib.DP_BF16, "auto", _lib.DP_F32)
+    assert L.dp_backward_workspace_size(C.byref(dims), C.byref(n)) == 0
+    seg = 12                                   # tokens per checkpoint at D_k = 128
+    ck = 2 * 3 * ((100 + seg - 1) // seg) * 128 * 64 * 4
+    assert n.value == 256 + ((ck + 255) // 256) * 256
+    d32 = _lib.make_dims(1, 100, 1, 32, 32, 1, _lib.DP_F32)
+    assert L.dp_backward_workspace_size(C.byref(d32), C.byref(n)) == 0
+    assert n.value == 256 + ((((100 + 47) // 48) * 32 * 32 * 4 + 255) // 256) * 256
+    explicit = _lib.make_dims(2, 100, 3, 128, 64, 2, _lib.DP_BF16, "recurrent")
+    assert L.dp_backward_workspace_size(C.byref(explicit), C.byref(n)) == 1
+    assert L.dp_backward_workspace_size(C.byref(dims), None) == 1
+    null = [None] * 15
+    assert L.dp_backward(C.byref(dims), *null, C.c_size_t(0), None) == 1
+    bad = _lib.make_dims(2, 100, 3, 96, 64, 2, _lib.DP_BF16)
+    assert L.dp_backward(C.byref(bad), *null, C.c_size_t(0), None) == 2
+    empty = _lib.make_dims(0, 100, 3, 128, 64, 2, _lib.DP_BF16)
+    assert L.dp_backward_workspace_size(C.byref(empty), C.byref(n)) == 0 and n.value == 256

@@ -1,0 +1,154 @@
+"""GPU parity of the backward pass (dp_backward) against the fp64 oracle
+backward, through the C ABI.
+
+Every gradient (dq, dk, dv, dbeta, dg, dh0) is compared element by element
+with oracle.backward on the same inputs and cotangents: small cases that
+span several checkpoint segments with a ragged tail, every n_h, gated and
+ungated, fp32 and bf16 inputs, fp32 and bf16 d_o; the degenerate sizes
+(T = 0, T = 1, one segment exactly); and, at the bench workload's full size,
+sampled heads against the oracle run on those heads alone plus a
+directional derivative of the whole loss by central differences of the
+forward oracle.
+
+Tolerance: the kernel runs in fp32 on inputs the oracle sees exactly (bf16
+upcasts exactly), so errors come from fp32 rounding (unit 6e-8) of the
+recurrence and of the gradient sums: about sqrt(T n_h D) accumulated
+roundings for the longest dependency chain, 4e-5 relative at the bench
+size (T n_h = 4096, D = 128). Each gradient tensor must satisfy
+max|err| <= TOL_REL * RMS(reference) with TOL_REL = 1e-4 (observed: about
+2e-6 on the small cases).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deltaproduct_householder_product_gb300 import workloads as W
+from tests.parity import err_stats
+
+pytestmark = pytest.mark.gpu
+
+TOL_REL = 1e-4
+NAMES = ("dq", "dk", "dv", "dbeta", "dg", "dh0")
+
+
+@pytest.fixture(scope="module")
+def dp():
+    from deltaproduct_householder_product_gb300 import build
+    build.build()
+    import deltaproduct_householder_product_gb300 as dp
+    assert torch.cuda.is_available()
+    return dp
+
+
+def cotangents(w, seed, do_dtype=torch.float32):
+    gen = torch.Generator().manual_seed(seed)
+    d_o = torch.randn(w.B, w.T, w.H, w.Dv, generator=gen).to(do_dtype)
+    dhf = torch.randn(w.B, w.H, w.Dk, w.Dv, generator=gen)
+    return d_o, dhf
+
+
+def run_both(dp, w, d_o, dhf, heads=None):
+    x = W.make_inputs(w)
+    xc = {k: (None if v is None else v.cuda()) for k, v in x.items()}
+    got = dp.backward(xc["q"], xc["k"], xc["v"], xc["beta"], xc["g"], xc["h0"], d_o=d_o.cuda(),
+                      dh_final=None if dhf is None else dhf.cuda())
+    torch.cuda.synchronize()
+    if heads is None:
+        ref = oracle.backward(x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"], d_o, dhf)
+        return got, ref, None
+    return got, x, heads
+
+
+def check(got, ref, what, tol=TOL_REL):
+    stats = {}
+    for n in NAMES:
+        if ref[n] is None:
+            assert got[n] is None, n
+            continue
+        s = err_stats(got[n], ref[n])
+        stats[n] = s
+        assert s["rel_max"] <= tol, f"{what} {n}: {s}"
+    return stats
+
+
+CASES = [
+    ("tiny-f32", W.TINY.scaled(T=29), 0),
+    ("d64-f32-gated", W.TINY.scaled(Dk=64, Dv=64, T=53, nh=3, gated=True, h0_std=0.02), 1),
+    ("base-nh1", W.BASE.scaled(B=2, H=2, T=40, nh=1), 2),
+    ("base-nh2", W.BASE.scaled(B=2, H=2, T=37), 3),
+    ("neardup-nh3", W.NEARDUP.scaled(B=1, H=2, T=30), 4),
+    ("gated-nh4", W.GATED.scaled(B=2, H=1, T=27), 5),
+    ("long-nh3-one-segment", W.LONG.scaled(B=1, H=3, T=12), 6),
+]
+
+
+@pytest.mark.parametrize("name,w,seed", CASES, ids=[c[0] for c in CASES])
+def test_backward_parity(dp, name, w, seed):
+    d_o, dhf = cotangents(w, 100 + seed)
+    got, ref, _ = run_both(dp, w, d_o, dhf)
+    stats = check(got, ref, name)
+    print(name, {n: round(s["rel_max"], 8) for n, s in stats.items()})
+
+
+def test_backward_bf16_cotangent_and_no_dh_final(dp):
+    w = W.GATED.scaled(B=1, H=2, T=26, nh=2)
+    d_o, _ = cotangents(w, 120, torch.bfloat16)
+    got, ref, _ = run_both(dp, w, d_o, None)
+    check(got, ref, "bf16 d_o")
+
+
+@pytest.mark.parametrize("T", [0, 1])
+def test_backward_degenerate_lengths(dp, T):
+    w = W.GATED.scaled(B=2, H=2, T=T, nh=2)
+    d_o, dhf = cotangents(w, 130 + T)
+    got, ref, _ = run_both(dp, w, d_o, dhf)
+    if T == 0:
+        assert torch.equal(got["dh0"].cpu(), dhf)
+    else:
+        check(got, ref, f"T={T}")
+
+
+def test_backward_full_size_sampled_heads(dp):
+    """Bench workload (B4 H8 T2048 n_h 2): the first and last heads against
+    the oracle run on those heads alone."""
+    w = W.BASE
+    d_o, dhf = cotangents(w, 140)
+    got, x, _ = run_both(dp, w, d_o, dhf, heads=True)
+    for b, h in ((0, 0), (w.B - 1, w.H - 1)):
+        sl = lambda t: None if t is None else t[b:b + 1, :, h:h + 1]
+        ref = oracle.backward(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["beta"]), sl(x["g"]),
+                              None if x["h0"] is None else x["h0"][b:b + 1, h:h + 1],
+                              sl(d_o), dhf[b:b + 1, h:h + 1])
+        part = {n: (None if got[n] is None else (got[n][b:b + 1, :, h:h + 1] if n != "dh0"
+                                                  else got[n][b:b + 1, h:h + 1]))
+                for n in NAMES}
+        stats = check(part, ref, f"head ({b},{h})")
+        print("full size head", (b, h), {n: round(s["rel_max"], 8) for n, s in stats.items()})
+
+
+def test_backward_directional_derivative_full_size(dp):
+    """<grad, delta> for a random direction delta in every input equals the
+    central difference of L = <d_o, o> + <dh_final, h_final> computed with
+    the fp64 forward oracle (gated workload's recipe at B2 H4 T1024 n_h 4)."""
+    w = W.GATED.scaled(B=2, H=4, T=1024)
+    d_o, dhf = cotangents(w, 150)
+    x = W.make_inputs(w)
+    xc = {k: (None if v is None else v.cuda()) for k, v in x.items()}
+    got = dp.backward(xc["q"], xc["k"], xc["v"], xc["beta"], xc["g"], xc["h0"], d_o=d_o.cuda(),
+                      dh_final=dhf.cuda())
+    gen = torch.Generator().manual_seed(151)
+    xd = {k: x[k].double() for k in x if x[k] is not None}
+    delta = {k: torch.randn(xd[k].shape, generator=gen, dtype=torch.float64) for k in xd}
+    delta["g"] *= 0.01   # keep the gates inside (0, 1)
+    grad_name = {"q": "dq", "k": "dk", "v": "dv", "beta": "dbeta", "g": "dg", "h0": "dh0"}
+    lin = sum(float((got[grad_name[k]].cpu().double() * delta[k]).sum()) for k in xd)
+
+    def loss(s):
+        z = {k: xd[k] + s * delta[k] for k in xd}
+        o, hf = oracle.forward(z["q"], z["k"], z["v"], z["beta"], z.get("g"), z.get("h0"))
+        return float((torch.from_numpy(o) * d_o.double()).sum() + (torch.from_numpy(hf) * dhf.double()).sum())
+    eps = 1e-4
+    fd = (loss(eps) - loss(-eps)) / (2 * eps)
+    print("directional derivative", lin, fd, abs(lin - fd) / abs(fd))
+    assert abs(lin - fd) <= 1e-4 * abs(fd), (lin, fd)
