@@ -19,15 +19,16 @@
 // global reduction (the D_v/32 CTAs of a head add in an unspecified order).
 //
 // Time order: the states needed in reverse are rebuilt, not kept. The CTA
-// first runs the recurrence forward once and stores its slice of the state
-// at the start of every L-th token into the workspace (checkpoints, read
-// back only by the same thread). It then walks the segments of L tokens
-// from the last: the segment is run forward again from its checkpoint,
-// keeping the state at the start of each token and each sub-step's error
-// v - H^T k in shared memory, and then its tokens are differentiated in
-// reverse. A sub-step's state is recomputed from the token's gated state
-// with the same operations as the forward, so every state used in the
-// backward is bit-identical to the forward's.
+// first runs the recurrence forward once, storing its slice of the state at
+// the start of every L-th token (checkpoints) and every sub-step's error
+// e = v - H^T k into the workspace; both are read back only by the CTA
+// that wrote them, after barriers. It then walks the segments of L tokens from the last:
+// the segment is replayed from its checkpoint with the stored errors (the
+// updates H += k (beta e)^T need no reduction), keeping each token's start
+// state in shared memory, and its tokens are differentiated in reverse. A
+// sub-step's state is recomputed from the token's gated state with the
+// same operations as the forward, so every state the backward uses is
+// bit-identical to the forward's.
 #include "internal.h"
 
 namespace dp {
@@ -99,6 +100,7 @@ struct BwdArgs {
     const float *dh_final;
     float *dq, *dk, *dv, *dbeta, *dg, *dh0;
     float *ckpt;   // [B*H][n_seg][DK][Dv]
+    float *errs;   // [B*H][T][nh][Dv] errors v - H^T k of every sub-step
 };
 
 template <int DK, typename TIn, typename TDo>
@@ -150,9 +152,12 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdArgs a)
         float v[4], be[4];
         float g, dov;
     };
-    auto fetch = [&](int t, bool bwd) {
+    // mode: 0 forward (v), 1 replay (stored errors in v[]), 2 backward (q, d_o, stored errors)
+    auto fetch = [&](int t, int mode) {
         TokIn in;
+        const bool bwd = mode == 2;
         const size_t tok = tok_of(t);
+        const float *et = a.errs + ((size_t)bh * T + t) * nh * Dv + col;
         const int nk = nh * DK, n = nk + (bwd ? DK : 0);
 #pragma unroll
         for (int m = 0; m < KQ; ++m) {
@@ -161,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdArgs a)
         }
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-            in.v[jj] = (!bwd && jj < nh) ? to_f(v[(tok * nh + jj) * Dv + col]) : 0.f;
+            in.v[jj] = jj >= nh ? 0.f : mode == 0 ? to_f(v[(tok * nh + jj) * Dv + col]) : mode == 1 ? et[jj * Dv] : 0.f;
             in.be[jj] = jj < nh ? to_f(beta[tok * nh + jj]) : 0.f;
         }
         in.g = g ? to_f(g[tok]) : 1.f;
@@ -184,8 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdArgs a)
 #pragma unroll
     for (int r = 0; r < R; ++r) S[r] = a.h0 ? a.h0[state_base + (size_t)(row0 + r) * Dv + col] : 0.f;
 
-    // one forward token on the state S (keys staged); `err` receives the
-    // errors v - H^T k when non-null
+    // one forward token on the state S (keys staged); its errors v - H^T k
+    // go to `err` ([nh][Dv] of this token, this CTA's columns)
     auto forward_token = [&](const TokIn &in, float *err) {
         if (g) {
 #pragma unroll
@@ -196,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdArgs a)
             if (jj >= nh) break;
             const float *kj = skey + jj * DK;
             const float e = in.v[jj] - matvec(kj, S);
-            if (err && w == 0) err[jj * kCols + lane] = e;
+            if (w == 0) err[jj * Dv] = e;
             const float u = in.be[jj] * e;
 #pragma unroll
             for (int r = 0; r < R; ++r) S[r] = fmaf(kj[row0 + r], u, S[r]);
@@ -205,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdArgs a)
 
     // ---- 1. forward once, checkpoint at every L-th token start
     TokIn cur{};
-    if (T > 0) cur = fetch(0, false);   // every fetch below names a token in [0, T)
+    if (T > 0) cur = fetch(0, 0);   // every fetch below names a token in [0, T)
     for (int t = 0; t < T; ++t) {
         if (t % L == 0) {
             float *c = ckpt + (size_t)(t / L) * DK * Dv;
@@ -213,11 +218,14 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdArgs a)
             for (int r = 0; r < R; ++r) c[(size_t)(row0 + r) * Dv + col] = S[r];
         }
         stage(cur, false);
-        // next: the following token, or the first token of the last segment
-        const TokIn nxt = fetch(t + 1 < T ? t + 1 : (n_seg - 1) * L, false);
-        forward_token(cur, nullptr);
+        const TokIn nxt = t + 1 < T ? fetch(t + 1, 0) : cur;
+        forward_token(cur, a.errs + ((size_t)bh * T + t) * nh * Dv + col);
         cur = nxt;
     }
+    // the replay starts with the last segment's first token, whose errors
+    // must all be written (and visible to the CTA) before they are fetched
+    __syncthreads();
+    if (T > 0) cur = fetch((n_seg - 1) * L, 1);
 
     // ---- 2. segments in reverse
     float dS[R];
@@ -230,15 +238,28 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdArgs a)
         const float *c = ckpt + (size_t)sgi * DK * Dv;
 #pragma unroll
         for (int r = 0; r < R; ++r) S[r] = c[(size_t)(row0 + r) * Dv + col];
-        // forward over the segment: token-start states and errors
+        // replay the segment with the stored errors: token-start states and
+        // errors into shared memory
         for (int t = t0; t < t1; ++t) {
             float *sp = spre + (size_t)(t - t0) * DK * kCols;
 #pragma unroll
             for (int r = 0; r < R; ++r) sp[(row0 + r) * kCols + lane] = S[r];
             stage(cur, false);
             const bool last = t + 1 == t1;
-            const TokIn nxt = fetch(last ? t1 - 1 : t + 1, last);
-            forward_token(cur, serr + (size_t)(t - t0) * nh * kCols);
+            const TokIn nxt = fetch(last ? t1 - 1 : t + 1, last ? 2 : 1);
+            if (g) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) S[r] *= cur.g;
+            }
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                if (jj >= nh) break;
+                const float *kj = skey + jj * DK;
+                if (w == 0) serr[((t - t0) * nh + jj) * kCols + lane] = cur.v[jj];
+                const float u = cur.be[jj] * cur.v[jj];
+#pragma unroll
+                for (int r = 0; r < R; ++r) S[r] = fmaf(kj[row0 + r], u, S[r]);
+            }
             cur = nxt;
         }
         // backward over the segment's tokens
@@ -247,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdArgs a)
             stage(cur, true);
             const TokIn in = cur;
             // next: the previous token, or the first token of the previous segment
-            cur = fetch(t > t0 ? t - 1 : (sgi > 0 ? (sgi - 1) * L : 0), t > t0);
+            cur = fetch(t > t0 ? t - 1 : (sgi > 0 ? (sgi - 1) * L : 0), t > t0 ? 2 : 1);
             const float gt = in.g;
             const float *sp = spre + (size_t)(t - t0) * DK * kCols;
             float Sg[R];
@@ -357,11 +378,18 @@ cudaError_t launch_typed(const BwdProblem &p, const BwdArgs &a)
 
 int backward_segment_tokens(int Dk) { return Dk == 32 ? Seg<32>::L : Dk == 64 ? Seg<64>::L : Seg<128>::L; }
 
-size_t backward_scratch_bytes(const BwdProblem &p)
+namespace {
+size_t backward_ckpt_bytes(const BwdProblem &p)
 {
     const int L = backward_segment_tokens(p.Dk);
     const size_t n_seg = p.T > 0 ? (size_t)(p.T + L - 1) / L : 0;
-    return (size_t)p.B * p.H * n_seg * p.Dk * p.Dv * sizeof(float);
+    return (((size_t)p.B * p.H * n_seg * p.Dk * p.Dv * sizeof(float)) + 255) & ~(size_t)255;
+}
+}  // namespace
+
+size_t backward_scratch_bytes(const BwdProblem &p)
+{
+    return backward_ckpt_bytes(p) + (size_t)p.B * p.H * p.T * p.nh * p.Dv * sizeof(float);
 }
 
 cudaError_t launch_backward(const BwdProblem &p)
@@ -379,6 +407,7 @@ cudaError_t launch_backward(const BwdProblem &p)
     a.d_o = p.d_o; a.dh_final = p.dh_final;
     a.dq = p.dq; a.dk = p.dk; a.dv = p.dv; a.dbeta = p.dbeta; a.dg = p.dg; a.dh0 = p.dh0;
     a.ckpt = (float *)p.scratch;
+    a.errs = (float *)((char *)p.scratch + backward_ckpt_bytes(p));
     if (p.dtype == DP_F32) return launch_typed<float, float>(p, a);
     return p.do_dtype == DP_F32 ? launch_typed<__nv_bfloat16, float>(p, a)
                                 : launch_typed<__nv_bfloat16, __nv_bfloat16>(p, a);

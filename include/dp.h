@@ -183,8 +183,9 @@ dp_status dp_state_io(int op, int B, int H, int Dk, int Dv, float *state,
  * The gradients with respect to the key rows and the scalars (dq, dk,
  * dbeta, dg) are sums over the value columns that the kernel accumulates
  * with fp32 atomic additions, so their last bits may vary between calls.
- * workspace: at least dp_backward_workspace_size bytes (status block and
- * the state checkpoints, fp32 D_k x D_v per (b,h) every few tokens). */
+ * workspace: at least dp_backward_workspace_size bytes (status block, the
+ * state checkpoints, fp32 D_k x D_v per (b,h) every few tokens, and every
+ * sub-step's error v - H^T k, fp32 B T H n_h D_v). */
 dp_status dp_backward_workspace_size(const dp_dims *dims, size_t *bytes);
 dp_status dp_backward(const dp_dims *dims,
                       const void *q, const void *k, const void *v,

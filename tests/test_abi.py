@@ -121,19 +121,22 @@ def test_varlen_validation(L):
 
 
 def test_backward_workspace_and_validation(L):
-    """dp_backward_workspace_size: status block plus one fp32 D_k x D_v
-    checkpoint per (b,h) every segment of tokens; dp_backward rejects NULL
+    """dp_backward_workspace_size: status block, one fp32 D_k x D_v
+    checkpoint per (b,h) every segment of tokens and every sub-step's error;
+    dp_backward rejects NULL
     inputs, an explicit impl and a short workspace before any launch."""
     import ctypes as C
     n = C.c_size_t(0)
     dims = _lib.make_dims(2, 100, 3, 128, 64, 2, _lib.DP_BF16, "auto", _lib.DP_F32)
     assert L.dp_backward_workspace_size(C.byref(dims), C.byref(n)) == 0
+    r256 = lambda x: (x + 255) // 256 * 256
     seg = 12                                   # tokens per checkpoint at D_k = 128
     ck = 2 * 3 * ((100 + seg - 1) // seg) * 128 * 64 * 4
-    assert n.value == 256 + ((ck + 255) // 256) * 256
+    errs = 2 * 100 * 3 * 2 * 64 * 4            # every sub-step's error, fp32
+    assert n.value == 256 + r256(r256(ck) + errs)
     d32 = _lib.make_dims(1, 100, 1, 32, 32, 1, _lib.DP_F32)
     assert L.dp_backward_workspace_size(C.byref(d32), C.byref(n)) == 0
-    assert n.value == 256 + ((((100 + 47) // 48) * 32 * 32 * 4 + 255) // 256) * 256
+    assert n.value == 256 + r256(r256(((100 + 47) // 48) * 32 * 32 * 4) + 100 * 32 * 4)
     explicit = _lib.make_dims(2, 100, 3, 128, 64, 2, _lib.DP_BF16, "recurrent")
     assert L.dp_backward_workspace_size(C.byref(explicit), C.byref(n)) == 1
     assert L.dp_backward_workspace_size(C.byref(dims), None) == 1
