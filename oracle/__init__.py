@@ -11,6 +11,9 @@ Three independent restatements live here:
   pseudocode (Sec.4, Appendix B.1).
 * ``backward`` -- reverse-mode gradients of that recurrence in C (the chain
   rule applied to each sub-step, readout and gate, in reverse token order).
+* ``prologue`` -- the element-wise input maps of Sec.4 (SiLU and L2
+  normalisation of keys, sigmoid / 2 sigmoid betas, sigmoid gates) applied
+  to raw projections, in numpy fp64.
 * ``product_form`` -- the per-token transition A_i = F_{n_h}...F_1 and write
   B_i = sum_j F_{n_h}...F_{j+1} C_j built by explicit matrix products
   (DeltaProduct paper, Sec.4, the expanded form of Eq.(3)).
@@ -133,4 +136,4 @@ def decode_step(q, k, v, beta, g, state, threads=None):
     return o[:, 0], hf
 
 
-from . import chunkwise, product_form  # noqa: E402,F401
+from . import chunkwise, product_form, prologue  # noqa: E402,F401
