@@ -55,6 +55,7 @@ def parse():
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
     ap.add_argument("--no-varlen", action="store_true", help="skip the packed variable-length measurement")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward-pass measurement")
+    ap.add_argument("--no-prologue", action="store_true", help="skip the fused-prologue measurement")
     ap.add_argument("--fused", action="store_true",
                     help="give dp_forward only the minimum workspace: the chunk path then "
                          "runs as one fused kernel instead of prep + state-pass kernels")
@@ -339,6 +340,59 @@ def backward_measure(dp, dev, hbm_peak, steps=5, warmup=2):
                          "frac": achieved / hbm_peak, "algorithmic_bytes": step_bytes}}
 
 
+def prologue_measure(dp, dev, hbm_peak, steps=50, warmup=5):
+    """The input prologue on the bench workload (B4 H8 T2048 n_h 2 D128
+    bf16, fp32 o), from raw projections: fused (dims.prologue: the kernels
+    map k, q, beta while loading them) against unfused (dp_prologue writes
+    the mapped tensors, then dp_forward reads them). CUDA events, inputs
+    resident, one workspace."""
+    from deltaproduct_householder_product_gb300 import _lib
+    w = W.BASE
+    x = {k: (None if v is None else v.to(dev)) for k, v in W.make_raw_inputs(w).items()}
+    flags = W.prologue_flags(w)
+    # the fast workspace of the prologue call (its records carry the mapped K, Q rows)
+    dims = _lib.make_dims(w.B, w.T, w.H, w.Dk, w.Dv, w.nh, w.torch_dtype, "auto", torch.float32,
+                          prologue=flags)
+    ws = torch.zeros(_lib.workspace_size(dims, fast=True), dtype=torch.uint8, device=dev)
+    o = torch.empty(w.B, w.T, w.H, w.Dv, dtype=torch.float32, device=dev)
+    hf = torch.empty(w.B, w.H, w.Dk, w.Dv, dtype=torch.float32, device=dev)
+
+    def fused():
+        dp.forward(x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"], out=o, h_final=hf, workspace=ws,
+                   prologue=flags)
+
+    def unfused():
+        q, k, b, g = dp.prologue(x["q"], x["k"], x["beta"], x["g"], flags=flags)
+        dp.forward(q, k, x["v"], b, g, x["h0"], out=o, h_final=hf, workspace=ws)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        stream = torch.cuda.current_stream()
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+    ms_f, ms_u = timed(fused), timed(unfused)
+    dp.check_status(ws)
+    step_bytes = W.algorithmic_bytes(w, out_bytes=4)
+    el = 2
+    tok = w.B * w.T * w.H
+    extra = 2 * el * tok * (w.Dk + w.nh * w.Dk + w.nh + (1 if w.gated else 0))   # mapped tensors out and back in
+    achieved = step_bytes / (ms_f * 1e-3) / 1e9
+    return {"workload": f"{w.name} from raw projections (SiLU+L2 keys, L2 queries, "
+                        f"{'2 ' if w.beta_max == 2.0 else ''}sigmoid betas)",
+            "flags": flags, "path": _lib.forward_path(dims, ws.numel()),
+            "ms_fused": ms_f, "ms_unfused": ms_u, "tokens_per_s_fused": w.B * w.T / (ms_f * 1e-3),
+            "unfused_extra_bytes": extra,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "algorithmic_bytes": step_bytes}}
+
+
 VARLEN_LENGTHS = [384, 2944, 1024, 512, 1792, 256, 896, 384]   # 8 sequences, 8192 tokens
 
 
@@ -501,6 +555,8 @@ def ours_arm(args, w):
         line["varlen"] = varlen_measure(dp, dev, hbm_peak)
     if not args.no_backward:
         line["backward"] = backward_measure(dp, dev, hbm_peak)
+    if not args.no_prologue:
+        line["prologue"] = prologue_measure(dp, dev, hbm_peak)
     if not args.no_cpu_baseline:
         v, desc, cores, _ = oracle_sample(w, x, 8.0, os.cpu_count() or 1)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores,

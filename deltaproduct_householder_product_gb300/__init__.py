@@ -12,8 +12,23 @@ from . import _lib
 from ._lib import DPError, STATE_EXPORT, STATE_IMPORT, STATE_ZERO  # noqa: F401
 
 __all__ = ["forward", "forward_varlen", "forward_noalloc", "forward_path", "supports", "decode_step", "state_io", "check_status",
+           "backward", "prologue", "prologue_flags",
            "workspace_size",
            "DPError", "abi_version"]
+
+
+PROLOGUE = {"key_silu_l2": 1, "query_l2": 2, "beta_sigmoid": 4, "beta_2sigmoid": 8, "gate_sigmoid": 16}
+
+
+def prologue_flags(prologue):
+    """dp_prologue_flags from an int, or from names (iterable or '+'-joined
+    string) among PROLOGUE's keys."""
+    if prologue is None:
+        return 0
+    if isinstance(prologue, int):
+        return prologue
+    names = prologue.split("+") if isinstance(prologue, str) else list(prologue)
+    return sum(PROLOGUE[n] for n in names if n)
 
 
 def abi_version():
@@ -21,18 +36,21 @@ def abi_version():
 
 
 def workspace_size(B, T, H, Dk, Dv, nh, dtype=torch.bfloat16, impl="auto", out_dtype=None,
-                   fast=False):
+                   fast=False, prologue=0):
     """Device workspace bytes dp_forward needs for this problem; with ``fast``,
     the size with which it takes its fastest path (the chunk path's parallel
-    prep kernel and per-chunk records)."""
-    return _lib.workspace_size(_lib.make_dims(B, T, H, Dk, Dv, nh, dtype, impl, out_dtype), fast)
+    prep kernel and per-chunk records). ``prologue`` as for ``forward``."""
+    return _lib.workspace_size(_lib.make_dims(B, T, H, Dk, Dv, nh, dtype, impl, out_dtype,
+                                              prologue=prologue_flags(prologue)), fast)
 
 
-def forward_path(B, T, H, Dk, Dv, nh, workspace_bytes, dtype=torch.bfloat16, impl="auto", out_dtype=None):
+def forward_path(B, T, H, Dk, Dv, nh, workspace_bytes, dtype=torch.bfloat16, impl="auto", out_dtype=None,
+                 prologue=0):
     """How ``forward`` runs this problem with a workspace of ``workspace_bytes``:
     "recurrent", "chunk_fused", "chunk_split" (two kernels) or "chunk_coop"
     (one cooperative launch)."""
-    return _lib.forward_path(_lib.make_dims(B, T, H, Dk, Dv, nh, dtype, impl, out_dtype), workspace_bytes)
+    return _lib.forward_path(_lib.make_dims(B, T, H, Dk, Dv, nh, dtype, impl, out_dtype,
+                                            prologue=prologue_flags(prologue)), workspace_bytes)
 
 
 def supports(impl, B, T, H, Dk, Dv, nh, dtype=torch.bfloat16):
@@ -47,7 +65,7 @@ def supports(impl, B, T, H, Dk, Dv, nh, dtype=torch.bfloat16):
 
 
 def forward(q, k, v, beta, g=None, h0=None, *, impl="auto", out=None, h_final=True,
-            workspace=None, stream=None, out_dtype=None):
+            workspace=None, stream=None, out_dtype=None, prologue=0):
     """Run the recurrence over whole sequences.
 
     q [B,T,H,Dk], k [B,T,H,nh,Dk], v [B,T,H,nh,Dv], beta [B,T,H,nh], g [B,T,H]
@@ -56,6 +74,8 @@ def forward(q, k, v, beta, g=None, h0=None, *, impl="auto", out=None, h_final=Tr
     (default: the input dtype; float32 is allowed with bfloat16 inputs, or
     taken from ``out``). ``h_final`` may be True (allocate),
     False/None (do not write) or a float32 [B,H,Dk,Dv] tensor (may be h0).
+    ``prologue``: dp_prologue_flags (int or names, see ``prologue_flags``):
+    the named inputs hold raw projections and the kernels map them on load.
     Returns (o, h_final_or_None).
     """
     B, T, H, nh, Dk = k.shape
@@ -72,7 +92,7 @@ def forward(q, k, v, beta, g=None, h0=None, *, impl="auto", out=None, h_final=Tr
         raise ValueError("h0 must be [B,H,Dk,Dv]")
     if out_dtype is None:
         out_dtype = out.dtype if out is not None else dt
-    dims = _lib.make_dims(B, T, H, Dk, Dv, nh, dt, impl, out_dtype)
+    dims = _lib.make_dims(B, T, H, Dk, Dv, nh, dt, impl, out_dtype, prologue=prologue_flags(prologue))
     if out is None:
         out = torch.empty((B, T, H, Dv), dtype=out_dtype, device=q.device)
     _lib._need_cuda("out", out, out_dtype)
@@ -134,7 +154,7 @@ def backward(q, k, v, beta, g=None, h0=None, *, d_o, dh_final=None, want_dh0=Tru
 
 
 def forward_varlen(q, k, v, beta, g=None, h0=None, *, cu_seqlens, max_seqlen=None, impl="auto", out=None,
-                   h_final=True, workspace=None, stream=None, out_dtype=None):
+                   h_final=True, workspace=None, stream=None, out_dtype=None, prologue=0):
     """Run the recurrence over N variable-length sequences packed along T.
 
     q [T,H,Dk], k [T,H,nh,Dk], v [T,H,nh,Dv], beta [T,H,nh], g [T,H] or None;
@@ -163,7 +183,7 @@ def forward_varlen(q, k, v, beta, g=None, h0=None, *, cu_seqlens, max_seqlen=Non
         max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if N > 0 else 0
     if out_dtype is None:
         out_dtype = out.dtype if out is not None else dt
-    dims = _lib.make_dims(N, T, H, Dk, Dv, nh, dt, impl, out_dtype, max_seqlen)
+    dims = _lib.make_dims(N, T, H, Dk, Dv, nh, dt, impl, out_dtype, max_seqlen, prologue_flags(prologue))
     if out is None:
         out = torch.empty((T, H, Dv), dtype=out_dtype, device=q.device)
     _lib._need_cuda("out", out, out_dtype)
@@ -205,7 +225,7 @@ def forward_noalloc(q, k, v, beta, g=None, h0=None, *, impl="auto", out, h_final
     return out, h_final
 
 
-def decode_step(q, k, v, beta, g, state, *, out=None, stream=None, out_dtype=None):
+def decode_step(q, k, v, beta, g, state, *, out=None, stream=None, out_dtype=None, prologue=0):
     """One token on a carried fp32 state (updated in place).
 
     q [B,H,Dk], k [B,H,nh,Dk], v [B,H,nh,Dv], beta [B,H,nh], g [B,H] or None,
@@ -224,12 +244,35 @@ def decode_step(q, k, v, beta, g, state, *, out=None, stream=None, out_dtype=Non
     if out is None:
         out = torch.empty((B, H, Dv), dtype=out_dtype, device=q.device)
     _lib._need_cuda("out", out, out_dtype)
-    dims = _lib.make_dims(B, 1, H, Dk, Dv, nh, dt, "auto", out_dtype)
+    dims = _lib.make_dims(B, 1, H, Dk, Dv, nh, dt, "auto", out_dtype, prologue=prologue_flags(prologue))
     rc = _lib.lib().dp_decode_step(dims, _lib._ptr(q), _lib._ptr(k), _lib._ptr(v),
                                    _lib._ptr(beta), _lib._ptr(g), _lib._ptr(state),
                                    _lib._ptr(out), _lib._stream(stream))
     _lib._check(rc, "dp_decode_step")
     return out
+
+
+def prologue(q, k, beta, g=None, *, flags, stream=None):
+    """dp_prologue: the input maps on their own (the unfused form). Inputs as
+    for ``forward`` (raw projections); returns (q, k, beta, g) with the
+    flagged ones mapped (new tensors in the input dtype) and the others
+    passed through."""
+    f = prologue_flags(flags)
+    B, T, H, nh, Dk = k.shape
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("beta", beta), ("g", g)):
+        _lib._need_cuda(name, t, dt)
+    dims = _lib.make_dims(B, T, H, Dk, Dk, nh, dt, "auto", dt, prologue=f)
+    q_o = torch.empty_like(q) if f & 2 else q
+    k_o = torch.empty_like(k) if f & 1 else k
+    b_o = torch.empty_like(beta) if f & 12 else beta
+    g_o = torch.empty_like(g) if (g is not None and f & 16) else g
+    rc = _lib.lib().dp_prologue(dims, _lib._ptr(q), _lib._ptr(k), _lib._ptr(beta), _lib._ptr(g),
+                                _lib._ptr(q_o) if f & 2 else None, _lib._ptr(k_o) if f & 1 else None,
+                                _lib._ptr(b_o) if f & 12 else None,
+                                _lib._ptr(g_o) if (g is not None and f & 16) else None, _lib._stream(stream))
+    _lib._check(rc, "dp_prologue")
+    return q_o, k_o, b_o, g_o
 
 
 def state_io(op, state, ext=None, transposed=False, stream=None):

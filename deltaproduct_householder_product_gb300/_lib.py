@@ -30,7 +30,7 @@ class Dims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
                 ("Dk", ctypes.c_int), ("Dv", ctypes.c_int), ("nh", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("impl", ctypes.c_int), ("out_dtype", ctypes.c_int),
-                ("max_seqlen", ctypes.c_int)]
+                ("max_seqlen", ctypes.c_int), ("prologue", ctypes.c_int)]
 
 
 _LIB = None
@@ -59,10 +59,11 @@ def lib():
         L.dp_forward_noalloc.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 9
         L.dp_backward_workspace_size.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(ctypes.c_size_t)]
         L.dp_backward.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 15 + [ctypes.c_size_t, _vp]
+        L.dp_prologue.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 9
         for name in ("dp_forward_workspace_size", "dp_forward_workspace_size_fast", "dp_forward_path",
                      "dp_forward", "dp_forward_varlen", "dp_decode_step",
                      "dp_state_io", "dp_check_status", "dp_forward_noalloc",
-                     "dp_backward_workspace_size", "dp_backward"):
+                     "dp_backward_workspace_size", "dp_backward", "dp_prologue"):
             getattr(L, name).restype = ctypes.c_int
         _LIB = L
     return _LIB
@@ -108,14 +109,17 @@ def _need_cuda(name, t, dtype=None):
         raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
 
 
-def make_dims(B, T, H, Dk, Dv, nh, dtype, impl="auto", out_dtype=None, max_seqlen=0):
+PRO_KEY_SILU_L2, PRO_QUERY_L2, PRO_BETA_SIGMOID, PRO_BETA_2SIGMOID, PRO_GATE_SIGMOID = 1, 2, 4, 8, 16
+
+
+def make_dims(B, T, H, Dk, Dv, nh, dtype, impl="auto", out_dtype=None, max_seqlen=0, prologue=0):
     dt = dtype if isinstance(dtype, int) else _dtype_code(dtype)
     if out_dtype is None:
         od = dt
     else:
         od = out_dtype if isinstance(out_dtype, int) else _dtype_code(out_dtype)
     return Dims(B, T, H, Dk, Dv, nh, dt, IMPLS[impl] if isinstance(impl, str) else int(impl), od,
-                max_seqlen)
+                max_seqlen, int(prologue))
 
 
 PATHS = {0: "recurrent", 1: "chunk_fused", 2: "chunk_split", 3: "chunk_coop"}

@@ -32,6 +32,9 @@ dp_status check_dims(const dp_dims *d, bool decode)
     if (d->out_dtype != d->dtype && d->out_dtype != DP_F32) return DP_ERR_INVALID_ARG;
     if (!supported_dim(d->Dk) || !supported_dim(d->Dv)) return DP_ERR_UNSUPPORTED;
     if (d->nh < 1 || d->nh > 4) return DP_ERR_UNSUPPORTED;
+    if ((d->prologue & ~31) != 0 ||
+        ((d->prologue & DP_PRO_BETA_SIGMOID) && (d->prologue & DP_PRO_BETA_2SIGMOID)))
+        return DP_ERR_INVALID_ARG;
     // indices are formed in 64-bit, but keep every extent within int range
     const long long tok = (long long)d->B * (decode ? 1 : d->T) * d->H;
     if (tok * d->nh * (d->Dk > d->Dv ? d->Dk : d->Dv) > (1ll << 40)) return DP_ERR_UNSUPPORTED;
@@ -61,6 +64,7 @@ dp::Problem make_problem(const dp_dims *d, int T)
     p.dtype = d->dtype;
     p.out_dtype = d->out_dtype;
     p.max_T = d->max_seqlen > 0 ? d->max_seqlen : T;
+    p.prologue = d->prologue;
     return p;
 }
 
@@ -265,7 +269,7 @@ dp::BwdProblem make_bwd(const dp_dims *d)
 dp_status check_bwd_dims(const dp_dims *d)
 {
     DP_TRY(check_dims(d, false));
-    if (d->impl != DP_IMPL_AUTO || d->max_seqlen != 0) return DP_ERR_INVALID_ARG;
+    if (d->impl != DP_IMPL_AUTO || d->max_seqlen != 0 || d->prologue != 0) return DP_ERR_INVALID_ARG;
     return DP_OK;
 }
 }  // namespace
@@ -319,3 +323,33 @@ dp_status dp_backward(const dp_dims *dims, const void *q, const void *k, const v
 }
 
 }  // extern "C"
+
+extern "C" dp_status dp_prologue(const dp_dims *dims, const void *q, const void *k, const void *beta, const void *g,
+                                 void *q_out, void *k_out, void *beta_out, void *g_out, dp_stream_t stream)
+{
+    DP_TRY(check_dims(dims, false));
+    if (dims->max_seqlen != 0) return DP_ERR_INVALID_ARG;
+    dp::Problem p = make_problem(dims, dims->T);
+    const int f = dims->prologue;
+    const size_t el = p.dtype == DP_F32 ? 4 : 2;
+    if ((size_t)p.B * p.T * p.H > 0) {
+        if (f & DP_PRO_KEY_SILU_L2) {
+            DP_TRY(check_ptr(k, 16));
+            DP_TRY(check_ptr(k_out, 16));
+        }
+        if (f & DP_PRO_QUERY_L2) {
+            DP_TRY(check_ptr(q, 16));
+            DP_TRY(check_ptr(q_out, 16));
+        }
+        if (f & (DP_PRO_BETA_SIGMOID | DP_PRO_BETA_2SIGMOID)) {
+            DP_TRY(check_ptr(beta, el));
+            DP_TRY(check_ptr(beta_out, el));
+        }
+        if ((f & DP_PRO_GATE_SIGMOID) && g) DP_TRY(check_ptr(g_out, el));
+        if ((f & DP_PRO_GATE_SIGMOID) && g) DP_TRY(check_ptr(g, el));
+    }
+    p.q = q; p.k = k; p.beta = beta; p.g = (f & DP_PRO_GATE_SIGMOID) ? g : nullptr;
+    p.stream = (cudaStream_t)stream;
+    if ((size_t)p.B * p.T * p.H == 0 || f == 0) return DP_OK;
+    return from_cuda(dp::launch_prologue(p, q_out, k_out, beta_out, p.g ? g_out : nullptr));
+}

@@ -128,6 +128,21 @@ constexpr uint32_t kRecBeta = kRecP + kNQ * kC * 4;   // + 2 KB
 constexpr uint32_t kRecL = kRecBeta + kC * 4;
 constexpr uint32_t kRecBytes = kRecL + kC * 4;        // 18688
 static_assert(kRecBytes % 16 == 0, "bulk copies move 16-byte multiples");
+// With a key or query prologue the record also carries the chunk's mapped
+// K and Q rows (the 48 rows of each 64-column KQ block, swizzled as in
+// shared memory), so the state pass copies them instead of mapping them.
+constexpr uint32_t kRecKQBlock = (kC + kNQ) * 128;    // 6144
+constexpr uint32_t kRecKQ = kRecBytes;
+constexpr uint32_t kRecKQBytes = 2 * kRecKQBlock;
+__host__ __device__ constexpr bool kq_in_record(int prologue)
+{
+    return (prologue & (DP_PRO_KEY_SILU_L2 | DP_PRO_QUERY_L2)) != 0;
+}
+__host__ __device__ constexpr uint32_t record_stride(int prologue)
+{
+    return kq_in_record(prologue) ? kRecBytes + kRecKQBytes : kRecBytes;
+}
+static_assert(record_stride(DP_PRO_KEY_SILU_L2) % 16 == 0, "bulk copies move 16-byte multiples");
 
 // Shared-memory layout of the state-pass kernel in each mode.
 template <bool kSplit>
@@ -141,7 +156,7 @@ struct Layout {
     static constexpr uint32_t kOffBar = kOffScratch + 2 * kScratch;
 };
 
-constexpr uint32_t kNumBars = 2 * kNS + 2 * 6 + 5;
+constexpr uint32_t kNumBars = 2 * kNS + 2 * 6 + 7;
 template <bool kSplit>
 constexpr uint32_t smem_bytes() { return Layout<kSplit>::kOffBar + kNumBars * 8 + 16 + 1024; }
 static_assert(smem_bytes<true>() <= 227 * 1024 && smem_bytes<false>() <= 227 * 1024, "shared memory");
@@ -154,7 +169,7 @@ struct Params {
     void *o;
     float *h_final;
     uint32_t *status;
-    uint8_t *rec;              // per-chunk records (split mode), [B*H][n_chunks][kRecBytes]
+    uint8_t *rec;              // per-chunk records (split mode), [B*H][n_chunks][rec_stride]
     uint32_t *flags;           // cooperative mode: record published, [B*H][n_chunks]
     uint32_t *sync;            // cooperative mode: [0] launch generation, [1] CTAs finished
     int T, H, nh, ct;
@@ -163,14 +178,18 @@ struct Params {
     const int *cu;             // packed sequences: token offsets [B+1] (NULL: dense [B,T] layout)
     int B;
     int max_T;                 // longest sequence (T for dense calls)
+    int prologue;              // dp_prologue_flags applied on load
+    uint32_t rec_stride;       // bytes per record: record_stride(prologue)
 };
 
 // The (sequence, head) pair one state-pass CTA, or one prep step, works on.
 // Dense calls (kPacked = false): sequence b is batch row b, T tokens, and
 // every extent comes straight from the kernel parameters. Packed calls: the
 // extent is read from cu (and checked) once.
-template <bool kPacked>
+template <bool kPk, bool kPr>
 struct Job {
+    static constexpr bool kPacked = kPk;   // offsets from cu (else the dense layout)
+    static constexpr bool kPro = kPr;      // input prologue (Params::prologue) applied on load
     int b, h;          // sequence and head
     int b_map, t0;     // packed: token t sits at row (b_map * T + t0 + t) of the token layouts
     int len, nc;       // packed: its tokens and chunks
@@ -182,10 +201,10 @@ struct Job {
     __device__ __forceinline__ bool ok() const { return kPacked ? valid : true; }
 };
 
-template <bool kPacked>
-__device__ __forceinline__ Job<kPacked> make_job(const Params &p, int bh)
+template <bool kPacked, bool kPro>
+__device__ __forceinline__ Job<kPacked, kPro> make_job(const Params &p, int bh)
 {
-    Job<kPacked> j;
+    Job<kPacked, kPro> j;
     j.b = bh / p.H;
     j.h = bh - j.b * p.H;
     j.b_map = j.t0 = j.len = j.nc = 0;
@@ -202,8 +221,8 @@ __device__ __forceinline__ Job<kPacked> make_job(const Params &p, int bh)
 }
 
 // (token, head) index of token t of the job: rows of q, g, o (x n_h for k, v, beta)
-template <bool kPacked>
-__device__ __forceinline__ size_t tok_row(const Params &p, const Job<kPacked> &j, int t)
+template <class J>
+__device__ __forceinline__ size_t tok_row(const Params &p, const J &j, int t)
 {
     return ((size_t)j.row_b() * p.T + j.first() + t) * p.H + j.h;
 }
@@ -229,8 +248,8 @@ __device__ __forceinline__ uint32_t read_generation(const uint32_t *sync)
     return v;
 }
 
-template <bool kPacked>
-__device__ __forceinline__ size_t rec_index(const Params &p, const Job<kPacked> &j, int c)
+template <class J>
+__device__ __forceinline__ size_t rec_index(const Params &p, const J &j, int c)
 {
     return ((size_t)j.b * p.H + j.h) * (size_t)p.n_chunks + c;
 }
@@ -279,7 +298,8 @@ enum : int {
     kBarScaled,                   // S scaled by Gamma_C (gated; one arrival per epilogue warp)
     kBarInit,                     // initial state in TMEM
     kBarFinal,                    // [2] every MMA of an issuer retired (teardown)
-    kBarCount = kBarFinal + 2
+    kBarNorm = kBarFinal + 2,     // [2] prologue applied to the group's stage (fused mode with a prologue)
+    kBarCount = kBarNorm + 2
 };
 static_assert(kBarCount == (int)kNumBars, "barrier count");
 
@@ -354,9 +374,9 @@ __device__ __forceinline__ void issue_gram(uint32_t d_tmem, uint32_t kq)
 // ------------------------------------------------------------------ TMA producer
 constexpr uint32_t kFlagTries = 1u << 24;   // x >= 64 ns each: seconds, then a timeout
 
-template <bool kSplit, bool kCoop, bool kPacked>
+template <bool kSplit, bool kCoop, class J>
 __device__ void tma_role(const Smem &s, const Params &p, const CUtensorMap *tk,
-                         const CUtensorMap *tv, const CUtensorMap *tq, const Job<kPacked> &jb)
+                         const CUtensorMap *tv, const CUtensorMap *tq, const J &jb)
 {
     const int h = jb.h;
     const int ct = p.ct, R = ct * p.nh;
@@ -365,7 +385,10 @@ __device__ void tma_role(const Smem &s, const Params &p, const CUtensorMap *tk,
     // K and V: 2 x R rows x 128 B each; Q: 2 x ct rows. Record: the T tiles
     // it uses (2 or 4) and P, beta, L.
     const uint32_t rec_t = (gated ? 4 : 2) * kTTile, rec_tail = kRecBytes - kRecP;
-    const uint32_t bytes = 512u * R + 256u * ct + (kSplit ? rec_t + rec_tail : 0u);
+    // mapped K and Q from the record (split modes with a key/query prologue)
+    const bool kq_rec = kSplit && J::kPro && kq_in_record(p.prologue);
+    const uint32_t bytes = (kq_rec ? 256u * R + kRecKQBytes : 512u * R + 256u * ct) +
+                           (kSplit ? rec_t + rec_tail : 0u);
     int last_use[kNS];
     for (int i = 0; i < kNS; ++i) last_use[i] = -1;
     for (int c = 0; c < jb.chunks(p); ++c) {
@@ -387,14 +410,18 @@ __device__ void tma_role(const Smem &s, const Params &p, const CUtensorMap *tk,
         uint64_t *bar = &s.bar[kBarFull + st];
         mbar_arrive_expect_tx(bar, bytes);
         const int t0 = jb.first() + c * ct, b = jb.row_b();
+        const uint8_t *rec = kSplit ? p.rec + rec_index(p, jb, c) * p.rec_stride : nullptr;
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
-            tma_load_5d(kq + kb * kKQBlock, tk, bar, kb * 64, 0, h, t0, b);
-            tma_load_4d(kq + kb * kKQBlock + kC * 128, tq, bar, kb * 64, h, t0, b);
+            if (kq_rec) {
+                bulk_load(kq + kb * kKQBlock, rec + kRecKQ + kb * kRecKQBlock, kRecKQBlock, bar);
+            } else {
+                tma_load_5d(kq + kb * kKQBlock, tk, bar, kb * 64, 0, h, t0, b);
+                tma_load_4d(kq + kb * kKQBlock + kC * 128, tq, bar, kb * 64, h, t0, b);
+            }
             tma_load_5d(vv + kb * kVBlock, tv, bar, kb * 64, 0, h, t0, b);
         }
         if (kSplit) {
-            const uint8_t *rec = p.rec + rec_index(p, jb, c) * kRecBytes;
             uint8_t *dst = kq + kStageIn;
             bulk_load(dst + kRecT, rec + kRecT, rec_t, bar);
             bulk_load(dst + kRecP, rec + kRecP, rec_tail, bar);
@@ -412,7 +439,7 @@ __device__ void tma_role(const Smem &s, const Params &p, const CUtensorMap *tk,
 // W^T = K^T (T diag(beta Gamma))^T. They run one chunk ahead of the state
 // pass and are issued by their own thread so that their issue latency
 // overlaps the state pass's.
-template <bool kSplit>
+template <bool kSplit, bool kPro>
 __device__ void prep_mma_role(const Smem &s, const Params &p, uint32_t tbase, int n)
 {
     const bool gated = p.g != nullptr;
@@ -457,7 +484,9 @@ __device__ void prep_mma_role(const Smem &s, const Params &p, uint32_t tbase, in
             if ((ok = uw_ready(c))) issue_uw(c);
     } else {
         for (int c = 0; c < n && ok; ++c) {
-            if (!(ok = wait_bar(s, kBarFull + c % kNS, (c / kNS) & 1, p.status))) break;
+            ok = kPro ? wait_bar(s, kBarNorm + (c & 1), (c >> 1) & 1, p.status)
+                      : wait_bar(s, kBarFull + c % kNS, (c / kNS) & 1, p.status);
+            if (!ok) break;
             tc_fence_after();
             issue_gram(tbase + kColGQ + (c & 1) * 32, smem_addr(s.stage(c % kNS)));
             mma_commit(&s.bar[kBarGQ + (c & 1)]);
@@ -510,13 +539,48 @@ __device__ void chain_role(const Smem &s, const Params &p, uint32_t tbase, int n
 }
 
 // ------------------------------------------------------------------ prep work
+// Input prologue on a landed KQ stage (bf16; two 64-column blocks of 64
+// rows x 128 B, 128-byte swizzle): SiLU + L2 normalisation of key rows
+// 0..R-1 and L2 normalisation of query rows kC..kC+ct-1, as the flags
+// select, in place, one warp per row, rounded back to bf16. The swizzle
+// only permutes 16-byte pieces within a row, and the maps are per element
+// plus a row norm, so each lane takes its 8 bytes where they lie (lane l:
+// block l/16, byte 8(l%16) of the row).
+__device__ void normalise_rows(uint8_t *kq, int R, int ct, int flags, int lt, int nthreads)
+{
+    const int lane = lt & 31, nw = nthreads >> 5;
+    const int nk = (flags & DP_PRO_KEY_SILU_L2) ? R : 0, nq = (flags & DP_PRO_QUERY_L2) ? ct : 0;
+    for (int i = lt >> 5; i < nk + nq; i += nw) {
+        const bool key = i < nk;
+        const int row = key ? i : kC + (i - nk);
+        uint2 *ptr = (uint2 *)(kq + (lane >> 4) * kKQBlock + row * 128 + (lane & 15) * 8);
+        uint2 raw = *ptr;
+        const float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&raw.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&raw.y));
+        float x[4] = {a.x, a.y, b.x, b.y}, ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (key) x[e] = pro_silu(x[e]);
+            ss = fmaf(x[e], x[e], ss);
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+        const float inv = pro_inv_norm(ss);
+        __nv_bfloat162 lo = __floats2bfloat162_rn(x[0] * inv, x[1] * inv);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(x[2] * inv, x[3] * inv);
+        raw.x = *reinterpret_cast<uint32_t *>(&lo);
+        raw.y = *reinterpret_cast<uint32_t *>(&hi);
+        *ptr = raw;
+    }
+}
+
 // Per-row betas and log-gates of one chunk (lane = extended row).
 struct RowVals {
     float beta, lg;
 };
 
-template <bool kPacked>
-__device__ __forceinline__ RowVals load_rows(const Params &p, const Job<kPacked> &jb, int c, int lane)
+template <class J>
+__device__ __forceinline__ RowVals load_rows(const Params &p, const J &jb, int c, int lane)
 {
     RowVals v{0.f, 0.f};
     if (c >= jb.chunks(p)) return v;
@@ -524,7 +588,10 @@ __device__ __forceinline__ RowVals load_rows(const Params &p, const Job<kPacked>
     if (lane < R && t < jb.tokens(p)) {   // rows past the sequence's end: beta = 0, exact no-ops
         const size_t tok = tok_row(p, jb, t);
         v.beta = __bfloat162float(p.beta[tok * nh + j]);
-        if (p.g != nullptr && j == 0) v.lg = fmaxf(logf(__bfloat162float(p.g[tok])), -80.f);
+        if (J::kPro) v.beta = pro_beta(v.beta, p.prologue);
+        if (p.g != nullptr && j == 0)
+            v.lg = J::kPro ? pro_log_gate(__bfloat162float(p.g[tok]), p.prologue)
+                           : fmaxf(logf(__bfloat162float(p.g[tok])), -80.f);
     }
     return v;
 }
@@ -740,8 +807,8 @@ __device__ bool phase_b(const Smem &s, const Params &p, uint32_t tbase, uint8_t 
 }
 
 // Prep group g of the state-pass kernel: chunks g, g + 2, ...
-template <bool kSplit, bool kPacked>
-__device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g, const Job<kPacked> &jb)
+template <bool kSplit, class J>
+__device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g, const J &jb)
 {
     const int lt = threadIdx.x - (kPrepWarp + 8 * g) * 32, lw = lt >> 5, lane = lt & 31;
     const uint32_t bar_id = 1 + g;
@@ -754,6 +821,7 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
             const uint8_t *kq = s.stage(st), *rec = kq + kStageIn;
             const bool ok = (lt != 0) || wait_bar(s, kBarFull + st, (c / kNS) & 1, p.status);
             if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) break;
+            // (with a key/query prologue the stage's K and Q arrive mapped, from the record)
             if (!phase_b(s, p, tbase, gt, kq, (const float *)(rec + kRecP), kC,
                          (const float *)(rec + kRecL), c, g, lt, bar_id))
                 break;
@@ -774,6 +842,14 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
         if (lw == 0) {
             scan_rows(rv, lane, w.beta_s, w.L_s);
             rv = load_rows(p, jb, c + 2, lane);          // next chunk of this group
+        }
+        if (J::kPro) {   // the prologue on the stage, before the Gram MMA reads it
+            const bool okf = (lt != 0) || wait_bar(s, kBarFull + st, (c / kNS) & 1, p.status);
+            if (group_any(bar_id, kPrepThreads, !okf || *s.abort)) break;
+            normalise_rows(const_cast<uint8_t *>(kq), p.ct * p.nh, p.ct, p.prologue, lt, kPrepThreads);
+            fence_proxy_async_smem();
+            named_sync(bar_id, kPrepThreads);
+            if (lt == 0) mbar_arrive(&s.bar[kBarNorm + g]);
         }
         // one thread polls the mbarriers; the group barrier spreads the outcome
         bool ok = true;
@@ -796,8 +872,8 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
 }
 
 // ------------------------------------------------------------------ epilogue
-template <typename TOut, bool kPacked>
-__device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, const Job<kPacked> &jb)
+template <typename TOut, class J>
+__device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, const J &jb)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t bar_id = 3;
@@ -839,8 +915,10 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, const J
         if (gated) {
             // Gamma_C: product of the chunk's token gates (log domain, clamped)
             float lg = 0.f;
-            if (lane < p.ct && t0 + lane < jb.tokens(p))
-                lg = fmaxf(logf(__bfloat162float(p.g[tok_row(p, jb, t0 + lane)])), -80.f);
+            if (lane < p.ct && t0 + lane < jb.tokens(p)) {
+                const float x = __bfloat162float(p.g[tok_row(p, jb, t0 + lane)]);
+                lg = J::kPro ? pro_log_gate(x, p.prologue) : fmaxf(logf(x), -80.f);
+            }
 #pragma unroll
             for (int d = 16; d > 0; d >>= 1) lg += __shfl_xor_sync(0xffffffffu, lg, d);
             const float gC = __expf(lg);
@@ -893,7 +971,7 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, const J
 }
 
 // ------------------------------------------------------------------ state-pass kernel
-template <typename TOut, bool kSplit, bool kCoop, bool kPacked>
+template <typename TOut, bool kSplit, bool kCoop, bool kPacked, bool kPro>
 __device__ __forceinline__ void state_pass_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                                const CUtensorMap &tm_q, const Params &p, int bh)
 {
@@ -910,7 +988,7 @@ __device__ __forceinline__ void state_pass_cta(const CUtensorMap &tm_k, const CU
     s.scratch_off = Lay::kOffScratch;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // a sequence with bad packed offsets runs no chunk
-    const Job<kPacked> jb = make_job<kPacked>(p, bh);
+    const Job<kPacked, kPro> jb = make_job<kPacked, kPro>(p, bh);
     if (kPacked && threadIdx.x == 0 && !jb.ok()) report_bad_sequence(p.status);
 
     // Zero every tile once: rows TMA never writes (padding rows, query rows
@@ -936,27 +1014,27 @@ __device__ __forceinline__ void state_pass_cta(const CUtensorMap &tm_k, const CU
     const uint32_t tbase = *s.tmem_slot;
 
     if (warp < kPrepWarp) {
-        epi_role<TOut, kPacked>(s, p, tbase, jb);
+        epi_role<TOut>(s, p, tbase, jb);
     } else if (warp < kTmaWarp) {
-        prep_role<kSplit, kPacked>(s, p, tbase, (warp - kPrepWarp) >> 3, jb);
+        prep_role<kSplit>(s, p, tbase, (warp - kPrepWarp) >> 3, jb);
     } else if (warp == kTmaWarp) {
-        if (lane == 0) tma_role<kSplit, kCoop, kPacked>(s, p, &tm_k, &tm_v, &tm_q, jb);
+        if (lane == 0) tma_role<kSplit, kCoop>(s, p, &tm_k, &tm_v, &tm_q, jb);
     } else if (warp == kChainWarp) {
         if (lane == 0) chain_role(s, p, tbase, jb.chunks(p));
     } else {
-        if (lane == 0) prep_mma_role<kSplit>(s, p, tbase, jb.chunks(p));
+        if (lane == 0) prep_mma_role<kSplit, kPro>(s, p, tbase, jb.chunks(p));
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
-template <typename TOut, bool kSplit, bool kPacked>
+template <typename TOut, bool kSplit, bool kPacked, bool kPro>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 const __grid_constant__ CUtensorMap tm_q, const Params p)
 {
-    state_pass_cta<TOut, kSplit, false, kPacked>(tm_k, tm_v, tm_q, p, blockIdx.x);
+    state_pass_cta<TOut, kSplit, false, kPacked, kPro>(tm_k, tm_v, tm_q, p, blockIdx.x);
 }
 
 // ------------------------------------------------------------------ prep kernel
@@ -967,11 +1045,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 // chunk's record, then P, beta and L. `bars` = [loads, Gram MMA], used at
 // phase `parity`. Returns false, uniformly over the group, after a timeout
 // (the group's loads and MMA drained first).
-template <bool kPacked>
+template <class J>
 __device__ bool prep_chunk(const Params &p, const CUtensorMap *tk, const CUtensorMap *tq,
                            uint8_t *stage, const PrepScratch &w, uint64_t *bars, uint32_t parity,
                            volatile uint32_t *abort, uint32_t tbase, uint32_t gq_col, int lt,
-                           uint32_t bar_id, const Job<kPacked> &jb, int c)
+                           uint32_t bar_id, const J &jb, int c)
 {
     const int lane = lt & 31, ct = p.ct, R = ct * p.nh;
     if (lt == 0) {
@@ -984,6 +1062,27 @@ __device__ bool prep_chunk(const Params &p, const CUtensorMap *tk, const CUtenso
         }
     }
     if (lt < 32) scan_rows(load_rows(p, jb, c, lane), lane, w.beta_s, w.L_s);
+    if (J::kPro) {   // the prologue on the tiles, before the Gram MMA reads them
+        bool landed = (lt != 0) || mbar_wait(&bars[0], parity, kWaitTries, abort);
+        if (group_any(bar_id, kPrepThreads, !landed || *abort)) {
+            if (lt == 0) {
+                flag_error(p.status, abort, kDevTimeout);
+                uint32_t no_abort = 0;   // the loads may still be in flight
+                mbar_wait(&bars[0], parity, kWaitTries, &no_abort);
+            }
+            return false;
+        }
+        normalise_rows(stage, R, ct, p.prologue, lt, kPrepThreads);
+        fence_proxy_async_smem();
+        named_sync(bar_id, kPrepThreads);
+        if (kq_in_record(p.prologue)) {   // the mapped rows, for the state pass
+            uint8_t *dst = p.rec + rec_index(p, jb, c) * p.rec_stride + kRecKQ;
+            for (uint32_t i = lt * 16; i < kRecKQBytes; i += kPrepThreads * 16) {
+                const uint32_t kb = i / kRecKQBlock, off = i - kb * kRecKQBlock;
+                *(uint4 *)(dst + i) = *(const uint4 *)(stage + kb * kKQBlock + off);
+            }
+        }
+    }
     bool ok = true;
     if (lt == 0) {
         bool issued = false;
@@ -1006,7 +1105,7 @@ __device__ bool prep_chunk(const Params &p, const CUtensorMap *tk, const CUtenso
     }
     if (group_any(bar_id, kPrepThreads, !ok || *abort)) return false;
     tc_fence_after();
-    uint8_t *rec = p.rec + rec_index(p, jb, c) * kRecBytes;
+    uint8_t *rec = p.rec + rec_index(p, jb, c) * p.rec_stride;
     phase_a(w, tbase, gq_col, rec + kRecT, lt, p.nh, ct, p.g != nullptr, bar_id);
     float *rp = (float *)(rec + kRecP);
     for (int i = lt; i < kNQ * kC; i += kPrepThreads) rp[i] = w.Ps[(i >> 5) * kLd + (i & 31)];
@@ -1027,7 +1126,7 @@ constexpr uint32_t kPKBar = kPKScratch + kPrepScratch;
 constexpr uint32_t kPKSmem = kPKBar + 2 * 8 + 16 + 1024;
 constexpr uint32_t kPKTmemCols = 32;
 
-template <bool kPacked>
+template <bool kPacked, bool kPro>
 __global__ void __launch_bounds__(kPrepKThreads, 4)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                   const Params p)
@@ -1039,7 +1138,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     volatile uint32_t *abort = tmem_slot + 1;
     const int lt = threadIdx.x, warp = lt >> 5;
     const int c = blockIdx.x % p.n_chunks;
-    const Job<kPacked> jb = make_job<kPacked>(p, blockIdx.x / p.n_chunks);
+    const Job<kPacked, kPro> jb = make_job<kPacked, kPro>(p, blockIdx.x / p.n_chunks);
     if (c >= jb.chunks(p)) return;   // past the sequence's end (packed calls), or a bad sequence
 
     // rows TMA does not write (padding, queries beyond the chunk) stay zero
@@ -1075,7 +1174,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 // finish advances the generation, so flags of earlier launches never match.
 constexpr uint32_t kCoopScratch = (kPrepScratch + 127) & ~127u;
 
-template <bool kPacked>
+template <bool kPacked, bool kPro>
 __device__ void prep_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const Params &p, int pcta,
                          int n_pcta)
 {
@@ -1112,7 +1211,7 @@ __device__ void prep_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const
         uint32_t k = 0;   // chunks prepared by this group: the phase of its barriers
         for (int idx = pcta * 2 + gi; idx < total; idx += n_pcta * 2) {
             const int c = idx / p.bh_count;
-            const Job<kPacked> jb = make_job<kPacked>(p, idx - c * p.bh_count);
+            const Job<kPacked, kPro> jb = make_job<kPacked, kPro>(p, idx - c * p.bh_count);
             if (c >= jb.chunks(p)) continue;   // past the sequence's end (packed calls): nobody waits for it
             if (!prep_chunk(p, &tm_k, &tm_q, base + gi * kStg, w, bar + 2 * gi, k & 1, abort, tbase,
                             gi * 32, lt, 1 + gi, jb, c))
@@ -1129,15 +1228,15 @@ __device__ void prep_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const
     if (warp == 0) tmem_dealloc(tbase, 64);
 }
 
-template <typename TOut, bool kPacked>
+template <typename TOut, bool kPacked, bool kPro>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_coop_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_q, const Params p)
 {
     if ((int)blockIdx.x < p.bh_count)
-        state_pass_cta<TOut, true, true, kPacked>(tm_k, tm_v, tm_q, p, blockIdx.x);
+        state_pass_cta<TOut, true, true, kPacked, kPro>(tm_k, tm_v, tm_q, p, blockIdx.x);
     else
-        prep_cta<kPacked>(tm_k, tm_q, p, blockIdx.x - p.bh_count, gridDim.x - p.bh_count);
+        prep_cta<kPacked, kPro>(tm_k, tm_q, p, blockIdx.x - p.bh_count, gridDim.x - p.bh_count);
     // every thread of this CTA is done (the role ended with a CTA barrier)
     if (threadIdx.x == 0) {
         __threadfence();
@@ -1175,10 +1274,36 @@ size_t n_chunks_total(const Problem &p) { return (size_t)p.B * p.H * chunks_per_
 size_t chunk_tc_records_bytes(const Problem &p)
 {
     const size_t n = n_chunks_total(p);
-    return n ? round256(n * kRecBytes) + round256(n * 4) + 256 : 0;
+    return n ? round256(n * record_stride(p.prologue)) + round256(n * 4) + 256 : 0;
 }
 
 namespace {
+// The kernel instantiation for a problem: output type, mode, packed
+// offsets, input prologue.
+template <typename TOut, bool kSplit>
+auto tc_kernel_mode(bool packed, bool pro)
+{
+    return packed ? (pro ? chunk_tc_kernel<TOut, kSplit, true, true> : chunk_tc_kernel<TOut, kSplit, true, false>)
+                  : (pro ? chunk_tc_kernel<TOut, kSplit, false, true> : chunk_tc_kernel<TOut, kSplit, false, false>);
+}
+template <typename TOut>
+auto tc_kernel_for(bool split, bool packed, bool pro)
+{
+    return split ? tc_kernel_mode<TOut, true>(packed, pro) : tc_kernel_mode<TOut, false>(packed, pro);
+}
+template <typename TOut>
+auto coop_kernel_typed(bool packed, bool pro)
+{
+    return packed ? (pro ? chunk_coop_kernel<TOut, true, true> : chunk_coop_kernel<TOut, true, false>)
+                  : (pro ? chunk_coop_kernel<TOut, false, true> : chunk_coop_kernel<TOut, false, false>);
+}
+auto coop_kernel_for(const Problem &p)
+{
+    const bool packed = p.cu != nullptr, pro = p.prologue != 0;
+    return p.out_dtype == DP_F32 ? coop_kernel_typed<float>(packed, pro)
+                                 : coop_kernel_typed<__nv_bfloat16>(packed, pro);
+}
+
 // Grid of the cooperative launch (state-pass CTAs + prep CTAs), or 0 when
 // this problem and device do not take it.
 cudaError_t coop_grid(const Problem &p, long long *grid)
@@ -1187,9 +1312,7 @@ cudaError_t coop_grid(const Problem &p, long long *grid)
     const size_t n_total = n_chunks_total(p);
     if (n_total == 0 || p.scratch_bytes < chunk_tc_records_bytes(p)) return cudaSuccess;
     int dev = 0, sms = 0, coop = 0, per_sm = 0;
-    const bool f32 = p.out_dtype == DP_F32, packed = p.cu != nullptr;
-    auto kernel = f32 ? (packed ? chunk_coop_kernel<float, true> : chunk_coop_kernel<float, false>)
-                      : (packed ? chunk_coop_kernel<__nv_bfloat16, true> : chunk_coop_kernel<__nv_bfloat16, false>);
+    auto kernel = coop_kernel_for(p);
     const uint32_t smem = smem_bytes<true>();
     cudaError_t e;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
@@ -1215,7 +1338,7 @@ cudaError_t chunk_tc_path(const Problem &p, int *path)
     const size_t n_total = n_chunks_total(p);
     if (grid > 0)
         *path = DP_PATH_CHUNK_COOP;
-    else if (n_total > 0 && p.scratch_bytes >= round256(n_total * kRecBytes))
+    else if (n_total > 0 && p.scratch_bytes >= round256(n_total * record_stride(p.prologue)))
         *path = DP_PATH_CHUNK_SPLIT;
     else
         *path = DP_PATH_CHUNK_FUSED;
@@ -1255,22 +1378,21 @@ cudaError_t launch_chunk_tc(const Problem &p)
     pr.nh = nh;
     pr.ct = ct;
     pr.max_T = p.max_T;
+    pr.prologue = p.prologue;
+    pr.rec_stride = record_stride(p.prologue);
     pr.n_chunks = (int)chunks_per_seq(p);
 
     // split whenever the workspace holds every chunk's record; cooperative
     // (one launch) when it also holds the flags and the heads leave at least
     // as many SMs for the prep CTAs as the state pass takes
     const size_t n_total = n_chunks_total(p);
-    const size_t rec_bytes = round256(n_total * kRecBytes);
+    const size_t rec_bytes = round256(n_total * record_stride(p.prologue));
     const bool split = p.scratch != nullptr && n_total > 0 && p.scratch_bytes >= rec_bytes;
     cudaError_t e;
     long long grid = 0;
     if (split && (e = coop_grid(p, &grid)) != cudaSuccess) return e;
     if (grid > 0) {
-        const bool packed = p.cu != nullptr;
-        auto kernel = p.out_dtype == DP_F32
-                          ? (packed ? chunk_coop_kernel<float, true> : chunk_coop_kernel<float, false>)
-                          : (packed ? chunk_coop_kernel<__nv_bfloat16, true> : chunk_coop_kernel<__nv_bfloat16, false>);
+        auto kernel = coop_kernel_for(p);
         pr.flags = (uint32_t *)((uint8_t *)p.scratch + rec_bytes);
         pr.sync = (uint32_t *)((uint8_t *)pr.flags + round256(n_total * 4));
         void *args[] = {(void *)&tk, (void *)&tv, (void *)&tq, (void *)&pr};
@@ -1279,9 +1401,10 @@ cudaError_t launch_chunk_tc(const Problem &p)
         if (e == cudaSuccess) return cudaSuccess;
         cudaGetLastError();   // not launchable together here: two launches instead
     }
-    const bool packed = p.cu != nullptr;
+    const bool packed = p.cu != nullptr, pro = p.prologue != 0;
     if (split) {
-        auto prep = packed ? chunk_prep_kernel<true> : chunk_prep_kernel<false>;
+        auto prep = packed ? (pro ? chunk_prep_kernel<true, true> : chunk_prep_kernel<true, false>)
+                           : (pro ? chunk_prep_kernel<false, true> : chunk_prep_kernel<false, false>);
         e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPKSmem);
         if (e != cudaSuccess) return e;
         const size_t n_ctas = (size_t)p.B * p.H * pr.n_chunks;
@@ -1289,13 +1412,8 @@ cudaError_t launch_chunk_tc(const Problem &p)
         prep<<<(unsigned)n_ctas, kPrepKThreads, kPKSmem, p.stream>>>(tk, tq, pr);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    auto kernel = p.out_dtype == DP_F32
-                      ? (split ? (packed ? chunk_tc_kernel<float, true, true> : chunk_tc_kernel<float, true, false>)
-                               : (packed ? chunk_tc_kernel<float, false, true> : chunk_tc_kernel<float, false, false>))
-                      : (split ? (packed ? chunk_tc_kernel<__nv_bfloat16, true, true>
-                                         : chunk_tc_kernel<__nv_bfloat16, true, false>)
-                               : (packed ? chunk_tc_kernel<__nv_bfloat16, false, true>
-                                         : chunk_tc_kernel<__nv_bfloat16, false, false>));
+    auto kernel = p.out_dtype == DP_F32 ? tc_kernel_for<float>(split, packed, pro)
+                                        : tc_kernel_for<__nv_bfloat16>(split, packed, pro);
     const uint32_t smem = split ? smem_bytes<true>() : smem_bytes<false>();
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

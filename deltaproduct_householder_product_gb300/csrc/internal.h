@@ -22,6 +22,7 @@ struct Problem {
     uint32_t *status;          // device status word (may be NULL for decode)
     const int *cu;             // packed sequences: int32 [B+1] token offsets (NULL: dense [B,T] layout)
     int max_T;                 // longest sequence (T for dense calls)
+    int prologue;              // dp_prologue_flags applied to the inputs on load
     void *scratch;             // workspace bytes after the status block
     size_t scratch_bytes;
     cudaStream_t stream;
@@ -65,6 +66,34 @@ cudaError_t launch_backward(const BwdProblem &p);
 cudaError_t launch_state_io(int op, int B, int H, int Dk, int Dv, float *state,
                             void *ext, int ext_dtype, int ext_transposed,
                             cudaStream_t stream);
+
+// Standalone input prologue (dp_prologue), dense layouts.
+cudaError_t launch_prologue(const Problem &p, void *q_out, void *k_out, void *beta_out, void *g_out);
+
+// ---- input prologue maps (dp_prologue_flags), fp32, shared by every kernel
+__device__ __forceinline__ float pro_sigmoid(float x) { return 1.f / (1.f + expf(-x)); }
+// Key rows: SiLU and the reciprocal norm with the hardware approximations
+// (relative error ~1e-6, far below the bf16 rounding the mapped rows get as
+// tensor-core operands); the maps sit next to the chunk kernel's MMA chain.
+__device__ __forceinline__ float pro_silu(float x) { return __fdividef(x, 1.f + __expf(-x)); }
+__device__ __forceinline__ float pro_inv_norm(float ss) { return ss > 0.f ? rsqrtf(ss) : 0.f; }
+__device__ __forceinline__ float pro_beta(float x, int flags)
+{
+    if (flags & DP_PRO_BETA_SIGMOID) return pro_sigmoid(x);
+    if (flags & DP_PRO_BETA_2SIGMOID) return 2.f * pro_sigmoid(x);
+    return x;
+}
+__device__ __forceinline__ float pro_gate(float x, int flags)
+{
+    return (flags & DP_PRO_GATE_SIGMOID) ? pro_sigmoid(x) : x;
+}
+// log of the gate, clamped at -80 (e^-80 stands in for a gate of 0); with
+// the sigmoid map, log sigmoid(x) = -softplus(-x) without forming sigmoid(x)
+__device__ __forceinline__ float pro_log_gate(float x, int flags)
+{
+    if (flags & DP_PRO_GATE_SIGMOID) return fmaxf(-(fmaxf(-x, 0.f) + log1pf(expf(-fabsf(x)))), -80.f);
+    return fmaxf(logf(x), -80.f);
+}
 
 // Device status codes written into the status word (first one wins).
 enum : uint32_t { kDevOk = 0, kDevTimeout = 1, kDevBadState = 2 };

@@ -27,11 +27,17 @@ constexpr int kCols = 32;
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ void from_f(float *p, float x) { *p = x; }
+// x rounded to T's precision (the identity for float)
+template <typename T> __device__ __forceinline__ float round_to(float x) { return x; }
+template <> __device__ __forceinline__ float round_to<__nv_bfloat16>(float x)
+{
+    return __bfloat162float(__float2bfloat16_rn(x));
+}
 __device__ __forceinline__ void from_f(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
 
 template <int DK, typename TIn, typename TOut>
 __global__ void __launch_bounds__(kWarps * 32)
-recurrent_kernel(int T, int H, int Dv, int nh, const int *cu, int N, int max_T, uint32_t *status,
+recurrent_kernel(int T, int H, int Dv, int nh, const int *cu, int N, int max_T, int pro, uint32_t *status,
                  const TIn *__restrict__ q, const TIn *__restrict__ k,
                  const TIn *__restrict__ v, const TIn *__restrict__ beta,
                  const TIn *__restrict__ g, const float *h0, TOut *__restrict__ o,
@@ -40,6 +46,7 @@ recurrent_kernel(int T, int H, int Dv, int nh, const int *cu, int N, int max_T, 
     constexpr int R = DK / kWarps;            // key rows per warp
     __shared__ float kbuf[2][DK];
     __shared__ float part[2][kWarps][kCols];
+    __shared__ float nred[2][kWarps];   // prologue: partial sums of squares
 
     const int bh = blockIdx.x;                // b * H + h
     const int b = bh / H, h = bh - b * H;
@@ -62,14 +69,34 @@ recurrent_kernel(int T, int H, int Dv, int nh, const int *cu, int N, int max_T, 
     for (int t = 0; t < sq.len; ++t) {
         const size_t tok = ((size_t)sq.b_map * T + sq.t0 + t) * H + h;
         if (g) {
-            const float gt = to_f(g[tok]);
+            const float gt = pro_gate(to_f(g[tok]), pro);
 #pragma unroll
             for (int r = 0; r < R; ++r) S[r] *= gt;
         }
         for (int j = 0; j <= nh; ++j) {
             // j < nh: one Householder step with key k_{t,j}; j == nh: readout with q_t
             const TIn *x = (j < nh) ? k + (tok * nh + j) * DK : q + tok * DK;
-            for (int i = threadIdx.x; i < DK; i += kWarps * 32) kbuf[buf][i] = to_f(x[i]);
+            // prologue: SiLU + L2 normalisation of keys, L2 of queries, each
+            // rounded to the input dtype like a given input (DK <= threads)
+            const bool silu = j < nh && (pro & DP_PRO_KEY_SILU_L2);
+            const bool norm = silu || (j == nh && (pro & DP_PRO_QUERY_L2));
+            float xv = 0.f;
+            if (threadIdx.x < DK) {
+                xv = to_f(x[threadIdx.x]);
+                if (silu) xv = pro_silu(xv);
+            }
+            if (norm) {
+                float ss = xv * xv;
+#pragma unroll
+                for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+                if (lane == 0) nred[buf][w] = ss;
+                __syncthreads();
+                float tot = 0.f;
+#pragma unroll
+                for (int i = 0; i < kWarps; ++i) tot += nred[buf][i];
+                xv = round_to<TIn>(xv * pro_inv_norm(tot));
+            }
+            if (threadIdx.x < DK) kbuf[buf][threadIdx.x] = xv;
             __syncthreads();
             float acc = 0.f;
 #pragma unroll
@@ -81,7 +108,7 @@ recurrent_kernel(int T, int H, int Dv, int nh, const int *cu, int N, int max_T, 
             for (int i = 0; i < kWarps; ++i) hx += part[buf][i][lane];
             if (j < nh) {
                 const float vj = to_f(v[(tok * nh + j) * Dv + col]);
-                const float bj = to_f(beta[tok * nh + j]);
+                const float bj = pro_beta(to_f(beta[tok * nh + j]), pro);
                 const float e = bj * (vj - hx);
 #pragma unroll
                 for (int r = 0; r < R; ++r) S[r] = fmaf(kbuf[buf][row0 + r], e, S[r]);
@@ -108,15 +135,15 @@ cudaError_t launch_typed(const Problem &p)
     switch (p.Dk) {
     case 32:
         recurrent_kernel<32, TIn, TOut><<<grid, block, 0, p.stream>>>(
-            p.T, p.H, p.Dv, p.nh, p.cu, p.B, p.max_T, p.status, q, k, v, be, g, p.h0, o, p.h_final);
+            p.T, p.H, p.Dv, p.nh, p.cu, p.B, p.max_T, p.prologue, p.status, q, k, v, be, g, p.h0, o, p.h_final);
         break;
     case 64:
         recurrent_kernel<64, TIn, TOut><<<grid, block, 0, p.stream>>>(
-            p.T, p.H, p.Dv, p.nh, p.cu, p.B, p.max_T, p.status, q, k, v, be, g, p.h0, o, p.h_final);
+            p.T, p.H, p.Dv, p.nh, p.cu, p.B, p.max_T, p.prologue, p.status, q, k, v, be, g, p.h0, o, p.h_final);
         break;
     default:
         recurrent_kernel<128, TIn, TOut><<<grid, block, 0, p.stream>>>(
-            p.T, p.H, p.Dv, p.nh, p.cu, p.B, p.max_T, p.status, q, k, v, be, g, p.h0, o, p.h_final);
+            p.T, p.H, p.Dv, p.nh, p.cu, p.B, p.max_T, p.prologue, p.status, q, k, v, be, g, p.h0, o, p.h_final);
         break;
     }
     return cudaGetLastError();

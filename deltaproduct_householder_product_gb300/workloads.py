@@ -97,6 +97,37 @@ def make_inputs(w: Workload):
     return out
 
 
+# dp_prologue_flags values (include/dp.h)
+PRO_KEY_SILU_L2, PRO_QUERY_L2, PRO_BETA_SIGMOID, PRO_BETA_2SIGMOID, PRO_GATE_SIGMOID = 1, 2, 4, 8, 16
+
+
+def prologue_flags(w: Workload):
+    """The prologue that maps ``make_raw_inputs(w)`` to the recipe's inputs."""
+    f = PRO_KEY_SILU_L2 | PRO_QUERY_L2 | (PRO_BETA_SIGMOID if w.beta_max == 1.0 else PRO_BETA_2SIGMOID)
+    assert w.beta_max in (1.0, 2.0), w.beta_max
+    return f | (PRO_GATE_SIGMOID if w.gated else 0)
+
+
+def make_raw_inputs(w: Workload):
+    """The draws of ``make_inputs`` before their element-wise maps (raw
+    projections: q, k, beta, g unmapped; v and h0 as in make_inputs), in the
+    same order from the same seed. Near-duplicate keys are a property of
+    mapped keys and are not produced here."""
+    assert w.near_dup_frac == 0, "near-duplicate keys have no raw form"
+    gen = torch.Generator().manual_seed(w.seed)
+    B, T, H, nh, Dk, Dv = w.B, w.T, w.H, w.nh, w.Dk, w.Dv
+    q = torch.randn(B, T, H, Dk, generator=gen)
+    k = torch.randn(B, T, H, nh, Dk, generator=gen)
+    v = torch.randn(B, T, H, nh, Dv, generator=gen)
+    beta = torch.randn(B, T, H, nh, generator=gen)
+    g = (torch.randn(B, T, H, generator=gen) + 3.0) if w.gated else None
+    h0 = (w.h0_std * torch.randn(B, H, Dk, Dv, generator=gen)) if w.h0_std > 0 else None
+    dt = w.torch_dtype
+    return dict(q=q.to(dt).contiguous(), k=k.to(dt).contiguous(), v=v.to(dt).contiguous(),
+                beta=beta.to(dt).contiguous(), g=None if g is None else g.to(dt).contiguous(),
+                h0=None if h0 is None else h0.float().contiguous())
+
+
 def make_decode_inputs(w: Workload, steps: int, seed: int = LONG_DECODE_SEED):
     """Fresh per-step inputs for ``steps`` decode calls: leading dim = step.
 

@@ -75,10 +75,28 @@ typedef struct {
     int out_dtype;   /* dp_dtype of o: equal to dtype, or DP_F32 with bf16 inputs */
     int max_seqlen;  /* dp_forward_varlen: the longest packed sequence (bounds the
                         workspace); 0 for every other call */
+    int prologue;    /* dp_prologue_flags applied to the inputs as they are loaded
+                        (dp_forward, dp_forward_varlen, dp_decode_step,
+                        dp_forward_noalloc); 0 = inputs used as given */
 } dp_dims;
 
+/* Input prologue (DeltaProduct paper, Sec.4: keys are psi(W x) / ||psi(W x)||
+ * with psi = SiLU, betas phi(U x) with phi = sigmoid or 2 sigmoid; the gated
+ * variant's gate is a sigmoid). With a flag set, the corresponding input
+ * holds the raw projection and the kernels apply the map while loading it,
+ * in fp32: the normalised keys and queries are then rounded to the input
+ * dtype (they are tensor-core operands), betas and gates stay fp32.
+ * BETA_SIGMOID and BETA_2SIGMOID are exclusive. */
+typedef enum {
+    DP_PRO_KEY_SILU_L2 = 1,    /* k <- SiLU(k) / ||SiLU(k)||_2 (a zero row stays zero) */
+    DP_PRO_QUERY_L2 = 2,       /* q <- q / ||q||_2 */
+    DP_PRO_BETA_SIGMOID = 4,   /* beta <- sigmoid(beta) */
+    DP_PRO_BETA_2SIGMOID = 8,  /* beta <- 2 sigmoid(beta) */
+    DP_PRO_GATE_SIGMOID = 16   /* g <- sigmoid(g) */
+} dp_prologue_flags;
+
 /* ABI version of this header (bumped on any signature change). */
-#define DP_ABI_VERSION 5
+#define DP_ABI_VERSION 6
 int dp_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -193,6 +211,18 @@ dp_status dp_backward(const dp_dims *dims,
                       const void *d_o, const float *dh_final,
                       float *dq, float *dk, float *dv, float *dbeta, float *dg,
                       float *dh0, void *workspace, size_t workspace_bytes,
+                      dp_stream_t stream);
+
+/* The prologue on its own (the unfused form): reads the raw q, k, beta, g
+ * of a dense problem (dims->prologue selects the maps; layouts as in
+ * dp_forward) and writes the mapped tensors to q_out, k_out, beta_out,
+ * g_out in the input dtype. Outputs whose flag is clear are not written
+ * (their pointer may be NULL); g and g_out are ignored without
+ * DP_PRO_GATE_SIGMOID. dp_forward with dims->prologue = 0 on the outputs
+ * computes what dp_forward with the flags computes on the raw inputs, up to
+ * rounding (here betas and gates are rounded to the input dtype). */
+dp_status dp_prologue(const dp_dims *dims, const void *q, const void *k, const void *beta,
+                      const void *g, void *q_out, void *k_out, void *beta_out, void *g_out,
                       dp_stream_t stream);
 
 /* Synchronises `stream`, returns the status the device recorded in the

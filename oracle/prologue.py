@@ -61,10 +61,27 @@ def apply(flags, q, k, beta, g=None):
     return q, k, beta, g
 
 
-def forward(flags, q, k, v, beta, g=None, h0=None, threads=None):
-    """The prologue, then the sequential recurrence (``oracle.forward``)."""
+def round_bf16(x):
+    """Round to the nearest bfloat16 (ties to even), returned as fp64."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float64)).to(torch.bfloat16).double().numpy()
+
+
+def forward(flags, q, k, v, beta, g=None, h0=None, threads=None, operand_dtype=None):
+    """The prologue, then the sequential recurrence (``oracle.forward``).
+
+    ``operand_dtype="bf16"``: the mapped keys and queries are rounded to
+    bfloat16 before the recurrence, as the library states for bf16 inputs
+    (they are tensor-core operands); betas and gates stay exact."""
     from . import forward as recurrence
     q2, k2, b2, g2 = apply(flags, _f64(q), _f64(k), _f64(beta), None if g is None else _f64(g))
+    if operand_dtype == "bf16":
+        if flags & KEY_SILU_L2:
+            k2 = round_bf16(k2)
+        if flags & QUERY_L2:
+            q2 = round_bf16(q2)
+    elif operand_dtype is not None:
+        raise ValueError(operand_dtype)
     return recurrence(q2, k2, v, b2, g2, h0, threads=threads)
 
 

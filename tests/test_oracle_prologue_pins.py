@@ -56,3 +56,11 @@ def test_prologue_then_recurrence():
     o2, hf2 = oracle.forward(qn, kn, v, 2 / (1 + np.exp(-b)), 1 / (1 + np.exp(-g)), None, threads=1)
     np.testing.assert_allclose(o, o2, rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(hf, hf2, rtol=1e-12, atol=1e-12)
+
+
+def test_bf16_operand_rounding():
+    """round_bf16 is round-to-nearest-even onto bfloat16's grid: exact on
+    representable values, half-way cases to the even neighbour."""
+    one_ulp = 2.0 ** -7                        # bf16 spacing in [1, 2)
+    xs = np.array([1.0, 1.0 + one_ulp, 1.0 + one_ulp / 2, 1.0 + 1.5 * one_ulp, 1.0 + 0.3 * one_ulp])
+    np.testing.assert_array_equal(P.round_bf16(xs), [1.0, 1.0 + one_ulp, 1.0, 1.0 + 2 * one_ulp, 1.0])
