@@ -11,6 +11,9 @@ Three independent restatements live here:
   pseudocode (Sec.4, Appendix B.1).
 * ``backward`` -- reverse-mode gradients of that recurrence in C (the chain
   rule applied to each sub-step, readout and gate, in reverse token order).
+* ``osdn`` -- the OSDN write-key variant: the phase-1 preconditioner scan
+  (d-scan, optional APF retention) that emits the write keys k~ = d (.) k,
+  then the recurrence above writing along k~.
 * ``prologue`` -- the element-wise input maps of Sec.4 (SiLU and L2
   normalisation of keys, sigmoid / 2 sigmoid betas, sigmoid gates) applied
   to raw projections, in numpy fp64.
@@ -44,6 +47,8 @@ def _lib():
         lib.oracle_forward.argtypes = [ctypes.c_int] * 6 + [dp] * 8 + [ctypes.c_int]
         lib.oracle_forward.restype = ctypes.c_int
         lib.oracle_backward.argtypes = [ctypes.c_int] * 6 + [dp] * 14 + [ctypes.c_int]
+        lib.oracle_forward_wk.argtypes = [ctypes.c_int] * 6 + [dp] * 9 + [ctypes.c_int]
+        lib.oracle_forward_wk.restype = ctypes.c_int
         lib.oracle_backward.restype = ctypes.c_int
         _LIB = lib
     return _LIB
@@ -67,15 +72,20 @@ def default_threads():
     return max(1, os.cpu_count() or 1)
 
 
-def forward(q, k, v, beta, g=None, h0=None, threads=None):
+def forward(q, k, v, beta, g=None, h0=None, threads=None, kw=None):
     """Sequential fp64 recurrence. Returns (o [B,T,H,Dv], h_final [B,H,Dk,Dv]).
+
+    ``kw`` [B,T,H,nh,Dk]: write keys (the OSDN variant writes the state along
+    kw while the prediction error still reads with k); None = k.
 
     Shapes: q [B,T,H,Dk], k [B,T,H,nh,Dk], v [B,T,H,nh,Dv], beta [B,T,H,nh],
     g [B,T,H] or None, h0 [B,H,Dk,Dv] or None. Inputs of any float dtype
     (numpy or torch) are upcast exactly to fp64.
     """
-    q, k, v, beta, g, h0 = (_as_f64(x) for x in (q, k, v, beta, g, h0))
+    q, k, v, beta, g, h0, kw = (_as_f64(x) for x in (q, k, v, beta, g, h0, kw))
     B, T, H, nh, Dk = k.shape
+    if kw is not None:
+        assert kw.shape == k.shape, kw.shape
     Dv = v.shape[-1]
     assert q.shape == (B, T, H, Dk), q.shape
     assert v.shape == (B, T, H, nh, Dv), v.shape
@@ -86,9 +96,9 @@ def forward(q, k, v, beta, g=None, h0=None, threads=None):
         assert h0.shape == (B, H, Dk, Dv), h0.shape
     o = np.zeros((B, T, H, Dv), dtype=np.float64)
     hf = np.zeros((B, H, Dk, Dv), dtype=np.float64)
-    rc = _lib().oracle_forward(B, T, H, Dk, Dv, nh, _ptr(q), _ptr(k), _ptr(v),
-                               _ptr(beta), _ptr(g), _ptr(h0), _ptr(o), _ptr(hf),
-                               int(threads or default_threads()))
+    rc = _lib().oracle_forward_wk(B, T, H, Dk, Dv, nh, _ptr(q), _ptr(k), _ptr(kw), _ptr(v),
+                                  _ptr(beta), _ptr(g), _ptr(h0), _ptr(o), _ptr(hf),
+                                  int(threads or default_threads()))
     if rc != 0:
         raise RuntimeError(f"oracle_forward failed with code {rc}")
     return o, hf
@@ -136,4 +146,4 @@ def decode_step(q, k, v, beta, g, state, threads=None):
     return o[:, 0], hf
 
 
-from . import chunkwise, product_form, prologue  # noqa: E402,F401
+from . import chunkwise, osdn, product_form, prologue  # noqa: E402,F401

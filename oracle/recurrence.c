@@ -37,6 +37,7 @@
 typedef struct {
     int B, T, H, Dk, Dv, nh;
     const double *q, *k, *v, *beta, *g, *h0;
+    const double *kw;       /* write keys (OSDN variant), or NULL: write with k */
     double *o, *h_final;
     int next;               /* next (b,h) pair to take; guarded by lock */
     int failed;
@@ -61,6 +62,7 @@ static int run_pair(oracle_job *J, int b, int h, double *S, double *e)
         }
         for (int j = 0; j < nh; ++j) {
             const double *kk = J->k + (tok * nh + j) * (size_t)Dk;
+            const double *kwr = J->kw ? J->kw + (tok * nh + j) * (size_t)Dk : kk;
             const double *vv = J->v + (tok * nh + j) * (size_t)Dv;
             const double bt = J->beta[tok * nh + j];
             /* e = v - H^T k  (accumulated row by row of H) */
@@ -69,9 +71,9 @@ static int run_pair(oracle_job *J, int b, int h, double *S, double *e)
                 const double *row = S + (size_t)r * Dv;
                 for (int c = 0; c < Dv; ++c) e[c] -= row[c] * kk[r];
             }
-            /* H += beta k e^T */
+            /* H += beta k e^T (OSDN: beta k~ e^T, the write key) */
             for (int r = 0; r < Dk; ++r) {
-                const double br = bt * kk[r];
+                const double br = bt * kwr[r];
                 double *row = S + (size_t)r * Dv;
                 for (int c = 0; c < Dv; ++c) row[c] += br * e[c];
             }
@@ -115,17 +117,34 @@ static void *worker(void *arg)
     return NULL;
 }
 
-/* Returns 0 on success, -1 on bad sizes, -2 on allocation/thread failure. */
+/* Returns 0 on success, -1 on bad sizes, -2 on allocation/thread failure.
+ * kw: write keys [B,T,H,nh,Dk] (OSDN, Sec.4.1 / Eq.(5) of the OSDN paper:
+ * the state is written along k~ = d (.) k while the residual still reads
+ * with k), or NULL for the plain recurrence. */
+int oracle_forward_wk(int B, int T, int H, int Dk, int Dv, int nh,
+                      const double *q, const double *k, const double *kw, const double *v,
+                      const double *beta, const double *g, const double *h0,
+                      double *o, double *h_final, int n_threads);
+
 int oracle_forward(int B, int T, int H, int Dk, int Dv, int nh,
                    const double *q, const double *k, const double *v,
                    const double *beta, const double *g, const double *h0,
                    double *o, double *h_final, int n_threads)
+{
+    return oracle_forward_wk(B, T, H, Dk, Dv, nh, q, k, NULL, v, beta, g, h0, o, h_final, n_threads);
+}
+
+int oracle_forward_wk(int B, int T, int H, int Dk, int Dv, int nh,
+                      const double *q, const double *k, const double *kw, const double *v,
+                      const double *beta, const double *g, const double *h0,
+                      double *o, double *h_final, int n_threads)
 {
     if (B < 0 || T < 0 || H < 0 || Dk <= 0 || Dv <= 0 || nh <= 0) return -1;
     if ((B * H > 0) && (!beta || !o || (T > 0 && (!q || !k || !v)))) return -1;
     oracle_job J;
     J.B = B; J.T = T; J.H = H; J.Dk = Dk; J.Dv = Dv; J.nh = nh;
     J.q = q; J.k = k; J.v = v; J.beta = beta; J.g = g; J.h0 = h0;
+    J.kw = kw;
     J.o = o; J.h_final = h_final;
     J.next = 0;
     J.failed = 0;
