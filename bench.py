@@ -56,6 +56,7 @@ def parse():
     ap.add_argument("--no-varlen", action="store_true", help="skip the packed variable-length measurement")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward-pass measurement")
     ap.add_argument("--no-prologue", action="store_true", help="skip the fused-prologue measurement")
+    ap.add_argument("--no-osdn", action="store_true", help="skip the OSDN write-key measurement")
     ap.add_argument("--fused", action="store_true",
                     help="give dp_forward only the minimum workspace: the chunk path then "
                          "runs as one fused kernel instead of prep + state-pass kernels")
@@ -393,6 +394,46 @@ def prologue_measure(dp, dev, hbm_peak, steps=50, warmup=5):
                          "frac": achieved / hbm_peak, "algorithmic_bytes": step_bytes}}
 
 
+def osdn_measure(dp, dev, hbm_peak, steps=10, warmup=2):
+    """OSDN write keys on the bench workload (B4 H8 T2048 n_h 2 D128 bf16,
+    fp32 o): phase 1 (dp_osdn_write_keys: the preconditioner scan, one warp
+    per head) and phase 2 (dp_forward_write_keys on the recurrent kernel),
+    each timed with CUDA events, inputs resident. Roofline of phase 2: the
+    forward's algorithmic bytes plus the write keys read."""
+    w = W.BASE
+    x = {k: (None if v is None else v.to(dev)) for k, v in W.make_inputs(w).items()}
+    o = torch.empty(w.B, w.T, w.H, w.Dv, dtype=torch.float32, device=dev)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        stream = torch.cuda.current_stream()
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+    kw, _ = dp.osdn_write_keys(x["k"], x["beta"])
+    ms1 = timed(lambda: dp.osdn_write_keys(x["k"], x["beta"]))
+    ms2 = timed(lambda: dp.forward_write_keys(x["q"], x["k"], kw, x["v"], x["beta"], x["g"], x["h0"], out=o,
+                                              h_final=False))
+    tok = w.B * w.T * w.H
+    scan_bytes = tok * w.nh * (2 * w.Dk * 2 + 2)                 # k and beta in, k~ out
+    fwd_bytes = W.algorithmic_bytes(w, out_bytes=4) + tok * w.nh * w.Dk * 2
+    a2 = fwd_bytes / (ms2 * 1e-3) / 1e9
+    return {"workload": f"{w.name} OSDN write keys (eta 0.003, d in [0.5, 2])",
+            "ms_scan": ms1, "ms_forward_write_keys": ms2, "tokens_per_s": w.B * w.T / ((ms1 + ms2) * 1e-3),
+            "kernels": "dscan_kernel (one warp per head), recurrent_kernel with write keys",
+            "scan_roofline": {"bound": "hbm", "achieved": scan_bytes / (ms1 * 1e-3) / 1e9, "peak": hbm_peak,
+                              "unit": "GB/s", "frac": scan_bytes / (ms1 * 1e-3) / 1e9 / hbm_peak,
+                              "algorithmic_bytes": scan_bytes},
+            "roofline": {"bound": "hbm", "achieved": a2, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": a2 / hbm_peak, "algorithmic_bytes": fwd_bytes}}
+
+
 VARLEN_LENGTHS = [384, 2944, 1024, 512, 1792, 256, 896, 384]   # 8 sequences, 8192 tokens
 
 
@@ -557,6 +598,8 @@ def ours_arm(args, w):
         line["backward"] = backward_measure(dp, dev, hbm_peak)
     if not args.no_prologue:
         line["prologue"] = prologue_measure(dp, dev, hbm_peak)
+    if not args.no_osdn:
+        line["osdn"] = osdn_measure(dp, dev, hbm_peak)
     if not args.no_cpu_baseline:
         v, desc, cores, _ = oracle_sample(w, x, 8.0, os.cpu_count() or 1)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores,

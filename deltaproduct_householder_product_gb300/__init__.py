@@ -12,7 +12,7 @@ from . import _lib
 from ._lib import DPError, STATE_EXPORT, STATE_IMPORT, STATE_ZERO  # noqa: F401
 
 __all__ = ["forward", "forward_varlen", "forward_noalloc", "forward_path", "supports", "decode_step", "state_io", "check_status",
-           "backward", "prologue", "prologue_flags",
+           "backward", "prologue", "prologue_flags", "osdn_write_keys", "forward_write_keys",
            "workspace_size",
            "DPError", "abi_version"]
 
@@ -273,6 +273,56 @@ def prologue(q, k, beta, g=None, *, flags, stream=None):
                                 _lib._ptr(g_o) if (g is not None and f & 16) else None, _lib._stream(stream))
     _lib._check(rc, "dp_prologue")
     return q_o, k_o, b_o, g_o
+
+
+def osdn_write_keys(k, beta, r=None, d0=None, *, eta=0.003, d_lo=0.5, d_hi=2.0, eps=1e-6, stream=None):
+    """dp_osdn_write_keys (OSDN phase 1): returns (kw, d_final) for keys k
+    [B,T,H,nh,Dk], betas [B,T,H,nh], APF retention r [B,T,H] or None, and
+    the initial preconditioner d0 [B,H,Dk] float32 or None (ones)."""
+    B, T, H, nh, Dk = k.shape
+    dt = k.dtype
+    for name, t in (("k", k), ("beta", beta), ("r", r)):
+        _lib._need_cuda(name, t, dt)
+    _lib._need_cuda("d0", d0, torch.float32)
+    dims = _lib.make_dims(B, T, H, Dk, Dk, nh, dt)
+    kw = torch.empty_like(k)
+    d_final = torch.empty((B, H, Dk), dtype=torch.float32, device=k.device)
+    rc = _lib.lib().dp_osdn_write_keys(dims, _lib._ptr(k), _lib._ptr(beta), _lib._ptr(r), _lib._ptr(d0),
+                                       eta, d_lo, d_hi, eps, _lib._ptr(kw), _lib._ptr(d_final),
+                                       _lib._stream(stream))
+    _lib._check(rc, "dp_osdn_write_keys")
+    return kw, d_final
+
+
+def forward_write_keys(q, k, kw, v, beta, g=None, h0=None, *, out=None, h_final=True, workspace=None,
+                       stream=None, out_dtype=None, prologue=0):
+    """dp_forward_write_keys (OSDN phase 2): ``forward`` with the state
+    written along the write keys kw (layout of k)."""
+    B, T, H, nh, Dk = k.shape
+    Dv = v.shape[-1]
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("kw", kw), ("v", v), ("beta", beta), ("g", g)):
+        _lib._need_cuda(name, t, dt)
+    _lib._need_cuda("h0", h0, torch.float32)
+    if kw.shape != k.shape:
+        raise ValueError("kw must have the shape of k")
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else dt
+    dims = _lib.make_dims(B, T, H, Dk, Dv, nh, dt, "auto", out_dtype, prologue=prologue_flags(prologue))
+    if out is None:
+        out = torch.empty((B, T, H, Dv), dtype=out_dtype, device=q.device)
+    if h_final is True:
+        h_final = torch.empty((B, H, Dk, Dv), dtype=torch.float32, device=q.device)
+    elif h_final is False:
+        h_final = None
+    if workspace is None:
+        workspace = torch.zeros(_lib.workspace_size(dims), dtype=torch.uint8, device=q.device)
+    rc = _lib.lib().dp_forward_write_keys(
+        dims, _lib._ptr(q), _lib._ptr(k), _lib._ptr(kw), _lib._ptr(v), _lib._ptr(beta), _lib._ptr(g),
+        _lib._ptr(h0), _lib._ptr(out), _lib._ptr(h_final), _lib._ptr(workspace),
+        workspace.numel() * workspace.element_size(), _lib._stream(stream))
+    _lib._check(rc, "dp_forward_write_keys")
+    return out, h_final
 
 
 def state_io(op, state, ext=None, transposed=False, stream=None):

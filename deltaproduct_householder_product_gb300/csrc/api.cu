@@ -353,3 +353,56 @@ extern "C" dp_status dp_prologue(const dp_dims *dims, const void *q, const void 
     if ((size_t)p.B * p.T * p.H == 0 || f == 0) return DP_OK;
     return from_cuda(dp::launch_prologue(p, q_out, k_out, beta_out, p.g ? g_out : nullptr));
 }
+
+extern "C" dp_status dp_osdn_write_keys(const dp_dims *dims, const void *k, const void *beta, const void *r,
+                                        const float *d0, float eta, float d_lo, float d_hi, float eps, void *kw,
+                                        float *d_final, dp_stream_t stream)
+{
+    DP_TRY(check_dims(dims, false));
+    if (dims->max_seqlen != 0 || dims->prologue != 0) return DP_ERR_INVALID_ARG;
+    if (!(d_lo > 0.f) || !(d_hi >= d_lo) || !(eps > 0.f) || !(eta >= 0.f)) return DP_ERR_INVALID_ARG;
+    dp::Problem p = make_problem(dims, dims->T);
+    const size_t el = p.dtype == DP_F32 ? 4 : 2;
+    if ((size_t)p.B * p.T * p.H > 0) {
+        DP_TRY(check_ptr(k, 16));
+        DP_TRY(check_ptr(beta, el));
+        DP_TRY(check_ptr(kw, 16));
+        if (r) DP_TRY(check_ptr(r, el));
+    }
+    if (d0) DP_TRY(check_ptr(d0, 16));
+    if (d_final) DP_TRY(check_ptr(d_final, 16));
+    p.k = k;
+    p.beta = beta;
+    p.stream = (cudaStream_t)stream;
+    if ((size_t)p.B * p.H == 0) return DP_OK;
+    const dp::OsdnScan sc{eta, d_lo, d_hi, eps};
+    return from_cuda(dp::launch_osdn_dscan(p, r, d0, sc, kw, d_final));
+}
+
+extern "C" dp_status dp_forward_write_keys(const dp_dims *dims, const void *q, const void *k, const void *kw,
+                                           const void *v, const void *beta, const void *g, const float *h0,
+                                           void *o, float *h_final, void *workspace, size_t workspace_bytes,
+                                           dp_stream_t stream)
+{
+    DP_TRY(check_dims(dims, false));
+    if (dims->max_seqlen != 0 || (dims->prologue & DP_PRO_KEY_SILU_L2)) return DP_ERR_INVALID_ARG;
+    if (dims->impl == DP_IMPL_CHUNK_TC) return DP_ERR_UNSUPPORTED;
+    dp::Problem p = make_problem(dims, dims->T);
+    p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g; p.h0 = h0; p.o = o; p.h_final = h_final;
+    p.kw = kw;
+    p.stream = (cudaStream_t)stream;
+    DP_TRY(check_io(p, g != nullptr));
+    if ((size_t)p.B * p.H * p.T > 0) DP_TRY(check_ptr(kw, 16));
+    if (h0) DP_TRY(check_ptr(h0, 16));
+    if (h_final) DP_TRY(check_ptr(h_final, 16));
+    size_t need = 0;
+    DP_TRY(dp_forward_workspace_size(dims, &need));
+    if (!workspace || workspace_bytes < need) return DP_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return DP_ERR_ALIGNMENT;
+    if (!device_pointer(workspace)) return DP_ERR_INVALID_ARG;
+    p.status = (uint32_t *)workspace;
+    p.scratch = (char *)workspace + kStatusBlock;
+    p.scratch_bytes = workspace_bytes - kStatusBlock;
+    if ((size_t)p.B * p.H == 0) return DP_OK;
+    return from_cuda(dp::launch_recurrent(p));
+}

@@ -23,6 +23,7 @@ struct Problem {
     const int *cu;             // packed sequences: int32 [B+1] token offsets (NULL: dense [B,T] layout)
     int max_T;                 // longest sequence (T for dense calls)
     int prologue;              // dp_prologue_flags applied to the inputs on load
+    const void *kw;            // OSDN write keys (layout of k), or NULL: write with k
     void *scratch;             // workspace bytes after the status block
     size_t scratch_bytes;
     cudaStream_t stream;
@@ -66,6 +67,14 @@ cudaError_t launch_backward(const BwdProblem &p);
 cudaError_t launch_state_io(int op, int B, int H, int Dk, int Dv, float *state,
                             void *ext, int ext_dtype, int ext_transposed,
                             cudaStream_t stream);
+
+// OSDN phase 1 (dp_osdn_write_keys): the preconditioner scan over the
+// extended rows, emitting the write keys k~ = d (.) k.
+struct OsdnScan {
+    float eta, d_lo, d_hi, eps;
+};
+cudaError_t launch_osdn_dscan(const Problem &p, const void *r, const float *d0, const OsdnScan &sc, void *kw,
+                              float *d_final);
 
 // Standalone input prologue (dp_prologue), dense layouts.
 cudaError_t launch_prologue(const Problem &p, void *q_out, void *k_out, void *beta_out, void *g_out);

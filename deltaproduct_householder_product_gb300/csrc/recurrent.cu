@@ -4,9 +4,11 @@
 // (Sec.4, Appendix B.1): H <- g H; for each of the n_h steps
 // e = v - H^T k, H <- H + beta k e^T; then o = H^T q.
 //
-// Serves three calls: the fp32 path of dp_forward (and any head size the
+// Serves four calls: the fp32 path of dp_forward (and any head size the
 // tensor-core kernel does not take), dp_decode_step (T = 1 with the state
-// updated in place), and the state import/export of dp_state_io.
+// updated in place), dp_forward_write_keys (the OSDN variant: the state is
+// written along the write key k~ while the error still reads with k), and
+// the state import/export of dp_state_io.
 //
 // Packed variable-length calls (cu != NULL): CTA row b is sequence b, whose
 // tokens are found through seq_range.
@@ -41,10 +43,11 @@ recurrent_kernel(int T, int H, int Dv, int nh, const int *cu, int N, int max_T, 
                  const TIn *__restrict__ q, const TIn *__restrict__ k,
                  const TIn *__restrict__ v, const TIn *__restrict__ beta,
                  const TIn *__restrict__ g, const float *h0, TOut *__restrict__ o,
-                 float *h_final)
+                 float *h_final, const TIn *__restrict__ kw)
 {
     constexpr int R = DK / kWarps;            // key rows per warp
     __shared__ float kbuf[2][DK];
+    __shared__ float kwbuf[2][DK];      // OSDN write keys (kw != NULL)
     __shared__ float part[2][kWarps][kCols];
     __shared__ float nred[2][kWarps];   // prologue: partial sums of squares
 
@@ -96,7 +99,10 @@ recurrent_kernel(int T, int H, int Dv, int nh, const int *cu, int N, int max_T, 
                 for (int i = 0; i < kWarps; ++i) tot += nred[buf][i];
                 xv = round_to<TIn>(xv * pro_inv_norm(tot));
             }
-            if (threadIdx.x < DK) kbuf[buf][threadIdx.x] = xv;
+            if (threadIdx.x < DK) {
+                kbuf[buf][threadIdx.x] = xv;
+                if (kw && j < nh) kwbuf[buf][threadIdx.x] = to_f(kw[(tok * nh + j) * DK + threadIdx.x]);
+            }
             __syncthreads();
             float acc = 0.f;
 #pragma unroll
@@ -110,8 +116,9 @@ recurrent_kernel(int T, int H, int Dv, int nh, const int *cu, int N, int max_T, 
                 const float vj = to_f(v[(tok * nh + j) * Dv + col]);
                 const float bj = pro_beta(to_f(beta[tok * nh + j]), pro);
                 const float e = bj * (vj - hx);
+                const float *wk = kw ? kwbuf[buf] : kbuf[buf];   // the write direction
 #pragma unroll
-                for (int r = 0; r < R; ++r) S[r] = fmaf(kbuf[buf][row0 + r], e, S[r]);
+                for (int r = 0; r < R; ++r) S[r] = fmaf(wk[row0 + r], e, S[r]);
             } else if (w == 0) {
                 from_f(o + tok * Dv + col, hx);
             }
@@ -135,15 +142,15 @@ cudaError_t launch_typed(const Problem &p)
     switch (p.Dk) {
     case 32:
         recurrent_kernel<32, TIn, TOut><<<grid, block, 0, p.stream>>>(
-            p.T, p.H, p.Dv, p.nh, p.cu, p.B, p.max_T, p.prologue, p.status, q, k, v, be, g, p.h0, o, p.h_final);
+            p.T, p.H, p.Dv, p.nh, p.cu, p.B, p.max_T, p.prologue, p.status, q, k, v, be, g, p.h0, o, p.h_final, (const TIn *)p.kw);
         break;
     case 64:
         recurrent_kernel<64, TIn, TOut><<<grid, block, 0, p.stream>>>(
-            p.T, p.H, p.Dv, p.nh, p.cu, p.B, p.max_T, p.prologue, p.status, q, k, v, be, g, p.h0, o, p.h_final);
+            p.T, p.H, p.Dv, p.nh, p.cu, p.B, p.max_T, p.prologue, p.status, q, k, v, be, g, p.h0, o, p.h_final, (const TIn *)p.kw);
         break;
     default:
         recurrent_kernel<128, TIn, TOut><<<grid, block, 0, p.stream>>>(
-            p.T, p.H, p.Dv, p.nh, p.cu, p.B, p.max_T, p.prologue, p.status, q, k, v, be, g, p.h0, o, p.h_final);
+            p.T, p.H, p.Dv, p.nh, p.cu, p.B, p.max_T, p.prologue, p.status, q, k, v, be, g, p.h0, o, p.h_final, (const TIn *)p.kw);
         break;
     }
     return cudaGetLastError();

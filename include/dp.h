@@ -96,7 +96,7 @@ typedef enum {
 } dp_prologue_flags;
 
 /* ABI version of this header (bumped on any signature change). */
-#define DP_ABI_VERSION 6
+#define DP_ABI_VERSION 7
 int dp_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -224,6 +224,32 @@ dp_status dp_backward(const dp_dims *dims,
 dp_status dp_prologue(const dp_dims *dims, const void *q, const void *k, const void *beta,
                       const void *g, void *q_out, void *k_out, void *beta_out, void *g_out,
                       dp_stream_t stream);
+
+/* OSDN write keys (the OSDN paper's online preconditioning applied to this
+ * recurrence). Phase 1, dp_osdn_write_keys: per (b,h), over the extended
+ * rows in order (token t, then its n_h keys), emit the write key
+ * k~ = d (.) k with the current d, then update
+ *   d <- clamp(r d + eta beta (1 - beta <d, k (.) k>) / max(||k||^2, eps) * (k (.) k),
+ *              d_lo, d_hi)
+ * (OSDN paper, Alg.1 / Eq.(3); APF retention r, Sec.4.4, applied once per
+ * token on its first row; r = 1 without APF). The paper's configuration:
+ * eta = 0.003, [d_lo, d_hi] = [0.5, 2], eps = 1e-6, d0 = 1.
+ *   k [B,T,H,n_h,D_k], beta [B,T,H,n_h] (dims->dtype; used as given:
+ *   dims->prologue must not map keys or betas), r [B,T,H] or NULL;
+ *   d0 [B,H,D_k] fp32 or NULL (ones); kw [B,T,H,n_h,D_k] output in
+ *   dims->dtype; d_final [B,H,D_k] fp32 or NULL. fp32 arithmetic.
+ * Phase 2, dp_forward_write_keys: dp_forward with the state written along
+ * the write key, H <- H + beta k~ (v - H^T k)^T, the error still read with
+ * k (OSDN paper, Sec.4.1, Eq.(5)); kw has the layout of k. Runs on the
+ * recurrent kernel family (dims->impl AUTO or RECURRENT); same workspace
+ * as dp_forward; dims->prologue must not map keys. */
+dp_status dp_osdn_write_keys(const dp_dims *dims, const void *k, const void *beta, const void *r,
+                             const float *d0, float eta, float d_lo, float d_hi, float eps,
+                             void *kw, float *d_final, dp_stream_t stream);
+dp_status dp_forward_write_keys(const dp_dims *dims, const void *q, const void *k, const void *kw,
+                                const void *v, const void *beta, const void *g, const float *h0,
+                                void *o, float *h_final, void *workspace, size_t workspace_bytes,
+                                dp_stream_t stream);
 
 /* Synchronises `stream`, returns the status the device recorded in the
  * workspace since it was last cleared, and clears it. */
