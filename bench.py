@@ -397,8 +397,9 @@ def prologue_measure(dp, dev, hbm_peak, steps=50, warmup=5):
 def osdn_measure(dp, dev, hbm_peak, steps=10, warmup=2):
     """OSDN write keys on the bench workload (B4 H8 T2048 n_h 2 D128 bf16,
     fp32 o): phase 1 (dp_osdn_write_keys: the preconditioner scan, one warp
-    per head) and phase 2 (dp_forward_write_keys on the recurrent kernel),
-    each timed with CUDA events, inputs resident. Roofline of phase 2: the
+    per head) and phase 2 (dp_forward_write_keys),
+    each timed with CUDA events, inputs resident (phase 2 on the tensor-core
+    chunk path, fast workspace). Roofline of phase 2: the
     forward's algorithmic bytes plus the write keys read."""
     w = W.BASE
     x = {k: (None if v is None else v.to(dev)) for k, v in W.make_inputs(w).items()}
@@ -426,7 +427,8 @@ def osdn_measure(dp, dev, hbm_peak, steps=10, warmup=2):
     a2 = fwd_bytes / (ms2 * 1e-3) / 1e9
     return {"workload": f"{w.name} OSDN write keys (eta 0.003, d in [0.5, 2])",
             "ms_scan": ms1, "ms_forward_write_keys": ms2, "tokens_per_s": w.B * w.T / ((ms1 + ms2) * 1e-3),
-            "kernels": "dscan_kernel (one warp per head), recurrent_kernel with write keys",
+            "kernels": "dscan_kernel (one warp per head); chunk_coop_kernel with write keys",
+            "path": "chunk_coop",
             "scan_roofline": {"bound": "hbm", "achieved": scan_bytes / (ms1 * 1e-3) / 1e9, "peak": hbm_peak,
                               "unit": "GB/s", "frac": scan_bytes / (ms1 * 1e-3) / 1e9 / hbm_peak,
                               "algorithmic_bytes": scan_bytes},

@@ -294,8 +294,8 @@ def osdn_write_keys(k, beta, r=None, d0=None, *, eta=0.003, d_lo=0.5, d_hi=2.0, 
     return kw, d_final
 
 
-def forward_write_keys(q, k, kw, v, beta, g=None, h0=None, *, out=None, h_final=True, workspace=None,
-                       stream=None, out_dtype=None, prologue=0):
+def forward_write_keys(q, k, kw, v, beta, g=None, h0=None, *, impl="auto", out=None, h_final=True,
+                       workspace=None, stream=None, out_dtype=None, prologue=0):
     """dp_forward_write_keys (OSDN phase 2): ``forward`` with the state
     written along the write keys kw (layout of k)."""
     B, T, H, nh, Dk = k.shape
@@ -308,7 +308,7 @@ def forward_write_keys(q, k, kw, v, beta, g=None, h0=None, *, out=None, h_final=
         raise ValueError("kw must have the shape of k")
     if out_dtype is None:
         out_dtype = out.dtype if out is not None else dt
-    dims = _lib.make_dims(B, T, H, Dk, Dv, nh, dt, "auto", out_dtype, prologue=prologue_flags(prologue))
+    dims = _lib.make_dims(B, T, H, Dk, Dv, nh, dt, impl, out_dtype, prologue=prologue_flags(prologue))
     if out is None:
         out = torch.empty((B, T, H, Dv), dtype=out_dtype, device=q.device)
     if h_final is True:
@@ -316,7 +316,7 @@ def forward_write_keys(q, k, kw, v, beta, g=None, h0=None, *, out=None, h_final=
     elif h_final is False:
         h_final = None
     if workspace is None:
-        workspace = torch.zeros(_lib.workspace_size(dims), dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(_lib.workspace_size(dims, fast=True), dtype=torch.uint8, device=q.device)
     rc = _lib.lib().dp_forward_write_keys(
         dims, _lib._ptr(q), _lib._ptr(k), _lib._ptr(kw), _lib._ptr(v), _lib._ptr(beta), _lib._ptr(g),
         _lib._ptr(h0), _lib._ptr(out), _lib._ptr(h_final), _lib._ptr(workspace),

@@ -386,7 +386,6 @@ extern "C" dp_status dp_forward_write_keys(const dp_dims *dims, const void *q, c
 {
     DP_TRY(check_dims(dims, false));
     if (dims->max_seqlen != 0 || (dims->prologue & DP_PRO_KEY_SILU_L2)) return DP_ERR_INVALID_ARG;
-    if (dims->impl == DP_IMPL_CHUNK_TC) return DP_ERR_UNSUPPORTED;
     dp::Problem p = make_problem(dims, dims->T);
     p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g; p.h0 = h0; p.o = o; p.h_final = h_final;
     p.kw = kw;
@@ -403,6 +402,15 @@ extern "C" dp_status dp_forward_write_keys(const dp_dims *dims, const void *q, c
     p.status = (uint32_t *)workspace;
     p.scratch = (char *)workspace + kStatusBlock;
     p.scratch_bytes = workspace_bytes - kStatusBlock;
+    // the chunk path takes write keys in its split modes (per-chunk records
+    // in the workspace), without a prologue; otherwise the recurrent kernel
+    bool tc = dims->impl != DP_IMPL_RECURRENT && dp::chunk_tc_supported(p) && p.prologue == 0 && p.T > 0;
+    if (tc) {
+        int path = DP_PATH_CHUNK_FUSED;
+        if (dp::chunk_tc_path(p, &path) != cudaSuccess) return DP_ERR_CUDA;
+        tc = path != DP_PATH_CHUNK_FUSED;
+    }
+    if (dims->impl == DP_IMPL_CHUNK_TC && !tc) return DP_ERR_UNSUPPORTED;
     if ((size_t)p.B * p.H == 0) return DP_OK;
-    return from_cuda(dp::launch_recurrent(p));
+    return from_cuda(tc ? dp::launch_chunk_tc(p) : dp::launch_recurrent(p));
 }

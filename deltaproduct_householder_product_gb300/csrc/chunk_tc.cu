@@ -180,16 +180,18 @@ struct Params {
     int max_T;                 // longest sequence (T for dense calls)
     int prologue;              // dp_prologue_flags applied on load
     uint32_t rec_stride;       // bytes per record: record_stride(prologue)
+    const __nv_bfloat16 *kw;   // OSDN write keys (layout of k), split modes only; NULL: write with k
 };
 
 // The (sequence, head) pair one state-pass CTA, or one prep step, works on.
 // Dense calls (kPacked = false): sequence b is batch row b, T tokens, and
 // every extent comes straight from the kernel parameters. Packed calls: the
 // extent is read from cu (and checked) once.
-template <bool kPk, bool kPr>
+template <bool kPk, bool kPr, bool kW = false>
 struct Job {
     static constexpr bool kPacked = kPk;   // offsets from cu (else the dense layout)
     static constexpr bool kPro = kPr;      // input prologue (Params::prologue) applied on load
+    static constexpr bool kWK = kW;        // OSDN write keys (Params::kw)
     int b, h;          // sequence and head
     int b_map, t0;     // packed: token t sits at row (b_map * T + t0 + t) of the token layouts
     int len, nc;       // packed: its tokens and chunks
@@ -201,10 +203,10 @@ struct Job {
     __device__ __forceinline__ bool ok() const { return kPacked ? valid : true; }
 };
 
-template <bool kPacked, bool kPro>
-__device__ __forceinline__ Job<kPacked, kPro> make_job(const Params &p, int bh)
+template <bool kPacked, bool kPro, bool kWK = false>
+__device__ __forceinline__ Job<kPacked, kPro, kWK> make_job(const Params &p, int bh)
 {
-    Job<kPacked, kPro> j;
+    Job<kPacked, kPro, kWK> j;
     j.b = bh / p.H;
     j.h = bh - j.b * p.H;
     j.b_map = j.t0 = j.len = j.nc = 0;
@@ -368,6 +370,21 @@ __device__ __forceinline__ void issue_gram(uint32_t d_tmem, uint32_t kq)
     for (int kk = 0; kk < 8; ++kk) {
         const uint64_t d = sdesc_sw128(kq + (kk >> 2) * kKQBlock + (kk & 3) * 32, 16, 1024);
         mma_ss(d_tmem, d, d, id_gq, kk > 0);
+    }
+}
+
+// The Gram MMA with write keys (OSDN): [K;Q] K~^T, B = the K~ tile (rows
+// 0..31 of two 64-column blocks of kKWBlock bytes), so G and P come out
+// asymmetric as the write-key chunk form needs.
+constexpr uint32_t kKWBlock = kC * 128;   // 4 KB: 32 rows x 128 B
+__device__ __forceinline__ void issue_gram_wk(uint32_t d_tmem, uint32_t kq, uint32_t kwt)
+{
+    const uint32_t id_gq = idesc_bf16(64, kC, false, false);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t a = sdesc_sw128(kq + (kk >> 2) * kKQBlock + (kk & 3) * 32, 16, 1024);
+        const uint64_t b = sdesc_sw128(kwt + (kk >> 2) * kKWBlock + (kk & 3) * 32, 16, 1024);
+        mma_ss(d_tmem, a, b, id_gq, kk > 0);
     }
 }
 
@@ -738,7 +755,7 @@ __device__ __forceinline__ int y_row_p(int g) { return g ? kD : 0; }
 // wait failed or the CTA is aborting.
 __device__ bool phase_b(const Smem &s, const Params &p, uint32_t tbase, uint8_t *gt,
                         const uint8_t *kq, const float *Psrc, int pld, const float *L_s, int c,
-                        int g, int lt, uint32_t bar_id)
+                        int g, int lt, uint32_t bar_id, const float *kw16 = nullptr)
 {
     const int lw = lt >> 5, lane = lt & 31, lq = lw & 3, hf = lw >> 2;
     const int nh = p.nh, ct = p.ct;
@@ -768,7 +785,8 @@ __device__ bool phase_b(const Smem &s, const Params &p, uint32_t tbase, uint8_t 
         *(float4 *)(dst + sw128_offset(kC + i, 2 * q)) = make_float4(f[0], f[1], f[2], f[3]);
         *(float4 *)(dst + sw128_offset(kC + i, 2 * q + 1)) = make_float4(f[4], f[5], f[6], f[7]);
     }
-    // decayed K^T: row dk, four groups of 4 chunk rows per thread
+    // decayed K^T (write keys: decayed K~^T, from kw16 = this thread's 16
+    // values): row dk, four groups of 4 chunk rows per thread
     {
         const int dk = lt & 127, q0 = (lt >> 7) * 4;
         const float Lend = L_s[kC - 1];
@@ -780,7 +798,8 @@ __device__ bool phase_b(const Smem &s, const Params &p, uint32_t tbase, uint8_t 
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
                 const int s2 = 4 * q + k4;
-                const float x = __bfloat162float(*(const __nv_bfloat16 *)(src + sw128_offset(s2, chunk) + e * 2));
+                const float x = kw16 ? kw16[s2 - 4 * q0]
+                                     : __bfloat162float(*(const __nv_bfloat16 *)(src + sw128_offset(s2, chunk) + e * 2));
                 f[k4] = gated ? x * __expf(Lend - L_s[s2]) : x;
             }
             *(float4 *)(gt + kGY + sw128_offset(y_row_k(g) + dk, q)) = make_float4(f[0], f[1], f[2], f[3]);
@@ -806,6 +825,22 @@ __device__ bool phase_b(const Smem &s, const Params &p, uint32_t tbase, uint8_t 
     return true;
 }
 
+// Write keys of chunk c for phase B's decayed K~^T: thread lt's column
+// dk = lt % 128 on chunk rows 16 (lt / 128) .. + 15 (zero past R or past the
+// sequence), read from global memory ahead of the chunk's turn.
+template <class J>
+__device__ __forceinline__ void load_kw_rows(const Params &p, const J &jb, int c, int lt, float (&kwv)[16])
+{
+    const int dk = lt & 127, r0 = 16 * (lt >> 7), nh = p.nh, R = p.ct * nh;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int s2 = r0 + i, tl = s2 / nh, j = s2 - tl * nh, t = c * p.ct + tl;
+        kwv[i] = (s2 < R && t < jb.tokens(p))
+                     ? __bfloat162float(p.kw[(tok_row(p, jb, t) * nh + j) * kD + dk])
+                     : 0.f;
+    }
+}
+
 // Prep group g of the state-pass kernel: chunks g, g + 2, ...
 template <bool kSplit, class J>
 __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g, const J &jb)
@@ -819,11 +854,16 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
         for (int c = g; c < jb.chunks(p); c += 2) {
             const int st = c % kNS;
             const uint8_t *kq = s.stage(st), *rec = kq + kStageIn;
+            // write keys: the chunk's rows from global memory, in flight
+            // while the stage lands (fetching them a whole iteration ahead
+            // costs registers the 80-register kernel spills: slower)
+            float kwv[16];
+            if (J::kWK) load_kw_rows(p, jb, c, lt, kwv);
             const bool ok = (lt != 0) || wait_bar(s, kBarFull + st, (c / kNS) & 1, p.status);
             if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) break;
             // (with a key/query prologue the stage's K and Q arrive mapped, from the record)
             if (!phase_b(s, p, tbase, gt, kq, (const float *)(rec + kRecP), kC,
-                         (const float *)(rec + kRecL), c, g, lt, bar_id))
+                         (const float *)(rec + kRecL), c, g, lt, bar_id, J::kWK ? kwv : nullptr))
                 break;
             if (lt == 0) {
                 mbar_arrive(&s.bar[kBarReady + g]);
@@ -971,7 +1011,7 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, const J
 }
 
 // ------------------------------------------------------------------ state-pass kernel
-template <typename TOut, bool kSplit, bool kCoop, bool kPacked, bool kPro>
+template <typename TOut, bool kSplit, bool kCoop, bool kPacked, bool kPro, bool kWK = false>
 __device__ __forceinline__ void state_pass_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                                const CUtensorMap &tm_q, const Params &p, int bh)
 {
@@ -988,7 +1028,7 @@ __device__ __forceinline__ void state_pass_cta(const CUtensorMap &tm_k, const CU
     s.scratch_off = Lay::kOffScratch;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // a sequence with bad packed offsets runs no chunk
-    const Job<kPacked, kPro> jb = make_job<kPacked, kPro>(p, bh);
+    const Job<kPacked, kPro, kWK> jb = make_job<kPacked, kPro, kWK>(p, bh);
     if (kPacked && threadIdx.x == 0 && !jb.ok()) report_bad_sequence(p.status);
 
     // Zero every tile once: rows TMA never writes (padding rows, query rows
@@ -1029,12 +1069,12 @@ __device__ __forceinline__ void state_pass_cta(const CUtensorMap &tm_k, const CU
     if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
-template <typename TOut, bool kSplit, bool kPacked, bool kPro>
+template <typename TOut, bool kSplit, bool kPacked, bool kPro, bool kWK = false>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 const __grid_constant__ CUtensorMap tm_q, const Params p)
 {
-    state_pass_cta<TOut, kSplit, false, kPacked, kPro>(tm_k, tm_v, tm_q, p, blockIdx.x);
+    state_pass_cta<TOut, kSplit, false, kPacked, kPro, kWK>(tm_k, tm_v, tm_q, p, blockIdx.x);
 }
 
 // ------------------------------------------------------------------ prep kernel
@@ -1047,18 +1087,19 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 // (the group's loads and MMA drained first).
 template <class J>
 __device__ bool prep_chunk(const Params &p, const CUtensorMap *tk, const CUtensorMap *tq,
-                           uint8_t *stage, const PrepScratch &w, uint64_t *bars, uint32_t parity,
+                           const CUtensorMap *tkw, uint8_t *kwt, uint8_t *stage, const PrepScratch &w, uint64_t *bars, uint32_t parity,
                            volatile uint32_t *abort, uint32_t tbase, uint32_t gq_col, int lt,
                            uint32_t bar_id, const J &jb, int c)
 {
     const int lane = lt & 31, ct = p.ct, R = ct * p.nh;
     if (lt == 0) {
-        mbar_arrive_expect_tx(&bars[0], 256u * R + 256u * ct);
+        mbar_arrive_expect_tx(&bars[0], 256u * R + 256u * ct + (J::kWK ? 256u * R : 0u));
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
             const int t0 = jb.first() + c * ct;
             tma_load_5d(stage + kb * kKQBlock, tk, &bars[0], kb * 64, 0, jb.h, t0, jb.row_b());
             tma_load_4d(stage + kb * kKQBlock + kC * 128, tq, &bars[0], kb * 64, jb.h, t0, jb.row_b());
+            if (J::kWK) tma_load_5d(kwt + kb * kKWBlock, tkw, &bars[0], kb * 64, 0, jb.h, t0, jb.row_b());
         }
     }
     if (lt < 32) scan_rows(load_rows(p, jb, c, lane), lane, w.beta_s, w.L_s);
@@ -1089,7 +1130,10 @@ __device__ bool prep_chunk(const Params &p, const CUtensorMap *tk, const CUtenso
         ok = mbar_wait(&bars[0], parity, kWaitTries, abort);
         if (ok) {
             tc_fence_after();
-            issue_gram(tbase + gq_col, smem_addr(stage));
+            if (J::kWK)
+                issue_gram_wk(tbase + gq_col, smem_addr(stage), smem_addr(kwt));
+            else
+                issue_gram(tbase + gq_col, smem_addr(stage));
             mma_commit(&bars[1]);
             issued = true;
             ok = mbar_wait(&bars[1], parity, kWaitTries, abort);
@@ -1121,15 +1165,16 @@ __device__ bool prep_chunk(const Params &p, const CUtensorMap *tk, const CUtenso
 
 // Phase A for every chunk of every head in parallel, one chunk per CTA.
 constexpr int kPrepKThreads = kPrepThreads;
-constexpr uint32_t kPKScratch = 2 * kKQBlock;                       // after the KQ tiles
+constexpr uint32_t kPKKW = 2 * kKQBlock;                            // K~ tile (write keys)
+constexpr uint32_t kPKScratch = kPKKW + 2 * kKWBlock;               // after the KQ and K~ tiles
 constexpr uint32_t kPKBar = kPKScratch + kPrepScratch;
 constexpr uint32_t kPKSmem = kPKBar + 2 * 8 + 16 + 1024;
 constexpr uint32_t kPKTmemCols = 32;
 
-template <bool kPacked, bool kPro>
+template <bool kPacked, bool kPro, bool kWK = false>
 __global__ void __launch_bounds__(kPrepKThreads, 4)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
-                  const Params p)
+                  const __grid_constant__ CUtensorMap tm_kw, const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -1138,11 +1183,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     volatile uint32_t *abort = tmem_slot + 1;
     const int lt = threadIdx.x, warp = lt >> 5;
     const int c = blockIdx.x % p.n_chunks;
-    const Job<kPacked, kPro> jb = make_job<kPacked, kPro>(p, blockIdx.x / p.n_chunks);
+    const Job<kPacked, kPro, kWK> jb = make_job<kPacked, kPro, kWK>(p, blockIdx.x / p.n_chunks);
     if (c >= jb.chunks(p)) return;   // past the sequence's end (packed calls), or a bad sequence
 
     // rows TMA does not write (padding, queries beyond the chunk) stay zero
-    for (uint32_t i = lt * 16; i < 2 * kKQBlock; i += kPrepKThreads * 16)
+    for (uint32_t i = lt * 16; i < kPKScratch; i += kPrepKThreads * 16)
         *(uint4 *)(base + i) = make_uint4(0, 0, 0, 0);
     if (lt == 0) {
         mbar_init(&bar[0], 1);
@@ -1151,6 +1196,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         fence_mbar_init();
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_q);
+        if (kWK) tma_prefetch_desc(&tm_kw);
     }
     if (warp == 0) tmem_alloc(tmem_slot, kPKTmemCols);
     fence_proxy_async_smem();
@@ -1158,7 +1204,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
-    prep_chunk(p, &tm_k, &tm_q, base, prep_scratch(base + kPKScratch), bar, 0, abort, tbase, 0, lt, 1, jb, c);
+    prep_chunk(p, &tm_k, &tm_q, &tm_kw, base + kPKKW, base, prep_scratch(base + kPKScratch), bar, 0, abort, tbase,
+               0, lt, 1, jb, c);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, kPKTmemCols);
@@ -1174,20 +1221,22 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 // finish advances the generation, so flags of earlier launches never match.
 constexpr uint32_t kCoopScratch = (kPrepScratch + 127) & ~127u;
 
-template <bool kPacked, bool kPro>
-__device__ void prep_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const Params &p, int pcta,
-                         int n_pcta)
+template <bool kPacked, bool kPro, bool kWK>
+__device__ void prep_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const CUtensorMap &tm_kw,
+                         const Params &p, int pcta, int n_pcta)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     constexpr uint32_t kStg = 2 * kKQBlock;                          // 16 KB per group
-    uint8_t *scr = base + 2 * kStg;
+    constexpr uint32_t kKWT = 2 * kKWBlock;                          // 8 KB K~ tile per group
+    uint8_t *kwt = base + 2 * kStg;
+    uint8_t *scr = kwt + 2 * kKWT;
     uint64_t *bar = (uint64_t *)(scr + 2 * kCoopScratch);            // [group][loads, MMA]
     uint32_t *tmem_slot = (uint32_t *)(bar + 4);
     volatile uint32_t *abort = tmem_slot + 1;
     const int warp = threadIdx.x >> 5;
 
-    for (uint32_t i = threadIdx.x * 16; i < 2 * kStg; i += kThreads * 16)
+    for (uint32_t i = threadIdx.x * 16; i < 2 * kStg + 2 * kKWT; i += kThreads * 16)
         *(uint4 *)(base + i) = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
         for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
@@ -1195,6 +1244,7 @@ __device__ void prep_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const
         fence_mbar_init();
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_q);
+        if (kWK) tma_prefetch_desc(&tm_kw);
     }
     if (warp == 0) tmem_alloc(tmem_slot, 64);
     fence_proxy_async_smem();
@@ -1211,10 +1261,10 @@ __device__ void prep_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const
         uint32_t k = 0;   // chunks prepared by this group: the phase of its barriers
         for (int idx = pcta * 2 + gi; idx < total; idx += n_pcta * 2) {
             const int c = idx / p.bh_count;
-            const Job<kPacked, kPro> jb = make_job<kPacked, kPro>(p, idx - c * p.bh_count);
+            const Job<kPacked, kPro, kWK> jb = make_job<kPacked, kPro, kWK>(p, idx - c * p.bh_count);
             if (c >= jb.chunks(p)) continue;   // past the sequence's end (packed calls): nobody waits for it
-            if (!prep_chunk(p, &tm_k, &tm_q, base + gi * kStg, w, bar + 2 * gi, k & 1, abort, tbase,
-                            gi * 32, lt, 1 + gi, jb, c))
+            if (!prep_chunk(p, &tm_k, &tm_q, &tm_kw, kwt + gi * kKWT, base + gi * kStg, w, bar + 2 * gi, k & 1,
+                            abort, tbase, gi * 32, lt, 1 + gi, jb, c))
                 break;
             ++k;
             if (lt == 0) {
@@ -1228,15 +1278,16 @@ __device__ void prep_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const
     if (warp == 0) tmem_dealloc(tbase, 64);
 }
 
-template <typename TOut, bool kPacked, bool kPro>
+template <typename TOut, bool kPacked, bool kPro, bool kWK = false>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_coop_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_q, const Params p)
+                  const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kw,
+                  const Params p)
 {
     if ((int)blockIdx.x < p.bh_count)
-        state_pass_cta<TOut, true, true, kPacked, kPro>(tm_k, tm_v, tm_q, p, blockIdx.x);
+        state_pass_cta<TOut, true, true, kPacked, kPro, kWK>(tm_k, tm_v, tm_q, p, blockIdx.x);
     else
-        prep_cta<kPacked, kPro>(tm_k, tm_q, p, blockIdx.x - p.bh_count, gridDim.x - p.bh_count);
+        prep_cta<kPacked, kPro, kWK>(tm_k, tm_q, tm_kw, p, blockIdx.x - p.bh_count, gridDim.x - p.bh_count);
     // every thread of this CTA is done (the role ended with a CTA barrier)
     if (threadIdx.x == 0) {
         __threadfence();
@@ -1279,7 +1330,7 @@ size_t chunk_tc_records_bytes(const Problem &p)
 
 namespace {
 // The kernel instantiation for a problem: output type, mode, packed
-// offsets, input prologue.
+// offsets, input prologue; write keys (dense, no prologue, split modes).
 template <typename TOut, bool kSplit>
 auto tc_kernel_mode(bool packed, bool pro)
 {
@@ -1287,8 +1338,9 @@ auto tc_kernel_mode(bool packed, bool pro)
                   : (pro ? chunk_tc_kernel<TOut, kSplit, false, true> : chunk_tc_kernel<TOut, kSplit, false, false>);
 }
 template <typename TOut>
-auto tc_kernel_for(bool split, bool packed, bool pro)
+auto tc_kernel_for(bool split, bool packed, bool pro, bool wk)
 {
+    if (wk) return chunk_tc_kernel<TOut, true, false, false, true>;
     return split ? tc_kernel_mode<TOut, true>(packed, pro) : tc_kernel_mode<TOut, false>(packed, pro);
 }
 template <typename TOut>
@@ -1299,9 +1351,9 @@ auto coop_kernel_typed(bool packed, bool pro)
 }
 auto coop_kernel_for(const Problem &p)
 {
-    const bool packed = p.cu != nullptr, pro = p.prologue != 0;
-    return p.out_dtype == DP_F32 ? coop_kernel_typed<float>(packed, pro)
-                                 : coop_kernel_typed<__nv_bfloat16>(packed, pro);
+    const bool packed = p.cu != nullptr, pro = p.prologue != 0, f32 = p.out_dtype == DP_F32;
+    if (p.kw) return f32 ? chunk_coop_kernel<float, false, false, true> : chunk_coop_kernel<__nv_bfloat16, false, false, true>;
+    return f32 ? coop_kernel_typed<float>(packed, pro) : coop_kernel_typed<__nv_bfloat16>(packed, pro);
 }
 
 // Grid of the cooperative launch (state-pass CTAs + prep CTAs), or 0 when
@@ -1350,7 +1402,7 @@ cudaError_t launch_chunk_tc(const Problem &p)
     const int nh = p.nh, ct = chunk_tokens(nh);
     // packed calls: one batch row of T tokens, sequences found through cu
     const cuuint64_t B = p.cu ? 1 : p.B, T = p.T, H = p.H;
-    CUtensorMap tk, tv, tq;
+    CUtensorMap tk, tv, tq, tkw;
     const cuuint64_t dk[5] = {kD, (cuuint64_t)nh, H, T, B};
     const cuuint64_t sk[4] = {kD * 2, (cuuint64_t)nh * kD * 2, H * nh * kD * 2, T * H * nh * kD * 2};
     const cuuint32_t bk[5] = {64, (cuuint32_t)nh, 1, (cuuint32_t)ct, 1};
@@ -1358,7 +1410,7 @@ cudaError_t launch_chunk_tc(const Problem &p)
     const cuuint64_t sq[3] = {kD * 2, H * kD * 2, T * H * kD * 2};
     const cuuint32_t bq[4] = {64, 1, (cuuint32_t)ct, 1};
     if (!encode(&tk, p.k, 5, dk, sk, bk) || !encode(&tv, p.v, 5, dk, sk, bk) ||
-        !encode(&tq, p.q, 4, dq, sq, bq))
+        !encode(&tq, p.q, 4, dq, sq, bq) || !encode(&tkw, p.kw ? p.kw : p.k, 5, dk, sk, bk))
         return cudaErrorInvalidValue;
     Params pr;
     pr.beta = (const __nv_bfloat16 *)p.beta;
@@ -1380,6 +1432,7 @@ cudaError_t launch_chunk_tc(const Problem &p)
     pr.max_T = p.max_T;
     pr.prologue = p.prologue;
     pr.rec_stride = record_stride(p.prologue);
+    pr.kw = (const __nv_bfloat16 *)p.kw;
     pr.n_chunks = (int)chunks_per_seq(p);
 
     // split whenever the workspace holds every chunk's record; cooperative
@@ -1388,6 +1441,8 @@ cudaError_t launch_chunk_tc(const Problem &p)
     const size_t n_total = n_chunks_total(p);
     const size_t rec_bytes = round256(n_total * record_stride(p.prologue));
     const bool split = p.scratch != nullptr && n_total > 0 && p.scratch_bytes >= rec_bytes;
+    // write keys: the split modes only (dense, no prologue; checked by the caller)
+    if (p.kw && (!split || p.cu || p.prologue)) return cudaErrorInvalidValue;
     cudaError_t e;
     long long grid = 0;
     if (split && (e = coop_grid(p, &grid)) != cudaSuccess) return e;
@@ -1395,7 +1450,7 @@ cudaError_t launch_chunk_tc(const Problem &p)
         auto kernel = coop_kernel_for(p);
         pr.flags = (uint32_t *)((uint8_t *)p.scratch + rec_bytes);
         pr.sync = (uint32_t *)((uint8_t *)pr.flags + round256(n_total * 4));
-        void *args[] = {(void *)&tk, (void *)&tv, (void *)&tq, (void *)&pr};
+        void *args[] = {(void *)&tk, (void *)&tv, (void *)&tq, (void *)&tkw, (void *)&pr};
         e = cudaLaunchCooperativeKernel((const void *)kernel, dim3((unsigned)grid), dim3(kThreads), args,
                                         smem_bytes<true>(), p.stream);
         if (e == cudaSuccess) return cudaSuccess;
@@ -1403,17 +1458,18 @@ cudaError_t launch_chunk_tc(const Problem &p)
     }
     const bool packed = p.cu != nullptr, pro = p.prologue != 0;
     if (split) {
-        auto prep = packed ? (pro ? chunk_prep_kernel<true, true> : chunk_prep_kernel<true, false>)
-                           : (pro ? chunk_prep_kernel<false, true> : chunk_prep_kernel<false, false>);
+        auto prep = p.kw     ? chunk_prep_kernel<false, false, true>
+                    : packed ? (pro ? chunk_prep_kernel<true, true> : chunk_prep_kernel<true, false>)
+                             : (pro ? chunk_prep_kernel<false, true> : chunk_prep_kernel<false, false>);
         e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPKSmem);
         if (e != cudaSuccess) return e;
         const size_t n_ctas = (size_t)p.B * p.H * pr.n_chunks;
         if (n_ctas > 0x7fffffffu) return cudaErrorInvalidValue;
-        prep<<<(unsigned)n_ctas, kPrepKThreads, kPKSmem, p.stream>>>(tk, tq, pr);
+        prep<<<(unsigned)n_ctas, kPrepKThreads, kPKSmem, p.stream>>>(tk, tq, tkw, pr);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    auto kernel = p.out_dtype == DP_F32 ? tc_kernel_for<float>(split, packed, pro)
-                                        : tc_kernel_for<__nv_bfloat16>(split, packed, pro);
+    auto kernel = p.out_dtype == DP_F32 ? tc_kernel_for<float>(split, packed, pro, p.kw != nullptr)
+                                        : tc_kernel_for<__nv_bfloat16>(split, packed, pro, p.kw != nullptr);
     const uint32_t smem = split ? smem_bytes<true>() : smem_bytes<false>();
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

@@ -240,9 +240,13 @@ dp_status dp_prologue(const dp_dims *dims, const void *q, const void *k, const v
  *   dims->dtype; d_final [B,H,D_k] fp32 or NULL. fp32 arithmetic.
  * Phase 2, dp_forward_write_keys: dp_forward with the state written along
  * the write key, H <- H + beta k~ (v - H^T k)^T, the error still read with
- * k (OSDN paper, Sec.4.1, Eq.(5)); kw has the layout of k. Runs on the
- * recurrent kernel family (dims->impl AUTO or RECURRENT); same workspace
- * as dp_forward; dims->prologue must not map keys. */
+ * k (OSDN paper, Sec.4.1, Eq.(5)); kw has the layout of k. The chunk
+ * (tensor-core) path takes it in its split modes, i.e. with a workspace of
+ * at least dp_forward_workspace_size_fast and dims->prologue = 0 (the Gram
+ * becomes K K~^T, the readout scores Q K~^T, the state update runs along
+ * K~, W keeps K); otherwise, or with dims->impl RECURRENT, the recurrent
+ * kernel; CHUNK_TC where the chunk path cannot take it returns
+ * DP_ERR_UNSUPPORTED. dims->prologue must not map keys. */
 dp_status dp_osdn_write_keys(const dp_dims *dims, const void *k, const void *beta, const void *r,
                              const float *d0, float eta, float d_lo, float d_hi, float eps,
                              void *kw, float *d_final, dp_stream_t stream);

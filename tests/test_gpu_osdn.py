@@ -1,6 +1,7 @@
 """GPU parity of the OSDN write-key variant through the C ABI: phase 1
 (dp_osdn_write_keys) against oracle.osdn.dscan, phase 2
-(dp_forward_write_keys) against the C oracle fed the same write keys, both
+(dp_forward_write_keys, recurrent kernel and tensor-core chunk path in
+both split modes) against the C oracle fed the same write keys, both
 phases against oracle.osdn.forward, the eta = 0 reduction to the plain
 recurrence (bit for bit), with and without APF retention, and sampled heads
 of the bench-sized workload.
@@ -63,7 +64,7 @@ def test_osdn_parity(dp, name, w, apf, d0, eta):
     kw, dfin = dp.osdn_write_keys(xc["k"], xc["beta"], rc, dc, eta=eta)
     ref_kw, ref_d = OS.dscan(x["k"], x["beta"], r, d, eta=eta)
     check_scan(kw, dfin, ref_kw, ref_d)
-    o, hf = dp.forward_write_keys(xc["q"], xc["k"], kw, xc["v"], xc["beta"], xc["g"], xc["h0"],
+    o, hf = dp.forward_write_keys(xc["q"], xc["k"], kw, xc["v"], xc["beta"], xc["g"], xc["h0"], impl="recurrent",
                                   out_dtype=torch.float32)
     # phase 2 alone: the oracle on the kernel's own write keys
     ro, rh = oracle.forward(x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"], kw=kw.cpu())
@@ -81,7 +82,7 @@ def test_eta_zero_is_plain_forward(dp):
     x, xc, *_ = inputs(w)
     kw, dfin = dp.osdn_write_keys(xc["k"], xc["beta"], eta=0.0)
     assert torch.equal(kw, xc["k"]) and torch.all(dfin == 1)
-    o1, h1 = dp.forward_write_keys(xc["q"], xc["k"], kw, xc["v"], xc["beta"], xc["g"], xc["h0"],
+    o1, h1 = dp.forward_write_keys(xc["q"], xc["k"], kw, xc["v"], xc["beta"], xc["g"], xc["h0"], impl="recurrent",
                                    out_dtype=torch.float32)
     o2, h2 = dp.forward(xc["q"], xc["k"], xc["v"], xc["beta"], xc["g"], xc["h0"], impl="recurrent",
                         out_dtype=torch.float32)
@@ -106,6 +107,7 @@ def test_osdn_full_size_sampled_heads(dp):
     x, xc, *_ = inputs(w)
     kw, dfin = dp.osdn_write_keys(xc["k"], xc["beta"])
     o, hf = dp.forward_write_keys(xc["q"], xc["k"], kw, xc["v"], xc["beta"], None, None, out_dtype=torch.float32)
+    # (AUTO: the tensor-core chunk path with the fast workspace)
     for b, hh in ((0, 0), (w.B - 1, w.H - 1)):
         sl = lambda t: t[b:b + 1, :, hh:hh + 1]
         rk, rd = OS.dscan(sl(x["k"]), sl(x["beta"]))
@@ -113,3 +115,66 @@ def test_osdn_full_size_sampled_heads(dp):
         ro, rh = oracle.forward(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["beta"]), None, None, kw=rk)
         assert_parity(sl(o), ro, "bf16", f"head ({b},{hh}) o")
         assert_parity(hf[b:b + 1, hh:hh + 1], rh, "bf16", f"head ({b},{hh}) h_final")
+
+
+def chunk_ws(dp, w, mode):
+    """Workspace selecting a split mode of the chunk path: "coop" (the fast
+    size) or "split" (the records only: prep kernel + state-pass kernel)."""
+    B, T, H, nh, D = w.B, w.T, w.H, w.nh, w.Dk
+    lo = dp.workspace_size(B, T, H, D, D, nh)
+    if mode == "coop":
+        n = dp.workspace_size(B, T, H, D, D, nh, fast=True)
+    else:
+        ct = min(16, 32 // nh)
+        n = lo + ((B * H * (-(-T // ct)) * 18688 + 255) // 256) * 256
+    return torch.zeros(n, dtype=torch.uint8, device="cuda")
+
+
+CHUNK_CASES = [("base", W.BASE.scaled(B=2, H=2, T=150), 0.003), ("gated-h0", W.GATED.scaled(B=1, H=3, T=90), 0.2),
+               ("neardup-nh3", W.NEARDUP.scaled(B=1, H=2, T=77), 0.5)]
+
+
+@pytest.mark.parametrize("mode", ["coop", "split"])
+@pytest.mark.parametrize("name,w,eta", CHUNK_CASES, ids=[c[0] for c in CHUNK_CASES])
+def test_chunk_path_write_keys(dp, name, w, eta, mode):
+    """The tensor-core path with write keys (asymmetric Gram K K~^T, readout
+    Q K~^T, state update along K~) against the oracle on the same write keys."""
+    x, xc, *_ = inputs(w)
+    kw, _ = dp.osdn_write_keys(xc["k"], xc["beta"], eta=eta)
+    ws = chunk_ws(dp, w, mode)
+    o, hf = dp.forward_write_keys(xc["q"], xc["k"], kw, xc["v"], xc["beta"], xc["g"], xc["h0"], impl="chunk_tc",
+                                  workspace=ws, out_dtype=torch.float32)
+    dp.check_status(ws)
+    ro, rh = oracle.forward(x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"], kw=kw.cpu())
+    assert_parity(o, ro, "bf16", f"{name} {mode} o")
+    assert_parity(hf, rh, "bf16", f"{name} {mode} h_final")
+
+
+@pytest.mark.parametrize("mode", ["coop", "split"])
+def test_chunk_write_keys_equal_keys_is_plain_chunk_forward(dp, mode):
+    """kw = k: the write-key chunk path computes the plain chunk path's
+    values in the same order, bit for bit."""
+    w = W.GATED.scaled(B=2, H=2, T=100, nh=2)
+    x, xc, *_ = inputs(w)
+    ws = chunk_ws(dp, w, mode)
+    o1, h1 = dp.forward_write_keys(xc["q"], xc["k"], xc["k"], xc["v"], xc["beta"], xc["g"], xc["h0"],
+                                   impl="chunk_tc", workspace=ws, out_dtype=torch.float32)
+    ws2 = chunk_ws(dp, w, mode)
+    o2, h2 = dp.forward(xc["q"], xc["k"], xc["v"], xc["beta"], xc["g"], xc["h0"], impl="chunk_tc", workspace=ws2,
+                        out_dtype=torch.float32)
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+
+
+def test_write_keys_fall_back_to_recurrent_without_records(dp):
+    """With the minimum workspace the write keys run on the recurrent kernel;
+    CHUNK_TC is then refused."""
+    w = W.BASE.scaled(B=1, H=2, T=40)
+    x, xc, *_ = inputs(w)
+    kw, _ = dp.osdn_write_keys(xc["k"], xc["beta"], eta=0.1)
+    lo = torch.zeros(dp.workspace_size(1, 40, 2, 128, 128, 2), dtype=torch.uint8, device="cuda")
+    o, _ = dp.forward_write_keys(xc["q"], xc["k"], kw, xc["v"], xc["beta"], workspace=lo, out_dtype=torch.float32)
+    o2, _ = dp.forward_write_keys(xc["q"], xc["k"], kw, xc["v"], xc["beta"], impl="recurrent",
+                                  out_dtype=torch.float32)
+    assert torch.equal(o, o2)
+    with pytest.raises(dp.DPError):
+        dp.forward_write_keys(xc["q"], xc["k"], kw, xc["v"], xc["beta"], impl="chunk_tc", workspace=lo)
