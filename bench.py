@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--no-backward", action="store_true", help="skip the backward-pass measurement")
     ap.add_argument("--no-prologue", action="store_true", help="skip the fused-prologue measurement")
     ap.add_argument("--no-osdn", action="store_true", help="skip the OSDN write-key measurement")
+    ap.add_argument("--only", choices=["decode", "varlen", "backward", "prologue", "osdn"],
+                    help="run just this measurement (one GPU) and print its object: for profiling")
     ap.add_argument("--fused", action="store_true",
                     help="give dp_forward only the minimum workspace: the chunk path then "
                          "runs as one fused kernel instead of prep + state-pass kernels")
@@ -615,9 +617,33 @@ def ours_arm(args, w):
 TRAFFIC = {("b4h8t2048-nh2-d128-bf16", "chunk_coop"): 146_669_312}
 
 
+def only_arm(args):
+    """One secondary measurement alone (the object the full line carries),
+    with --steps / --warmup as given: a short command to profile it with."""
+    import deltaproduct_householder_product_gb300 as dp
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    hbm_peak, _, _ = measured_peaks()
+    steps, warmup = max(1, args.steps), max(1, args.warmup)
+    if args.only == "decode":
+        out = decode_measure(dev, hbm_peak, reps=steps)
+    elif args.only == "varlen":
+        out = varlen_measure(dp, dev, hbm_peak, steps=steps, warmup=warmup)
+    elif args.only == "backward":
+        out = backward_measure(dp, dev, hbm_peak, steps=steps, warmup=warmup)
+    elif args.only == "prologue":
+        out = prologue_measure(dp, dev, hbm_peak, steps=steps, warmup=warmup)
+    else:
+        out = osdn_measure(dp, dev, hbm_peak, steps=steps, warmup=warmup)
+    print(json.dumps({"only": args.only, **out}))
+
+
 def main():
     args = parse()
     w = WORKLOADS[args.workload]
+    if args.only:
+        only_arm(args)
+        return
     if args.impl == "reference":
         reference_arm(args, w)
     else:
