@@ -841,6 +841,21 @@ __device__ __forceinline__ void load_kw_rows(const Params &p, const J &jb, int c
     }
 }
 
+// The same rows of chunk c pulled into L2 ahead of load_kw_rows (no
+// registers held: the kernel runs at its register cap).
+template <class J>
+__device__ __forceinline__ void prefetch_kw_rows(const Params &p, const J &jb, int c, int lt)
+{
+    const int dk = lt & 127, r0 = 16 * (lt >> 7), nh = p.nh, R = p.ct * nh;
+    if ((dk & 63) != 0) return;   // one 128-byte line per 64 columns of a row
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int s2 = r0 + i, tl = s2 / nh, j = s2 - tl * nh, t = c * p.ct + tl;
+        if (s2 < R && t < jb.tokens(p))
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p.kw + (tok_row(p, jb, t) * nh + j) * kD + dk));
+    }
+}
+
 // Prep group g of the state-pass kernel: chunks g, g + 2, ...
 template <bool kSplit, class J>
 __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g, const J &jb)
@@ -858,7 +873,10 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
             // while the stage lands (fetching them a whole iteration ahead
             // costs registers the 80-register kernel spills: slower)
             float kwv[16];
-            if (J::kWK) load_kw_rows(p, jb, c, lt, kwv);
+            if (J::kWK) {
+                if (c + 2 < jb.chunks(p)) prefetch_kw_rows(p, jb, c + 2, lt);
+                load_kw_rows(p, jb, c, lt, kwv);
+            }
             const bool ok = (lt != 0) || wait_bar(s, kBarFull + st, (c / kNS) & 1, p.status);
             if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) break;
             // (with a key/query prologue the stage's K and Q arrive mapped, from the record)

@@ -90,6 +90,21 @@ __global__ void __launch_bounds__(128) dscan_kernel(int n_heads, int Tn, int H, 
     // extended row x -> (token t, key j): offsets of its key and beta
     auto beta_at = [&](int x) { return (((size_t)b * Tn + x / nh) * H + h) * nh + x % nh; };
     auto key_at = [&](int x) { return beta_at(x) * DK + lane * E; };
+    // walking a row cursor instead: +1 key within a token, else on to the
+    // next token's first key (H n_h rows further, less the n_h - 1 passed)
+    struct Cursor {
+        size_t off;
+        int j;
+    };
+    const size_t tok_step = ((size_t)H * nh - (nh - 1)) * DK;
+    auto advance = [&](Cursor &cu) {
+        if (++cu.j < nh) {
+            cu.off += DK;
+        } else {
+            cu.j = 0;
+            cu.off += tok_step;
+        }
+    };
     // per-row scalars of rows x0 .. x0 + 31 (lane l: row x0 + l)
     auto scalars = [&](int x0, float &bt, float &rt) {
         const int x = x0 + lane;
@@ -97,10 +112,12 @@ __global__ void __launch_bounds__(128) dscan_kernel(int n_heads, int Tn, int H, 
         rt = (r && x < rows && x % nh == 0) ? ld(r, beta_at(x) / nh) : 1.f;
     };
     // prime the ring: rows 0 .. kRing-2, one commit group per row
+    Cursor cx{key_at(0), 0}, cy = cx;   // row x (being scanned) and row x + kRing - 1 (being fetched)
 #pragma unroll 1
     for (int x = 0; x < kRing - 1; ++x) {
-        if (x < rows) cp_async<kB>(ring[w][x][lane], k + key_at(x));
+        if (x < rows) cp_async<kB>(ring[w][x][lane], k + cy.off);
         cp_commit();
+        advance(cy);
     }
     float b_cur, r_cur, b_nxt = 0.f, r_nxt = 1.f;
     scalars(0, b_cur, r_cur);
@@ -112,8 +129,9 @@ __global__ void __launch_bounds__(128) dscan_kernel(int n_heads, int Tn, int H, 
             // row x + kRing - 1 into the slot row x - 1 used (read a row ago;
             // an empty group past the end keeps the count), then wait for row x
             const int y = x + kRing - 1;
-            if (y < rows) cp_async<kB>(ring[w][y % kRing][lane], k + key_at(y));
+            if (y < rows) cp_async<kB>(ring[w][y % kRing][lane], k + cy.off);
             cp_commit();
+            advance(cy);
             cp_wait<kRing - 1>();   // groups complete in order: row x has landed
             float kk[E];
             unpack<T, E>(ring[w][x % kRing][lane], kk);
@@ -126,7 +144,8 @@ __global__ void __launch_bounds__(128) dscan_kernel(int n_heads, int Tn, int H, 
                 n2 += s2;
                 ds = fmaf(d[e], s2, ds);
             }
-            store_row<T, E>(kw + key_at(x), kt);
+            store_row<T, E>(kw + cx.off, kt);
+            advance(cx);
 #pragma unroll
             for (int m = 16; m >= 1; m >>= 1) {
                 n2 += __shfl_xor_sync(0xffffffffu, n2, m);
