@@ -128,6 +128,11 @@ constexpr uint32_t kRecBeta = kRecP + kNQ * kC * 4;   // + 2 KB
 constexpr uint32_t kRecL = kRecBeta + kC * 4;
 constexpr uint32_t kRecBytes = kRecL + kC * 4;        // 18688
 static_assert(kRecBytes % 16 == 0, "bulk copies move 16-byte multiples");
+// Write keys without a gate: the two T-tile slots the Gamma pair would use
+// carry the chunk's K~ tile instead (two 64-column blocks of 32 rows x
+// 128 B, swizzled as in shared memory), so the state pass finds it in its
+// stage with the record.
+constexpr uint32_t kRecKW = kRecT + 2 * kTTile;
 // With a key or query prologue the record also carries the chunk's mapped
 // K and Q rows (the 48 rows of each 64-column KQ block, swizzled as in
 // shared memory), so the state pass copies them instead of mapping them.
@@ -401,7 +406,7 @@ __device__ void tma_role(const Smem &s, const Params &p, const CUtensorMap *tk,
     const bool gated = p.g != nullptr;
     // K and V: 2 x R rows x 128 B each; Q: 2 x ct rows. Record: the T tiles
     // it uses (2 or 4) and P, beta, L.
-    const uint32_t rec_t = (gated ? 4 : 2) * kTTile, rec_tail = kRecBytes - kRecP;
+    const uint32_t rec_t = ((gated || J::kWK) ? 4 : 2) * kTTile, rec_tail = kRecBytes - kRecP;
     // mapped K and Q from the record (split modes with a key/query prologue)
     const bool kq_rec = kSplit && J::kPro && kq_in_record(p.prologue);
     const uint32_t bytes = (kq_rec ? 256u * R + kRecKQBytes : 512u * R + 256u * ct) +
@@ -755,7 +760,8 @@ __device__ __forceinline__ int y_row_p(int g) { return g ? kD : 0; }
 // wait failed or the CTA is aborting.
 __device__ bool phase_b(const Smem &s, const Params &p, uint32_t tbase, uint8_t *gt,
                         const uint8_t *kq, const float *Psrc, int pld, const float *L_s, int c,
-                        int g, int lt, uint32_t bar_id, const float *kw16 = nullptr)
+                        int g, int lt, uint32_t bar_id, const float *kw16 = nullptr,
+                        const uint8_t *ksrc = nullptr, uint32_t kblock = kKQBlock)
 {
     const int lw = lt >> 5, lane = lt & 31, lq = lw & 3, hf = lw >> 2;
     const int nh = p.nh, ct = p.ct;
@@ -786,11 +792,12 @@ __device__ bool phase_b(const Smem &s, const Params &p, uint32_t tbase, uint8_t 
         *(float4 *)(dst + sw128_offset(kC + i, 2 * q + 1)) = make_float4(f[4], f[5], f[6], f[7]);
     }
     // decayed K^T (write keys: decayed K~^T, from kw16 = this thread's 16
-    // values): row dk, four groups of 4 chunk rows per thread
+    // values, or from the K~ tile at ksrc with blocks kblock bytes apart):
+    // row dk, four groups of 4 chunk rows per thread
     {
         const int dk = lt & 127, q0 = (lt >> 7) * 4;
         const float Lend = L_s[kC - 1];
-        const uint8_t *src = kq + (dk >> 6) * kKQBlock;
+        const uint8_t *src = (ksrc ? ksrc : kq) + (dk >> 6) * kblock;
         const int chunk = (dk & 63) >> 3, e = dk & 7;
 #pragma unroll
         for (int q = q0; q < q0 + 4; ++q) {
@@ -873,7 +880,8 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
             // while the stage lands (fetching them a whole iteration ahead
             // costs registers the 80-register kernel spills: slower)
             float kwv[16];
-            if (J::kWK) {
+            const bool kw_global = J::kWK && gated;   // ungated: K~ arrives in the record
+            if (kw_global) {
                 if (c + 2 < jb.chunks(p)) prefetch_kw_rows(p, jb, c + 2, lt);
                 load_kw_rows(p, jb, c, lt, kwv);
             }
@@ -881,7 +889,9 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
             if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) break;
             // (with a key/query prologue the stage's K and Q arrive mapped, from the record)
             if (!phase_b(s, p, tbase, gt, kq, (const float *)(rec + kRecP), kC,
-                         (const float *)(rec + kRecL), c, g, lt, bar_id, J::kWK ? kwv : nullptr))
+                         (const float *)(rec + kRecL), c, g, lt, bar_id, kw_global ? kwv : nullptr,
+                         (J::kWK && !gated) ? rec + kRecKW : nullptr,
+                         (J::kWK && !gated) ? kKWBlock : kKQBlock))
                 break;
             if (lt == 0) {
                 mbar_arrive(&s.bar[kBarReady + g]);
@@ -1168,6 +1178,9 @@ __device__ bool prep_chunk(const Params &p, const CUtensorMap *tk, const CUtenso
     if (group_any(bar_id, kPrepThreads, !ok || *abort)) return false;
     tc_fence_after();
     uint8_t *rec = p.rec + rec_index(p, jb, c) * p.rec_stride;
+    if (J::kWK && p.g == nullptr)   // the K~ tile, for the state pass (see kRecKW)
+        for (uint32_t i = lt * 16; i < 2 * kKWBlock; i += kPrepThreads * 16)
+            *(uint4 *)(rec + kRecKW + i) = *(const uint4 *)(kwt + i);
     phase_a(w, tbase, gq_col, rec + kRecT, lt, p.nh, ct, p.g != nullptr, bar_id);
     float *rp = (float *)(rec + kRecP);
     for (int i = lt; i < kNQ * kC; i += kPrepThreads) rp[i] = w.Ps[(i >> 5) * kLd + (i & 31)];
