@@ -72,6 +72,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x, world, device):
+    """The largest of each rank's ``x`` (a time): the job is as slow as its
+    slowest replica. Identity at world size 1."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank, world, ms):
+    """Whole-job throughput: the tokens all replicas processed over the
+    slowest replica's time per step."""
+    return tokens_per_rank * world / (ms * 1e-3)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -529,11 +545,7 @@ def ours_arm(args, w):
     torch.cuda.synchronize()
     clocks = sampler.stop()
     clocks["window"] = "timed region" + (" + soak of the same step" if wall_timed < 1.5 else "")
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, dev)
     for c in copies:
         dp.check_status(c["ws"])
 
@@ -583,19 +595,15 @@ def ours_arm(args, w):
     s_out.wait_stream(stream)
     e1.record(s_out)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
 
     if rank != 0:
         return
-    tokens = w.B * w.T * world
+    tokens = w.B * w.T
     hbm_peak, _, peak_kind = measured_peaks()
     achieved = wbytes / (ms * 1e-3) / 1e9
     line = {
-        "metric": METRIC, "value": tokens / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": job_tokens_per_s(tokens, world, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "out_dtype": "f32",
         "data": "synthetic",
@@ -605,7 +613,7 @@ def ours_arm(args, w):
                    "l2": f"{n_copies} rotating input/output copies "
                          f"({n_copies * wbytes / 1e6:.0f} MB > 129 MB L2)",
                    "parallelism": f"replicas x{world}"},
-        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": job_tokens_per_s(tokens, world, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "pipeline": "copy-in, compute and copy-out streams over two device buffer sets"},
         "gpu_launches": args.steps * launches,
