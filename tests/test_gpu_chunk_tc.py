@@ -281,3 +281,31 @@ def test_long_state_carry_and_decode(dp):
     rdo, rdh = oracle.forward(seq["q"], seq["k"], seq["v"], seq["beta"], None, rh)
     assert_parity(torch.stack([o_dec[:, 0, h] for h in hs]).unsqueeze(2), rdo, "bf16", "decode o")
     assert_parity(gather_heads(st, pairs, False), rdh, "bf16", "decode state")
+
+
+@pytest.mark.parametrize("impl", ["chunk_tc", "recurrent"])
+def test_linearity_in_h0_and_v(dp, impl):
+    """o and h_final are linear in (h0, v) for fixed keys, betas and gates
+    (DeltaProduct paper, Sec.4: the update is affine in H with an additive
+    term in v). Doubling both doubles every intermediate exactly, so the
+    outputs double bit for bit; two problems whose v and h0 add up to the
+    original's (disjoint supports, so the sum is exact) give outputs that
+    add up to the original's up to rounding (the bf16 rule)."""
+    w = W.GATED.scaled(B=1, H=2, T=70, nh=2)
+    x = W.make_inputs(w)
+    xc = {k: (None if v is None else v.cuda()) for k, v in x.items()}
+    run = lambda v, h0: dp.forward(xc["q"], xc["k"], v, xc["beta"], xc["g"], h0, impl=impl,
+                                   out_dtype=torch.float32)
+    o1, h1 = run(xc["v"], xc["h0"])
+    o2, h2 = run(2 * xc["v"], 2 * xc["h0"])
+    assert torch.equal(o2, 2 * o1) and torch.equal(h2, 2 * h1)
+    # additivity: split v and h0 into two problems with disjoint supports, so
+    # that the parts sum to the originals exactly
+    gen = torch.Generator().manual_seed(17)
+    mv = (torch.rand(xc["v"].shape, generator=gen) < 0.5).cuda()
+    mh = (torch.rand(xc["h0"].shape, generator=gen) < 0.5).cuda()
+    zv, zh = torch.zeros_like(xc["v"]), torch.zeros_like(xc["h0"])
+    oa, ha = run(torch.where(mv, xc["v"], zv), torch.where(mh, xc["h0"], zh))
+    ob, hb = run(torch.where(mv, zv, xc["v"]), torch.where(mh, zh, xc["h0"]))
+    assert_parity(oa + ob, o1.cpu().double().numpy(), "bf16", "additivity of o")
+    assert_parity(ha + hb, h1.cpu().double().numpy(), "bf16", "additivity of h_final")
