@@ -37,7 +37,9 @@ template <> __device__ __forceinline__ float round_to<__nv_bfloat16>(float x)
 }
 __device__ __forceinline__ void from_f(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
 
-template <int DK, typename TIn, typename TOut>
+// kExtra: the input prologue or write keys are in use (the plain
+// instantiation carries neither, for the decode step's latency).
+template <int DK, typename TIn, typename TOut, bool kExtra>
 __global__ void __launch_bounds__(kWarps * 32)
 recurrent_kernel(int T, int H, int Dv, int nh, const int *cu, int N, int max_T, int pro, uint32_t *status,
                  const TIn *__restrict__ q, const TIn *__restrict__ k,
@@ -72,7 +74,7 @@ recurrent_kernel(int T, int H, int Dv, int nh, const int *cu, int N, int max_T, 
     for (int t = 0; t < sq.len; ++t) {
         const size_t tok = ((size_t)sq.b_map * T + sq.t0 + t) * H + h;
         if (g) {
-            const float gt = pro_gate(to_f(g[tok]), pro);
+            const float gt = kExtra ? pro_gate(to_f(g[tok]), pro) : to_f(g[tok]);
 #pragma unroll
             for (int r = 0; r < R; ++r) S[r] *= gt;
         }
@@ -81,8 +83,8 @@ recurrent_kernel(int T, int H, int Dv, int nh, const int *cu, int N, int max_T, 
             const TIn *x = (j < nh) ? k + (tok * nh + j) * DK : q + tok * DK;
             // prologue: SiLU + L2 normalisation of keys, L2 of queries, each
             // rounded to the input dtype like a given input (DK <= threads)
-            const bool silu = j < nh && (pro & DP_PRO_KEY_SILU_L2);
-            const bool norm = silu || (j == nh && (pro & DP_PRO_QUERY_L2));
+            const bool silu = kExtra && j < nh && (pro & DP_PRO_KEY_SILU_L2);
+            const bool norm = kExtra && (silu || (j == nh && (pro & DP_PRO_QUERY_L2)));
             float xv = 0.f;
             if (threadIdx.x < DK) {
                 xv = to_f(x[threadIdx.x]);
@@ -101,7 +103,7 @@ recurrent_kernel(int T, int H, int Dv, int nh, const int *cu, int N, int max_T, 
             }
             if (threadIdx.x < DK) {
                 kbuf[buf][threadIdx.x] = xv;
-                if (kw && j < nh) kwbuf[buf][threadIdx.x] = to_f(kw[(tok * nh + j) * DK + threadIdx.x]);
+                if (kExtra && kw && j < nh) kwbuf[buf][threadIdx.x] = to_f(kw[(tok * nh + j) * DK + threadIdx.x]);
             }
             __syncthreads();
             float acc = 0.f;
@@ -114,9 +116,9 @@ recurrent_kernel(int T, int H, int Dv, int nh, const int *cu, int N, int max_T, 
             for (int i = 0; i < kWarps; ++i) hx += part[buf][i][lane];
             if (j < nh) {
                 const float vj = to_f(v[(tok * nh + j) * Dv + col]);
-                const float bj = pro_beta(to_f(beta[tok * nh + j]), pro);
+                const float bj = kExtra ? pro_beta(to_f(beta[tok * nh + j]), pro) : to_f(beta[tok * nh + j]);
                 const float e = bj * (vj - hx);
-                const float *wk = kw ? kwbuf[buf] : kbuf[buf];   // the write direction
+                const float *wk = (kExtra && kw) ? kwbuf[buf] : kbuf[buf];   // the write direction
 #pragma unroll
                 for (int r = 0; r < R; ++r) S[r] = fmaf(wk[row0 + r], e, S[r]);
             } else if (w == 0) {
@@ -132,26 +134,26 @@ recurrent_kernel(int T, int H, int Dv, int nh, const int *cu, int N, int max_T, 
     }
 }
 
+template <int DK, typename TIn, typename TOut>
+void launch_dk(const Problem &p, dim3 grid, dim3 block)
+{
+    const TIn *q = (const TIn *)p.q, *k = (const TIn *)p.k, *v = (const TIn *)p.v;
+    const TIn *be = (const TIn *)p.beta, *g = (const TIn *)p.g, *kw = (const TIn *)p.kw;
+    TOut *o = (TOut *)p.o;
+    auto kernel = (p.prologue != 0 || p.kw != nullptr) ? recurrent_kernel<DK, TIn, TOut, true>
+                                                       : recurrent_kernel<DK, TIn, TOut, false>;
+    kernel<<<grid, block, 0, p.stream>>>(p.T, p.H, p.Dv, p.nh, p.cu, p.B, p.max_T, p.prologue, p.status, q, k, v, be,
+                                         g, p.h0, o, p.h_final, kw);
+}
+
 template <typename TIn, typename TOut>
 cudaError_t launch_typed(const Problem &p)
 {
     dim3 grid(p.B * p.H, p.Dv / kCols), block(kWarps * 32);
-    const TIn *q = (const TIn *)p.q, *k = (const TIn *)p.k, *v = (const TIn *)p.v;
-    const TIn *be = (const TIn *)p.beta, *g = (const TIn *)p.g;
-    TOut *o = (TOut *)p.o;
     switch (p.Dk) {
-    case 32:
-        recurrent_kernel<32, TIn, TOut><<<grid, block, 0, p.stream>>>(
-            p.T, p.H, p.Dv, p.nh, p.cu, p.B, p.max_T, p.prologue, p.status, q, k, v, be, g, p.h0, o, p.h_final, (const TIn *)p.kw);
-        break;
-    case 64:
-        recurrent_kernel<64, TIn, TOut><<<grid, block, 0, p.stream>>>(
-            p.T, p.H, p.Dv, p.nh, p.cu, p.B, p.max_T, p.prologue, p.status, q, k, v, be, g, p.h0, o, p.h_final, (const TIn *)p.kw);
-        break;
-    default:
-        recurrent_kernel<128, TIn, TOut><<<grid, block, 0, p.stream>>>(
-            p.T, p.H, p.Dv, p.nh, p.cu, p.B, p.max_T, p.prologue, p.status, q, k, v, be, g, p.h0, o, p.h_final, (const TIn *)p.kw);
-        break;
+    case 32: launch_dk<32, TIn, TOut>(p, grid, block); break;
+    case 64: launch_dk<64, TIn, TOut>(p, grid, block); break;
+    default: launch_dk<128, TIn, TOut>(p, grid, block); break;
     }
     return cudaGetLastError();
 }
