@@ -12,7 +12,7 @@ from . import _lib
 from ._lib import DPError, STATE_EXPORT, STATE_IMPORT, STATE_ZERO  # noqa: F401
 
 __all__ = ["forward", "forward_varlen", "forward_noalloc", "forward_path", "supports", "decode_step", "state_io", "check_status",
-           "backward", "prologue", "prologue_flags", "osdn_write_keys", "forward_write_keys",
+           "backward", "backward_varlen", "prologue", "prologue_flags", "osdn_write_keys", "forward_write_keys",
            "workspace_size",
            "DPError", "abi_version"]
 
@@ -151,6 +151,39 @@ def backward(q, k, v, beta, g=None, h0=None, *, d_o, dh_final=None, want_dh0=Tru
         workspace.numel() * workspace.element_size(), _lib._stream(stream))
     _lib._check(rc, "dp_backward")
     return out
+
+
+def backward_varlen(q, k, v, beta, g=None, h0=None, *, cu_seqlens, max_seqlen=None, d_o, dh_final=None,
+                    want_dh0=True, workspace=None, stream=None):
+    """``backward`` over packed variable-length sequences (the layouts of
+    ``forward_varlen``; dh_final and dh0 are [N,H,Dk,Dv])."""
+    T, H, nh, Dk = k.shape
+    Dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g)):
+        _lib._need_cuda(name, t, dt)
+    _lib._need_cuda("cu_seqlens", cu_seqlens, torch.int32)
+    _lib._need_cuda("h0", h0, torch.float32)
+    _lib._need_cuda("d_o", d_o)
+    _lib._need_cuda("dh_final", dh_final, torch.float32)
+    if max_seqlen is None:
+        max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if N > 0 else 0
+    dims = _lib.make_dims(N, T, H, Dk, Dv, nh, dt, "auto", d_o.dtype, max(int(max_seqlen), 1 if T > 0 else 0))
+    f32 = dict(dtype=torch.float32, device=q.device)
+    out = {"dq": torch.empty((T, H, Dk), **f32), "dk": torch.empty((T, H, nh, Dk), **f32),
+           "dv": torch.empty((T, H, nh, Dv), **f32), "dbeta": torch.empty((T, H, nh), **f32),
+           "dg": None if g is None else torch.empty((T, H), **f32),
+           "dh0": torch.empty((N, H, Dk, Dv), **f32) if want_dh0 else None}
+    if workspace is None:
+        workspace = torch.zeros(_lib.backward_workspace_size(dims), dtype=torch.uint8, device=q.device)
+    rc = _lib.lib().dp_backward_varlen(
+        dims, _lib._ptr(cu_seqlens), _lib._ptr(q), _lib._ptr(k), _lib._ptr(v), _lib._ptr(beta), _lib._ptr(g),
+        _lib._ptr(h0), _lib._ptr(d_o), _lib._ptr(dh_final), _lib._ptr(out["dq"]), _lib._ptr(out["dk"]),
+        _lib._ptr(out["dv"]), _lib._ptr(out["dbeta"]), _lib._ptr(out["dg"]), _lib._ptr(out["dh0"]),
+        _lib._ptr(workspace), workspace.numel() * workspace.element_size(), _lib._stream(stream))
+    _lib._check(rc, "dp_backward_varlen")
+    return out, workspace
 
 
 def forward_varlen(q, k, v, beta, g=None, h0=None, *, cu_seqlens, max_seqlen=None, impl="auto", out=None,

@@ -60,6 +60,7 @@ def lib():
         L.dp_backward_workspace_size.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(ctypes.c_size_t)]
         L.dp_backward.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 15 + [ctypes.c_size_t, _vp]
         L.dp_prologue.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 9
+        L.dp_backward_varlen.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 16 + [ctypes.c_size_t, _vp]
         L.dp_osdn_write_keys.argtypes = [ctypes.POINTER(Dims), _vp, _vp, _vp, _vp] + [ctypes.c_float] * 4 + \
             [_vp, _vp, _vp]
         L.dp_forward_write_keys.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 10 + [ctypes.c_size_t, _vp]
@@ -67,7 +68,7 @@ def lib():
                      "dp_forward", "dp_forward_varlen", "dp_decode_step",
                      "dp_state_io", "dp_check_status", "dp_forward_noalloc",
                      "dp_backward_workspace_size", "dp_backward", "dp_prologue",
-                     "dp_osdn_write_keys", "dp_forward_write_keys"):
+                     "dp_osdn_write_keys", "dp_forward_write_keys", "dp_backward_varlen"):
             getattr(L, name).restype = ctypes.c_int
         _LIB = L
     return _LIB

@@ -263,33 +263,27 @@ dp::BwdProblem make_bwd(const dp_dims *d)
     p.B = d->B; p.T = d->T; p.H = d->H; p.Dk = d->Dk; p.Dv = d->Dv; p.nh = d->nh;
     p.dtype = d->dtype;
     p.do_dtype = d->out_dtype;
+    p.max_T = d->max_seqlen > 0 ? d->max_seqlen : d->T;
     return p;
 }
 
-dp_status check_bwd_dims(const dp_dims *d)
+// varlen: dims->max_seqlen bounds the packed sequences (checked by check_dims);
+// dense calls leave it 0
+dp_status check_bwd_dims(const dp_dims *d, bool varlen)
 {
     DP_TRY(check_dims(d, false));
-    if (d->impl != DP_IMPL_AUTO || d->max_seqlen != 0 || d->prologue != 0) return DP_ERR_INVALID_ARG;
-    return DP_OK;
-}
-}  // namespace
-
-extern "C" {
-
-dp_status dp_backward_workspace_size(const dp_dims *dims, size_t *bytes)
-{
-    if (!bytes) return DP_ERR_INVALID_ARG;
-    DP_TRY(check_bwd_dims(dims));
-    *bytes = kStatusBlock + ((dp::backward_scratch_bytes(make_bwd(dims)) + 255) & ~(size_t)255);
+    if (d->impl != DP_IMPL_AUTO || d->prologue != 0) return DP_ERR_INVALID_ARG;
+    if (!varlen && d->max_seqlen != 0) return DP_ERR_INVALID_ARG;
+    if (varlen && d->T > 0 && d->max_seqlen < 1) return DP_ERR_INVALID_ARG;
     return DP_OK;
 }
 
-dp_status dp_backward(const dp_dims *dims, const void *q, const void *k, const void *v, const void *beta,
-                      const void *g, const float *h0, const void *d_o, const float *dh_final, float *dq,
-                      float *dk, float *dv, float *dbeta, float *dg, float *dh0, void *workspace,
-                      size_t workspace_bytes, dp_stream_t stream)
+dp_status backward_impl(const dp_dims *dims, const int *cu, const void *q, const void *k, const void *v,
+                        const void *beta, const void *g, const float *h0, const void *d_o, const float *dh_final,
+                        float *dq, float *dk, float *dv, float *dbeta, float *dg, float *dh0, void *workspace,
+                        size_t workspace_bytes, dp_stream_t stream)
 {
-    DP_TRY(check_bwd_dims(dims));
+    DP_TRY(check_bwd_dims(dims, cu != nullptr));
     dp::BwdProblem p = make_bwd(dims);
     const size_t el = p.dtype == DP_F32 ? 4 : 2;
     if ((size_t)p.B * p.H * p.T > 0) {
@@ -305,21 +299,55 @@ dp_status dp_backward(const dp_dims *dims, const void *q, const void *k, const v
         DP_TRY(check_ptr(dbeta, 4));
         if (g) DP_TRY(check_ptr(dg, 4));
     }
+    if (cu) DP_TRY(check_ptr(cu, 4));
     if (h0) DP_TRY(check_ptr(h0, 16));
     if (dh_final) DP_TRY(check_ptr(dh_final, 16));
     if (dh0) DP_TRY(check_ptr(dh0, 16));
-    size_t need = 0;
-    DP_TRY(dp_backward_workspace_size(dims, &need));
+    const size_t need = kStatusBlock + ((dp::backward_scratch_bytes(p) + 255) & ~(size_t)255);
     if (!workspace || workspace_bytes < need) return DP_ERR_WORKSPACE;
     if (!aligned16(workspace)) return DP_ERR_ALIGNMENT;
     if (!device_pointer(workspace)) return DP_ERR_INVALID_ARG;
     p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g; p.h0 = h0;
     p.d_o = d_o; p.dh_final = dh_final;
     p.dq = dq; p.dk = dk; p.dv = dv; p.dbeta = dbeta; p.dg = g ? dg : nullptr; p.dh0 = dh0;
+    p.cu = cu;
+    p.status = (uint32_t *)workspace;
     p.scratch = (char *)workspace + kStatusBlock;
     p.stream = (cudaStream_t)stream;
     if ((size_t)p.B * p.H == 0) return DP_OK;
     return from_cuda(dp::launch_backward(p));
+}
+}  // namespace
+
+extern "C" {
+
+dp_status dp_backward_workspace_size(const dp_dims *dims, size_t *bytes)
+{
+    if (!bytes) return DP_ERR_INVALID_ARG;
+    DP_TRY(check_bwd_dims(dims, dims && dims->max_seqlen != 0));
+    *bytes = kStatusBlock + ((dp::backward_scratch_bytes(make_bwd(dims)) + 255) & ~(size_t)255);
+    return DP_OK;
+}
+
+dp_status dp_backward(const dp_dims *dims, const void *q, const void *k, const void *v, const void *beta,
+                      const void *g, const float *h0, const void *d_o, const float *dh_final, float *dq,
+                      float *dk, float *dv, float *dbeta, float *dg, float *dh0, void *workspace,
+                      size_t workspace_bytes, dp_stream_t stream)
+{
+    return backward_impl(dims, nullptr, q, k, v, beta, g, h0, d_o, dh_final, dq, dk, dv, dbeta, dg, dh0,
+                         workspace, workspace_bytes, stream);
+}
+
+dp_status dp_backward_varlen(const dp_dims *dims, const int *cu_seqlens, const void *q, const void *k,
+                             const void *v, const void *beta, const void *g, const float *h0, const void *d_o,
+                             const float *dh_final, float *dq, float *dk, float *dv, float *dbeta, float *dg,
+                             float *dh0, void *workspace, size_t workspace_bytes, dp_stream_t stream)
+{
+    if (!dims) return DP_ERR_INVALID_ARG;
+    if ((size_t)dims->B * dims->H == 0) return check_bwd_dims(dims, true);
+    if (!cu_seqlens) return DP_ERR_INVALID_ARG;
+    return backward_impl(dims, cu_seqlens, q, k, v, beta, g, h0, d_o, dh_final, dq, dk, dv, dbeta, dg, dh0,
+                         workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -18,6 +18,10 @@
 // are sums over all value columns, so each CTA adds its part with a
 // global reduction (the D_v/32 CTAs of a head add in an unspecified order).
 //
+// Packed variable-length sequences (cu != NULL): CTA row b is sequence b,
+// found through seq_range; checkpoints and errors are laid out for the
+// longest sequence per (sequence, head).
+//
 // Time order: the states needed in reverse are rebuilt, not kept. The CTA
 // first runs the recurrence forward once, storing its slice of the state at
 // the start of every L-th token (checkpoints) and every sub-step's error
@@ -99,8 +103,11 @@ struct BwdArgs {
     const void *d_o;
     const float *dh_final;
     float *dq, *dk, *dv, *dbeta, *dg, *dh0;
-    float *ckpt;   // [B*H][n_seg][DK][Dv]
-    float *errs;   // [B*H][T][nh][Dv] errors v - H^T k of every sub-step
+    float *ckpt;   // [B*H][n_seg of max_T][DK][Dv]
+    float *errs;   // [B*H][max_T][nh][Dv] errors v - H^T k of every sub-step
+    const int *cu; // packed sequences: token offsets [B+1] (NULL: dense [B,T] layout)
+    int max_T;     // longest sequence (T for dense calls)
+    uint32_t *status;
 };
 
 template <int DK, typename TIn, typename TDo>
@@ -118,14 +125,23 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdArgs a)
     const TIn *q = (const TIn *)a.q, *k = (const TIn *)a.k, *v = (const TIn *)a.v;
     const TIn *beta = (const TIn *)a.beta, *g = (const TIn *)a.g;
     const TDo *d_o = (const TDo *)a.d_o;
-    const int T = a.T, H = a.H, Dv = a.Dv, nh = a.nh;
+    const int Tl = a.T, H = a.H, Dv = a.Dv, nh = a.nh;   // Tl: token rows of the layout
     const int bh = blockIdx.x, b = bh / H, h = bh - b * H;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int col = blockIdx.y * kCols + lane, row0 = w * R;
     const size_t state_base = (size_t)bh * DK * Dv;
+    // this sequence's tokens (packed calls: checked against the offsets'
+    // contract first; a sequence that breaks it is not touched)
+    const SeqRange sq = seq_range(a.cu, b, gridDim.x / H, Tl, a.max_T);
+    if (!sq.ok) {
+        if (threadIdx.x == 0 && blockIdx.y == 0) report_bad_sequence(a.status);
+        return;
+    }
+    const int T = sq.len;
     const int n_seg = (T + L - 1) / L;
-    float *ckpt = a.ckpt + (size_t)bh * n_seg * DK * Dv;
-    auto tok_of = [&](int t) { return ((size_t)b * T + t) * H + h; };
+    float *ckpt = a.ckpt + (size_t)bh * ((a.max_T + L - 1) / L) * DK * Dv;
+    float *errs = a.errs + (size_t)bh * a.max_T * nh * Dv;
+    auto tok_of = [&](int t) { return ((size_t)sq.b_map * Tl + sq.t0 + t) * H + h; };
 
     // M^T x for the CTA's columns (x: D_k floats in shared memory); one
     // barrier (the partial buffers alternate between calls).
@@ -157,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdArgs a)
         TokIn in;
         const bool bwd = mode == 2;
         const size_t tok = tok_of(t);
-        const float *et = a.errs + ((size_t)bh * T + t) * nh * Dv + col;
+        const float *et = errs + (size_t)t * nh * Dv + col;
         const int nk = nh * DK, n = nk + (bwd ? DK : 0);
 #pragma unroll
         for (int m = 0; m < KQ; ++m) {
@@ -219,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdArgs a)
         }
         stage(cur, false);
         const TokIn nxt = t + 1 < T ? fetch(t + 1, 0) : cur;
-        forward_token(cur, a.errs + ((size_t)bh * T + t) * nh * Dv + col);
+        forward_token(cur, errs + (size_t)t * nh * Dv + col);
         cur = nxt;
     }
     // the replay starts with the last segment's first token, whose errors
@@ -382,19 +398,19 @@ namespace {
 size_t backward_ckpt_bytes(const BwdProblem &p)
 {
     const int L = backward_segment_tokens(p.Dk);
-    const size_t n_seg = p.T > 0 ? (size_t)(p.T + L - 1) / L : 0;
+    const size_t n_seg = p.max_T > 0 ? (size_t)(p.max_T + L - 1) / L : 0;
     return (((size_t)p.B * p.H * n_seg * p.Dk * p.Dv * sizeof(float)) + 255) & ~(size_t)255;
 }
 }  // namespace
 
 size_t backward_scratch_bytes(const BwdProblem &p)
 {
-    return backward_ckpt_bytes(p) + (size_t)p.B * p.H * p.T * p.nh * p.Dv * sizeof(float);
+    return backward_ckpt_bytes(p) + (size_t)p.B * p.H * p.max_T * p.nh * p.Dv * sizeof(float);
 }
 
 cudaError_t launch_backward(const BwdProblem &p)
 {
-    const size_t tok = (size_t)p.B * p.T * p.H;
+    const size_t tok = (size_t)(p.cu ? 1 : p.B) * p.T * p.H;   // token-heads of the layout
     cudaError_t e;
     // the key-row and scalar gradients are accumulated by global reductions
     if ((e = cudaMemsetAsync(p.dq, 0, tok * p.Dk * sizeof(float), p.stream)) != cudaSuccess) return e;
@@ -407,6 +423,9 @@ cudaError_t launch_backward(const BwdProblem &p)
     a.d_o = p.d_o; a.dh_final = p.dh_final;
     a.dq = p.dq; a.dk = p.dk; a.dv = p.dv; a.dbeta = p.dbeta; a.dg = p.dg; a.dh0 = p.dh0;
     a.ckpt = (float *)p.scratch;
+    a.cu = p.cu;
+    a.max_T = p.max_T;
+    a.status = p.status;
     a.errs = (float *)((char *)p.scratch + backward_ckpt_bytes(p));
     if (p.dtype == DP_F32) return launch_typed<float, float>(p, a);
     return p.do_dtype == DP_F32 ? launch_typed<__nv_bfloat16, float>(p, a)

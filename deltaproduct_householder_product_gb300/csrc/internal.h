@@ -54,6 +54,9 @@ struct BwdProblem {
     const void *d_o;
     const float *dh_final;
     float *dq, *dk, *dv, *dbeta, *dg, *dh0;
+    const int *cu;             // packed sequences: int32 [B+1] token offsets (NULL: dense)
+    int max_T;                 // longest sequence (T for dense calls)
+    uint32_t *status;          // device status word
     void *scratch;             // checkpoint area (backward_scratch_bytes)
     cudaStream_t stream;
 };

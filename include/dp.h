@@ -96,7 +96,7 @@ typedef enum {
 } dp_prologue_flags;
 
 /* ABI version of this header (bumped on any signature change). */
-#define DP_ABI_VERSION 7
+#define DP_ABI_VERSION 8
 int dp_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -189,8 +189,8 @@ dp_status dp_state_io(int op, int B, int H, int Dk, int Dv, float *state,
 /* Backward pass: gradients of L = <d_o, o> + <dh_final, h_final> through
  * the recurrence dp_forward computes (DeltaProduct paper, Sec.4 Eq.(2)-(3),
  * gated variant), for training. Same dims and input layouts as dp_forward
- * (dims->impl and dims->max_seqlen must be 0; dims->out_dtype is the type
- * of d_o).
+ * (dims->impl, dims->prologue and dims->max_seqlen must be 0;
+ * dims->out_dtype is the type of d_o).
  *   d_o      [B,T,H,D_v] gradient of the outputs;
  *   dh_final [B,H,D_k,D_v] fp32 gradient of the final state, NULL = zeros;
  * outputs, fp32, written in full:
@@ -205,6 +205,19 @@ dp_status dp_state_io(int op, int B, int H, int Dk, int Dv, float *state,
  * state checkpoints, fp32 D_k x D_v per (b,h) every few tokens, and every
  * sub-step's error v - H^T k, fp32 B T H n_h D_v). */
 dp_status dp_backward_workspace_size(const dp_dims *dims, size_t *bytes);
+/* dp_backward over packed variable-length sequences: layouts, cu_seqlens
+ * and dims->max_seqlen as in dp_forward_varlen (the gradients take the
+ * layouts of their inputs: dq [T,H,D_k], ..., dh0 [N,H,D_k,D_v]); the
+ * workspace (dp_backward_workspace_size with the same dims) holds the
+ * checkpoints and errors for max_seqlen per (sequence, head). Sequences
+ * whose offsets break the contract record DP_ERR_DEVICE and are skipped. */
+dp_status dp_backward_varlen(const dp_dims *dims, const int *cu_seqlens,
+                             const void *q, const void *k, const void *v,
+                             const void *beta, const void *g, const float *h0,
+                             const void *d_o, const float *dh_final,
+                             float *dq, float *dk, float *dv, float *dbeta, float *dg,
+                             float *dh0, void *workspace, size_t workspace_bytes,
+                             dp_stream_t stream);
 dp_status dp_backward(const dp_dims *dims,
                       const void *q, const void *k, const void *v,
                       const void *beta, const void *g, const float *h0,

@@ -152,3 +152,51 @@ def test_backward_directional_derivative_full_size(dp):
     fd = (loss(eps) - loss(-eps)) / (2 * eps)
     print("directional derivative", lin, fd, abs(lin - fd) / abs(fd))
     assert abs(lin - fd) <= 1e-4 * abs(fd), (lin, fd)
+
+
+def varlen_case(lengths, nh, seed, gated=True):
+    T = int(sum(lengths))
+    w = (W.GATED if gated else W.BASE).scaled(B=1, H=2, T=max(T, 1), nh=nh, seed=seed)
+    x = W.make_inputs(w)
+    pk = {k: (None if x[k] is None else x[k][0, :T].contiguous()) for k in ("q", "k", "v", "beta", "g")}
+    gen = torch.Generator().manual_seed(seed + 1)
+    N = len(lengths)
+    pk["h0"] = 0.02 * torch.randn(N, 2, 128, 128, generator=gen)
+    d_o = torch.randn(T, 2, 128, generator=gen)
+    dhf = torch.randn(N, 2, 128, 128, generator=gen)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32)
+    return pk, d_o, dhf, cu
+
+
+@pytest.mark.parametrize("lengths,nh", [([0, 1, 15, 30, 13], 2), ([40, 0, 7], 3), ([5], 1)])
+def test_backward_varlen_parity(dp, lengths, nh):
+    """Packed sequences: each sequence's gradients against the oracle's
+    backward on that sequence alone."""
+    x, d_o, dhf, cu = varlen_case(lengths, nh, seed=60 + nh)
+    xc = {k: (None if v is None else v.cuda()) for k, v in x.items()}
+    got, ws = dp.backward_varlen(xc["q"], xc["k"], xc["v"], xc["beta"], xc["g"], xc["h0"], cu_seqlens=cu.cuda(),
+                                 d_o=d_o.cuda(), dh_final=dhf.cuda())
+    dp.check_status(ws)
+    a = 0
+    for s, n in enumerate(lengths):
+        sl = lambda t: None if t is None else t[a:a + n].unsqueeze(0)
+        ref = oracle.backward(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["beta"]), sl(x["g"]), x["h0"][s:s + 1],
+                              d_o[a:a + n].unsqueeze(0), dhf[s:s + 1])
+        part = {nm: (got[nm][s:s + 1] if nm == "dh0" else (None if got[nm] is None else got[nm][a:a + n].unsqueeze(0)))
+                for nm in NAMES}
+        if n == 0:
+            assert torch.equal(part["dh0"].cpu(), dhf[s:s + 1])
+        else:
+            check(part, ref, f"sequence {s} (length {n})")
+        a += n
+
+
+def test_backward_varlen_bad_offsets(dp):
+    x, d_o, dhf, cu = varlen_case([20, 20], 2, seed=70)
+    xc = {k: (None if v is None else v.cuda()) for k, v in x.items()}
+    bad = torch.tensor([0, 30, 20], dtype=torch.int32, device="cuda")
+    _, ws = dp.backward_varlen(xc["q"], xc["k"], xc["v"], xc["beta"], xc["g"], xc["h0"], cu_seqlens=bad,
+                               max_seqlen=30, d_o=d_o.cuda(), dh_final=dhf.cuda())
+    with pytest.raises(dp.DPError) as e:
+        dp.check_status(ws)
+    assert e.value.code == 7
