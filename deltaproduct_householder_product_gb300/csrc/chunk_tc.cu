@@ -16,14 +16,27 @@
 //   S   = Gamma_C S0 + K^T diag(Gamma_C/Gamma) U'        state pass, part 2
 //   o_t = Gamma_r S0^T q_t + sum_{s<=r} E_rs (q_t.k_s) u'_s,  r = last row of t
 //
-// Two ways to run it, same arithmetic and bit-identical results:
+// Three ways to run it, same arithmetic and bit-identical results:
 //  * split (two kernels): chunk_prep_kernel does "phase A" (G, P, T: the work
 //    that needs only one chunk's inputs) for every chunk of every head at
 //    once and writes a record per chunk into the workspace; the state-pass
 //    kernel then streams the records in with the inputs. The sequential
 //    kernel keeps only the work that has to follow the state.
+//  * cooperative (one launch, chunk_coop_kernel): state-pass CTAs and prep
+//    CTAs side by side, each record published through a flag.
 //  * fused (one kernel, no workspace beyond the status word): the state-pass
 //    kernel's prep groups do phase A themselves, one chunk ahead.
+// Compile-time variants (the Job type's flags), so that the plain
+// instantiation carries none of their code:
+//  * packed sequences (kPacked): each CTA reads its sequence's range from
+//    cu_seqlens; chunk c of sequence s starts at token cu[s] + c*ct.
+//  * input prologue (kPro): SiLU + L2 keys, L2 queries, sigmoid betas and
+//    gates mapped on load; in the split modes the prep maps K and Q and
+//    passes them in the record, in the fused mode the prep groups map the
+//    stage in place.
+//  * OSDN write keys (kWK, split modes): the Gram takes the write keys K~ as
+//    its B operand (G = tril(diag(beta)(K K~^T * E), -1), P from Q K~^T) and
+//    the state update runs along K~ (decayed K~^T tile); W keeps K.
 //
 // State-pass kernel organisation (one CTA per (batch, head), the state S^T
 // resident in TMEM for the whole sequence, lanes = value columns):
