@@ -62,6 +62,9 @@ def parse():
     ap.add_argument("--fused", action="store_true",
                     help="give dp_forward only the minimum workspace: the chunk path then "
                          "runs as one fused kernel instead of prep + state-pass kernels")
+    ap.add_argument("--split", action="store_true",
+                    help="give the forward a workspace that holds the per-chunk records but not the "
+                         "cooperative flags, so it runs as prep + state-pass kernels (for profiling)")
     return ap.parse_args()
 
 
@@ -164,13 +167,16 @@ def make_copies(w, n_copies, device):
     return x, copies
 
 
-def forward_calls(dp, L, w, copies, kernel, stream, fused=False):
+def forward_calls(dp, L, w, copies, kernel, stream, fused=False, split=False):
     """Pre-marshalled dp_forward calls, one per input copy (keeps per-call host
     work to the ABI call itself)."""
     import ctypes
     from deltaproduct_householder_product_gb300 import _lib
     dims = _lib.make_dims(w.B, w.T, w.H, w.Dk, w.Dv, w.nh, w.torch_dtype, kernel, OUT_DTYPE)
     need = _lib.workspace_size(dims, fast=not fused)
+    if split:   # records only: n_chunks x 18688 B after the 256-B status block
+        ct = min(16, 32 // w.nh)
+        need = 256 + (w.B * w.H * (-(-w.T // ct)) * 18688 + 255) // 256 * 256
     calls = []
     s = ctypes.c_void_p(stream.cuda_stream)
     for c in copies:
@@ -512,7 +518,7 @@ def ours_arm(args, w):
     wbytes = W.algorithmic_bytes(w, out_bytes=4)
     n_copies = max(2, -(-3 * L2_BYTES // wbytes))          # rotate copies: > 3x L2 in total
     x, copies = make_copies(w, n_copies, dev)
-    calls, dims, path = forward_calls(dp, L, w, copies, args.kernel, stream, args.fused)
+    calls, dims, path = forward_calls(dp, L, w, copies, args.kernel, stream, args.fused, args.split)
     launches = _lib.LAUNCHES[path]
 
     run_calls(calls, args.warmup)
