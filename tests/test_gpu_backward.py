@@ -200,3 +200,30 @@ def test_backward_varlen_bad_offsets(dp):
     with pytest.raises(dp.DPError) as e:
         dp.check_status(ws)
     assert e.value.code == 7
+
+
+def test_backward_chains_across_calls(dp):
+    """A sequence cut in two: the second call starts from the first call's
+    final state and hands its dh0 to the first call as dh_final; the
+    gradients equal the single call's (the way a trainer carries state
+    across segments)."""
+    w = W.GATED.scaled(B=2, H=2, T=60, nh=2)
+    d_o, dhf = cotangents(w, 160)
+    x = W.make_inputs(w)
+    xc = {k: (None if v is None else v.cuda()) for k, v in x.items()}
+    full = dp.backward(xc["q"], xc["k"], xc["v"], xc["beta"], xc["g"], xc["h0"], d_o=d_o.cuda(), dh_final=dhf.cuda())
+    t1 = 23
+    part = lambda t, a, b: None if t is None else t[:, a:b].contiguous()
+    xs1 = {k: part(xc[k], 0, t1) for k in ("q", "k", "v", "beta", "g")}
+    xs2 = {k: part(xc[k], t1, w.T) for k in ("q", "k", "v", "beta", "g")}
+    _, h_mid = dp.forward(xs1["q"], xs1["k"], xs1["v"], xs1["beta"], xs1["g"], xc["h0"], impl="recurrent",
+                          out_dtype=torch.float32)
+    g2 = dp.backward(xs2["q"], xs2["k"], xs2["v"], xs2["beta"], xs2["g"], h_mid, d_o=d_o[:, t1:].contiguous().cuda(),
+                     dh_final=dhf.cuda())
+    g1 = dp.backward(xs1["q"], xs1["k"], xs1["v"], xs1["beta"], xs1["g"], xc["h0"],
+                     d_o=d_o[:, :t1].contiguous().cuda(), dh_final=g2["dh0"])
+    for n in ("dq", "dk", "dv", "dbeta", "dg"):
+        s = err_stats(torch.cat([g1[n], g2[n]], 1), full[n].cpu().double().numpy())
+        assert s["rel_max"] <= TOL_REL, (n, s)
+    s = err_stats(g1["dh0"], full["dh0"].cpu().double().numpy())
+    assert s["rel_max"] <= TOL_REL, ("dh0", s)
