@@ -338,20 +338,23 @@ def backward_measure(dp, dev, hbm_peak, steps=5, warmup=2):
     dims = _lib.make_dims(w.B, w.T, w.H, w.Dk, w.Dv, w.nh, w.torch_dtype, "auto", torch.float32)
     ws = torch.zeros(_lib.backward_workspace_size(dims), dtype=torch.uint8, device=dev)
 
-    def call():
-        return dp.backward(x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"], d_o=d_o, dh_final=dhf,
-                           workspace=ws)
-    for _ in range(warmup):
-        call()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    stream = torch.cuda.current_stream()
-    e0.record(stream)
-    for _ in range(steps):
-        call()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
+    def timed(impl):
+        def call():
+            return dp.backward(x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"], d_o=d_o, dh_final=dhf,
+                               workspace=ws, impl=impl)
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        stream = torch.cuda.current_stream()
+        e0.record(stream)
+        for _ in range(steps):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+    ms = timed("auto")
+    ms_rec = timed("recurrent")
     nh, Dk, Dv = w.nh, w.Dk, w.Dv
     gated = 1 if w.gated else 0
     per_tok = 2 * (Dk + nh * Dk + nh * Dv + nh + gated) + 4 * Dv + 4 * (Dk + nh * Dk + nh * Dv + nh + gated)
@@ -359,8 +362,11 @@ def backward_measure(dp, dev, hbm_peak, steps=5, warmup=2):
     step_bytes = w.B * w.T * w.H * per_tok + w.B * w.H * states
     achieved = step_bytes / (ms * 1e-3) / 1e9
     return {"workload": f"{w.name} backward (fp32 d_o, dh_final and gradients)", "ms_per_call": ms,
-            "tokens_per_s": w.B * w.T / (ms * 1e-3), "kernel": "backward_kernel (recurrent, CUDA cores)",
-            "checkpoint_bytes": int(ws.numel()),
+            "tokens_per_s": w.B * w.T / (ms * 1e-3),
+            "kernel": ("chunked: cb_prep, cb_chains, cb_grad (CUDA cores)" if not w.gated
+                       else "backward_kernel (recurrent, CUDA cores)"),
+            "recurrent_ms_per_call": ms_rec,
+            "workspace_bytes": int(ws.numel()),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "algorithmic_bytes": step_bytes}}
 

@@ -114,13 +114,16 @@ def forward(q, k, v, beta, g=None, h0=None, *, impl="auto", out=None, h_final=Tr
 
 
 def backward(q, k, v, beta, g=None, h0=None, *, d_o, dh_final=None, want_dh0=True, workspace=None,
-             stream=None):
+             stream=None, impl="auto"):
     """Gradients of <d_o, o> + <dh_final, h_final> through ``forward``.
 
     Inputs as for ``forward``; d_o [B,T,H,Dv] (float32, or the input dtype);
     dh_final float32 [B,H,Dk,Dv] or None (zeros). Returns a dict of float32
     tensors dq, dk, dv, dbeta, dg (None when ungated) and dh0 (None unless
-    ``want_dh0``), in the layouts of the corresponding inputs.
+    ``want_dh0``), in the layouts of the corresponding inputs. ``impl``:
+    "auto" (the chunked form for ungated problems with Dk = Dv = 128, else
+    the recurrent form), "recurrent", or "chunk_tc" (the chunked form;
+    unsupported where it does not apply).
     """
     B, T, H, nh, Dk = k.shape
     Dv = v.shape[-1]
@@ -134,7 +137,7 @@ def backward(q, k, v, beta, g=None, h0=None, *, d_o, dh_final=None, want_dh0=Tru
         raise ValueError("inconsistent shapes for q, k, v, beta")
     if d_o.shape != (B, T, H, Dv):
         raise ValueError("d_o must be [B,T,H,Dv]")
-    dims = _lib.make_dims(B, T, H, Dk, Dv, nh, dt, "auto", d_o.dtype)
+    dims = _lib.make_dims(B, T, H, Dk, Dv, nh, dt, impl, d_o.dtype)
     f32 = dict(dtype=torch.float32, device=q.device)
     out = {"dq": torch.empty((B, T, H, Dk), **f32), "dk": torch.empty((B, T, H, nh, Dk), **f32),
            "dv": torch.empty((B, T, H, nh, Dv), **f32), "dbeta": torch.empty((B, T, H, nh), **f32),

@@ -272,10 +272,32 @@ dp::BwdProblem make_bwd(const dp_dims *d)
 dp_status check_bwd_dims(const dp_dims *d, bool varlen)
 {
     DP_TRY(check_dims(d, false));
-    if (d->impl != DP_IMPL_AUTO || d->prologue != 0) return DP_ERR_INVALID_ARG;
+    if (d->prologue != 0) return DP_ERR_INVALID_ARG;
+    if (d->impl != DP_IMPL_AUTO && d->impl != DP_IMPL_RECURRENT && d->impl != DP_IMPL_CHUNK_TC)
+        return DP_ERR_INVALID_ARG;
     if (!varlen && d->max_seqlen != 0) return DP_ERR_INVALID_ARG;
     if (varlen && d->T > 0 && d->max_seqlen < 1) return DP_ERR_INVALID_ARG;
     return DP_OK;
+}
+
+size_t bwd_recurrent_need(const dp::BwdProblem &p)
+{
+    return kStatusBlock + ((dp::backward_scratch_bytes(p) + 255) & ~(size_t)255);
+}
+size_t bwd_chunk_need(const dp::BwdProblem &p)
+{
+    return kStatusBlock + ((dp::backward_chunk_scratch_bytes(p) + 255) & ~(size_t)255);
+}
+// workspace the dims ask for: the recurrent form's, and the chunked form's
+// where the shape allows it (AUTO, CHUNK_TC)
+size_t bwd_workspace_bytes(const dp_dims *d, const dp::BwdProblem &p, bool varlen)
+{
+    size_t n = d->impl == DP_IMPL_CHUNK_TC ? 0 : bwd_recurrent_need(p);
+    if (d->impl != DP_IMPL_RECURRENT && !varlen && dp::backward_chunk_shape_ok(p)) {
+        const size_t c = bwd_chunk_need(p);
+        n = c > n ? c : n;
+    }
+    return n;
 }
 
 dp_status backward_impl(const dp_dims *dims, const int *cu, const void *q, const void *k, const void *v,
@@ -303,7 +325,14 @@ dp_status backward_impl(const dp_dims *dims, const int *cu, const void *q, const
     if (h0) DP_TRY(check_ptr(h0, 16));
     if (dh_final) DP_TRY(check_ptr(dh_final, 16));
     if (dh0) DP_TRY(check_ptr(dh0, 16));
-    const size_t need = kStatusBlock + ((dp::backward_scratch_bytes(p) + 255) & ~(size_t)255);
+    p.g = g;
+    p.cu = cu;
+    // AUTO takes the chunked form for ungated dense problems with D = 128
+    // when the workspace holds its records, else the recurrent form
+    bool chunked = dims->impl != DP_IMPL_RECURRENT && dp::backward_chunk_supported(p);
+    if (dims->impl == DP_IMPL_CHUNK_TC && !chunked) return DP_ERR_UNSUPPORTED;
+    if (chunked && dims->impl == DP_IMPL_AUTO && workspace_bytes < bwd_chunk_need(p)) chunked = false;
+    const size_t need = chunked ? bwd_chunk_need(p) : bwd_recurrent_need(p);
     if (!workspace || workspace_bytes < need) return DP_ERR_WORKSPACE;
     if (!aligned16(workspace)) return DP_ERR_ALIGNMENT;
     if (!device_pointer(workspace)) return DP_ERR_INVALID_ARG;
@@ -315,7 +344,7 @@ dp_status backward_impl(const dp_dims *dims, const int *cu, const void *q, const
     p.scratch = (char *)workspace + kStatusBlock;
     p.stream = (cudaStream_t)stream;
     if ((size_t)p.B * p.H == 0) return DP_OK;
-    return from_cuda(dp::launch_backward(p));
+    return from_cuda(chunked ? dp::launch_backward_chunk(p) : dp::launch_backward(p));
 }
 }  // namespace
 
@@ -325,7 +354,7 @@ dp_status dp_backward_workspace_size(const dp_dims *dims, size_t *bytes)
 {
     if (!bytes) return DP_ERR_INVALID_ARG;
     DP_TRY(check_bwd_dims(dims, dims && dims->max_seqlen != 0));
-    *bytes = kStatusBlock + ((dp::backward_scratch_bytes(make_bwd(dims)) + 255) & ~(size_t)255);
+    *bytes = bwd_workspace_bytes(dims, make_bwd(dims), dims->max_seqlen != 0);
     return DP_OK;
 }
 

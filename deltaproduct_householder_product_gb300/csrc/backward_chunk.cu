@@ -1,0 +1,688 @@
+// Chunked backward pass of the ungated recurrence (D_k = D_v = 128), fp32 on
+// CUDA cores.
+//
+// The extended sequence of every (batch, head) is cut into chunks of ct
+// whole tokens (R = ct n_h <= 32 rows, padded to 32 with zero rows, which
+// are exact no-ops), as in the forward. Per chunk, with S0 the state at its
+// start (OSDN paper, App.A.2, write key = read key; DeltaProduct paper,
+// Sec.5.1, readout at each token's last row):
+//   A = I + tril(diag(beta) K K^T, -1),  T = A^{-1}
+//   W = T diag(beta) K,  U = T diag(beta) V,  U' = U - W S0
+//   S1 = S0 + K^T U',   O = Q S0 + P U',  P = (Q K^T) masked to s <= last(t)
+// and, given dO and dS1 (the gradient at the chunk's end), by the chain rule
+//   dU' = P^T dO + K dS1,   dS0 = dS1 + Q^T dO - W^T dU'          (chain)
+//   dQ  = dO S0^T + dP K,   dP = (dO U'^T) masked
+//   dK  = dP^T Q + U' dS1^T + diag(beta) T^T dW + (B dG) K + (B dG)^T K
+//   dV  = diag(beta) T^T dU',  dW = -dU' S0^T,  B = diag(beta)
+//   dbeta = rowsum(K o T^T dW) + rowsum(V o T^T dU') + rowsum(dG o K K^T)
+//   dT = dW (B K)^T + dU' (B V)^T,  dG = strictly lower part of -T^T dT T^T
+// Three launches:
+//   cb_prep    every chunk at once: T, W, U, P, K K^T into its record;
+//   cb_chains  per (b,h) and 32 value columns, chunk by chunk, two
+//              independent CTAs: the forward chain (S <- S + K^T (U - W S))
+//              stores S0 and U' of every chunk; the reverse chain (the
+//              transposed recurrence above, from the last chunk) stores dS1
+//              and dU' of every chunk and dh0. The next chunk's tiles are
+//              copied in (cp.async) while the current one is processed;
+//   cb_grad    every chunk at once: dq, dk, dv, dbeta from its blocks. The
+//              three products with the 128 x 128 boundary states (dO S0^T,
+//              dU' S0^T, U' dS1^T) take 60% of its arithmetic; each thread
+//              holds a quarter row of S0 and of dS1 in registers for them.
+// The chains carry the only sequential dependency, as 32 x 128 x 128
+// products per chunk instead of a matrix-vector product per sub-step.
+#include "internal.h"
+
+namespace dp {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kC = 32;     // rows per chunk (padded)
+constexpr int kQ = 16;     // token rows per chunk (padded)
+constexpr int kS = 132;    // fp32 row stride of [.][128] tiles: float4-aligned, rows spread over the banks
+constexpr int kL = kC + 1; // row stride of [.][32] tiles
+
+// record of one chunk (fp32): W [32][128] | U [32][128] | T [32][32] | P [16][32] | K K^T [32][32]
+constexpr size_t kRecW = 0, kRecU = kC * kD, kRecT = 2 * kC * kD, kRecP = kRecT + kC * kC;
+constexpr size_t kRecKK = kRecP + kQ * kC;
+constexpr size_t kRecFloats = kRecKK + kC * kC;
+constexpr size_t kStateFloats = (size_t)kD * kD;   // S0 or dS1 of one chunk
+constexpr size_t kRowsFloats = (size_t)kC * kD;    // U' or dU' of one chunk
+
+struct CbArgs {
+    int B, T, H, nh, ct, nc;
+    const void *q, *k, *v, *beta;
+    const float *h0;
+    const void *d_o;
+    const float *dh_final;
+    float *dq, *dk, *dv, *dbeta, *dh0;
+    float *rec, *S0, *dS1, *Up, *dUp;   // workspace areas, [B*H*nc] chunks each
+};
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// bf16 -> fp32 is exact: the bf16 bits are the high half of the fp32 word
+__device__ __forceinline__ void unpack8(const uint4 u, float *x)
+{
+    x[0] = __uint_as_float(u.x << 16), x[1] = __uint_as_float(u.x & 0xffff0000u);
+    x[2] = __uint_as_float(u.y << 16), x[3] = __uint_as_float(u.y & 0xffff0000u);
+    x[4] = __uint_as_float(u.z << 16), x[5] = __uint_as_float(u.z & 0xffff0000u);
+    x[6] = __uint_as_float(u.w << 16), x[7] = __uint_as_float(u.w & 0xffff0000u);
+}
+// 8 consecutive elements (16-byte aligned) as fp32, from shared memory
+__device__ __forceinline__ void lds8(const __nv_bfloat16 *p, float *x) { unpack8(*(const uint4 *)p, x); }
+__device__ __forceinline__ void lds8(const float *p, float *x)
+{
+    const float4 a = ((const float4 *)p)[0], b = ((const float4 *)p)[1];
+    x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+}
+// ... and from global memory (read-only during the kernel)
+__device__ __forceinline__ void ldg8(const __nv_bfloat16 *p, float *x) { unpack8(__ldg((const uint4 *)p), x); }
+__device__ __forceinline__ void ldg8(const float *p, float *x)
+{
+    const float4 a = __ldg((const float4 *)p), b = __ldg((const float4 *)p + 1);
+    x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+}
+__device__ __forceinline__ float4 ld4(const float *p) { return *(const float4 *)p; }
+__device__ __forceinline__ void st4(float *p, float4 v) { *(float4 *)p = v; }
+__device__ __forceinline__ float dot4(float4 a, float4 b, float acc)
+{
+    return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, fmaf(a.x, b.x, acc))));
+}
+__device__ __forceinline__ float4 axpy4(float s, float4 x, float4 y)
+{
+    return make_float4(fmaf(s, x.x, y.x), fmaf(s, x.y, y.y), fmaf(s, x.z, y.z), fmaf(s, x.w, y.w));
+}
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src)
+{
+    const unsigned s = (unsigned)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+// The chunk's rows: row r (< 32) = token c*ct + r / nh, key r % nh; valid
+// while r < R and the token < T.
+struct ChunkRows {
+    size_t tok0;   // (b, first token of the chunk, h) row index of the [B,T,H] layouts
+    int nt;        // tokens of the chunk (<= ct)
+    int R;         // valid extended rows (nt * nh)
+};
+__device__ __forceinline__ ChunkRows chunk_rows(const CbArgs &a, int bh, int c)
+{
+    const int b = bh / a.H, h = bh - b * a.H, t0 = c * a.ct;
+    ChunkRows cr;
+    cr.tok0 = ((size_t)b * a.T + t0) * a.H + h;
+    cr.nt = min(a.ct, a.T - t0);
+    cr.R = cr.nt * a.nh;
+    return cr;
+}
+__device__ __forceinline__ size_t key_row(const CbArgs &a, const ChunkRows &cr, int r)
+{
+    const int t = r / a.nh, j = r - t * a.nh;
+    return (cr.tok0 + (size_t)t * a.H) * a.nh + j;
+}
+__device__ __forceinline__ size_t token_row(const CbArgs &a, const ChunkRows &cr, int t)
+{
+    return cr.tok0 + (size_t)t * a.H;
+}
+
+// fp32 [rows][kS] tile of the chunk's key rows (kKeys) or token rows of a
+// [.,128] tensor, zero past the valid rows; every thread takes part.
+template <bool kKeys, int kRows, typename TIn>
+__device__ __forceinline__ void stage_f32(const CbArgs &a, const ChunkRows &cr, const TIn *src, float *dst)
+{
+    for (int i = threadIdx.x; i < kRows * 16; i += blockDim.x) {
+        const int r = i >> 4, e = (i & 15) * 8;
+        float x[8];
+        if (r < (kKeys ? cr.R : cr.nt)) {
+            ldg8(src + (kKeys ? key_row(a, cr, r) : token_row(a, cr, r)) * kD + e, x);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[j] = 0.f;
+        }
+        st4(dst + r * kS + e, make_float4(x[0], x[1], x[2], x[3]));
+        st4(dst + r * kS + e + 4, make_float4(x[4], x[5], x[6], x[7]));
+    }
+}
+template <typename TIn>
+__device__ __forceinline__ void stage_betas(const CbArgs &a, const ChunkRows &cr, float *be)
+{
+    const TIn *beta = (const TIn *)a.beta;
+    for (int r = threadIdx.x; r < kC; r += blockDim.x) be[r] = r < cr.R ? to_f(beta[key_row(a, cr, r)]) : 0.f;
+}
+
+// ------------------------------------------------------------------ 1. prep
+constexpr int kPrepThreads = 256;
+constexpr int kPrepSmemFloats = 2 * kC * kS + kQ * kS + 2 * kC * kL + kC;
+
+template <typename TIn>
+__global__ void __launch_bounds__(kPrepThreads) cb_prep(const CbArgs a)
+{
+    extern __shared__ float4 sm_prep[];
+    float *Ks = (float *)sm_prep, *Vs = Ks + kC * kS, *Qs = Vs + kC * kS;
+    float *KK = Qs + kQ * kS, *Ts = KK + kC * kL, *be = Ts + kC * kL;
+    const int ci = blockIdx.x, bh = ci / a.nc, c = ci - bh * a.nc;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const ChunkRows cr = chunk_rows(a, bh, c);
+    float *rec = a.rec + (size_t)ci * kRecFloats;
+    stage_f32<true, kC, TIn>(a, cr, (const TIn *)a.k, Ks);
+    stage_f32<true, kC, TIn>(a, cr, (const TIn *)a.v, Vs);
+    stage_f32<false, kQ, TIn>(a, cr, (const TIn *)a.q, Qs);
+    stage_betas<TIn>(a, cr, be);
+    __syncthreads();
+    // K K^T rows w, w+8, w+16, w+24 and P rows w, w+8; lane = column s
+    {
+        float acc[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const float *ks = Ks + lane * kS;
+#pragma unroll 4
+        for (int d = 0; d < kD; d += 4) {
+            const float4 y = ld4(ks + d);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[i] = dot4(ld4(Ks + (w + 8 * i) * kS + d), y, acc[i]);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) acc[4 + i] = dot4(ld4(Qs + (w + 8 * i) * kS + d), y, acc[4 + i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            KK[(w + 8 * i) * kL + lane] = acc[i];
+            rec[kRecKK + (w + 8 * i) * kC + lane] = acc[i];
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int t = w + 8 * i;
+            rec[kRecP + t * kC + lane] = lane <= t * a.nh + a.nh - 1 ? acc[4 + i] : 0.f;
+        }
+    }
+    __syncthreads();
+    // T = (I + tril(B K K^T, -1))^{-1}: forward substitution, lane = column
+    if (w == 0) {
+        const int s = lane;
+        for (int r = 0; r < kC; ++r) {
+            float x = (r == s) ? 1.f : 0.f;
+            for (int m = s; m < r; ++m) x = fmaf(-be[r] * KK[r * kL + m], Ts[m * kL + s], x);
+            Ts[r * kL + s] = x;
+            rec[kRecT + r * kC + s] = x;
+        }
+    }
+    __syncthreads();
+    // W = T B K, U = T B V: warp w rows 4w .. 4w+3, lane = 4 columns
+    {
+        const int d = lane * 4, r0 = 4 * w;
+        float4 wa[4], ua[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) wa[i] = ua[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int m = 0; m <= r0 + 3; ++m) {   // T is lower triangular
+            const float4 k4 = ld4(Ks + m * kS + d), v4 = ld4(Vs + m * kS + d);
+            const float bm = be[m];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float tb = Ts[(r0 + i) * kL + m] * bm;
+                wa[i] = axpy4(tb, k4, wa[i]);
+                ua[i] = axpy4(tb, v4, ua[i]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            st4(rec + kRecW + (r0 + i) * kD + d, wa[i]);
+            st4(rec + kRecU + (r0 + i) * kD + d, ua[i]);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ 2. chains
+// CTA: (b,h), 32 value columns (blockIdx.y) and the direction (blockIdx.z).
+// Thread (warp w, lane): state rows 8w .. 8w+7 of column lane, and rows
+// 2w, 2w+1 of the chunk's U' (dU').
+constexpr int kChainThreads = 512;
+
+template <typename TIn>
+struct FwdStage {   // one chunk's operands of the forward chain
+    static constexpr size_t kW = (size_t)kC * kD * 4, kK = (size_t)kC * kD * sizeof(TIn), kU = (size_t)kC * 32 * 4;
+    static constexpr size_t kBytes = kW + kK + kU;
+};
+template <typename TIn, typename TDo>
+struct BwdStage {   // ... and of the reverse chain
+    static constexpr size_t kW = (size_t)kC * kD * 4, kK = (size_t)kC * kD * sizeof(TIn);
+    static constexpr size_t kQb = (size_t)kQ * kD * sizeof(TIn), kO = (size_t)kQ * 32 * sizeof(TDo);
+    static constexpr size_t kP = (size_t)kQ * kC * 4;
+    static constexpr size_t kBytes = kW + kK + kQb + kO + kP;
+};
+constexpr size_t kChainShared = (size_t)kD * 32 * 4 + (size_t)kC * kL * 4;   // state tile + rows tile
+template <typename TIn, typename TDo>
+constexpr size_t chain_smem_bytes()
+{
+    const size_t f = 2 * FwdStage<TIn>::kBytes, b = 2 * BwdStage<TIn, TDo>::kBytes;
+    return (f > b ? f : b) + kChainShared;
+}
+
+// cp.async of the chunk's key rows (TIn, [32][128]), zero rows past R
+template <typename TIn>
+__device__ __forceinline__ void copy_key_rows(const CbArgs &a, const ChunkRows &cr, const TIn *src, TIn *dst)
+{
+    constexpr int kPer = 16 / sizeof(TIn), kPerRow = kD / kPer;
+    for (int i = threadIdx.x; i < kC * kPerRow; i += kChainThreads) {
+        const int r = i / kPerRow, e = (i - r * kPerRow) * kPer;
+        if (r < cr.R) cp_async16(dst + r * kD + e, src + key_row(a, cr, r) * kD + e);
+        else *(uint4 *)(dst + r * kD + e) = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+// cp.async of the chunk's token rows, columns [col0, col0 + kCols), zero rows past nt
+template <int kCols, typename T>
+__device__ __forceinline__ void copy_token_rows(const CbArgs &a, const ChunkRows &cr, const T *src, int col0, T *dst)
+{
+    constexpr int kPer = 16 / sizeof(T), kPerRow = kCols / kPer;
+    for (int i = threadIdx.x; i < kQ * kPerRow; i += kChainThreads) {
+        const int t = i / kPerRow, e = (i - t * kPerRow) * kPer;
+        if (t < cr.nt) cp_async16(dst + t * kCols + e, src + token_row(a, cr, t) * kD + col0 + e);
+        else *(uint4 *)(dst + t * kCols + e) = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+__device__ __forceinline__ void copy_floats(const float *src, float *dst, int n)
+{
+    for (int i = threadIdx.x * 4; i < n; i += kChainThreads * 4) cp_async16(dst + i, src + i);
+}
+
+template <typename TIn>
+__device__ __forceinline__ void fwd_chain(const CbArgs &a, char *smem)
+{
+    using St = FwdStage<TIn>;
+    float *Ssm = (float *)(smem + 2 * St::kBytes), *up = Ssm + kD * 32;
+    const int bh = blockIdx.x, cg = blockIdx.y * 32, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int col = cg + lane, row0 = w * 8, r0 = 2 * w;
+    auto prefetch = [&](int c) {
+        char *base = smem + (c & 1) * St::kBytes;
+        const float *rec = a.rec + ((size_t)bh * a.nc + c) * kRecFloats;
+        copy_floats(rec + kRecW, (float *)base, kC * kD);
+        float *Ud = (float *)(base + St::kW + St::kK);
+        for (int i = threadIdx.x; i < kC * 8; i += kChainThreads) {
+            const int r = i >> 3, e = (i & 7) * 4;
+            cp_async16(Ud + r * 32 + e, rec + kRecU + r * kD + cg + e);
+        }
+        copy_key_rows<TIn>(a, chunk_rows(a, bh, c), (const TIn *)a.k, (TIn *)(base + St::kW));
+        cp_async_commit();
+    };
+    float S[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) S[i] = a.h0 ? a.h0[((size_t)bh * kD + row0 + i) * kD + col] : 0.f;
+    if (a.nc > 0) prefetch(0);
+    for (int c = 0; c < a.nc; ++c) {
+        const size_t ci = (size_t)bh * a.nc + c;
+        float *s0 = a.S0 + ci * kStateFloats;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            s0[(row0 + i) * kD + col] = S[i];
+            Ssm[(row0 + i) * 32 + lane] = S[i];
+        }
+        cp_async_wait_all();
+        __syncthreads();   // chunk c's stage and the state tile are complete; chunk c-1's stage is free
+        if (c + 1 < a.nc) prefetch(c + 1);
+        const char *base = smem + (c & 1) * St::kBytes;
+        const float *Wc = (const float *)base;
+        const TIn *Kc = (const TIn *)(base + St::kW);
+        const float *Uc = (const float *)(base + St::kW + St::kK);
+        // U' = U - W S, rows r0, r0 + 1
+        float u0 = Uc[r0 * 32 + lane], u1 = Uc[(r0 + 1) * 32 + lane];
+#pragma unroll 4
+        for (int k = 0; k < kD; k += 4) {
+            const float4 x0 = ld4(Wc + r0 * kD + k), x1 = ld4(Wc + (r0 + 1) * kD + k);
+            const float4 s = make_float4(Ssm[k * 32 + lane], Ssm[(k + 1) * 32 + lane], Ssm[(k + 2) * 32 + lane],
+                                         Ssm[(k + 3) * 32 + lane]);
+            u0 -= dot4(x0, s, 0.f);
+            u1 -= dot4(x1, s, 0.f);
+        }
+        up[r0 * kL + lane] = u0;
+        up[(r0 + 1) * kL + lane] = u1;
+        a.Up[ci * kRowsFloats + r0 * kD + col] = u0;
+        a.Up[ci * kRowsFloats + (r0 + 1) * kD + col] = u1;
+        __syncthreads();
+        // S += K^T U'
+#pragma unroll 4
+        for (int r = 0; r < kC; ++r) {
+            float kx[8];
+            lds8(Kc + r * kD + row0, kx);
+            const float u = up[r * kL + lane];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) S[i] = fmaf(kx[i], u, S[i]);
+        }
+    }
+}
+
+template <typename TIn, typename TDo>
+__device__ __forceinline__ void bwd_chain(const CbArgs &a, char *smem)
+{
+    using St = BwdStage<TIn, TDo>;
+    float *dSsm = (float *)(smem + 2 * St::kBytes), *dup = dSsm + kD * 32;
+    const int bh = blockIdx.x, cg = blockIdx.y * 32, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int col = cg + lane, row0 = w * 8, r0 = 2 * w;
+    auto prefetch = [&](int c) {
+        char *base = smem + (c & 1) * St::kBytes;
+        const float *rec = a.rec + ((size_t)bh * a.nc + c) * kRecFloats;
+        const ChunkRows cr = chunk_rows(a, bh, c);
+        copy_floats(rec + kRecW, (float *)base, kC * kD);
+        copy_key_rows<TIn>(a, cr, (const TIn *)a.k, (TIn *)(base + St::kW));
+        copy_token_rows<kD, TIn>(a, cr, (const TIn *)a.q, 0, (TIn *)(base + St::kW + St::kK));
+        copy_token_rows<32, TDo>(a, cr, (const TDo *)a.d_o, cg, (TDo *)(base + St::kW + St::kK + St::kQb));
+        copy_floats(rec + kRecP, (float *)(base + St::kW + St::kK + St::kQb + St::kO), kQ * kC);
+        cp_async_commit();
+    };
+    float dS[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dS[i] = a.dh_final ? a.dh_final[((size_t)bh * kD + row0 + i) * kD + col] : 0.f;
+    if (a.nc > 0) prefetch(a.nc - 1);
+    for (int c = a.nc - 1; c >= 0; --c) {
+        const size_t ci = (size_t)bh * a.nc + c;
+        float *ds1 = a.dS1 + ci * kStateFloats;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            ds1[(row0 + i) * kD + col] = dS[i];
+            dSsm[(row0 + i) * 32 + lane] = dS[i];
+        }
+        cp_async_wait_all();
+        __syncthreads();
+        if (c > 0) prefetch(c - 1);
+        const char *base = smem + (c & 1) * St::kBytes;
+        const float *Wc = (const float *)base;
+        const TIn *Kc = (const TIn *)(base + St::kW);
+        const TIn *Qc = (const TIn *)(base + St::kW + St::kK);
+        const TDo *Oc = (const TDo *)(base + St::kW + St::kK + St::kQb);
+        const float *Pc = (const float *)(base + St::kW + St::kK + St::kQb + St::kO);
+        // dU' = P^T dO + K dS1, rows r0, r0 + 1
+        float g0 = 0.f, g1 = 0.f;
+#pragma unroll 4
+        for (int t = 0; t < kQ; ++t) {
+            const float o = to_f(Oc[t * 32 + lane]);
+            g0 = fmaf(Pc[t * kC + r0], o, g0);
+            g1 = fmaf(Pc[t * kC + r0 + 1], o, g1);
+        }
+#pragma unroll 2
+        for (int k = 0; k < kD; k += 8) {
+            float k0[8], k1[8];
+            lds8(Kc + r0 * kD + k, k0);
+            lds8(Kc + (r0 + 1) * kD + k, k1);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float s = dSsm[(k + j) * 32 + lane];
+                g0 = fmaf(k0[j], s, g0);
+                g1 = fmaf(k1[j], s, g1);
+            }
+        }
+        dup[r0 * kL + lane] = g0;
+        dup[(r0 + 1) * kL + lane] = g1;
+        a.dUp[ci * kRowsFloats + r0 * kD + col] = g0;
+        a.dUp[ci * kRowsFloats + (r0 + 1) * kD + col] = g1;
+        __syncthreads();
+        // dS0 = dS1 + Q^T dO - W^T dU'
+#pragma unroll 4
+        for (int t = 0; t < kQ; ++t) {
+            float qx[8];
+            lds8(Qc + t * kD + row0, qx);
+            const float o = to_f(Oc[t * 32 + lane]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dS[i] = fmaf(qx[i], o, dS[i]);
+        }
+#pragma unroll 4
+        for (int r = 0; r < kC; ++r) {
+            float wx[8];
+            lds8(Wc + r * kD + row0, wx);
+            const float g = dup[r * kL + lane];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dS[i] = fmaf(-wx[i], g, dS[i]);
+        }
+    }
+    if (a.dh0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a.dh0[((size_t)bh * kD + row0 + i) * kD + col] = dS[i];
+    }
+}
+
+template <typename TIn, typename TDo>
+__global__ void __launch_bounds__(kChainThreads, 2) cb_chains(const CbArgs a)
+{
+    extern __shared__ float4 sm_chain[];
+    if (blockIdx.z == 0) fwd_chain<TIn>(a, (char *)sm_chain);
+    else bwd_chain<TIn, TDo>(a, (char *)sm_chain);
+}
+
+// ------------------------------------------------------------------ 3. per-chunk gradients
+constexpr int kGradThreads = 512;
+constexpr int kGradSmemFloats = 6 * kC * kS + 3 * kQ * kS + 4 * kC * kL + kQ * kL + kC;
+
+// sum over the 4 lanes of a quad (all four get it)
+__device__ __forceinline__ float quad_sum(float x)
+{
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    return x + __shfl_xor_sync(0xffffffffu, x, 2);
+}
+
+template <typename TIn, typename TDo>
+__global__ void __launch_bounds__(kGradThreads, 1) cb_grad(const CbArgs a)
+{
+    extern __shared__ float4 sm_grad[];
+    float *Ks = (float *)sm_grad, *Vs = Ks + kC * kS, *Ups = Vs + kC * kS, *dUps = Ups + kC * kS;
+    float *dWs = dUps + kC * kS, *dKs = dWs + kC * kS;
+    float *Qs = dKs + kC * kS, *dOs = Qs + kQ * kS, *dQs = dOs + kQ * kS;
+    float *Ts = dQs + kQ * kS, *KKs = Ts + kC * kL, *dTs = KKs + kC * kL, *Xs = dTs + kC * kL;
+    float *dPs = Xs + kC * kL, *be = dPs + kQ * kL;
+    const int ci = blockIdx.x, bh = ci / a.nc, c = ci - bh * a.nc;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const ChunkRows cr = chunk_rows(a, bh, c);
+    const float *rec = a.rec + (size_t)ci * kRecFloats;
+
+    // the thread's quarter rows of S0 and dS1: row kk = tid / 4, float4
+    // columns 16 i + 4 qq (qq = tid % 4), i = 0 .. 7
+    const int kk = tid >> 2, qq = tid & 3;
+    float4 s0q[8], ds1q[8];
+    {
+        const float *s0 = a.S0 + (size_t)ci * kStateFloats + kk * kD + 4 * qq;
+        const float *ds1 = a.dS1 + (size_t)ci * kStateFloats + kk * kD + 4 * qq;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            s0q[i] = __ldg((const float4 *)(s0 + 16 * i));
+            ds1q[i] = __ldg((const float4 *)(ds1 + 16 * i));
+        }
+    }
+    stage_f32<true, kC, TIn>(a, cr, (const TIn *)a.k, Ks);
+    stage_f32<true, kC, TIn>(a, cr, (const TIn *)a.v, Vs);
+    stage_f32<false, kQ, TIn>(a, cr, (const TIn *)a.q, Qs);
+    stage_f32<false, kQ, TDo>(a, cr, (const TDo *)a.d_o, dOs);
+    stage_betas<TIn>(a, cr, be);
+    {
+        const float *up = a.Up + (size_t)ci * kRowsFloats, *dup = a.dUp + (size_t)ci * kRowsFloats;
+        for (int i = tid; i < kC * kD / 4; i += kGradThreads) {
+            const int r = i >> 5, e = (i & 31) * 4;
+            st4(Ups + r * kS + e, __ldg((const float4 *)(up + r * kD + e)));
+            st4(dUps + r * kS + e, __ldg((const float4 *)(dup + r * kD + e)));
+        }
+        for (int i = tid; i < kC * kC; i += kGradThreads) {
+            Ts[(i >> 5) * kL + (i & 31)] = rec[kRecT + i];
+            KKs[(i >> 5) * kL + (i & 31)] = rec[kRecKK + i];
+        }
+    }
+    __syncthreads();
+
+    // dP = (dO U'^T) masked: row t = w, column s = lane
+    {
+        float acc = 0.f;
+        const float *x = dOs + w * kS, *y = Ups + lane * kS;
+#pragma unroll 8
+        for (int d = 0; d < kD; d += 4) acc = dot4(ld4(x + d), ld4(y + d), acc);
+        dPs[w * kL + lane] = lane <= w * a.nh + a.nh - 1 ? acc : 0.f;
+    }
+    // dQ0 = dO S0^T, dW = -dU' S0^T, dK0 = U' dS1^T: column kk, over quads
+    {
+        auto row_dot = [&](const float *x, const float4 *sq) {
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc = dot4(ld4(x + 16 * i + 4 * qq), sq[i], acc);
+            return quad_sum(acc);
+        };
+#pragma unroll 2
+        for (int t = 0; t < kQ; ++t) {
+            const float v = row_dot(dOs + t * kS, s0q);
+            if (qq == 0) dQs[t * kS + kk] = v;
+        }
+#pragma unroll 2
+        for (int r = 0; r < kC; ++r) {
+            const float vw = row_dot(dUps + r * kS, s0q);
+            const float vk = row_dot(Ups + r * kS, ds1q);
+            if (qq == 0) {
+                dWs[r * kS + kk] = -vw;
+                dKs[r * kS + kk] = vk;
+            }
+        }
+    }
+    __syncthreads();
+
+    // dQ = dQ0 + dP K (row t = w, columns 4 lane .. 4 lane + 3) -> global
+    {
+        const int d = 4 * lane;
+        float4 acc = ld4(dQs + w * kS + d);
+#pragma unroll 8
+        for (int s = 0; s < kC; ++s) acc = axpy4(dPs[w * kL + s], ld4(Ks + s * kS + d), acc);
+        if (w < cr.nt) st4(a.dq + token_row(a, cr, w) * kD + d, acc);
+    }
+    // dT = (dW K^T + dU' V^T) B: rows 2w, 2w+1, column m = lane
+    {
+        float t0 = 0.f, t1 = 0.f;
+        const float *km = Ks + lane * kS, *vm = Vs + lane * kS;
+        const float *w0 = dWs + 2 * w * kS, *w1 = w0 + kS, *u0 = dUps + 2 * w * kS, *u1 = u0 + kS;
+#pragma unroll 4
+        for (int d = 0; d < kD; d += 4) {
+            const float4 k4 = ld4(km + d), v4 = ld4(vm + d);
+            t0 = dot4(ld4(u0 + d), v4, dot4(ld4(w0 + d), k4, t0));
+            t1 = dot4(ld4(u1 + d), v4, dot4(ld4(w1 + d), k4, t1));
+        }
+        dTs[2 * w * kL + lane] = t0 * be[lane];
+        dTs[(2 * w + 1) * kL + lane] = t1 * be[lane];
+    }
+    __syncthreads();
+    // X = dT T^T: rows 2w, 2w+1, column m = lane
+    {
+        float x0 = 0.f, x1 = 0.f;
+#pragma unroll 8
+        for (int j = 0; j < kC; ++j) {
+            const float tm = Ts[lane * kL + j];
+            x0 = fmaf(dTs[2 * w * kL + j], tm, x0);
+            x1 = fmaf(dTs[(2 * w + 1) * kL + j], tm, x1);
+        }
+        Xs[2 * w * kL + lane] = x0;
+        Xs[(2 * w + 1) * kL + lane] = x1;
+    }
+    __syncthreads();
+    // dG = strictly lower part of -T^T X (into dT's tile): rows 2w, 2w+1, column s = lane
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int r = 2 * w + i;
+        float g = 0.f;
+        for (int j = r; j < kC; ++j) g = fmaf(-Ts[j * kL + r], Xs[j * kL + lane], g);   // T[j][r] = 0 for j < r
+        dTs[r * kL + lane] = lane < r ? g : 0.f;
+    }
+    __syncthreads();
+    // rows m = 2w, 2w+1, columns 4 lane .. 4 lane + 3:
+    //   dK = dK0 + dP^T Q + B (T^T dW + dG K) + (B dG)^T K,  dV = B T^T dU'
+    //   dbeta = sum over columns of K o T^T dW + V o T^T dU', + sum_s dG o K K^T
+    {
+        const int d = 4 * lane;
+#pragma unroll 1
+        for (int i = 0; i < 2; ++i) {
+            const int m = 2 * w + i;
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 tw = z, tu = z, gk = z, gtk = z, pq = z;
+            for (int r = m; r < kC; ++r) {
+                const float t = Ts[r * kL + m];
+                tw = axpy4(t, ld4(dWs + r * kS + d), tw);
+                tu = axpy4(t, ld4(dUps + r * kS + d), tu);
+            }
+            for (int s = 0; s < m; ++s) gk = axpy4(dTs[m * kL + s], ld4(Ks + s * kS + d), gk);
+            for (int r = m + 1; r < kC; ++r) gtk = axpy4(be[r] * dTs[r * kL + m], ld4(Ks + r * kS + d), gtk);
+#pragma unroll 4
+            for (int t = 0; t < kQ; ++t) pq = axpy4(dPs[t * kL + m], ld4(Qs + t * kS + d), pq);
+            const float bm = be[m];
+            const float4 k0 = ld4(dKs + m * kS + d);
+            const float4 dk = make_float4(k0.x + pq.x + bm * (tw.x + gk.x) + gtk.x, k0.y + pq.y + bm * (tw.y + gk.y) + gtk.y,
+                                          k0.z + pq.z + bm * (tw.z + gk.z) + gtk.z, k0.w + pq.w + bm * (tw.w + gk.w) + gtk.w);
+            const float4 dv = make_float4(bm * tu.x, bm * tu.y, bm * tu.z, bm * tu.w);
+            float db = dot4(ld4(Ks + m * kS + d), tw, dot4(ld4(Vs + m * kS + d), tu, 0.f));
+            if (lane < m) db = fmaf(dTs[m * kL + lane], KKs[m * kL + lane], db);
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) db += __shfl_xor_sync(0xffffffffu, db, o);
+            if (m < cr.R) {
+                const size_t row = key_row(a, cr, m);
+                st4(a.dk + row * kD + d, dk);
+                st4(a.dv + row * kD + d, dv);
+                if (lane == 0) a.dbeta[row] = db;
+            }
+        }
+    }
+}
+
+template <typename TIn, typename TDo>
+cudaError_t launch_typed(const BwdProblem &p, const CbArgs &a)
+{
+    const size_t n_chunks = (size_t)p.B * p.H * a.nc;
+    cudaError_t e;
+    const int chain_smem = (int)chain_smem_bytes<TIn, TDo>();
+    if ((e = cudaFuncSetAttribute(cb_chains<TIn, TDo>, cudaFuncAttributeMaxDynamicSharedMemorySize, chain_smem)) !=
+        cudaSuccess)
+        return e;
+    if (n_chunks == 0) {   // T = 0: dh0 = dh_final (the reverse chains only)
+        cb_chains<TIn, TDo><<<dim3(p.B * p.H, kD / 32, 2), kChainThreads, chain_smem, p.stream>>>(a);
+        return cudaGetLastError();
+    }
+    const int prep_smem = (int)(kPrepSmemFloats * sizeof(float));
+    if ((e = cudaFuncSetAttribute(cb_prep<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem)) != cudaSuccess)
+        return e;
+    cb_prep<TIn><<<(unsigned)n_chunks, kPrepThreads, prep_smem, p.stream>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    cb_chains<TIn, TDo><<<dim3(p.B * p.H, kD / 32, 2), kChainThreads, chain_smem, p.stream>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int grad_smem = (int)(kGradSmemFloats * sizeof(float));
+    if ((e = cudaFuncSetAttribute(cb_grad<TIn, TDo>, cudaFuncAttributeMaxDynamicSharedMemorySize, grad_smem)) !=
+        cudaSuccess)
+        return e;
+    cb_grad<TIn, TDo><<<(unsigned)n_chunks, kGradThreads, grad_smem, p.stream>>>(a);
+    return cudaGetLastError();
+}
+
+int chunk_tokens(int nh) { return (kC / nh < kQ) ? kC / nh : kQ; }
+
+}  // namespace
+
+bool backward_chunk_shape_ok(const BwdProblem &p)
+{
+    return p.cu == nullptr && p.Dk == kD && p.Dv == kD && p.nh >= 1 && p.nh <= kC;
+}
+
+bool backward_chunk_supported(const BwdProblem &p) { return p.g == nullptr && backward_chunk_shape_ok(p); }
+
+size_t backward_chunk_scratch_bytes(const BwdProblem &p)
+{
+    if (!backward_chunk_shape_ok(p)) return 0;
+    const int ct = chunk_tokens(p.nh);
+    const size_t nc = (size_t)(p.T + ct - 1) / ct, n = (size_t)p.B * p.H * nc;
+    return n * (kRecFloats + 2 * kStateFloats + 2 * kRowsFloats) * sizeof(float);
+}
+
+cudaError_t launch_backward_chunk(const BwdProblem &p)
+{
+    CbArgs a;
+    a.B = p.B; a.T = p.T; a.H = p.H; a.nh = p.nh;
+    a.ct = chunk_tokens(p.nh);
+    a.nc = (p.T + a.ct - 1) / a.ct;
+    a.q = p.q; a.k = p.k; a.v = p.v; a.beta = p.beta; a.h0 = p.h0;
+    a.d_o = p.d_o; a.dh_final = p.dh_final;
+    a.dq = p.dq; a.dk = p.dk; a.dv = p.dv; a.dbeta = p.dbeta; a.dh0 = p.dh0;
+    const size_t n = (size_t)p.B * p.H * a.nc;
+    a.rec = (float *)p.scratch;
+    a.S0 = a.rec + n * kRecFloats;
+    a.dS1 = a.S0 + n * kStateFloats;
+    a.Up = a.dS1 + n * kStateFloats;
+    a.dUp = a.Up + n * kRowsFloats;
+    if (p.dtype == DP_F32) return launch_typed<float, float>(p, a);
+    return p.do_dtype == DP_F32 ? launch_typed<__nv_bfloat16, float>(p, a)
+                                : launch_typed<__nv_bfloat16, __nv_bfloat16>(p, a);
+}
+
+}  // namespace dp

@@ -66,6 +66,12 @@ struct BwdProblem {
 int backward_segment_tokens(int Dk);
 size_t backward_scratch_bytes(const BwdProblem &p);
 cudaError_t launch_backward(const BwdProblem &p);
+// Chunked backward (ungated, dense, D_k = D_v = 128): per-chunk records and
+// the chunk-boundary states and gradients in the scratch area.
+bool backward_chunk_shape_ok(const BwdProblem &p);   // dims only (g not known)
+bool backward_chunk_supported(const BwdProblem &p);  // dims and g == NULL
+size_t backward_chunk_scratch_bytes(const BwdProblem &p);
+cudaError_t launch_backward_chunk(const BwdProblem &p);
 
 cudaError_t launch_state_io(int op, int B, int H, int Dk, int Dv, float *state,
                             void *ext, int ext_dtype, int ext_transposed,

@@ -123,8 +123,8 @@ def test_varlen_validation(L):
 def test_backward_workspace_and_validation(L):
     """dp_backward_workspace_size: status block, one fp32 D_k x D_v
     checkpoint per (b,h) every segment of tokens and every sub-step's error;
-    dp_backward rejects NULL
-    inputs, an explicit impl and a short workspace before any launch."""
+    dp_backward rejects NULL inputs, an unknown impl and a short workspace
+    before any launch."""
     import ctypes as C
     n = C.c_size_t(0)
     dims = _lib.make_dims(2, 100, 3, 128, 64, 2, _lib.DP_BF16, "auto", _lib.DP_F32)
@@ -138,7 +138,26 @@ def test_backward_workspace_and_validation(L):
     assert L.dp_backward_workspace_size(C.byref(d32), C.byref(n)) == 0
     assert n.value == 256 + r256(r256(((100 + 47) // 48) * 32 * 32 * 4) + 100 * 32 * 4)
     explicit = _lib.make_dims(2, 100, 3, 128, 64, 2, _lib.DP_BF16, "recurrent")
-    assert L.dp_backward_workspace_size(C.byref(explicit), C.byref(n)) == 1
+    m = C.c_size_t(0)
+    assert L.dp_backward_workspace_size(C.byref(explicit), C.byref(m)) == 0
+    assert m.value == 256 + r256(r256(ck) + errs)
+    assert L.dp_backward_workspace_size(C.byref(_lib.make_dims(2, 100, 3, 128, 64, 2, _lib.DP_BF16, 7)),
+                                        C.byref(m)) == 1
+    # D_k = D_v = 128: the chunked form's records (ct = 16 tokens per chunk at
+    # n_h = 2; per chunk W, U [32,128], T [32,32], P [16,32], K K^T [32,32],
+    # the state at its start and the gradient at its end [128,128], U' and
+    # dU' [32,128], fp32)
+    rec = lambda impl: _lib.make_dims(2, 100, 3, 128, 128, 2, _lib.DP_BF16, impl, _lib.DP_F32)
+    ck128 = 2 * 3 * ((100 + seg - 1) // seg) * 128 * 128 * 4
+    need_rec = 256 + r256(r256(ck128) + 2 * 100 * 3 * 2 * 128 * 4)
+    chunks = 2 * 3 * ((100 + 15) // 16)
+    need_chunk = 256 + r256(chunks * (2 * 32 * 128 + 32 * 32 + 16 * 32 + 32 * 32 + 2 * 128 * 128 + 2 * 32 * 128) * 4)
+    for impl, want in (("recurrent", need_rec), ("chunk_tc", need_chunk), ("auto", max(need_rec, need_chunk))):
+        assert L.dp_backward_workspace_size(C.byref(rec(impl)), C.byref(m)) == 0 and m.value == want, impl
+    # packed sequences take the recurrent form only
+    vl = _lib.make_dims(2, 100, 3, 128, 128, 2, _lib.DP_BF16, "auto", _lib.DP_F32, max_seqlen=60)
+    assert L.dp_backward_workspace_size(C.byref(vl), C.byref(m)) == 0
+    assert m.value == 256 + r256(r256(2 * 3 * 5 * 128 * 128 * 4) + 2 * 60 * 3 * 2 * 128 * 4)
     assert L.dp_backward_workspace_size(C.byref(dims), None) == 1
     null = [None] * 15
     assert L.dp_backward(C.byref(dims), *null, C.c_size_t(0), None) == 1

@@ -48,11 +48,11 @@ def cotangents(w, seed, do_dtype=torch.float32):
     return d_o, dhf
 
 
-def run_both(dp, w, d_o, dhf, heads=None):
+def run_both(dp, w, d_o, dhf, heads=None, impl="auto"):
     x = W.make_inputs(w)
     xc = {k: (None if v is None else v.cuda()) for k, v in x.items()}
     got = dp.backward(xc["q"], xc["k"], xc["v"], xc["beta"], xc["g"], xc["h0"], d_o=d_o.cuda(),
-                      dh_final=None if dhf is None else dhf.cuda())
+                      dh_final=None if dhf is None else dhf.cuda(), impl=impl)
     torch.cuda.synchronize()
     if heads is None:
         ref = oracle.backward(x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"], d_o, dhf)
@@ -227,3 +227,48 @@ def test_backward_chains_across_calls(dp):
         assert s["rel_max"] <= TOL_REL, (n, s)
     s = err_stats(g1["dh0"], full["dh0"].cpu().double().numpy())
     assert s["rel_max"] <= TOL_REL, ("dh0", s)
+
+
+# Ungated, D_k = D_v = 128: the chunked form (auto's choice) and the recurrent
+# form, each against the oracle. Chunks hold min(16, 32 / n_h) tokens; the
+# cases cut the sequence into several chunks with a ragged last one, a
+# single exact chunk, one token, and both input dtypes.
+CHUNK_CASES = [
+    ("nh1-ragged", W.BASE.scaled(B=2, H=2, T=40, nh=1), 20),
+    ("nh2-h0", W.BASE.scaled(B=1, H=2, T=37, h0_std=0.02), 21),
+    ("nh3-neardup", W.NEARDUP.scaled(B=1, H=2, T=31), 22),
+    ("nh4-beta2-h0", W.GATED.scaled(B=1, H=2, T=27, gated=False), 23),
+    ("f32-nh2", W.BASE.scaled(B=1, H=1, T=20, dtype="f32"), 24),
+    ("one-chunk", W.BASE.scaled(B=1, H=1, T=16), 25),
+    ("one-token", W.BASE.scaled(B=2, H=1, T=1), 26),
+]
+
+
+@pytest.mark.parametrize("impl", ["chunk_tc", "recurrent"])
+@pytest.mark.parametrize("name,w,seed", CHUNK_CASES, ids=[c[0] for c in CHUNK_CASES])
+def test_backward_ungated_forms(dp, name, w, seed, impl):
+    d_o, dhf = cotangents(w, 200 + seed)
+    got, ref, _ = run_both(dp, w, d_o, dhf, impl=impl)
+    stats = check(got, ref, f"{impl} {name}")
+    print(impl, name, {n: round(s["rel_max"], 8) for n, s in stats.items()})
+
+
+def test_backward_chunked_bf16_cotangent_and_empty(dp):
+    w = W.BASE.scaled(B=1, H=2, T=45, nh=3)
+    d_o, _ = cotangents(w, 230, torch.bfloat16)
+    got, ref, _ = run_both(dp, w, d_o, None, impl="chunk_tc")
+    check(got, ref, "chunked, bf16 d_o")
+    w0 = W.BASE.scaled(B=2, H=2, T=0)
+    d_o, dhf = cotangents(w0, 231)
+    got, _, _ = run_both(dp, w0, d_o, dhf, impl="chunk_tc")
+    assert torch.equal(got["dh0"].cpu(), dhf)
+
+
+def test_backward_chunked_unsupported(dp):
+    """The chunked form takes ungated dense problems with D = 128 only."""
+    w = W.GATED.scaled(B=1, H=1, T=8, nh=2)
+    x = {k: (None if v is None else v.cuda()) for k, v in W.make_inputs(w).items()}
+    with pytest.raises(dp.DPError) as e:
+        dp.backward(x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"], d_o=torch.zeros(1, 8, 1, 128, device="cuda"),
+                    impl="chunk_tc")
+    assert e.value.code == 2
