@@ -16,18 +16,21 @@
 //   dV  = diag(beta) T^T dU',  dW = -dU' S0^T,  B = diag(beta)
 //   dbeta = rowsum(K o T^T dW) + rowsum(V o T^T dU') + rowsum(dG o K K^T)
 //   dT = dW (B K)^T + dU' (B V)^T,  dG = strictly lower part of -T^T dT T^T
-// Three launches:
-//   cb_prep    every chunk at once: T, W, U, P, K K^T into its record;
+// Four launches:
+//   cb_prep    every chunk at once: T, W, U, P, K K^T and fp32 K, Q into its
+//              record;
 //   cb_chains  per (b,h) and 32 value columns, chunk by chunk, two
 //              independent CTAs: the forward chain (S <- S + K^T (U - W S))
 //              stores S0 and U' of every chunk; the reverse chain (the
 //              transposed recurrence above, from the last chunk) stores dS1
-//              and dU' of every chunk and dh0. The next chunk's tiles are
+//              and dU' of every chunk and dh0. The next chunk's operands are
 //              copied in (cp.async) while the current one is processed;
-//   cb_grad    every chunk at once: dq, dk, dv, dbeta from its blocks. The
-//              three products with the 128 x 128 boundary states (dO S0^T,
-//              dU' S0^T, U' dS1^T) take 60% of its arithmetic; each thread
-//              holds a quarter row of S0 and of dS1 in registers for them.
+//   cb_grad_s  every chunk at once, the products with the 128 x 128
+//              boundary states (60% of the per-chunk arithmetic):
+//              dq <- dO S0^T, dk <- U' dS1^T, dW = -dU' S0^T and dP; each
+//              thread holds a quarter row of S0, then of dS1, in registers;
+//   cb_grad_r  every chunk at once, the rest: dq += dP K, dk += ..., dv,
+//              dbeta.
 // The chains carry the only sequential dependency, as 32 x 128 x 128
 // products per chunk instead of a matrix-vector product per sub-step.
 #include "internal.h"
@@ -41,10 +44,13 @@ constexpr int kQ = 16;     // token rows per chunk (padded)
 constexpr int kS = 132;    // fp32 row stride of [.][128] tiles: float4-aligned, rows spread over the banks
 constexpr int kL = kC + 1; // row stride of [.][32] tiles
 
-// record of one chunk (fp32): W [32][128] | U [32][128] | T [32][32] | P [16][32] | K K^T [32][32]
+// record of one chunk (fp32): W [32][128] | U [32][128] | T [32][32] |
+// P [16][32] | K K^T [32][32] | K [32][128] | Q [16][128] (K and Q as fp32
+// for the chains). After the chains, cb_grad_s overwrites W with dW and P
+// with dP, which cb_grad_r reads.
 constexpr size_t kRecW = 0, kRecU = kC * kD, kRecT = 2 * kC * kD, kRecP = kRecT + kC * kC;
-constexpr size_t kRecKK = kRecP + kQ * kC;
-constexpr size_t kRecFloats = kRecKK + kC * kC;
+constexpr size_t kRecKK = kRecP + kQ * kC, kRecK = kRecKK + kC * kC, kRecQ = kRecK + kC * kD;
+constexpr size_t kRecFloats = kRecQ + kQ * kD;
 constexpr size_t kStateFloats = (size_t)kD * kD;   // S0 or dS1 of one chunk
 constexpr size_t kRowsFloats = (size_t)kC * kD;    // U' or dU' of one chunk
 
@@ -69,14 +75,8 @@ __device__ __forceinline__ void unpack8(const uint4 u, float *x)
     x[4] = __uint_as_float(u.z << 16), x[5] = __uint_as_float(u.z & 0xffff0000u);
     x[6] = __uint_as_float(u.w << 16), x[7] = __uint_as_float(u.w & 0xffff0000u);
 }
-// 8 consecutive elements (16-byte aligned) as fp32, from shared memory
-__device__ __forceinline__ void lds8(const __nv_bfloat16 *p, float *x) { unpack8(*(const uint4 *)p, x); }
-__device__ __forceinline__ void lds8(const float *p, float *x)
-{
-    const float4 a = ((const float4 *)p)[0], b = ((const float4 *)p)[1];
-    x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
-}
-// ... and from global memory (read-only during the kernel)
+// 8 consecutive elements (16-byte aligned) as fp32, from global memory
+// (read-only during the kernel)
 __device__ __forceinline__ void ldg8(const __nv_bfloat16 *p, float *x) { unpack8(__ldg((const uint4 *)p), x); }
 __device__ __forceinline__ void ldg8(const float *p, float *x)
 {
@@ -172,6 +172,12 @@ __global__ void __launch_bounds__(kPrepThreads) cb_prep(const CbArgs a)
     stage_f32<false, kQ, TIn>(a, cr, (const TIn *)a.q, Qs);
     stage_betas<TIn>(a, cr, be);
     __syncthreads();
+    // fp32 K and Q (zero padding rows included) for the chains
+    for (int i = threadIdx.x; i < (kC + kQ) * kD / 4; i += kPrepThreads) {
+        const int r = i >> 5, e = (i & 31) * 4;
+        if (r < kC) st4(rec + kRecK + r * kD + e, ld4(Ks + r * kS + e));
+        else st4(rec + kRecQ + (r - kC) * kD + e, ld4(Qs + (r - kC) * kS + e));
+    }
     // K K^T rows w, w+8, w+16, w+24 and P rows w, w+8; lane = column s
     {
         float acc[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -234,73 +240,69 @@ __global__ void __launch_bounds__(kPrepThreads) cb_prep(const CbArgs a)
 // ------------------------------------------------------------------ 2. chains
 // CTA: (b,h), 32 value columns (blockIdx.y) and the direction (blockIdx.z).
 // Thread (warp w, lane): state rows 8w .. 8w+7 of column lane, and rows
-// 2w, 2w+1 of the chunk's U' (dU').
+// 2w, 2w+1 of the chunk's U' (dU'). The state and U' (dU') are also kept
+// transposed in shared memory ([column][row]) so that a thread reads its
+// column four rows at a time.
 constexpr int kChainThreads = 512;
+constexpr int kTS = kD + 4;    // row stride of the transposed state tile
+constexpr int kTU = kC + 4;    // row stride of the transposed U' tile
 
-template <typename TIn>
-struct FwdStage {   // one chunk's operands of the forward chain
-    static constexpr size_t kW = (size_t)kC * kD * 4, kK = (size_t)kC * kD * sizeof(TIn), kU = (size_t)kC * 32 * 4;
+struct FwdStage {   // one chunk's operands of the forward chain (fp32)
+    static constexpr size_t kW = (size_t)kC * kD * 4, kK = (size_t)kC * kD * 4, kU = (size_t)kC * 32 * 4;
     static constexpr size_t kBytes = kW + kK + kU;
 };
-template <typename TIn, typename TDo>
+template <typename TDo>
 struct BwdStage {   // ... and of the reverse chain
-    static constexpr size_t kW = (size_t)kC * kD * 4, kK = (size_t)kC * kD * sizeof(TIn);
-    static constexpr size_t kQb = (size_t)kQ * kD * sizeof(TIn), kO = (size_t)kQ * 32 * sizeof(TDo);
-    static constexpr size_t kP = (size_t)kQ * kC * 4;
+    static constexpr size_t kW = (size_t)kC * kD * 4, kK = (size_t)kC * kD * 4, kQb = (size_t)kQ * kD * 4;
+    static constexpr size_t kO = (size_t)kQ * 32 * sizeof(TDo), kP = (size_t)kQ * kC * 4;
     static constexpr size_t kBytes = kW + kK + kQb + kO + kP;
 };
-constexpr size_t kChainShared = (size_t)kD * 32 * 4 + (size_t)kC * kL * 4;   // state tile + rows tile
-template <typename TIn, typename TDo>
+constexpr size_t kChainShared = (size_t)32 * kTS * 4 + (size_t)32 * kTU * 4;
+template <typename TDo>
 constexpr size_t chain_smem_bytes()
 {
-    const size_t f = 2 * FwdStage<TIn>::kBytes, b = 2 * BwdStage<TIn, TDo>::kBytes;
+    const size_t f = 2 * FwdStage::kBytes, b = 2 * BwdStage<TDo>::kBytes;
     return (f > b ? f : b) + kChainShared;
 }
 
-// cp.async of the chunk's key rows (TIn, [32][128]), zero rows past R
-template <typename TIn>
-__device__ __forceinline__ void copy_key_rows(const CbArgs &a, const ChunkRows &cr, const TIn *src, TIn *dst)
+// cp.async of the chunk's token rows of d_o, columns [col0, col0 + 32), zero rows past nt
+template <typename T>
+__device__ __forceinline__ void copy_do_rows(const CbArgs &a, const ChunkRows &cr, const T *src, int col0, T *dst)
 {
-    constexpr int kPer = 16 / sizeof(TIn), kPerRow = kD / kPer;
-    for (int i = threadIdx.x; i < kC * kPerRow; i += kChainThreads) {
-        const int r = i / kPerRow, e = (i - r * kPerRow) * kPer;
-        if (r < cr.R) cp_async16(dst + r * kD + e, src + key_row(a, cr, r) * kD + e);
-        else *(uint4 *)(dst + r * kD + e) = make_uint4(0u, 0u, 0u, 0u);
-    }
-}
-// cp.async of the chunk's token rows, columns [col0, col0 + kCols), zero rows past nt
-template <int kCols, typename T>
-__device__ __forceinline__ void copy_token_rows(const CbArgs &a, const ChunkRows &cr, const T *src, int col0, T *dst)
-{
-    constexpr int kPer = 16 / sizeof(T), kPerRow = kCols / kPer;
+    constexpr int kPer = 16 / sizeof(T), kPerRow = 32 / kPer;
     for (int i = threadIdx.x; i < kQ * kPerRow; i += kChainThreads) {
         const int t = i / kPerRow, e = (i - t * kPerRow) * kPer;
-        if (t < cr.nt) cp_async16(dst + t * kCols + e, src + token_row(a, cr, t) * kD + col0 + e);
-        else *(uint4 *)(dst + t * kCols + e) = make_uint4(0u, 0u, 0u, 0u);
+        if (t < cr.nt) cp_async16(dst + t * 32 + e, src + token_row(a, cr, t) * kD + col0 + e);
+        else *(uint4 *)(dst + t * 32 + e) = make_uint4(0u, 0u, 0u, 0u);
     }
 }
 __device__ __forceinline__ void copy_floats(const float *src, float *dst, int n)
 {
     for (int i = threadIdx.x * 4; i < n; i += kChainThreads * 4) cp_async16(dst + i, src + i);
 }
+// 8 consecutive fp32 of shared memory (32-byte aligned)
+__device__ __forceinline__ void lds8f(const float *p, float *x)
+{
+    const float4 a = ((const float4 *)p)[0], b = ((const float4 *)p)[1];
+    x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+}
 
-template <typename TIn>
 __device__ __forceinline__ void fwd_chain(const CbArgs &a, char *smem)
 {
-    using St = FwdStage<TIn>;
-    float *Ssm = (float *)(smem + 2 * St::kBytes), *up = Ssm + kD * 32;
+    using St = FwdStage;
+    float *Ssm = (float *)(smem + 2 * St::kBytes), *upT = Ssm + 32 * kTS;
     const int bh = blockIdx.x, cg = blockIdx.y * 32, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int col = cg + lane, row0 = w * 8, r0 = 2 * w;
     auto prefetch = [&](int c) {
         char *base = smem + (c & 1) * St::kBytes;
         const float *rec = a.rec + ((size_t)bh * a.nc + c) * kRecFloats;
         copy_floats(rec + kRecW, (float *)base, kC * kD);
+        copy_floats(rec + kRecK, (float *)(base + St::kW), kC * kD);
         float *Ud = (float *)(base + St::kW + St::kK);
         for (int i = threadIdx.x; i < kC * 8; i += kChainThreads) {
             const int r = i >> 3, e = (i & 7) * 4;
             cp_async16(Ud + r * 32 + e, rec + kRecU + r * kD + cg + e);
         }
-        copy_key_rows<TIn>(a, chunk_rows(a, bh, c), (const TIn *)a.k, (TIn *)(base + St::kW));
         cp_async_commit();
     };
     float S[8];
@@ -311,59 +313,61 @@ __device__ __forceinline__ void fwd_chain(const CbArgs &a, char *smem)
         const size_t ci = (size_t)bh * a.nc + c;
         float *s0 = a.S0 + ci * kStateFloats;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            s0[(row0 + i) * kD + col] = S[i];
-            Ssm[(row0 + i) * 32 + lane] = S[i];
-        }
+        for (int i = 0; i < 8; ++i) s0[(row0 + i) * kD + col] = S[i];
+        st4(Ssm + lane * kTS + row0, make_float4(S[0], S[1], S[2], S[3]));
+        st4(Ssm + lane * kTS + row0 + 4, make_float4(S[4], S[5], S[6], S[7]));
         cp_async_wait_all();
         __syncthreads();   // chunk c's stage and the state tile are complete; chunk c-1's stage is free
         if (c + 1 < a.nc) prefetch(c + 1);
         const char *base = smem + (c & 1) * St::kBytes;
-        const float *Wc = (const float *)base;
-        const TIn *Kc = (const TIn *)(base + St::kW);
+        const float *Wc = (const float *)base, *Kc = (const float *)(base + St::kW);
         const float *Uc = (const float *)(base + St::kW + St::kK);
         // U' = U - W S, rows r0, r0 + 1
-        float u0 = Uc[r0 * 32 + lane], u1 = Uc[(r0 + 1) * 32 + lane];
-#pragma unroll 4
+        float acc0 = 0.f, acc1 = 0.f;
+        const float *sc = Ssm + lane * kTS;
+#pragma unroll 8
         for (int k = 0; k < kD; k += 4) {
-            const float4 x0 = ld4(Wc + r0 * kD + k), x1 = ld4(Wc + (r0 + 1) * kD + k);
-            const float4 s = make_float4(Ssm[k * 32 + lane], Ssm[(k + 1) * 32 + lane], Ssm[(k + 2) * 32 + lane],
-                                         Ssm[(k + 3) * 32 + lane]);
-            u0 -= dot4(x0, s, 0.f);
-            u1 -= dot4(x1, s, 0.f);
+            const float4 s = ld4(sc + k);
+            acc0 = dot4(ld4(Wc + r0 * kD + k), s, acc0);
+            acc1 = dot4(ld4(Wc + (r0 + 1) * kD + k), s, acc1);
         }
-        up[r0 * kL + lane] = u0;
-        up[(r0 + 1) * kL + lane] = u1;
+        const float u0 = Uc[r0 * 32 + lane] - acc0, u1 = Uc[(r0 + 1) * 32 + lane] - acc1;
+        upT[lane * kTU + r0] = u0;
+        upT[lane * kTU + r0 + 1] = u1;
         a.Up[ci * kRowsFloats + r0 * kD + col] = u0;
         a.Up[ci * kRowsFloats + (r0 + 1) * kD + col] = u1;
         __syncthreads();
         // S += K^T U'
-#pragma unroll 4
-        for (int r = 0; r < kC; ++r) {
-            float kx[8];
-            lds8(Kc + r * kD + row0, kx);
-            const float u = up[r * kL + lane];
+#pragma unroll 2
+        for (int r = 0; r < kC; r += 4) {
+            const float4 u4 = ld4(upT + lane * kTU + r);
+            const float u[4] = {u4.x, u4.y, u4.z, u4.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) S[i] = fmaf(kx[i], u, S[i]);
+            for (int j = 0; j < 4; ++j) {
+                float kx[8];
+                lds8f(Kc + (r + j) * kD + row0, kx);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) S[i] = fmaf(kx[i], u[j], S[i]);
+            }
         }
     }
 }
 
-template <typename TIn, typename TDo>
+template <typename TDo>
 __device__ __forceinline__ void bwd_chain(const CbArgs &a, char *smem)
 {
-    using St = BwdStage<TIn, TDo>;
-    float *dSsm = (float *)(smem + 2 * St::kBytes), *dup = dSsm + kD * 32;
+    using St = BwdStage<TDo>;
+    float *dSsm = (float *)(smem + 2 * St::kBytes), *dupT = dSsm + 32 * kTS;
     const int bh = blockIdx.x, cg = blockIdx.y * 32, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int col = cg + lane, row0 = w * 8, r0 = 2 * w;
     auto prefetch = [&](int c) {
         char *base = smem + (c & 1) * St::kBytes;
         const float *rec = a.rec + ((size_t)bh * a.nc + c) * kRecFloats;
-        const ChunkRows cr = chunk_rows(a, bh, c);
         copy_floats(rec + kRecW, (float *)base, kC * kD);
-        copy_key_rows<TIn>(a, cr, (const TIn *)a.k, (TIn *)(base + St::kW));
-        copy_token_rows<kD, TIn>(a, cr, (const TIn *)a.q, 0, (TIn *)(base + St::kW + St::kK));
-        copy_token_rows<32, TDo>(a, cr, (const TDo *)a.d_o, cg, (TDo *)(base + St::kW + St::kK + St::kQb));
+        copy_floats(rec + kRecK, (float *)(base + St::kW), kC * kD);
+        copy_floats(rec + kRecQ, (float *)(base + St::kW + St::kK), kQ * kD);
+        copy_do_rows<TDo>(a, chunk_rows(a, bh, c), (const TDo *)a.d_o, cg,
+                          (TDo *)(base + St::kW + St::kK + St::kQb));
         copy_floats(rec + kRecP, (float *)(base + St::kW + St::kK + St::kQb + St::kO), kQ * kC);
         cp_async_commit();
     };
@@ -375,41 +379,34 @@ __device__ __forceinline__ void bwd_chain(const CbArgs &a, char *smem)
         const size_t ci = (size_t)bh * a.nc + c;
         float *ds1 = a.dS1 + ci * kStateFloats;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            ds1[(row0 + i) * kD + col] = dS[i];
-            dSsm[(row0 + i) * 32 + lane] = dS[i];
-        }
+        for (int i = 0; i < 8; ++i) ds1[(row0 + i) * kD + col] = dS[i];
+        st4(dSsm + lane * kTS + row0, make_float4(dS[0], dS[1], dS[2], dS[3]));
+        st4(dSsm + lane * kTS + row0 + 4, make_float4(dS[4], dS[5], dS[6], dS[7]));
         cp_async_wait_all();
         __syncthreads();
         if (c > 0) prefetch(c - 1);
         const char *base = smem + (c & 1) * St::kBytes;
-        const float *Wc = (const float *)base;
-        const TIn *Kc = (const TIn *)(base + St::kW);
-        const TIn *Qc = (const TIn *)(base + St::kW + St::kK);
+        const float *Wc = (const float *)base, *Kc = (const float *)(base + St::kW);
+        const float *Qc = (const float *)(base + St::kW + St::kK);
         const TDo *Oc = (const TDo *)(base + St::kW + St::kK + St::kQb);
         const float *Pc = (const float *)(base + St::kW + St::kK + St::kQb + St::kO);
         // dU' = P^T dO + K dS1, rows r0, r0 + 1
         float g0 = 0.f, g1 = 0.f;
+        const float *sc = dSsm + lane * kTS;
+#pragma unroll 8
+        for (int k = 0; k < kD; k += 4) {
+            const float4 s = ld4(sc + k);
+            g0 = dot4(ld4(Kc + r0 * kD + k), s, g0);
+            g1 = dot4(ld4(Kc + (r0 + 1) * kD + k), s, g1);
+        }
 #pragma unroll 4
         for (int t = 0; t < kQ; ++t) {
             const float o = to_f(Oc[t * 32 + lane]);
             g0 = fmaf(Pc[t * kC + r0], o, g0);
             g1 = fmaf(Pc[t * kC + r0 + 1], o, g1);
         }
-#pragma unroll 2
-        for (int k = 0; k < kD; k += 8) {
-            float k0[8], k1[8];
-            lds8(Kc + r0 * kD + k, k0);
-            lds8(Kc + (r0 + 1) * kD + k, k1);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float s = dSsm[(k + j) * 32 + lane];
-                g0 = fmaf(k0[j], s, g0);
-                g1 = fmaf(k1[j], s, g1);
-            }
-        }
-        dup[r0 * kL + lane] = g0;
-        dup[(r0 + 1) * kL + lane] = g1;
+        dupT[lane * kTU + r0] = g0;
+        dupT[lane * kTU + r0 + 1] = g1;
         a.dUp[ci * kRowsFloats + r0 * kD + col] = g0;
         a.dUp[ci * kRowsFloats + (r0 + 1) * kD + col] = g1;
         __syncthreads();
@@ -417,18 +414,22 @@ __device__ __forceinline__ void bwd_chain(const CbArgs &a, char *smem)
 #pragma unroll 4
         for (int t = 0; t < kQ; ++t) {
             float qx[8];
-            lds8(Qc + t * kD + row0, qx);
+            lds8f(Qc + t * kD + row0, qx);
             const float o = to_f(Oc[t * 32 + lane]);
 #pragma unroll
             for (int i = 0; i < 8; ++i) dS[i] = fmaf(qx[i], o, dS[i]);
         }
-#pragma unroll 4
-        for (int r = 0; r < kC; ++r) {
-            float wx[8];
-            lds8(Wc + r * kD + row0, wx);
-            const float g = dup[r * kL + lane];
+#pragma unroll 2
+        for (int r = 0; r < kC; r += 4) {
+            const float4 g4 = ld4(dupT + lane * kTU + r);
+            const float g[4] = {g4.x, g4.y, g4.z, g4.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) dS[i] = fmaf(-wx[i], g, dS[i]);
+            for (int j = 0; j < 4; ++j) {
+                float wx[8];
+                lds8f(Wc + (r + j) * kD + row0, wx);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) dS[i] = fmaf(-wx[i], g[j], dS[i]);
+            }
         }
     }
     if (a.dh0) {
@@ -437,17 +438,16 @@ __device__ __forceinline__ void bwd_chain(const CbArgs &a, char *smem)
     }
 }
 
-template <typename TIn, typename TDo>
+template <typename TDo>
 __global__ void __launch_bounds__(kChainThreads, 2) cb_chains(const CbArgs a)
 {
     extern __shared__ float4 sm_chain[];
-    if (blockIdx.z == 0) fwd_chain<TIn>(a, (char *)sm_chain);
-    else bwd_chain<TIn, TDo>(a, (char *)sm_chain);
+    if (blockIdx.z == 0) fwd_chain(a, (char *)sm_chain);
+    else bwd_chain<TDo>(a, (char *)sm_chain);
 }
 
 // ------------------------------------------------------------------ 3. per-chunk gradients
 constexpr int kGradThreads = 512;
-constexpr int kGradSmemFloats = 6 * kC * kS + 3 * kQ * kS + 4 * kC * kL + kQ * kL + kC;
 
 // sum over the 4 lanes of a quad (all four get it)
 __device__ __forceinline__ float quad_sum(float x)
@@ -456,38 +456,27 @@ __device__ __forceinline__ float quad_sum(float x)
     return x + __shfl_xor_sync(0xffffffffu, x, 2);
 }
 
-template <typename TIn, typename TDo>
-__global__ void __launch_bounds__(kGradThreads, 1) cb_grad(const CbArgs a)
-{
-    extern __shared__ float4 sm_grad[];
-    float *Ks = (float *)sm_grad, *Vs = Ks + kC * kS, *Ups = Vs + kC * kS, *dUps = Ups + kC * kS;
-    float *dWs = dUps + kC * kS, *dKs = dWs + kC * kS;
-    float *Qs = dKs + kC * kS, *dOs = Qs + kQ * kS, *dQs = dOs + kQ * kS;
-    float *Ts = dQs + kQ * kS, *KKs = Ts + kC * kL, *dTs = KKs + kC * kL, *Xs = dTs + kC * kL;
-    float *dPs = Xs + kC * kL, *be = dPs + kQ * kL;
-    const int ci = blockIdx.x, bh = ci / a.nc, c = ci - bh * a.nc;
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const ChunkRows cr = chunk_rows(a, bh, c);
-    const float *rec = a.rec + (size_t)ci * kRecFloats;
+// 3a. products with the boundary states. Thread: row kk = tid / 4 of S0
+// (then dS1), float4 columns 16 i + 4 qq (qq = tid % 4), i = 0 .. 7; a row
+// of the left operand times that row is a dot product over the quad.
+constexpr int kGradSSmemFloats = (kQ + 2 * kC) * kS;
 
-    // the thread's quarter rows of S0 and dS1: row kk = tid / 4, float4
-    // columns 16 i + 4 qq (qq = tid % 4), i = 0 .. 7
-    const int kk = tid >> 2, qq = tid & 3;
-    float4 s0q[8], ds1q[8];
+template <typename TDo>
+__global__ void __launch_bounds__(kGradThreads, 2) cb_grad_s(const CbArgs a)
+{
+    extern __shared__ float4 sm_grad_s[];
+    float *dOs = (float *)sm_grad_s, *Ups = dOs + kQ * kS, *dUps = Ups + kC * kS;
+    const int ci = blockIdx.x, bh = ci / a.nc, c = ci - bh * a.nc;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, kk = tid >> 2, qq = tid & 3;
+    const ChunkRows cr = chunk_rows(a, bh, c);
+    float *rec = a.rec + (size_t)ci * kRecFloats;
+    float4 sq[8];
     {
         const float *s0 = a.S0 + (size_t)ci * kStateFloats + kk * kD + 4 * qq;
-        const float *ds1 = a.dS1 + (size_t)ci * kStateFloats + kk * kD + 4 * qq;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            s0q[i] = __ldg((const float4 *)(s0 + 16 * i));
-            ds1q[i] = __ldg((const float4 *)(ds1 + 16 * i));
-        }
+        for (int i = 0; i < 8; ++i) sq[i] = __ldg((const float4 *)(s0 + 16 * i));
     }
-    stage_f32<true, kC, TIn>(a, cr, (const TIn *)a.k, Ks);
-    stage_f32<true, kC, TIn>(a, cr, (const TIn *)a.v, Vs);
-    stage_f32<false, kQ, TIn>(a, cr, (const TIn *)a.q, Qs);
     stage_f32<false, kQ, TDo>(a, cr, (const TDo *)a.d_o, dOs);
-    stage_betas<TIn>(a, cr, be);
     {
         const float *up = a.Up + (size_t)ci * kRowsFloats, *dup = a.dUp + (size_t)ci * kRowsFloats;
         for (int i = tid; i < kC * kD / 4; i += kGradThreads) {
@@ -495,53 +484,91 @@ __global__ void __launch_bounds__(kGradThreads, 1) cb_grad(const CbArgs a)
             st4(Ups + r * kS + e, __ldg((const float4 *)(up + r * kD + e)));
             st4(dUps + r * kS + e, __ldg((const float4 *)(dup + r * kD + e)));
         }
-        for (int i = tid; i < kC * kC; i += kGradThreads) {
-            Ts[(i >> 5) * kL + (i & 31)] = rec[kRecT + i];
-            KKs[(i >> 5) * kL + (i & 31)] = rec[kRecKK + i];
-        }
     }
     __syncthreads();
-
-    // dP = (dO U'^T) masked: row t = w, column s = lane
+    // dP = (dO U'^T) masked: row t = w, column s = lane -> the record's P slot
     {
         float acc = 0.f;
         const float *x = dOs + w * kS, *y = Ups + lane * kS;
 #pragma unroll 8
         for (int d = 0; d < kD; d += 4) acc = dot4(ld4(x + d), ld4(y + d), acc);
-        dPs[w * kL + lane] = lane <= w * a.nh + a.nh - 1 ? acc : 0.f;
+        rec[kRecP + w * kC + lane] = lane <= w * a.nh + a.nh - 1 ? acc : 0.f;
     }
-    // dQ0 = dO S0^T, dW = -dU' S0^T, dK0 = U' dS1^T: column kk, over quads
-    {
-        auto row_dot = [&](const float *x, const float4 *sq) {
-            float acc = 0.f;
+    auto row_dot = [&](const float *x) {
+        float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc = dot4(ld4(x + 16 * i + 4 * qq), sq[i], acc);
-            return quad_sum(acc);
-        };
-#pragma unroll 2
-        for (int t = 0; t < kQ; ++t) {
-            const float v = row_dot(dOs + t * kS, s0q);
-            if (qq == 0) dQs[t * kS + kk] = v;
+        for (int i = 0; i < 8; i += 2) {
+            acc0 = dot4(ld4(x + 16 * i + 4 * qq), sq[i], acc0);
+            acc1 = dot4(ld4(x + 16 * (i + 1) + 4 * qq), sq[i + 1], acc1);
         }
+        return quad_sum(acc0 + acc1);
+    };
+    // dq <- dO S0^T, dW = -dU' S0^T (the record's W slot)
 #pragma unroll 2
-        for (int r = 0; r < kC; ++r) {
-            const float vw = row_dot(dUps + r * kS, s0q);
-            const float vk = row_dot(Ups + r * kS, ds1q);
-            if (qq == 0) {
-                dWs[r * kS + kk] = -vw;
-                dKs[r * kS + kk] = vk;
-            }
-        }
+    for (int t = 0; t < kQ; ++t) {
+        const float v = row_dot(dOs + t * kS);
+        if (qq == 0 && t < cr.nt) a.dq[token_row(a, cr, t) * kD + kk] = v;
+    }
+#pragma unroll 2
+    for (int r = 0; r < kC; ++r) {
+        const float v = row_dot(dUps + r * kS);
+        if (qq == 0) rec[kRecW + r * kD + kk] = -v;
+    }
+    // dk <- U' dS1^T
+    {
+        const float *ds1 = a.dS1 + (size_t)ci * kStateFloats + kk * kD + 4 * qq;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sq[i] = __ldg((const float4 *)(ds1 + 16 * i));
+    }
+#pragma unroll 2
+    for (int r = 0; r < kC; ++r) {
+        const float v = row_dot(Ups + r * kS);
+        if (qq == 0 && r < cr.R) a.dk[key_row(a, cr, r) * kD + kk] = v;
+    }
+}
+
+// 3b. the rest of the chunk's gradients
+constexpr int kGradRSmemFloats = 4 * kC * kS + kQ * kS + 4 * kC * kL + kQ * kL + kC;
+
+template <typename TIn>
+__global__ void __launch_bounds__(kGradThreads, 2) cb_grad_r(const CbArgs a)
+{
+    extern __shared__ float4 sm_grad_r[];
+    float *Ks = (float *)sm_grad_r, *Vs = Ks + kC * kS, *dUps = Vs + kC * kS, *dWs = dUps + kC * kS;
+    float *Qs = dWs + kC * kS;
+    float *Ts = Qs + kQ * kS, *KKs = Ts + kC * kL, *dTs = KKs + kC * kL, *Xs = dTs + kC * kL;
+    float *dPs = Xs + kC * kL, *be = dPs + kQ * kL;
+    const int ci = blockIdx.x, bh = ci / a.nc, c = ci - bh * a.nc;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const ChunkRows cr = chunk_rows(a, bh, c);
+    const float *rec = a.rec + (size_t)ci * kRecFloats;
+    const float *dup = a.dUp + (size_t)ci * kRowsFloats;
+    for (int i = tid; i < kC * kD / 4; i += kGradThreads) {
+        const int r = i >> 5, e = (i & 31) * 4;
+        st4(Ks + r * kS + e, __ldg((const float4 *)(rec + kRecK + r * kD + e)));
+        st4(dUps + r * kS + e, __ldg((const float4 *)(dup + r * kD + e)));
+        st4(dWs + r * kS + e, __ldg((const float4 *)(rec + kRecW + r * kD + e)));
+        if (r < kQ) st4(Qs + r * kS + e, __ldg((const float4 *)(rec + kRecQ + r * kD + e)));
+    }
+    stage_f32<true, kC, TIn>(a, cr, (const TIn *)a.v, Vs);
+    stage_betas<TIn>(a, cr, be);
+    for (int i = tid; i < kC * kC; i += kGradThreads) {
+        Ts[(i >> 5) * kL + (i & 31)] = rec[kRecT + i];
+        KKs[(i >> 5) * kL + (i & 31)] = rec[kRecKK + i];
+        if (i < kQ * kC) dPs[(i >> 5) * kL + (i & 31)] = rec[kRecP + i];
     }
     __syncthreads();
 
-    // dQ = dQ0 + dP K (row t = w, columns 4 lane .. 4 lane + 3) -> global
+    // dq += dP K (row t = w, columns 4 lane .. 4 lane + 3)
     {
         const int d = 4 * lane;
-        float4 acc = ld4(dQs + w * kS + d);
+        if (w < cr.nt) {
+            float *dq = a.dq + token_row(a, cr, w) * kD + d;
+            float4 acc = ld4(dq);
 #pragma unroll 8
-        for (int s = 0; s < kC; ++s) acc = axpy4(dPs[w * kL + s], ld4(Ks + s * kS + d), acc);
-        if (w < cr.nt) st4(a.dq + token_row(a, cr, w) * kD + d, acc);
+            for (int s = 0; s < kC; ++s) acc = axpy4(dPs[w * kL + s], ld4(Ks + s * kS + d), acc);
+            st4(dq, acc);
+        }
     }
     // dT = (dW K^T + dU' V^T) B: rows 2w, 2w+1, column m = lane
     {
@@ -581,13 +608,14 @@ __global__ void __launch_bounds__(kGradThreads, 1) cb_grad(const CbArgs a)
     }
     __syncthreads();
     // rows m = 2w, 2w+1, columns 4 lane .. 4 lane + 3:
-    //   dK = dK0 + dP^T Q + B (T^T dW + dG K) + (B dG)^T K,  dV = B T^T dU'
+    //   dk += dP^T Q + B (T^T dW + dG K) + (B dG)^T K,  dv = B T^T dU'
     //   dbeta = sum over columns of K o T^T dW + V o T^T dU', + sum_s dG o K K^T
     {
         const int d = 4 * lane;
 #pragma unroll 1
         for (int i = 0; i < 2; ++i) {
             const int m = 2 * w + i;
+            if (m >= cr.R) break;   // warp-uniform
             const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
             float4 tw = z, tu = z, gk = z, gtk = z, pq = z;
             for (int r = m; r < kC; ++r) {
@@ -600,20 +628,18 @@ __global__ void __launch_bounds__(kGradThreads, 1) cb_grad(const CbArgs a)
 #pragma unroll 4
             for (int t = 0; t < kQ; ++t) pq = axpy4(dPs[t * kL + m], ld4(Qs + t * kS + d), pq);
             const float bm = be[m];
-            const float4 k0 = ld4(dKs + m * kS + d);
+            const size_t row = key_row(a, cr, m);
+            float *dkp = a.dk + row * kD + d;
+            const float4 k0 = ld4(dkp);
             const float4 dk = make_float4(k0.x + pq.x + bm * (tw.x + gk.x) + gtk.x, k0.y + pq.y + bm * (tw.y + gk.y) + gtk.y,
                                           k0.z + pq.z + bm * (tw.z + gk.z) + gtk.z, k0.w + pq.w + bm * (tw.w + gk.w) + gtk.w);
-            const float4 dv = make_float4(bm * tu.x, bm * tu.y, bm * tu.z, bm * tu.w);
             float db = dot4(ld4(Ks + m * kS + d), tw, dot4(ld4(Vs + m * kS + d), tu, 0.f));
             if (lane < m) db = fmaf(dTs[m * kL + lane], KKs[m * kL + lane], db);
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) db += __shfl_xor_sync(0xffffffffu, db, o);
-            if (m < cr.R) {
-                const size_t row = key_row(a, cr, m);
-                st4(a.dk + row * kD + d, dk);
-                st4(a.dv + row * kD + d, dv);
-                if (lane == 0) a.dbeta[row] = db;
-            }
+            st4(dkp, dk);
+            st4(a.dv + row * kD + d, make_float4(bm * tu.x, bm * tu.y, bm * tu.z, bm * tu.w));
+            if (lane == 0) a.dbeta[row] = db;
         }
     }
 }
@@ -623,12 +649,13 @@ cudaError_t launch_typed(const BwdProblem &p, const CbArgs &a)
 {
     const size_t n_chunks = (size_t)p.B * p.H * a.nc;
     cudaError_t e;
-    const int chain_smem = (int)chain_smem_bytes<TIn, TDo>();
-    if ((e = cudaFuncSetAttribute(cb_chains<TIn, TDo>, cudaFuncAttributeMaxDynamicSharedMemorySize, chain_smem)) !=
+    const int chain_smem = (int)chain_smem_bytes<TDo>();
+    if ((e = cudaFuncSetAttribute(cb_chains<TDo>, cudaFuncAttributeMaxDynamicSharedMemorySize, chain_smem)) !=
         cudaSuccess)
         return e;
+    const dim3 chain_grid(p.B * p.H, kD / 32, 2);
     if (n_chunks == 0) {   // T = 0: dh0 = dh_final (the reverse chains only)
-        cb_chains<TIn, TDo><<<dim3(p.B * p.H, kD / 32, 2), kChainThreads, chain_smem, p.stream>>>(a);
+        cb_chains<TDo><<<chain_grid, kChainThreads, chain_smem, p.stream>>>(a);
         return cudaGetLastError();
     }
     const int prep_smem = (int)(kPrepSmemFloats * sizeof(float));
@@ -636,13 +663,19 @@ cudaError_t launch_typed(const BwdProblem &p, const CbArgs &a)
         return e;
     cb_prep<TIn><<<(unsigned)n_chunks, kPrepThreads, prep_smem, p.stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    cb_chains<TIn, TDo><<<dim3(p.B * p.H, kD / 32, 2), kChainThreads, chain_smem, p.stream>>>(a);
+    cb_chains<TDo><<<chain_grid, kChainThreads, chain_smem, p.stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const int grad_smem = (int)(kGradSmemFloats * sizeof(float));
-    if ((e = cudaFuncSetAttribute(cb_grad<TIn, TDo>, cudaFuncAttributeMaxDynamicSharedMemorySize, grad_smem)) !=
+    const int gs_smem = (int)(kGradSSmemFloats * sizeof(float));
+    if ((e = cudaFuncSetAttribute(cb_grad_s<TDo>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs_smem)) !=
         cudaSuccess)
         return e;
-    cb_grad<TIn, TDo><<<(unsigned)n_chunks, kGradThreads, grad_smem, p.stream>>>(a);
+    cb_grad_s<TDo><<<(unsigned)n_chunks, kGradThreads, gs_smem, p.stream>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int gr_smem = (int)(kGradRSmemFloats * sizeof(float));
+    if ((e = cudaFuncSetAttribute(cb_grad_r<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, gr_smem)) !=
+        cudaSuccess)
+        return e;
+    cb_grad_r<TIn><<<(unsigned)n_chunks, kGradThreads, gr_smem, p.stream>>>(a);
     return cudaGetLastError();
 }
 

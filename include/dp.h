@@ -189,8 +189,16 @@ dp_status dp_state_io(int op, int B, int H, int Dk, int Dv, float *state,
 /* Backward pass: gradients of L = <d_o, o> + <dh_final, h_final> through
  * the recurrence dp_forward computes (DeltaProduct paper, Sec.4 Eq.(2)-(3),
  * gated variant), for training. Same dims and input layouts as dp_forward
- * (dims->impl, dims->prologue and dims->max_seqlen must be 0;
- * dims->out_dtype is the type of d_o).
+ * (dims->prologue and dims->max_seqlen must be 0; dims->out_dtype is the
+ * type of d_o). dims->impl picks the form:
+ *   DP_IMPL_AUTO       the chunked form for ungated problems with
+ *                      D_k = D_v = 128 when the workspace holds its records,
+ *                      else the recurrent form;
+ *   DP_IMPL_RECURRENT  the recurrent form (any shape, gated or not);
+ *   DP_IMPL_CHUNK_TC   the chunked form (WY representation of each chunk of
+ *                      tokens, OSDN paper App.A.2, differentiated per chunk;
+ *                      fp32 on CUDA cores), DP_ERR_UNSUPPORTED when g != NULL
+ *                      or D_k, D_v != 128.
  *   d_o      [B,T,H,D_v] gradient of the outputs;
  *   dh_final [B,H,D_k,D_v] fp32 gradient of the final state, NULL = zeros;
  * outputs, fp32, written in full:
@@ -198,12 +206,17 @@ dp_status dp_state_io(int op, int B, int H, int Dk, int Dv, float *state,
  *   dbeta [B,T,H,n_h], dg [B,T,H] (required iff g != NULL, else ignored),
  *   dh0 [B,H,D_k,D_v] (NULL = not written; the gradient with respect to
  *   h0, or to the zero initial state when h0 is NULL).
- * The gradients with respect to the key rows and the scalars (dq, dk,
- * dbeta, dg) are sums over the value columns that the kernel accumulates
- * with fp32 atomic additions, so their last bits may vary between calls.
- * workspace: at least dp_backward_workspace_size bytes (status block, the
- * state checkpoints, fp32 D_k x D_v per (b,h) every few tokens, and every
- * sub-step's error v - H^T k, fp32 B T H n_h D_v). */
+ * In the recurrent form the gradients with respect to the key rows and the
+ * scalars (dq, dk, dbeta, dg) are sums over the value columns that the
+ * kernel accumulates with fp32 atomic additions, so their last bits may
+ * vary between calls; the chunked form has no atomics and is deterministic.
+ * workspace: at least dp_backward_workspace_size bytes for the same dims
+ * (and impl): the status block, then for the recurrent form the state
+ * checkpoints (fp32 D_k x D_v per (b,h) every few tokens) and every
+ * sub-step's error v - H^T k (fp32 B T H n_h D_v); for the chunked form, per
+ * chunk of min(16, 32 / n_h) tokens, its WY record and the fp32 state at its
+ * start and state gradient at its end (about 200 KB per chunk). AUTO's size
+ * covers both forms. */
 dp_status dp_backward_workspace_size(const dp_dims *dims, size_t *bytes);
 /* dp_backward over packed variable-length sequences: layouts, cu_seqlens
  * and dims->max_seqlen as in dp_forward_varlen (the gradients take the
