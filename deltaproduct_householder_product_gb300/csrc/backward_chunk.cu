@@ -19,7 +19,7 @@
 // Four launches:
 //   cb_prep    every chunk at once: T, W, U, P, K K^T and fp32 K, Q into its
 //              record;
-//   cb_chains  per (b,h) and 32 value columns, chunk by chunk, two
+//   cb_chains  per (b,h) and 64 value columns, chunk by chunk, two
 //              independent CTAs: the forward chain (S <- S + K^T (U - W S))
 //              stores S0 and U' of every chunk; the reverse chain (the
 //              transposed recurrence above, from the last chunk) stores dS1
@@ -28,7 +28,8 @@
 //   cb_grad_s  every chunk at once, the products with the 128 x 128
 //              boundary states (60% of the per-chunk arithmetic):
 //              dq <- dO S0^T, dk <- U' dS1^T, dW = -dU' S0^T and dP; each
-//              thread holds a quarter row of S0, then of dS1, in registers;
+//              thread holds quarter rows of two rows of S0, then of dS1, in
+//              registers;
 //   cb_grad_r  every chunk at once, the rest: dq += dP K, dk += ..., dv,
 //              dbeta.
 // The chains carry the only sequential dependency, as 32 x 128 x 128
@@ -238,26 +239,32 @@ __global__ void __launch_bounds__(kPrepThreads) cb_prep(const CbArgs a)
 }
 
 // ------------------------------------------------------------------ 2. chains
-// CTA: (b,h), 32 value columns (blockIdx.y) and the direction (blockIdx.z).
-// Thread (warp w, lane): state rows 8w .. 8w+7 of column lane, and rows
-// 2w, 2w+1 of the chunk's U' (dU'). The state and U' (dU') are also kept
-// transposed in shared memory ([column][row]) so that a thread reads its
-// column four rows at a time.
-constexpr int kChainThreads = 512;
-constexpr int kTS = kD + 4;    // row stride of the transposed state tile
-constexpr int kTU = kC + 4;    // row stride of the transposed U' tile
+// CTA: (b,h), 64 value columns (blockIdx.y) and the direction (blockIdx.z),
+// 256 threads, one CTA per SM. Every operand a thread reads from shared
+// memory feeds several of its FMAs (a 128-bit shared load costs four
+// wavefronts even when all lanes read the same address):
+//   state owner: warp w, lane = (ro, cq): rows 16w + 8ro .. + 7, columns
+//     4cq .. 4cq + 3 (8 x 4 registers); per chunk row r it reads 8 key (W)
+//     values and 4 U' (dU') values for 32 FMAs;
+//   U' (dU'): thread (kh, rq, cq): rows 4rq .. 4rq + 3, columns 4cq .. +3,
+//     half kh of the 128-term contraction (4 x 4 FMAs per 8 values read);
+//     the two halves meet in shared memory.
+constexpr int kChainThreads = 256;
+constexpr int kCols = 64;          // value columns per chain CTA
+constexpr int kSS = kCols + 4;     // row stride of the state and U' tiles
 
 struct FwdStage {   // one chunk's operands of the forward chain (fp32)
-    static constexpr size_t kW = (size_t)kC * kD * 4, kK = (size_t)kC * kD * 4, kU = (size_t)kC * 32 * 4;
+    static constexpr size_t kW = (size_t)kC * kD * 4, kK = (size_t)kC * kD * 4, kU = (size_t)kC * kCols * 4;
     static constexpr size_t kBytes = kW + kK + kU;
 };
 template <typename TDo>
 struct BwdStage {   // ... and of the reverse chain
     static constexpr size_t kW = (size_t)kC * kD * 4, kK = (size_t)kC * kD * 4, kQb = (size_t)kQ * kD * 4;
-    static constexpr size_t kO = (size_t)kQ * 32 * sizeof(TDo), kP = (size_t)kQ * kC * 4;
+    static constexpr size_t kO = (size_t)kQ * kCols * sizeof(TDo), kP = (size_t)kQ * kC * 4;
     static constexpr size_t kBytes = kW + kK + kQb + kO + kP;
 };
-constexpr size_t kChainShared = (size_t)32 * kTS * 4 + (size_t)32 * kTU * 4;
+// state tile [128][kSS], U' tile [32][kSS], partial sums [128 threads][16]
+constexpr size_t kChainShared = (size_t)(kD + kC) * kSS * 4 + (size_t)128 * 16 * 4;
 template <typename TDo>
 constexpr size_t chain_smem_bytes()
 {
@@ -265,91 +272,168 @@ constexpr size_t chain_smem_bytes()
     return (f > b ? f : b) + kChainShared;
 }
 
-// cp.async of the chunk's token rows of d_o, columns [col0, col0 + 32), zero rows past nt
+// cp.async of the chunk's token rows of d_o, columns [col0, col0 + kCols), zero rows past nt
 template <typename T>
 __device__ __forceinline__ void copy_do_rows(const CbArgs &a, const ChunkRows &cr, const T *src, int col0, T *dst)
 {
-    constexpr int kPer = 16 / sizeof(T), kPerRow = 32 / kPer;
+    constexpr int kPer = 16 / sizeof(T), kPerRow = kCols / kPer;
     for (int i = threadIdx.x; i < kQ * kPerRow; i += kChainThreads) {
         const int t = i / kPerRow, e = (i - t * kPerRow) * kPer;
-        if (t < cr.nt) cp_async16(dst + t * 32 + e, src + token_row(a, cr, t) * kD + col0 + e);
-        else *(uint4 *)(dst + t * 32 + e) = make_uint4(0u, 0u, 0u, 0u);
+        if (t < cr.nt) cp_async16(dst + t * kCols + e, src + token_row(a, cr, t) * kD + col0 + e);
+        else *(uint4 *)(dst + t * kCols + e) = make_uint4(0u, 0u, 0u, 0u);
     }
 }
 __device__ __forceinline__ void copy_floats(const float *src, float *dst, int n)
 {
     for (int i = threadIdx.x * 4; i < n; i += kChainThreads * 4) cp_async16(dst + i, src + i);
 }
-// 8 consecutive fp32 of shared memory (32-byte aligned)
-__device__ __forceinline__ void lds8f(const float *p, float *x)
+// 4 consecutive d_o values (8- or 16-byte aligned) as fp32
+__device__ __forceinline__ float4 ld4o(const float *p) { return ld4(p); }
+__device__ __forceinline__ float4 ld4o(const __nv_bfloat16 *p)
 {
-    const float4 a = ((const float4 *)p)[0], b = ((const float4 *)p)[1];
-    x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+    const uint2 u = *(const uint2 *)p;
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xffff0000u));
+}
+__device__ __forceinline__ float f4(const float4 v, int j) { return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w; }
+
+// Thread roles of a chain CTA.
+struct ChainLanes {
+    int sr0, sc0;        // state block: rows sr0 .. sr0 + 7, columns sc0 .. sc0 + 3
+    int kh, ur0, uc0;    // U' block: contraction half, rows ur0 .. + 3, columns uc0 .. + 3
+    __device__ ChainLanes()
+    {
+        const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+        sr0 = 16 * w + 8 * (lane >> 4);
+        sc0 = 4 * (lane & 15);
+        kh = tid >> 7;
+        ur0 = 4 * ((tid >> 4) & 7);
+        uc0 = 4 * (tid & 15);
+    }
+};
+
+// the state block into the state tile and global memory (row-major, columns cg + ...)
+__device__ __forceinline__ void put_state(const float (*S)[4], float *tile, float *g, const ChainLanes &L, int cg)
+{
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 v = make_float4(S[i][0], S[i][1], S[i][2], S[i][3]);
+        st4(tile + (L.sr0 + i) * kSS + L.sc0, v);
+        st4(g + (L.sr0 + i) * kD + cg + L.sc0, v);
+    }
+}
+// acc[i][j] = sum over k in half kh of X[ur0 + i][k] St[k][uc0 + j]
+__device__ __forceinline__ void rows_times_state(const float *X, const float *St, const ChainLanes &L,
+                                                 float (*acc)[4])
+{
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    const int k0 = 64 * L.kh;
+#pragma unroll 2
+    for (int k = k0; k < k0 + 64; k += 4) {
+        float4 x[4], s[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] = ld4(X + (L.ur0 + i) * kD + k);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) s[q] = ld4(St + (k + q) * kSS + L.uc0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float xv = f4(x[i], q);
+                acc[i][0] = fmaf(xv, s[q].x, acc[i][0]);
+                acc[i][1] = fmaf(xv, s[q].y, acc[i][1]);
+                acc[i][2] = fmaf(xv, s[q].z, acc[i][2]);
+                acc[i][3] = fmaf(xv, s[q].w, acc[i][3]);
+            }
+    }
+}
+// the second half's partial sums join the first half's (two barriers inside)
+__device__ __forceinline__ void join_halves(float (*acc)[4], float *red, const ChainLanes &L)
+{
+    float *slot = red + (threadIdx.x & 127) * 16;
+    if (L.kh == 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) st4(slot + 4 * i, make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
+    }
+    __syncthreads();
+    if (L.kh == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 v = ld4(slot + 4 * i);
+            acc[i][0] += v.x, acc[i][1] += v.y, acc[i][2] += v.z, acc[i][3] += v.w;
+        }
+    }
+}
+// S[i][j] += sgn * sum_r X[r][sr0 + i] Y[r][sc0 + j], r < kN (X stride kD, Y stride kSS)
+template <int kN>
+__device__ __forceinline__ void update_state(float (*S)[4], const float *X, const float *Y, const ChainLanes &L,
+                                             float sgn)
+{
+#pragma unroll 4
+    for (int r = 0; r < kN; ++r) {
+        const float4 x0 = ld4(X + r * kD + L.sr0), x1 = ld4(X + r * kD + L.sr0 + 4);
+        const float4 y = ld4(Y + r * kSS + L.sc0);
+        const float yv[4] = {sgn * y.x, sgn * y.y, sgn * y.z, sgn * y.w};
+        const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) S[i][j] = fmaf(xv[i], yv[j], S[i][j]);
+    }
 }
 
 __device__ __forceinline__ void fwd_chain(const CbArgs &a, char *smem)
 {
     using St = FwdStage;
-    float *Ssm = (float *)(smem + 2 * St::kBytes), *upT = Ssm + 32 * kTS;
-    const int bh = blockIdx.x, cg = blockIdx.y * 32, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int col = cg + lane, row0 = w * 8, r0 = 2 * w;
+    float *Ssm = (float *)(smem + 2 * St::kBytes), *Usm = Ssm + kD * kSS, *red = Usm + kC * kSS;
+    const int bh = blockIdx.x, cg = blockIdx.y * kCols;
+    const ChainLanes L;
     auto prefetch = [&](int c) {
         char *base = smem + (c & 1) * St::kBytes;
         const float *rec = a.rec + ((size_t)bh * a.nc + c) * kRecFloats;
         copy_floats(rec + kRecW, (float *)base, kC * kD);
         copy_floats(rec + kRecK, (float *)(base + St::kW), kC * kD);
         float *Ud = (float *)(base + St::kW + St::kK);
-        for (int i = threadIdx.x; i < kC * 8; i += kChainThreads) {
-            const int r = i >> 3, e = (i & 7) * 4;
-            cp_async16(Ud + r * 32 + e, rec + kRecU + r * kD + cg + e);
+        for (int i = threadIdx.x; i < kC * kCols / 4; i += kChainThreads) {
+            const int r = i / (kCols / 4), e = (i % (kCols / 4)) * 4;
+            cp_async16(Ud + r * kCols + e, rec + kRecU + r * kD + cg + e);
         }
         cp_async_commit();
     };
-    float S[8];
+    float S[8][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) S[i] = a.h0 ? a.h0[((size_t)bh * kD + row0 + i) * kD + col] : 0.f;
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            S[i][j] = a.h0 ? a.h0[((size_t)bh * kD + L.sr0 + i) * kD + cg + L.sc0 + j] : 0.f;
     if (a.nc > 0) prefetch(0);
     for (int c = 0; c < a.nc; ++c) {
         const size_t ci = (size_t)bh * a.nc + c;
-        float *s0 = a.S0 + ci * kStateFloats;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) s0[(row0 + i) * kD + col] = S[i];
-        st4(Ssm + lane * kTS + row0, make_float4(S[0], S[1], S[2], S[3]));
-        st4(Ssm + lane * kTS + row0 + 4, make_float4(S[4], S[5], S[6], S[7]));
+        put_state(S, Ssm, a.S0 + ci * kStateFloats, L, cg);
         cp_async_wait_all();
         __syncthreads();   // chunk c's stage and the state tile are complete; chunk c-1's stage is free
         if (c + 1 < a.nc) prefetch(c + 1);
         const char *base = smem + (c & 1) * St::kBytes;
         const float *Wc = (const float *)base, *Kc = (const float *)(base + St::kW);
         const float *Uc = (const float *)(base + St::kW + St::kK);
-        // U' = U - W S, rows r0, r0 + 1
-        float acc0 = 0.f, acc1 = 0.f;
-        const float *sc = Ssm + lane * kTS;
-#pragma unroll 8
-        for (int k = 0; k < kD; k += 4) {
-            const float4 s = ld4(sc + k);
-            acc0 = dot4(ld4(Wc + r0 * kD + k), s, acc0);
-            acc1 = dot4(ld4(Wc + (r0 + 1) * kD + k), s, acc1);
-        }
-        const float u0 = Uc[r0 * 32 + lane] - acc0, u1 = Uc[(r0 + 1) * 32 + lane] - acc1;
-        upT[lane * kTU + r0] = u0;
-        upT[lane * kTU + r0 + 1] = u1;
-        a.Up[ci * kRowsFloats + r0 * kD + col] = u0;
-        a.Up[ci * kRowsFloats + (r0 + 1) * kD + col] = u1;
-        __syncthreads();
-        // S += K^T U'
-#pragma unroll 2
-        for (int r = 0; r < kC; r += 4) {
-            const float4 u4 = ld4(upT + lane * kTU + r);
-            const float u[4] = {u4.x, u4.y, u4.z, u4.w};
+        // U' = U - W S
+        float acc[4][4];
+        rows_times_state(Wc, Ssm, L, acc);
+        join_halves(acc, red, L);
+        if (L.kh == 0) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float kx[8];
-                lds8f(Kc + (r + j) * kD + row0, kx);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) S[i] = fmaf(kx[i], u[j], S[i]);
+            for (int i = 0; i < 4; ++i) {
+                const float4 u = ld4(Uc + (L.ur0 + i) * kCols + L.uc0);
+                const float4 v = make_float4(u.x - acc[i][0], u.y - acc[i][1], u.z - acc[i][2], u.w - acc[i][3]);
+                st4(Usm + (L.ur0 + i) * kSS + L.uc0, v);
+                st4(a.Up + ci * kRowsFloats + (L.ur0 + i) * kD + cg + L.uc0, v);
             }
         }
+        __syncthreads();
+        update_state<kC>(S, Kc, Usm, L, 1.f);   // S += K^T U'
     }
 }
 
@@ -357,9 +441,9 @@ template <typename TDo>
 __device__ __forceinline__ void bwd_chain(const CbArgs &a, char *smem)
 {
     using St = BwdStage<TDo>;
-    float *dSsm = (float *)(smem + 2 * St::kBytes), *dupT = dSsm + 32 * kTS;
-    const int bh = blockIdx.x, cg = blockIdx.y * 32, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int col = cg + lane, row0 = w * 8, r0 = 2 * w;
+    float *dSsm = (float *)(smem + 2 * St::kBytes), *dUsm = dSsm + kD * kSS, *red = dUsm + kC * kSS;
+    const int bh = blockIdx.x, cg = blockIdx.y * kCols;
+    const ChainLanes L;
     auto prefetch = [&](int c) {
         char *base = smem + (c & 1) * St::kBytes;
         const float *rec = a.rec + ((size_t)bh * a.nc + c) * kRecFloats;
@@ -371,17 +455,16 @@ __device__ __forceinline__ void bwd_chain(const CbArgs &a, char *smem)
         copy_floats(rec + kRecP, (float *)(base + St::kW + St::kK + St::kQb + St::kO), kQ * kC);
         cp_async_commit();
     };
-    float dS[8];
+    float dS[8][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) dS[i] = a.dh_final ? a.dh_final[((size_t)bh * kD + row0 + i) * kD + col] : 0.f;
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            dS[i][j] = a.dh_final ? a.dh_final[((size_t)bh * kD + L.sr0 + i) * kD + cg + L.sc0 + j] : 0.f;
     if (a.nc > 0) prefetch(a.nc - 1);
     for (int c = a.nc - 1; c >= 0; --c) {
         const size_t ci = (size_t)bh * a.nc + c;
-        float *ds1 = a.dS1 + ci * kStateFloats;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) ds1[(row0 + i) * kD + col] = dS[i];
-        st4(dSsm + lane * kTS + row0, make_float4(dS[0], dS[1], dS[2], dS[3]));
-        st4(dSsm + lane * kTS + row0 + 4, make_float4(dS[4], dS[5], dS[6], dS[7]));
+        put_state(dS, dSsm, a.dS1 + ci * kStateFloats, L, cg);
         cp_async_wait_all();
         __syncthreads();
         if (c > 0) prefetch(c - 1);
@@ -390,56 +473,57 @@ __device__ __forceinline__ void bwd_chain(const CbArgs &a, char *smem)
         const float *Qc = (const float *)(base + St::kW + St::kK);
         const TDo *Oc = (const TDo *)(base + St::kW + St::kK + St::kQb);
         const float *Pc = (const float *)(base + St::kW + St::kK + St::kQb + St::kO);
-        // dU' = P^T dO + K dS1, rows r0, r0 + 1
-        float g0 = 0.f, g1 = 0.f;
-        const float *sc = dSsm + lane * kTS;
-#pragma unroll 8
-        for (int k = 0; k < kD; k += 4) {
-            const float4 s = ld4(sc + k);
-            g0 = dot4(ld4(Kc + r0 * kD + k), s, g0);
-            g1 = dot4(ld4(Kc + (r0 + 1) * kD + k), s, g1);
-        }
+        // dU' = K dS1 + P^T dO
+        float g[4][4];
+        rows_times_state(Kc, dSsm, L, g);
+        if (L.kh == 1) {   // the second half also takes P^T dO
 #pragma unroll 4
-        for (int t = 0; t < kQ; ++t) {
-            const float o = to_f(Oc[t * 32 + lane]);
-            g0 = fmaf(Pc[t * kC + r0], o, g0);
-            g1 = fmaf(Pc[t * kC + r0 + 1], o, g1);
+            for (int t = 0; t < kQ; ++t) {
+                const float4 p = ld4(Pc + t * kC + L.ur0), o = ld4o(Oc + t * kCols + L.uc0);
+                const float pv[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    g[i][0] = fmaf(pv[i], o.x, g[i][0]);
+                    g[i][1] = fmaf(pv[i], o.y, g[i][1]);
+                    g[i][2] = fmaf(pv[i], o.z, g[i][2]);
+                    g[i][3] = fmaf(pv[i], o.w, g[i][3]);
+                }
+            }
         }
-        dupT[lane * kTU + r0] = g0;
-        dupT[lane * kTU + r0 + 1] = g1;
-        a.dUp[ci * kRowsFloats + r0 * kD + col] = g0;
-        a.dUp[ci * kRowsFloats + (r0 + 1) * kD + col] = g1;
+        join_halves(g, red, L);
+        if (L.kh == 0) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 v = make_float4(g[i][0], g[i][1], g[i][2], g[i][3]);
+                st4(dUsm + (L.ur0 + i) * kSS + L.uc0, v);
+                st4(a.dUp + ci * kRowsFloats + (L.ur0 + i) * kD + cg + L.uc0, v);
+            }
+        }
         __syncthreads();
         // dS0 = dS1 + Q^T dO - W^T dU'
 #pragma unroll 4
         for (int t = 0; t < kQ; ++t) {
-            float qx[8];
-            lds8f(Qc + t * kD + row0, qx);
-            const float o = to_f(Oc[t * 32 + lane]);
+            const float4 x0 = ld4(Qc + t * kD + L.sr0), x1 = ld4(Qc + t * kD + L.sr0 + 4);
+            const float4 o = ld4o(Oc + t * kCols + L.sc0);
+            const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            const float ov[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) dS[i] = fmaf(qx[i], o, dS[i]);
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) dS[i][j] = fmaf(xv[i], ov[j], dS[i][j]);
         }
-#pragma unroll 2
-        for (int r = 0; r < kC; r += 4) {
-            const float4 g4 = ld4(dupT + lane * kTU + r);
-            const float g[4] = {g4.x, g4.y, g4.z, g4.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float wx[8];
-                lds8f(Wc + (r + j) * kD + row0, wx);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) dS[i] = fmaf(-wx[i], g[j], dS[i]);
-            }
-        }
+        update_state<kC>(dS, Wc, dUsm, L, -1.f);
     }
     if (a.dh0) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) a.dh0[((size_t)bh * kD + row0 + i) * kD + col] = dS[i];
+        for (int i = 0; i < 8; ++i)
+            st4(a.dh0 + ((size_t)bh * kD + L.sr0 + i) * kD + cg + L.sc0,
+                make_float4(dS[i][0], dS[i][1], dS[i][2], dS[i][3]));
     }
 }
 
 template <typename TDo>
-__global__ void __launch_bounds__(kChainThreads, 2) cb_chains(const CbArgs a)
+__global__ void __launch_bounds__(kChainThreads, 1) cb_chains(const CbArgs a)
 {
     extern __shared__ float4 sm_chain[];
     if (blockIdx.z == 0) fwd_chain(a, (char *)sm_chain);
@@ -456,13 +540,15 @@ __device__ __forceinline__ float quad_sum(float x)
     return x + __shfl_xor_sync(0xffffffffu, x, 2);
 }
 
-// 3a. products with the boundary states. Thread: row kk = tid / 4 of S0
-// (then dS1), float4 columns 16 i + 4 qq (qq = tid % 4), i = 0 .. 7; a row
-// of the left operand times that row is a dot product over the quad.
+// 3a. products with the boundary states. Thread (256 per CTA): rows kk and
+// kk + 64 of S0 (then of dS1), kk = tid / 4, float4 columns 16 i + 4 qq
+// (qq = tid % 4), i = 0 .. 7; a row of the left operand times those rows is
+// a dot product over the quad, each value read feeding both rows.
+constexpr int kGradSThreads = 256;
 constexpr int kGradSSmemFloats = (kQ + 2 * kC) * kS;
 
 template <typename TDo>
-__global__ void __launch_bounds__(kGradThreads, 2) cb_grad_s(const CbArgs a)
+__global__ void __launch_bounds__(kGradSThreads, 2) cb_grad_s(const CbArgs a)
 {
     extern __shared__ float4 sm_grad_s[];
     float *dOs = (float *)sm_grad_s, *Ups = dOs + kQ * kS, *dUps = Ups + kC * kS;
@@ -470,60 +556,78 @@ __global__ void __launch_bounds__(kGradThreads, 2) cb_grad_s(const CbArgs a)
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, kk = tid >> 2, qq = tid & 3;
     const ChunkRows cr = chunk_rows(a, bh, c);
     float *rec = a.rec + (size_t)ci * kRecFloats;
-    float4 sq[8];
-    {
-        const float *s0 = a.S0 + (size_t)ci * kStateFloats + kk * kD + 4 * qq;
+    float4 sa[8], sb[8];
+    auto load_rows = [&](const float *m) {
+        const float *p0 = m + (size_t)ci * kStateFloats + kk * kD + 4 * qq, *p1 = p0 + 64 * kD;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) sq[i] = __ldg((const float4 *)(s0 + 16 * i));
-    }
+        for (int i = 0; i < 8; ++i) {
+            sa[i] = __ldg((const float4 *)(p0 + 16 * i));
+            sb[i] = __ldg((const float4 *)(p1 + 16 * i));
+        }
+    };
+    load_rows(a.S0);
     stage_f32<false, kQ, TDo>(a, cr, (const TDo *)a.d_o, dOs);
     {
         const float *up = a.Up + (size_t)ci * kRowsFloats, *dup = a.dUp + (size_t)ci * kRowsFloats;
-        for (int i = tid; i < kC * kD / 4; i += kGradThreads) {
+        for (int i = tid; i < kC * kD / 4; i += kGradSThreads) {
             const int r = i >> 5, e = (i & 31) * 4;
             st4(Ups + r * kS + e, __ldg((const float4 *)(up + r * kD + e)));
             st4(dUps + r * kS + e, __ldg((const float4 *)(dup + r * kD + e)));
         }
     }
     __syncthreads();
-    // dP = (dO U'^T) masked: row t = w, column s = lane -> the record's P slot
-    {
+    // dP = (dO U'^T) masked: rows t = w, w + 8, column s = lane -> the record's P slot
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int t = w + 8 * h;
         float acc = 0.f;
-        const float *x = dOs + w * kS, *y = Ups + lane * kS;
+        const float *x = dOs + t * kS, *y = Ups + lane * kS;
 #pragma unroll 8
         for (int d = 0; d < kD; d += 4) acc = dot4(ld4(x + d), ld4(y + d), acc);
-        rec[kRecP + w * kC + lane] = lane <= w * a.nh + a.nh - 1 ? acc : 0.f;
+        rec[kRecP + t * kC + lane] = lane <= t * a.nh + a.nh - 1 ? acc : 0.f;
     }
-    auto row_dot = [&](const float *x) {
-        float acc0 = 0.f, acc1 = 0.f;
+    auto row_dot2 = [&](const float *x, float &v0, float &v1) {
+        float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-            acc0 = dot4(ld4(x + 16 * i + 4 * qq), sq[i], acc0);
-            acc1 = dot4(ld4(x + 16 * (i + 1) + 4 * qq), sq[i + 1], acc1);
+        for (int i = 0; i < 8; ++i) {
+            const float4 xv = ld4(x + 16 * i + 4 * qq);
+            a0 = dot4(xv, sa[i], a0);
+            a1 = dot4(xv, sb[i], a1);
         }
-        return quad_sum(acc0 + acc1);
+        v0 = quad_sum(a0);
+        v1 = quad_sum(a1);
     };
     // dq <- dO S0^T, dW = -dU' S0^T (the record's W slot)
 #pragma unroll 2
     for (int t = 0; t < kQ; ++t) {
-        const float v = row_dot(dOs + t * kS);
-        if (qq == 0 && t < cr.nt) a.dq[token_row(a, cr, t) * kD + kk] = v;
+        float v0, v1;
+        row_dot2(dOs + t * kS, v0, v1);
+        if (qq == 0 && t < cr.nt) {
+            float *dq = a.dq + token_row(a, cr, t) * kD;
+            dq[kk] = v0;
+            dq[kk + 64] = v1;
+        }
     }
 #pragma unroll 2
     for (int r = 0; r < kC; ++r) {
-        const float v = row_dot(dUps + r * kS);
-        if (qq == 0) rec[kRecW + r * kD + kk] = -v;
+        float v0, v1;
+        row_dot2(dUps + r * kS, v0, v1);
+        if (qq == 0) {
+            rec[kRecW + r * kD + kk] = -v0;
+            rec[kRecW + r * kD + kk + 64] = -v1;
+        }
     }
     // dk <- U' dS1^T
-    {
-        const float *ds1 = a.dS1 + (size_t)ci * kStateFloats + kk * kD + 4 * qq;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) sq[i] = __ldg((const float4 *)(ds1 + 16 * i));
-    }
+    load_rows(a.dS1);
 #pragma unroll 2
     for (int r = 0; r < kC; ++r) {
-        const float v = row_dot(Ups + r * kS);
-        if (qq == 0 && r < cr.R) a.dk[key_row(a, cr, r) * kD + kk] = v;
+        float v0, v1;
+        row_dot2(Ups + r * kS, v0, v1);
+        if (qq == 0 && r < cr.R) {
+            float *dk = a.dk + key_row(a, cr, r) * kD;
+            dk[kk] = v0;
+            dk[kk + 64] = v1;
+        }
     }
 }
 
@@ -653,7 +757,7 @@ cudaError_t launch_typed(const BwdProblem &p, const CbArgs &a)
     if ((e = cudaFuncSetAttribute(cb_chains<TDo>, cudaFuncAttributeMaxDynamicSharedMemorySize, chain_smem)) !=
         cudaSuccess)
         return e;
-    const dim3 chain_grid(p.B * p.H, kD / 32, 2);
+    const dim3 chain_grid(p.B * p.H, kD / kCols, 2);
     if (n_chunks == 0) {   // T = 0: dh0 = dh_final (the reverse chains only)
         cb_chains<TDo><<<chain_grid, kChainThreads, chain_smem, p.stream>>>(a);
         return cudaGetLastError();
@@ -669,7 +773,7 @@ cudaError_t launch_typed(const BwdProblem &p, const CbArgs &a)
     if ((e = cudaFuncSetAttribute(cb_grad_s<TDo>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs_smem)) !=
         cudaSuccess)
         return e;
-    cb_grad_s<TDo><<<(unsigned)n_chunks, kGradThreads, gs_smem, p.stream>>>(a);
+    cb_grad_s<TDo><<<(unsigned)n_chunks, kGradSThreads, gs_smem, p.stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int gr_smem = (int)(kGradRSmemFloats * sizeof(float));
     if ((e = cudaFuncSetAttribute(cb_grad_r<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, gr_smem)) !=
