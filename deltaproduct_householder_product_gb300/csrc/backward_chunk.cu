@@ -131,7 +131,7 @@ __device__ __forceinline__ size_t token_row(const CbArgs &a, const ChunkRows &cr
 
 // fp32 [rows][kS] tile of the chunk's key rows (kKeys) or token rows of a
 // [.,128] tensor, zero past the valid rows; every thread takes part.
-template <bool kKeys, int kRows, typename TIn>
+template <bool kKeys, int kRows, typename TIn, int kStride = kS>
 __device__ __forceinline__ void stage_f32(const CbArgs &a, const ChunkRows &cr, const TIn *src, float *dst)
 {
     for (int i = threadIdx.x; i < kRows * 16; i += blockDim.x) {
@@ -143,8 +143,8 @@ __device__ __forceinline__ void stage_f32(const CbArgs &a, const ChunkRows &cr, 
 #pragma unroll
             for (int j = 0; j < 8; ++j) x[j] = 0.f;
         }
-        st4(dst + r * kS + e, make_float4(x[0], x[1], x[2], x[3]));
-        st4(dst + r * kS + e + 4, make_float4(x[4], x[5], x[6], x[7]));
+        st4(dst + r * kStride + e, make_float4(x[0], x[1], x[2], x[3]));
+        st4(dst + r * kStride + e + 4, make_float4(x[4], x[5], x[6], x[7]));
     }
 }
 template <typename TIn>
@@ -631,14 +631,17 @@ __global__ void __launch_bounds__(kGradSThreads, 2) cb_grad_s(const CbArgs a)
     }
 }
 
-// 3b. the rest of the chunk's gradients
-constexpr int kGradRSmemFloats = 4 * kC * kS + kQ * kS + 4 * kC * kL + kQ * kL + kC;
+// 3b. the rest of the chunk's gradients. K and V tiles use a row stride of
+// 136 floats: in the dT product a quarter-warp reads rows m, m + 2 of them
+// at four interleaved column chunks, which then fall in distinct banks.
+constexpr int kSR = kD + 8;
+constexpr int kGradRSmemFloats = 2 * kC * kSR + 2 * kC * kS + kQ * kS + 4 * kC * kL + kQ * kL + kC;
 
 template <typename TIn>
 __global__ void __launch_bounds__(kGradThreads, 2) cb_grad_r(const CbArgs a)
 {
     extern __shared__ float4 sm_grad_r[];
-    float *Ks = (float *)sm_grad_r, *Vs = Ks + kC * kS, *dUps = Vs + kC * kS, *dWs = dUps + kC * kS;
+    float *Ks = (float *)sm_grad_r, *Vs = Ks + kC * kSR, *dUps = Vs + kC * kSR, *dWs = dUps + kC * kS;
     float *Qs = dWs + kC * kS;
     float *Ts = Qs + kQ * kS, *KKs = Ts + kC * kL, *dTs = KKs + kC * kL, *Xs = dTs + kC * kL;
     float *dPs = Xs + kC * kL, *be = dPs + kQ * kL;
@@ -649,12 +652,12 @@ __global__ void __launch_bounds__(kGradThreads, 2) cb_grad_r(const CbArgs a)
     const float *dup = a.dUp + (size_t)ci * kRowsFloats;
     for (int i = tid; i < kC * kD / 4; i += kGradThreads) {
         const int r = i >> 5, e = (i & 31) * 4;
-        st4(Ks + r * kS + e, __ldg((const float4 *)(rec + kRecK + r * kD + e)));
+        st4(Ks + r * kSR + e, __ldg((const float4 *)(rec + kRecK + r * kD + e)));
         st4(dUps + r * kS + e, __ldg((const float4 *)(dup + r * kD + e)));
         st4(dWs + r * kS + e, __ldg((const float4 *)(rec + kRecW + r * kD + e)));
         if (r < kQ) st4(Qs + r * kS + e, __ldg((const float4 *)(rec + kRecQ + r * kD + e)));
     }
-    stage_f32<true, kC, TIn>(a, cr, (const TIn *)a.v, Vs);
+    stage_f32<true, kC, TIn, kSR>(a, cr, (const TIn *)a.v, Vs);
     stage_betas<TIn>(a, cr, be);
     for (int i = tid; i < kC * kC; i += kGradThreads) {
         Ts[(i >> 5) * kL + (i & 31)] = rec[kRecT + i];
@@ -670,23 +673,42 @@ __global__ void __launch_bounds__(kGradThreads, 2) cb_grad_r(const CbArgs a)
             float *dq = a.dq + token_row(a, cr, w) * kD + d;
             float4 acc = ld4(dq);
 #pragma unroll 8
-            for (int s = 0; s < kC; ++s) acc = axpy4(dPs[w * kL + s], ld4(Ks + s * kS + d), acc);
+            for (int s = 0; s < kC; ++s) acc = axpy4(dPs[w * kL + s], ld4(Ks + s * kSR + d), acc);
             st4(dq, acc);
         }
     }
-    // dT = (dW K^T + dU' V^T) B: rows 2w, 2w+1, column m = lane
+    // dT = (dW K^T + dU' V^T) B. Thread: columns m = 2 mp, 2 mp + 1, rows
+    // 4 rq .. 4 rq + 3, float4 column chunks j = dq (mod 4) of the 128-term
+    // contraction; the four quarters meet by quad shuffles.
     {
-        float t0 = 0.f, t1 = 0.f;
-        const float *km = Ks + lane * kS, *vm = Vs + lane * kS;
-        const float *w0 = dWs + 2 * w * kS, *w1 = w0 + kS, *u0 = dUps + 2 * w * kS, *u1 = u0 + kS;
-#pragma unroll 4
-        for (int d = 0; d < kD; d += 4) {
-            const float4 k4 = ld4(km + d), v4 = ld4(vm + d);
-            t0 = dot4(ld4(u0 + d), v4, dot4(ld4(w0 + d), k4, t0));
-            t1 = dot4(ld4(u1 + d), v4, dot4(ld4(w1 + d), k4, t1));
+        const int dq = tid & 3, mp = (tid >> 2) & 15, rq = tid >> 6;
+        float t[4][2];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) t[i][0] = t[i][1] = 0.f;
+#pragma unroll 2
+        for (int jj = 0; jj < 8; ++jj) {
+            const int d = 4 * (4 * jj + dq);
+            const float4 k0 = ld4(Ks + (2 * mp) * kSR + d), k1 = ld4(Ks + (2 * mp + 1) * kSR + d);
+            const float4 v0 = ld4(Vs + (2 * mp) * kSR + d), v1 = ld4(Vs + (2 * mp + 1) * kSR + d);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 x = ld4(dWs + (4 * rq + i) * kS + d), y = ld4(dUps + (4 * rq + i) * kS + d);
+                t[i][0] = dot4(y, v0, dot4(x, k0, t[i][0]));
+                t[i][1] = dot4(y, v1, dot4(x, k1, t[i][1]));
+            }
         }
-        dTs[2 * w * kL + lane] = t0 * be[lane];
-        dTs[(2 * w + 1) * kL + lane] = t1 * be[lane];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) t[i][j] = quad_sum(t[i][j]);
+        // lane dq stores row 4 rq + dq
+        const int r = 4 * rq + dq;
+        float o0 = t[0][0], o1 = t[0][1];
+#pragma unroll
+        for (int i = 1; i < 4; ++i)
+            if (dq == i) o0 = t[i][0], o1 = t[i][1];
+        dTs[r * kL + 2 * mp] = o0 * be[2 * mp];
+        dTs[r * kL + 2 * mp + 1] = o1 * be[2 * mp + 1];
     }
     __syncthreads();
     // X = dT T^T: rows 2w, 2w+1, column m = lane
@@ -711,39 +733,54 @@ __global__ void __launch_bounds__(kGradThreads, 2) cb_grad_r(const CbArgs a)
         dTs[r * kL + lane] = lane < r ? g : 0.f;
     }
     __syncthreads();
-    // rows m = 2w, 2w+1, columns 4 lane .. 4 lane + 3:
+    // rows m0 = 2w, m1 = 2w + 1 together (every loaded row feeds both),
+    // columns 4 lane .. 4 lane + 3:
     //   dk += dP^T Q + B (T^T dW + dG K) + (B dG)^T K,  dv = B T^T dU'
     //   dbeta = sum over columns of K o T^T dW + V o T^T dU', + sum_s dG o K K^T
-    {
+    // (T and dG are lower triangular, so the joint ranges add only zeros)
+    const int m0 = 2 * w, m1 = m0 + 1;
+    if (m0 < cr.R) {   // warp-uniform
         const int d = 4 * lane;
-#pragma unroll 1
-        for (int i = 0; i < 2; ++i) {
-            const int m = 2 * w + i;
-            if (m >= cr.R) break;   // warp-uniform
-            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-            float4 tw = z, tu = z, gk = z, gtk = z, pq = z;
-            for (int r = m; r < kC; ++r) {
-                const float t = Ts[r * kL + m];
-                tw = axpy4(t, ld4(dWs + r * kS + d), tw);
-                tu = axpy4(t, ld4(dUps + r * kS + d), tu);
-            }
-            for (int s = 0; s < m; ++s) gk = axpy4(dTs[m * kL + s], ld4(Ks + s * kS + d), gk);
-            for (int r = m + 1; r < kC; ++r) gtk = axpy4(be[r] * dTs[r * kL + m], ld4(Ks + r * kS + d), gtk);
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        // gt: (B dG)^T K + dP^T Q, the terms of dk outside B (...)
+        float4 tw0 = z, tw1 = z, tu0 = z, tu1 = z, gk0 = z, gk1 = z, gt0 = z, gt1 = z;
+        for (int r = m0; r < kC; ++r) {
+            const float4 x = ld4(dWs + r * kS + d), y = ld4(dUps + r * kS + d);
+            const float t0 = Ts[r * kL + m0], t1 = Ts[r * kL + m1];
+            tw0 = axpy4(t0, x, tw0), tw1 = axpy4(t1, x, tw1);
+            tu0 = axpy4(t0, y, tu0), tu1 = axpy4(t1, y, tu1);
+        }
+        for (int s2 = 0; s2 < m1; ++s2) {
+            const float4 k4 = ld4(Ks + s2 * kSR + d);
+            gk0 = axpy4(dTs[m0 * kL + s2], k4, gk0), gk1 = axpy4(dTs[m1 * kL + s2], k4, gk1);
+        }
+        for (int r = m1; r < kC; ++r) {
+            const float4 k4 = ld4(Ks + r * kSR + d);
+            gt0 = axpy4(be[r] * dTs[r * kL + m0], k4, gt0), gt1 = axpy4(be[r] * dTs[r * kL + m1], k4, gt1);
+        }
 #pragma unroll 4
-            for (int t = 0; t < kQ; ++t) pq = axpy4(dPs[t * kL + m], ld4(Qs + t * kS + d), pq);
+        for (int t = 0; t < kQ; ++t) {
+            const float4 q4 = ld4(Qs + t * kS + d);
+            gt0 = axpy4(dPs[t * kL + m0], q4, gt0), gt1 = axpy4(dPs[t * kL + m1], q4, gt1);
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int m = m0 + i;
+            const float4 tw = i ? tw1 : tw0, tu = i ? tu1 : tu0, gk = i ? gk1 : gk0, gt = i ? gt1 : gt0;
             const float bm = be[m];
-            const size_t row = key_row(a, cr, m);
-            float *dkp = a.dk + row * kD + d;
-            const float4 k0 = ld4(dkp);
-            const float4 dk = make_float4(k0.x + pq.x + bm * (tw.x + gk.x) + gtk.x, k0.y + pq.y + bm * (tw.y + gk.y) + gtk.y,
-                                          k0.z + pq.z + bm * (tw.z + gk.z) + gtk.z, k0.w + pq.w + bm * (tw.w + gk.w) + gtk.w);
-            float db = dot4(ld4(Ks + m * kS + d), tw, dot4(ld4(Vs + m * kS + d), tu, 0.f));
+            float db = dot4(ld4(Ks + m * kSR + d), tw, dot4(ld4(Vs + m * kSR + d), tu, 0.f));
             if (lane < m) db = fmaf(dTs[m * kL + lane], KKs[m * kL + lane], db);
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) db += __shfl_xor_sync(0xffffffffu, db, o);
-            st4(dkp, dk);
-            st4(a.dv + row * kD + d, make_float4(bm * tu.x, bm * tu.y, bm * tu.z, bm * tu.w));
-            if (lane == 0) a.dbeta[row] = db;
+            if (m < cr.R) {
+                const size_t row = key_row(a, cr, m);
+                float *dkp = a.dk + row * kD + d;
+                const float4 k0 = ld4(dkp);
+                st4(dkp, make_float4(k0.x + bm * (tw.x + gk.x) + gt.x, k0.y + bm * (tw.y + gk.y) + gt.y,
+                                     k0.z + bm * (tw.z + gk.z) + gt.z, k0.w + bm * (tw.w + gk.w) + gt.w));
+                st4(a.dv + row * kD + d, make_float4(bm * tu.x, bm * tu.y, bm * tu.z, bm * tu.w));
+                if (lane == 0) a.dbeta[row] = db;
+            }
         }
     }
 }
