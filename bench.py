@@ -355,6 +355,33 @@ def backward_measure(dp, dev, hbm_peak, steps=5, warmup=2):
         return e0.elapsed_time(e1) / steps
     ms = timed("auto")
     ms_rec = timed("recurrent")
+    # the gated recipe at the same batch, heads and length (n_h = 4): the
+    # chunked form (impl="chunk_tc"; "auto" keeps the recurrent form for
+    # gated problems) against the recurrent one
+    wg = W.GATED.scaled(B=w.B, H=w.H, T=w.T)
+    xg = {k: (None if v is None else v.to(dev)) for k, v in W.make_inputs(wg).items()}
+    dims_g = _lib.make_dims(wg.B, wg.T, wg.H, wg.Dk, wg.Dv, wg.nh, wg.torch_dtype, "chunk_tc", torch.float32)
+    ws_g = torch.zeros(_lib.backward_workspace_size(dims_g), dtype=torch.uint8, device=dev)
+
+    def timed_g(impl):
+        def call():
+            return dp.backward(xg["q"], xg["k"], xg["v"], xg["beta"], xg["g"], xg["h0"], d_o=d_o, dh_final=dhf,
+                               workspace=ws_g, impl=impl)
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        stream = torch.cuda.current_stream()
+        e0.record(stream)
+        for _ in range(steps):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+    gated_form = {"workload": f"{wg.name} recipe at B{wg.B} H{wg.H} T{wg.T}",
+                  "chunked_ms_per_call": timed_g("chunk_tc"), "recurrent_ms_per_call": timed_g("recurrent")}
+    gated_form["chunked_tokens_per_s"] = wg.B * wg.T / (gated_form["chunked_ms_per_call"] * 1e-3)
+    del xg, ws_g
     nh, Dk, Dv = w.nh, w.Dk, w.Dv
     gated = 1 if w.gated else 0
     per_tok = 2 * (Dk + nh * Dk + nh * Dv + nh + gated) + 4 * Dv + 4 * (Dk + nh * Dk + nh * Dv + nh + gated)
@@ -365,7 +392,7 @@ def backward_measure(dp, dev, hbm_peak, steps=5, warmup=2):
             "tokens_per_s": w.B * w.T / (ms * 1e-3),
             "kernel": ("chunked: cb_prep, cb_chains, cb_grad (CUDA cores)" if not w.gated
                        else "backward_kernel (recurrent, CUDA cores)"),
-            "recurrent_ms_per_call": ms_rec,
+            "recurrent_ms_per_call": ms_rec, "gated": gated_form,
             "workspace_bytes": int(ws.numel()),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "algorithmic_bytes": step_bytes}}

@@ -328,8 +328,10 @@ dp_status backward_impl(const dp_dims *dims, const int *cu, const void *q, const
     p.g = g;
     p.cu = cu;
     // AUTO takes the chunked form for ungated dense problems with D = 128
-    // when the workspace holds its records, else the recurrent form
-    bool chunked = dims->impl != DP_IMPL_RECURRENT && dp::backward_chunk_supported(p);
+    // when the workspace holds its records, else the recurrent form;
+    // CHUNK_TC also takes gated dense problems with D = 128
+    bool chunked = dims->impl != DP_IMPL_RECURRENT && dp::backward_chunk_supported(p) &&
+                   (g == nullptr || dims->impl == DP_IMPL_CHUNK_TC);
     if (dims->impl == DP_IMPL_CHUNK_TC && !chunked) return DP_ERR_UNSUPPORTED;
     if (chunked && dims->impl == DP_IMPL_AUTO && workspace_bytes < bwd_chunk_need(p)) chunked = false;
     const size_t need = chunked ? bwd_chunk_need(p) : bwd_recurrent_need(p);

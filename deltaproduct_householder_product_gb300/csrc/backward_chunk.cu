@@ -47,11 +47,21 @@ constexpr int kL = kC + 1; // row stride of [.][32] tiles
 
 // record of one chunk (fp32): W [32][128] | U [32][128] | T [32][32] |
 // P [16][32] | K K^T [32][32] | K [32][128] | Q [16][128] (K and Q as fp32
-// for the chains). After the chains, cb_grad_s overwrites W with dW and P
-// with dP, which cb_grad_r reads.
+// for the chains), and for gated problems: Kd [32][128] (the keys decayed to
+// the chunk's end, (Gamma_C / Gamma_r) k_r, for the chains) | Pr [16][32]
+// (Q K^T masked, before the decay; P holds it decayed) | E [32][32]
+// (Gamma_r / Gamma_s, s <= r) | Gamma [32] | ratio [32] (Gamma_C /
+// Gamma_r) | lg [32] (the rows' log gates) | aux [4] (<dS1, S0>). After the
+// chains, cb_grad_s overwrites W with dW and P with dP (before the decay),
+// which cb_grad_r reads.
 constexpr size_t kRecW = 0, kRecU = kC * kD, kRecT = 2 * kC * kD, kRecP = kRecT + kC * kC;
 constexpr size_t kRecKK = kRecP + kQ * kC, kRecK = kRecKK + kC * kC, kRecQ = kRecK + kC * kD;
-constexpr size_t kRecFloats = kRecQ + kQ * kD;
+constexpr size_t kRecKd = kRecQ + kQ * kD, kRecPr = kRecKd + kC * kD, kRecE = kRecPr + kQ * kC;
+constexpr size_t kRecGm = kRecE + kC * kC, kRecRt = kRecGm + kC, kRecLg = kRecRt + kC, kRecAux = kRecLg + kC;
+constexpr size_t kRecFloats = kRecAux + 4;
+// log gates below this are taken as it (a gate of 1.8e-35: the forward's
+// chunk path clamps the same way)
+constexpr float kMinLogGate = -80.f;
 constexpr size_t kStateFloats = (size_t)kD * kD;   // S0 or dS1 of one chunk
 constexpr size_t kRowsFloats = (size_t)kC * kD;    // U' or dU' of one chunk
 
@@ -63,6 +73,9 @@ struct CbArgs {
     const float *dh_final;
     float *dq, *dk, *dv, *dbeta, *dh0;
     float *rec, *S0, *dS1, *Up, *dUp;   // workspace areas, [B*H*nc] chunks each
+    const void *g;                      // gates [B,T,H] (gated instantiations)
+    float *dg;
+    uint32_t *status;
 };
 
 __device__ __forceinline__ float to_f(float x) { return x; }
@@ -156,14 +169,60 @@ __device__ __forceinline__ void stage_betas(const CbArgs &a, const ChunkRows &cr
 
 // ------------------------------------------------------------------ 1. prep
 constexpr int kPrepThreads = 256;
-constexpr int kPrepSmemFloats = 2 * kC * kS + kQ * kS + 2 * kC * kL + kC;
+constexpr int kPrepSmemFloats = 2 * kC * kS + kQ * kS + 3 * kC * kL + 4 * kC;
 
+// Gated chunks: the rows' log gates lg_r (log g_t at a token's first row,
+// clamped below at kMinLogGate; 0 elsewhere and on padding rows) and every
+// decay factor as exp of a directly accumulated range sum of them (never a
+// difference of prefix sums, so a zero gate cuts the decay exactly):
+// E[r][s] = exp(sum_{s < x <= r} lg_x), Gamma_r = exp(sum_{x <= r} lg_x),
+// ratio_r = Gamma_C / Gamma_r = exp(sum_{r < x < 32} lg_x). A gate < 0 or
+// NaN records a device error.
 template <typename TIn>
+__device__ __forceinline__ void prep_gates(const CbArgs &a, const ChunkRows &cr, float *lg, float *Gm, float *Rt,
+                                           float *E, float *rec)
+{
+    const int tid = threadIdx.x;
+    if (tid < kC) {
+        float x = 0.f;
+        if (tid < cr.R && tid % a.nh == 0) {
+            const float gv = to_f(((const TIn *)a.g)[token_row(a, cr, tid / a.nh)]);
+            if (!(gv >= 0.f)) report_bad_sequence(a.status);
+            x = gv > 0.f ? fmaxf(logf(gv), kMinLogGate) : kMinLogGate;
+        }
+        lg[tid] = x;
+        rec[kRecLg + tid] = x;
+    }
+    __syncthreads();
+    for (int i = tid; i < kC * kC; i += blockDim.x) {
+        const int r = i >> 5, s2 = i & 31;
+        float e = 0.f;
+        if (s2 <= r) {
+            float acc = 0.f;   // sum_{s < x <= r} lg_x
+            for (int x2 = s2 + 1; x2 <= r; ++x2) acc += lg[x2];
+            e = expf(acc);
+        }
+        E[r * kL + s2] = e;
+        rec[kRecE + i] = e;
+    }
+    if (tid < kC) {
+        const int r = tid;
+        float sg = 0.f, sr = 0.f;   // sum_{x <= r} lg_x, sum_{r < x < 32} lg_x
+        for (int x2 = 0; x2 <= r; ++x2) sg += lg[x2];
+        for (int x2 = r + 1; x2 < kC; ++x2) sr += lg[x2];
+        const float gm = expf(sg), rt = expf(sr);
+        Gm[r] = gm, Rt[r] = rt;
+        rec[kRecGm + r] = gm, rec[kRecRt + r] = rt;
+    }
+}
+
+template <typename TIn, bool kG>
 __global__ void __launch_bounds__(kPrepThreads) cb_prep(const CbArgs a)
 {
     extern __shared__ float4 sm_prep[];
     float *Ks = (float *)sm_prep, *Vs = Ks + kC * kS, *Qs = Vs + kC * kS;
-    float *KK = Qs + kQ * kS, *Ts = KK + kC * kL, *be = Ts + kC * kL;
+    float *KK = Qs + kQ * kS, *Ts = KK + kC * kL, *E = Ts + kC * kL, *be = E + kC * kL;
+    float *lg = be + kC, *Gm = lg + kC, *Rt = Gm + kC;
     const int ci = blockIdx.x, bh = ci / a.nc, c = ci - bh * a.nc;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const ChunkRows cr = chunk_rows(a, bh, c);
@@ -172,12 +231,21 @@ __global__ void __launch_bounds__(kPrepThreads) cb_prep(const CbArgs a)
     stage_f32<true, kC, TIn>(a, cr, (const TIn *)a.v, Vs);
     stage_f32<false, kQ, TIn>(a, cr, (const TIn *)a.q, Qs);
     stage_betas<TIn>(a, cr, be);
+    if (kG) prep_gates<TIn>(a, cr, lg, Gm, Rt, E, rec);
     __syncthreads();
-    // fp32 K and Q (zero padding rows included) for the chains
+    // fp32 K and Q (zero padding rows included) for the chains; gated: Kd
     for (int i = threadIdx.x; i < (kC + kQ) * kD / 4; i += kPrepThreads) {
         const int r = i >> 5, e = (i & 31) * 4;
-        if (r < kC) st4(rec + kRecK + r * kD + e, ld4(Ks + r * kS + e));
-        else st4(rec + kRecQ + (r - kC) * kD + e, ld4(Qs + (r - kC) * kS + e));
+        if (r < kC) {
+            const float4 k4 = ld4(Ks + r * kS + e);
+            st4(rec + kRecK + r * kD + e, k4);
+            if (kG) {
+                const float f = Rt[r];
+                st4(rec + kRecKd + r * kD + e, make_float4(f * k4.x, f * k4.y, f * k4.z, f * k4.w));
+            }
+        } else {
+            st4(rec + kRecQ + (r - kC) * kD + e, ld4(Qs + (r - kC) * kS + e));
+        }
     }
     // K K^T rows w, w+8, w+16, w+24 and P rows w, w+8; lane = column s
     {
@@ -193,28 +261,36 @@ __global__ void __launch_bounds__(kPrepThreads) cb_prep(const CbArgs a)
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            KK[(w + 8 * i) * kL + lane] = acc[i];
-            rec[kRecKK + (w + 8 * i) * kC + lane] = acc[i];
+            const int r = w + 8 * i;
+            rec[kRecKK + r * kC + lane] = acc[i];
+            // G = B (K K^T o E), strictly lower: the substitution's operand
+            KK[r * kL + lane] = lane < r ? be[r] * acc[i] * (kG ? E[r * kL + lane] : 1.f) : 0.f;
         }
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-            const int t = w + 8 * i;
-            rec[kRecP + t * kC + lane] = lane <= t * a.nh + a.nh - 1 ? acc[4 + i] : 0.f;
+            const int t = w + 8 * i, last = t * a.nh + a.nh - 1;
+            const float p = lane <= last ? acc[4 + i] : 0.f;
+            if (kG) {
+                rec[kRecPr + t * kC + lane] = p;
+                rec[kRecP + t * kC + lane] = last < kC ? p * E[last * kL + lane] : 0.f;
+            } else {
+                rec[kRecP + t * kC + lane] = p;
+            }
         }
     }
     __syncthreads();
-    // T = (I + tril(B K K^T, -1))^{-1}: forward substitution, lane = column
+    // T = (I + G)^{-1}: forward substitution, lane = column
     if (w == 0) {
         const int s = lane;
         for (int r = 0; r < kC; ++r) {
             float x = (r == s) ? 1.f : 0.f;
-            for (int m = s; m < r; ++m) x = fmaf(-be[r] * KK[r * kL + m], Ts[m * kL + s], x);
+            for (int m = s; m < r; ++m) x = fmaf(-KK[r * kL + m], Ts[m * kL + s], x);
             Ts[r * kL + s] = x;
             rec[kRecT + r * kC + s] = x;
         }
     }
     __syncthreads();
-    // W = T B K, U = T B V: warp w rows 4w .. 4w+3, lane = 4 columns
+    // W = T diag(beta Gamma) K, U = T diag(beta) V: warp w rows 4w .. 4w+3, lane = 4 columns
     {
         const int d = lane * 4, r0 = 4 * w;
         float4 wa[4], ua[4];
@@ -222,12 +298,12 @@ __global__ void __launch_bounds__(kPrepThreads) cb_prep(const CbArgs a)
         for (int i = 0; i < 4; ++i) wa[i] = ua[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int m = 0; m <= r0 + 3; ++m) {   // T is lower triangular
             const float4 k4 = ld4(Ks + m * kS + d), v4 = ld4(Vs + m * kS + d);
-            const float bm = be[m];
+            const float bm = be[m], bg = kG ? bm * Gm[m] : bm;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float tb = Ts[(r0 + i) * kL + m] * bm;
-                wa[i] = axpy4(tb, k4, wa[i]);
-                ua[i] = axpy4(tb, v4, ua[i]);
+                const float t = Ts[(r0 + i) * kL + m];
+                wa[i] = axpy4(t * bg, k4, wa[i]);
+                ua[i] = axpy4(t * bm, v4, ua[i]);
             }
         }
 #pragma unroll
@@ -253,15 +329,17 @@ constexpr int kChainThreads = 256;
 constexpr int kCols = 64;          // value columns per chain CTA
 constexpr int kSS = kCols + 4;     // row stride of the state and U' tiles
 
-struct FwdStage {   // one chunk's operands of the forward chain (fp32)
+struct FwdStage {   // one chunk's operands of the forward chain (fp32; Gamma for gated problems)
     static constexpr size_t kW = (size_t)kC * kD * 4, kK = (size_t)kC * kD * 4, kU = (size_t)kC * kCols * 4;
-    static constexpr size_t kBytes = kW + kK + kU;
+    static constexpr size_t kG = (size_t)kC * 4;
+    static constexpr size_t kBytes = kW + kK + kU + kG;
 };
 template <typename TDo>
 struct BwdStage {   // ... and of the reverse chain
     static constexpr size_t kW = (size_t)kC * kD * 4, kK = (size_t)kC * kD * 4, kQb = (size_t)kQ * kD * 4;
     static constexpr size_t kO = (size_t)kQ * kCols * sizeof(TDo), kP = (size_t)kQ * kC * 4;
-    static constexpr size_t kBytes = kW + kK + kQb + kO + kP;
+    static constexpr size_t kG = (size_t)kC * 4;
+    static constexpr size_t kBytes = kW + kK + kQb + kO + kP + kG;
 };
 // state tile [128][kSS], U' tile [32][kSS], partial sums [128 threads][16]
 constexpr size_t kChainShared = (size_t)(kD + kC) * kSS * 4 + (size_t)128 * 16 * 4;
@@ -385,6 +463,7 @@ __device__ __forceinline__ void update_state(float (*S)[4], const float *X, cons
     }
 }
 
+template <bool kGt>
 __device__ __forceinline__ void fwd_chain(const CbArgs &a, char *smem)
 {
     using St = FwdStage;
@@ -395,7 +474,8 @@ __device__ __forceinline__ void fwd_chain(const CbArgs &a, char *smem)
         char *base = smem + (c & 1) * St::kBytes;
         const float *rec = a.rec + ((size_t)bh * a.nc + c) * kRecFloats;
         copy_floats(rec + kRecW, (float *)base, kC * kD);
-        copy_floats(rec + kRecK, (float *)(base + St::kW), kC * kD);
+        copy_floats(rec + (kGt ? kRecKd : kRecK), (float *)(base + St::kW), kC * kD);
+        if (kGt) copy_floats(rec + kRecGm, (float *)(base + St::kW + St::kK + St::kU), kC);
         float *Ud = (float *)(base + St::kW + St::kK);
         for (int i = threadIdx.x; i < kC * kCols / 4; i += kChainThreads) {
             const int r = i / (kCols / 4), e = (i % (kCols / 4)) * 4;
@@ -433,11 +513,18 @@ __device__ __forceinline__ void fwd_chain(const CbArgs &a, char *smem)
             }
         }
         __syncthreads();
+        if (kGt) {   // S <- Gamma_C S + Kd^T U'
+            const float gc = ((const float *)(base + St::kW + St::kK + St::kU))[kC - 1];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) S[i][j] *= gc;
+        }
         update_state<kC>(S, Kc, Usm, L, 1.f);   // S += K^T U'
     }
 }
 
-template <typename TDo>
+template <typename TDo, bool kGt>
 __device__ __forceinline__ void bwd_chain(const CbArgs &a, char *smem)
 {
     using St = BwdStage<TDo>;
@@ -448,8 +535,9 @@ __device__ __forceinline__ void bwd_chain(const CbArgs &a, char *smem)
         char *base = smem + (c & 1) * St::kBytes;
         const float *rec = a.rec + ((size_t)bh * a.nc + c) * kRecFloats;
         copy_floats(rec + kRecW, (float *)base, kC * kD);
-        copy_floats(rec + kRecK, (float *)(base + St::kW), kC * kD);
+        copy_floats(rec + (kGt ? kRecKd : kRecK), (float *)(base + St::kW), kC * kD);
         copy_floats(rec + kRecQ, (float *)(base + St::kW + St::kK), kQ * kD);
+        if (kGt) copy_floats(rec + kRecGm, (float *)(base + St::kW + St::kK + St::kQb + St::kO + St::kP), kC);
         copy_do_rows<TDo>(a, chunk_rows(a, bh, c), (const TDo *)a.d_o, cg,
                           (TDo *)(base + St::kW + St::kK + St::kQb));
         copy_floats(rec + kRecP, (float *)(base + St::kW + St::kK + St::kQb + St::kO), kQ * kC);
@@ -500,13 +588,26 @@ __device__ __forceinline__ void bwd_chain(const CbArgs &a, char *smem)
             }
         }
         __syncthreads();
-        // dS0 = dS1 + Q^T dO - W^T dU'
+        // dS0 = Gamma_C dS1 + Q^T diag(Gamma_last(t)) dO - W^T dU'
+        const float *Gc = (const float *)(base + St::kW + St::kK + St::kQb + St::kO + St::kP);
+        if (kGt) {
+            const float gc = Gc[kC - 1];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) dS[i][j] *= gc;
+        }
 #pragma unroll 4
         for (int t = 0; t < kQ; ++t) {
             const float4 x0 = ld4(Qc + t * kD + L.sr0), x1 = ld4(Qc + t * kD + L.sr0 + 4);
             const float4 o = ld4o(Oc + t * kCols + L.sc0);
             const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            const float ov[4] = {o.x, o.y, o.z, o.w};
+            float gq = 1.f;
+            if (kGt) {
+                const int last = t * a.nh + a.nh - 1;
+                gq = last < kC ? Gc[last] : 0.f;
+            }
+            const float ov[4] = {gq * o.x, gq * o.y, gq * o.z, gq * o.w};
 #pragma unroll
             for (int i = 0; i < 8; ++i)
 #pragma unroll
@@ -522,12 +623,12 @@ __device__ __forceinline__ void bwd_chain(const CbArgs &a, char *smem)
     }
 }
 
-template <typename TDo>
+template <typename TDo, bool kGt>
 __global__ void __launch_bounds__(kChainThreads, 1) cb_chains(const CbArgs a)
 {
     extern __shared__ float4 sm_chain[];
-    if (blockIdx.z == 0) fwd_chain(a, (char *)sm_chain);
-    else bwd_chain<TDo>(a, (char *)sm_chain);
+    if (blockIdx.z == 0) fwd_chain<kGt>(a, (char *)sm_chain);
+    else bwd_chain<TDo, kGt>(a, (char *)sm_chain);
 }
 
 // ------------------------------------------------------------------ 3. per-chunk gradients
@@ -547,10 +648,11 @@ __device__ __forceinline__ float quad_sum(float x)
 constexpr int kGradSThreads = 256;
 constexpr int kGradSSmemFloats = (kQ + 2 * kC) * kS;
 
-template <typename TDo>
+template <typename TDo, bool kG>
 __global__ void __launch_bounds__(kGradSThreads, 2) cb_grad_s(const CbArgs a)
 {
     extern __shared__ float4 sm_grad_s[];
+    __shared__ float wsum[kGradSThreads / 32];
     float *dOs = (float *)sm_grad_s, *Ups = dOs + kQ * kS, *dUps = Ups + kC * kS;
     const int ci = blockIdx.x, bh = ci / a.nc, c = ci - bh * a.nc;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, kk = tid >> 2, qq = tid & 3;
@@ -617,8 +719,28 @@ __global__ void __launch_bounds__(kGradSThreads, 2) cb_grad_s(const CbArgs a)
             rec[kRecW + r * kD + kk + 64] = -v1;
         }
     }
-    // dk <- U' dS1^T
-    load_rows(a.dS1);
+    // dk <- U' dS1^T (gated: the decayed keys' gradient, and <dS1, S0> into aux)
+    if (kG) {
+        const float *p0 = a.dS1 + (size_t)ci * kStateFloats + kk * kD + 4 * qq, *p1 = p0 + 64 * kD;
+        float part = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 x = __ldg((const float4 *)(p0 + 16 * i)), y = __ldg((const float4 *)(p1 + 16 * i));
+            part = dot4(x, sa[i], dot4(y, sb[i], part));
+            sa[i] = x, sb[i] = y;
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (lane == 0) wsum[w] = part;
+        __syncthreads();
+        if (tid == 0) {
+            float tot = 0.f;
+            for (int i = 0; i < kGradSThreads / 32; ++i) tot += wsum[i];
+            rec[kRecAux] = tot;
+        }
+    } else {
+        load_rows(a.dS1);
+    }
 #pragma unroll 2
     for (int r = 0; r < kC; ++r) {
         float v0, v1;
@@ -635,16 +757,19 @@ __global__ void __launch_bounds__(kGradSThreads, 2) cb_grad_s(const CbArgs a)
 // 136 floats: in the dT product a quarter-warp reads rows m, m + 2 of them
 // at four interleaved column chunks, which then fall in distinct banks.
 constexpr int kSR = kD + 8;
-constexpr int kGradRSmemFloats = 2 * kC * kSR + 2 * kC * kS + kQ * kS + 4 * kC * kL + kQ * kL + kC;
+constexpr int kGradRSmemFloats =
+    2 * kC * kSR + 2 * kC * kS + kQ * kS + 5 * kC * kL + 2 * kQ * kL + 6 * kC + kQ;
 
-template <typename TIn>
+template <typename TIn, bool kG>
 __global__ void __launch_bounds__(kGradThreads, 2) cb_grad_r(const CbArgs a)
 {
     extern __shared__ float4 sm_grad_r[];
     float *Ks = (float *)sm_grad_r, *Vs = Ks + kC * kSR, *dUps = Vs + kC * kSR, *dWs = dUps + kC * kS;
     float *Qs = dWs + kC * kS;
-    float *Ts = Qs + kQ * kS, *KKs = Ts + kC * kL, *dTs = KKs + kC * kL, *Xs = dTs + kC * kL;
-    float *dPs = Xs + kC * kL, *be = dPs + kQ * kL;
+    float *Ts = Qs + kQ * kS, *KKs = Ts + kC * kL, *dTs = KKs + kC * kL, *Xs = dTs + kC * kL, *Es = Xs + kC * kL;
+    float *dPs = Es + kC * kL, *dEq = dPs + kQ * kL;
+    float *be = dEq + kQ * kL, *Gm = be + kC, *Rt = Gm + kC, *lg = Rt + kC, *dGm = lg + kC, *dRt = dGm + kC;
+    float *dGq = dRt + kC;
     const int ci = blockIdx.x, bh = ci / a.nc, c = ci - bh * a.nc;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const ChunkRows cr = chunk_rows(a, bh, c);
@@ -660,35 +785,69 @@ __global__ void __launch_bounds__(kGradThreads, 2) cb_grad_r(const CbArgs a)
     stage_f32<true, kC, TIn, kSR>(a, cr, (const TIn *)a.v, Vs);
     stage_betas<TIn>(a, cr, be);
     for (int i = tid; i < kC * kC; i += kGradThreads) {
-        Ts[(i >> 5) * kL + (i & 31)] = rec[kRecT + i];
-        KKs[(i >> 5) * kL + (i & 31)] = rec[kRecKK + i];
-        if (i < kQ * kC) dPs[(i >> 5) * kL + (i & 31)] = rec[kRecP + i];
+        const int r = i >> 5, s2 = i & 31;
+        Ts[r * kL + s2] = rec[kRecT + i];
+        KKs[r * kL + s2] = rec[kRecKK + i];
+        if (kG) Es[r * kL + s2] = rec[kRecE + i];
+        if (i < kQ * kC) {
+            // dP of the decayed scores P o Eq, and (gated) the gradient of Eq
+            const float dpe = rec[kRecP + i];
+            if (kG) {
+                const int last = r * a.nh + a.nh - 1;
+                dPs[r * kL + s2] = last < kC ? dpe * rec[kRecE + last * kC + s2] : 0.f;
+                dEq[r * kL + s2] = dpe * rec[kRecPr + i];
+            } else {
+                dPs[r * kL + s2] = dpe;
+            }
+        }
+    }
+    if (kG && tid < kC) {
+        Gm[tid] = rec[kRecGm + tid], Rt[tid] = rec[kRecRt + tid], lg[tid] = rec[kRecLg + tid];
+        dGm[tid] = 0.f, dRt[tid] = 0.f;
+        if (tid < kQ) dGq[tid] = 0.f;
     }
     __syncthreads();
 
-    // dq += dP K (row t = w, columns 4 lane .. 4 lane + 3)
+    // dq = Gamma_last(t) dQ0 + dP K (row t = w, columns 4 lane .. 4 lane + 3);
+    // gated: dGq_t = q_t . dQ0_t
     {
         const int d = 4 * lane;
-        if (w < cr.nt) {
+        if (w < cr.nt) {   // warp-uniform
             float *dq = a.dq + token_row(a, cr, w) * kD + d;
-            float4 acc = ld4(dq);
+            const float4 q0 = ld4(dq);
+            float4 acc = q0;
+            if (kG) {
+                const int last = w * a.nh + a.nh - 1;
+                const float gq = Gm[last];
+                acc = make_float4(gq * q0.x, gq * q0.y, gq * q0.z, gq * q0.w);
+                float pg = dot4(ld4(Qs + w * kS + d), q0, 0.f);
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) pg += __shfl_xor_sync(0xffffffffu, pg, o);
+                if (lane == 0) dGq[w] = pg;
+            }
 #pragma unroll 8
-            for (int s = 0; s < kC; ++s) acc = axpy4(dPs[w * kL + s], ld4(Ks + s * kSR + d), acc);
+            for (int s2 = 0; s2 < kC; ++s2) acc = axpy4(dPs[w * kL + s2], ld4(Ks + s2 * kSR + d), acc);
             st4(dq, acc);
         }
     }
-    // dT = (dW K^T + dU' V^T) B. Thread: columns m = 2 mp, 2 mp + 1, rows
-    // 4 rq .. 4 rq + 3, float4 column chunks j = dq (mod 4) of the 128-term
-    // contraction; the four quarters meet by quad shuffles.
+    // dT = dW (diag(beta Gamma) K)^T + dU' (diag(beta) V)^T. Thread: columns
+    // m = 2 mp, 2 mp + 1, rows 4 rq .. 4 rq + 3, float4 column chunks
+    // j = dq (mod 4) of the 128-term contraction; the four quarters meet by
+    // quad shuffles.
     {
         const int dq = tid & 3, mp = (tid >> 2) & 15, rq = tid >> 6;
+        const float g0 = kG ? Gm[2 * mp] : 1.f, g1 = kG ? Gm[2 * mp + 1] : 1.f;
         float t[4][2];
 #pragma unroll
         for (int i = 0; i < 4; ++i) t[i][0] = t[i][1] = 0.f;
 #pragma unroll 2
         for (int jj = 0; jj < 8; ++jj) {
             const int d = 4 * (4 * jj + dq);
-            const float4 k0 = ld4(Ks + (2 * mp) * kSR + d), k1 = ld4(Ks + (2 * mp + 1) * kSR + d);
+            float4 k0 = ld4(Ks + (2 * mp) * kSR + d), k1 = ld4(Ks + (2 * mp + 1) * kSR + d);
+            if (kG) {   // the W term's keys carry Gamma_m
+                k0 = make_float4(g0 * k0.x, g0 * k0.y, g0 * k0.z, g0 * k0.w);
+                k1 = make_float4(g1 * k1.x, g1 * k1.y, g1 * k1.z, g1 * k1.w);
+            }
             const float4 v0 = ld4(Vs + (2 * mp) * kSR + d), v1 = ld4(Vs + (2 * mp + 1) * kSR + d);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -733,16 +892,34 @@ __global__ void __launch_bounds__(kGradThreads, 2) cb_grad_r(const CbArgs a)
         dTs[r * kL + lane] = lane < r ? g : 0.f;
     }
     __syncthreads();
+    if (kG) {
+        // dG o E into dT's tile; into X's tile the coefficient of E[r][s]
+        // (s < r): beta_r dG[r][s] (K K^T)[r][s], plus dEq[t][s] on the row
+        // r = last(t) of token t
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int r = 2 * w + i, s2 = lane;
+            const float g = dTs[r * kL + s2];
+            float x = be[r] * g * KKs[r * kL + s2];
+            const int t = r / a.nh;
+            if (r - t * a.nh == a.nh - 1 && t < kQ && s2 < r) x += dEq[t * kL + s2];
+            Xs[r * kL + s2] = s2 < r ? x : 0.f;
+            dTs[r * kL + s2] = g * Es[r * kL + s2];
+        }
+        __syncthreads();
+    }
     // rows m0 = 2w, m1 = 2w + 1 together (every loaded row feeds both),
     // columns 4 lane .. 4 lane + 3:
-    //   dk += dP^T Q + B (T^T dW + dG K) + (B dG)^T K,  dv = B T^T dU'
-    //   dbeta = sum over columns of K o T^T dW + V o T^T dU', + sum_s dG o K K^T
-    // (T and dG are lower triangular, so the joint ranges add only zeros)
+    //   dk = ratio dKd + dP^T Q + diag(beta Gamma) T^T dW + B (dG o E) K + (B (dG o E))^T K
+    //   dv = B T^T dU'
+    //   dbeta = Gamma (K o T^T dW) + V o T^T dU' + (dG o E o K K^T), each summed over a row
+    // (T and dG are lower triangular, so the joint ranges add only zeros;
+    // ungated: Gamma = ratio = E = 1)
     const int m0 = 2 * w, m1 = m0 + 1;
     if (m0 < cr.R) {   // warp-uniform
         const int d = 4 * lane;
         const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-        // gt: (B dG)^T K + dP^T Q, the terms of dk outside B (...)
+        // gt: (B dG)^T K + dP^T Q, the terms of dk outside the beta Gamma (...) group
         float4 tw0 = z, tw1 = z, tu0 = z, tu1 = z, gk0 = z, gk1 = z, gt0 = z, gt1 = z;
         for (int r = m0; r < kC; ++r) {
             const float4 x = ld4(dWs + r * kS + d), y = ld4(dUps + r * kS + d);
@@ -767,57 +944,113 @@ __global__ void __launch_bounds__(kGradThreads, 2) cb_grad_r(const CbArgs a)
         for (int i = 0; i < 2; ++i) {
             const int m = m0 + i;
             const float4 tw = i ? tw1 : tw0, tu = i ? tu1 : tu0, gk = i ? gk1 : gk0, gt = i ? gt1 : gt0;
-            const float bm = be[m];
-            float db = dot4(ld4(Ks + m * kSR + d), tw, dot4(ld4(Vs + m * kSR + d), tu, 0.f));
-            if (lane < m) db = fmaf(dTs[m * kL + lane], KKs[m * kL + lane], db);
+            const float bm = be[m], gm = kG ? Gm[m] : 1.f, rt = kG ? Rt[m] : 1.f;
+            const size_t row = key_row(a, cr, m < cr.R ? m : 0);
+            float *dkp = a.dk + row * kD + d;
+            const float4 km = ld4(Ks + m * kSR + d);
+            const float4 k0 = m < cr.R ? ld4(dkp) : z;   // dKd (gated) or U' dS1^T
+            // ungated: rest carries the whole dbeta (gm = 1, dbg unused)
+            float dbg = kG ? dot4(km, tw, 0.f) : 0.f;
+            float rest = dot4(ld4(Vs + m * kSR + d), tu, kG ? 0.f : dot4(km, tw, 0.f));
+            if (lane < m) rest = fmaf(dTs[m * kL + lane], KKs[m * kL + lane], rest);
+            float drt = kG ? dot4(km, k0, 0.f) : 0.f;
 #pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) db += __shfl_xor_sync(0xffffffffu, db, o);
-            if (m < cr.R) {
-                const size_t row = key_row(a, cr, m);
-                float *dkp = a.dk + row * kD + d;
-                const float4 k0 = ld4(dkp);
-                st4(dkp, make_float4(k0.x + bm * (tw.x + gk.x) + gt.x, k0.y + bm * (tw.y + gk.y) + gt.y,
-                                     k0.z + bm * (tw.z + gk.z) + gt.z, k0.w + bm * (tw.w + gk.w) + gt.w));
-                st4(a.dv + row * kD + d, make_float4(bm * tu.x, bm * tu.y, bm * tu.z, bm * tu.w));
-                if (lane == 0) a.dbeta[row] = db;
+            for (int o = 16; o >= 1; o >>= 1) {
+                rest += __shfl_xor_sync(0xffffffffu, rest, o);
+                if (kG) {
+                    dbg += __shfl_xor_sync(0xffffffffu, dbg, o);
+                    drt += __shfl_xor_sync(0xffffffffu, drt, o);
+                }
             }
+            if (m < cr.R) {
+                const float bg = bm * gm;
+                st4(dkp, make_float4(rt * k0.x + bg * tw.x + bm * gk.x + gt.x, rt * k0.y + bg * tw.y + bm * gk.y + gt.y,
+                                     rt * k0.z + bg * tw.z + bm * gk.z + gt.z, rt * k0.w + bg * tw.w + bm * gk.w + gt.w));
+                st4(a.dv + row * kD + d, make_float4(bm * tu.x, bm * tu.y, bm * tu.z, bm * tu.w));
+                if (lane == 0) {
+                    a.dbeta[row] = fmaf(dbg, gm, rest);
+                    if (kG) dGm[m] = dbg * bm, dRt[m] = drt;
+                }
+            }
+        }
+    }
+    if (!kG) return;
+    __syncthreads();
+    // dg of token gi (warp gi, lane = row r; the gate sits on row r' = gi n_h):
+    // the sum over every decay factor that contains gamma_r' of its
+    // coefficient times the factor without gamma_r' (an exp of a range sum
+    // that skips r'), so no division by the gate.
+    const int gi = w, rp = gi * a.nh;
+    if (rp < cr.R) {   // warp-uniform
+        const int r = lane;
+        float term = 0.f;
+        if (r >= rp) {
+            const int t = r / a.nh;
+            const float cg = dGm[r] + ((r - t * a.nh == a.nh - 1 && t < kQ) ? dGq[t] : 0.f);
+            float sg = 0.f;   // sum_{x <= r, x != r'} lg
+            for (int x = 0; x <= r; ++x) sg += x == rp ? 0.f : lg[x];
+            term = cg * expf(sg);
+            float acc = 0.f;  // sum_{s < x <= r, x != r'} lg, s from r' - 1 down
+            for (int x = rp + 1; x <= r; ++x) acc += lg[x];
+            for (int s2 = rp - 1; s2 >= 0; --s2) {
+                term = fmaf(Xs[r * kL + s2], expf(acc), term);
+                acc += lg[s2];
+            }
+        } else {
+            float sr = 0.f;   // sum_{r < x < 32, x != r'} lg
+            for (int x = r + 1; x < kC; ++x) sr += x == rp ? 0.f : lg[x];
+            term = dRt[r] * expf(sr);
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
+        if (lane == 0) {
+            float sc = 0.f;   // sum_{x < 32, x != r'} lg
+            for (int x = 0; x < kC; ++x) sc += x == rp ? 0.f : lg[x];
+            a.dg[token_row(a, cr, gi)] = fmaf(rec[kRecAux], expf(sc), term);
         }
     }
 }
 
-template <typename TIn, typename TDo>
+template <typename TIn, typename TDo, bool kG>
 cudaError_t launch_typed(const BwdProblem &p, const CbArgs &a)
 {
     const size_t n_chunks = (size_t)p.B * p.H * a.nc;
     cudaError_t e;
     const int chain_smem = (int)chain_smem_bytes<TDo>();
-    if ((e = cudaFuncSetAttribute(cb_chains<TDo>, cudaFuncAttributeMaxDynamicSharedMemorySize, chain_smem)) !=
+    if ((e = cudaFuncSetAttribute(cb_chains<TDo, kG>, cudaFuncAttributeMaxDynamicSharedMemorySize, chain_smem)) !=
         cudaSuccess)
         return e;
     const dim3 chain_grid(p.B * p.H, kD / kCols, 2);
     if (n_chunks == 0) {   // T = 0: dh0 = dh_final (the reverse chains only)
-        cb_chains<TDo><<<chain_grid, kChainThreads, chain_smem, p.stream>>>(a);
+        cb_chains<TDo, kG><<<chain_grid, kChainThreads, chain_smem, p.stream>>>(a);
         return cudaGetLastError();
     }
     const int prep_smem = (int)(kPrepSmemFloats * sizeof(float));
-    if ((e = cudaFuncSetAttribute(cb_prep<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem)) != cudaSuccess)
+    if ((e = cudaFuncSetAttribute(cb_prep<TIn, kG>, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem)) !=
+        cudaSuccess)
         return e;
-    cb_prep<TIn><<<(unsigned)n_chunks, kPrepThreads, prep_smem, p.stream>>>(a);
+    cb_prep<TIn, kG><<<(unsigned)n_chunks, kPrepThreads, prep_smem, p.stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    cb_chains<TDo><<<chain_grid, kChainThreads, chain_smem, p.stream>>>(a);
+    cb_chains<TDo, kG><<<chain_grid, kChainThreads, chain_smem, p.stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int gs_smem = (int)(kGradSSmemFloats * sizeof(float));
-    if ((e = cudaFuncSetAttribute(cb_grad_s<TDo>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs_smem)) !=
+    if ((e = cudaFuncSetAttribute(cb_grad_s<TDo, kG>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs_smem)) !=
         cudaSuccess)
         return e;
-    cb_grad_s<TDo><<<(unsigned)n_chunks, kGradSThreads, gs_smem, p.stream>>>(a);
+    cb_grad_s<TDo, kG><<<(unsigned)n_chunks, kGradSThreads, gs_smem, p.stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int gr_smem = (int)(kGradRSmemFloats * sizeof(float));
-    if ((e = cudaFuncSetAttribute(cb_grad_r<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, gr_smem)) !=
+    if ((e = cudaFuncSetAttribute(cb_grad_r<TIn, kG>, cudaFuncAttributeMaxDynamicSharedMemorySize, gr_smem)) !=
         cudaSuccess)
         return e;
-    cb_grad_r<TIn><<<(unsigned)n_chunks, kGradThreads, gr_smem, p.stream>>>(a);
+    cb_grad_r<TIn, kG><<<(unsigned)n_chunks, kGradThreads, gr_smem, p.stream>>>(a);
     return cudaGetLastError();
+}
+
+template <typename TIn, typename TDo>
+cudaError_t launch_gated_or_not(const BwdProblem &p, const CbArgs &a)
+{
+    return p.g ? launch_typed<TIn, TDo, true>(p, a) : launch_typed<TIn, TDo, false>(p, a);
 }
 
 int chunk_tokens(int nh) { return (kC / nh < kQ) ? kC / nh : kQ; }
@@ -829,7 +1062,7 @@ bool backward_chunk_shape_ok(const BwdProblem &p)
     return p.cu == nullptr && p.Dk == kD && p.Dv == kD && p.nh >= 1 && p.nh <= kC;
 }
 
-bool backward_chunk_supported(const BwdProblem &p) { return p.g == nullptr && backward_chunk_shape_ok(p); }
+bool backward_chunk_supported(const BwdProblem &p) { return backward_chunk_shape_ok(p); }
 
 size_t backward_chunk_scratch_bytes(const BwdProblem &p)
 {
@@ -854,9 +1087,10 @@ cudaError_t launch_backward_chunk(const BwdProblem &p)
     a.dS1 = a.S0 + n * kStateFloats;
     a.Up = a.dS1 + n * kStateFloats;
     a.dUp = a.Up + n * kRowsFloats;
-    if (p.dtype == DP_F32) return launch_typed<float, float>(p, a);
-    return p.do_dtype == DP_F32 ? launch_typed<__nv_bfloat16, float>(p, a)
-                                : launch_typed<__nv_bfloat16, __nv_bfloat16>(p, a);
+    a.g = p.g; a.dg = p.dg; a.status = p.status;
+    if (p.dtype == DP_F32) return launch_gated_or_not<float, float>(p, a);
+    return p.do_dtype == DP_F32 ? launch_gated_or_not<__nv_bfloat16, float>(p, a)
+                                : launch_gated_or_not<__nv_bfloat16, __nv_bfloat16>(p, a);
 }
 
 }  // namespace dp

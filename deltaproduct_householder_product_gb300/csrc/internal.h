@@ -69,7 +69,7 @@ cudaError_t launch_backward(const BwdProblem &p);
 // Chunked backward (ungated, dense, D_k = D_v = 128): per-chunk records and
 // the chunk-boundary states and gradients in the scratch area.
 bool backward_chunk_shape_ok(const BwdProblem &p);   // dims only (g not known)
-bool backward_chunk_supported(const BwdProblem &p);  // dims and g == NULL
+bool backward_chunk_supported(const BwdProblem &p);  // gated or not (AUTO takes it ungated only)
 size_t backward_chunk_scratch_bytes(const BwdProblem &p);
 cudaError_t launch_backward_chunk(const BwdProblem &p);
 

@@ -145,13 +145,17 @@ def test_backward_workspace_and_validation(L):
                                         C.byref(m)) == 1
     # D_k = D_v = 128: the chunked form's records (ct = 16 tokens per chunk at
     # n_h = 2; per chunk W, U [32,128], T [32,32], P [16,32], K K^T [32,32],
-    # K [32,128], Q [16,128], the state at its start and the gradient at its
-    # end [128,128], U' and dU' [32,128], fp32)
+    # K [32,128], Q [16,128], for gated problems the decayed keys [32,128],
+    # the undecayed scores [16,32], the decays [32,32], three [32] vectors
+    # (Gamma, Gamma_C / Gamma, log gates) and <dS1, S0> in 4 floats, the state
+    # at its start and the gradient at its end [128,128], U' and dU'
+    # [32,128], fp32)
     rec = lambda impl: _lib.make_dims(2, 100, 3, 128, 128, 2, _lib.DP_BF16, impl, _lib.DP_F32)
     ck128 = 2 * 3 * ((100 + seg - 1) // seg) * 128 * 128 * 4
     need_rec = 256 + r256(r256(ck128) + 2 * 100 * 3 * 2 * 128 * 4)
     chunks = 2 * 3 * ((100 + 15) // 16)
-    need_chunk = 256 + r256(chunks * (2 * 32 * 128 + 32 * 32 + 16 * 32 + 32 * 32 + 32 * 128 + 16 * 128 + 2 * 128 * 128 + 2 * 32 * 128) * 4)
+    need_chunk = 256 + r256(chunks * (2 * 32 * 128 + 32 * 32 + 16 * 32 + 32 * 32 + 32 * 128 + 16 * 128 + 32 * 128 + 16 * 32 + 32 * 32 + 3 * 32 + 4
+                                + 2 * 128 * 128 + 2 * 32 * 128) * 4)
     for impl, want in (("recurrent", need_rec), ("chunk_tc", need_chunk), ("auto", max(need_rec, need_chunk))):
         assert L.dp_backward_workspace_size(C.byref(rec(impl)), C.byref(m)) == 0 and m.value == want, impl
     # packed sequences take the recurrent form only

@@ -265,10 +265,81 @@ def test_backward_chunked_bf16_cotangent_and_empty(dp):
 
 
 def test_backward_chunked_unsupported(dp):
-    """The chunked form takes ungated dense problems with D = 128 only."""
-    w = W.GATED.scaled(B=1, H=1, T=8, nh=2)
+    """The chunked form takes dense problems with D = 128 only."""
+    w = W.TINY.scaled(B=1, H=1, T=8, nh=2, Dk=64, Dv=64)
     x = {k: (None if v is None else v.cuda()) for k, v in W.make_inputs(w).items()}
     with pytest.raises(dp.DPError) as e:
-        dp.backward(x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"], d_o=torch.zeros(1, 8, 1, 128, device="cuda"),
+        dp.backward(x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"], d_o=torch.zeros(1, 8, 1, 64, device="cuda"),
                     impl="chunk_tc")
     assert e.value.code == 2
+
+
+# Gated, D = 128, chunked form (impl="chunk_tc"; "auto" keeps the recurrent
+# form for gated problems): every gradient including dg against the oracle.
+GATED_CHUNK_CASES = [
+    ("nh1", W.GATED.scaled(B=1, H=2, T=40, nh=1), 40),
+    ("nh2", W.GATED.scaled(B=2, H=1, T=37, nh=2), 41),
+    ("nh3", W.GATED.scaled(B=1, H=2, T=31, nh=3), 42),
+    ("nh4", W.GATED.scaled(B=1, H=2, T=27, nh=4), 43),
+    ("f32-nh2", W.GATED.scaled(B=1, H=1, T=20, nh=2, dtype="f32"), 44),
+    ("one-token", W.GATED.scaled(B=2, H=1, T=1, nh=2), 45),
+]
+
+
+@pytest.mark.parametrize("name,w,seed", GATED_CHUNK_CASES, ids=[c[0] for c in GATED_CHUNK_CASES])
+def test_backward_gated_chunked(dp, name, w, seed):
+    d_o, dhf = cotangents(w, 300 + seed)
+    got, ref, _ = run_both(dp, w, d_o, dhf, impl="chunk_tc")
+    stats = check(got, ref, f"gated chunked {name}")
+    print("gated chunked", name, {n: round(s["rel_max"], 8) for n, s in stats.items()})
+
+
+def test_backward_gated_chunked_zero_and_small_gates(dp):
+    """Gates of exactly 0 (a reset inside a chunk) and tiny gates: the
+    chunked form takes every decay and the gate gradient as range sums of
+    log gates that skip the gate itself (no division by it), so dg stays the
+    oracle's exact derivative."""
+    w = W.GATED.scaled(B=1, H=2, T=45, nh=2)
+    x = W.make_inputs(w)
+    g = x["g"].float().clone()
+    g[0, 5, 0] = 0.0
+    g[0, 20, 1] = 0.0
+    g[0, 21, 1] = 1e-6
+    g[0, 33, 0] = 1e-3
+    x["g"] = g.to(x["g"].dtype)
+    d_o, dhf = cotangents(w, 350)
+    xc = {k: (None if v is None else v.cuda()) for k, v in x.items()}
+    got = dp.backward(xc["q"], xc["k"], xc["v"], xc["beta"], xc["g"], xc["h0"], d_o=d_o.cuda(), dh_final=dhf.cuda(),
+                      impl="chunk_tc")
+    ref = oracle.backward(x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"], d_o, dhf)
+    check(got, ref, "zero and small gates")
+
+
+def test_backward_gated_chunked_negative_gate_reported(dp):
+    w = W.GATED.scaled(B=1, H=1, T=20, nh=2)
+    x = W.make_inputs(w)
+    g = x["g"].float().clone()
+    g[0, 7, 0] = -0.5
+    x["g"] = g.to(x["g"].dtype)
+    xc = {k: (None if v is None else v.cuda()) for k, v in x.items()}
+    dims = dp._lib.make_dims(1, 20, 1, 128, 128, 2, xc["q"].dtype, "chunk_tc", torch.float32)
+    ws = torch.zeros(dp._lib.backward_workspace_size(dims), dtype=torch.uint8, device="cuda")
+    dp.backward(xc["q"], xc["k"], xc["v"], xc["beta"], xc["g"], xc["h0"], d_o=torch.zeros(1, 20, 1, 128, device="cuda"),
+                impl="chunk_tc", workspace=ws)
+    with pytest.raises(dp.DPError) as e:
+        dp.check_status(ws)
+    assert e.value.code == 7
+
+
+def test_backward_auto_keeps_recurrent_for_gated(dp):
+    """AUTO on a gated problem runs the recurrent form: its gradients equal
+    impl="recurrent"'s bit for bit up to the atomics' order (compared at
+    1e-6 of RMS), and differ from the chunked form's rounding."""
+    w = W.GATED.scaled(B=1, H=2, T=30, nh=2)
+    d_o, dhf = cotangents(w, 360)
+    got_auto, ref, _ = run_both(dp, w, d_o, dhf, impl="auto")
+    got_rec, _, _ = run_both(dp, w, d_o, dhf, impl="recurrent")
+    for n in NAMES:
+        if ref[n] is not None:
+            s = err_stats(got_auto[n], got_rec[n].cpu().double().numpy())
+            assert s["rel_max"] <= 1e-6, (n, s)
