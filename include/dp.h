@@ -197,8 +197,11 @@ dp_status dp_state_io(int op, int B, int H, int Dk, int Dv, float *state,
  *   DP_IMPL_RECURRENT  the recurrent form (any shape, gated or not);
  *   DP_IMPL_CHUNK_TC   the chunked form (WY representation of each chunk of
  *                      tokens, OSDN paper App.A.2, differentiated per chunk;
- *                      fp32 on CUDA cores), DP_ERR_UNSUPPORTED when g != NULL
- *                      or D_k, D_v != 128.
+ *                      fp32 on CUDA cores), gated or not; DP_ERR_UNSUPPORTED
+ *                      when D_k, D_v != 128. Gated: gates g >= 0 (a gate
+ *                      below 1.8e-35, zero included, is taken as 1.8e-35, as
+ *                      the forward's chunk path does); a negative or NaN
+ *                      gate records DP_ERR_DEVICE (dp_check_status).
  *   d_o      [B,T,H,D_v] gradient of the outputs;
  *   dh_final [B,H,D_k,D_v] fp32 gradient of the final state, NULL = zeros;
  * outputs, fp32, written in full:
