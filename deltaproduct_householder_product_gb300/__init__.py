@@ -157,9 +157,10 @@ def backward(q, k, v, beta, g=None, h0=None, *, d_o, dh_final=None, want_dh0=Tru
 
 
 def backward_varlen(q, k, v, beta, g=None, h0=None, *, cu_seqlens, max_seqlen=None, d_o, dh_final=None,
-                    want_dh0=True, workspace=None, stream=None):
+                    want_dh0=True, workspace=None, stream=None, impl="auto"):
     """``backward`` over packed variable-length sequences (the layouts of
-    ``forward_varlen``; dh_final and dh0 are [N,H,Dk,Dv])."""
+    ``forward_varlen``; dh_final and dh0 are [N,H,Dk,Dv]); ``impl`` as for
+    ``backward``."""
     T, H, nh, Dk = k.shape
     Dv = v.shape[-1]
     N = cu_seqlens.numel() - 1
@@ -172,7 +173,7 @@ def backward_varlen(q, k, v, beta, g=None, h0=None, *, cu_seqlens, max_seqlen=No
     _lib._need_cuda("dh_final", dh_final, torch.float32)
     if max_seqlen is None:
         max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if N > 0 else 0
-    dims = _lib.make_dims(N, T, H, Dk, Dv, nh, dt, "auto", d_o.dtype, max(int(max_seqlen), 1 if T > 0 else 0))
+    dims = _lib.make_dims(N, T, H, Dk, Dv, nh, dt, impl, d_o.dtype, max(int(max_seqlen), 1 if T > 0 else 0))
     f32 = dict(dtype=torch.float32, device=q.device)
     out = {"dq": torch.empty((T, H, Dk), **f32), "dk": torch.empty((T, H, nh, Dk), **f32),
            "dv": torch.empty((T, H, nh, Dv), **f32), "dbeta": torch.empty((T, H, nh), **f32),

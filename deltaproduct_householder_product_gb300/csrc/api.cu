@@ -290,10 +290,10 @@ size_t bwd_chunk_need(const dp::BwdProblem &p)
 }
 // workspace the dims ask for: the recurrent form's, and the chunked form's
 // where the shape allows it (AUTO, CHUNK_TC)
-size_t bwd_workspace_bytes(const dp_dims *d, const dp::BwdProblem &p, bool varlen)
+size_t bwd_workspace_bytes(const dp_dims *d, const dp::BwdProblem &p)
 {
     size_t n = d->impl == DP_IMPL_CHUNK_TC ? 0 : bwd_recurrent_need(p);
-    if (d->impl != DP_IMPL_RECURRENT && !varlen && dp::backward_chunk_shape_ok(p)) {
+    if (d->impl != DP_IMPL_RECURRENT && dp::backward_chunk_shape_ok(p)) {
         const size_t c = bwd_chunk_need(p);
         n = c > n ? c : n;
     }
@@ -327,9 +327,9 @@ dp_status backward_impl(const dp_dims *dims, const int *cu, const void *q, const
     if (dh0) DP_TRY(check_ptr(dh0, 16));
     p.g = g;
     p.cu = cu;
-    // AUTO takes the chunked form for ungated dense problems with D = 128
-    // when the workspace holds its records, else the recurrent form;
-    // CHUNK_TC also takes gated dense problems with D = 128
+    // AUTO takes the chunked form for ungated problems with D = 128 (dense
+    // or packed) when the workspace holds its records, else the recurrent
+    // form; CHUNK_TC also takes gated problems with D = 128
     bool chunked = dims->impl != DP_IMPL_RECURRENT && dp::backward_chunk_supported(p) &&
                    (g == nullptr || dims->impl == DP_IMPL_CHUNK_TC);
     if (dims->impl == DP_IMPL_CHUNK_TC && !chunked) return DP_ERR_UNSUPPORTED;
@@ -356,7 +356,7 @@ dp_status dp_backward_workspace_size(const dp_dims *dims, size_t *bytes)
 {
     if (!bytes) return DP_ERR_INVALID_ARG;
     DP_TRY(check_bwd_dims(dims, dims && dims->max_seqlen != 0));
-    *bytes = bwd_workspace_bytes(dims, make_bwd(dims), dims->max_seqlen != 0);
+    *bytes = bwd_workspace_bytes(dims, make_bwd(dims));
     return DP_OK;
 }
 

@@ -66,7 +66,9 @@ constexpr size_t kStateFloats = (size_t)kD * kD;   // S0 or dS1 of one chunk
 constexpr size_t kRowsFloats = (size_t)kC * kD;    // U' or dU' of one chunk
 
 struct CbArgs {
-    int B, T, H, nh, ct, nc;
+    int B, T, H, nh, ct, nc;            // nc: chunks per (sequence, head) at the longest length
+    const int *cu;                      // packed sequences: int32 [B+1] token offsets (NULL: dense)
+    int max_T;                          // longest sequence (T for dense calls)
     const void *q, *k, *v, *beta;
     const float *h0;
     const void *d_o;
@@ -116,21 +118,32 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src)
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
-// The chunk's rows: row r (< 32) = token c*ct + r / nh, key r % nh; valid
-// while r < R and the token < T.
+// The chunk's rows: row r (< 32) = token c*ct + r / nh of its sequence, key
+// r % nh; valid while r < R. Packed calls: the sequence's token range from
+// the offsets (a sequence that breaks their rules has no tokens).
 struct ChunkRows {
-    size_t tok0;   // (b, first token of the chunk, h) row index of the [B,T,H] layouts
-    int nt;        // tokens of the chunk (<= ct)
+    size_t tok0;   // (sequence, first token of the chunk, h) row index of the [.,T,H] layouts
+    int nt;        // tokens of the chunk (<= ct; 0 past the sequence's end)
     int R;         // valid extended rows (nt * nh)
+    int len;       // tokens of the sequence
+    bool ok;       // the sequence's offsets keep the rules
 };
 __device__ __forceinline__ ChunkRows chunk_rows(const CbArgs &a, int bh, int c)
 {
     const int b = bh / a.H, h = bh - b * a.H, t0 = c * a.ct;
+    const SeqRange sr = seq_range(a.cu, b, a.B, a.T, a.max_T);
     ChunkRows cr;
-    cr.tok0 = ((size_t)b * a.T + t0) * a.H + h;
-    cr.nt = min(a.ct, a.T - t0);
+    cr.tok0 = ((size_t)sr.b_map * a.T + sr.t0 + t0) * a.H + h;
+    cr.nt = max(0, min(a.ct, sr.len - t0));
     cr.R = cr.nt * a.nh;
+    cr.len = sr.len;
+    cr.ok = sr.ok;
     return cr;
+}
+// chunks of the (sequence, head) of CTA row bh
+__device__ __forceinline__ int seq_chunks(const CbArgs &a, int bh)
+{
+    return (chunk_rows(a, bh, 0).len + a.ct - 1) / a.ct;
 }
 __device__ __forceinline__ size_t key_row(const CbArgs &a, const ChunkRows &cr, int r)
 {
@@ -226,6 +239,8 @@ __global__ void __launch_bounds__(kPrepThreads) cb_prep(const CbArgs a)
     const int ci = blockIdx.x, bh = ci / a.nc, c = ci - bh * a.nc;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const ChunkRows cr = chunk_rows(a, bh, c);
+    if (!cr.ok && c == 0 && threadIdx.x == 0) report_bad_sequence(a.status);
+    if (cr.nt == 0) return;   // past the sequence's end (packed calls)
     float *rec = a.rec + (size_t)ci * kRecFloats;
     stage_f32<true, kC, TIn>(a, cr, (const TIn *)a.k, Ks);
     stage_f32<true, kC, TIn>(a, cr, (const TIn *)a.v, Vs);
@@ -489,13 +504,14 @@ __device__ __forceinline__ void fwd_chain(const CbArgs &a, char *smem)
 #pragma unroll
         for (int j = 0; j < 4; ++j)
             S[i][j] = a.h0 ? a.h0[((size_t)bh * kD + L.sr0 + i) * kD + cg + L.sc0 + j] : 0.f;
-    if (a.nc > 0) prefetch(0);
-    for (int c = 0; c < a.nc; ++c) {
+    const int ncs = seq_chunks(a, bh);
+    if (ncs > 0) prefetch(0);
+    for (int c = 0; c < ncs; ++c) {
         const size_t ci = (size_t)bh * a.nc + c;
         put_state(S, Ssm, a.S0 + ci * kStateFloats, L, cg);
         cp_async_wait_all();
         __syncthreads();   // chunk c's stage and the state tile are complete; chunk c-1's stage is free
-        if (c + 1 < a.nc) prefetch(c + 1);
+        if (c + 1 < ncs) prefetch(c + 1);
         const char *base = smem + (c & 1) * St::kBytes;
         const float *Wc = (const float *)base, *Kc = (const float *)(base + St::kW);
         const float *Uc = (const float *)(base + St::kW + St::kK);
@@ -549,8 +565,9 @@ __device__ __forceinline__ void bwd_chain(const CbArgs &a, char *smem)
 #pragma unroll
         for (int j = 0; j < 4; ++j)
             dS[i][j] = a.dh_final ? a.dh_final[((size_t)bh * kD + L.sr0 + i) * kD + cg + L.sc0 + j] : 0.f;
-    if (a.nc > 0) prefetch(a.nc - 1);
-    for (int c = a.nc - 1; c >= 0; --c) {
+    const int ncs = seq_chunks(a, bh);
+    if (ncs > 0) prefetch(ncs - 1);
+    for (int c = ncs - 1; c >= 0; --c) {
         const size_t ci = (size_t)bh * a.nc + c;
         put_state(dS, dSsm, a.dS1 + ci * kStateFloats, L, cg);
         cp_async_wait_all();
@@ -657,6 +674,7 @@ __global__ void __launch_bounds__(kGradSThreads, 2) cb_grad_s(const CbArgs a)
     const int ci = blockIdx.x, bh = ci / a.nc, c = ci - bh * a.nc;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, kk = tid >> 2, qq = tid & 3;
     const ChunkRows cr = chunk_rows(a, bh, c);
+    if (cr.nt == 0) return;   // past the sequence's end (packed calls)
     float *rec = a.rec + (size_t)ci * kRecFloats;
     float4 sa[8], sb[8];
     auto load_rows = [&](const float *m) {
@@ -773,6 +791,7 @@ __global__ void __launch_bounds__(kGradThreads, 2) cb_grad_r(const CbArgs a)
     const int ci = blockIdx.x, bh = ci / a.nc, c = ci - bh * a.nc;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const ChunkRows cr = chunk_rows(a, bh, c);
+    if (cr.nt == 0) return;   // past the sequence's end (packed calls)
     const float *rec = a.rec + (size_t)ci * kRecFloats;
     const float *dup = a.dUp + (size_t)ci * kRowsFloats;
     for (int i = tid; i < kC * kD / 4; i += kGradThreads) {
@@ -1059,7 +1078,7 @@ int chunk_tokens(int nh) { return (kC / nh < kQ) ? kC / nh : kQ; }
 
 bool backward_chunk_shape_ok(const BwdProblem &p)
 {
-    return p.cu == nullptr && p.Dk == kD && p.Dv == kD && p.nh >= 1 && p.nh <= kC;
+    return p.Dk == kD && p.Dv == kD && p.nh >= 1 && p.nh <= kC;
 }
 
 bool backward_chunk_supported(const BwdProblem &p) { return backward_chunk_shape_ok(p); }
@@ -1068,7 +1087,7 @@ size_t backward_chunk_scratch_bytes(const BwdProblem &p)
 {
     if (!backward_chunk_shape_ok(p)) return 0;
     const int ct = chunk_tokens(p.nh);
-    const size_t nc = (size_t)(p.T + ct - 1) / ct, n = (size_t)p.B * p.H * nc;
+    const size_t nc = (size_t)(p.max_T + ct - 1) / ct, n = (size_t)p.B * p.H * nc;
     return n * (kRecFloats + 2 * kStateFloats + 2 * kRowsFloats) * sizeof(float);
 }
 
@@ -1077,7 +1096,9 @@ cudaError_t launch_backward_chunk(const BwdProblem &p)
     CbArgs a;
     a.B = p.B; a.T = p.T; a.H = p.H; a.nh = p.nh;
     a.ct = chunk_tokens(p.nh);
-    a.nc = (p.T + a.ct - 1) / a.ct;
+    a.cu = p.cu;
+    a.max_T = p.max_T;
+    a.nc = (p.max_T + a.ct - 1) / a.ct;
     a.q = p.q; a.k = p.k; a.v = p.v; a.beta = p.beta; a.h0 = p.h0;
     a.d_o = p.d_o; a.dh_final = p.dh_final;
     a.dq = p.dq; a.dk = p.dk; a.dv = p.dv; a.dbeta = p.dbeta; a.dh0 = p.dh0;

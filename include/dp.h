@@ -223,10 +223,12 @@ dp_status dp_state_io(int op, int B, int H, int Dk, int Dv, float *state,
 dp_status dp_backward_workspace_size(const dp_dims *dims, size_t *bytes);
 /* dp_backward over packed variable-length sequences: layouts, cu_seqlens
  * and dims->max_seqlen as in dp_forward_varlen (the gradients take the
- * layouts of their inputs: dq [T,H,D_k], ..., dh0 [N,H,D_k,D_v]); the
- * workspace (dp_backward_workspace_size with the same dims) holds the
- * checkpoints and errors for max_seqlen per (sequence, head). Sequences
- * whose offsets break the contract record DP_ERR_DEVICE and are skipped. */
+ * layouts of their inputs: dq [T,H,D_k], ..., dh0 [N,H,D_k,D_v]); forms as
+ * in dp_backward (dims->impl); the workspace (dp_backward_workspace_size
+ * with the same dims) holds the recurrent form's checkpoints and errors or
+ * the chunked form's records for max_seqlen per (sequence, head); each
+ * sequence is cut into its own chunks. Sequences whose offsets break the
+ * contract record DP_ERR_DEVICE and are skipped. */
 dp_status dp_backward_varlen(const dp_dims *dims, const int *cu_seqlens,
                              const void *q, const void *k, const void *v,
                              const void *beta, const void *g, const float *h0,

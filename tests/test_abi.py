@@ -154,14 +154,17 @@ def test_backward_workspace_and_validation(L):
     ck128 = 2 * 3 * ((100 + seg - 1) // seg) * 128 * 128 * 4
     need_rec = 256 + r256(r256(ck128) + 2 * 100 * 3 * 2 * 128 * 4)
     chunks = 2 * 3 * ((100 + 15) // 16)
-    need_chunk = 256 + r256(chunks * (2 * 32 * 128 + 32 * 32 + 16 * 32 + 32 * 32 + 32 * 128 + 16 * 128 + 32 * 128 + 16 * 32 + 32 * 32 + 3 * 32 + 4
-                                + 2 * 128 * 128 + 2 * 32 * 128) * 4)
+    per_chunk = (2 * 32 * 128 + 32 * 32 + 16 * 32 + 32 * 32 + 32 * 128 + 16 * 128 + 32 * 128 + 16 * 32 + 32 * 32
+                 + 3 * 32 + 4 + 2 * 128 * 128 + 2 * 32 * 128) * 4
+    need_chunk = 256 + r256(chunks * per_chunk)
     for impl, want in (("recurrent", need_rec), ("chunk_tc", need_chunk), ("auto", max(need_rec, need_chunk))):
         assert L.dp_backward_workspace_size(C.byref(rec(impl)), C.byref(m)) == 0 and m.value == want, impl
-    # packed sequences take the recurrent form only
-    vl = _lib.make_dims(2, 100, 3, 128, 128, 2, _lib.DP_BF16, "auto", _lib.DP_F32, max_seqlen=60)
-    assert L.dp_backward_workspace_size(C.byref(vl), C.byref(m)) == 0
-    assert m.value == 256 + r256(r256(2 * 3 * 5 * 128 * 128 * 4) + 2 * 60 * 3 * 2 * 128 * 4)
+    # packed sequences: both forms, sized for max_seqlen per (sequence, head)
+    vl = lambda impl: _lib.make_dims(2, 100, 3, 128, 128, 2, _lib.DP_BF16, impl, _lib.DP_F32, max_seqlen=60)
+    rec_vl = 256 + r256(r256(2 * 3 * 5 * 128 * 128 * 4) + 2 * 60 * 3 * 2 * 128 * 4)
+    chunk_vl = 256 + r256(2 * 3 * ((60 + 15) // 16) * per_chunk)
+    for impl, want in (("recurrent", rec_vl), ("chunk_tc", chunk_vl), ("auto", max(rec_vl, chunk_vl))):
+        assert L.dp_backward_workspace_size(C.byref(vl(impl)), C.byref(m)) == 0 and m.value == want, impl
     assert L.dp_backward_workspace_size(C.byref(dims), None) == 1
     null = [None] * 15
     assert L.dp_backward(C.byref(dims), *null, C.c_size_t(0), None) == 1

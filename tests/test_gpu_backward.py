@@ -168,14 +168,17 @@ def varlen_case(lengths, nh, seed, gated=True):
     return pk, d_o, dhf, cu
 
 
-@pytest.mark.parametrize("lengths,nh", [([0, 1, 15, 30, 13], 2), ([40, 0, 7], 3), ([5], 1)])
-def test_backward_varlen_parity(dp, lengths, nh):
+@pytest.mark.parametrize("gated,impl", [(True, "auto"), (True, "chunk_tc"), (False, "auto"), (False, "recurrent")],
+                         ids=["gated-recurrent", "gated-chunked", "ungated-chunked", "ungated-recurrent"])
+@pytest.mark.parametrize("lengths,nh", [([0, 1, 15, 30, 13], 2), ([40, 0, 7], 3), ([5], 1), ([17, 33], 4)])
+def test_backward_varlen_parity(dp, lengths, nh, gated, impl):
     """Packed sequences: each sequence's gradients against the oracle's
-    backward on that sequence alone."""
-    x, d_o, dhf, cu = varlen_case(lengths, nh, seed=60 + nh)
+    backward on that sequence alone, in both forms (the chunked one cuts
+    each sequence into its own chunks)."""
+    x, d_o, dhf, cu = varlen_case(lengths, nh, seed=60 + nh, gated=gated)
     xc = {k: (None if v is None else v.cuda()) for k, v in x.items()}
     got, ws = dp.backward_varlen(xc["q"], xc["k"], xc["v"], xc["beta"], xc["g"], xc["h0"], cu_seqlens=cu.cuda(),
-                                 d_o=d_o.cuda(), dh_final=dhf.cuda())
+                                 d_o=d_o.cuda(), dh_final=dhf.cuda(), impl=impl)
     dp.check_status(ws)
     a = 0
     for s, n in enumerate(lengths):
@@ -191,8 +194,9 @@ def test_backward_varlen_parity(dp, lengths, nh):
         a += n
 
 
-def test_backward_varlen_bad_offsets(dp):
-    x, d_o, dhf, cu = varlen_case([20, 20], 2, seed=70)
+@pytest.mark.parametrize("gated", [True, False], ids=["recurrent", "chunked"])
+def test_backward_varlen_bad_offsets(dp, gated):
+    x, d_o, dhf, cu = varlen_case([20, 20], 2, seed=70, gated=gated)
     xc = {k: (None if v is None else v.cuda()) for k, v in x.items()}
     bad = torch.tensor([0, 30, 20], dtype=torch.int32, device="cuda")
     _, ws = dp.backward_varlen(xc["q"], xc["k"], xc["v"], xc["beta"], xc["g"], xc["h0"], cu_seqlens=bad,
