@@ -390,7 +390,7 @@ def backward_measure(dp, dev, hbm_peak, steps=5, warmup=2):
     achieved = step_bytes / (ms * 1e-3) / 1e9
     return {"workload": f"{w.name} backward (fp32 d_o, dh_final and gradients)", "ms_per_call": ms,
             "tokens_per_s": w.B * w.T / (ms * 1e-3),
-            "kernel": ("chunked: cb_prep, cb_chains, cb_grad (CUDA cores)" if not w.gated
+            "kernel": ("chunked: cb_prep, cb_chains, cb_grad_s, cb_grad_r (CUDA cores)" if not w.gated
                        else "backward_kernel (recurrent, CUDA cores)"),
             "recurrent_ms_per_call": ms_rec, "gated": gated_form,
             "workspace_bytes": int(ws.numel()),
