@@ -13,7 +13,7 @@ from ._lib import DPError, STATE_EXPORT, STATE_IMPORT, STATE_ZERO  # noqa: F401
 
 __all__ = ["forward", "forward_varlen", "forward_noalloc", "forward_path", "supports", "decode_step", "state_io", "check_status",
            "backward", "backward_varlen", "prologue", "prologue_flags", "osdn_write_keys", "forward_write_keys",
-           "workspace_size",
+           "workspace_size", "set_wait_fault",
            "DPError", "abi_version"]
 
 
@@ -372,6 +372,14 @@ def state_io(op, state, ext=None, transposed=False, stream=None):
                                 ext_dt, int(bool(transposed)), _lib._stream(stream))
     _lib._check(rc, "dp_state_io")
     return state if op != STATE_EXPORT else ext
+
+
+def set_wait_fault(withhold_first_record=False, flag_wait_polls=0):
+    """dp_test_set_wait_fault: fault injection for tests of the cooperative
+    mode's bounded record wait (process-wide; ``set_wait_fault()`` restores
+    normal operation)."""
+    _lib._check(_lib.lib().dp_test_set_wait_fault(int(bool(withhold_first_record)), int(flag_wait_polls)),
+                "dp_test_set_wait_fault")
 
 
 def check_status(workspace, stream=None):

@@ -64,11 +64,13 @@ def lib():
         L.dp_osdn_write_keys.argtypes = [ctypes.POINTER(Dims), _vp, _vp, _vp, _vp] + [ctypes.c_float] * 4 + \
             [_vp, _vp, _vp]
         L.dp_forward_write_keys.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 10 + [ctypes.c_size_t, _vp]
+        L.dp_test_set_wait_fault.argtypes = [ctypes.c_int, ctypes.c_uint]
         for name in ("dp_forward_workspace_size", "dp_forward_workspace_size_fast", "dp_forward_path",
                      "dp_forward", "dp_forward_varlen", "dp_decode_step",
                      "dp_state_io", "dp_check_status", "dp_forward_noalloc",
                      "dp_backward_workspace_size", "dp_backward", "dp_prologue",
-                     "dp_osdn_write_keys", "dp_forward_write_keys", "dp_backward_varlen"):
+                     "dp_osdn_write_keys", "dp_forward_write_keys", "dp_backward_varlen",
+                     "dp_test_set_wait_fault"):
             getattr(L, name).restype = ctypes.c_int
         _LIB = L
     return _LIB

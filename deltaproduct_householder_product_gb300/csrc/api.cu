@@ -234,6 +234,13 @@ dp_status dp_state_io(int op, int B, int H, int Dk, int Dv, float *state, void *
                                          ext_transposed, (cudaStream_t)stream));
 }
 
+dp_status dp_test_set_wait_fault(int withhold_first_record, unsigned int flag_wait_polls)
+{
+    if (withhold_first_record != 0 && withhold_first_record != 1) return DP_ERR_INVALID_ARG;
+    dp::set_coop_fault({flag_wait_polls, withhold_first_record});
+    return DP_OK;
+}
+
 dp_status dp_check_status(const void *workspace, dp_stream_t stream)
 {
     if (!workspace) return DP_ERR_INVALID_ARG;

@@ -67,6 +67,8 @@
 // in the caller's status word, drains what it has in flight and exits.
 #include <string.h>
 
+#include <atomic>
+
 #include "internal.h"
 #include "sm100.cuh"
 
@@ -189,7 +191,8 @@ struct Params {
     uint32_t *status;
     uint8_t *rec;              // per-chunk records (split mode), [B*H][n_chunks][rec_stride]
     uint32_t *flags;           // cooperative mode: record published, [B*H][n_chunks]
-    uint32_t *sync;            // cooperative mode: [0] launch generation, [1] CTAs finished
+    uint32_t flag_tries;       // cooperative mode: polls of a flag before the wait gives up
+    int withhold_first;        // cooperative mode, fault-injection hook: the first record is never published
     int T, H, nh, ct;
     int n_chunks;              // chunks of the longest sequence: records per (sequence, head)
     int bh_count;
@@ -247,8 +250,11 @@ __device__ __forceinline__ size_t tok_row(const Params &p, const J &j, int t)
     return ((size_t)j.row_b() * p.T + j.first() + t) * p.H + j.h;
 }
 
-// Cooperative mode: a record is published by storing generation + 1 into
-// its flag (release); the state pass acquires it before loading the record.
+// Cooperative mode: a record is published by storing 1 into its flag
+// (release); the state pass acquires it before loading the record. The
+// host clears every flag on the stream before each cooperative launch, so
+// no value left in the workspace by an earlier call (of any shape) can
+// pass for a published record.
 __device__ __forceinline__ void flag_publish(uint32_t *flag, uint32_t v)
 {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(v) : "memory");
@@ -258,13 +264,6 @@ __device__ __forceinline__ uint32_t flag_read(const uint32_t *flag)
 {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ uint32_t read_generation(const uint32_t *sync)
-{
-    uint32_t v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(sync) : "memory");
     return v;
 }
 
@@ -407,7 +406,7 @@ __device__ __forceinline__ void issue_gram_wk(uint32_t d_tmem, uint32_t kq, uint
 }
 
 // ------------------------------------------------------------------ TMA producer
-constexpr uint32_t kFlagTries = 1u << 24;   // x >= 64 ns each: seconds, then a timeout
+constexpr uint32_t kFlagTries = 1u << 24;   // default flag polls: x >= 64 ns each, seconds, then a timeout
 
 template <bool kSplit, bool kCoop, class J>
 __device__ void tma_role(const Smem &s, const Params &p, const CUtensorMap *tk,
@@ -415,7 +414,6 @@ __device__ void tma_role(const Smem &s, const Params &p, const CUtensorMap *tk,
 {
     const int h = jb.h;
     const int ct = p.ct, R = ct * p.nh;
-    const uint32_t want = kCoop ? read_generation(p.sync) + 1 : 0;
     const bool gated = p.g != nullptr;
     // K and V: 2 x R rows x 128 B each; Q: 2 x ct rows. Record: the T tiles
     // it uses (2 or 4) and P, beta, L.
@@ -434,8 +432,8 @@ __device__ void tma_role(const Smem &s, const Params &p, const CUtensorMap *tk,
             // it, then order the bulk copy (async proxy) after that read
             const uint32_t *flag = p.flags + rec_index(p, jb, c);
             uint32_t tries = 0;
-            while (flag_read(flag) != want && ++tries < kFlagTries && !*s.abort) __nanosleep(64);
-            if (tries >= kFlagTries || *s.abort) {
+            while (flag_read(flag) != 1u && ++tries < p.flag_tries && !*s.abort) __nanosleep(64);
+            if (tries >= p.flag_tries || *s.abort) {
                 flag_error(p.status, s.abort, kDevTimeout);
                 break;
             }
@@ -1261,8 +1259,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 // (warps 0-7 and 8-15), and publish each record through its flag. The
 // state pass waits for a record's flag (bounded) before loading it. All CTAs
 // are resident together (cooperative launch), and no prep CTA waits on a
-// state-pass CTA. Flags carry the launch generation + 1; the last CTA to
-// finish advances the generation, so flags of earlier launches never match.
+// state-pass CTA. The host zeroes the flags before the launch.
 constexpr uint32_t kCoopScratch = (kPrepScratch + 127) & ~127u;
 
 template <bool kPacked, bool kPro, bool kWK>
@@ -1296,7 +1293,6 @@ __device__ void prep_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
-    const uint32_t want = read_generation(p.sync) + 1;
 
     if (warp < 16) {
         const int gi = warp >> 3, lt = threadIdx.x - gi * kPrepThreads;
@@ -1311,9 +1307,9 @@ __device__ void prep_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const
                             abort, tbase, gi * 32, lt, 1 + gi, jb, c))
                 break;
             ++k;
-            if (lt == 0) {
+            if (lt == 0 && !(p.withhold_first && idx == 0)) {
                 __threadfence();
-                flag_publish(p.flags + rec_index(p, jb, c), want);
+                flag_publish(p.flags + rec_index(p, jb, c), 1u);
             }
         }
     }
@@ -1332,17 +1328,22 @@ chunk_coop_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         state_pass_cta<TOut, true, true, kPacked, kPro, kWK>(tm_k, tm_v, tm_q, p, blockIdx.x);
     else
         prep_cta<kPacked, kPro, kWK>(tm_k, tm_q, tm_kw, p, blockIdx.x - p.bh_count, gridDim.x - p.bh_count);
-    // every thread of this CTA is done (the role ended with a CTA barrier)
-    if (threadIdx.x == 0) {
-        __threadfence();
-        if (atomicAdd(&p.sync[1], 1u) == gridDim.x - 1) {
-            atomicExch(&p.sync[1], 0u);
-            atomicAdd(&p.sync[0], 1u);
-        }
-    }
 }
 
 }  // namespace
+
+namespace {
+std::atomic<uint32_t> g_fault_tries{0};
+std::atomic<int> g_fault_withhold{0};
+}  // namespace
+
+CoopFault coop_fault() { return {g_fault_tries.load(), g_fault_withhold.load()}; }
+
+void set_coop_fault(CoopFault f)
+{
+    g_fault_tries.store(f.flag_tries);
+    g_fault_withhold.store(f.withhold_first);
+}
 
 bool chunk_tc_supported(const Problem &p)
 {
@@ -1365,11 +1366,11 @@ size_t chunks_per_seq(const Problem &p)
 size_t n_chunks_total(const Problem &p) { return (size_t)p.B * p.H * chunks_per_seq(p); }
 }  // namespace
 
-// Records, then one flag per chunk, then the two cooperative-mode words.
+// Records, then one flag per chunk (cooperative mode).
 size_t chunk_tc_records_bytes(const Problem &p)
 {
     const size_t n = n_chunks_total(p);
-    return n ? round256(n * record_stride(p.prologue)) + round256(n * 4) + 256 : 0;
+    return n ? round256(n * record_stride(p.prologue)) + round256(n * 4) : 0;
 }
 
 namespace {
@@ -1465,7 +1466,8 @@ cudaError_t launch_chunk_tc(const Problem &p)
     pr.status = p.status;
     pr.rec = (uint8_t *)p.scratch;
     pr.flags = nullptr;
-    pr.sync = nullptr;
+    pr.flag_tries = kFlagTries;
+    pr.withhold_first = 0;
     pr.bh_count = p.B * p.H;
     pr.cu = p.cu;
     pr.B = p.B;
@@ -1493,7 +1495,11 @@ cudaError_t launch_chunk_tc(const Problem &p)
     if (grid > 0) {
         auto kernel = coop_kernel_for(p);
         pr.flags = (uint32_t *)((uint8_t *)p.scratch + rec_bytes);
-        pr.sync = (uint32_t *)((uint8_t *)pr.flags + round256(n_total * 4));
+        const CoopFault f = coop_fault();
+        if (f.flag_tries) pr.flag_tries = f.flag_tries;
+        pr.withhold_first = f.withhold_first;
+        // every flag starts at zero, whatever an earlier call left in the workspace
+        if ((e = cudaMemsetAsync(pr.flags, 0, n_total * 4, p.stream)) != cudaSuccess) return e;
         void *args[] = {(void *)&tk, (void *)&tv, (void *)&tq, (void *)&tkw, (void *)&pr};
         e = cudaLaunchCooperativeKernel((const void *)kernel, dim3((unsigned)grid), dim3(kThreads), args,
                                         smem_bytes<true>(), p.stream);

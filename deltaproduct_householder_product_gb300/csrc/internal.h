@@ -43,6 +43,16 @@ size_t chunk_tc_records_bytes(const Problem &p);
 // (a dp_path value).
 cudaError_t chunk_tc_path(const Problem &p, int *path);
 cudaError_t launch_chunk_tc(const Problem &p);
+// Fault-injection setting of the cooperative mode (dp_test_set_wait_fault):
+// flag_tries = polls of a record flag before the wait expires (0: the
+// default, seconds); withhold_first = the prep CTAs never publish the first
+// record, so the state pass's wait for it expires. Process-wide.
+struct CoopFault {
+    uint32_t flag_tries;
+    int withhold_first;
+};
+CoopFault coop_fault();
+void set_coop_fault(CoopFault f);
 
 // One validated backward problem (dp_backward; layouts in dp.h).
 struct BwdProblem {

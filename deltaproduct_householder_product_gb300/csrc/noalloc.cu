@@ -31,9 +31,12 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 void *g_scratch_addr[kMaxDevices];
 std::mutex g_scratch_lock;
 
-// Device address of the scratch array on the current device (looked up on
-// the first call made with that device current).
-dp_status scratch_for_current_device(void **out)
+// Device address of the scratch array on the current device. Outside stream
+// capture it is looked up on every call (cheap), so a context rebuilt after
+// cudaDeviceReset never receives the old context's address; a call made while
+// `stream` is capturing uses the address cached by the last uncaptured call
+// on that device and fails with DP_ERR_CUDA if there was none.
+dp_status scratch_for_current_device(cudaStream_t stream, void **out)
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -41,8 +44,13 @@ dp_status scratch_for_current_device(void **out)
         return DP_ERR_CUDA;
     }
     if (dev < 0 || dev >= kMaxDevices) return DP_ERR_UNSUPPORTED;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+        cudaGetLastError();
+        return DP_ERR_CUDA;
+    }
     std::lock_guard<std::mutex> guard(g_scratch_lock);
-    if (!g_scratch_addr[dev]) {
+    if (cap == cudaStreamCaptureStatusNone) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
             cudaGetLastError();
@@ -50,6 +58,7 @@ dp_status scratch_for_current_device(void **out)
         }
         g_scratch_addr[dev] = p;
     }
+    if (!g_scratch_addr[dev]) return DP_ERR_CUDA;
     *out = g_scratch_addr[dev];
     return DP_OK;
 }
@@ -66,11 +75,15 @@ extern "C" dp_status dp_forward_noalloc(const dp_dims *dims, const void *q, cons
     if (s != DP_OK) return s;
     if (need > kNoAllocScratchBytes) return DP_ERR_WORKSPACE;
     void *scratch = nullptr;
-    s = scratch_for_current_device(&scratch);
+    s = scratch_for_current_device((cudaStream_t)stream, &scratch);
     if (s != DP_OK) return s;
     // The array is zero at load. The kernels write the status word only on a
     // device-side error, and this call clears it again behind its own kernel,
-    // so the next call's kernel starts from zero.
+    // so the next call's kernel starts from zero. The rest of the array holds
+    // whatever the last call left: per-chunk records (rewritten by every call
+    // before they are read) and the cooperative mode's flags (cleared by
+    // dp_forward before each cooperative launch), so calls of different
+    // shapes may follow one another on a stream.
     s = dp_forward(dims, q, k, v, beta, g, h0, o, h_final, scratch, kNoAllocScratchBytes, stream);
     if (s != DP_OK) return s;
     if (cudaMemsetAsync(scratch, 0, need, (cudaStream_t)stream) != cudaSuccess) return DP_ERR_CUDA;

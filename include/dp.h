@@ -96,7 +96,7 @@ typedef enum {
 } dp_prologue_flags;
 
 /* ABI version of this header (bumped on any signature change). */
-#define DP_ABI_VERSION 8
+#define DP_ABI_VERSION 9
 int dp_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -109,15 +109,17 @@ dp_status dp_forward_workspace_size(const dp_dims *dims, size_t *bytes);
 /* Bytes of device workspace with which dp_forward runs its fastest path
  * (>= dp_forward_workspace_size). For the tensor-core chunk path this adds,
  * per (batch, head, chunk) of ceil(T / ct) chunks, ct = min(16, 32 / n_h)
- * tokens, an 18688-byte record and a 4-byte flag, plus 256 bytes: every
+ * tokens, an 18688-byte record and a 4-byte flag (each area rounded up to
+ * 256 bytes): every
  * chunk's UT transform is then prepared in parallel (by the other CTAs of
  * one cooperative launch when B*H leaves at least half the SMs free, else by
  * a first kernel) and the state pass streams the records in. With at least
  * dp_forward_workspace_size bytes but less than this, dp_forward runs one
  * fused kernel instead: slower, bit-identical results. Both sizes are equal
- * for the recurrent path. Like the status word, the flags must start at
- * zero: zero the workspace once after allocating it; calls sharing a
- * workspace must be ordered (one stream). */
+ * for the recurrent path. The library clears the flags on the stream before
+ * every cooperative launch, so a workspace may be reused by calls of any
+ * shapes, in any order; calls sharing a workspace must be ordered (one
+ * stream). */
 dp_status dp_forward_workspace_size_fast(const dp_dims *dims, size_t *bytes);
 
 /* How dp_forward runs a problem given `workspace_bytes` of workspace
@@ -290,6 +292,23 @@ dp_status dp_forward_write_keys(const dp_dims *dims, const void *q, const void *
  * workspace since it was last cleared, and clears it. */
 dp_status dp_check_status(const void *workspace, dp_stream_t stream);
 
+/* Fault injection for tests of the device-side bounded waits (a library
+ * facility; the paper has no counterpart). Applies to the cooperative mode
+ * of the chunk path (DP_PATH_CHUNK_COOP), process-wide, to every launch
+ * made after the call until it is called again with (0, 0):
+ *   withhold_first_record  1: the prep CTAs never publish the record of the
+ *                          first chunk (batch 0, head 0, chunk 0), so the
+ *                          state pass's wait for it must expire; 0: normal.
+ *   flag_wait_polls        polls of a record flag (about 64 ns or more
+ *                          each) before that wait gives up; 0 restores the
+ *                          default (2^24 polls, about a second or more).
+ * An expired wait makes the waiting CTA record DP_ERR_TIMEOUT in the
+ * workspace's status word, drain what it has in flight, release its tensor
+ * memory and return; the other CTAs finish normally, so the launch ends and
+ * the context stays usable. Nothing faults, traps or hangs. Returns
+ * DP_ERR_INVALID_ARG unless withhold_first_record is 0 or 1. */
+dp_status dp_test_set_wait_fault(int withhold_first_record, unsigned int flag_wait_polls);
+
 /* dp_forward for callers that cannot allocate device memory (their HBM is
  * owned by a framework allocator or a fixed memory budget, or cudaMalloc's
  * implicit synchronisation is not acceptable on their path). This entry
@@ -298,13 +317,16 @@ dp_status dp_check_status(const void *workspace, dp_stream_t stream);
  * the scratch lives in a fixed 64 KiB device array inside libdp.so that
  * every GPU loading the library holds until the process exits, and the call
  * allocates nothing. Problems whose dp_forward_workspace_size exceeds 64 KiB
- * return DP_ERR_WORKSPACE. The first call made with a device current looks
- * up the array's device address (cudaGetSymbolAddress); make that first
- * call before any stream capture. All calls on a device share the array:
- * calls whose kernels overlap on the GPU (unordered streams) race on it;
- * calls ordered on one stream are safe. Device-side wait timeouts are not
- * reported by this entry point (each call clears the array's status word
- * behind its kernel); host-side validation and launch errors are. */
+ * return DP_ERR_WORKSPACE. Each call made outside stream capture looks up
+ * the array's device address on the current device (cudaGetSymbolAddress);
+ * a call made while `stream` is capturing reuses the address the last
+ * uncaptured call on that device found, so make one call before any stream
+ * capture. All calls on a device share the array and it keeps what the
+ * last call left: calls whose kernels overlap on the GPU (unordered
+ * streams) race on it; calls ordered on one stream are safe, whatever their
+ * shapes. Device-side wait timeouts are not reported by this entry point
+ * (each call clears the array's status word behind its kernel); host-side
+ * validation and launch errors are. */
 dp_status dp_forward_noalloc(const dp_dims *dims,
                              const void *q, const void *k, const void *v,
                              const void *beta, const void *g,

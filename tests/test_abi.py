@@ -172,3 +172,13 @@ def test_backward_workspace_and_validation(L):
     assert L.dp_backward(C.byref(bad), *null, C.c_size_t(0), None) == 2
     empty = _lib.make_dims(0, 100, 3, 128, 64, 2, _lib.DP_BF16)
     assert L.dp_backward_workspace_size(C.byref(empty), C.byref(n)) == 0 and n.value == 256
+
+
+def test_wait_fault_hook_validation(L):
+    """dp_test_set_wait_fault takes 0 or 1 for its withhold switch (anything
+    else is rejected without changing the setting) and (0, 0) restores
+    normal operation. Host-only: no kernel runs."""
+    assert L.dp_test_set_wait_fault(2, 0) == 1
+    assert L.dp_test_set_wait_fault(-1, 5) == 1
+    assert L.dp_test_set_wait_fault(0, 1000) == 0
+    assert L.dp_test_set_wait_fault(0, 0) == 0

@@ -137,6 +137,80 @@ def test_workspace_reuse_across_calls(dp):
         assert torch.equal(hf, h_f)
 
 
+def test_workspace_reuse_across_shapes(dp):
+    """One workspace, zeroed once, reused by calls of different shapes: a
+    split-mode problem with more than 4096 chunks (80 heads of the near-
+    duplicate recipe) leaves record bytes all over the area where a small
+    problem's cooperative flags live; the cooperative calls that follow
+    (two seeds, another shape, the first seed again) must each equal the
+    same call on a fresh zeroed workspace bit for bit and meet the bf16 rule
+    against the oracle (DeltaProduct paper, Sec.4: the result depends on the
+    inputs only, not on what earlier calls left in the scratch memory)."""
+    big = W.NEARDUP.scaled(B=8, H=10, T=520)
+    xb = cuda(W.make_inputs(big))
+    size = workspace_for(dp, xb, "chunk_tc", "split")
+    assert dp.forward_path(*_dims(xb)[:6], size) == "chunk_split"
+    assert 8 * 10 * (-(-520 // 10)) > 4096
+    small = [W.BASE.scaled(B=2, H=3, T=200, seed=21), W.BASE.scaled(B=2, H=3, T=200, seed=22),
+             W.GATED.scaled(B=1, H=2, T=120, nh=3), W.BASE.scaled(B=2, H=3, T=200, seed=21)]
+    ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
+    for w in small:
+        assert size >= workspace_for(dp, W.make_inputs(w), "chunk_tc", "split")
+    dp.forward(xb["q"], xb["k"], xb["v"], xb["beta"], xb["g"], xb["h0"], impl="chunk_tc", workspace=ws,
+               out_dtype=torch.float32)
+    dp.check_status(ws)
+    for w in small:
+        x = W.make_inputs(w)
+        g = cuda(x)
+        assert dp.forward_path(*_dims(g)[:6], size) == "chunk_coop"
+        o, hf = dp.forward(g["q"], g["k"], g["v"], g["beta"], g["g"], g["h0"], impl="chunk_tc",
+                           workspace=ws, out_dtype=torch.float32)
+        dp.check_status(ws)
+        o_f, h_f = run(dp, x, path="split")
+        assert torch.equal(o, o_f), w
+        assert torch.equal(hf, h_f), w
+        ro, rh = ref(x)
+        assert_parity(o, ro, "bf16", "o")
+        assert_parity(hf, rh, "bf16", "h_final")
+
+
+def test_coop_wait_timeout_is_reported(dp):
+    """A device-side bounded wait that expires (SURVEY's failure-detection
+    case, made on purpose without a fault): the prep CTAs withhold the first
+    record, so the state pass's wait for its flag runs out after a short
+    limit. The call returns, the status word reads DP_ERR_TIMEOUT, the other
+    heads' results are still right, and the next normal call on the same
+    stream and workspace is clean and matches the oracle."""
+    import time
+    w = W.BASE.scaled(B=1, H=3, T=40)
+    x = W.make_inputs(w)
+    g = cuda(x)
+    size = workspace_for(dp, x, "chunk_tc", "split")
+    assert dp.forward_path(*_dims(g)[:6], size) == "chunk_coop"
+    ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
+    ro, rh = ref(x)
+    o = torch.zeros(w.B, w.T, w.H, w.Dv, dtype=torch.float32, device="cuda")
+    try:
+        dp.set_wait_fault(True, 4096)
+        t0 = time.perf_counter()
+        dp.forward(g["q"], g["k"], g["v"], g["beta"], g["g"], g["h0"], impl="chunk_tc", workspace=ws, out=o)
+        torch.cuda.synchronize()
+        elapsed = time.perf_counter() - t0
+    finally:
+        dp.set_wait_fault()
+    with pytest.raises(dp.DPError) as err:
+        dp.check_status(ws)
+    assert err.value.code == 6                        # DP_ERR_TIMEOUT
+    assert elapsed < 10.0, elapsed                    # 4096 polls: milliseconds
+    assert_parity(o[:, :, 1:], ro[:, :, 1:], "bf16", "o of the heads that were not starved")
+    dp.check_status(ws)                               # read-and-clear: clean again
+    o2, h2 = dp.forward(g["q"], g["k"], g["v"], g["beta"], g["g"], g["h0"], impl="chunk_tc", workspace=ws,
+                        out_dtype=torch.float32)
+    dp.check_status(ws)
+    assert_parity(o2, ro, "bf16", "o after the timeout")
+    assert_parity(h2, rh, "bf16", "h_final after the timeout")
+
+
 @pytest.mark.parametrize("base", [W.BASE, W.GATED, W.NEARDUP], ids=lambda w: w.name)
 def test_bf16_output_is_rounded_fp32_output(dp, base):
     """The bf16-output variant runs the same arithmetic and only rounds the final
