@@ -1,9 +1,13 @@
 """Throughput benchmark of the DeltaProduct forward on GB300.
 
-One step = one dp_forward call over the whole workload
-(B4 H8 T2048 n_h2 D128 bf16 by default): every row of the hot path (extended
-sequence, gate, chunk Gram, UT transform, W/U, state pass, masked readout,
-state I/O) runs inside that call.
+One step = one dp_forward call over the whole workload (by default the
+largest single-GPU configuration: the gated B4 H16 T8192 n_h 4 D128 bf16
+workload with a nonzero initial state and the final state returned): every
+row of the hot path (extended sequence, gate, chunk Gram, UT transform, W/U,
+state pass, masked readout, state I/O) runs inside that call. The same line
+carries the other bf16 workloads (B4 H8 T2048 n_h 2; B8 H16 T4096 n_h 3 with
+near-duplicate keys; B1 H16 T32768 n_h 3 as one call and as 8 carried
+4096-token calls), each timed the same way, under "configs".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -35,11 +39,14 @@ import torch  # noqa: E402
 from deltaproduct_householder_product_gb300 import workloads as W  # noqa: E402
 
 WORKLOADS = {"base": W.BASE, "neardup": W.NEARDUP, "gated": W.GATED, "long": W.LONG}
+# the workloads reported beside the headline one, in this order
+SIDE_CONFIGS = ("base", "neardup", "long")
 METRIC = "DeltaProduct fwd tokens/s on 1 GB300; % of tensor-pipe/HBM roofline"
 L2_BYTES = 129 * 2 ** 20
-# o is written in fp32: the parity tolerance is stated on the kernel's fp32
-# arithmetic, and this is the configuration the parity tests check
-OUT_DTYPE = torch.float32
+# o is written in the input dtype (bf16), the size the algorithmic byte count
+# takes; the parity tests check the fp32 o against the oracle and the bf16 o
+# against the fp32 o rounded once (bit for bit)
+OUT_DTYPE = torch.bfloat16
 
 
 def parse():
@@ -48,7 +55,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="base", choices=list(WORKLOADS))
+    ap.add_argument("--workload", default="gated", choices=list(WORKLOADS))
+    ap.add_argument("--no-configs", action="store_true",
+                    help="measure only --workload, not the other bf16 workloads beside it")
     ap.add_argument("--kernel", default="auto", choices=["auto", "recurrent", "chunk_tc"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -536,6 +545,104 @@ def varlen_measure(dp, dev, hbm_peak, steps=20, warmup=3):
                          "frac": achieved / hbm_peak, "algorithmic_bytes": wbytes}}
 
 
+def roofline_obj(w, ms, hbm_peak, peak_kind, path, scope):
+    """HBM roofline of one forward: algorithmic bytes (inputs, bf16 o, state
+    I/O) over the measured time per call."""
+    wbytes = W.algorithmic_bytes(w, out_bytes=OUT_DTYPE.itemsize)
+    achieved = wbytes / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+            "frac": achieved / hbm_peak, "traffic": TRAFFIC.get((w.name, path)),
+            "peak_kind": peak_kind, "algorithmic_bytes": wbytes, "scope": scope}
+
+
+def timed_forward(dp, L, w, dev, steps, warmup, kernel):
+    """Time `steps` dp_forward calls over rotating device copies of the
+    workload (more than 3x the L2 in total, so no call finds its inputs in
+    L2), after `warmup` calls, with CUDA events on the launching stream.
+    Returns (ms per call, path, launches per call, number of copies)."""
+    from deltaproduct_householder_product_gb300 import _lib
+    stream = torch.cuda.current_stream()
+    wbytes = W.algorithmic_bytes(w, out_bytes=OUT_DTYPE.itemsize)
+    n_copies = max(2, -(-3 * L2_BYTES // wbytes))
+    _, copies = make_copies(w, n_copies, dev)
+    calls, _, path = forward_calls(dp, L, w, copies, kernel, stream)
+    run_calls(calls, warmup)
+    torch.cuda.synchronize()
+    for c in copies:
+        dp.check_status(c["ws"])
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    run_calls(calls, steps, start=warmup)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    for c in copies:
+        dp.check_status(c["ws"])
+    ms = ev0.elapsed_time(ev1) / steps
+    del copies, calls
+    torch.cuda.empty_cache()
+    return ms, path, _lib.LAUNCHES[path], n_copies
+
+
+def carried_calls_measure(dp, dev, w, n_calls, steps, warmup):
+    """The long workload as `n_calls` sequential dp_forward calls of T /
+    n_calls tokens each, the state carried from one call to the next (h0 and
+    h_final the same buffer): time per whole sequence, CUDA events."""
+    seg = w.T // n_calls
+    x = W.make_inputs(w)
+    parts = []
+    for s in range(n_calls):
+        sl = slice(s * seg, (s + 1) * seg)
+        parts.append({k: x[k][:, sl].contiguous().to(dev) for k in ("q", "k", "v", "beta")})
+    state = torch.zeros(w.B, w.H, w.Dk, w.Dv, dtype=torch.float32, device=dev)
+    o = [torch.empty(w.B, seg, w.H, w.Dv, dtype=OUT_DTYPE, device=dev) for _ in range(n_calls)]
+    ws = torch.zeros(dp.workspace_size(w.B, seg, w.H, w.Dk, w.Dv, w.nh, w.torch_dtype, fast=True),
+                     dtype=torch.uint8, device=dev)
+
+    def one():
+        state.zero_()
+        for s in range(n_calls):
+            p = parts[s]
+            dp.forward(p["q"], p["k"], p["v"], p["beta"], None, state, out=o[s], h_final=state, workspace=ws)
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dp.check_status(ws)
+    ms = e0.elapsed_time(e1) / steps
+    path = dp.forward_path(w.B, seg, w.H, w.Dk, w.Dv, w.nh, ws.numel())
+    return ms, path
+
+
+def side_configs(dp, L, dev, args, hbm_peak, peak_kind):
+    """The other bf16 workloads, each timed like the headline one."""
+    out = {}
+    steps, warmup = max(3, min(args.steps, 50)), max(3, args.warmup)
+    for name in SIDE_CONFIGS:
+        if name == args.workload:
+            continue
+        w = WORKLOADS[name]
+        ms, path, launches, n_copies = timed_forward(dp, L, w, dev, steps, warmup, args.kernel)
+        out[w.name] = {"ms": ms, "tokens_per_s": w.B * w.T / (ms * 1e-3), "path": path,
+                       "launches_per_call": launches, "steps": steps, "warmup": warmup,
+                       "l2": f"{n_copies} rotating copies",
+                       "roofline": roofline_obj(w, ms, hbm_peak, peak_kind, path, "one forward")}
+        if name == "long":
+            cms, cpath = carried_calls_measure(dp, dev, w, W.LONG_CALLS, max(3, steps // 5), 2)
+            out[w.name + f" as {W.LONG_CALLS} carried calls"] = {
+                "ms": cms, "tokens_per_s": w.B * w.T / (cms * 1e-3), "path": cpath,
+                "calls": W.LONG_CALLS, "tokens_per_call": w.T // W.LONG_CALLS,
+                "roofline": roofline_obj(w, cms, hbm_peak, peak_kind, cpath,
+                                         f"{W.LONG_CALLS} carried calls over distinct inputs")}
+        torch.cuda.empty_cache()
+    return out
+
+
 def ours_arm(args, w):
     import deltaproduct_householder_product_gb300 as dp
     from deltaproduct_householder_product_gb300 import _lib
@@ -547,8 +654,9 @@ def ours_arm(args, w):
     dev = torch.device("cuda", local)
     L = _lib.lib()
     stream = torch.cuda.current_stream()
+    hbm_peak, _, peak_kind = measured_peaks()
 
-    wbytes = W.algorithmic_bytes(w, out_bytes=4)
+    wbytes = W.algorithmic_bytes(w, out_bytes=OUT_DTYPE.itemsize)
     n_copies = max(2, -(-3 * L2_BYTES // wbytes))          # rotate copies: > 3x L2 in total
     x, copies = make_copies(w, n_copies, dev)
     calls, dims, path = forward_calls(dp, L, w, copies, args.kernel, stream, args.fused, args.split)
@@ -579,8 +687,8 @@ def ours_arm(args, w):
     soak_until = time.perf_counter() + max(0.0, 1.5 - wall_timed)
     i = args.warmup + args.steps
     while time.perf_counter() < soak_until:
-        run_calls(calls, 50, start=i)
-        i += 50
+        run_calls(calls, 20, start=i)
+        i += 20
     torch.cuda.synchronize()
     clocks = sampler.stop()
     clocks["window"] = "timed region" + (" + soak of the same step" if wall_timed < 1.5 else "")
@@ -635,19 +743,20 @@ def ours_arm(args, w):
     e1.record(s_out)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
+    del copies, calls, bufs, host, o_host, hf_host
+    torch.cuda.empty_cache()
 
     if rank != 0:
         return
     tokens = w.B * w.T
-    hbm_peak, _, peak_kind = measured_peaks()
-    achieved = wbytes / (ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": job_tokens_per_s(tokens, world, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "out_dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32", "out_dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "nh": w.nh, "Dk": w.Dk,
-                   "Dv": w.Dv, "kernel": args.kernel, "gated": w.gated,
+                   "Dv": w.Dv, "kernel": args.kernel, "gated": w.gated, "h0": w.h0_std > 0,
                    "path": path,
                    "l2": f"{n_copies} rotating input/output copies "
                          f"({n_copies * wbytes / 1e6:.0f} MB > 129 MB L2)",
@@ -656,13 +765,12 @@ def ours_arm(args, w):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "pipeline": "copy-in, compute and copy-out streams over two device buffer sets"},
         "gpu_launches": args.steps * launches,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak,
-                     "traffic": TRAFFIC.get((w.name, path)),
-                     "peak_kind": peak_kind, "algorithmic_bytes": wbytes,
-                     "scope": "one forward: every launch dp_forward enqueues"},
+        "roofline": roofline_obj(w, ms, hbm_peak, peak_kind, path,
+                                 "one forward: every launch dp_forward enqueues"),
         "clocks": clocks,
     }
+    if not args.no_configs:
+        line["configs"] = side_configs(dp, L, dev, args, hbm_peak, peak_kind)
     if not args.no_decode:
         line["decode"] = decode_measure(dev, hbm_peak)
     if not args.no_varlen:
@@ -681,9 +789,9 @@ def ours_arm(args, w):
 
 
 # DRAM bytes (read + write) per forward, summed over its launches, from an ncu
-# capture of the current kernels; keyed by (workload, path); absent = not
-# captured for this build
-TRAFFIC = {("b4h8t2048-nh2-d128-bf16", "chunk_coop"): 142_394_112}
+# capture of the current kernels (bf16 o); keyed by (workload, path); absent
+# = not captured for the kernels as they stand
+TRAFFIC = {}
 
 
 def only_arm(args):
