@@ -62,7 +62,10 @@
 //              buffers): write the fp32 B tiles of the state pass (P, Gamma q,
 //              decayed K^T, and -W once the W MMA is done).
 //  * warps 0-3 epilogue: initial state in, outputs and final state out; for
-//              gated inputs also S <- Gamma_C S between the two halves.
+//              gated inputs the stored state is S / sigma (sigma: the chunk
+//              decays since the last rescale, folded into the B tiles), and
+//              on the few chunks that rescale it the epilogue multiplies it
+//              by sigma Gamma_C between the two halves.
 // Every wait on an mbarrier is bounded; on expiry the CTA records a timeout
 // in the caller's status word, drains what it has in flight and exits.
 #include <string.h>
@@ -313,8 +316,8 @@ enum : int {
     kBarReady = kBarUW + 2,       // [2] state-pass B tiles written
     kBarM2 = kBarReady + 2,       // [2] chunk's state pass and readout done
     kBarOFree = kBarM2 + 2,       // [2] O buffers drained by the epilogue (one arrival per warp)
-    kBarM1 = kBarOFree + 2,       // first half (U', S^T q) done (gated)
-    kBarScaled,                   // S scaled by Gamma_C (gated; one arrival per epilogue warp)
+    kBarM1 = kBarOFree + 2,       // first half (U', S^T q) done (gated, rescaling chunks only)
+    kBarScaled,                   // stored state rescaled (gated; one arrival per epilogue warp)
     kBarInit,                     // initial state in TMEM
     kBarFinal,                    // [2] every MMA of an issuer retired (teardown)
     kBarNorm = kBarFinal + 2,     // [2] prologue applied to the group's stage (fused mode with a prologue)
@@ -327,6 +330,7 @@ struct Smem {
     uint64_t *bar;
     uint32_t *tmem_slot;
     volatile uint32_t *abort;
+    volatile uint32_t *renorm;   // [2] gated: the group's chunk rescales the stored state (see epi_role)
     uint32_t stage_bytes, group_off, group_bytes, scratch_off;
     __device__ uint8_t *stage(int st) const { return base + st * stage_bytes; }
     __device__ uint8_t *group(int g) const { return base + group_off + g * group_bytes; }
@@ -545,6 +549,7 @@ __device__ void chain_role(const Smem &s, const Params &p, uint32_t tbase, int n
     const uint32_t id_x = idesc_tf32(128, kXRows);
     const uint32_t id_y = idesc_tf32(128, kYRows);
     bool ok = wait_bar(s, kBarInit, 0, p.status);
+    uint32_t n_renorm = 0;
     for (int c = 0; c < n && ok; ++c) {
         const int g = c & 1;
         const uint32_t gb = smem_addr(s.group(g));
@@ -555,9 +560,10 @@ __device__ void chain_role(const Smem &s, const Params &p, uint32_t tbase, int n
         for (int kk = 0; kk < 16; ++kk)
             mma_ts_tf32(tbase + col_un(g), tbase + kColS + kk * 8,
                         sdesc_sw128(gb + kGX + (kk >> 2) * kXBlock + (kk & 3) * 32, 16, 1024), id_x, 1);
-        if (gated) {
+        if (gated && s.renorm[g]) {   // this chunk rescales the stored state
             mma_commit(&s.bar[kBarM1]);
-            if (!(ok = wait_bar(s, kBarScaled, c & 1, p.status))) break;
+            if (!(ok = wait_bar(s, kBarScaled, n_renorm & 1, p.status))) break;
+            ++n_renorm;
             tc_fence_after();
         }
         const uint32_t d_y = g ? tbase + kColS : tbase + kColOa0;   // O_a[0] | S  or  S | O_a[1]
@@ -641,6 +647,39 @@ __device__ __forceinline__ void scan_rows(RowVals rv, int lane, float *beta_s, f
     }
     beta_s[lane] = rv.beta;
     L_s[lane] = lg;
+}
+
+// Gated inputs: the state kept in TMEM is S^ with S = sigma S^, sigma the
+// product of the chunk decays Gamma_C since the last rescale, so that most
+// chunks need no pass over the state: sigma folds into the state pass's B
+// tiles (-W and Gamma q rows times sigma_c, decayed K rows over sigma_{c+1}).
+// A chunk whose decay would take log sigma below kRenormLog rescales S^ by
+// sigma_c Gamma_C instead (the epilogue, between the two halves of the
+// state pass) and restarts sigma at 1; so sigma >= e^-27 and the B-tile
+// factors stay below e^27. Every role evaluates this sequence from the same
+// fp32 values with the same operations, so all agree bit for bit.
+constexpr float kRenormLog = -27.f;
+
+__device__ __forceinline__ bool renorm_at(float ls, float lgc) { return ls + lgc < kRenormLog; }
+__device__ __forceinline__ float ls_after(float ls, float lgc)
+{
+    const float x = ls + lgc;
+    return x < kRenormLog ? 0.f : x;
+}
+
+// log Gamma_C of chunk c: the chunk's cumulative log-gate at its last row,
+// by the same loads and the same scan as scan_rows (so it equals the L[kC-1]
+// the prep side computes for that chunk, bit for bit). Whole warp.
+template <class J>
+__device__ __forceinline__ float chunk_lgc(const Params &p, const J &jb, int c, int lane)
+{
+    float lg = load_rows(p, jb, c, lane).lg;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, lg, d);
+        if (lane >= d) lg += y;
+    }
+    return __shfl_sync(0xffffffffu, lg, 31);
 }
 
 struct PrepScratch {
@@ -771,8 +810,9 @@ __device__ __forceinline__ int y_row_p(int g) { return g ? kD : 0; }
 // wait failed or the CTA is aborting.
 __device__ bool phase_b(const Smem &s, const Params &p, uint32_t tbase, uint8_t *gt,
                         const uint8_t *kq, const float *Psrc, int pld, const float *L_s, int c,
-                        int g, int lt, uint32_t bar_id, const float *kw16 = nullptr,
-                        const uint8_t *ksrc = nullptr, uint32_t kblock = kKQBlock)
+                        int g, int lt, uint32_t bar_id, float ls_cur, float ls_next,
+                        const float *kw16 = nullptr, const uint8_t *ksrc = nullptr,
+                        uint32_t kblock = kKQBlock)
 {
     const int lw = lt >> 5, lane = lt & 31, lq = lw & 3, hf = lw >> 2;
     const int nh = p.nh, ct = p.ct;
@@ -789,7 +829,7 @@ __device__ bool phase_b(const Smem &s, const Params &p, uint32_t tbase, uint8_t 
     {
         const int i = lt >> 4, kb4 = (lt >> 2) & 3, q = lt & 3;
         const bool valid = i < ct;
-        const float gr = !valid ? 0.f : (gated ? __expf(L_s[i * nh + nh - 1]) : 1.f);
+        const float gr = !valid ? 0.f : (gated ? __expf(L_s[i * nh + nh - 1] + ls_cur) : 1.f);
         const uint4 u = *(const uint4 *)(kq + (kb4 >> 1) * kKQBlock + sw128_offset(kC + i, (kb4 & 1) * 4 + q));
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
         float f[8];
@@ -807,7 +847,7 @@ __device__ bool phase_b(const Smem &s, const Params &p, uint32_t tbase, uint8_t 
     // row dk, four groups of 4 chunk rows per thread
     {
         const int dk = lt & 127, q0 = (lt >> 7) * 4;
-        const float Lend = L_s[kC - 1];
+        const float Lend = L_s[kC - 1] - ls_next;
         const uint8_t *src = (ksrc ? ksrc : kq) + (dk >> 6) * kblock;
         const int chunk = (dk & 63) >> 3, e = dk & 7;
 #pragma unroll
@@ -833,9 +873,10 @@ __device__ bool phase_b(const Smem &s, const Params &p, uint32_t tbase, uint8_t 
         tmem_wait_ld();
         const int dk = 32 * lq + lane, pos = dk & 31;
         uint8_t *dst = gt + kGX + (dk >> 5) * kXBlock + (pos & 3) * 4;
+        const float nsig = gated ? -__expf(ls_cur) : -1.f;
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-            *(float *)(dst + sw128_offset(16 * hf + j, pos >> 2)) = -__uint_as_float(r[j]);
+            *(float *)(dst + sw128_offset(16 * hf + j, pos >> 2)) = nsig * __uint_as_float(r[j]);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -882,6 +923,18 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
     const uint32_t bar_id = 1 + g;
     uint8_t *gt = s.group(g);
     const bool gated = p.g != nullptr;
+    // gated: log sigma before chunk ls_at (see kRenormLog); advanced over
+    // every chunk, the other group's included, and the group's own last
+    // chunk's log Gamma_C kept so that only the other group's is recomputed
+    float ls = 0.f, lgc_own = 0.f;
+    int ls_at = 0, lgc_own_c = -1;
+    auto advance_ls = [&](int c) {
+        while (ls_at < c) {
+            const float l = (ls_at == lgc_own_c) ? lgc_own : chunk_lgc(p, jb, ls_at, lane);
+            ls = ls_after(ls, l);
+            ++ls_at;
+        }
+    };
 
     if (kSplit) {
         for (int c = g; c < jb.chunks(p); c += 2) {
@@ -896,18 +949,25 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
                 if (c + 2 < jb.chunks(p)) prefetch_kw_rows(p, jb, c + 2, lt);
                 load_kw_rows(p, jb, c, lt, kwv);
             }
+            if (gated) advance_ls(c);
             const bool ok = (lt != 0) || wait_bar(s, kBarFull + st, (c / kNS) & 1, p.status);
             if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) break;
+            const float *Lrec = (const float *)(rec + kRecL);
+            const float lgc = gated ? Lrec[kC - 1] : 0.f, ls_next = ls_after(ls, lgc);
             // (with a key/query prologue the stage's K and Q arrive mapped, from the record)
-            if (!phase_b(s, p, tbase, gt, kq, (const float *)(rec + kRecP), kC,
-                         (const float *)(rec + kRecL), c, g, lt, bar_id, kw_global ? kwv : nullptr,
-                         (J::kWK && !gated) ? rec + kRecKW : nullptr,
+            if (!phase_b(s, p, tbase, gt, kq, (const float *)(rec + kRecP), kC, Lrec, c, g, lt, bar_id, ls,
+                         ls_next, kw_global ? kwv : nullptr, (J::kWK && !gated) ? rec + kRecKW : nullptr,
                          (J::kWK && !gated) ? kKWBlock : kKQBlock))
                 break;
             if (lt == 0) {
+                // the chain read the previous chunk's flag before that chunk's
+                // state pass, which phase_b has waited for
+                s.renorm[g] = (gated && renorm_at(ls, lgc)) ? 1u : 0u;
                 mbar_arrive(&s.bar[kBarReady + g]);
                 mbar_arrive(&s.bar[kBarEmpty + st]);
             }
+            lgc_own = lgc;
+            lgc_own_c = c;
         }
         return;
     }
@@ -918,6 +978,7 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
     for (int c = g; c < jb.chunks(p); c += 2) {
         const int st = c % kNS;
         const uint8_t *kq = s.stage(st);
+        if (gated) advance_ls(c);
         if (lw == 0) {
             scan_rows(rv, lane, w.beta_s, w.L_s);
             rv = load_rows(p, jb, c + 2, lane);          // next chunk of this group
@@ -942,11 +1003,15 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
         fence_proxy_async_smem();
         named_sync(bar_id, kPrepThreads);
         if (lt == 0) mbar_arrive(&s.bar[kBarTb + g]);
-        if (!phase_b(s, p, tbase, gt, kq, w.Ps, kLd, w.L_s, c, g, lt, bar_id)) break;
+        const float lgc = gated ? w.L_s[kC - 1] : 0.f, ls_next = ls_after(ls, lgc);
+        if (!phase_b(s, p, tbase, gt, kq, w.Ps, kLd, w.L_s, c, g, lt, bar_id, ls, ls_next)) break;
         if (lt == 0) {
+            s.renorm[g] = (gated && renorm_at(ls, lgc)) ? 1u : 0u;
             mbar_arrive(&s.bar[kBarReady + g]);
             mbar_arrive(&s.bar[kBarEmpty + st]);
         }
+        lgc_own = lgc;
+        lgc_own_c = c;
     }
 }
 
@@ -988,20 +1053,19 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, const J
     // waits for the chain's commits itself and arrives once per warp on the
     // barriers the chain waits for, and it releases a chunk's O buffers
     // before storing the outputs from registers.
+    // Gated: the stored state is S^ = S / sigma (see kRenormLog); chunks
+    // that rescale it are handled here, and h_final is sigma S^.
     bool failed = false;
+    float ls = 0.f;
+    uint32_t n_renorm = 0;
     for (int c = 0; c < jb.chunks(p); ++c) {
         const int g = c & 1, t0 = c * p.ct;
-        if (gated) {
-            // Gamma_C: product of the chunk's token gates (log domain, clamped)
-            float lg = 0.f;
-            if (lane < p.ct && t0 + lane < jb.tokens(p)) {
-                const float x = __bfloat162float(p.g[tok_row(p, jb, t0 + lane)]);
-                lg = J::kPro ? pro_log_gate(x, p.prologue) : fmaxf(logf(x), -80.f);
-            }
-#pragma unroll
-            for (int d = 16; d > 0; d >>= 1) lg += __shfl_xor_sync(0xffffffffu, lg, d);
-            const float gC = __expf(lg);
-            if (!warp_wait(s, kBarM1, c & 1, p.status)) { failed = true; break; }
+        const float lgc = gated ? chunk_lgc(p, jb, c, lane) : 0.f;
+        if (gated && renorm_at(ls, lgc)) {
+            // S^ <- sigma_c Gamma_C S^ between the chunk's two state-pass halves
+            const float gC = __expf(ls + lgc);
+            if (!warp_wait(s, kBarM1, n_renorm & 1, p.status)) { failed = true; break; }
+            ++n_renorm;
             tc_fence_after();
             uint32_t r[32];
             for (int c0 = 0; c0 < kD; c0 += 32) {
@@ -1016,6 +1080,7 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, const J
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.bar[kBarScaled]);
         }
+        ls = ls_after(ls, lgc);
         if (!warp_wait(s, kBarM2 + g, (c >> 1) & 1, p.status)) { failed = true; break; }
         tc_fence_after();
         uint32_t ra[16], rb[16];
@@ -1039,12 +1104,13 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, const J
             if (i < p.ct && t0 + i < jb.tokens(p)) store_out(oc, (size_t)i * tok_stride, __uint_as_float(ra[i]));
     }
     if (!failed && jb.ok() && p.h_final) {
+        const float sig = gated ? __expf(ls) : 1.f;
         uint32_t r[32];
         for (int c0 = 0; c0 < kD; c0 += 32) {
             tmem_ld32(trow + kColS + c0, r);
             tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) p.h_final[(bh * kD + c0 + j) * kD + tid] = __uint_as_float(r[j]);
+            for (int j = 0; j < 32; ++j) p.h_final[(bh * kD + c0 + j) * kD + tid] = sig * __uint_as_float(r[j]);
         }
     }
 }
@@ -1061,6 +1127,7 @@ __device__ __forceinline__ void state_pass_cta(const CUtensorMap &tm_k, const CU
     s.bar = (uint64_t *)(s.base + Lay::kOffBar);
     s.tmem_slot = (uint32_t *)(s.bar + kNumBars);
     s.abort = s.tmem_slot + 1;
+    s.renorm = s.tmem_slot + 2;
     s.stage_bytes = Lay::kStage;
     s.group_off = Lay::kOffGroup;
     s.group_bytes = Lay::kGroup;
@@ -1116,124 +1183,238 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     state_pass_cta<TOut, kSplit, false, kPacked, kPro, kWK>(tm_k, tm_v, tm_q, p, blockIdx.x);
 }
 
-// ------------------------------------------------------------------ prep kernel
-// Prep of one chunk by a group of 256 threads (`lt` = 0..255; warps whose
-// index mod 4 is lt / 32 mod 4, for TMEM lane access): TMA its K and Q tiles
-// into `stage` (rows TMA never writes must already be zero), Gram MMA into
-// TMEM columns `gq_col`, phase_a with the T tiles going straight to the
-// chunk's record, then P, beta and L. `bars` = [loads, Gram MMA], used at
-// phase `parity`. Returns false, uniformly over the group, after a timeout
-// (the group's loads and MMA drained first).
-template <class J>
-__device__ bool prep_chunk(const Params &p, const CUtensorMap *tk, const CUtensorMap *tq,
-                           const CUtensorMap *tkw, uint8_t *kwt, uint8_t *stage, const PrepScratch &w, uint64_t *bars, uint32_t parity,
-                           volatile uint32_t *abort, uint32_t tbase, uint32_t gq_col, int lt,
-                           uint32_t bar_id, const J &jb, int c)
+// ------------------------------------------------------------------ chunk prep (split and cooperative modes)
+// One prep group = 256 threads (`lt` 0..255; warps whose index mod 4 is
+// lt / 32 mod 4, for TMEM lane access) working through its share of the
+// chunks (every `stride`-th index of the chunk-major order from `first`),
+// two deep: while the group solves chunk k (phase A, the T tiles straight
+// into the chunk's record), the Gram MMA of chunk k + 1 runs and the K, Q
+// tiles of chunk k + 2 are in flight. Per group: two stages (KQ tiles, and
+// K~ tiles with write keys; rows TMA never writes are zero), two 32-column
+// Gram accumulators, four mbarriers (loads into stage 0 / 1, Gram MMA into
+// accumulator 0 / 1); chunk k uses stage and accumulator k % 2, as their
+// (k / 2)-th use.
+struct PrepGroup {
+    uint8_t *stage;            // stage 0; stage 1 follows at pg_stage_bytes
+    uint64_t *bar;             // [0, 1] stage loads, [2, 3] Gram MMAs
+    uint32_t tcol;             // TMEM address of accumulator 0 (accumulator 1: + 32 columns)
+    PrepScratch w;
+    uint32_t bar_id;           // named barrier of the group
+    int lt;
+};
+constexpr uint32_t kPGKQ = 2 * kKQBlock;   // KQ tiles of a stage (16 KB)
+__host__ __device__ constexpr uint32_t pg_stage_bytes(bool wk) { return wk ? kPGKQ + 2 * kKWBlock : kPGKQ; }
+
+// The next chunk index at or after `idx` in a group's share that holds a
+// chunk (packed calls skip chunks past a sequence's end, and sequences with
+// bad offsets); `total` when none is left.
+template <bool kPacked, bool kPro, bool kWK>
+__device__ __forceinline__ int next_chunk(const Params &p, int idx, int stride, int total)
 {
-    const int lane = lt & 31, ct = p.ct, R = ct * p.nh;
-    if (lt == 0) {
-        mbar_arrive_expect_tx(&bars[0], 256u * R + 256u * ct + (J::kWK ? 256u * R : 0u));
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-            const int t0 = jb.first() + c * ct;
-            tma_load_5d(stage + kb * kKQBlock, tk, &bars[0], kb * 64, 0, jb.h, t0, jb.row_b());
-            tma_load_4d(stage + kb * kKQBlock + kC * 128, tq, &bars[0], kb * 64, jb.h, t0, jb.row_b());
-            if (J::kWK) tma_load_5d(kwt + kb * kKWBlock, tkw, &bars[0], kb * 64, 0, jb.h, t0, jb.row_b());
+    if (kPacked) {
+        for (; idx < total; idx += stride) {
+            const int c = idx / p.bh_count;
+            if (c < make_job<kPacked, kPro, kWK>(p, idx - c * p.bh_count).chunks(p)) break;
         }
     }
-    if (lt < 32) scan_rows(load_rows(p, jb, c, lane), lane, w.beta_s, w.L_s);
-    if (J::kPro) {   // the prologue on the tiles, before the Gram MMA reads them
-        bool landed = (lt != 0) || mbar_wait(&bars[0], parity, kWaitTries, abort);
-        if (group_any(bar_id, kPrepThreads, !landed || *abort)) {
-            if (lt == 0) {
-                flag_error(p.status, abort, kDevTimeout);
-                uint32_t no_abort = 0;   // the loads may still be in flight
-                mbar_wait(&bars[0], parity, kWaitTries, &no_abort);
-            }
-            return false;
-        }
-        normalise_rows(stage, R, ct, p.prologue, lt, kPrepThreads);
-        fence_proxy_async_smem();
-        named_sync(bar_id, kPrepThreads);
-        if (kq_in_record(p.prologue)) {   // the mapped rows, for the state pass
-            uint8_t *dst = p.rec + rec_index(p, jb, c) * p.rec_stride + kRecKQ;
-            for (uint32_t i = lt * 16; i < kRecKQBytes; i += kPrepThreads * 16) {
-                const uint32_t kb = i / kRecKQBlock, off = i - kb * kRecKQBlock;
-                *(uint4 *)(dst + i) = *(const uint4 *)(stage + kb * kKQBlock + off);
-            }
-        }
-    }
-    bool ok = true;
-    if (lt == 0) {
-        bool issued = false;
-        ok = mbar_wait(&bars[0], parity, kWaitTries, abort);
-        if (ok) {
-            tc_fence_after();
-            if (J::kWK)
-                issue_gram_wk(tbase + gq_col, smem_addr(stage), smem_addr(kwt));
-            else
-                issue_gram(tbase + gq_col, smem_addr(stage));
-            mma_commit(&bars[1]);
-            issued = true;
-            ok = mbar_wait(&bars[1], parity, kWaitTries, abort);
-        }
-        if (!ok) {
-            flag_error(p.status, abort, kDevTimeout);
-            // the loads or the MMA may still be in flight: let them finish
-            // (bounded) before shared memory and TMEM are released
-            uint32_t no_abort = 0;
-            mbar_wait(&bars[0], parity, kWaitTries, &no_abort);
-            if (issued) mbar_wait(&bars[1], parity, kWaitTries, &no_abort);
-        }
-    }
-    if (group_any(bar_id, kPrepThreads, !ok || *abort)) return false;
-    tc_fence_after();
-    uint8_t *rec = p.rec + rec_index(p, jb, c) * p.rec_stride;
-    if (J::kWK && p.g == nullptr)   // the K~ tile, for the state pass (see kRecKW)
-        for (uint32_t i = lt * 16; i < 2 * kKWBlock; i += kPrepThreads * 16)
-            *(uint4 *)(rec + kRecKW + i) = *(const uint4 *)(kwt + i);
-    phase_a(w, tbase, gq_col, rec + kRecT, lt, p.nh, ct, p.g != nullptr, bar_id);
-    float *rp = (float *)(rec + kRecP);
-    for (int i = lt; i < kNQ * kC; i += kPrepThreads) rp[i] = w.Ps[(i >> 5) * kLd + (i & 31)];
-    if (lt < kC) {
-        ((float *)(rec + kRecBeta))[lt] = w.beta_s[lt];
-        ((float *)(rec + kRecL))[lt] = w.L_s[lt];
-    }
-    // the record is complete and the scratch free for the next chunk
-    tc_fence_before();
-    named_sync(bar_id, kPrepThreads);
-    return true;
+    return idx < total ? idx : total;
 }
 
-// Phase A for every chunk of every head in parallel, one chunk per CTA.
-constexpr int kPrepKThreads = kPrepThreads;
-constexpr uint32_t kPKKW = 2 * kKQBlock;                            // K~ tile (write keys)
-constexpr uint32_t kPKScratch = kPKKW + 2 * kKWBlock;               // after the KQ and K~ tiles
-constexpr uint32_t kPKBar = kPKScratch + kPrepScratch;
-constexpr uint32_t kPKSmem = kPKBar + 2 * 8 + 16 + 1024;
-constexpr uint32_t kPKTmemCols = 32;
+// K and Q tiles (and K~ tiles) of chunk c of job jb into `stage`.
+template <class J>
+__device__ __forceinline__ void prep_issue_load(const Params &p, const CUtensorMap *tk, const CUtensorMap *tq,
+                                                const CUtensorMap *tkw, uint8_t *stage, uint64_t *bar,
+                                                const J &jb, int c)
+{
+    const int ct = p.ct, R = ct * p.nh, t0 = jb.first() + c * ct;
+    mbar_arrive_expect_tx(bar, 256u * R + 256u * ct + (J::kWK ? 256u * R : 0u));
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb) {
+        tma_load_5d(stage + kb * kKQBlock, tk, bar, kb * 64, 0, jb.h, t0, jb.row_b());
+        tma_load_4d(stage + kb * kKQBlock + kC * 128, tq, bar, kb * 64, jb.h, t0, jb.row_b());
+        if (J::kWK) tma_load_5d(stage + kPGKQ + kb * kKWBlock, tkw, bar, kb * 64, 0, jb.h, t0, jb.row_b());
+    }
+}
+
+template <bool kPacked, bool kPro, bool kWK>
+__device__ void prep_loop(const Params &p, const CUtensorMap *tk, const CUtensorMap *tq, const CUtensorMap *tkw,
+                          const PrepGroup &G, volatile uint32_t *abort, int first, int stride, bool publish)
+{
+    using J = Job<kPacked, kPro, kWK>;
+    constexpr uint32_t kSt = pg_stage_bytes(kWK);
+    const int lt = G.lt, lane = lt & 31, ct = p.ct, R = ct * p.nh;
+    const int total = p.n_chunks * p.bh_count;
+    const bool gated = p.g != nullptr;
+    // group work on a landed stage before its Gram MMA: the prologue's row
+    // maps (and the mapped rows into the record), the K~ tile into the record
+    constexpr bool kStageWork = kPro || kWK;
+    // lt == 0: loads and MMAs issued and not yet waited for (drained on a timeout)
+    bool ld_out[2] = {false, false}, mma_out[2] = {false, false};
+    uint32_t ld_par[2] = {0, 0}, mma_par[2] = {0, 0};
+
+    auto job_of = [&](int idx, int &c) {
+        c = idx / p.bh_count;
+        return make_job<kPacked, kPro, kWK>(p, idx - c * p.bh_count);
+    };
+    auto issue_load = [&](int idx, int st, uint32_t par) {
+        int c;
+        const J jb = job_of(idx, c);
+        prep_issue_load(p, tk, tq, tkw, G.stage + st * kSt, &G.bar[st], jb, c);
+        ld_out[st] = true;
+        ld_par[st] = par;
+    };
+    // Gram MMA of local chunk k (index idx): wait for its stage, do the
+    // stage work, issue. A failed wait sets the abort flag, which every
+    // later group_any of the group sees.
+    auto gram = [&](int k, int idx) {
+        const int st = k & 1;
+        const uint32_t par = (k >> 1) & 1;
+        uint8_t *stage = G.stage + st * kSt;
+        bool ok = true;
+        if (kStageWork) {
+            ok = (lt != 0) || mbar_wait(&G.bar[st], par, kWaitTries, abort);
+            if (lt == 0) {
+                if (ok) ld_out[st] = false;
+                else flag_error(p.status, abort, kDevTimeout);
+            }
+            if (group_any(G.bar_id, kPrepThreads, !ok || *abort)) return false;
+            int c;
+            const J jb = job_of(idx, c);
+            uint8_t *rec = p.rec + rec_index(p, jb, c) * p.rec_stride;
+            if (kPro) {
+                normalise_rows(stage, R, ct, p.prologue, lt, kPrepThreads);
+                fence_proxy_async_smem();
+                named_sync(G.bar_id, kPrepThreads);
+                if (kq_in_record(p.prologue))   // the mapped rows, for the state pass
+                    for (uint32_t i = lt * 16; i < kRecKQBytes; i += kPrepThreads * 16) {
+                        const uint32_t kb = i / kRecKQBlock, off = i - kb * kRecKQBlock;
+                        *(uint4 *)(rec + kRecKQ + i) = *(const uint4 *)(stage + kb * kKQBlock + off);
+                    }
+            }
+            if (kWK && !gated)   // the K~ tile, for the state pass (see kRecKW)
+                for (uint32_t i = lt * 16; i < 2 * kKWBlock; i += kPrepThreads * 16)
+                    *(uint4 *)(rec + kRecKW + i) = *(const uint4 *)(stage + kPGKQ + i);
+        }
+        if (lt == 0) {
+            if (!kStageWork) {
+                ok = mbar_wait(&G.bar[st], par, kWaitTries, abort);
+                if (ok) ld_out[st] = false;
+                else flag_error(p.status, abort, kDevTimeout);
+            }
+            if (ok) {
+                tc_fence_after();
+                if (kWK)
+                    issue_gram_wk(G.tcol + st * 32, smem_addr(stage), smem_addr(stage + kPGKQ));
+                else
+                    issue_gram(G.tcol + st * 32, smem_addr(stage));
+                mma_commit(&G.bar[2 + st]);
+                mma_out[st] = true;
+                mma_par[st] = par;
+            }
+        }
+        return true;
+    };
+
+    int idx = next_chunk<kPacked, kPro, kWK>(p, first, stride, total);
+    bool ok = idx < total;
+    int nxt = ok ? next_chunk<kPacked, kPro, kWK>(p, idx + stride, stride, total) : total;
+    if (ok && lt == 0) {
+        issue_load(idx, 0, 0);
+        if (nxt < total) issue_load(nxt, 1, 0);
+    }
+    RowVals rv{0.f, 0.f};
+    if (ok && lt < 32) {
+        int c;
+        const J jb = job_of(idx, c);
+        rv = load_rows(p, jb, c, lane);
+    }
+    if (ok) ok = gram(0, idx);
+    for (int k = 0; ok; ++k) {
+        const int st = k & 1;
+        // the Gram MMA of chunk k is done
+        bool okw = true;
+        if (lt == 0) {
+            okw = mbar_wait(&G.bar[2 + st], (k >> 1) & 1, kWaitTries, abort);
+            if (okw) mma_out[st] = false;
+            else flag_error(p.status, abort, kDevTimeout);
+        }
+        if (group_any(G.bar_id, kPrepThreads, !okw || *abort)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        // stage st is free: the tiles of chunk k + 2 go into it
+        const int nn = nxt < total ? next_chunk<kPacked, kPro, kWK>(p, nxt + stride, stride, total) : total;
+        if (lt == 0 && nn < total) issue_load(nn, st, ((k + 2) >> 1) & 1);
+        // the Gram MMA of chunk k + 1 (its tiles were requested one chunk ago)
+        if (nxt < total && !(ok = gram(k + 1, nxt))) break;
+        // betas and cumulative log-gates of chunk k; those of chunk k + 1 in flight
+        if (lt < 32) {
+            scan_rows(rv, lane, G.w.beta_s, G.w.L_s);
+            rv = RowVals{0.f, 0.f};
+            if (nxt < total) {
+                int c;
+                const J jb = job_of(nxt, c);
+                rv = load_rows(p, jb, c, lane);
+            }
+        }
+        named_sync(G.bar_id, kPrepThreads);
+        int c;
+        const J jb = job_of(idx, c);
+        uint8_t *rec = p.rec + rec_index(p, jb, c) * p.rec_stride;
+        phase_a(G.w, G.tcol, st * 32, rec + kRecT, lt, p.nh, ct, gated, G.bar_id);
+        float *rp = (float *)(rec + kRecP);
+        for (int i = lt; i < kNQ * kC; i += kPrepThreads) rp[i] = G.w.Ps[(i >> 5) * kLd + (i & 31)];
+        if (lt < kC) {
+            ((float *)(rec + kRecBeta))[lt] = G.w.beta_s[lt];
+            ((float *)(rec + kRecL))[lt] = G.w.L_s[lt];
+        }
+        // the record is complete, the scratch and accumulator st free
+        tc_fence_before();
+        named_sync(G.bar_id, kPrepThreads);
+        if (publish && lt == 0 && !(p.withhold_first && idx == 0)) {
+            __threadfence();
+            flag_publish(p.flags + rec_index(p, jb, c), 1u);
+        }
+        if (nxt >= total) break;
+        idx = nxt;
+        nxt = nn;
+    }
+    if (lt == 0) {   // after a timeout: let what is in flight finish before smem and TMEM go
+        uint32_t no_abort = 0;
+        for (int st = 0; st < 2; ++st) {
+            if (ld_out[st]) mbar_wait(&G.bar[st], ld_par[st], kWaitTries, &no_abort);
+            if (mma_out[st]) mbar_wait(&G.bar[2 + st], mma_par[st], kWaitTries, &no_abort);
+        }
+    }
+}
+
+// Split mode: every chunk of every head, by persistent CTAs of one prep
+// group each (several per SM).
+constexpr uint32_t pk_smem(bool wk)
+{
+    return 2 * pg_stage_bytes(wk) + kPrepScratch + 4 * 8 + 16 + 1024;
+}
+constexpr uint32_t kPKTmemCols = 64;
 
 template <bool kPacked, bool kPro, bool kWK = false>
-__global__ void __launch_bounds__(kPrepKThreads, 4)
+__global__ void __launch_bounds__(kPrepThreads, 4)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_kw, const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
+    constexpr uint32_t kSt = pg_stage_bytes(kWK);
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint64_t *bar = (uint64_t *)(base + kPKBar);                     // [0] loads, [1] Gram MMA
-    uint32_t *tmem_slot = (uint32_t *)(bar + 2);
+    uint64_t *bar = (uint64_t *)(base + 2 * kSt + kPrepScratch);
+    uint32_t *tmem_slot = (uint32_t *)(bar + 4);
     volatile uint32_t *abort = tmem_slot + 1;
     const int lt = threadIdx.x, warp = lt >> 5;
-    const int c = blockIdx.x % p.n_chunks;
-    const Job<kPacked, kPro, kWK> jb = make_job<kPacked, kPro, kWK>(p, blockIdx.x / p.n_chunks);
-    if (c >= jb.chunks(p)) return;   // past the sequence's end (packed calls), or a bad sequence
 
     // rows TMA does not write (padding, queries beyond the chunk) stay zero
-    for (uint32_t i = lt * 16; i < kPKScratch; i += kPrepKThreads * 16)
+    for (uint32_t i = lt * 16; i < 2 * kSt; i += kPrepThreads * 16)
         *(uint4 *)(base + i) = make_uint4(0, 0, 0, 0);
     if (lt == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
         *abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tm_k);
@@ -1246,8 +1427,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
-    prep_chunk(p, &tm_k, &tm_q, &tm_kw, base + kPKKW, base, prep_scratch(base + kPKScratch), bar, 0, abort, tbase,
-               0, lt, 1, jb, c);
+    const PrepGroup G{base, bar, tbase, prep_scratch(base + 2 * kSt), 1, lt};
+    prep_loop<kPacked, kPro, kWK>(p, &tm_k, &tm_q, &tm_kw, G, abort, blockIdx.x, gridDim.x, false);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, kPKTmemCols);
@@ -1255,10 +1436,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 
 // ------------------------------------------------------------------ cooperative mode
 // One launch: CTAs 0 .. B*H-1 run the state pass (split mode), the others
-// prepare the chunks in chunk-major order, two chunks at a time per CTA
-// (warps 0-7 and 8-15), and publish each record through its flag. The
-// state pass waits for a record's flag (bounded) before loading it. All CTAs
-// are resident together (cooperative launch), and no prep CTA waits on a
+// prepare the chunks in chunk-major order, two prep groups per CTA (warps
+// 0-7 and 8-15), and publish each record through its flag. The state pass
+// waits for a record's flag (bounded) before loading it. All CTAs are
+// resident together (cooperative launch), and no prep CTA waits on a
 // state-pass CTA. The host zeroes the flags before the launch.
 constexpr uint32_t kCoopScratch = (kPrepScratch + 127) & ~127u;
 
@@ -1267,27 +1448,25 @@ __device__ void prep_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const
                          const Params &p, int pcta, int n_pcta)
 {
     extern __shared__ uint8_t smem_raw[];
+    constexpr uint32_t kSt = pg_stage_bytes(kWK);
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    constexpr uint32_t kStg = 2 * kKQBlock;                          // 16 KB per group
-    constexpr uint32_t kKWT = 2 * kKWBlock;                          // 8 KB K~ tile per group
-    uint8_t *kwt = base + 2 * kStg;
-    uint8_t *scr = kwt + 2 * kKWT;
-    uint64_t *bar = (uint64_t *)(scr + 2 * kCoopScratch);            // [group][loads, MMA]
-    uint32_t *tmem_slot = (uint32_t *)(bar + 4);
+    uint8_t *scr = base + 4 * kSt;                                   // [group 0 stages | group 1 stages]
+    uint64_t *bar = (uint64_t *)(scr + 2 * kCoopScratch);            // [group][4]
+    uint32_t *tmem_slot = (uint32_t *)(bar + 8);
     volatile uint32_t *abort = tmem_slot + 1;
     const int warp = threadIdx.x >> 5;
 
-    for (uint32_t i = threadIdx.x * 16; i < 2 * kStg + 2 * kKWT; i += kThreads * 16)
+    for (uint32_t i = threadIdx.x * 16; i < 4 * kSt; i += kThreads * 16)
         *(uint4 *)(base + i) = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
+        for (int i = 0; i < 8; ++i) mbar_init(&bar[i], 1);
         *abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_q);
         if (kWK) tma_prefetch_desc(&tm_kw);
     }
-    if (warp == 0) tmem_alloc(tmem_slot, 64);
+    if (warp == 0) tmem_alloc(tmem_slot, 128);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -1296,26 +1475,307 @@ __device__ void prep_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const
 
     if (warp < 16) {
         const int gi = warp >> 3, lt = threadIdx.x - gi * kPrepThreads;
-        const int total = p.n_chunks * p.bh_count;
-        const PrepScratch w = prep_scratch(scr + gi * kCoopScratch);
-        uint32_t k = 0;   // chunks prepared by this group: the phase of its barriers
-        for (int idx = pcta * 2 + gi; idx < total; idx += n_pcta * 2) {
-            const int c = idx / p.bh_count;
-            const Job<kPacked, kPro, kWK> jb = make_job<kPacked, kPro, kWK>(p, idx - c * p.bh_count);
-            if (c >= jb.chunks(p)) continue;   // past the sequence's end (packed calls): nobody waits for it
-            if (!prep_chunk(p, &tm_k, &tm_q, &tm_kw, kwt + gi * kKWT, base + gi * kStg, w, bar + 2 * gi, k & 1,
-                            abort, tbase, gi * 32, lt, 1 + gi, jb, c))
-                break;
-            ++k;
-            if (lt == 0 && !(p.withhold_first && idx == 0)) {
-                __threadfence();
-                flag_publish(p.flags + rec_index(p, jb, c), 1u);
-            }
-        }
+        const PrepGroup G{base + gi * 2 * kSt, bar + 4 * gi, tbase + gi * 64,
+                          prep_scratch(scr + gi * kCoopScratch), (uint32_t)(1 + gi), lt};
+        prep_loop<kPacked, kPro, kWK>(p, &tm_k, &tm_q, &tm_kw, G, abort, pcta * 2 + gi, n_pcta * 2, true);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, 64);
+    if (warp == 0) tmem_dealloc(tbase, 128);
+}
+
+// ------------------------------------------------------------------ warp-per-chunk prep
+// The prep of the plain path (no prologue, no write keys) in the split and
+// cooperative modes: each consumer warp solves whole chunks on its own
+// (lane i = extended row i), so nothing waits on a group barrier, and
+// producer threads keep the loads and Gram MMAs ahead of them.
+//  * producer thread (one per 8 consumer warps, 4 slots): TMA of the
+//    chunk's K and Q tiles into the slot's stage, then one MMA
+//    D = [K-rows at the consumer's TMEM lane quarter] x [K; Q]^T (M = 128,
+//    N = 48: columns 0-31 the Gram row k_i.k_s, columns 32-47 k_i.q_t); the
+//    A operand's start is moved back by 32 rows per quarter so that the K
+//    rows land in the lanes the consumer warp may read (the other lanes get
+//    rows of neighbouring shared memory and are never read).
+//  * consumer warp: the rows' betas and log-gates, G^T (strictly lower
+//    part, scaled) into its scratch, the readout weights P straight into the
+//    record, then row i of T = (I + G)^-1 by back-substitution (row i needs
+//    only G: T[i][j] = -sum_{s>j} T[i][s] G[s][j]), written as the bf16 hi/lo
+//    tiles of T diag(beta) (and T diag(beta Gamma)) in the record's
+//    swizzled layout; in the cooperative mode it publishes the record.
+// Slot s of a producer holds local chunks k = s, s + 4, ... (its (k / 4)-th
+// use), with mbarriers "loaded" (TMA bytes) and "free" (the consumer has
+// read the accumulator: stage and TMEM columns reusable); the Gram MMA of
+// chunk k completes on the mbarrier of its consumer warp k % 8, whose j-th
+// phase is that warp's j-th chunk. (A per-slot completion barrier would
+// let a warp that finished its chunk on a slot wait for its next one there
+// while another warp's chunk still stands in between: two phases ahead,
+// which a parity wait cannot tell from the phase before.)
+constexpr int kWCons = 16;                       // consumer warps (8 per producer)
+constexpr int kWConsPerProd = 8;
+constexpr int kWSlots = 4;                       // slots per producer
+constexpr int kWLg = 36;                         // G^T row stride (floats; 16-byte aligned rows)
+constexpr uint32_t kWScr = 5120;                 // per consumer warp: G^T [32][36], L [32], beta [32]
+constexpr uint32_t kWStage = 2 * kKQBlock;       // 16 KB: the KQ tiles
+constexpr uint32_t kWStages = 8 * kWScr;         // stages after consumers 0-7's scratch (>= 12 KB lead)
+constexpr uint32_t kWScr2 = kWStages + 2 * kWSlots * kWStage;   // consumers 8-15 (>= 8 KB tail)
+constexpr uint32_t kWBar = kWScr2 + 8 * kWScr;
+constexpr int kWBars = 2 * kWSlots + kWConsPerProd;   // per producer: [slot][loaded, free], [consumer] Gram done
+constexpr uint32_t kWSmem = kWBar + 2 * kWBars * 8 + 16 + 1024;
+static_assert(kWStages % 1024 == 0 && kWStages >= 3 * 4096, "stage alignment and A-shift lead");
+// the M = 128 A operand of the last stage's second block (quarter 0) reads 16 KB from its start
+static_assert(kWStages + (2 * kWSlots - 1) * kWStage + kKQBlock + 16 * 1024 <= kWBar, "A-operand tail");
+
+static_assert(kWSmem <= smem_bytes<true>(), "the warp prep fits the cooperative kernel's shared memory");
+
+__device__ __forceinline__ uint8_t *wprep_scratch(uint8_t *base, int w)
+{
+    return base + (w < 8 ? w * kWScr : kWScr2 + (w - 8) * kWScr);
+}
+
+// The chunk-index stream of producer `pr`: every (2 n_pcta)-th chunk from
+// 2 pcta + pr, skipping chunks that do not exist (packed calls).
+template <bool kPacked>
+__device__ __forceinline__ int wstream_next(const Params &p, int idx, int stride, int total)
+{
+    return next_chunk<kPacked, false, false>(p, idx, stride, total);
+}
+
+template <bool kPacked>
+__device__ void wprep_producer(const Params &p, const CUtensorMap *tk, const CUtensorMap *tq, uint8_t *base,
+                               uint64_t *bar, uint32_t tcol, int pr, int first, int stride, volatile uint32_t *abort)
+{
+    using J = Job<kPacked, false, false>;
+    const int total = p.n_chunks * p.bh_count;
+    constexpr int kLag = 2;   // the Gram MMA of chunk k is issued with the loads of chunk k + kLag
+    const uint32_t idesc = idesc_bf16(128, kC + kNQ, false, false);
+    bool ok = true;
+    int issued_ld = 0, issued_mma = 0;   // chunks whose loads / MMAs were issued
+    auto stage = [&](int k) { return base + kWStages + (pr * kWSlots + (k & (kWSlots - 1))) * kWStage; };
+    auto mma = [&](int k) {
+        const int sl = k & (kWSlots - 1);
+        if (!mbar_wait(&bar[sl * 2 + 0], (k >> 2) & 1, kWaitTries, abort)) return false;
+        tc_fence_after();
+        const int q = (pr * kWConsPerProd + (k & (kWConsPerProd - 1))) & 3;   // consumer warp's lane quarter
+        const uint32_t st = smem_addr(stage(k));
+        const uint32_t d = tcol + sl * 64;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kKQBlock + (kk & 3) * 32;
+            mma_ss(d, sdesc_sw128(st + off - 4096u * q, 16, 1024), sdesc_sw128(st + off, 16, 1024), idesc, kk > 0);
+        }
+        mma_commit(&bar[2 * kWSlots + (k & (kWConsPerProd - 1))]);
+        return true;
+    };
+    int idx = wstream_next<kPacked>(p, first, stride, total);
+    for (int k = 0; idx < total && ok; ++k) {
+        const int sl = k & (kWSlots - 1);
+        // the slot's previous chunk (k - 4): its consumer has read the accumulator
+        if (k >= kWSlots && !(ok = mbar_wait(&bar[sl * 2 + 1], ((k >> 2) - 1) & 1, kWaitTries, abort))) break;
+        const int c = idx / p.bh_count;
+        const J jb = make_job<kPacked, false, false>(p, idx - c * p.bh_count);
+        const int ct = p.ct, R = ct * p.nh, t0 = jb.first() + c * ct;
+        uint64_t *lb = &bar[sl * 2 + 0];
+        uint8_t *stg = stage(k);
+        mbar_arrive_expect_tx(lb, 256u * R + 256u * ct);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+            tma_load_5d(stg + kb * kKQBlock, tk, lb, kb * 64, 0, jb.h, t0, jb.row_b());
+            tma_load_4d(stg + kb * kKQBlock + kC * 128, tq, lb, kb * 64, jb.h, t0, jb.row_b());
+        }
+        issued_ld = k + 1;
+        if (k >= kLag) {
+            if (!(ok = mma(k - kLag))) break;
+            issued_mma = k - kLag + 1;
+        }
+        idx = wstream_next<kPacked>(p, idx + stride, stride, total);
+    }
+    for (int k = issued_mma; ok && k < issued_ld; ++k) {
+        if (!(ok = mma(k))) break;
+        issued_mma = k + 1;
+    }
+    if (!ok) {   // a wait expired: record it, let what was issued finish before smem and TMEM go
+        flag_error(p.status, abort, kDevTimeout);
+        uint32_t no_abort = 0;
+        for (int k = issued_mma; k < issued_ld; ++k)   // loads without their MMA
+            mbar_wait(&bar[(k & (kWSlots - 1)) * 2 + 0], (k >> 2) & 1, kWaitTries, &no_abort);
+        // the last MMA of each consumer (its phase is the barrier's latest)
+        for (int k = issued_mma > kWConsPerProd ? issued_mma - kWConsPerProd : 0; k < issued_mma; ++k)
+            mbar_wait(&bar[2 * kWSlots + (k & (kWConsPerProd - 1))], (k >> 3) & 1, kWaitTries, &no_abort);
+    }
+}
+
+template <bool kPacked>
+__device__ void wprep_consumer(const Params &p, uint8_t *scr, uint64_t *bar, uint32_t tcol, int w, int first,
+                               int stride, bool publish, volatile uint32_t *abort)
+{
+    using J = Job<kPacked, false, false>;
+    const int lane = threadIdx.x & 31, q = w & 3, lc = w & (kWConsPerProd - 1);
+    const int total = p.n_chunks * p.bh_count, nh = p.nh, ct = p.ct;
+    const bool gated = p.g != nullptr;
+    float *Gt = (float *)scr, *Ls = Gt + 32 * kWLg, *Bs = Ls + 32;
+    int idx = wstream_next<kPacked>(p, first, stride, total);
+    for (int k = 0; k < lc && idx < total; ++k) idx = wstream_next<kPacked>(p, idx + stride, stride, total);
+    for (int k = lc; idx < total; k += kWConsPerProd) {
+        const int sl = k & (kWSlots - 1);
+        const int c = idx / p.bh_count;
+        const J jb = make_job<kPacked, false, false>(p, idx - c * p.bh_count);
+        const RowVals rv = load_rows(p, jb, c, lane);
+        bool ok = true;
+        if (lane == 0) {
+            ok = mbar_wait(&bar[2 * kWSlots + lc], (k >> 3) & 1, kWaitTries, abort);
+            if (!ok) flag_error(p.status, abort, kDevTimeout);
+        }
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) || *abort) break;
+        tc_fence_after();
+        uint32_t gr[32], pt[16];
+        const uint32_t ta = tcol + sl * 64 + ((uint32_t)(32 * q) << 16);
+        tmem_ld16(ta, *reinterpret_cast<uint32_t(*)[16]>(&gr[0]));
+        tmem_ld16(ta + 16, *reinterpret_cast<uint32_t(*)[16]>(&gr[16]));
+        tmem_ld16(ta + 32, pt);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[sl * 2 + 1]);   // accumulator read: the slot may be reused
+        // betas and cumulative log-gates (lane = row), as scan_rows computes them
+        float L = rv.lg;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, L, d);
+            if (lane >= d) L += y;
+        }
+        Ls[lane] = L;
+        Bs[lane] = rv.beta;
+        __syncwarp();
+        uint8_t *rec = p.rec + rec_index(p, jb, c) * p.rec_stride;
+        // G^T[j][i] = G[i][j] = beta_i (k_i.k_j) E_ij for j < i, 0 otherwise
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            float gv = 0.f;
+            if (j < lane) {
+                gv = rv.beta * __uint_as_float(gr[j]);
+                if (gated) gv *= __expf(L - Ls[j]);
+            }
+            Gt[j * kWLg + lane] = gv;
+        }
+        // readout weights P[t][s] (lane = s): (q_t.k_s) E_{r(t) s} for s <= r(t), the token's last row
+        float *rp = (float *)(rec + kRecP);
+#pragma unroll
+        for (int t = 0; t < kNQ; ++t) {
+            const int rr = t * nh + nh - 1;
+            float x = 0.f;
+            if (t < ct && lane <= rr) {
+                x = __uint_as_float(pt[t]);
+                if (gated) x *= __expf(Ls[rr] - L);
+            }
+            rp[t * kC + lane] = x;
+        }
+        ((float *)(rec + kRecBeta))[lane] = rv.beta;
+        ((float *)(rec + kRecL))[lane] = L;
+        __syncwarp();
+        // row `lane` of T = (I + G)^-1: T[i][j] = -sum_{s > j} T[i][s] G[s][j] for j < i
+        float t[32];
+#pragma unroll
+        for (int s2 = 0; s2 < 32; ++s2) t[s2] = (s2 == lane) ? 1.f : 0.f;
+#pragma unroll
+        for (int j = 30; j >= 0; --j) {
+            const float *row = Gt + j * kWLg;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int c4 = (j + 1) >> 2; c4 < 8; ++c4) {
+                const float4 v = *(const float4 *)(row + 4 * c4);
+                const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int s2 = 4 * c4 + e;
+                    if (s2 > j) {
+                        if (e & 1) a1 = fmaf(t[s2], vv[e], a1);
+                        else a0 = fmaf(t[s2], vv[e], a0);
+                    }
+                }
+            }
+            if (j < lane) t[j] = -(a0 + a1);
+        }
+        // T diag(beta) and T diag(beta Gamma): bf16 hi + lo tiles, row `lane`
+#pragma unroll
+        for (int pr = 0; pr < 2; ++pr) {
+            if (pr == 1 && !gated) break;
+            uint8_t *hi = rec + kRecT + 2 * pr * kTTile, *lo = hi + kTTile;
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t wh[4], wl[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int s0 = ch * 8 + 2 * e;
+                    float v0 = t[s0] * Bs[s0], v1 = t[s0 + 1] * Bs[s0 + 1];
+                    if (pr) {
+                        v0 *= __expf(Ls[s0]);
+                        v1 *= __expf(Ls[s0 + 1]);
+                    }
+                    split_pack(v0, v1, wh[e], wl[e]);
+                }
+                *(uint4 *)(hi + sw128_offset(lane, ch)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+                *(uint4 *)(lo + sw128_offset(lane, ch)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+            }
+        }
+        __syncwarp();   // every lane's record writes happen before the publication
+        if (publish && lane == 0 && !(p.withhold_first && idx == 0)) {
+            __threadfence();
+            flag_publish(p.flags + rec_index(p, jb, c), 1u);
+        }
+        for (int n = 0; n < kWConsPerProd && idx < total; ++n)
+            idx = wstream_next<kPacked>(p, idx + stride, stride, total);
+    }
+}
+
+// A prep CTA (kThreads threads): warps 0-15 consumers, warps 16 and 17 the
+// producers of consumers 0-7 and 8-15. Producer pr's chunk stream is every
+// (2 n_pcta)-th chunk of the chunk-major order from 2 pcta + pr.
+template <bool kPacked>
+__device__ void wprep_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const Params &p, int pcta, int n_pcta,
+                          bool publish)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t *bar = (uint64_t *)(base + kWBar);   // [producer][kWBars]
+    uint32_t *tmem_slot = (uint32_t *)(bar + 2 * kWBars);
+    volatile uint32_t *abort = tmem_slot + 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // rows TMA does not write (K padding rows, queries beyond the chunk) stay zero
+    for (uint32_t i = threadIdx.x * 16; i < 2 * kWSlots * kWStage; i += kThreads * 16)
+        *(uint4 *)(base + kWStages + i) = make_uint4(0, 0, 0, 0);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2 * kWBars; ++i) mbar_init(&bar[i], 1);
+        *abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_q);
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, 512);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+    if (warp < kWCons) {
+        const int pr = warp / kWConsPerProd;
+        wprep_consumer<kPacked>(p, wprep_scratch(base, warp), bar + pr * kWBars, tbase + pr * 256, warp,
+                                2 * pcta + pr, 2 * n_pcta, publish, abort);
+    } else if (warp < kWCons + 2 && lane == 0) {
+        const int pr = warp - kWCons;
+        wprep_producer<kPacked>(p, &tm_k, &tm_q, base, bar + pr * kWBars, tbase + pr * 256, pr, 2 * pcta + pr,
+                                2 * n_pcta, abort);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
+// Split mode, plain path: one warp-per-chunk prep CTA per SM.
+template <bool kPacked>
+__global__ void __launch_bounds__(kThreads, 1)
+chunk_wprep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q, const Params p)
+{
+    wprep_cta<kPacked>(tm_k, tm_q, p, blockIdx.x, gridDim.x, false);
 }
 
 template <typename TOut, bool kPacked, bool kPro, bool kWK = false>
@@ -1326,6 +1786,8 @@ chunk_coop_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 {
     if ((int)blockIdx.x < p.bh_count)
         state_pass_cta<TOut, true, true, kPacked, kPro, kWK>(tm_k, tm_v, tm_q, p, blockIdx.x);
+    else if (!kPro && !kWK)
+        wprep_cta<kPacked>(tm_k, tm_q, p, blockIdx.x - p.bh_count, gridDim.x - p.bh_count, true);
     else
         prep_cta<kPacked, kPro, kWK>(tm_k, tm_q, tm_kw, p, blockIdx.x - p.bh_count, gridDim.x - p.bh_count);
 }
@@ -1507,15 +1969,36 @@ cudaError_t launch_chunk_tc(const Problem &p)
         cudaGetLastError();   // not launchable together here: two launches instead
     }
     const bool packed = p.cu != nullptr, pro = p.prologue != 0;
-    if (split) {
+    if (split && !pro && !p.kw) {
+        auto prep = packed ? chunk_wprep_kernel<true> : chunk_wprep_kernel<false>;
+        int dev = 0, sms = 0;
+        if ((e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWSmem)) != cudaSuccess ||
+            (e = cudaGetDevice(&dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return e;
+        if (n_total > 0x7fffffffu) return cudaErrorInvalidValue;
+        // persistent: one CTA per SM, each with two producers of 8 consumer warps
+        const unsigned n_ctas = (unsigned)((n_total + 1) / 2 < (size_t)sms ? (n_total + 1) / 2 : sms);
+        prep<<<n_ctas, kThreads, kWSmem, p.stream>>>(tk, tq, pr);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    } else if (split) {
         auto prep = p.kw     ? chunk_prep_kernel<false, false, true>
                     : packed ? (pro ? chunk_prep_kernel<true, true> : chunk_prep_kernel<true, false>)
                              : (pro ? chunk_prep_kernel<false, true> : chunk_prep_kernel<false, false>);
-        e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPKSmem);
-        if (e != cudaSuccess) return e;
-        const size_t n_ctas = (size_t)p.B * p.H * pr.n_chunks;
-        if (n_ctas > 0x7fffffffu) return cudaErrorInvalidValue;
-        prep<<<(unsigned)n_ctas, kPrepKThreads, kPKSmem, p.stream>>>(tk, tq, tkw, pr);
+        const uint32_t psmem = pk_smem(p.kw != nullptr);
+        int dev = 0, sms = 0, per_sm = 0;
+        if ((e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(prep, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                      (int)cudaSharedmemCarveoutMaxShared)) != cudaSuccess ||
+            (e = cudaGetDevice(&dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prep, kPrepThreads, psmem)) != cudaSuccess)
+            return e;
+        if (n_total > 0x7fffffffu) return cudaErrorInvalidValue;
+        // persistent: as many one-group CTAs as fit, each taking every grid-th chunk
+        const size_t slots = (size_t)sms * (per_sm > 0 ? per_sm : 1);
+        const unsigned n_ctas = (unsigned)(n_total < slots ? n_total : slots);
+        prep<<<n_ctas, kPrepThreads, psmem, p.stream>>>(tk, tq, tkw, pr);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     auto kernel = p.out_dtype == DP_F32 ? tc_kernel_for<float>(split, packed, pro, p.kw != nullptr)

@@ -97,16 +97,22 @@ def test_workspace_sizes(dp):
                                           (W.GATED, 1, 129, False), (W.NEARDUP, 4, 50, True),
                                           (W.LONG, 2, 17, False)],
                          ids=lambda v: getattr(v, "name", str(v)))
-def test_split_equals_fused_bitwise(dp, base, nh, T, h0):
-    """Every way of running the chunk path shares every arithmetic step (the
-    prep CTAs or kernel run the fused kernel's phase A and hand its bytes
-    over unchanged), so outputs and final states agree bit for bit."""
+def test_split_modes_agree_bitwise(dp, base, nh, T, h0):
+    """The cooperative launch and the two-kernel split mode share every
+    arithmetic step (the same prep writes the same records, the same state
+    pass reads them), so outputs and final states agree bit for bit. The
+    fused mode solves the UT transform with another summation order: it
+    meets the bf16 rule against the oracle, like the others."""
     x = W.make_inputs(base.scaled(B=2, H=3, T=T, nh=nh))
+    o_s, h_s = run(dp, x, h0=h0, path="split")
+    o_2, h_2 = run(dp, x, h0=h0, path="split2")
+    assert torch.equal(o_s, o_2)
+    assert torch.equal(h_s, h_2)
     o_f, h_f = run(dp, x, h0=h0, path="fused")
-    for path in ("split", "split2"):
-        o_s, h_s = run(dp, x, h0=h0, path=path)
-        assert torch.equal(o_s, o_f), path
-        assert torch.equal(h_s, h_f), path
+    ro, rh = ref(x, h0=h0)
+    for o, h in ((o_s, h_s), (o_f, h_f)):
+        assert_parity(o, ro, "bf16", "o")
+        assert_parity(h, rh, "bf16", "h_final")
 
 
 def test_forward_path_names_the_launch(dp):
@@ -132,7 +138,7 @@ def test_workspace_reuse_across_calls(dp):
         o, hf = dp.forward(g["q"], g["k"], g["v"], g["beta"], g["g"], g["h0"], impl="chunk_tc",
                            workspace=ws, out_dtype=torch.float32)
         dp.check_status(ws)
-        o_f, h_f = run(dp, x, path="fused")
+        o_f, h_f = run(dp, x, path="split")   # the same mode on a fresh workspace
         assert torch.equal(o, o_f)
         assert torch.equal(hf, h_f)
 
@@ -243,6 +249,29 @@ def test_gate_reset_and_beta_zero(dp):
     x["g"][:, 45] = 0.0
     x["beta"][:, 20:40] = 0.0
     o, hf = run(dp, x)
+    ro, rh = ref(x)
+    assert_parity(o, ro, "bf16", "o")
+    assert_parity(hf, rh, "bf16", "h_final")
+
+
+@pytest.mark.parametrize("path", ["split", "split2", "fused"])
+@pytest.mark.parametrize("nh", [1, 2, 3, 4])
+def test_gated_rescale_schedule(dp, nh, path):
+    """Gated chunks keep the state divided by the running product of chunk
+    decays and rescale it only when that product would fall below e^-27:
+    with gates in [0.3, 0.7] (a rescale every few chunks), runs of gates of
+    exactly 1 (no decay) and exact zeros (a reset, which always rescales),
+    outputs and final states still meet the bf16 rule against the oracle
+    (DeltaProduct paper, Sec.4: H <- g_t H once per token)."""
+    w = W.GATED.scaled(B=2, H=3, T=203, nh=nh)
+    x = W.make_inputs(w)
+    gen = torch.Generator().manual_seed(40 + nh)
+    g = 0.3 + 0.4 * torch.rand(x["g"].shape, generator=gen)
+    g[:, 40:90] = 1.0
+    g[:, 17] = 0.0
+    g[:, 150:153] = 0.0
+    x["g"] = g.to(torch.bfloat16)
+    o, hf = run(dp, x, path=path)
     ro, rh = ref(x)
     assert_parity(o, ro, "bf16", "o")
     assert_parity(hf, rh, "bf16", "h_final")

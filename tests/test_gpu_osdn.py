@@ -152,8 +152,10 @@ def test_chunk_path_write_keys(dp, name, w, eta, mode):
 
 @pytest.mark.parametrize("mode", ["coop", "split"])
 def test_chunk_write_keys_equal_keys_is_plain_chunk_forward(dp, mode):
-    """kw = k: the write-key chunk path computes the plain chunk path's
-    values in the same order, bit for bit."""
+    """kw = k: the write-key chunk path computes what the plain chunk path
+    computes (the plain path's prep solves the UT transform with another
+    summation order, so the two agree up to rounding: each meets the bf16
+    rule against the oracle, and against each other)."""
     w = W.GATED.scaled(B=2, H=2, T=100, nh=2)
     x, xc, *_ = inputs(w)
     ws = chunk_ws(dp, w, mode)
@@ -162,7 +164,11 @@ def test_chunk_write_keys_equal_keys_is_plain_chunk_forward(dp, mode):
     ws2 = chunk_ws(dp, w, mode)
     o2, h2 = dp.forward(xc["q"], xc["k"], xc["v"], xc["beta"], xc["g"], xc["h0"], impl="chunk_tc", workspace=ws2,
                         out_dtype=torch.float32)
-    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+    ro, rh = oracle.forward(x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"])
+    for o, h in ((o1, h1), (o2, h2)):
+        assert_parity(o, ro, "bf16", f"{mode} o")
+        assert_parity(h, rh, "bf16", f"{mode} h_final")
+    assert_parity(o1, o2.cpu().double().numpy(), "bf16", "write-key path vs plain path")
 
 
 def test_write_keys_fall_back_to_recurrent_without_records(dp):
