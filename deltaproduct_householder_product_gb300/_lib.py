@@ -129,8 +129,8 @@ def make_dims(B, T, H, Dk, Dv, nh, dtype, impl="auto", out_dtype=None, max_seqle
                 max_seqlen, int(prologue))
 
 
-PATHS = {0: "recurrent", 1: "chunk_fused", 2: "chunk_split", 3: "chunk_coop"}
-LAUNCHES = {"recurrent": 1, "chunk_fused": 1, "chunk_split": 2, "chunk_coop": 1}
+PATHS = {0: "recurrent", 1: "chunk_fused", 2: "chunk_split", 3: "chunk_coop", 4: "chunk_seg"}
+LAUNCHES = {"recurrent": 1, "chunk_fused": 1, "chunk_split": 2, "chunk_coop": 1, "chunk_seg": 4}
 
 
 def forward_path(dims, workspace_bytes):

@@ -128,7 +128,7 @@ dp_status dp_forward_workspace_size_fast(const dp_dims *dims, size_t *bytes)
 {
     DP_TRY(dp_forward_workspace_size(dims, bytes));
     dp::Problem p = make_problem(dims, dims->T);
-    if (use_chunk_tc(dims, p)) *bytes += (dp::chunk_tc_records_bytes(p) + 255) & ~(size_t)255;
+    if (use_chunk_tc(dims, p)) *bytes += (dp::chunk_tc_fast_bytes(p) + 255) & ~(size_t)255;
     return DP_OK;
 }
 

@@ -205,35 +205,69 @@ struct Params {
     int prologue;              // dp_prologue_flags applied on load
     uint32_t rec_stride;       // bytes per record: record_stride(prologue)
     const __nv_bfloat16 *kw;   // OSDN write keys (layout of k), split modes only; NULL: write with k
+    // segmented mode (see launch_chunk_tc): P segments of seg_chunks chunks per sequence
+    int seg_count, seg_chunks;
+    float *seg_h;              // [B*H][P][2][D][D]: end state of each segment's part 0 and part 1
+    float *seg_o0;             // [B,T,H,D_v]: readout of part 0 (segments >= 1)
+    float *seg_qt;             // [B,T,H,D_k]: readout of part 1 (segments >= 1)
 };
 
 // The (sequence, head) pair one state-pass CTA, or one prep step, works on.
 // Dense calls (kPacked = false): sequence b is batch row b, T tokens, and
 // every extent comes straight from the kernel parameters. Packed calls: the
 // extent is read from cu (and checked) once.
-template <bool kPk, bool kPr, bool kW = false>
+template <bool kPk, bool kPr, bool kW = false, bool kSg = false>
 struct Job {
     static constexpr bool kPacked = kPk;   // offsets from cu (else the dense layout)
     static constexpr bool kPro = kPr;      // input prologue (Params::prologue) applied on load
     static constexpr bool kWK = kW;        // OSDN write keys (Params::kw)
+    static constexpr bool kSeg = kSg;      // one segment of a dense sequence (segmented mode)
     int b, h;          // sequence and head
-    int b_map, t0;     // packed: token t sits at row (b_map * T + t0 + t) of the token layouts
-    int len, nc;       // packed: its tokens and chunks
+    int b_map, t0;     // packed / segment: token t sits at row (row_b() * T + t0 + t) of the token layouts
+    int len, nc;       // packed / segment: its tokens and chunks
+    int c0;            // segment: its first chunk in the sequence's chunk grid (records)
+    int seg, part;     // segment: index, and 0 = the state from the segment's start state, 1 = its transition
     bool valid;        // packed: false when the offsets broke their contract for this sequence
     __device__ __forceinline__ int row_b() const { return kPacked ? b_map : b; }
-    __device__ __forceinline__ int first() const { return kPacked ? t0 : 0; }
-    __device__ __forceinline__ int tokens(const Params &p) const { return kPacked ? len : p.T; }
-    __device__ __forceinline__ int chunks(const Params &p) const { return kPacked ? nc : p.n_chunks; }
+    __device__ __forceinline__ int first() const { return (kPacked || kSeg) ? t0 : 0; }
+    __device__ __forceinline__ int tokens(const Params &p) const { return (kPacked || kSeg) ? len : p.T; }
+    __device__ __forceinline__ int chunks(const Params &p) const { return (kPacked || kSeg) ? nc : p.n_chunks; }
     __device__ __forceinline__ bool ok() const { return kPacked ? valid : true; }
 };
 
-template <bool kPacked, bool kPro, bool kWK = false>
-__device__ __forceinline__ Job<kPacked, kPro, kWK> make_job(const Params &p, int bh)
+template <bool kPacked, bool kPro, bool kWK = false, bool kSeg = false>
+__device__ __forceinline__ Job<kPacked, kPro, kWK, kSeg> make_job(const Params &p, int bh)
 {
-    Job<kPacked, kPro, kWK> j;
+    Job<kPacked, kPro, kWK, kSeg> j;
+    if (kSeg) {
+        // segmented mode: CTA bh < B*H runs segment 0 of sequence bh from its
+        // initial state; the others run, for segments 1 .. P-1 of every
+        // sequence, the state from zero (part 0) and the transition (part 1)
+        const int nbh = p.bh_count;
+        int q = bh, seg = 0, part = 0;
+        if (bh >= nbh) {
+            const int r = bh - nbh, per = 2 * (p.seg_count - 1);
+            q = r / per;
+            seg = 1 + (r - q * per) / 2;
+            part = (r - q * per) & 1;
+        }
+        j.b = q / p.H;
+        j.h = q - j.b * p.H;
+        j.b_map = j.b;
+        j.seg = seg;
+        j.part = part;
+        j.c0 = seg * p.seg_chunks;
+        j.t0 = j.c0 * p.ct;
+        const int rest = p.T - j.t0, cap = p.seg_chunks * p.ct;
+        j.len = rest < cap ? (rest > 0 ? rest : 0) : cap;
+        j.nc = (j.len + p.ct - 1) / p.ct;
+        j.valid = true;
+        return j;
+    }
     j.b = bh / p.H;
     j.h = bh - j.b * p.H;
     j.b_map = j.t0 = j.len = j.nc = 0;
+    j.c0 = j.seg = j.part = 0;
     j.valid = true;
     if (kPacked) {
         const SeqRange r = seq_range(p.cu, j.b, p.B, p.T, p.max_T);
@@ -273,7 +307,7 @@ __device__ __forceinline__ uint32_t flag_read(const uint32_t *flag)
 template <class J>
 __device__ __forceinline__ size_t rec_index(const Params &p, const J &j, int c)
 {
-    return ((size_t)j.b * p.H + j.h) * (size_t)p.n_chunks + c;
+    return ((size_t)j.b * p.H + j.h) * (size_t)p.n_chunks + (J::kSeg ? j.c0 + c : c);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
@@ -294,14 +328,16 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     return fn;
 }
 
-// bf16 tensor map with a 64-element (128-byte) inner box and 128-byte swizzle.
+// Tensor map with a 128-byte inner box and 128-byte swizzle (64 bf16, or
+// 32 fp32 elements).
 bool encode(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
-            const cuuint64_t *strides_bytes, const cuuint32_t *box)
+            const cuuint64_t *strides_bytes, const cuuint32_t *box,
+            CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16)
 {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base),
+    return enc(map, type, (cuuint32_t)rank, const_cast<void *>(base),
                dims, strides_bytes, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -426,7 +462,9 @@ __device__ void tma_role(const Smem &s, const Params &p, const CUtensorMap *tk,
     const uint32_t rec_t = ((gated || J::kWK) ? 4 : 2) * kTTile, rec_tail = kRecBytes - kRecP;
     // mapped K and Q from the record (split modes with a key/query prologue)
     const bool kq_rec = kSplit && J::kPro && kq_in_record(p.prologue);
-    const uint32_t bytes = (kq_rec ? 256u * R + kRecKQBytes : 512u * R + 256u * ct) +
+    // segmented mode, transition part: no values (the V tiles stay zero, so U = 0)
+    const bool no_v = J::kSeg && jb.part == 1;
+    const uint32_t bytes = (kq_rec ? 256u * R + kRecKQBytes : (no_v ? 256u : 512u) * R + 256u * ct) +
                            (kSplit ? rec_t + rec_tail : 0u);
     int last_use[kNS];
     for (int i = 0; i < kNS; ++i) last_use[i] = -1;
@@ -458,7 +496,7 @@ __device__ void tma_role(const Smem &s, const Params &p, const CUtensorMap *tk,
                 tma_load_5d(kq + kb * kKQBlock, tk, bar, kb * 64, 0, h, t0, b);
                 tma_load_4d(kq + kb * kKQBlock + kC * 128, tq, bar, kb * 64, h, t0, b);
             }
-            tma_load_5d(vv + kb * kVBlock, tv, bar, kb * 64, 0, h, t0, b);
+            if (!no_v) tma_load_5d(vv + kb * kVBlock, tv, bar, kb * 64, 0, h, t0, b);
         }
         if (kSplit) {
             uint8_t *dst = kq + kStageIn;
@@ -1082,16 +1120,25 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, const J
     const uint32_t trow = tbase + ((uint32_t)(warp * 32) << 16);
     const size_t bh = (size_t)jb.b * p.H + jb.h;
     const bool gated = p.g != nullptr;
-    // o row of the sequence's first token, this thread's value column
+    // o row of the sequence's first token, this thread's value column.
+    // Segmented mode, segments >= 1: the readout goes to fp32 workspace
+    // arrays of o's layout (part 0: o from a zero start state; part 1: the
+    // start state's weights q~ = A_{<=t}^T q_t), which the correction adds up.
+    const bool ws_out = J::kSeg && jb.seg > 0;
     TOut *const o_seq = (TOut *)p.o + tok_row(p, jb, 0) * kD + tid;
+    float *const w_seq = J::kSeg ? (jb.part ? p.seg_qt : p.seg_o0) + tok_row(p, jb, 0) * kD + tid : nullptr;
     const size_t tok_stride = (size_t)p.H * kD;
 
-    {   // S^T <- h0^T (lane = dv, column = dk), or zeros; readout accumulators zero
+    {   // S^T <- h0^T (lane = dv, column = dk), or zeros (or, for a segment's
+        // transition part, the identity); readout accumulators zero
+        const float *h0 = ws_out ? nullptr : p.h0;
+        const bool ident = ws_out && jb.part == 1;
         uint32_t r[32];
         for (int c0 = 0; c0 < kD; c0 += 32) {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                r[j] = __float_as_uint(p.h0 ? p.h0[(bh * kD + c0 + j) * kD + tid] : 0.f);
+                r[j] = __float_as_uint(ident ? (c0 + j == tid ? 1.f : 0.f)
+                                             : (h0 ? h0[(bh * kD + c0 + j) * kD + tid] : 0.f));
             tmem_st32(trow + kColS + c0, r);
         }
         uint32_t z[16];
@@ -1156,25 +1203,36 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, const J
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.bar[kBarOFree + g]);
-        TOut *oc = o_seq + (size_t)t0 * tok_stride;
+        if (ws_out) {
+            float *oc = w_seq + (size_t)t0 * tok_stride;
 #pragma unroll
-        for (int i = 0; i < kNQ; ++i)
-            if (i < p.ct && t0 + i < jb.tokens(p)) store_out(oc, (size_t)i * tok_stride, __uint_as_float(ra[i]));
+            for (int i = 0; i < kNQ; ++i)
+                if (i < p.ct && t0 + i < jb.tokens(p)) store_out(oc, (size_t)i * tok_stride, __uint_as_float(ra[i]));
+        } else {
+            TOut *oc = o_seq + (size_t)t0 * tok_stride;
+#pragma unroll
+            for (int i = 0; i < kNQ; ++i)
+                if (i < p.ct && t0 + i < jb.tokens(p)) store_out(oc, (size_t)i * tok_stride, __uint_as_float(ra[i]));
+        }
     }
-    if (!failed && jb.ok() && p.h_final) {
+    // segmented mode: every part's end state goes to the workspace (the
+    // combine step turns them into start states and the final state)
+    float *const hdst = J::kSeg ? p.seg_h + (((size_t)bh * p.seg_count + jb.seg) * 2 + jb.part) * kD * kD
+                                : (p.h_final ? p.h_final + bh * kD * kD : nullptr);
+    if (!failed && jb.ok() && hdst) {
         const float sig = gated ? __expf(ls) : 1.f;
         uint32_t r[32];
         for (int c0 = 0; c0 < kD; c0 += 32) {
             tmem_ld32(trow + kColS + c0, r);
             tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) p.h_final[(bh * kD + c0 + j) * kD + tid] = sig * __uint_as_float(r[j]);
+            for (int j = 0; j < 32; ++j) hdst[(size_t)(c0 + j) * kD + tid] = sig * __uint_as_float(r[j]);
         }
     }
 }
 
 // ------------------------------------------------------------------ state-pass kernel
-template <typename TOut, bool kSplit, bool kCoop, bool kPacked, bool kPro, bool kWK = false>
+template <typename TOut, bool kSplit, bool kCoop, bool kPacked, bool kPro, bool kWK = false, bool kSeg = false>
 __device__ __forceinline__ void state_pass_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                                const CUtensorMap &tm_q, const Params &p, int bh)
 {
@@ -1192,7 +1250,7 @@ __device__ __forceinline__ void state_pass_cta(const CUtensorMap &tm_k, const CU
     s.scratch_off = Lay::kOffScratch;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // a sequence with bad packed offsets runs no chunk
-    const Job<kPacked, kPro, kWK> jb = make_job<kPacked, kPro, kWK>(p, bh);
+    const Job<kPacked, kPro, kWK, kSeg> jb = make_job<kPacked, kPro, kWK, kSeg>(p, bh);
     if (kPacked && threadIdx.x == 0 && !jb.ok()) report_bad_sequence(p.status);
 
     // Zero every tile once: rows TMA never writes (padding rows, query rows
@@ -1607,7 +1665,7 @@ __device__ void wprep_producer(const Params &p, const CUtensorMap *tk, const CUt
 {
     using J = Job<kPacked, false, false>;
     const int total = p.n_chunks * p.bh_count;
-    constexpr int kLag = 2;   // the Gram MMA of chunk k is issued with the loads of chunk k + kLag
+    constexpr int kLag = 3;   // the Gram MMA of chunk k is issued with the loads of chunk k + kLag (< kWSlots)
     const uint32_t idesc = idesc_bf16(128, kC + kNQ, false, false);
     bool ok = true;
     int issued_ld = 0, issued_mma = 0;   // chunks whose loads / MMAs were issued
@@ -1839,6 +1897,168 @@ chunk_wprep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     wprep_cta<kPacked>(tm_k, tm_q, p, blockIdx.x, gridDim.x, false);
 }
 
+// ------------------------------------------------------------------ segmented mode
+// For sequences too few to fill the GPU, each (b, h) sequence is cut into P
+// segments of whole chunks, and the recurrence's affine form (DeltaProduct
+// paper, Sec.2 Eq.(1): S_end = A S_start + B per segment, associative)
+// lets the segments run at once:
+//  1. state pass (chunk_seg_kernel, one CTA per job): segment 0 from h0,
+//     writing o; every later segment twice, from a zero state (part 0:
+//     readout o0, end state B_s) and, with its values left out, from the
+//     identity (part 1: end state A_s, readout q~_t = A_{<=t}^T q_t);
+//  2. seg_combine_kernel: S_1 = segment 0's end state, S_{s+1} = A_s S_s +
+//     B_s, in order (fp32, CUDA cores); S_s^T for the correction, S_P is
+//     h_final;
+//  3. seg_correct_kernel: o_t = o0_t + S_s^T q~_t for the tokens of segment
+//     s >= 1 (tf32 tensor-core MMA per tile of 128 tokens).
+template <typename TOut>
+__global__ void __launch_bounds__(kThreads, 1)
+chunk_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                 const __grid_constant__ CUtensorMap tm_q, const Params p)
+{
+    state_pass_cta<TOut, true, false, false, false, false, true>(tm_k, tm_v, tm_q, p, blockIdx.x);
+}
+
+constexpr int kCombThreads = 256;
+constexpr int kCombLd = kD + 4;                          // A row stride in shared memory (floats)
+constexpr uint32_t kCombSmem = (kD * kCombLd + kD * 33) * 4;
+// grid: B*H x 4 blocks of 32 value columns (the columns of the state evolve
+// independently: S[:, J] <- A S[:, J] + B[:, J]); A_s is staged in shared
+// memory by coalesced loads, the block of S stays there.
+__global__ void __launch_bounds__(kCombThreads)
+seg_combine_kernel(const float *seg_h, float *seg_st, float *h_final, int P)
+{
+    extern __shared__ float comb_smem[];
+    float *As = comb_smem;                               // [kD][kCombLd]
+    float(*S)[33] = reinterpret_cast<float(*)[33]>(comb_smem + kD * kCombLd);
+    const int bh = blockIdx.x >> 2, vb = (blockIdx.x & 3) * 32, tid = threadIdx.x;
+    const float *base = seg_h + (size_t)bh * P * 2 * kD * kD;
+    for (int i = tid; i < kD * 32; i += kCombThreads) S[i >> 5][i & 31] = base[(size_t)(i >> 5) * kD + vb + (i & 31)];
+    __syncthreads();
+    const int row = tid >> 1, v0 = (tid & 1) * 16;
+    for (int sg = 1; sg < P; ++sg) {
+        // start state of segment sg, transposed: [v][k]
+        float *st = seg_st + ((size_t)bh * P + sg) * kD * kD;
+        for (int i = tid; i < kD * 32; i += kCombThreads) st[(size_t)(vb + (i >> 7)) * kD + (i & 127)] = S[i & 127][i >> 7];
+        const float *A = base + ((size_t)sg * 2 + 1) * kD * kD;
+        for (int i = tid; i < kD * kD / 4; i += kCombThreads) {
+            const float4 a = __ldg((const float4 *)A + i);
+            *(float4 *)(As + (i >> 5) * kCombLd + 4 * (i & 31)) = a;
+        }
+        const float *Bm = base + ((size_t)sg * 2) * kD * kD + (size_t)row * kD + vb + v0;
+        float acc[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[j] = __ldg(Bm + j);
+        __syncthreads();
+        const float *Ar = As + row * kCombLd;
+        for (int k4 = 0; k4 < kD / 4; ++k4) {
+            const float4 a = *(const float4 *)(Ar + 4 * k4);
+            const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc[j] = fmaf(av[e], S[4 * k4 + e][v0 + j], acc[j]);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) S[row][v0 + j] = acc[j];
+        __syncthreads();
+    }
+    if (h_final)
+        for (int i = tid; i < kD * 32; i += kCombThreads)
+            h_final[(size_t)bh * kD * kD + (size_t)(i >> 5) * kD + vb + (i & 31)] = S[i >> 5][i & 31];
+}
+
+constexpr int kCorrTok = 64;                             // tokens per tile (two CTAs per SM)
+constexpr uint32_t kCorrBlock = 128 * 128;               // A: 128 rows x 32 fp32
+constexpr uint32_t kCorrBBlock = kCorrTok * 128;         // B: kCorrTok rows x 32 fp32
+constexpr uint32_t kCorrSmem = 4 * kCorrBlock + 4 * kCorrBBlock + 2 * 8 + 16 + 1024;
+
+template <typename TOut>
+__global__ void __launch_bounds__(128, 2)
+seg_correct_kernel(const __grid_constant__ CUtensorMap tm_st, const __grid_constant__ CUtensorMap tm_qt,
+                   const Params p, int tiles)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *sA = base, *sB = base + 4 * kCorrBlock;    // S_s^T (rows v), q~ tile (rows t)
+    uint64_t *bar = (uint64_t *)(sB + 4 * kCorrBBlock);
+    uint32_t *tmem_slot = (uint32_t *)(bar + 2);
+    volatile uint32_t *abort = tmem_slot + 1;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tile = blockIdx.x % tiles, r = blockIdx.x / tiles, nseg = p.seg_count - 1;
+    const int sg = 1 + r % nseg, bh = r / nseg, b = bh / p.H, h = bh - b * p.H;
+    const int seg0 = sg * p.seg_chunks * p.ct, seg_len = min(p.seg_chunks * p.ct, p.T - seg0);
+    const int tok0 = seg0 + tile * kCorrTok, ntok = min(kCorrTok, seg_len - tile * kCorrTok);
+    if (ntok <= 0) return;   // the same for the whole CTA
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, kCorrTok);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+    bool ok = true;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bar[0], 4 * kCorrBlock + 4 * kCorrBBlock);
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) {
+            tma_load_3d(sA + kb * kCorrBlock, &tm_st, &bar[0], kb * 32, 0, bh * p.seg_count + sg);
+            tma_load_4d(sB + kb * kCorrBBlock, &tm_qt, &bar[0], kb * 32, h, tok0, b);
+        }
+        uint32_t no_abort = 0;
+        ok = mbar_wait(&bar[0], 0, kWaitTries, &no_abort);
+        if (ok) {
+            tc_fence_after();
+            const uint32_t idesc = idesc_tf32(128, kCorrTok);
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) {
+                const uint32_t ka = (kk >> 2) * kCorrBlock + (kk & 3) * 32, kb = (kk >> 2) * kCorrBBlock + (kk & 3) * 32;
+                mma_ss_tf32(tbase, sdesc_sw128(smem_addr(sA) + ka, 16, 1024), sdesc_sw128(smem_addr(sB) + kb, 16, 1024),
+                            idesc, kk > 0);
+            }
+            mma_commit(&bar[1]);
+            ok = mbar_wait(&bar[1], 0, kWaitTries, &no_abort);
+        }
+        if (!ok) {
+            if (p.status) atomicCAS(p.status, 0u, kDevTimeout);
+            *abort = 1;
+            mbar_wait(&bar[0], 0, kWaitTries, &no_abort);   // let what is in flight land
+            mbar_wait(&bar[1], 0, kWaitTries, &no_abort);
+        }
+    }
+    __syncthreads();
+    tc_fence_after();
+    if (!*abort) {
+        // lane = value column v; TMEM column = token of the tile
+        const uint32_t trow = tbase + ((uint32_t)(warp * 32) << 16);
+        const size_t tok_stride = (size_t)p.H * kD;
+        const size_t row0 = (((size_t)b * p.T + tok0) * p.H + h) * kD + tid;
+        for (int c0 = 0; c0 < kCorrTok; c0 += 32) {
+            // the 32 tokens' o0 values first (read-only path, all in flight
+            // together), then the sums
+            float a[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                a[j] = c0 + j < ntok ? __ldg(p.seg_o0 + row0 + (size_t)(c0 + j) * tok_stride) : 0.f;
+            uint32_t d[32];
+            tmem_ld32(trow + c0, d);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (c0 + j < ntok)
+                    store_out((TOut *)p.o, row0 + (size_t)(c0 + j) * tok_stride, __uint_as_float(d[j]) + a[j]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, kCorrTok);
+}
+
 template <typename TOut, bool kPacked, bool kPro, bool kWK = false>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_coop_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -1897,6 +2117,68 @@ size_t chunk_tc_records_bytes(const Problem &p)
 }
 
 namespace {
+constexpr int kSegMinChunks = 16;   // shortest segment worth a CTA pair
+
+// Segments per sequence for the segmented mode (>= 2) and their length in
+// chunks, or 0 when the mode does not apply: dense plain problems whose
+// B*H (2P - 1) state-pass CTAs fit the SMs at once with P >= 2.
+int seg_plan(const Problem &p, int *seg_chunks)
+{
+    *seg_chunks = 0;
+    if (p.cu || p.prologue || p.kw || p.T <= 0) return 0;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    const long long bh = (long long)p.B * p.H, nch = (long long)chunks_per_seq(p);
+    if (bh <= 0) return 0;
+    long long P = (sms / bh + 1) / 2;
+    if (P > nch / kSegMinChunks) P = nch / kSegMinChunks;
+    // two segments do not pay for the separate prep, combine and correction
+    // (measured: the cooperative launch is faster there)
+    if (P < 3) return 0;
+    const long long L = (nch + P - 1) / P;
+    P = (nch + L - 1) / L;   // no empty segment
+    if (P < 3) return 0;
+    *seg_chunks = (int)L;
+    return (int)P;
+}
+
+// Segmented-mode workspace after the status block: records, the parts' end
+// states [B*H][P][2] and the start states S_s^T [B*H][P] (D x D fp32 each),
+// the two fp32 readouts of o's size.
+struct SegLayout {
+    size_t rec, h, st, o0, qt, total;
+};
+SegLayout seg_layout(const Problem &p, int P)
+{
+    const size_t bh = (size_t)p.B * p.H, d2 = (size_t)kD * kD * 4, tok = (size_t)p.B * p.T * p.H * kD * 4;
+    SegLayout l;
+    l.rec = 0;
+    l.h = round256(n_chunks_total(p) * record_stride(0));
+    l.st = l.h + round256(bh * P * 2 * d2);
+    l.o0 = l.st + round256(bh * P * d2);
+    l.qt = l.o0 + round256(tok);
+    l.total = l.qt + round256(tok);
+    return l;
+}
+}  // namespace
+
+size_t chunk_tc_fast_bytes(const Problem &p)
+{
+    size_t r = chunk_tc_records_bytes(p);
+    int L = 0;
+    const int P = seg_plan(p, &L);
+    if (P >= 2) {
+        const size_t sb = seg_layout(p, P).total;
+        if (sb > r) r = sb;
+    }
+    return r;
+}
+
+namespace {
 // The kernel instantiation for a problem: output type, mode, packed
 // offsets, input prologue; write keys (dense, no prologue, split modes).
 template <typename TOut, bool kSplit>
@@ -1952,6 +2234,12 @@ cudaError_t coop_grid(const Problem &p, long long *grid)
 
 cudaError_t chunk_tc_path(const Problem &p, int *path)
 {
+    int L = 0;
+    const int P = seg_plan(p, &L);
+    if (P >= 2 && p.scratch_bytes >= seg_layout(p, P).total) {
+        *path = DP_PATH_CHUNK_SEG;
+        return cudaSuccess;
+    }
     long long grid = 0;
     const cudaError_t e = coop_grid(p, &grid);
     if (e != cudaSuccess) return e;
@@ -1964,6 +2252,72 @@ cudaError_t chunk_tc_path(const Problem &p, int *path)
         *path = DP_PATH_CHUNK_FUSED;
     return cudaSuccess;
 }
+
+namespace {
+// Segmented mode (see seg_combine_kernel): prep of every chunk, the state
+// pass over B*H (2P - 1) jobs, the combine, the correction.
+cudaError_t launch_segmented(const Problem &p, Params pr, const CUtensorMap &tk, const CUtensorMap &tv,
+                             const CUtensorMap &tq, int P, int L, const SegLayout &lay)
+{
+    uint8_t *ws = (uint8_t *)p.scratch;
+    pr.rec = ws + lay.rec;
+    pr.seg_count = P;
+    pr.seg_chunks = L;
+    pr.seg_h = (float *)(ws + lay.h);
+    pr.seg_o0 = (float *)(ws + lay.o0);
+    pr.seg_qt = (float *)(ws + lay.qt);
+    float *seg_st = (float *)(ws + lay.st);
+    const size_t n_total = n_chunks_total(p), bh = (size_t)p.B * p.H;
+    cudaError_t e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    {   // 1. records
+        auto prep = chunk_wprep_kernel<false>;
+        if ((e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWSmem)) != cudaSuccess)
+            return e;
+        const unsigned n_ctas = (unsigned)((n_total + 1) / 2 < (size_t)sms ? (n_total + 1) / 2 : sms);
+        prep<<<n_ctas, kThreads, kWSmem, p.stream>>>(tk, tq, pr);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    {   // 2. state pass of every job
+        auto kernel = p.out_dtype == DP_F32 ? chunk_seg_kernel<float> : chunk_seg_kernel<__nv_bfloat16>;
+        const uint32_t smem = smem_bytes<true>();
+        if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+            return e;
+        kernel<<<(unsigned)(bh * (2 * P - 1)), kThreads, smem, p.stream>>>(tk, tv, tq, pr);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    // 3. start states and the final state
+    if ((e = cudaFuncSetAttribute(seg_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCombSmem)) !=
+        cudaSuccess)
+        return e;
+    seg_combine_kernel<<<(unsigned)(bh * 4), kCombThreads, kCombSmem, p.stream>>>(pr.seg_h, seg_st, p.h_final, P);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    {   // 4. correction of the outputs of segments >= 1
+        CUtensorMap tm_st, tm_qt;
+        const cuuint64_t dst[3] = {kD, kD, (cuuint64_t)bh * P};
+        const cuuint64_t sst[2] = {kD * 4, kD * kD * 4};
+        const cuuint32_t bst[3] = {32, 128, 1};
+        const cuuint64_t dqt[4] = {kD, (cuuint64_t)p.H, (cuuint64_t)p.T, (cuuint64_t)p.B};
+        const cuuint64_t sqt[3] = {kD * 4, (cuuint64_t)p.H * kD * 4, (cuuint64_t)p.T * p.H * kD * 4};
+        const cuuint32_t bqt[4] = {32, 1, (cuuint32_t)kCorrTok, 1};
+        if (!encode(&tm_st, seg_st, 3, dst, sst, bst, CU_TENSOR_MAP_DATA_TYPE_FLOAT32) ||
+            !encode(&tm_qt, pr.seg_qt, 4, dqt, sqt, bqt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+            return cudaErrorInvalidValue;
+        const int tiles = (L * pr.ct + kCorrTok - 1) / kCorrTok;
+        auto kernel = p.out_dtype == DP_F32 ? seg_correct_kernel<float> : seg_correct_kernel<__nv_bfloat16>;
+        if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCorrSmem)) != cudaSuccess)
+            return e;
+        const size_t grid = bh * (P - 1) * tiles;
+        if (grid > 0x7fffffffu) return cudaErrorInvalidValue;
+        kernel<<<(unsigned)grid, 128, kCorrSmem, p.stream>>>(tm_st, tm_qt, pr, tiles);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+}  // namespace
 
 cudaError_t launch_chunk_tc(const Problem &p)
 {
@@ -2004,15 +2358,23 @@ cudaError_t launch_chunk_tc(const Problem &p)
     pr.kw = (const __nv_bfloat16 *)p.kw;
     pr.n_chunks = (int)chunks_per_seq(p);
 
+    pr.seg_count = pr.seg_chunks = 0;
+    pr.seg_h = pr.seg_o0 = pr.seg_qt = nullptr;
+    const size_t n_total = n_chunks_total(p);
+    cudaError_t e;
+    {
+        int L = 0;
+        const int P = seg_plan(p, &L);
+        if (P >= 2 && p.scratch != nullptr && p.scratch_bytes >= seg_layout(p, P).total)
+            return launch_segmented(p, pr, tk, tv, tq, P, L, seg_layout(p, P));
+    }
     // split whenever the workspace holds every chunk's record; cooperative
     // (one launch) when it also holds the flags and the heads leave at least
     // as many SMs for the prep CTAs as the state pass takes
-    const size_t n_total = n_chunks_total(p);
     const size_t rec_bytes = round256(n_total * record_stride(p.prologue));
     const bool split = p.scratch != nullptr && n_total > 0 && p.scratch_bytes >= rec_bytes;
     // write keys: the split modes only (dense, no prologue; checked by the caller)
     if (p.kw && (!split || p.cu || p.prologue)) return cudaErrorInvalidValue;
-    cudaError_t e;
     long long grid = 0;
     if (split && (e = coop_grid(p, &grid)) != cudaSuccess) return e;
     if (grid > 0) {

@@ -39,6 +39,10 @@ bool chunk_tc_supported(const Problem &p);
 // let launch_chunk_tc split into a parallel prep kernel and the state-pass
 // kernel; with less scratch it runs the fused single kernel.
 size_t chunk_tc_records_bytes(const Problem &p);
+// Workspace bytes (after the status block) of the fastest way to run this
+// problem on the current device: the records, or the segmented mode's
+// larger workspace where that mode applies.
+size_t chunk_tc_fast_bytes(const Problem &p);
 // Which way launch_chunk_tc runs this problem with p.scratch_bytes of scratch
 // (a dp_path value).
 cudaError_t chunk_tc_path(const Problem &p, int *path);

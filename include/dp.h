@@ -96,7 +96,7 @@ typedef enum {
 } dp_prologue_flags;
 
 /* ABI version of this header (bumped on any signature change). */
-#define DP_ABI_VERSION 9
+#define DP_ABI_VERSION 10
 int dp_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -107,19 +107,28 @@ const char *dp_status_string(dp_status s);
 dp_status dp_forward_workspace_size(const dp_dims *dims, size_t *bytes);
 
 /* Bytes of device workspace with which dp_forward runs its fastest path
- * (>= dp_forward_workspace_size). For the tensor-core chunk path this adds,
- * per (batch, head, chunk) of ceil(T / ct) chunks, ct = min(16, 32 / n_h)
- * tokens, an 18688-byte record and a 4-byte flag (each area rounded up to
- * 256 bytes): every
- * chunk's UT transform is then prepared in parallel (by the other CTAs of
- * one cooperative launch when B*H leaves at least half the SMs free, else by
- * a first kernel) and the state pass streams the records in. With at least
- * dp_forward_workspace_size bytes but less than this, dp_forward runs one
- * fused kernel instead: slower, bit-identical results. Both sizes are equal
- * for the recurrent path. The library clears the flags on the stream before
- * every cooperative launch, so a workspace may be reused by calls of any
- * shapes, in any order; calls sharing a workspace must be ordered (one
- * stream). */
+ * (>= dp_forward_workspace_size; it depends on the current device's SM
+ * count). For the tensor-core chunk path this adds, per (batch, head,
+ * chunk) of ceil(T / ct) chunks, ct = min(16, 32 / n_h) tokens, an
+ * 18688-byte record and a 4-byte flag (each area rounded up to 256 bytes):
+ * every chunk's UT transform is then prepared in parallel (by the other
+ * CTAs of one cooperative launch when B*H leaves at least half the SMs
+ * free, else by a first kernel) and the state pass streams the records in.
+ * Dense problems without prologue or write keys whose B*H is small enough
+ * that each sequence can be cut into P >= 2 segments of at least 16 chunks
+ * with B*H*(2P - 1) <= the SM count take the segmented mode instead
+ * (DP_PATH_CHUNK_SEG; the recurrence is affine in the state, so each segment
+ * runs from a zero state and from the identity at once and a short combine
+ * chains them); its workspace adds, after the records, 3 B*H*P fp32 D x D
+ * matrices and two fp32 arrays of o's size. With at least
+ * dp_forward_workspace_size bytes but less than the records, dp_forward
+ * runs one fused kernel instead. The split, cooperative and fused modes
+ * agree with each other up to rounding (split and cooperative bit for bit);
+ * the segmented mode adds the rounding of its combine and correction. Both
+ * sizes are equal for the recurrent path. The library clears the flags on
+ * the stream before every cooperative launch, so a workspace may be reused
+ * by calls of any shapes, in any order; calls sharing a workspace must be
+ * ordered (one stream). */
 dp_status dp_forward_workspace_size_fast(const dp_dims *dims, size_t *bytes);
 
 /* How dp_forward runs a problem given `workspace_bytes` of workspace
@@ -131,7 +140,8 @@ typedef enum {
     DP_PATH_RECURRENT = 0,    /* token-by-token SIMT kernel */
     DP_PATH_CHUNK_FUSED = 1,  /* one tensor-core kernel, prep inside */
     DP_PATH_CHUNK_SPLIT = 2,  /* prep kernel, then the state-pass kernel */
-    DP_PATH_CHUNK_COOP = 3    /* one cooperative launch: prep CTAs beside the state pass */
+    DP_PATH_CHUNK_COOP = 3,   /* one cooperative launch: prep CTAs beside the state pass */
+    DP_PATH_CHUNK_SEG = 4     /* segmented: each sequence cut into segments run at once (four launches) */
 } dp_path;
 dp_status dp_forward_path(const dp_dims *dims, size_t workspace_bytes, int *path);
 

@@ -320,10 +320,15 @@ def test_full_size_sampled_heads(dp, base):
 
 def test_state_carry_on_chunk_boundaries_is_bit_exact(dp):
     """When every call length is a multiple of the chunk (32 tokens at n_h = 2),
-    carrying the state across calls runs exactly the same arithmetic."""
+    carrying the state across calls runs exactly the same arithmetic (in the
+    two-kernel split mode for every call: the segmented mode, which a longer
+    call would take, adds the rounding of its combine)."""
     w = W.BASE.scaled(B=2, H=4, T=1024)
-    xc = cuda(W.make_inputs(w))
-    o_one, h_one = dp.forward(xc["q"], xc["k"], xc["v"], xc["beta"], impl="chunk_tc",
+    x = W.make_inputs(w)
+    xc = cuda(x)
+    ws = torch.zeros(workspace_for(dp, x, "chunk_tc", "split2"), dtype=torch.uint8, device="cuda")
+    assert dp.forward_path(*_dims(xc)[:6], ws.numel()) == "chunk_split"
+    o_one, h_one = dp.forward(xc["q"], xc["k"], xc["v"], xc["beta"], impl="chunk_tc", workspace=ws,
                               out_dtype=torch.float32)
     state = torch.zeros_like(h_one)
     outs = []
@@ -331,11 +336,43 @@ def test_state_carry_on_chunk_boundaries_is_bit_exact(dp):
         sl = slice(s * 256, (s + 1) * 256)
         o_s, _ = dp.forward(xc["q"][:, sl].contiguous(), xc["k"][:, sl].contiguous(),
                             xc["v"][:, sl].contiguous(), xc["beta"][:, sl].contiguous(), None,
-                            state, impl="chunk_tc", h_final=state, out_dtype=torch.float32)
+                            state, impl="chunk_tc", h_final=state, workspace=ws, out_dtype=torch.float32)
         outs.append(o_s)
     torch.cuda.synchronize()
     assert torch.equal(torch.cat(outs, 1), o_one)
     assert torch.equal(state, h_one)
+
+
+SEG_CASES = [(W.BASE, 2, 805, True), (W.BASE, 2, 1027, False), (W.GATED, 4, 530, True), (W.GATED, 3, 700, False),
+             (W.NEARDUP, 3, 651, True), (W.LONG, 1, 1100, True), (W.GATED, 1, 1040, True)]
+
+
+@pytest.mark.parametrize("base,nh,T,h0", SEG_CASES, ids=lambda v: getattr(v, "name", str(v)))
+def test_segmented_mode_parity(dp, base, nh, T, h0):
+    """Few heads, long sequences: each sequence is cut into segments that run
+    at once (from a zero state and from the identity), then chained and
+    corrected (DeltaProduct paper, Sec.2 Eq.(1): the recurrence is affine in
+    the state, so a segment's end state is A_s S_start + B_s). Outputs and
+    final states meet the bf16 rule against the oracle; ragged segment tails,
+    gates, h0 and every n_h."""
+    w = base.scaled(B=1, H=2, T=T, nh=nh)
+    x = W.make_inputs(w)
+    xc = cuda(x)
+    size = workspace_for(dp, x, "chunk_tc", "split")
+    assert dp.forward_path(*_dims(xc)[:6], size) == "chunk_seg"
+    ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
+    o, hf = dp.forward(xc["q"], xc["k"], xc["v"], xc["beta"], xc["g"], xc["h0"] if h0 else None,
+                       impl="chunk_tc", workspace=ws, out_dtype=torch.float32)
+    dp.check_status(ws)
+    ro, rh = ref(x, h0=h0)
+    assert_parity(o, ro, "bf16", "o")
+    assert_parity(hf, rh, "bf16", "h_final")
+    # bf16 output: the same fp32 values rounded once; no final state asked for
+    o16, none = dp.forward(xc["q"], xc["k"], xc["v"], xc["beta"], xc["g"], xc["h0"] if h0 else None,
+                           impl="chunk_tc", workspace=ws, out_dtype=torch.bfloat16, h_final=False)
+    dp.check_status(ws)
+    assert none is None
+    assert torch.equal(o16, o.to(torch.bfloat16))
 
 
 def test_long_state_carry_and_decode(dp):
