@@ -214,6 +214,7 @@ dp_status dp_decode_step(const dp_dims *dims, const void *q, const void *k, cons
     p.h0 = state;
     p.h_final = state;
     p.stream = (cudaStream_t)stream;
+    p.decode = true;
     if ((size_t)p.B * p.H == 0) return DP_OK;
     DP_TRY(check_io(p, g != nullptr));
     DP_TRY(check_ptr(state, 16));

@@ -27,6 +27,7 @@ struct Problem {
     void *scratch;             // workspace bytes after the status block
     size_t scratch_bytes;
     cudaStream_t stream;
+    bool decode;               // dp_decode_step: launched as a programmatic dependent launch
 };
 
 // Sequential (token by token) SIMT kernel: any supported D_k, D_v, n_h and

@@ -49,10 +49,18 @@ recurrent_kernel(int T, int H, int Dv, int nh, const int *cu, int N, int max_T, 
 {
     constexpr int R = DK / kWarps;            // key rows per warp
     __shared__ float kbuf[2][DK];
+    __shared__ float xrows[5][DK];      // plain instantiation: the token's n_h keys and its query
     __shared__ float kwbuf[2][DK];      // OSDN write keys (kw != NULL)
     __shared__ float part[2][kWarps][kCols];
     __shared__ float nred[2][kWarps];   // prologue: partial sums of squares
 
+    // Launched with programmatic stream serialization (the decode step), a
+    // kernel may start while the one before it on the stream finishes: it
+    // waits for that grid's completion and memory before touching anything,
+    // and lets the next launch get resident right away. Without the launch
+    // attribute both instructions do nothing.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int bh = blockIdx.x;                // b * H + h
     const int b = bh / H, h = bh - b * H;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -73,6 +81,50 @@ recurrent_kernel(int T, int H, int Dv, int nh, const int *cu, int N, int max_T, 
     int buf = 0;   // alternating buffers: one barrier per matvec
     for (int t = 0; t < sq.len; ++t) {
         const size_t tok = ((size_t)sq.b_map * T + sq.t0 + t) * H + h;
+        if (!kExtra) {
+            // every row of the token (n_h keys, the query) and this thread's
+            // values and betas in one round of loads, so that the n_h + 1
+            // matvecs wait on no global load (the decode step's latency)
+            if (threadIdx.x < DK) {
+                for (int j = 0; j < nh; ++j) xrows[j][threadIdx.x] = to_f(k[(tok * nh + j) * DK + threadIdx.x]);
+                xrows[nh][threadIdx.x] = to_f(q[tok * DK + threadIdx.x]);
+            }
+            float vj[4], bj[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (j < nh) {
+                    vj[j] = to_f(v[(tok * nh + j) * Dv + col]);
+                    bj[j] = to_f(beta[tok * nh + j]);
+                }
+            const float gt = g ? to_f(g[tok]) : 1.f;
+            __syncthreads();
+            if (g) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) S[r] *= gt;
+            }
+#pragma unroll
+            for (int j = 0; j <= 4; ++j) {
+                if (j > nh) break;
+                const float *x = xrows[j];
+                float a4[4] = {0.f, 0.f, 0.f, 0.f};   // four independent chains
+#pragma unroll
+                for (int r = 0; r < R; ++r) a4[r & 3] = fmaf(S[r], x[row0 + r], a4[r & 3]);
+                part[buf][w][lane] = (a4[0] + a4[1]) + (a4[2] + a4[3]);
+                __syncthreads();
+                float hx = 0.f;
+#pragma unroll
+                for (int i = 0; i < kWarps; ++i) hx += part[buf][i][lane];
+                if (j < nh) {
+                    const float e = bj[j] * (vj[j] - hx);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) S[r] = fmaf(x[row0 + r], e, S[r]);
+                } else if (w == 0) {
+                    from_f(o + tok * Dv + col, hx);
+                }
+                buf ^= 1;
+            }
+            continue;
+        }
         if (g) {
             const float gt = kExtra ? pro_gate(to_f(g[tok]), pro) : to_f(g[tok]);
 #pragma unroll
@@ -142,8 +194,26 @@ void launch_dk(const Problem &p, dim3 grid, dim3 block)
     TOut *o = (TOut *)p.o;
     auto kernel = (p.prologue != 0 || p.kw != nullptr) ? recurrent_kernel<DK, TIn, TOut, true>
                                                        : recurrent_kernel<DK, TIn, TOut, false>;
-    kernel<<<grid, block, 0, p.stream>>>(p.T, p.H, p.Dv, p.nh, p.cu, p.B, p.max_T, p.prologue, p.status, q, k, v, be,
-                                         g, p.h0, o, p.h_final, kw);
+    if (!p.decode) {
+        kernel<<<grid, block, 0, p.stream>>>(p.T, p.H, p.Dv, p.nh, p.cu, p.B, p.max_T, p.prologue, p.status, q, k, v,
+                                             be, g, p.h0, o, p.h_final, kw);
+        return;
+    }
+    // decode step: programmatic dependent launch, so that consecutive steps
+    // (one launch each, in a loop or a captured graph) overlap their launch
+    // latency with the step before (see griddepcontrol in the kernel)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = p.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, kernel, p.T, p.H, p.Dv, p.nh, p.cu, p.B, p.max_T, p.prologue, p.status, q, k, v, be, g,
+                       p.h0, o, p.h_final, kw);
 }
 
 template <typename TIn, typename TOut>
