@@ -1608,7 +1608,8 @@ __device__ void prep_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const
 // cooperative modes: each consumer warp solves whole chunks on its own
 // (lane i = extended row i), so nothing waits on a group barrier, and
 // producer threads keep the loads and Gram MMAs ahead of them.
-//  * producer thread (one per 8 consumer warps, 4 slots): TMA of the
+//  * producer (one per 8 consumer warps, 4 slots; a loader thread and an
+//    MMA thread, so that load issue and MMA issue overlap): TMA of the
 //    chunk's K and Q tiles into the slot's stage, then one MMA
 //    D = [K-rows at the consumer's TMEM lane quarter] x [K; Q]^T (M = 128,
 //    N = 48: columns 0-31 the Gram row k_i.k_s, columns 32-47 k_i.q_t); the
@@ -1659,23 +1660,62 @@ __device__ __forceinline__ int wstream_next(const Params &p, int idx, int stride
     return next_chunk<kPacked, false, false>(p, idx, stride, total);
 }
 
+// Producer pr's loader thread: the K and Q tiles of its chunks into the
+// slots' stages, each slot once the consumer of the chunk four back has read
+// its accumulator (which also means the Gram MMA that read the stage is done).
 template <bool kPacked>
-__device__ void wprep_producer(const Params &p, const CUtensorMap *tk, const CUtensorMap *tq, uint8_t *base,
-                               uint64_t *bar, uint32_t tcol, int pr, int first, int stride, volatile uint32_t *abort)
+__device__ void wprep_loader(const Params &p, const CUtensorMap *tk, const CUtensorMap *tq, uint8_t *base,
+                             uint64_t *bar, int pr, int first, int stride, volatile uint32_t *abort)
 {
     using J = Job<kPacked, false, false>;
+    const int total = p.n_chunks * p.bh_count, ct = p.ct, R = ct * p.nh;
+    bool ok = true;
+    int issued = 0;
+    int idx = wstream_next<kPacked>(p, first, stride, total);
+    for (int k = 0; idx < total; ++k) {
+        const int sl = k & (kWSlots - 1);
+        if (k >= kWSlots && !(ok = mbar_wait(&bar[sl * 2 + 1], ((k >> 2) - 1) & 1, kWaitTries, abort))) break;
+        const int c = idx / p.bh_count;
+        const J jb = make_job<kPacked, false, false>(p, idx - c * p.bh_count);
+        const int t0 = jb.first() + c * ct;
+        uint64_t *lb = &bar[sl * 2 + 0];
+        uint8_t *stg = base + kWStages + (pr * kWSlots + sl) * kWStage;
+        mbar_arrive_expect_tx(lb, 256u * R + 256u * ct);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+            tma_load_5d(stg + kb * kKQBlock, tk, lb, kb * 64, 0, jb.h, t0, jb.row_b());
+            tma_load_4d(stg + kb * kKQBlock + kC * 128, tq, lb, kb * 64, jb.h, t0, jb.row_b());
+        }
+        issued = k + 1;
+        idx = wstream_next<kPacked>(p, idx + stride, stride, total);
+    }
+    if (!ok) {   // a wait expired: record it; the loads in flight land before smem goes
+        flag_error(p.status, abort, kDevTimeout);
+        uint32_t no_abort = 0;
+        for (int k = issued > kWSlots ? issued - kWSlots : 0; k < issued; ++k)
+            mbar_wait(&bar[(k & (kWSlots - 1)) * 2 + 0], (k >> 2) & 1, kWaitTries, &no_abort);
+    }
+}
+
+// Producer pr's MMA thread: the Gram MMA of each chunk once its tiles have
+// landed (the loader only refills a slot after its accumulator was read, so
+// the MMA never overwrites one still needed), completing on the consumer
+// warp's barrier.
+template <bool kPacked>
+__device__ void wprep_mma(const Params &p, uint8_t *base, uint64_t *bar, uint32_t tcol, int pr, int first, int stride,
+                          volatile uint32_t *abort)
+{
     const int total = p.n_chunks * p.bh_count;
-    constexpr int kLag = 3;   // the Gram MMA of chunk k is issued with the loads of chunk k + kLag (< kWSlots)
     const uint32_t idesc = idesc_bf16(128, kC + kNQ, false, false);
     bool ok = true;
-    int issued_ld = 0, issued_mma = 0;   // chunks whose loads / MMAs were issued
-    auto stage = [&](int k) { return base + kWStages + (pr * kWSlots + (k & (kWSlots - 1))) * kWStage; };
-    auto mma = [&](int k) {
+    int issued = 0;
+    int idx = wstream_next<kPacked>(p, first, stride, total);
+    for (int k = 0; idx < total; ++k) {
         const int sl = k & (kWSlots - 1);
-        if (!mbar_wait(&bar[sl * 2 + 0], (k >> 2) & 1, kWaitTries, abort)) return false;
+        if (!(ok = mbar_wait(&bar[sl * 2 + 0], (k >> 2) & 1, kWaitTries, abort))) break;
         tc_fence_after();
         const int q = (pr * kWConsPerProd + (k & (kWConsPerProd - 1))) & 3;   // consumer warp's lane quarter
-        const uint32_t st = smem_addr(stage(k));
+        const uint32_t st = smem_addr(base + kWStages + (pr * kWSlots + sl) * kWStage);
         const uint32_t d = tcol + sl * 64;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -1683,42 +1723,13 @@ __device__ void wprep_producer(const Params &p, const CUtensorMap *tk, const CUt
             mma_ss(d, sdesc_sw128(st + off - 4096u * q, 16, 1024), sdesc_sw128(st + off, 16, 1024), idesc, kk > 0);
         }
         mma_commit(&bar[2 * kWSlots + (k & (kWConsPerProd - 1))]);
-        return true;
-    };
-    int idx = wstream_next<kPacked>(p, first, stride, total);
-    for (int k = 0; idx < total && ok; ++k) {
-        const int sl = k & (kWSlots - 1);
-        // the slot's previous chunk (k - 4): its consumer has read the accumulator
-        if (k >= kWSlots && !(ok = mbar_wait(&bar[sl * 2 + 1], ((k >> 2) - 1) & 1, kWaitTries, abort))) break;
-        const int c = idx / p.bh_count;
-        const J jb = make_job<kPacked, false, false>(p, idx - c * p.bh_count);
-        const int ct = p.ct, R = ct * p.nh, t0 = jb.first() + c * ct;
-        uint64_t *lb = &bar[sl * 2 + 0];
-        uint8_t *stg = stage(k);
-        mbar_arrive_expect_tx(lb, 256u * R + 256u * ct);
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-            tma_load_5d(stg + kb * kKQBlock, tk, lb, kb * 64, 0, jb.h, t0, jb.row_b());
-            tma_load_4d(stg + kb * kKQBlock + kC * 128, tq, lb, kb * 64, jb.h, t0, jb.row_b());
-        }
-        issued_ld = k + 1;
-        if (k >= kLag) {
-            if (!(ok = mma(k - kLag))) break;
-            issued_mma = k - kLag + 1;
-        }
+        issued = k + 1;
         idx = wstream_next<kPacked>(p, idx + stride, stride, total);
     }
-    for (int k = issued_mma; ok && k < issued_ld; ++k) {
-        if (!(ok = mma(k))) break;
-        issued_mma = k + 1;
-    }
-    if (!ok) {   // a wait expired: record it, let what was issued finish before smem and TMEM go
+    if (!ok) {   // a wait expired: record it; the MMAs issued retire before TMEM goes
         flag_error(p.status, abort, kDevTimeout);
         uint32_t no_abort = 0;
-        for (int k = issued_mma; k < issued_ld; ++k)   // loads without their MMA
-            mbar_wait(&bar[(k & (kWSlots - 1)) * 2 + 0], (k >> 2) & 1, kWaitTries, &no_abort);
-        // the last MMA of each consumer (its phase is the barrier's latest)
-        for (int k = issued_mma > kWConsPerProd ? issued_mma - kWConsPerProd : 0; k < issued_mma; ++k)
+        for (int k = issued > kWConsPerProd ? issued - kWConsPerProd : 0; k < issued; ++k)
             mbar_wait(&bar[2 * kWSlots + (k & (kWConsPerProd - 1))], (k >> 3) & 1, kWaitTries, &no_abort);
     }
 }
@@ -1846,8 +1857,9 @@ __device__ void wprep_consumer(const Params &p, uint8_t *scr, uint64_t *bar, uin
     }
 }
 
-// A prep CTA (kThreads threads): warps 0-15 consumers, warps 16 and 17 the
-// producers of consumers 0-7 and 8-15. Producer pr's chunk stream is every
+// A prep CTA (kThreads threads): warps 0-15 consumers; for consumers 0-7
+// and 8-15 the MMA threads of warps 16 and 17 and the loader threads of
+// warps 18 and 19. Producer pr's chunk stream is every
 // (2 n_pcta)-th chunk of the chunk-major order from 2 pcta + pr.
 template <bool kPacked>
 __device__ void wprep_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const Params &p, int pcta, int n_pcta,
@@ -1881,8 +1893,10 @@ __device__ void wprep_cta(const CUtensorMap &tm_k, const CUtensorMap &tm_q, cons
                                 2 * pcta + pr, 2 * n_pcta, publish, abort);
     } else if (warp < kWCons + 2 && lane == 0) {
         const int pr = warp - kWCons;
-        wprep_producer<kPacked>(p, &tm_k, &tm_q, base, bar + pr * kWBars, tbase + pr * 256, pr, 2 * pcta + pr,
-                                2 * n_pcta, abort);
+        wprep_mma<kPacked>(p, base, bar + pr * kWBars, tbase + pr * 256, pr, 2 * pcta + pr, 2 * n_pcta, abort);
+    } else if (warp < kWCons + 4 && lane == 0) {
+        const int pr = warp - kWCons - 2;
+        wprep_loader<kPacked>(p, &tm_k, &tm_q, base, bar + pr * kWBars, pr, 2 * pcta + pr, 2 * n_pcta, abort);
     }
     tc_fence_before();
     __syncthreads();

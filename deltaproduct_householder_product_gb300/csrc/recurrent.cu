@@ -158,10 +158,10 @@ recurrent_kernel(int T, int H, int Dv, int nh, const int *cu, int N, int max_T, 
                 if (kExtra && kw && j < nh) kwbuf[buf][threadIdx.x] = to_f(kw[(tok * nh + j) * DK + threadIdx.x]);
             }
             __syncthreads();
-            float acc = 0.f;
+            float a4[4] = {0.f, 0.f, 0.f, 0.f};   // the plain instantiation's summation order
 #pragma unroll
-            for (int r = 0; r < R; ++r) acc = fmaf(S[r], kbuf[buf][row0 + r], acc);
-            part[buf][w][lane] = acc;
+            for (int r = 0; r < R; ++r) a4[r & 3] = fmaf(S[r], kbuf[buf][row0 + r], a4[r & 3]);
+            part[buf][w][lane] = (a4[0] + a4[1]) + (a4[2] + a4[3]);
             __syncthreads();
             float hx = 0.f;
 #pragma unroll
