@@ -754,13 +754,31 @@ __device__ __forceinline__ float ls_after(float ls, float lgc)
     return x < kRenormLog ? 0.f : x;
 }
 
-// log Gamma_C of chunk c: the chunk's cumulative log-gate at its last row,
-// by the same loads and the same scan as scan_rows (so it equals the L[kC-1]
+// log Gamma_C of a chunk (its cumulative log-gate at its last row) in two
+// steps, so that the load runs ahead of its use: gate_raw fetches row
+// `lane`'s raw bf16 gate (its token's gate on the token's first row, by the
+// read-only path so that the load may be issued before the stores that
+// precede its use), or kNoGate; gate_lgc makes the same per-row values and
+// the same scan as load_rows and scan_rows (so the result equals the L[kC-1]
 // the prep side computes for that chunk, bit for bit). Whole warp.
+constexpr uint32_t kNoGate = 0xFFFFFFFFu;
 template <class J>
-__device__ __forceinline__ float chunk_lgc(const Params &p, const J &jb, int c, int lane)
+__device__ __forceinline__ uint32_t gate_raw(const Params &p, const J &jb, int c, int lane)
 {
-    float lg = load_rows(p, jb, c, lane).lg;
+    const int nh = p.nh, R = p.ct * nh, tl = lane / nh, j = lane - tl * nh, t = c * p.ct + tl;
+    if (c < jb.chunks(p) && lane < R && j == 0 && t < jb.tokens(p))
+        return (uint32_t)__ldg((const unsigned short *)p.g + tok_row(p, jb, t));
+    return kNoGate;
+}
+
+template <class J>
+__device__ __forceinline__ float gate_lgc(const Params &p, uint32_t raw, int lane)
+{
+    float lg = 0.f;
+    if (raw != kNoGate) {
+        const float x = __uint_as_float(raw << 16);   // the bf16 value, exactly
+        lg = J::kPro ? pro_log_gate(x, p.prologue) : fmaxf(logf(x), -80.f);
+    }
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
         const float y = __shfl_up_sync(0xffffffffu, lg, d);
@@ -1019,17 +1037,17 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
     const uint32_t bar_id = 1 + g;
     uint8_t *gt = s.group(g);
     const bool gated = p.g != nullptr;
-    // gated: log sigma before chunk ls_at (see kRenormLog); advanced over
-    // every chunk, the other group's included, and the group's own last
-    // chunk's log Gamma_C kept so that only the other group's is recomputed
+    // gated: log sigma before the group's chunk (see kRenormLog), folded
+    // over every chunk in order: the group's own previous chunk (c - 2, its
+    // log Gamma_C kept) and the other group's (c - 1, its gates fetched one
+    // iteration ahead)
     float ls = 0.f, lgc_own = 0.f;
-    int ls_at = 0, lgc_own_c = -1;
+    bool have_own = false;
+    uint32_t graw_other = (p.g != nullptr && g == 1) ? gate_raw(p, jb, 0, lane) : kNoGate;
     auto advance_ls = [&](int c) {
-        while (ls_at < c) {
-            const float l = (ls_at == lgc_own_c) ? lgc_own : chunk_lgc(p, jb, ls_at, lane);
-            ls = ls_after(ls, l);
-            ++ls_at;
-        }
+        if (have_own) ls = ls_after(ls, lgc_own);
+        if (c >= 1) ls = ls_after(ls, gate_lgc<J>(p, graw_other, lane));
+        graw_other = gate_raw(p, jb, c + 1, lane);
     };
 
     if (kSplit) {
@@ -1063,7 +1081,7 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
                 mbar_arrive(&s.bar[kBarEmpty + st]);
             }
             lgc_own = lgc;
-            lgc_own_c = c;
+            have_own = true;
         }
         return;
     }
@@ -1107,7 +1125,7 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
             mbar_arrive(&s.bar[kBarEmpty + st]);
         }
         lgc_own = lgc;
-        lgc_own_c = c;
+        have_own = true;
     }
 }
 
@@ -1163,9 +1181,11 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, const J
     bool failed = false;
     float ls = 0.f;
     uint32_t n_renorm = 0;
+    uint32_t graw = gated ? gate_raw(p, jb, 0, lane) : kNoGate;   // gates one chunk ahead
     for (int c = 0; c < jb.chunks(p); ++c) {
         const int g = c & 1, t0 = c * p.ct;
-        const float lgc = gated ? chunk_lgc(p, jb, c, lane) : 0.f;
+        const float lgc = gated ? gate_lgc<J>(p, graw, lane) : 0.f;
+        if (gated) graw = gate_raw(p, jb, c + 1, lane);
         if (gated && renorm_at(ls, lgc)) {
             // S^ <- sigma_c Gamma_C S^ between the chunk's two state-pass halves
             const float gC = __expf(ls + lgc);
@@ -1183,7 +1203,7 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, const J
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&s.bar[kBarScaled]);
+            if (lane == 0) mbar_arrive_relaxed(&s.bar[kBarScaled]);   // TMEM only, as OFree below
         }
         ls = ls_after(ls, lgc);
         if (!warp_wait(s, kBarM2 + g, (c >> 1) & 1, p.status)) { failed = true; break; }
@@ -1202,7 +1222,9 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, const J
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s.bar[kBarOFree + g]);
+        // relaxed: the chain needs only the TMEM clears above (complete after
+        // wait::st), not this warp's output stores of the previous chunk
+        if (lane == 0) mbar_arrive_relaxed(&s.bar[kBarOFree + g]);
         if (ws_out) {
             float *oc = w_seq + (size_t)t0 * tok_stride;
 #pragma unroll
