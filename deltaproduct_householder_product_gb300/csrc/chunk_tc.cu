@@ -179,7 +179,7 @@ struct Layout {
     static constexpr uint32_t kOffBar = kOffScratch + 2 * kScratch;
 };
 
-constexpr uint32_t kNumBars = 2 * kNS + 2 * 8 + 7;
+constexpr uint32_t kNumBars = 2 * kNS + 2 * 6 + 7;
 template <bool kSplit>
 constexpr uint32_t smem_bytes() { return Layout<kSplit>::kOffBar + kNumBars * 8 + 16 + 1024; }
 static_assert(smem_bytes<true>() <= 227 * 1024 && smem_bytes<false>() <= 227 * 1024, "shared memory");
@@ -357,9 +357,7 @@ enum : int {
     kBarInit,                     // initial state in TMEM
     kBarFinal,                    // [2] every MMA of an issuer retired (teardown)
     kBarNorm = kBarFinal + 2,     // [2] prologue applied to the group's stage (fused mode with a prologue)
-    kBarW = kBarNorm + 2,         // [2] W MMA done (split modes: issued as soon as W's TMEM buffer is read)
-    kBarU = kBarW + 2,            // [2] U MMA done (split modes, ungated: issued by the prep MMA thread)
-    kBarCount = kBarU + 2
+    kBarCount = kBarNorm + 2
 };
 static_assert(kBarCount == (int)kNumBars, "barrier count");
 
@@ -557,38 +555,8 @@ __device__ void prep_mma_role(const Smem &s, const Params &p, uint32_t tbase, in
 
     bool ok = true;
     if (kSplit) {
-        // W of chunk c as soon as its stage has landed and phase B of chunk
-        // c - 2 has read W's buffer (TMEM columns only phase B reads). U of
-        // chunk c: gated, the chain thread issues it just before the chunk's
-        // state pass (in order with the MMAs that accumulate onto it);
-        // ungated, this thread issues it once the state pass of chunk c - 2
-        // (which read U'[c % 2]) is done, and phase B waits for it (with the
-        // shorter ungated phase B, two issuing threads beat one).
-        for (int c = 0; c < n && ok; ++c) {
-            const int g = c & 1;
-            const uint32_t kq = smem_addr(s.stage(c % kNS)), vv = kq + 2 * kKQBlock;
-            const uint32_t tt = kq + kStageIn + kRecT, tg = tt + (gated ? 2 * kTTile : 0);
-            if (!(ok = wait_bar(s, kBarFull + c % kNS, (c / kNS) & 1, p.status))) break;
-            if (c >= 2 && !(ok = wait_bar(s, kBarReady + g, ((c - 2) >> 1) & 1, p.status))) break;
-            tc_fence_after();
-#pragma unroll
-            for (int part = 0; part < 2; ++part)
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk)
-                    mma_ss(tbase + kColW + g * 32, sdesc_sw128(kq + kk * 2048, kKQBlock, 1024),
-                           sdesc_sw128(tg + part * kTTile + kk * 32, 16, 1024), id_uw, part | kk);
-            mma_commit(&s.bar[kBarW + g]);
-            if (gated) continue;
-            if (c >= 2 && !(ok = wait_bar(s, kBarM2 + g, ((c - 2) >> 1) & 1, p.status))) break;
-            tc_fence_after();
-#pragma unroll
-            for (int part = 0; part < 2; ++part)
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk)
-                    mma_ss(tbase + col_un(g), sdesc_sw128(vv + kk * 2048, kVBlock, 1024),
-                           sdesc_sw128(tt + part * kTTile + kk * 32, 16, 1024), id_uw, part | kk);
-            mma_commit(&s.bar[kBarU + g]);
-        }
+        for (int c = 0; c < n && ok; ++c)
+            if ((ok = uw_ready(c))) issue_uw(c);
     } else {
         for (int c = 0; c < n && ok; ++c) {
             ok = kPro ? wait_bar(s, kBarNorm + (c & 1), (c >> 1) & 1, p.status)
@@ -613,13 +581,11 @@ __device__ void prep_mma_role(const Smem &s, const Params &p, uint32_t tbase, in
 //   [U'^T | O_b] += S^T [-W; Gamma q]^T          (16 instructions, N = 48)
 //   [S^T | O_a] or [O_a | S^T] += U'^T [K^T; P]   (4 instructions, N = 144)
 // Consecutive MMAs run in issue order, so S -> U' -> S needs no round trip.
-template <bool kSplit>
 __device__ void chain_role(const Smem &s, const Params &p, uint32_t tbase, int n)
 {
     const bool gated = p.g != nullptr;
     const uint32_t id_x = idesc_tf32(128, kXRows);
     const uint32_t id_y = idesc_tf32(128, kYRows);
-    const uint32_t id_u = idesc_bf16(128, kC, true, false);
     bool ok = wait_bar(s, kBarInit, 0, p.status);
     uint32_t n_renorm = 0;
     for (int c = 0; c < n && ok; ++c) {
@@ -628,20 +594,6 @@ __device__ void chain_role(const Smem &s, const Params &p, uint32_t tbase, int n
         if (!(ok = wait_bar(s, kBarReady + g, (c >> 1) & 1, p.status))) break;
         if (c >= 2 && !(ok = wait_bar(s, kBarOFree + g, ((c - 2) >> 1) & 1, p.status))) break;
         tc_fence_after();
-        if (kSplit && gated) {
-            // U^T = V^T (T diag(beta))^T into U'[g]: issued here, in front of
-            // the chunk's state pass, so that the tensor pipe runs it in order
-            // with the MMAs that accumulate onto it (its stage landed before
-            // phase B signalled the chunk ready)
-            const uint32_t kq = smem_addr(s.stage(c % kNS)), vv = kq + 2 * kKQBlock;
-            const uint32_t tt = kq + kStageIn + kRecT;
-#pragma unroll
-            for (int part = 0; part < 2; ++part)
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk)
-                    mma_ss(tbase + col_un(g), sdesc_sw128(vv + kk * 2048, kVBlock, 1024),
-                           sdesc_sw128(tt + part * kTTile + kk * 32, 16, 1024), id_u, part | kk);
-        }
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk)
             mma_ts_tf32(tbase + col_un(g), tbase + kColS + kk * 8,
@@ -657,7 +609,6 @@ __device__ void chain_role(const Smem &s, const Params &p, uint32_t tbase, int n
         for (int kk = 0; kk < 4; ++kk)
             mma_ts_tf32(d_y, tbase + col_un(g) + kk * 8, sdesc_sw128(gb + kGY + kk * 32, 16, 1024), id_y, 1);
         mma_commit(&s.bar[kBarM2 + g]);
-        if (kSplit && gated) mma_commit(&s.bar[kBarEmpty + c % kNS]);   // U has read the stage
     }
     mma_commit(&s.bar[kBarFinal]);
     uint32_t no_abort = 0;
@@ -913,7 +864,6 @@ __device__ __forceinline__ int y_row_p(int g) { return g ? kD : 0; }
 // `Psrc` (row stride `pld` floats), the cumulative log-gates from `L_s`, K
 // and Q from the stage at `kq`. Returns false, uniformly over the group, if a
 // wait failed or the CTA is aborting.
-template <bool kSplit>
 __device__ bool phase_b(const Smem &s, const Params &p, uint32_t tbase, uint8_t *gt,
                         const uint8_t *kq, const float *Psrc, int pld, const float *L_s, int c,
                         int g, int lt, uint32_t bar_id, float ls_cur, float ls_next,
@@ -923,69 +873,62 @@ __device__ bool phase_b(const Smem &s, const Params &p, uint32_t tbase, uint8_t 
     const int lw = lt >> 5, lane = lt & 31, lq = lw & 3, hf = lw >> 2;
     const int nh = p.nh, ct = p.ct;
     const bool gated = p.g != nullptr;
-    // Every value that does not need the group's buffer is computed first,
-    // into registers, so that the work left after the buffer frees (the
-    // state pass of chunk c - 2 retires) is stores only.
+    bool ok = (c < 2 || lt != 0) || wait_bar(s, kBarM2 + g, ((c - 2) >> 1) & 1, p.status);
+    if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) return false;
     // P (16 rows x 8 float4)
-    float4 pv = make_float4(0.f, 0.f, 0.f, 0.f);
     if (lt < kNQ * 8) {
-        const float *src = Psrc + (lt >> 3) * pld + 4 * (lt & 7);
-        pv = make_float4(src[0], src[1], src[2], src[3]);
+        const int i = lt >> 3, ch = lt & 7;
+        const float *src = Psrc + i * pld + 4 * ch;
+        *(float4 *)(gt + kGY + sw128_offset(y_row_p(g) + i, ch)) = make_float4(src[0], src[1], src[2], src[3]);
     }
     // Gamma-scaled q: (token row i, dk block kb4, 8-element group q)
-    const int qi = lt >> 4, qkb4 = (lt >> 2) & 3, qq = lt & 3;
-    float gq[8];
     {
-        const float gr = qi >= ct ? 0.f : (gated ? __expf(L_s[qi * nh + nh - 1] + ls_cur) : 1.f);
-        const uint4 u = *(const uint4 *)(kq + (qkb4 >> 1) * kKQBlock + sw128_offset(kC + qi, (qkb4 & 1) * 4 + qq));
+        const int i = lt >> 4, kb4 = (lt >> 2) & 3, q = lt & 3;
+        const bool valid = i < ct;
+        const float gr = !valid ? 0.f : (gated ? __expf(L_s[i * nh + nh - 1] + ls_cur) : 1.f);
+        const uint4 u = *(const uint4 *)(kq + (kb4 >> 1) * kKQBlock + sw128_offset(kC + i, (kb4 & 1) * 4 + q));
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        float f[8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            gq[2 * e] = __uint_as_float(w[e] << 16) * gr;
-            gq[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u) * gr;
+            f[2 * e] = __uint_as_float(w[e] << 16) * gr;
+            f[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u) * gr;
         }
+        uint8_t *dst = gt + kGX + kb4 * kXBlock;
+        *(float4 *)(dst + sw128_offset(kC + i, 2 * q)) = make_float4(f[0], f[1], f[2], f[3]);
+        *(float4 *)(dst + sw128_offset(kC + i, 2 * q + 1)) = make_float4(f[4], f[5], f[6], f[7]);
     }
     // decayed K^T (write keys: decayed K~^T, from kw16 = this thread's 16
     // values, or from the K~ tile at ksrc with blocks kblock bytes apart):
     // row dk, four groups of 4 chunk rows per thread
-    const int dk = lt & 127, q0 = (lt >> 7) * 4;
-    float kd[4][4];
     {
+        const int dk = lt & 127, q0 = (lt >> 7) * 4;
         const float Lend = L_s[kC - 1] - ls_next;
         const uint8_t *src = (ksrc ? ksrc : kq) + (dk >> 6) * kblock;
         const int chunk = (dk & 63) >> 3, e = dk & 7;
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = q0; q < q0 + 4; ++q) {
+            float f[4];
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
-                const int s2 = 4 * (q0 + q) + k4;
+                const int s2 = 4 * q + k4;
                 const float x = kw16 ? kw16[s2 - 4 * q0]
                                      : __bfloat162float(*(const __nv_bfloat16 *)(src + sw128_offset(s2, chunk) + e * 2));
-                kd[q][k4] = gated ? x * __expf(Lend - L_s[s2]) : x;
+                f[k4] = gated ? x * __expf(Lend - L_s[s2]) : x;
             }
+            *(float4 *)(gt + kGY + sw128_offset(y_row_k(g) + dk, q)) = make_float4(f[0], f[1], f[2], f[3]);
+        }
     }
-    // the buffer is free once the state pass of chunk c - 2 has retired
-    bool ok = (c < 2 || lt != 0) || wait_bar(s, kBarM2 + g, ((c - 2) >> 1) & 1, p.status);
-    if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) return false;
-    if (lt < kNQ * 8) *(float4 *)(gt + kGY + sw128_offset(y_row_p(g) + (lt >> 3), lt & 7)) = pv;
-    {
-        uint8_t *dst = gt + kGX + qkb4 * kXBlock;
-        *(float4 *)(dst + sw128_offset(kC + qi, 2 * qq)) = make_float4(gq[0], gq[1], gq[2], gq[3]);
-        *(float4 *)(dst + sw128_offset(kC + qi, 2 * qq + 1)) = make_float4(gq[4], gq[5], gq[6], gq[7]);
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        *(float4 *)(gt + kGY + sw128_offset(y_row_k(g) + dk, q0 + q)) = make_float4(kd[q][0], kd[q][1], kd[q][2], kd[q][3]);
     // -W (lane = dk; half hf takes chunk rows 16*hf .. 16*hf + 15)
-    ok = (lt != 0) || wait_bar(s, (kSplit ? kBarW : kBarUW) + g, (c >> 1) & 1, p.status);
+    ok = (lt != 0) || wait_bar(s, kBarUW + g, (c >> 1) & 1, p.status);
     if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) return false;
     tc_fence_after();
     {
         uint32_t r[16];
         tmem_ld16(tbase + ((uint32_t)(lq * 32) << 16) + kColW + g * 32 + 16 * hf, r);
         tmem_wait_ld();
-        const int dkw = 32 * lq + lane, pos = dkw & 31;
-        uint8_t *dst = gt + kGX + (dkw >> 5) * kXBlock + (pos & 3) * 4;
+        const int dk = 32 * lq + lane, pos = dk & 31;
+        uint8_t *dst = gt + kGX + (dk >> 5) * kXBlock + (pos & 3) * 4;
         const float nsig = gated ? -__expf(ls_cur) : -1.f;
 #pragma unroll
         for (int j = 0; j < 16; ++j)
@@ -993,9 +936,8 @@ __device__ bool phase_b(const Smem &s, const Params &p, uint32_t tbase, uint8_t 
     }
     fence_proxy_async_smem();
     tc_fence_before();
-    // split modes, ungated: U (into U'[g]) is complete before the chain's first MMA of the chunk
-    ok = !kSplit || gated || lt != 0 || wait_bar(s, kBarU + g, (c >> 1) & 1, p.status);
-    return !group_any(bar_id, kPrepThreads, !ok || *s.abort);
+    named_sync(bar_id, kPrepThreads);
+    return true;
 }
 
 // Write keys of chunk c for phase B's decayed K~^T: thread lt's column
@@ -1069,7 +1011,7 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
             const float *Lrec = (const float *)(rec + kRecL);
             const float lgc = gated ? Lrec[kC - 1] : 0.f, ls_next = ls_after(ls, lgc);
             // (with a key/query prologue the stage's K and Q arrive mapped, from the record)
-            if (!phase_b<true>(s, p, tbase, gt, kq, (const float *)(rec + kRecP), kC, Lrec, c, g, lt, bar_id, ls,
+            if (!phase_b(s, p, tbase, gt, kq, (const float *)(rec + kRecP), kC, Lrec, c, g, lt, bar_id, ls,
                          ls_next, kw_global ? kwv : nullptr, (J::kWK && !gated) ? rec + kRecKW : nullptr,
                          (J::kWK && !gated) ? kKWBlock : kKQBlock))
                 break;
@@ -1118,7 +1060,7 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
         named_sync(bar_id, kPrepThreads);
         if (lt == 0) mbar_arrive(&s.bar[kBarTb + g]);
         const float lgc = gated ? w.L_s[kC - 1] : 0.f, ls_next = ls_after(ls, lgc);
-        if (!phase_b<false>(s, p, tbase, gt, kq, w.Ps, kLd, w.L_s, c, g, lt, bar_id, ls, ls_next)) break;
+        if (!phase_b(s, p, tbase, gt, kq, w.Ps, kLd, w.L_s, c, g, lt, bar_id, ls, ls_next)) break;
         if (lt == 0) {
             s.renorm[g] = (gated && renorm_at(ls, lgc)) ? 1u : 0u;
             mbar_arrive(&s.bar[kBarReady + g]);
@@ -1281,10 +1223,7 @@ __device__ __forceinline__ void state_pass_cta(const CUtensorMap &tm_k, const CU
         *(uint4 *)(s.base + i) = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
         for (int i = 0; i < (int)kNumBars; ++i)
-            // split modes, gated: a stage is released by its prep group and by
-            // the chain's commit after the U MMA that reads it
-            mbar_init(&s.bar[i], (i == kBarOFree || i == kBarOFree + 1 || i == kBarScaled) ? kPrepWarp
-                                 : (kSplit && p.g && i >= kBarEmpty && i < kBarEmpty + kNS) ? 2 : 1);
+            mbar_init(&s.bar[i], (i == kBarOFree || i == kBarOFree + 1 || i == kBarScaled) ? kPrepWarp : 1);
         *s.abort = 0;
         fence_mbar_init();
     }
@@ -1307,7 +1246,7 @@ __device__ __forceinline__ void state_pass_cta(const CUtensorMap &tm_k, const CU
     } else if (warp == kTmaWarp) {
         if (lane == 0) tma_role<kSplit, kCoop>(s, p, &tm_k, &tm_v, &tm_q, jb);
     } else if (warp == kChainWarp) {
-        if (lane == 0) chain_role<kSplit>(s, p, tbase, jb.chunks(p));
+        if (lane == 0) chain_role(s, p, tbase, jb.chunks(p));
     } else {
         if (lane == 0) prep_mma_role<kSplit, kPro>(s, p, tbase, jb.chunks(p));
     }
