@@ -167,6 +167,10 @@ __host__ __device__ constexpr uint32_t record_stride(int prologue)
 }
 static_assert(record_stride(DP_PRO_KEY_SILU_L2) % 16 == 0, "bulk copies move 16-byte multiples");
 
+// Output staging of one epilogue warp: a chunk's kNQ token rows of its 32
+// value columns (fp32 rows of 128 B, bf16 rows of 64 B).
+constexpr uint32_t kOutTile = kNQ * 128;
+
 // Shared-memory layout of the state-pass kernel in each mode.
 template <bool kSplit>
 struct Layout {
@@ -176,10 +180,11 @@ struct Layout {
     static constexpr uint32_t kScratch = kSplit ? 0 : kPrepScratch;
     static constexpr uint32_t kOffGroup = kNS * kStage;
     static constexpr uint32_t kOffScratch = kOffGroup + 2 * kGroup;
-    static constexpr uint32_t kOffBar = kOffScratch + 2 * kScratch;
+    static constexpr uint32_t kOffOut = kOffScratch + 2 * kScratch;
+    static constexpr uint32_t kOffBar = kOffOut + 4 * kOutTile;
 };
 
-constexpr uint32_t kNumBars = 2 * kNS + 2 * 6 + 7;
+constexpr uint32_t kNumBars = 2 * kNS + 2 * 7 + 7;
 template <bool kSplit>
 constexpr uint32_t smem_bytes() { return Layout<kSplit>::kOffBar + kNumBars * 8 + 16 + 1024; }
 static_assert(smem_bytes<true>() <= 227 * 1024 && smem_bytes<false>() <= 227 * 1024, "shared memory");
@@ -349,8 +354,9 @@ enum : int {
     kBarGQ = kBarEmpty + kNS,     // [2] Gram MMA of the group's chunk done (fused)
     kBarTb = kBarGQ + 2,          // [2] T tiles written (fused)
     kBarUW = kBarTb + 2,          // [2] U and W MMAs done
-    kBarReady = kBarUW + 2,       // [2] state-pass B tiles written
-    kBarM2 = kBarReady + 2,       // [2] chunk's state pass and readout done
+    kBarReady = kBarUW + 2,       // [2] X = [-W; Gamma q] written
+    kBarReadyY = kBarReady + 2,   // [2] Y = decayed K^T and P written, stage read
+    kBarM2 = kBarReadyY + 2,      // [2] chunk's state pass and readout done
     kBarOFree = kBarM2 + 2,       // [2] O buffers drained by the epilogue (one arrival per warp)
     kBarM1 = kBarOFree + 2,       // first half (U', S^T q) done (gated, rescaling chunks only)
     kBarScaled,                   // stored state rescaled (gated; one arrival per epilogue warp)
@@ -367,8 +373,9 @@ struct Smem {
     uint32_t *tmem_slot;
     volatile uint32_t *abort;
     volatile uint32_t *renorm;   // [2] gated: the group's chunk rescales the stored state (see epi_role)
-    uint32_t stage_bytes, group_off, group_bytes, scratch_off;
+    uint32_t stage_bytes, group_off, group_bytes, scratch_off, out_off;
     __device__ uint8_t *stage(int st) const { return base + st * stage_bytes; }
+    __device__ uint8_t *out_tile(int warp) const { return base + out_off + warp * kOutTile; }
     __device__ uint8_t *group(int g) const { return base + group_off + g * group_bytes; }
     __device__ uint8_t *scratch(int g) const { return base + scratch_off + g * kPrepScratch; }
 };
@@ -417,6 +424,35 @@ __device__ __forceinline__ void split_pack(float a, float b, uint32_t &hi, uint3
 
 __device__ __forceinline__ void store_out(float *o, size_t i, float x) { o[i] = x; }
 __device__ __forceinline__ void store_out(__nv_bfloat16 *o, size_t i, float x) { o[i] = __float2bfloat16_rn(x); }
+
+// One chunk's outputs from one epilogue warp: lane = value column (32 of
+// them, from o0 on), v[i] = token i's value, rows 0 .. n_rows-1 stored, row
+// i at o0 + i * tok_stride. The block turns around in the warp's staging
+// tile so that each lane stores 16 contiguous bytes (4 lanes per bf16 row, 8
+// per fp32 row): a few wide stores instead of one 2- or 4-byte store per
+// token. o0 is 16-byte aligned (o is, and the column block starts at a
+// multiple of 32 elements).
+template <typename T>
+__device__ __forceinline__ void store_rows(T *o0, size_t tok_stride, const uint32_t (&v)[kNQ], int n_rows,
+                                           uint8_t *stg, int lane)
+{
+    constexpr int kRowB = 32 * (int)sizeof(T);   // bytes of a row
+    constexpr int kLanesRow = kRowB / 16;
+    constexpr int kRowsPer = 32 / kLanesRow;      // rows per store instruction
+    __syncwarp();   // the previous chunk's reads of the tile are done
+#pragma unroll
+    for (int i = 0; i < kNQ; ++i)
+        if (i < n_rows) store_out((T *)(stg + i * kRowB), lane, __uint_as_float(v[i]));
+    __syncwarp();
+    const int r0 = lane / kLanesRow, piece = lane % kLanesRow;
+#pragma unroll
+    for (int k = 0; k < kNQ / kRowsPer; ++k) {
+        const int r = r0 + k * kRowsPer;
+        if (r < n_rows)
+            *(uint4 *)((uint8_t *)(o0 + (size_t)r * tok_stride) + piece * 16) =
+                *(const uint4 *)(stg + r * kRowB + piece * 16);
+    }
+}
 
 // Gram MMA [K;Q] K^T of the chunk in the KQ tiles at `kq` (A = 64 rows: K
 // rows 0-31, Q rows 32-47, zero rows; B = the K rows), into 32 TMEM columns.
@@ -604,6 +640,9 @@ __device__ void chain_role(const Smem &s, const Params &p, uint32_t tbase, int n
             ++n_renorm;
             tc_fence_after();
         }
+        // the Y tile is written while the first half runs
+        if (!(ok = wait_bar(s, kBarReadyY + g, (c >> 1) & 1, p.status))) break;
+        tc_fence_after();
         const uint32_t d_y = g ? tbase + kColS : tbase + kColOa0;   // O_a[0] | S  or  S | O_a[1]
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
@@ -860,27 +899,25 @@ __device__ void phase_a(const PrepScratch &w, uint32_t tbase, uint32_t gq_col, u
 __device__ __forceinline__ int y_row_k(int g) { return g ? 0 : kNQ; }
 __device__ __forceinline__ int y_row_p(int g) { return g ? kD : 0; }
 
-// Phase B of chunk c (group g): the state pass's fp32 B tiles. P comes from
-// `Psrc` (row stride `pld` floats), the cumulative log-gates from `L_s`, K
-// and Q from the stage at `kq`. Returns false, uniformly over the group, if a
-// wait failed or the CTA is aborting.
-__device__ bool phase_b(const Smem &s, const Params &p, uint32_t tbase, uint8_t *gt,
+// Phase B of chunk c (group g, stage st): the state pass's fp32 B tiles. P
+// comes from `Psrc` (row stride `pld` floats), the cumulative log-gates from
+// `L_s`, K and Q from the stage at `kq`. X = [-W; Gamma q] is signalled
+// first (the chain starts the chunk's first half on it), then Y = [K^T; P]
+// (decayed K^T, needed by the second half only) together with the release
+// of the stage. `renorm` is the chunk's rescale flag for the chain. Returns
+// false, uniformly over the group, if a wait failed or the CTA is aborting.
+__device__ __forceinline__ bool phase_b_gated(const Smem &s, const Params &p, uint32_t tbase, uint8_t *gt,
                         const uint8_t *kq, const float *Psrc, int pld, const float *L_s, int c,
-                        int g, int lt, uint32_t bar_id, float ls_cur, float ls_next,
+                        int g, int st, int lt, uint32_t bar_id, float ls_cur, float ls_next, bool renorm,
                         const float *kw16 = nullptr, const uint8_t *ksrc = nullptr,
                         uint32_t kblock = kKQBlock)
 {
     const int lw = lt >> 5, lane = lt & 31, lq = lw & 3, hf = lw >> 2;
     const int nh = p.nh, ct = p.ct;
-    const bool gated = p.g != nullptr;
+    constexpr bool gated = true;
+    // the group's tiles are free once the state pass of chunk c - 2 has retired
     bool ok = (c < 2 || lt != 0) || wait_bar(s, kBarM2 + g, ((c - 2) >> 1) & 1, p.status);
     if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) return false;
-    // P (16 rows x 8 float4)
-    if (lt < kNQ * 8) {
-        const int i = lt >> 3, ch = lt & 7;
-        const float *src = Psrc + i * pld + 4 * ch;
-        *(float4 *)(gt + kGY + sw128_offset(y_row_p(g) + i, ch)) = make_float4(src[0], src[1], src[2], src[3]);
-    }
     // Gamma-scaled q: (token row i, dk block kb4, 8-element group q)
     {
         const int i = lt >> 4, kb4 = (lt >> 2) & 3, q = lt & 3;
@@ -897,27 +934,6 @@ __device__ bool phase_b(const Smem &s, const Params &p, uint32_t tbase, uint8_t 
         uint8_t *dst = gt + kGX + kb4 * kXBlock;
         *(float4 *)(dst + sw128_offset(kC + i, 2 * q)) = make_float4(f[0], f[1], f[2], f[3]);
         *(float4 *)(dst + sw128_offset(kC + i, 2 * q + 1)) = make_float4(f[4], f[5], f[6], f[7]);
-    }
-    // decayed K^T (write keys: decayed K~^T, from kw16 = this thread's 16
-    // values, or from the K~ tile at ksrc with blocks kblock bytes apart):
-    // row dk, four groups of 4 chunk rows per thread
-    {
-        const int dk = lt & 127, q0 = (lt >> 7) * 4;
-        const float Lend = L_s[kC - 1] - ls_next;
-        const uint8_t *src = (ksrc ? ksrc : kq) + (dk >> 6) * kblock;
-        const int chunk = (dk & 63) >> 3, e = dk & 7;
-#pragma unroll
-        for (int q = q0; q < q0 + 4; ++q) {
-            float f[4];
-#pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-                const int s2 = 4 * q + k4;
-                const float x = kw16 ? kw16[s2 - 4 * q0]
-                                     : __bfloat162float(*(const __nv_bfloat16 *)(src + sw128_offset(s2, chunk) + e * 2));
-                f[k4] = gated ? x * __expf(Lend - L_s[s2]) : x;
-            }
-            *(float4 *)(gt + kGY + sw128_offset(y_row_k(g) + dk, q)) = make_float4(f[0], f[1], f[2], f[3]);
-        }
     }
     // -W (lane = dk; half hf takes chunk rows 16*hf .. 16*hf + 15)
     ok = (lt != 0) || wait_bar(s, kBarUW + g, (c >> 1) & 1, p.status);
@@ -937,7 +953,135 @@ __device__ bool phase_b(const Smem &s, const Params &p, uint32_t tbase, uint8_t 
     fence_proxy_async_smem();
     tc_fence_before();
     named_sync(bar_id, kPrepThreads);
+    if (lt == 0) {
+        // the chain reads the flag after the X barrier; its previous value
+        // (chunk c - 2) was read before the state pass waited for above
+        s.renorm[g] = renorm ? 1u : 0u;
+        mbar_arrive(&s.bar[kBarReady + g]);
+    }
+    // P (16 rows x 8 float4)
+    if (lt < kNQ * 8) {
+        const int i = lt >> 3, ch = lt & 7;
+        const float *src = Psrc + i * pld + 4 * ch;
+        *(float4 *)(gt + kGY + sw128_offset(y_row_p(g) + i, ch)) = make_float4(src[0], src[1], src[2], src[3]);
+    }
+    // decayed K^T (write keys: decayed K~^T, from kw16 = this thread's 16
+    // values, or from the K~ tile at ksrc with blocks kblock bytes apart):
+    // row dk, four groups of 4 chunk rows per thread. The decay of chunk row
+    // s2 is one exponential per row, taken by lane s2 - 4 q0 of every warp
+    // and passed around (the warp's rows are 4 q0 .. 4 q0 + 15).
+    {
+        const int dk = lt & 127, q0 = (lt >> 7) * 4;
+        const float Lend = L_s[kC - 1] - ls_next;
+        const float dec = gated ? __expf(Lend - L_s[4 * q0 + (lane & 15)]) : 1.f;
+        const uint8_t *src = (ksrc ? ksrc : kq) + (dk >> 6) * kblock;
+        const int chunk = (dk & 63) >> 3, e = dk & 7;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float f[4];
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+                const int s2 = 4 * (q0 + q) + k4;
+                const float x = kw16 ? kw16[4 * q + k4]
+                                     : __bfloat162float(*(const __nv_bfloat16 *)(src + sw128_offset(s2, chunk) + e * 2));
+                const float d = __shfl_sync(0xffffffffu, dec, 4 * q + k4);
+                f[k4] = gated ? x * d : x;
+            }
+            *(float4 *)(gt + kGY + sw128_offset(y_row_k(g) + dk, q0 + q)) = make_float4(f[0], f[1], f[2], f[3]);
+        }
+    }
+    fence_proxy_async_smem();
+    named_sync(bar_id, kPrepThreads);
+    if (lt == 0) {
+        mbar_arrive(&s.bar[kBarReadyY + g]);
+        mbar_arrive(&s.bar[kBarEmpty + st]);
+    }
     return true;
+}
+
+// Phase B without a gate: the tiles are quick to make, so X and Y are
+// signalled together at the end (same arguments as phase_b_gated; kw16 is
+// unused: ungated write keys arrive in the record at ksrc).
+__device__ __forceinline__ bool phase_b_plain(const Smem &s, const Params &p, uint32_t tbase, uint8_t *gt,
+                        const uint8_t *kq, const float *Psrc, int pld, const float *L_s, int c,
+                        int g, int st, int lt, uint32_t bar_id, float ls_cur, float ls_next, bool renorm,
+                        const float *kw16 = nullptr, const uint8_t *ksrc = nullptr,
+                        uint32_t kblock = kKQBlock)
+{
+    const int lw = lt >> 5, lane = lt & 31, lq = lw & 3, hf = lw >> 2;
+    const int ct = p.ct;
+    bool ok = (c < 2 || lt != 0) || wait_bar(s, kBarM2 + g, ((c - 2) >> 1) & 1, p.status);
+    if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) return false;
+    // P (16 rows x 8 float4)
+    if (lt < kNQ * 8) {
+        const int i = lt >> 3, ch = lt & 7;
+        const float *src = Psrc + i * pld + 4 * ch;
+        *(float4 *)(gt + kGY + sw128_offset(y_row_p(g) + i, ch)) = make_float4(src[0], src[1], src[2], src[3]);
+    }
+    // q rows (token row i, dk block kb4, 8-element group q); zero past the chunk's tokens
+    {
+        const int i = lt >> 4, kb4 = (lt >> 2) & 3, q = lt & 3;
+        const float gr = i < ct ? 1.f : 0.f;
+        const uint4 u = *(const uint4 *)(kq + (kb4 >> 1) * kKQBlock + sw128_offset(kC + i, (kb4 & 1) * 4 + q));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            f[2 * e] = __uint_as_float(w[e] << 16) * gr;
+            f[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u) * gr;
+        }
+        uint8_t *dst = gt + kGX + kb4 * kXBlock;
+        *(float4 *)(dst + sw128_offset(kC + i, 2 * q)) = make_float4(f[0], f[1], f[2], f[3]);
+        *(float4 *)(dst + sw128_offset(kC + i, 2 * q + 1)) = make_float4(f[4], f[5], f[6], f[7]);
+    }
+    // K^T (or K~^T from ksrc): row dk, four groups of 4 chunk rows per thread
+    {
+        const int dk = lt & 127, q0 = (lt >> 7) * 4;
+        const uint8_t *src = (ksrc ? ksrc : kq) + (dk >> 6) * kblock;
+        const int chunk = (dk & 63) >> 3, e = dk & 7;
+#pragma unroll
+        for (int q = q0; q < q0 + 4; ++q) {
+            float f[4];
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4)
+                f[k4] = __bfloat162float(*(const __nv_bfloat16 *)(src + sw128_offset(4 * q + k4, chunk) + e * 2));
+            *(float4 *)(gt + kGY + sw128_offset(y_row_k(g) + dk, q)) = make_float4(f[0], f[1], f[2], f[3]);
+        }
+    }
+    // -W (lane = dk; half hf takes chunk rows 16*hf .. 16*hf + 15)
+    ok = (lt != 0) || wait_bar(s, kBarUW + g, (c >> 1) & 1, p.status);
+    if (group_any(bar_id, kPrepThreads, !ok || *s.abort)) return false;
+    tc_fence_after();
+    {
+        uint32_t r[16];
+        tmem_ld16(tbase + ((uint32_t)(lq * 32) << 16) + kColW + g * 32 + 16 * hf, r);
+        tmem_wait_ld();
+        const int dk = 32 * lq + lane, pos = dk & 31;
+        uint8_t *dst = gt + kGX + (dk >> 5) * kXBlock + (pos & 3) * 4;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            *(float *)(dst + sw128_offset(16 * hf + j, pos >> 2)) = -__uint_as_float(r[j]);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    named_sync(bar_id, kPrepThreads);
+    if (lt == 0) {
+        s.renorm[g] = 0u;
+        mbar_arrive(&s.bar[kBarReady + g]);
+        mbar_arrive(&s.bar[kBarReadyY + g]);
+        mbar_arrive(&s.bar[kBarEmpty + st]);
+    }
+    return true;
+}
+
+__device__ __forceinline__ bool phase_b(const Smem &s, const Params &p, uint32_t tbase, uint8_t *gt,
+                        const uint8_t *kq, const float *Psrc, int pld, const float *L_s, int c,
+                        int g, int st, int lt, uint32_t bar_id, float ls_cur, float ls_next, bool renorm,
+                        const float *kw16 = nullptr, const uint8_t *ksrc = nullptr,
+                        uint32_t kblock = kKQBlock)
+{
+    return p.g ? phase_b_gated(s, p, tbase, gt, kq, Psrc, pld, L_s, c, g, st, lt, bar_id, ls_cur, ls_next, renorm, kw16, ksrc, kblock)
+               : phase_b_plain(s, p, tbase, gt, kq, Psrc, pld, L_s, c, g, st, lt, bar_id, ls_cur, ls_next, renorm, kw16, ksrc, kblock);
 }
 
 // Write keys of chunk c for phase B's decayed K~^T: thread lt's column
@@ -1011,17 +1155,10 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
             const float *Lrec = (const float *)(rec + kRecL);
             const float lgc = gated ? Lrec[kC - 1] : 0.f, ls_next = ls_after(ls, lgc);
             // (with a key/query prologue the stage's K and Q arrive mapped, from the record)
-            if (!phase_b(s, p, tbase, gt, kq, (const float *)(rec + kRecP), kC, Lrec, c, g, lt, bar_id, ls,
-                         ls_next, kw_global ? kwv : nullptr, (J::kWK && !gated) ? rec + kRecKW : nullptr,
-                         (J::kWK && !gated) ? kKWBlock : kKQBlock))
+            if (!phase_b(s, p, tbase, gt, kq, (const float *)(rec + kRecP), kC, Lrec, c, g, st, lt, bar_id, ls, ls_next,
+                         gated && renorm_at(ls, lgc), kw_global ? kwv : nullptr,
+                         (J::kWK && !gated) ? rec + kRecKW : nullptr, (J::kWK && !gated) ? kKWBlock : kKQBlock))
                 break;
-            if (lt == 0) {
-                // the chain read the previous chunk's flag before that chunk's
-                // state pass, which phase_b has waited for
-                s.renorm[g] = (gated && renorm_at(ls, lgc)) ? 1u : 0u;
-                mbar_arrive(&s.bar[kBarReady + g]);
-                mbar_arrive(&s.bar[kBarEmpty + st]);
-            }
             lgc_own = lgc;
             have_own = true;
         }
@@ -1060,12 +1197,9 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
         named_sync(bar_id, kPrepThreads);
         if (lt == 0) mbar_arrive(&s.bar[kBarTb + g]);
         const float lgc = gated ? w.L_s[kC - 1] : 0.f, ls_next = ls_after(ls, lgc);
-        if (!phase_b(s, p, tbase, gt, kq, w.Ps, kLd, w.L_s, c, g, lt, bar_id, ls, ls_next)) break;
-        if (lt == 0) {
-            s.renorm[g] = (gated && renorm_at(ls, lgc)) ? 1u : 0u;
-            mbar_arrive(&s.bar[kBarReady + g]);
-            mbar_arrive(&s.bar[kBarEmpty + st]);
-        }
+        if (!phase_b(s, p, tbase, gt, kq, w.Ps, kLd, w.L_s, c, g, st, lt, bar_id, ls, ls_next,
+                     gated && renorm_at(ls, lgc)))
+            break;
         lgc_own = lgc;
         have_own = true;
     }
@@ -1085,8 +1219,10 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, const J
     // arrays of o's layout (part 0: o from a zero start state; part 1: the
     // start state's weights q~ = A_{<=t}^T q_t), which the correction adds up.
     const bool ws_out = J::kSeg && jb.seg > 0;
-    TOut *const o_seq = (TOut *)p.o + tok_row(p, jb, 0) * kD + tid;
-    float *const w_seq = J::kSeg ? (jb.part ? p.seg_qt : p.seg_o0) + tok_row(p, jb, 0) * kD + tid : nullptr;
+    // (from this warp's block of 32 value columns)
+    TOut *const o_seq = (TOut *)p.o + tok_row(p, jb, 0) * kD + warp * 32;
+    float *const w_seq = J::kSeg ? (jb.part ? p.seg_qt : p.seg_o0) + tok_row(p, jb, 0) * kD + warp * 32 : nullptr;
+    uint8_t *const stg = s.out_tile(warp);
     const size_t tok_stride = (size_t)p.H * kD;
 
     {   // S^T <- h0^T (lane = dv, column = dk), or zeros (or, for a segment's
@@ -1167,17 +1303,11 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, const J
         // relaxed: the chain needs only the TMEM clears above (complete after
         // wait::st), not this warp's output stores of the previous chunk
         if (lane == 0) mbar_arrive_relaxed(&s.bar[kBarOFree + g]);
-        if (ws_out) {
-            float *oc = w_seq + (size_t)t0 * tok_stride;
-#pragma unroll
-            for (int i = 0; i < kNQ; ++i)
-                if (i < p.ct && t0 + i < jb.tokens(p)) store_out(oc, (size_t)i * tok_stride, __uint_as_float(ra[i]));
-        } else {
-            TOut *oc = o_seq + (size_t)t0 * tok_stride;
-#pragma unroll
-            for (int i = 0; i < kNQ; ++i)
-                if (i < p.ct && t0 + i < jb.tokens(p)) store_out(oc, (size_t)i * tok_stride, __uint_as_float(ra[i]));
-        }
+        const int n_rows = min(p.ct, jb.tokens(p) - t0);
+        if (ws_out)
+            store_rows(w_seq + (size_t)t0 * tok_stride, tok_stride, ra, n_rows, stg, lane);
+        else
+            store_rows(o_seq + (size_t)t0 * tok_stride, tok_stride, ra, n_rows, stg, lane);
     }
     // segmented mode: every part's end state goes to the workspace (the
     // combine step turns them into start states and the final state)
@@ -1212,6 +1342,7 @@ __device__ __forceinline__ void state_pass_cta(const CUtensorMap &tm_k, const CU
     s.group_off = Lay::kOffGroup;
     s.group_bytes = Lay::kGroup;
     s.scratch_off = Lay::kOffScratch;
+    s.out_off = Lay::kOffOut;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // a sequence with bad packed offsets runs no chunk
     const Job<kPacked, kPro, kWK, kSeg> jb = make_job<kPacked, kPro, kWK, kSeg>(p, bh);
