@@ -71,6 +71,9 @@ def parse():
     ap.add_argument("--fused", action="store_true",
                     help="give dp_forward only the minimum workspace: the chunk path then "
                          "runs as one fused kernel instead of prep + state-pass kernels")
+    ap.add_argument("--B", type=int, help="batch of the workload (default: its own); for small profiling cases")
+    ap.add_argument("--H", type=int, help="heads of the workload (default: its own)")
+    ap.add_argument("--T", type=int, help="tokens per sequence of the workload (default: its own)")
     ap.add_argument("--split", action="store_true",
                     help="give the forward a workspace that holds the per-chunk records but not the "
                          "cooperative flags, so it runs as prep + state-pass kernels (for profiling)")
@@ -818,6 +821,10 @@ def only_arm(args):
 def main():
     args = parse()
     w = WORKLOADS[args.workload]
+    resize = {k: getattr(args, k) for k in ("B", "H", "T") if getattr(args, k)}
+    if resize:   # the same recipe at another size (named as such)
+        w = w.scaled(**resize)
+        w = w.scaled(name=f"{WORKLOADS[args.workload].name} at B{w.B} H{w.H} T{w.T}")
     if args.only:
         only_arm(args)
         return

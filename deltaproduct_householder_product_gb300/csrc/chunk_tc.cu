@@ -309,10 +309,44 @@ __device__ __forceinline__ uint32_t flag_read(const uint32_t *flag)
     return v;
 }
 
+// Once the state pass has issued the loads of a chunk it stores 2 into the
+// chunk's flag. The warp prep paces itself on these marks: it loads chunk c
+// of a head only once that head's state pass has taken chunk c - kPaceLead,
+// so the records it writes (and the K and Q rows it reads, which the state
+// pass reads again) are still in L2 when the state pass gets to them. The
+// marks order nothing (relaxed): they only hold the prep back.
+constexpr int kPaceLead = 16;
+__device__ __forceinline__ void flag_mark_taken(uint32_t *flag)
+{
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(2u) : "memory");
+}
+
+__device__ __forceinline__ uint32_t flag_peek(const uint32_t *flag)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    return v;
+}
+
 template <class J>
 __device__ __forceinline__ size_t rec_index(const Params &p, const J &j, int c)
 {
     return ((size_t)j.b * p.H + j.h) * (size_t)p.n_chunks + (J::kSeg ? j.c0 + c : c);
+}
+
+// Cooperative mode: a chunk's record is read once, by the state pass's
+// bulk copy, and is dead once that copy has landed. Its L2 lines are then
+// dropped without a write-back (only lines wholly inside the record), so
+// that records, which the prep writes only a few chunks ahead of the state
+// pass, never travel to DRAM and back. Thread lt of nthreads drops every
+// nthreads-th line.
+template <class J>
+__device__ __forceinline__ void discard_record(const Params &p, const J &j, int c, int lt, int nthreads)
+{
+    const uintptr_t r0 = (uintptr_t)(p.rec + rec_index(p, j, c) * p.rec_stride);
+    const uintptr_t a = (r0 + 127) & ~(uintptr_t)127, e = (r0 + p.rec_stride) & ~(uintptr_t)127;
+    for (uintptr_t l = a + (uintptr_t)lt * 128; l < e; l += (uintptr_t)nthreads * 128)
+        asm volatile("discard.global.L2 [%0], 128;" ::"l"(l) : "memory");
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
@@ -537,6 +571,7 @@ __device__ void tma_role(const Smem &s, const Params &p, const CUtensorMap *tk,
             bulk_load(dst + kRecT, rec + kRecT, rec_t, bar);
             bulk_load(dst + kRecP, rec + kRecP, rec_tail, bar);
         }
+        if (kCoop) flag_mark_taken(p.flags + rec_index(p, jb, c));
         last_use[st] = u;
     }
     // every issued load must have landed before shared memory is released
@@ -1159,6 +1194,8 @@ __device__ void prep_role(const Smem &s, const Params &p, uint32_t tbase, int g,
                          gated && renorm_at(ls, lgc), kw_global ? kwv : nullptr,
                          (J::kWK && !gated) ? rec + kRecKW : nullptr, (J::kWK && !gated) ? kKWBlock : kKQBlock))
                 break;
+            // (after the chunk's signals: the group has time until the state pass frees its tiles)
+            if (p.flags && !J::kSeg) discard_record(p, jb, c, lt, kPrepThreads);
             lgc_own = lgc;
             have_own = true;
         }
@@ -1770,6 +1807,13 @@ __device__ void wprep_loader(const Params &p, const CUtensorMap *tk, const CUten
         const int c = idx / p.bh_count;
         const J jb = make_job<kPacked, false, false>(p, idx - c * p.bh_count);
         const int t0 = jb.first() + c * ct;
+        if (p.flags && c >= kPaceLead && c - kPaceLead < jb.chunks(p)) {
+            // cooperative mode: no further than kPaceLead chunks ahead of the head's state pass
+            const uint32_t *f = p.flags + rec_index(p, jb, c - kPaceLead);
+            uint32_t tries = 0;
+            while (flag_peek(f) != 2u && ++tries < p.flag_tries && !*abort) __nanosleep(128);
+            if (flag_peek(f) != 2u) { ok = false; break; }
+        }
         uint64_t *lb = &bar[sl * 2 + 0];
         uint8_t *stg = base + kWStages + (pr * kWSlots + sl) * kWStage;
         mbar_arrive_expect_tx(lb, 256u * R + 256u * ct);

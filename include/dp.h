@@ -114,6 +114,9 @@ dp_status dp_forward_workspace_size(const dp_dims *dims, size_t *bytes);
  * every chunk's UT transform is then prepared in parallel (by the other
  * CTAs of one cooperative launch when B*H leaves at least half the SMs
  * free, else by a first kernel) and the state pass streams the records in.
+ * In the cooperative mode the prep runs at most 16 chunks ahead of each
+ * head's state pass and the state pass drops each record from L2 once it
+ * has read it, so records live in L2 only and do not reach DRAM.
  * Dense problems without prologue or write keys whose B*H is small enough
  * that each sequence can be cut into P >= 2 segments of at least 16 chunks
  * with B*H*(2P - 1) <= the SM count take the segmented mode instead
@@ -315,7 +318,9 @@ dp_status dp_check_status(const void *workspace, dp_stream_t stream);
  * An expired wait makes the waiting CTA record DP_ERR_TIMEOUT in the
  * workspace's status word, drain what it has in flight, release its tensor
  * memory and return; the other CTAs finish normally, so the launch ends and
- * the context stays usable. Nothing faults, traps or hangs. Returns
+ * the context stays usable (a head stuck at chunk c holds the prep of its
+ * chunks >= c + 16 back, and prep work queued behind them then times out
+ * too: every wait is bounded). Nothing faults, traps or hangs. Returns
  * DP_ERR_INVALID_ARG unless withhold_first_record is 0 or 1. */
 dp_status dp_test_set_wait_fault(int withhold_first_record, unsigned int flag_wait_polls);
 
