@@ -16,16 +16,22 @@
 //   S   = Gamma_C S0 + K^T diag(Gamma_C/Gamma) U'        state pass, part 2
 //   o_t = Gamma_r S0^T q_t + sum_{s<=r} E_rs (q_t.k_s) u'_s,  r = last row of t
 //
-// Three ways to run it, same arithmetic and bit-identical results:
-//  * split (two kernels): chunk_prep_kernel does "phase A" (G, P, T: the work
-//    that needs only one chunk's inputs) for every chunk of every head at
-//    once and writes a record per chunk into the workspace; the state-pass
-//    kernel then streams the records in with the inputs. The sequential
-//    kernel keeps only the work that has to follow the state.
+// Four ways to run it (split and cooperative bit-identical; fused and
+// segmented equal to them up to rounding):
+//  * split (two kernels): the warp-per-chunk prep kernel (chunk_wprep_kernel;
+//    chunk_prep_kernel with a prologue or write keys) does "phase A" (G, P,
+//    T: the work that needs only one chunk's inputs) for every chunk of every
+//    head at once and writes a record per chunk into the workspace; the
+//    state-pass kernel then streams the records in with the inputs. The
+//    sequential kernel keeps only the work that has to follow the state.
 //  * cooperative (one launch, chunk_coop_kernel): state-pass CTAs and prep
-//    CTAs side by side, each record published through a flag.
+//    CTAs side by side, each record published through a flag; the prep
+//    stays at most kPaceLead chunks ahead of each head's state pass.
 //  * fused (one kernel, no workspace beyond the status word): the state-pass
 //    kernel's prep groups do phase A themselves, one chunk ahead.
+//  * segmented (chunk_seg_kernel, seg_combine_kernel, seg_correct_kernel):
+//    long sequences cut into segments that run at once, chained by their
+//    affine transitions (see seg_combine_kernel).
 // Compile-time variants (the Job type's flags), so that the plain
 // instantiation carries none of their code:
 //  * packed sequences (kPacked): each CTA reads its sequence's range from
