@@ -548,13 +548,15 @@ def varlen_measure(dp, dev, hbm_peak, steps=20, warmup=3):
                          "frac": achieved / hbm_peak, "algorithmic_bytes": wbytes}}
 
 
-def roofline_obj(w, ms, hbm_peak, peak_kind, path, scope):
+def roofline_obj(w, ms, hbm_peak, peak_kind, path, scope, captured=True):
     """HBM roofline of one forward: algorithmic bytes (inputs, bf16 o, state
-    I/O) over the measured time per call."""
+    I/O) over the measured time per call. `captured`: the measured DRAM
+    traffic of one forward of this workload and path applies (not for other
+    call patterns over the same tokens)."""
     wbytes = W.algorithmic_bytes(w, out_bytes=OUT_DTYPE.itemsize)
     achieved = wbytes / (ms * 1e-3) / 1e9
     return {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-            "frac": achieved / hbm_peak, "traffic": TRAFFIC.get((w.name, path)),
+            "frac": achieved / hbm_peak, "traffic": TRAFFIC.get((w.name, path)) if captured else None,
             "peak_kind": peak_kind, "algorithmic_bytes": wbytes, "scope": scope}
 
 
@@ -641,7 +643,7 @@ def side_configs(dp, L, dev, args, hbm_peak, peak_kind):
                 "ms": cms, "tokens_per_s": w.B * w.T / (cms * 1e-3), "path": cpath,
                 "calls": W.LONG_CALLS, "tokens_per_call": w.T // W.LONG_CALLS,
                 "roofline": roofline_obj(w, cms, hbm_peak, peak_kind, cpath,
-                                         f"{W.LONG_CALLS} carried calls over distinct inputs")}
+                                         f"{W.LONG_CALLS} carried calls over distinct inputs", captured=False)}
         torch.cuda.empty_cache()
     return out
 
