@@ -2158,6 +2158,14 @@ seg_correct_kernel(const __grid_constant__ CUtensorMap tm_st, const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
+    // every thread's o0 values (lane = value column v, kCorrTok tokens) are
+    // fetched before the tiles land and the MMAs run, so that their DRAM
+    // latency overlaps those
+    const size_t tok_stride = (size_t)p.H * kD;
+    const size_t row0 = (((size_t)b * p.T + tok0) * p.H + h) * kD + tid;
+    float a[kCorrTok];
+#pragma unroll
+    for (int j = 0; j < kCorrTok; ++j) a[j] = j < ntok ? __ldg(p.seg_o0 + row0 + (size_t)j * tok_stride) : 0.f;
     bool ok = true;
     if (tid == 0) {
         mbar_arrive_expect_tx(&bar[0], 4 * kCorrBlock + 4 * kCorrBBlock);
@@ -2192,22 +2200,15 @@ seg_correct_kernel(const __grid_constant__ CUtensorMap tm_st, const __grid_const
     if (!*abort) {
         // lane = value column v; TMEM column = token of the tile
         const uint32_t trow = tbase + ((uint32_t)(warp * 32) << 16);
-        const size_t tok_stride = (size_t)p.H * kD;
-        const size_t row0 = (((size_t)b * p.T + tok0) * p.H + h) * kD + tid;
-        for (int c0 = 0; c0 < kCorrTok; c0 += 32) {
-            // the 32 tokens' o0 values first (read-only path, all in flight
-            // together), then the sums
-            float a[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-                a[j] = c0 + j < ntok ? __ldg(p.seg_o0 + row0 + (size_t)(c0 + j) * tok_stride) : 0.f;
+        for (int c0 = 0; c0 < kCorrTok; c0 += 32) {
             uint32_t d[32];
             tmem_ld32(trow + c0, d);
             tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 32; ++j)
                 if (c0 + j < ntok)
-                    store_out((TOut *)p.o, row0 + (size_t)(c0 + j) * tok_stride, __uint_as_float(d[j]) + a[j]);
+                    store_out((TOut *)p.o, row0 + (size_t)(c0 + j) * tok_stride, __uint_as_float(d[j]) + a[c0 + j]);
         }
     }
     tc_fence_before();
