@@ -217,6 +217,43 @@ def test_coop_wait_timeout_is_reported(dp):
     assert_parity(h2, rh, "bf16", "h_final after the timeout")
 
 
+def test_coop_pacing_wait_timeout_is_reported(dp):
+    """The prep's pacing wait (it loads chunk c of a head only once the
+    head's state pass has taken chunk c - 16) is bounded too: with the first
+    record withheld, head 0's state pass never takes a chunk, so the prep's
+    wait for its chunk 16 runs out as well (prep work queued behind it times
+    out in turn). The call returns within the polls' time, reports
+    DP_ERR_TIMEOUT, and the next normal call on the same workspace is clean
+    and matches the oracle."""
+    import time
+    w = W.BASE.scaled(B=1, H=3, T=480)                 # 30 chunks per head (16 tokens each)
+    x = W.make_inputs(w)
+    g = cuda(x)
+    size = workspace_for(dp, x, "chunk_tc", "split")
+    assert dp.forward_path(*_dims(g)[:6], size) == "chunk_coop"
+    ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
+    ro, rh = ref(x)
+    o = torch.zeros(w.B, w.T, w.H, w.Dv, dtype=torch.float32, device="cuda")
+    try:
+        dp.set_wait_fault(True, 4096)
+        t0 = time.perf_counter()
+        dp.forward(g["q"], g["k"], g["v"], g["beta"], g["g"], g["h0"], impl="chunk_tc", workspace=ws, out=o)
+        torch.cuda.synchronize()
+        elapsed = time.perf_counter() - t0
+    finally:
+        dp.set_wait_fault()
+    with pytest.raises(dp.DPError) as err:
+        dp.check_status(ws)
+    assert err.value.code == 6                        # DP_ERR_TIMEOUT
+    assert elapsed < 10.0, elapsed
+    dp.check_status(ws)
+    o2, h2 = dp.forward(g["q"], g["k"], g["v"], g["beta"], g["g"], g["h0"], impl="chunk_tc", workspace=ws,
+                        out_dtype=torch.float32)
+    dp.check_status(ws)
+    assert_parity(o2, ro, "bf16", "o after the timeout")
+    assert_parity(h2, rh, "bf16", "h_final after the timeout")
+
+
 @pytest.mark.parametrize("base", [W.BASE, W.GATED, W.NEARDUP], ids=lambda w: w.name)
 def test_bf16_output_is_rounded_fp32_output(dp, base):
     """The bf16-output variant runs the same arithmetic and only rounds the final
