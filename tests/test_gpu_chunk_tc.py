@@ -181,8 +181,8 @@ def test_workspace_reuse_across_shapes(dp):
 
 
 def test_coop_wait_timeout_is_reported(dp):
-    """A device-side bounded wait that expires (SURVEY's failure-detection
-    case, made on purpose without a fault): the prep CTAs withhold the first
+    """A device-side bounded wait that expires (failure detection, made to
+    happen on purpose without a fault): the prep CTAs withhold the first
     record, so the state pass's wait for its flag runs out after a short
     limit. The call returns, the status word reads DP_ERR_TIMEOUT, the other
     heads' results are still right, and the next normal call on the same
