@@ -658,9 +658,45 @@ __device__ void prep_mma_role(const Smem &s, const Params &p, uint32_t tbase, in
 //   [U'^T | O_b] += S^T [-W; Gamma q]^T          (16 instructions, N = 48)
 //   [S^T | O_a] or [O_a | S^T] += U'^T [K^T; P]   (4 instructions, N = 144)
 // Consecutive MMAs run in issue order, so S -> U' -> S needs no round trip.
-__device__ void chain_role(const Smem &s, const Params &p, uint32_t tbase, int n)
+// Any other instruction of the issuing thread between two of its MMAs costs
+// the tensor pipe about as much as several MMAs (measured: a wait, a fence,
+// a commit or a branch between the two halves of a chunk adds ~450 cycles).
+// Without a gate phase B signals both tiles at once, so every wait of a
+// chunk comes before its first MMA and its 20 MMAs go out back to back.
+__device__ void chain_role_plain(const Smem &s, const Params &p, uint32_t tbase, int n)
 {
-    const bool gated = p.g != nullptr;
+    const uint32_t id_x = idesc_tf32(128, kXRows);
+    const uint32_t id_y = idesc_tf32(128, kYRows);
+    bool ok = wait_bar(s, kBarInit, 0, p.status);
+    for (int c = 0; c < n && ok; ++c) {
+        const int g = c & 1;
+        const uint32_t gb = smem_addr(s.group(g));
+        const uint32_t d_x = tbase + col_un(g);
+        const uint32_t d_y = g ? tbase + kColS : tbase + kColOa0;   // O_a[0] | S  or  S | O_a[1]
+        if (!(ok = wait_bar(s, kBarReady + g, (c >> 1) & 1, p.status))) break;
+        if (!(ok = wait_bar(s, kBarReadyY + g, (c >> 1) & 1, p.status))) break;
+        if (c >= 2 && !(ok = wait_bar(s, kBarOFree + g, ((c - 2) >> 1) & 1, p.status))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk)
+            mma_ts_tf32(d_x, tbase + kColS + kk * 8,
+                        sdesc_sw128(gb + kGX + (kk >> 2) * kXBlock + (kk & 3) * 32, 16, 1024), id_x, 1);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_ts_tf32(d_y, d_x + kk * 8, sdesc_sw128(gb + kGY + kk * 32, 16, 1024), id_y, 1);
+        mma_commit(&s.bar[kBarM2 + g]);
+    }
+    mma_commit(&s.bar[kBarFinal]);
+    uint32_t no_abort = 0;
+    mbar_wait(&s.bar[kBarFinal], 0, kWaitTries, &no_abort);
+}
+
+// With a gate: the chain starts a chunk on the X tile while phase B writes
+// the Y tile (a wait between the halves costs less than phase B's Y time),
+// and a chunk that rescales the stored state hands it to the epilogue
+// between the halves.
+__device__ void chain_role_gated(const Smem &s, const Params &p, uint32_t tbase, int n)
+{
     const uint32_t id_x = idesc_tf32(128, kXRows);
     const uint32_t id_y = idesc_tf32(128, kYRows);
     bool ok = wait_bar(s, kBarInit, 0, p.status);
@@ -675,13 +711,12 @@ __device__ void chain_role(const Smem &s, const Params &p, uint32_t tbase, int n
         for (int kk = 0; kk < 16; ++kk)
             mma_ts_tf32(tbase + col_un(g), tbase + kColS + kk * 8,
                         sdesc_sw128(gb + kGX + (kk >> 2) * kXBlock + (kk & 3) * 32, 16, 1024), id_x, 1);
-        if (gated && s.renorm[g]) {   // this chunk rescales the stored state
+        if (s.renorm[g]) {   // this chunk rescales the stored state
             mma_commit(&s.bar[kBarM1]);
             if (!(ok = wait_bar(s, kBarScaled, n_renorm & 1, p.status))) break;
             ++n_renorm;
             tc_fence_after();
         }
-        // the Y tile is written while the first half runs
         if (!(ok = wait_bar(s, kBarReadyY + g, (c >> 1) & 1, p.status))) break;
         tc_fence_after();
         const uint32_t d_y = g ? tbase + kColS : tbase + kColOa0;   // O_a[0] | S  or  S | O_a[1]
@@ -1420,7 +1455,10 @@ __device__ __forceinline__ void state_pass_cta(const CUtensorMap &tm_k, const CU
     } else if (warp == kTmaWarp) {
         if (lane == 0) tma_role<kSplit, kCoop>(s, p, &tm_k, &tm_v, &tm_q, jb);
     } else if (warp == kChainWarp) {
-        if (lane == 0) chain_role(s, p, tbase, jb.chunks(p));
+        if (lane == 0) {
+            if (p.g) chain_role_gated(s, p, tbase, jb.chunks(p));
+            else chain_role_plain(s, p, tbase, jb.chunks(p));
+        }
     } else {
         if (lane == 0) prep_mma_role<kSplit, kPro>(s, p, tbase, jb.chunks(p));
     }
