@@ -337,8 +337,10 @@ def test_backward_gated_chunked_negative_gate_reported(dp):
 
 def test_backward_auto_keeps_recurrent_for_gated(dp):
     """AUTO on a gated problem runs the recurrent form: its gradients equal
-    impl="recurrent"'s bit for bit up to the atomics' order (compared at
-    1e-6 of RMS), and differ from the chunked form's rounding."""
+    impl="recurrent"'s up to the order of that kernel's fp32 atomics (the
+    value-column CTAs of a head add their parts of dq, dk, dbeta and dg),
+    compared at 1e-5 of RMS (two runs of the recurrent form have differed by
+    1.1e-6)."""
     w = W.GATED.scaled(B=1, H=2, T=30, nh=2)
     d_o, dhf = cotangents(w, 360)
     got_auto, ref, _ = run_both(dp, w, d_o, dhf, impl="auto")
@@ -346,4 +348,4 @@ def test_backward_auto_keeps_recurrent_for_gated(dp):
     for n in NAMES:
         if ref[n] is not None:
             s = err_stats(got_auto[n], got_rec[n].cpu().double().numpy())
-            assert s["rel_max"] <= 1e-6, (n, s)
+            assert s["rel_max"] <= 1e-5, (n, s)
