@@ -190,7 +190,7 @@ struct Layout {
     static constexpr uint32_t kOffBar = kOffOut + 4 * kOutTile;
 };
 
-constexpr uint32_t kNumBars = 2 * kNS + 2 * 7 + 7;
+constexpr uint32_t kNumBars = 2 * kNS + 2 * 7 + 8;
 template <bool kSplit>
 constexpr uint32_t smem_bytes() { return Layout<kSplit>::kOffBar + kNumBars * 8 + 16 + 1024; }
 static_assert(smem_bytes<true>() <= 227 * 1024 && smem_bytes<false>() <= 227 * 1024, "shared memory");
@@ -403,7 +403,8 @@ enum : int {
     kBarInit,                     // initial state in TMEM
     kBarFinal,                    // [2] every MMA of an issuer retired (teardown)
     kBarNorm = kBarFinal + 2,     // [2] prologue applied to the group's stage (fused mode with a prologue)
-    kBarCount = kBarNorm + 2
+    kBarXD = kBarNorm + 2,        // chain: a chunk's first-half MMAs retired (U' complete)
+    kBarCount
 };
 static_assert(kBarCount == (int)kNumBars, "barrier count");
 
@@ -657,12 +658,16 @@ __device__ void prep_mma_role(const Smem &s, const Params &p, uint32_t tbase, in
 // State-pass MMAs (tf32, A = the fp32 accumulators in TMEM):
 //   [U'^T | O_b] += S^T [-W; Gamma q]^T          (16 instructions, N = 48)
 //   [S^T | O_a] or [O_a | S^T] += U'^T [K^T; P]   (4 instructions, N = 144)
-// Consecutive MMAs run in issue order, so S -> U' -> S needs no round trip.
-// Any other instruction of the issuing thread between two of its MMAs costs
-// the tensor pipe about as much as several MMAs (measured: a wait, a fence,
-// a commit or a branch between the two halves of a chunk adds ~450 cycles).
-// Without a gate phase B signals both tiles at once, so every wait of a
-// chunk comes before its first MMA and its 20 MMAs go out back to back.
+// The second group reads as its A operand what the first wrote (U'), and the
+// next chunk's first group reads what the second wrote (S). The tcgen05
+// memory model runs one thread's MMAs in issue order only when they share
+// the accumulator and the shape, which these do not: each such hand-off
+// waits for the producing MMAs' commit (the first group's on kBarXD, the
+// second group's on the chunk's M2 barrier) and fences before the consuming
+// MMAs. (Issued back to back, the second group read a partly written U' in
+// about one chunk of 10^5 under a full CTA's load.) Any other instruction
+// of the issuing thread between two of its MMAs costs the tensor pipe about
+// as much as several MMAs, so the waits of a chunk sit at these two points.
 __device__ void chain_role_plain(const Smem &s, const Params &p, uint32_t tbase, int n)
 {
     const uint32_t id_x = idesc_tf32(128, kXRows);
@@ -676,11 +681,16 @@ __device__ void chain_role_plain(const Smem &s, const Params &p, uint32_t tbase,
         if (!(ok = wait_bar(s, kBarReady + g, (c >> 1) & 1, p.status))) break;
         if (!(ok = wait_bar(s, kBarReadyY + g, (c >> 1) & 1, p.status))) break;
         if (c >= 2 && !(ok = wait_bar(s, kBarOFree + g, ((c - 2) >> 1) & 1, p.status))) break;
+        // S as the previous chunk's second group left it
+        if (c >= 1 && !(ok = wait_bar(s, kBarM2 + (g ^ 1), ((c - 1) >> 1) & 1, p.status))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk)
             mma_ts_tf32(d_x, tbase + kColS + kk * 8,
                         sdesc_sw128(gb + kGX + (kk >> 2) * kXBlock + (kk & 3) * 32, 16, 1024), id_x, 1);
+        mma_commit(&s.bar[kBarXD]);
+        if (!(ok = wait_bar(s, kBarXD, c & 1, p.status))) break;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
             mma_ts_tf32(d_y, d_x + kk * 8, sdesc_sw128(gb + kGY + kk * 32, 16, 1024), id_y, 1);
@@ -692,9 +702,10 @@ __device__ void chain_role_plain(const Smem &s, const Params &p, uint32_t tbase,
 }
 
 // With a gate: the chain starts a chunk on the X tile while phase B writes
-// the Y tile (a wait between the halves costs less than phase B's Y time),
-// and a chunk that rescales the stored state hands it to the epilogue
-// between the halves.
+// the Y tile (the chain waits for the first group's commit anyway, and the
+// Y tile is mostly ready by then), and a chunk that rescales the stored
+// state hands it to the epilogue between the halves. The hand-offs between
+// the MMA groups wait for commits as in chain_role_plain.
 __device__ void chain_role_gated(const Smem &s, const Params &p, uint32_t tbase, int n)
 {
     const uint32_t id_x = idesc_tf32(128, kXRows);
@@ -706,16 +717,19 @@ __device__ void chain_role_gated(const Smem &s, const Params &p, uint32_t tbase,
         const uint32_t gb = smem_addr(s.group(g));
         if (!(ok = wait_bar(s, kBarReady + g, (c >> 1) & 1, p.status))) break;
         if (c >= 2 && !(ok = wait_bar(s, kBarOFree + g, ((c - 2) >> 1) & 1, p.status))) break;
+        if (c >= 1 && !(ok = wait_bar(s, kBarM2 + (g ^ 1), ((c - 1) >> 1) & 1, p.status))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk)
             mma_ts_tf32(tbase + col_un(g), tbase + kColS + kk * 8,
                         sdesc_sw128(gb + kGX + (kk >> 2) * kXBlock + (kk & 3) * 32, 16, 1024), id_x, 1);
-        if (s.renorm[g]) {   // this chunk rescales the stored state
-            mma_commit(&s.bar[kBarM1]);
+        mma_commit(&s.bar[kBarXD]);
+        const bool rescale = s.renorm[g] != 0u;   // this chunk rescales the stored state
+        if (rescale) mma_commit(&s.bar[kBarM1]);
+        if (!(ok = wait_bar(s, kBarXD, c & 1, p.status))) break;
+        if (rescale) {
             if (!(ok = wait_bar(s, kBarScaled, n_renorm & 1, p.status))) break;
             ++n_renorm;
-            tc_fence_after();
         }
         if (!(ok = wait_bar(s, kBarReadyY + g, (c >> 1) & 1, p.status))) break;
         tc_fence_after();
@@ -1359,7 +1373,8 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, const J
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_relaxed(&s.bar[kBarScaled]);   // TMEM only, as OFree below
+            // (a release arrive, as for kBarOFree below)
+            if (lane == 0) mbar_arrive(&s.bar[kBarScaled]);
         }
         ls = ls_after(ls, lgc);
         if (!warp_wait(s, kBarM2 + g, (c >> 1) & 1, p.status)) { failed = true; break; }
@@ -1378,9 +1393,10 @@ __device__ void epi_role(const Smem &s, const Params &p, uint32_t tbase, const J
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        // relaxed: the chain needs only the TMEM clears above (complete after
-        // wait::st), not this warp's output stores of the previous chunk
-        if (lane == 0) mbar_arrive_relaxed(&s.bar[kBarOFree + g]);
+        // a release arrive: with the chain's acquiring wait and its
+        // tcgen05.fence::after_thread_sync it orders the chain's next MMAs on
+        // these columns after the clears above
+        if (lane == 0) mbar_arrive(&s.bar[kBarOFree + g]);
         const int n_rows = min(p.ct, jb.tokens(p) - t0);
         if (ws_out)
             store_rows(w_seq + (size_t)t0 * tok_stride, tok_stride, ra, n_rows, stg, lane);
