@@ -665,7 +665,7 @@ __device__ void prep_mma_role(const Smem &s, const Params &p, uint32_t tbase, in
 // waits for the producing MMAs' commit (the first group's on kBarXD, the
 // second group's on the chunk's M2 barrier) and fences before the consuming
 // MMAs. (Issued back to back, the second group read a partly written U' in
-// about one chunk of 10^5 under a full CTA's load.) Any other instruction
+// a few chunks per 10^5 under a full CTA's load.) Any other instruction
 // of the issuing thread between two of its MMAs costs the tensor pipe about
 // as much as several MMAs, so the waits of a chunk sit at these two points.
 __device__ void chain_role_plain(const Smem &s, const Params &p, uint32_t tbase, int n)

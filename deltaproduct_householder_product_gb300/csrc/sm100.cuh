@@ -30,14 +30,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// Arrive without release semantics: for signals that order only tensor-memory
-// or tensor-core work the arriving thread has already waited for, so that the
-// arrive does not wait for the thread's earlier global stores to be performed.
-__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t *bar)
-{
-    asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
