@@ -51,11 +51,11 @@
 //  * warp 21   state-pass MMA issuer (one thread, tf32):
 //              [U' | O_b] += S [-W; Gamma q]^T and [S | O_a] += U'^T [K^T; P].
 //              These MMAs read S and U' straight from their fp32 TMEM
-//              accumulators as the A operand; consecutive MMAs are executed
-//              in issue order, so the chain S -> U' -> S needs no thread
-//              round trip. The readout rides along in the same instructions
-//              (stacked B operands), since each MMA instruction costs about
-//              the same issue time whatever its N.
+//              accumulators as the A operand; each hand-off (S -> U' -> S)
+//              waits for the producing group's commit (see chain_role_plain).
+//              The readout rides along in the same instructions (stacked B
+//              operands), since each MMA instruction costs about the same
+//              issue time whatever its N.
 //  * warp 22   prep MMA issuer (bf16: [K;Q] K^T in fused mode, U, W), one
 //              chunk ahead, on its own thread so its issue latency overlaps
 //              the state pass.
